@@ -1,0 +1,205 @@
+"""CPU oracle for paged decode attention (test infrastructure only).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
+leg may import this package.  The product path (the CUDA library and its
+Python binding) never imports it and shares no code with it.
+
+The arithmetic lives in ``pkv_oracle.c`` (plain C, float64); this module
+compiles it with gcc on first use and wraps it with ctypes.  ``formulas.py``
+holds the pages' byte-accounting formulas.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from typing import Optional
+
+import numpy as np
+
+from .formulas import (  # noqa: F401
+    kv_bytes_per_token,
+    kv_bytes,
+    kv_bytes_per_token_grouped,
+    decode_kv_read_seconds,
+    blocks_for_tokens,
+    last_block_waste_tokens,
+    tokens_that_fit,
+    naive_utilisation,
+)
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "pkv_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "libpkv_oracle.so")
+_lock = threading.Lock()
+_lib: Optional[ctypes.CDLL] = None
+
+ORACLE_OK = 0
+ORACLE_BAD_ARG = -1
+ORACLE_BAD_BLOCK = -2
+ORACLE_BAD_SLOT = -3
+ORACLE_BAD_CTX = -4
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle (gcc, -O2, OpenMP, no fast-math, no FP contraction)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
+           "-fno-fast-math", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
+    """Declare the C signatures on a loaded oracle library."""
+    P = ctypes.c_void_p
+    i32, i64, f32 = ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+    lib.pkv_oracle_e4m3_decode.restype = ctypes.c_double
+    lib.pkv_oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+    lib.pkv_oracle_e4m3_encode.restype = ctypes.c_uint8
+    lib.pkv_oracle_e4m3_encode.argtypes = [f32]
+    lib.pkv_oracle_e4m3_decode_array.restype = None
+    lib.pkv_oracle_e4m3_decode_array.argtypes = [P, P, i64]
+    lib.pkv_oracle_e4m3_quantize_array.restype = None
+    lib.pkv_oracle_e4m3_quantize_array.argtypes = [P, P, P, i64]
+    lib.pkv_oracle_kv_append.restype = ctypes.c_int
+    lib.pkv_oracle_kv_append.argtypes = [P, P, P, i32, P, P, i32, P, P,
+                                         i32, i32, i32, i32, i32, i32]
+    lib.pkv_oracle_paged_decode.restype = ctypes.c_int
+    lib.pkv_oracle_paged_decode.argtypes = [P, i32, i32, P, P, i32, P, P,
+                                            i32, i32, i32, i32, i32,
+                                            P, i32, P, P, i32, i32, f32, P, P, i32]
+    lib.pkv_oracle_num_threads.restype = ctypes.c_int
+    lib.pkv_oracle_num_threads.argtypes = []
+    return lib
+
+
+def load_library(path: str) -> ctypes.CDLL:
+    """Load another build of the oracle source (used to plant mistakes in tests)."""
+    return _bind(ctypes.CDLL(path))
+
+
+def _load(lib: Optional[ctypes.CDLL] = None) -> ctypes.CDLL:
+    global _lib
+    if lib is not None:
+        return lib
+    with _lock:
+        if _lib is None:
+            _lib = _bind(ctypes.CDLL(build()))
+    return _lib
+
+
+def _ptr(a: Optional[np.ndarray]):
+    return None if a is None else ctypes.c_void_p(a.ctypes.data)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def num_threads() -> int:
+    return int(_load().pkv_oracle_num_threads())
+
+
+# ---------------------------------------------------------------------------
+# E4M3 codec
+# ---------------------------------------------------------------------------
+def e4m3_decode(codes, lib=None) -> np.ndarray:
+    """float64 values of E4M3 codes (any shape)."""
+    c = _c(codes, np.uint8)
+    out = np.empty(c.shape, dtype=np.float64)
+    _load(lib).pkv_oracle_e4m3_decode_array(_ptr(c), _ptr(out), c.size)
+    return out
+
+
+def e4m3_encode(x: float, lib=None) -> int:
+    return int(_load(lib).pkv_oracle_e4m3_encode(float(np.float32(x))))
+
+
+def e4m3_quantize(x_bf16_bits, scales_per_elem, lib=None) -> np.ndarray:
+    """E4M3 codes of float(x) / scale (binary32 division), elementwise."""
+    x = _c(x_bf16_bits, np.uint16)
+    s = _c(np.broadcast_to(scales_per_elem, x.shape), np.float32)
+    out = np.empty(x.shape, dtype=np.uint8)
+    _load(lib).pkv_oracle_e4m3_quantize_array(_ptr(x), _ptr(s), _ptr(out), x.size)
+    return out
+
+
+def quantize_cache(src_bits: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """E4M3 cache [S][NB][Hkv][bs][D] from bf16 source and [S][NB][Hkv] scales."""
+    S, NB, Hkv, bs, D = src_bits.shape
+    out = np.empty(src_bits.shape, dtype=np.uint8)
+    lib = _load()
+    # one page-chunk at a time keeps the broadcast scale array small
+    flat_src = src_bits.reshape(S * NB * Hkv, bs * D)
+    flat_out = out.reshape(S * NB * Hkv, bs * D)
+    flat_sc = scales.reshape(-1)
+    step = 1 << 13
+    for s in range(0, flat_src.shape[0], step):
+        e = min(flat_src.shape[0], s + step)
+        x = np.ascontiguousarray(flat_src[s:e])
+        sc = np.ascontiguousarray(np.repeat(flat_sc[s:e, None], bs * D, axis=1), dtype=np.float32)
+        o = np.empty(x.shape, dtype=np.uint8)
+        lib.pkv_oracle_e4m3_quantize_array(_ptr(x), _ptr(sc), _ptr(o), x.size)
+        flat_out[s:e] = o
+    return out
+
+
+# ---------------------------------------------------------------------------
+# KV append and paged decode
+# ---------------------------------------------------------------------------
+def kv_append(k_new, v_new, slot_mapping, k_cache: np.ndarray, v_cache: np.ndarray,
+              k_scale=None, v_scale=None, slot: int = 0, lib=None) -> int:
+    """In-place scatter of new tokens into ``k_cache``/``v_cache`` (numpy).
+
+    Caches are ``[S][NB][Hkv][bs][D]`` uint16 (bf16 bits) or uint8 (E4M3).
+    Returns the oracle status (0 = ok)."""
+    fp8 = k_cache.dtype == np.uint8
+    S, NB, Hkv, bs, D = k_cache.shape
+    kn = _c(k_new, np.uint16)
+    vn = _c(v_new, np.uint16)
+    sm = _c(slot_mapping, np.int64)
+    assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+    ks = _c(k_scale, np.float32) if fp8 else None
+    vs = _c(v_scale, np.float32) if fp8 else None
+    return int(_load(lib).pkv_oracle_kv_append(
+        _ptr(kn), _ptr(vn), _ptr(sm), int(sm.shape[0]), _ptr(k_cache), _ptr(v_cache),
+        int(fp8), _ptr(ks), _ptr(vs), S, NB, Hkv, bs, D, int(slot)))
+
+
+def paged_decode(q_bits, k_cache, v_cache, block_tables, context_lens, kv_group_ptr,
+                 layer: int, scale: float, k_scale=None, v_scale=None,
+                 pairs=None, lib=None) -> np.ndarray:
+    """float64 [B][Hq][D] attention output (see pkv_oracle.c for the definition).
+
+    ``pairs``: optional int array [n][2] of (b, h) to compute; other entries
+    of the result are NaN.  Raises ValueError on an oracle status != 0."""
+    q = _c(q_bits, np.uint16)
+    B, Hq, D = q.shape
+    fp8 = k_cache.dtype == np.uint8
+    kc = _c(k_cache, k_cache.dtype)
+    vc = _c(v_cache, v_cache.dtype)
+    S, NB, Hkv, bs, Dc = kc.shape
+    assert Dc == D
+    bt = _c(block_tables, np.int32)
+    cl = _c(context_lens, np.int32)
+    gp = _c(kv_group_ptr, np.int32)
+    ks = _c(k_scale, np.float32) if fp8 else None
+    vs = _c(v_scale, np.float32) if fp8 else None
+    out = np.full((B, Hq, D), np.nan if pairs is not None else 0.0, dtype=np.float64)
+    pr = None if pairs is None else _c(pairs, np.int32).reshape(-1, 2)
+    rc = _load(lib).pkv_oracle_paged_decode(
+        _ptr(q), B, Hq, _ptr(kc), _ptr(vc), int(fp8), _ptr(ks), _ptr(vs),
+        S, NB, Hkv, bs, D, _ptr(bt), int(bt.shape[1]), _ptr(cl), _ptr(gp), int(gp.shape[0]),
+        int(layer), float(np.float32(scale)), _ptr(out), _ptr(pr),
+        0 if pr is None else int(pr.shape[0]))
+    if rc != ORACLE_OK:
+        raise ValueError(f"oracle paged_decode status {rc}")
+    return out

@@ -1,0 +1,377 @@
+"""Pins of the CPU oracle against things other than itself.
+
+* torch's float64 scaled_dot_product_attention on the dense logical sequence
+  (a library routine; the paged cache here is built by scattering the dense
+  sequence into random physical blocks, the opposite direction of the
+  oracle's gather) -- "PagedAttention" on the bandwidth-wall page: the block
+  table maps logical to physical blocks and the kernel finds K/V through it;
+* torch's float8_e4m3fn conversion (library) and the OCP E4M3 field values
+  for the codec -- "Quantized KV Cache / FP8 KV cache";
+* closed forms (one token, equal keys, one dominant key) and invariants
+  (physical block permutation, shared prefix blocks, poisoned unused rows,
+  GQA vs repeated MHA heads, the cross-layer shared-with pointer).
+
+Every pin is a function of the oracle library so that ``test_planted_mistakes``
+can run the same pins against copies of the oracle with a mistake planted in
+them and check that at least one pin fails for each.
+"""
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+from workloads import bf16_bits_from_f32, bf16_bits_to_f32, normal_bf16_bits
+from tests._paged import (dense_bf16_seqs, paged_from_dense, sdpa_reference,
+                          torch_e4m3_to_f64, torch_f32_to_e4m3)
+
+TOL = 1e-12
+
+
+def _f64(bits):
+    return bf16_bits_to_f32(bits).astype(np.float64)
+
+
+# ---------------------------------------------------------------------------
+# attention pins
+# ---------------------------------------------------------------------------
+def pin_sdpa_bf16(lib=None):
+    configs = [  # (Hq, Hkv, D, bs, lens)
+        (8, 2, 64, 16, [37, 100]),
+        (4, 4, 64, 16, [1, 16, 17, 0]),
+        (8, 1, 128, 32, [33, 64, 5]),
+        (16, 2, 128, 16, [48, 250]),
+        (8, 8, 128, 32, [31, 32, 95]),
+    ]
+    for i, (Hq, Hkv, D, bs, lens) in enumerate(configs):
+        ks, vs = dense_bf16_seqs(100 + i, lens, Hkv, D)
+        kc, vc, bt, ctx, _ = paged_from_dense(ks, vs, bs, seed=200 + i)
+        q = normal_bf16_bits(300 + i, (len(lens), Hq, D))
+        scale = float(np.float32(1 / np.sqrt(D)))
+        got = oracle.paged_decode(q, kc, vc, bt, ctx, [0], 0, scale, lib=lib)
+        want = sdpa_reference(q, [_f64(k) for k in ks], [_f64(v) for v in vs], scale)
+        np.testing.assert_allclose(got, want, rtol=TOL, atol=TOL, err_msg=f"config {i}")
+
+
+def pin_large_logits(lib=None):
+    # logits of order +-1e3: the softmax must subtract the running maximum
+    lens, Hq, Hkv, D, bs = [40, 7], 4, 2, 64, 16
+    rng = np.random.Generator(np.random.PCG64(5))
+    ks = [bf16_bits_from_f32(rng.standard_normal((n, Hkv, D), dtype=np.float32) * 20) for n in lens]
+    vs = [bf16_bits_from_f32(rng.standard_normal((n, Hkv, D), dtype=np.float32)) for n in lens]
+    q = bf16_bits_from_f32(rng.standard_normal((2, Hq, D), dtype=np.float32) * 20)
+    kc, vc, bt, ctx, _ = paged_from_dense(ks, vs, bs, seed=6)
+    got = oracle.paged_decode(q, kc, vc, bt, ctx, [0], 0, 0.125, lib=lib)
+    want = sdpa_reference(q, [_f64(k) for k in ks], [_f64(v) for v in vs], 0.125)
+    assert np.all(np.isfinite(got))
+    np.testing.assert_allclose(got, want, rtol=1e-10, atol=1e-10)
+
+
+def pin_closed_forms(lib=None):
+    Hq, Hkv, D, bs = 4, 2, 64, 16
+    # one token: the output is that token's V, exactly
+    ks, vs = dense_bf16_seqs(7, [1], Hkv, D)
+    kc, vc, bt, ctx, _ = paged_from_dense(ks, vs, bs, seed=8)
+    q = normal_bf16_bits(9, (1, Hq, D))
+    got = oracle.paged_decode(q, kc, vc, bt, ctx, [0], 0, 0.125, lib=lib)
+    for h in range(Hq):
+        assert np.array_equal(got[0, h], _f64(vs[0][0, h // (Hq // Hkv)]))
+    # all keys equal: the output is the mean of V
+    n = 45
+    k_one = normal_bf16_bits(10, (1, Hkv, D))
+    ks = [np.repeat(k_one, n, axis=0)]
+    vs = [normal_bf16_bits(11, (n, Hkv, D))]
+    kc, vc, bt, ctx, _ = paged_from_dense(ks, vs, bs, seed=12)
+    got = oracle.paged_decode(q, kc, vc, bt, ctx, [0], 0, 0.125, lib=lib)
+    mean = _f64(vs[0]).mean(axis=0)
+    for h in range(Hq):
+        np.testing.assert_allclose(got[0, h], mean[h // (Hq // Hkv)], rtol=TOL, atol=TOL)
+    # one dominant key: the output is that token's V
+    n, j = 50, 29
+    kd = np.zeros((n, Hkv, D), dtype=np.float32)
+    kd[j, :, 0] = 64.0
+    qd = np.zeros((1, Hq, D), dtype=np.float32)
+    qd[0, :, 0] = 8.0
+    ks = [bf16_bits_from_f32(kd)]
+    vs = [normal_bf16_bits(13, (n, Hkv, D))]
+    kc, vc, bt, ctx, _ = paged_from_dense(ks, vs, bs, seed=14)
+    got = oracle.paged_decode(bf16_bits_from_f32(qd), kc, vc, bt, ctx, [0], 0, 0.125, lib=lib)
+    for h in range(Hq):
+        np.testing.assert_allclose(got[0, h], _f64(vs[0][j, h // (Hq // Hkv)]), rtol=0, atol=1e-12)
+
+
+def pin_permutation_invariance(lib=None):
+    Hq, Hkv, D, bs, lens = 8, 2, 64, 16, [70, 33, 16]
+    ks, vs = dense_bf16_seqs(20, lens, Hkv, D)
+    q = normal_bf16_bits(21, (3, Hq, D))
+    outs = []
+    for seed in (1, 2, 3):
+        kc, vc, bt, ctx, _ = paged_from_dense(ks, vs, bs, seed=seed, spare=4)
+        outs.append(oracle.paged_decode(q, kc, vc, bt, ctx, [0], 0, 0.125, lib=lib))
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+
+
+def pin_shared_prefix(lib=None):
+    # three sequences whose first two blocks hold the same tokens: aliasing
+    # those blocks in the tables must give the same result as private copies
+    Hq, Hkv, D, bs = 4, 1, 64, 16
+    prefix_k = normal_bf16_bits(30, (32, Hkv, D))
+    prefix_v = normal_bf16_bits(31, (32, Hkv, D))
+    tails = [10, 0, 21]
+    ks = [np.concatenate([prefix_k, normal_bf16_bits(32 + i, (t, Hkv, D))]) for i, t in enumerate(tails)]
+    vs = [np.concatenate([prefix_v, normal_bf16_bits(40 + i, (t, Hkv, D))]) for i, t in enumerate(tails)]
+    q = normal_bf16_bits(33, (3, Hq, D))
+    kc, vc, bt, ctx, pl = paged_from_dense(ks, vs, bs, seed=34)
+    private = oracle.paged_decode(q, kc, vc, bt, ctx, [0], 0, 0.125, lib=lib)
+    bt2 = bt.copy()
+    for b in (1, 2):
+        bt2[b, :2] = bt[0, :2]          # alias sequence 0's prefix blocks
+        for p in pl[b][:2]:             # and poison the private copies
+            kc[0, p] = 0x7FC0
+            vc[0, p] = 0x7FC0
+    aliased = oracle.paged_decode(q, kc, vc, bt2, ctx, [0], 0, 0.125, lib=lib)
+    assert np.array_equal(private, aliased)
+
+
+def pin_poisoned_unused(lib=None):
+    Hq, Hkv, D, bs, lens = 8, 2, 64, 16, [37, 100, 16]
+    ks, vs = dense_bf16_seqs(50, lens, Hkv, D)
+    q = normal_bf16_bits(51, (3, Hq, D))
+    kc, vc, bt, ctx, _ = paged_from_dense(ks, vs, bs, seed=52, spare=3, MB=9)
+    clean = oracle.paged_decode(q, kc, vc, bt, ctx, [0], 0, 0.125, lib=lib)
+    kp = np.where(kc == 0, np.uint16(0x7FC0), kc)   # unused rows were zero-filled
+    vp = np.where(vc == 0, np.uint16(0x7FC0), vc)
+    btp = np.where(bt < 0, np.int32(10 ** 6), bt)
+    dirty = oracle.paged_decode(q, kp, vp, btp, ctx, [0], 0, 0.125, lib=lib)
+    assert np.all(np.isfinite(dirty))
+    assert np.array_equal(clean, dirty)
+
+
+def pin_gqa_equals_repeated_mha(lib=None):
+    Hq, Hkv, D, bs, lens = 8, 2, 128, 32, [40, 77]
+    G = Hq // Hkv
+    ks, vs = dense_bf16_seqs(60, lens, Hkv, D)
+    q = normal_bf16_bits(61, (2, Hq, D))
+    kc, vc, bt, ctx, _ = paged_from_dense(ks, vs, bs, seed=62)
+    gqa = oracle.paged_decode(q, kc, vc, bt, ctx, [0], 0, 0.0883883, lib=lib)
+    kr = np.ascontiguousarray(np.repeat(kc, G, axis=2))
+    vr = np.ascontiguousarray(np.repeat(vc, G, axis=2))
+    mha = oracle.paged_decode(q, kr, vr, bt, ctx, [0], 0, 0.0883883, lib=lib)
+    assert np.array_equal(gqa, mha)
+
+
+def pin_shared_with_pointer(lib=None):
+    # two cache slots with different contents; layer l reads slot ptr[l]
+    Hq, Hkv, D, bs, lens = 4, 2, 64, 16, [20, 50]
+    ptr = [1, 0, 1]
+    ks0, vs0 = dense_bf16_seqs(70, lens, Hkv, D)
+    ks1, vs1 = dense_bf16_seqs(71, lens, Hkv, D)
+    kc, vc, bt, ctx, _ = paged_from_dense(ks0, vs0, bs, seed=72, slots=2, slot=0)
+    kc1, vc1, _, _, _ = paged_from_dense(ks1, vs1, bs, seed=72, slots=2, slot=1)
+    kc[1], vc[1] = kc1[1], vc1[1]
+    q = normal_bf16_bits(73, (2, Hq, D))
+    for layer, slot in enumerate(ptr):
+        got = oracle.paged_decode(q, kc, vc, bt, ctx, ptr, layer, 0.125, lib=lib)
+        ks, vs = (ks0, vs0) if slot == 0 else (ks1, vs1)
+        want = sdpa_reference(q, [_f64(k) for k in ks], [_f64(v) for v in vs], 0.125)
+        np.testing.assert_allclose(got, want, rtol=TOL, atol=TOL)
+
+
+def pin_sdpa_fp8(lib=None):
+    # E4M3 pages with one scale per (block, KV head): the reference decodes
+    # the same codes with torch and multiplies by the page's scale
+    Hq, Hkv, D, bs, lens = 8, 2, 128, 32, [70, 31]
+    rng = np.random.Generator(np.random.PCG64(80))
+    codes = [rng.integers(0, 256, size=(n, Hkv, D), dtype=np.uint8) for n in lens]
+    vcodes = [rng.integers(0, 256, size=(n, Hkv, D), dtype=np.uint8) for n in lens]
+    for c in codes + vcodes:                        # no NaN codes in real data
+        c[(c & 0x7F) == 0x7F] = 0x3F
+    kc, vc, bt, ctx, pl = paged_from_dense(codes, vcodes, bs, seed=81)
+    NB = kc.shape[1]
+    ks = rng.uniform(0.01, 2.0, size=(1, NB, Hkv)).astype(np.float32)
+    vsc = rng.uniform(0.01, 2.0, size=(1, NB, Hkv)).astype(np.float32)
+    q = normal_bf16_bits(82, (2, Hq, D))
+    got = oracle.paged_decode(q, kc, vc, bt, ctx, [0], 0, 0.0883883, k_scale=ks, v_scale=vsc, lib=lib)
+    kd, vd = [], []
+    for b, n in enumerate(lens):
+        tok_blk = np.array([pl[b][t // bs] for t in range(n)])
+        kd.append(torch_e4m3_to_f64(codes[b]) * ks[0, tok_blk][:, :, None].astype(np.float64))
+        vd.append(torch_e4m3_to_f64(vcodes[b]) * vsc[0, tok_blk][:, :, None].astype(np.float64))
+    want = sdpa_reference(q, kd, vd, 0.0883883)
+    np.testing.assert_allclose(got, want, rtol=TOL, atol=TOL)
+
+
+def pin_bad_inputs_rejected(lib=None):
+    Hq, Hkv, D, bs, lens = 4, 2, 64, 16, [20]
+    ks, vs = dense_bf16_seqs(90, lens, Hkv, D)
+    kc, vc, bt, ctx, _ = paged_from_dense(ks, vs, bs, seed=91)
+    q = normal_bf16_bits(92, (1, Hq, D))
+    bad = bt.copy()
+    bad[0, 1] = kc.shape[1]
+    with pytest.raises(ValueError):
+        oracle.paged_decode(q, kc, vc, bad, ctx, [0], 0, 0.125, lib=lib)
+    with pytest.raises(ValueError):
+        oracle.paged_decode(q, kc, vc, bt, np.array([bt.shape[1] * bs + 1], np.int32), [0], 0, 0.125, lib=lib)
+
+
+# ---------------------------------------------------------------------------
+# codec pins
+# ---------------------------------------------------------------------------
+def pin_e4m3_decode_all_codes(lib=None):
+    codes = np.arange(256, dtype=np.uint8)
+    got = oracle.e4m3_decode(codes, lib=lib)
+    want = torch_e4m3_to_f64(codes)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(want[~nan]))
+    # OCP E4M3 anchors: max 448 = S.1111.110, min normal 2^-6, min subnormal 2^-9, 1.0
+    anchors = {0x7E: 448.0, 0xFE: -448.0, 0x08: 2.0 ** -6, 0x01: 2.0 ** -9, 0x38: 1.0, 0x00: 0.0}
+    for c, v in anchors.items():
+        assert got[c] == v
+    assert np.isnan(got[0x7F]) and np.isnan(got[0xFF])
+
+
+def pin_e4m3_encode_matches_library(lib=None):
+    # every bf16 pattern whose magnitude is below 464 (where a non-saturating
+    # RNE conversion and the saturating one agree), as float32
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    x = bf16_bits_to_f32(bits)
+    keep = np.isfinite(x) & (np.abs(x) < 464)
+    x = x[keep]
+    got = oracle.e4m3_quantize(bf16_bits_from_f32(x), np.float32(1.0), lib=lib)
+    want = torch_f32_to_e4m3(x)
+    assert np.array_equal(got, want)
+    # saturation of finite values above the range, and NaN stays NaN
+    for v in (464.0, 480.0, 1e4, 3e38, float("inf")):
+        assert oracle.e4m3_encode(v, lib=lib) == 0x7E
+        assert oracle.e4m3_encode(-v, lib=lib) == 0xFE
+    assert oracle.e4m3_encode(float("nan"), lib=lib) & 0x7F == 0x7F
+    # round trip of every finite code
+    for c in range(256):
+        if c & 0x7F == 0x7F:
+            continue
+        v = oracle.e4m3_decode(np.array([c], np.uint8), lib=lib)[0]
+        assert oracle.e4m3_encode(v, lib=lib) == c
+
+
+def pin_e4m3_scaled_quantize(lib=None):
+    rng = np.random.Generator(np.random.PCG64(95))
+    x = normal_bf16_bits(96, (4096,))
+    for s in (np.float32(1.0), np.float32(0.0091), np.float32(3.7), np.float32(1 / 448)):
+        got = oracle.e4m3_quantize(x, s, lib=lib)
+        q = (bf16_bits_to_f32(x) / s).astype(np.float32)
+        q = np.clip(q, -448, 448)
+        assert np.array_equal(got, torch_f32_to_e4m3(q))
+    del rng
+
+
+# ---------------------------------------------------------------------------
+# append pins
+# ---------------------------------------------------------------------------
+def pin_append_scatter(lib=None):
+    S, NB, Hkv, bs, D = 2, 9, 2, 16, 64
+    rng = np.random.Generator(np.random.PCG64(97))
+    kc = rng.integers(0, 1 << 16, size=(S, NB, Hkv, bs, D), dtype=np.uint16)
+    vc = rng.integers(0, 1 << 16, size=(S, NB, Hkv, bs, D), dtype=np.uint16)
+    k0, v0 = kc.copy(), vc.copy()
+    N = 20
+    slots = rng.choice(NB * bs, size=N, replace=False).astype(np.int64)
+    slots[3] = -1
+    kn = normal_bf16_bits(98, (N, Hkv, D))
+    vn = normal_bf16_bits(99, (N, Hkv, D))
+    assert oracle.kv_append(kn, vn, slots, kc, vc, slot=1, lib=lib) == 0
+    for i, s in enumerate(slots):
+        if s < 0:
+            continue
+        blk, off = divmod(int(s), bs)
+        for h in range(Hkv):
+            assert np.array_equal(kc[1, blk, h, off], kn[i, h])
+            assert np.array_equal(vc[1, blk, h, off], vn[i, h])
+            k0[1, blk, h, off] = kn[i, h]
+            v0[1, blk, h, off] = vn[i, h]
+    assert np.array_equal(kc, k0) and np.array_equal(vc, v0)   # nothing else moved
+    bad = slots.copy()
+    bad[0] = NB * bs
+    kc2 = kc.copy()
+    assert oracle.kv_append(kn, vn, bad, kc2, vc, slot=1, lib=lib) == oracle.ORACLE_BAD_SLOT
+    assert np.array_equal(kc2, kc)
+
+
+def pin_append_fp8(lib=None):
+    S, NB, Hkv, bs, D = 1, 6, 2, 32, 128
+    rng = np.random.Generator(np.random.PCG64(100))
+    kc = np.zeros((S, NB, Hkv, bs, D), np.uint8)
+    vc = np.zeros((S, NB, Hkv, bs, D), np.uint8)
+    ks = rng.uniform(0.005, 0.05, size=(S, NB, Hkv)).astype(np.float32)
+    vs = rng.uniform(0.005, 0.05, size=(S, NB, Hkv)).astype(np.float32)
+    N = 12
+    slots = rng.choice(NB * bs, size=N, replace=False).astype(np.int64)
+    kn = normal_bf16_bits(101, (N, Hkv, D))
+    vn = normal_bf16_bits(102, (N, Hkv, D))
+    assert oracle.kv_append(kn, vn, slots, kc, vc, ks, vs, lib=lib) == 0
+    for i, s in enumerate(slots):
+        blk, off = divmod(int(s), bs)
+        for h in range(Hkv):
+            qk = np.clip(bf16_bits_to_f32(kn[i, h]) / ks[0, blk, h], -448, 448).astype(np.float32)
+            qv = np.clip(bf16_bits_to_f32(vn[i, h]) / vs[0, blk, h], -448, 448).astype(np.float32)
+            assert np.array_equal(kc[0, blk, h, off], torch_f32_to_e4m3(qk))
+            assert np.array_equal(vc[0, blk, h, off], torch_f32_to_e4m3(qv))
+
+
+PINS = [pin_sdpa_bf16, pin_large_logits, pin_closed_forms, pin_permutation_invariance,
+        pin_shared_prefix, pin_poisoned_unused, pin_gqa_equals_repeated_mha,
+        pin_shared_with_pointer, pin_sdpa_fp8, pin_bad_inputs_rejected,
+        pin_e4m3_decode_all_codes, pin_e4m3_encode_matches_library, pin_e4m3_scaled_quantize,
+        pin_append_scatter, pin_append_fp8]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
+def test_pin(pin):
+    pin()
+
+
+# ---------------------------------------------------------------------------
+# planted mistakes: each must make at least one pin fail
+# ---------------------------------------------------------------------------
+MUTANTS = [
+    ("gather_wrong_block", "block_tables[(int64_t)b * MB + t / bs];\n        int64_t page",
+     "block_tables[(int64_t)b * MB + (t / bs) / 2];\n        int64_t page"),
+    ("gqa_strided_heads", "int32_t g = h / G;", "int32_t g = h % Hkv;"),
+    ("scale_dropped", "s[t] = (double)scale * dot;", "s[t] = dot;"),
+    ("no_max_subtraction", "s[t] = exp(s[t] - smax);", "s[t] = exp(s[t]);"),
+    ("no_normalisation", "double p = s[t] / z;", "double p = s[t];"),
+    ("rows_reversed", "page, bs, D, t % bs, d)", "page, bs, D, bs - 1 - t % bs, d)"),
+    ("last_dim_dropped", "for (int32_t d = 0; d < D; ++d)\n          dot +=",
+     "for (int32_t d = 0; d < D - 1; ++d)\n          dot +="),
+    ("v_from_k_cache", "cache_value(v_cache, fp8, v_scale", "cache_value(k_cache, fp8, k_scale"),
+    ("slot_ignored", "int64_t page = ((int64_t)slot * NB + blk) * Hkv + g;",
+     "int64_t page = ((int64_t)0 * NB + blk) * Hkv + g;"),
+    ("fp8_scale_dropped", "* (double)scales[page];", "* 1.0;"),
+    ("e4m3_wrong_bias", "mag = ldexp(1.0 + (double)mantissa / 8.0, exponent - 7);",
+     "mag = ldexp(1.0 + (double)mantissa / 8.0, exponent - 6);"),
+    ("e4m3_ties_up", "else code = (lo % 2 == 0) ? lo : lo + 1;", "else code = lo + 1;"),
+    ("append_wrong_offset", "int64_t blk = s / bs, off = s % bs;", "int64_t blk = s / bs, off = (s + 1) % bs;"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_planted_mistakes(name, old, new, tmp_path):
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "pkv_oracle.c")).read()
+    assert src.count(old) >= 1, f"mutation anchor not found: {name}"
+    mutated = src.replace(old, new)
+    c = tmp_path / f"{name}.c"
+    so = tmp_path / f"{name}.so"
+    c.write_text(mutated)
+    subprocess.run(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+                    "-o", str(so), str(c), "-lm"], check=True)
+    lib = oracle.load_library(str(so))
+    failed = []
+    for pin in PINS:
+        try:
+            pin(lib)
+        except (AssertionError, ValueError):
+            failed.append(pin.__name__)
+    assert failed, f"no pin caught the planted mistake {name}"
