@@ -1,0 +1,200 @@
+/*
+ * pkv -- paged KV-cache decode attention for NVIDIA GB300 (sm_103a).
+ *
+ * C ABI.  Every pointer argument is a plain address; "device" pointers are
+ * CUDA device (or managed) memory owned by the caller, "host" pointers are
+ * ordinary host memory owned by the caller.  The library keeps no reference
+ * to any argument after a call returns.  All GPU work is enqueued on the
+ * caller's stream (`stream` is a cudaStream_t; NULL = the legacy default
+ * stream) and runs asynchronously; a PKV_OK return means "validated and
+ * launched", not "finished".
+ *
+ * Citations name the web page and section the operation comes from:
+ *   [BW] "KV Cache Engineering: PagedAttention, Continuous Batching,
+ *        Attention Variants, and the Bandwidth Wall"
+ *   [PC] "KV-Cache Engineering: Paged Attention, Prefix Cache,
+ *        Disaggregation (2026)"
+ *
+ * Data layout (the pages draw physical blocks as opaque boxes; this layout
+ * is the library's choice):
+ *   k_cache, v_cache  [S][NB][Hkv][bs][D]   S cache slots (layer groups),
+ *                     NB physical blocks, Hkv KV heads, bs tokens per block,
+ *                     D head_dim.  Element type bf16 or FP8 E4M3 (1 byte).
+ *                     One (slot, block, KV head) page is a contiguous
+ *                     bs*D run.
+ *   k_scale, v_scale  fp32 [S][NB][Hkv]     E4M3 caches only: one scale per
+ *                     page; stored value = e4m3(x / scale).
+ *   q, out            bf16 [B][Hq][D]       one query token per sequence.
+ *   block_tables      int32 [B][MB]         logical block j of sequence b is
+ *                     physical block block_tables[b*MB + j].
+ *   context_lens      int32 [B]             tokens sequence b attends to,
+ *                     including the token appended this step; 0 = inactive.
+ * Query head h belongs to KV head h / G with G = Hq / Hkv (contiguous GQA
+ * groups; G = 1 is MHA, Hkv = 1 is MQA).
+ *
+ * Errors.  Argument problems the host can see (null or misaligned pointers,
+ * unsupported shapes, a shared-with pointer outside the slots, a workspace
+ * that is too small) return a status before anything is launched.
+ * Problems only the data shows (a block id outside [0, NB), a slot outside
+ * [-1, NB*bs), a context length outside [0, MB*bs]) are skipped on the
+ * device: the offending page, token or sequence contributes nothing, and a
+ * sticky device error word records the kind of fault; read it with
+ * pkv_read_device_error().  Kernels never trap.  With the environment
+ * variable PKV_VALIDATE=1 the host also copies the tables back and checks
+ * them before launching (slow; synchronises the stream).
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PKV_ABI_VERSION 1
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARG = 1,   /* null pointer, bad size, bad index argument */
+  PKV_ERR_UNSUPPORTED = 2,   /* shape or dtype this build has no kernel for */
+  PKV_ERR_ALIGNMENT = 3,     /* a tensor is not 16-byte aligned */
+  PKV_ERR_CUDA = 4,          /* a CUDA runtime/driver call or launch failed */
+  PKV_ERR_DEVICE_INDEX = 5,  /* the device error word was non-zero */
+  PKV_ERR_WORKSPACE = 6      /* workspace missing or smaller than required */
+} pkv_status;
+
+typedef enum { PKV_KV_BF16 = 0, PKV_KV_FP8_E4M3 = 1 } pkv_kv_dtype;
+
+/* Bits of the device error word. */
+#define PKV_DEVERR_BLOCK_ID 0x1u     /* block table entry outside [0, NB) */
+#define PKV_DEVERR_SLOT 0x2u         /* slot_mapping entry outside [-1, NB*bs) */
+#define PKV_DEVERR_CONTEXT_LEN 0x4u  /* context length outside [0, MB*bs] */
+#define PKV_DEVERR_TIMEOUT 0x8u      /* a bounded wait on a copy gave up */
+
+/* Shape of one paged cache (both K and V).  Supported: block_size 16 or 32;
+ * head_dim 64 or 128 for bf16, 128 for E4M3. */
+typedef struct {
+  int32_t num_slots;    /* S: independent caches (layer groups) */
+  int32_t num_blocks;   /* NB: physical blocks per slot */
+  int32_t block_size;   /* bs: tokens per block */
+  int32_t num_kv_heads; /* Hkv */
+  int32_t head_dim;     /* D */
+  int32_t dtype;        /* pkv_kv_dtype */
+} pkv_cache_desc;
+
+/* How the decode computes its dot products. */
+typedef enum {
+  PKV_MATH_AUTO = 0, /* the library picks (tensor-core mma when supported) */
+  PKV_MATH_FFMA = 1, /* fp32 CUDA-core FMAs; G must be 1, 2, 4 or 8 */
+  PKV_MATH_MMA = 2   /* mma.sync tiles (bf16, or f16 for E4M3); G <= 16 */
+} pkv_decode_math;
+
+/* Tuning knobs of pkv_paged_decode; a NULL pointer or zero fields = auto. */
+typedef struct {
+  int32_t partition_blocks; /* blocks per split-K partition, 1..64 (0 = auto) */
+  int32_t math;             /* pkv_decode_math */
+  int32_t warps_per_cta;    /* 1..8 (0 = auto) */
+  int32_t stages;           /* pages in each warp's copy ring, 2..8 (0 = auto) */
+} pkv_decode_opts;
+
+/*
+ * Write new tokens' K and V into their physical slots.
+ * Source: [BW] "What the KV Cache Stores and Why" (each step computes K and
+ * V for the new token only and stores them) and "Continuous Batching" (a
+ * growing sequence takes blocks from the free pool).
+ *
+ *   cache        shape of k_cache / v_cache (host).
+ *   slot         cache slot (layer group) to write, in [0, S).
+ *   k, v         device bf16 [N][Hkv][D]: the new tokens.
+ *   slot_mapping device int64 [N]: physical block * bs + offset; -1 skips the
+ *                token (padding).  Other out-of-range values set
+ *                PKV_DEVERR_SLOT and skip the token.  Two tokens with the
+ *                same slot in one call: unspecified which one lands.
+ *   k_cache, v_cache  device, written in place.
+ *   k_scale, v_scale  device fp32 [S][NB][Hkv], E4M3 caches only (may be NULL
+ *                for bf16): stored byte = e4m3_rn_satfinite(float(x) / scale),
+ *                IEEE binary32 division.  bf16 caches receive the bits as is.
+ * Returns PKV_OK after launching one kernel (none when N == 0).
+ */
+pkv_status pkv_kv_append(const pkv_cache_desc* cache, int32_t slot,
+                         const void* k, const void* v, const int64_t* slot_mapping,
+                         int32_t num_tokens, void* k_cache, void* v_cache,
+                         const float* k_scale, const float* v_scale, void* stream);
+
+/*
+ * Bytes of device workspace pkv_paged_decode needs for these sizes (0 on a
+ * bad argument).  The workspace holds the split-K partials and a small work
+ * queue header; it must be zero-filled once before its first use, and each
+ * call leaves the header ready for the next call on the same stream.  Calls
+ * that run at the same time need separate workspaces.
+ */
+size_t pkv_decode_workspace_bytes(const pkv_cache_desc* cache, int32_t batch,
+                                  int32_t num_q_heads, int32_t max_blocks_per_seq,
+                                  const pkv_decode_opts* opts);
+
+/*
+ * Single-token decode attention over the paged cache, one query token per
+ * sequence:
+ *   out[b][h][:] = sum_t softmax_t(scale * q[b][h] . K_t) V_t,
+ *   t = 0 .. context_lens[b]-1, K_t = k_cache[slot][block_tables[b][t/bs]]
+ *   [h/G][t%bs] (V_t alike), slot = kv_group_ptr[layer].
+ * Sources: [BW] "What the KV Cache Stores and Why" (attend the new Q over all
+ * cached K,V), "PagedAttention" (block table maps logical to physical
+ * blocks; only the last block is partly filled), "Attention Variants"
+ * (grouped-query heads), "FP8 KV cache" (dequantise on read); [PC]
+ * cross-layer KV sharing Q&A (each logical layer has a shared-with pointer
+ * naming its group's cache).
+ *
+ *   q              device bf16 [B][Hq][D].
+ *   k/v_cache      device [S][NB][Hkv][bs][D] as described by `cache`.
+ *   k/v_scale      device fp32 [S][NB][Hkv], E4M3 only (NULL for bf16).
+ *   block_tables   device int32 [B][max_blocks_per_seq]; entries past a
+ *                  sequence's last block are never read.
+ *   context_lens   device int32 [B].
+ *   kv_group_ptr   HOST int32 [num_layers]: the cache slot layer l reads
+ *                  (the shared-with pointer); layers of one group name the
+ *                  same slot.  `layer` selects the entry for this call.
+ *   scale          softmax scale applied to the fp32 logits (e.g. 1/sqrt(D)).
+ *   out            device bf16 [B][Hq][D]; must not overlap q.  Sequences with
+ *                  context_lens 0 get zeros.
+ *   workspace      device, pkv_decode_workspace_bytes() bytes, see there.
+ * Accumulation is fp32; out is rounded to bf16 (round to nearest even).
+ * The reduction order depends only on logical token positions and the
+ * partition size, never on which physical blocks hold the tokens.
+ * Launches up to three kernels: a planner, the decode, and (when some
+ * sequence spans more than one partition) the split-K merge.
+ */
+pkv_status pkv_paged_decode(const pkv_cache_desc* cache,
+                            const void* q, int32_t batch, int32_t num_q_heads,
+                            const void* k_cache, const void* v_cache,
+                            const float* k_scale, const float* v_scale,
+                            const int32_t* block_tables, int32_t max_blocks_per_seq,
+                            const int32_t* context_lens,
+                            const int32_t* kv_group_ptr, int32_t num_layers, int32_t layer,
+                            float scale, void* out,
+                            void* workspace, size_t workspace_bytes,
+                            const pkv_decode_opts* opts, void* stream);
+
+/*
+ * Synchronise `stream`, copy the current device's sticky error word into
+ * *flags (PKV_DEVERR_* bits) and clear it.  Returns PKV_ERR_DEVICE_INDEX if
+ * it was non-zero, PKV_OK if it was zero.
+ */
+pkv_status pkv_read_device_error(uint32_t* flags, void* stream);
+
+/* Static text for a status code. */
+const char* pkv_status_string(pkv_status status);
+
+/* Text of the last error on the calling thread (host validation or CUDA). */
+const char* pkv_last_error_message(void);
+
+/* PKV_ABI_VERSION of the built library. */
+int32_t pkv_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

@@ -1,0 +1,228 @@
+"""Paged KV-cache decode attention for GB300 (sm_103a): Python binding.
+
+A thin ctypes layer over the C ABI in ``include/pkv.h`` (library
+``_lib/libpkv.so``, built in-tree by ``_build.py``).  It only marshals
+arguments: torch tensors supply device pointers and the current CUDA
+stream; every step of the computation runs in the library's kernels.  There
+is no CPU fallback: if the library is missing or the call fails, a
+:class:`PkvError` is raised.
+
+Layouts (see the header for the full contract):
+  k_cache, v_cache  [S][NB][Hkv][bs][D]  torch.bfloat16, or torch.uint8 holding
+                    E4M3 codes (FP8 cache);
+  k_scale, v_scale  float32 [S][NB][Hkv] (FP8 cache only);
+  q, out            bfloat16 [B][Hq][D];
+  block_tables      int32 [B][MB];  context_lens int32 [B];
+  kv_group_ptr      host int32 [L] (shared-with pointer per layer).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libpkv.so")
+
+PKV_OK = 0
+STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "alignment", 4: "cuda",
+                5: "device index error", 6: "workspace"}
+KV_BF16, KV_FP8_E4M3 = 0, 1
+MATH_AUTO, MATH_FFMA, MATH_MMA = 0, 1, 2
+DEVERR_BLOCK_ID, DEVERR_SLOT, DEVERR_CONTEXT_LEN, DEVERR_TIMEOUT = 1, 2, 4, 8
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"pkv status {status} ({STATUS_NAMES.get(status, '?')}): {message}")
+        self.status = status
+
+
+class CacheDesc(ctypes.Structure):
+    _fields_ = [("num_slots", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
+                ("block_size", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
+class DecodeOpts(ctypes.Structure):
+    _fields_ = [("partition_blocks", ctypes.c_int32), ("math", ctypes.c_int32),
+                ("warps_per_cta", ctypes.c_int32), ("stages", ctypes.c_int32)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def load() -> ctypes.CDLL:
+    """Load the built library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise PkvError(4, f"CUDA library not built: {LIB_PATH} is missing "
+                              "(run paged_kv_cache_274_gb300._build.build())")
+        lib = ctypes.CDLL(LIB_PATH)
+        P, i32, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+        pdesc, popts = ctypes.POINTER(CacheDesc), ctypes.POINTER(DecodeOpts)
+        lib.pkv_kv_append.restype = ctypes.c_int
+        lib.pkv_kv_append.argtypes = [pdesc, i32, P, P, P, i32, P, P, P, P, P]
+        lib.pkv_decode_workspace_bytes.restype = sz
+        lib.pkv_decode_workspace_bytes.argtypes = [pdesc, i32, i32, i32, popts]
+        lib.pkv_paged_decode.restype = ctypes.c_int
+        lib.pkv_paged_decode.argtypes = [pdesc, P, i32, i32, P, P, P, P, P, i32, P, P, i32, i32,
+                                         f32, P, P, sz, popts, P]
+        lib.pkv_read_device_error.restype = ctypes.c_int
+        lib.pkv_read_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), P]
+        lib.pkv_status_string.restype = ctypes.c_char_p
+        lib.pkv_status_string.argtypes = [ctypes.c_int]
+        lib.pkv_last_error_message.restype = ctypes.c_char_p
+        lib.pkv_last_error_message.argtypes = []
+        lib.pkv_abi_version.restype = ctypes.c_int32
+        lib.pkv_abi_version.argtypes = []
+        _lib = lib
+        return lib
+
+
+def _check(status: int):
+    if status != PKV_OK:
+        msg = load().pkv_last_error_message().decode(errors="replace")
+        raise PkvError(status, msg)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need_cuda(name: str, t: torch.Tensor, dtype=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise PkvError(1, f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise PkvError(1, f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise PkvError(1, f"{name} must be {dtype}, got {t.dtype}")
+
+
+def cache_desc(k_cache: torch.Tensor) -> CacheDesc:
+    """Descriptor of a [S][NB][Hkv][bs][D] cache tensor (bf16, or uint8 = E4M3)."""
+    if k_cache.dim() != 5:
+        raise PkvError(1, "cache must be 5-D [S][NB][Hkv][bs][D]")
+    if k_cache.dtype == torch.bfloat16:
+        dt = KV_BF16
+    elif k_cache.dtype == torch.uint8:
+        dt = KV_FP8_E4M3
+    else:
+        raise PkvError(1, f"cache dtype {k_cache.dtype} (bfloat16 or uint8 E4M3 codes)")
+    S, NB, Hkv, bs, D = (int(x) for x in k_cache.shape)
+    return CacheDesc(S, NB, bs, Hkv, D, dt)
+
+
+def kv_append(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+              k_cache: torch.Tensor, v_cache: torch.Tensor,
+              k_scale: Optional[torch.Tensor] = None, v_scale: Optional[torch.Tensor] = None,
+              slot: int = 0, stream=None) -> None:
+    """Write new tokens k, v [N][Hkv][D] (bf16) into cache slot ``slot`` at
+    ``slot_mapping`` (int64 [N], -1 = skip)."""
+    desc = cache_desc(k_cache)
+    for n, t in (("k", k), ("v", v)):
+        _need_cuda(n, t, torch.bfloat16)
+    _need_cuda("slot_mapping", slot_mapping, torch.int64)
+    _need_cuda("k_cache", k_cache)
+    _need_cuda("v_cache", v_cache, k_cache.dtype)
+    N = int(slot_mapping.shape[0])
+    if k.shape != (N, desc.num_kv_heads, desc.head_dim) or v.shape != k.shape:
+        raise PkvError(1, f"k/v must be [{N}][{desc.num_kv_heads}][{desc.head_dim}]")
+    if desc.dtype == KV_FP8_E4M3:
+        _need_cuda("k_scale", k_scale, torch.float32)
+        _need_cuda("v_scale", v_scale, torch.float32)
+    _check(load().pkv_kv_append(ctypes.byref(desc), int(slot), _ptr(k), _ptr(v), _ptr(slot_mapping),
+                                N, _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                                _stream_handle(stream)))
+
+
+def decode_opts(partition_blocks: int = 0, math: int = MATH_AUTO, warps: int = 0,
+                stages: int = 0) -> DecodeOpts:
+    return DecodeOpts(int(partition_blocks), int(math), int(warps), int(stages))
+
+
+def decode_workspace_bytes(k_cache: torch.Tensor, batch: int, num_q_heads: int,
+                           max_blocks_per_seq: int, opts: Optional[DecodeOpts] = None) -> int:
+    desc = cache_desc(k_cache)
+    n = load().pkv_decode_workspace_bytes(ctypes.byref(desc), int(batch), int(num_q_heads),
+                                          int(max_blocks_per_seq),
+                                          ctypes.byref(opts) if opts is not None else None)
+    if n == 0:
+        raise PkvError(1, "bad arguments for the decode workspace")
+    return int(n)
+
+
+def new_decode_workspace(k_cache: torch.Tensor, batch: int, num_q_heads: int,
+                         max_blocks_per_seq: int, opts: Optional[DecodeOpts] = None) -> torch.Tensor:
+    """Zero-filled device workspace for :func:`paged_decode`."""
+    n = decode_workspace_bytes(k_cache, batch, num_q_heads, max_blocks_per_seq, opts)
+    return torch.zeros(n, dtype=torch.uint8, device=k_cache.device)
+
+
+def paged_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                 block_tables: torch.Tensor, context_lens: torch.Tensor,
+                 kv_group_ptr: Sequence[int] = (0,), layer: int = 0,
+                 scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                 workspace: Optional[torch.Tensor] = None,
+                 k_scale: Optional[torch.Tensor] = None, v_scale: Optional[torch.Tensor] = None,
+                 opts: Optional[DecodeOpts] = None, stream=None) -> torch.Tensor:
+    """One decode step of one layer: returns out [B][Hq][D] (bf16)."""
+    desc = cache_desc(k_cache)
+    _need_cuda("q", q, torch.bfloat16)
+    _need_cuda("k_cache", k_cache)
+    _need_cuda("v_cache", v_cache, k_cache.dtype)
+    _need_cuda("block_tables", block_tables, torch.int32)
+    _need_cuda("context_lens", context_lens, torch.int32)
+    B, Hq, D = (int(x) for x in q.shape)
+    if D != desc.head_dim or block_tables.dim() != 2 or block_tables.shape[0] != B:
+        raise PkvError(1, "q / block_tables shapes do not match the cache")
+    MB = int(block_tables.shape[1])
+    if out is None:
+        out = torch.empty_like(q)
+    _need_cuda("out", out, torch.bfloat16)
+    if desc.dtype == KV_FP8_E4M3:
+        _need_cuda("k_scale", k_scale, torch.float32)
+        _need_cuda("v_scale", v_scale, torch.float32)
+    if workspace is None:
+        workspace = new_decode_workspace(k_cache, B, Hq, MB, opts)
+    gp = (ctypes.c_int32 * len(kv_group_ptr))(*[int(x) for x in kv_group_ptr])
+    if scale is None:
+        scale = D ** -0.5
+    _check(load().pkv_paged_decode(
+        ctypes.byref(desc), _ptr(q), B, Hq, _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+        _ptr(v_scale), _ptr(block_tables), MB, _ptr(context_lens), gp, len(kv_group_ptr),
+        int(layer), float(scale), _ptr(out), _ptr(workspace), int(workspace.numel()),
+        ctypes.byref(opts) if opts is not None else None, _stream_handle(stream)))
+    return out
+
+
+def read_device_error(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device error word."""
+    flags = ctypes.c_uint32(0)
+    st = load().pkv_read_device_error(ctypes.byref(flags), _stream_handle(stream))
+    if st not in (PKV_OK, 5):
+        _check(st)
+    return int(flags.value)
+
+
+def build(force: bool = False) -> str:
+    from . import _build
+    return _build.build(force=force)

@@ -1,0 +1,21 @@
+// Kernel table for one (head_dim, KV dtype) family of the decode kernel.
+#pragma once
+
+#include "paged_decode.cuh"
+
+namespace pkv {
+
+template <int D, int BS, bool FP8>
+const void* decode_kernel_for(int math, int gt) {
+  if (math == PKV_MATH_MMA) return reinterpret_cast<const void*>(&paged_decode_kernel<D, BS, FP8, PKV_MATH_MMA, 0>);
+  if (math != PKV_MATH_FFMA) return nullptr;
+  switch (gt) {
+    case 1: return reinterpret_cast<const void*>(&paged_decode_kernel<D, BS, FP8, PKV_MATH_FFMA, 1>);
+    case 2: return reinterpret_cast<const void*>(&paged_decode_kernel<D, BS, FP8, PKV_MATH_FFMA, 2>);
+    case 4: return reinterpret_cast<const void*>(&paged_decode_kernel<D, BS, FP8, PKV_MATH_FFMA, 4>);
+    case 8: return reinterpret_cast<const void*>(&paged_decode_kernel<D, BS, FP8, PKV_MATH_FFMA, 8>);
+    default: return nullptr;
+  }
+}
+
+}  // namespace pkv

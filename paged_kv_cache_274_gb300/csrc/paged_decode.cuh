@@ -1,0 +1,711 @@
+// Paged single-token decode attention, sm_103a.
+//
+// Sources ("KV Cache Engineering: PagedAttention, Continuous Batching,
+// Attention Variants, and the Bandwidth Wall"): "What the KV Cache Stores
+// and Why" (the new query attends over every cached K,V), "PagedAttention"
+// (the kernel reaches physical blocks through the per-sequence block table;
+// only the last block is partly filled), "Attention Variants" (GQA: a group
+// of query heads shares one K/V head), "FP8 KV cache" (dequantise on read),
+// "Two Costs: Capacity and Bandwidth" (every step streams the whole cache,
+// so the kernel is bound by HBM bandwidth).
+//
+// Structure
+//   * Work unit = (sequence b, KV head, partition p): a run of up to `ppu`
+//     consecutive logical blocks.  Units are handed out one at a time from a
+//     global counter to warps of a persistent grid (each warp is an
+//     independent streamer: no cross-warp synchronisation).
+//   * Each warp owns a ring of `stages` shared-memory stages.  Lane 0 reads
+//     the physical block id from the block table and issues two tensor-map
+//     bulk copies (TMA) per K and V page into a stage, with 128-byte
+//     swizzling; completion is tracked by one mbarrier per stage.  The warp
+//     consumes stages in logical order and refills each one as soon as it
+//     is done with it, so `stages - 1` pages are in flight per warp.
+//   * All G query heads of the unit's KV group are computed from the one
+//     K/V page read (GQA reuse).  Online softmax in the log2 domain with
+//     fp32 state; the reduction order depends only on logical positions.
+//   * A unit that covers its whole sequence writes the bf16 output; other
+//     units write (max, sum, unnormalised output) partials that the merge
+//     kernel combines (flash-decoding split-K).
+//   * Two math back-ends share the pipeline: MMA (mma.sync m16n8k16 with the
+//     group's heads on M, tokens on N for q.K^T, and head_dim on N, tokens
+//     on K for P.V) and FFMA (fp32 CUDA-core dot products).
+#pragma once
+
+#include "pkv_device.cuh"
+
+namespace pkv {
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: a copy that has not landed by then never will
+
+struct DecodeParams {
+  const __nv_bfloat16* q;
+  __nv_bfloat16* out;
+  const int32_t* block_tables;
+  const float* k_scale;
+  const float* v_scale;
+  int32_t* work_counter;
+  const int32_t* unit_start;
+  const int32_t* ctx_eff;
+  float* part_ml;
+  float* part_o;
+  unsigned* err;
+  int B, Hq, Hkv, G, MB, NB, pmax, ppu, stages;
+  int row_base;
+  float scale_log2;
+};
+
+template <int D, int BS, bool FP8>
+struct PageGeom {
+  static constexpr int kElem = FP8 ? 1 : 2;
+  static constexpr int kRowBytes = D * kElem;          // bytes of one token row
+  static constexpr int kRegions = kRowBytes / 128;      // 128-byte wide tensor-map boxes
+  static constexpr int kBoxInner = 128 / kElem;         // elements per box row
+  static constexpr int kRegionBytes = BS * 128;
+  static constexpr int kTensorBytes = kRegions * kRegionBytes;  // one K (or V) page
+  static constexpr int kStageBytes = 2 * kTensorBytes;
+  static_assert(kRowBytes % 128 == 0, "rows must be whole 128-byte boxes");
+};
+
+// Shared memory layout per CTA: [warps][stages] stage buffers (1024-aligned),
+// then [warps][8] mbarriers, then [warps][BS * 16] floats of P scratch.
+template <int D, int BS, bool FP8>
+__host__ __device__ constexpr size_t decode_smem_layout_bytes(int warps, int stages) {
+  return 1024 /* alignment slack */ +
+         static_cast<size_t>(warps) * stages * PageGeom<D, BS, FP8>::kStageBytes +
+         static_cast<size_t>(warps) * 8 * sizeof(uint64_t) +
+         static_cast<size_t>(warps) * BS * 16 * sizeof(float);
+}
+
+// ---------------------------------------------------------------------------
+// MMA back-end state and page step
+// ---------------------------------------------------------------------------
+template <int D, int BS, bool FP8>
+struct MmaState {
+  uint32_t qa[D / 16][4];  // A fragments of q (rows = heads of the group)
+  float o[D / 8][4];       // C fragments of the output (rows = heads, cols = d)
+  float m[2];              // running max of rows g and g+8 (log2 domain)
+  float l[2];              // this lane's share of the running sums
+};
+
+template <int D, int BS, bool FP8>
+__device__ __forceinline__ void mma_load_q(MmaState<D, BS, FP8>& st, const __nv_bfloat16* qg,
+                                           int G, int lane) {
+  const int g = lane >> 2, tig = lane & 3;
+#pragma unroll
+  for (int s = 0; s < D / 16; ++s) {
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int row = g + 8 * half;
+      uint32_t lo = 0, hi = 0;
+      if (row < G) {
+        const __nv_bfloat16* qr = qg + static_cast<size_t>(row) * D;
+        if (!FP8) {
+          // k = 2tig, 2tig+1 -> d = 16s + 2tig (+1); k + 8 -> d + 8
+          lo = *reinterpret_cast<const uint32_t*>(qr + 16 * s + 2 * tig);
+          hi = *reinterpret_cast<const uint32_t*>(qr + 16 * s + 8 + 2 * tig);
+        } else {
+          // E4M3 pages are read 4 bytes per lane per chunk: k = 2tig, 2tig+1
+          // -> d = 16s + 4tig (+1); k + 8 -> d = 16s + 4tig + 2 (+1)
+          const uint32_t w0 = *reinterpret_cast<const uint32_t*>(qr + 16 * s + 4 * tig);
+          const uint32_t w1 = *reinterpret_cast<const uint32_t*>(qr + 16 * s + 4 * tig + 2);
+          lo = pack_f16x2(bf16lo_to_f32(w0), bf16hi_to_f32(w0));
+          hi = pack_f16x2(bf16lo_to_f32(w1), bf16hi_to_f32(w1));
+        }
+      }
+      st.qa[s][half] = lo;       // a0a1 (row g) / a2a3 (row g+8)
+      st.qa[s][2 + half] = hi;   // a4a5 (row g) / a6a7 (row g+8)
+    }
+  }
+#pragma unroll
+  for (int n = 0; n < D / 8; ++n) st.o[n][0] = st.o[n][1] = st.o[n][2] = st.o[n][3] = 0.f;
+  st.m[0] = st.m[1] = -INFINITY;
+  st.l[0] = st.l[1] = 0.f;
+}
+
+// One page (BS tokens) of the online softmax with tensor-core tiles.
+// `valid` = tokens of the page that belong to the sequence (0..BS).
+template <int D, int BS, bool FP8>
+__device__ __forceinline__ void mma_page(MmaState<D, BS, FP8>& st, uint8_t* stage, int valid,
+                                         float sl, float vscale, int lane) {
+  using Geo = PageGeom<D, BS, FP8>;
+  const int g = lane >> 2, tig = lane & 3;
+  const uint32_t kbase = smem_addr(stage);
+  const uint32_t vbase = kbase + Geo::kTensorBytes;
+
+  // ---- S = q . K^T  (rows = heads, cols = tokens) ----
+  float s[BS / 8][4];
+#pragma unroll
+  for (int nt = 0; nt < BS / 8; ++nt) {
+    s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+    const int row = nt * 8 + (lane & 7);
+    if (!FP8) {
+#pragma unroll
+      for (int kk = 0; kk < D / 32; ++kk) {
+        const int region = kk >> 1;
+        const int chunk = (kk & 1) * 4 + (lane >> 3);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kbase + region * Geo::kRegionBytes + swz128(row, chunk), b0, b1, b2, b3);
+        mma_bf16(s[nt], st.qa[2 * kk], b0, b1);
+        mma_bf16(s[nt], st.qa[2 * kk + 1], b2, b3);
+      }
+    } else {
+#pragma unroll
+      for (int c4 = 0; c4 < D / 64; ++c4) {
+        uint32_t r[4];
+        ldsm_x4(kbase + swz128(row, c4 * 4 + (lane >> 3)), r[0], r[1], r[2], r[3]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t b0 = e4m3x2_to_f16x2(r[i] & 0xffffu);
+          const uint32_t b1 = e4m3x2_to_f16x2(r[i] >> 16);
+          mma_f16(s[nt], st.qa[c4 * 4 + i], b0, b1);
+        }
+      }
+    }
+  }
+
+  // ---- online softmax (log2 domain) ----
+  float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+  for (int nt = 0; nt < BS / 8; ++nt) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int tok = nt * 8 + 2 * tig + (e & 1);
+      float v = s[nt][e] * sl;
+      if (tok >= valid) v = -INFINITY;
+      s[nt][e] = v;
+      mx[e >> 1] = fmaxf(mx[e >> 1], v);
+    }
+  }
+  float alpha[2], muse[2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    mx[r] = fmaxf(mx[r], __shfl_xor_sync(kFull, mx[r], 1));
+    mx[r] = fmaxf(mx[r], __shfl_xor_sync(kFull, mx[r], 2));
+    const float mnew = fmaxf(st.m[r], mx[r]);
+    muse[r] = (mnew == -INFINITY) ? 0.f : mnew;
+    alpha[r] = exp2f(st.m[r] - muse[r]);
+    st.m[r] = mnew;
+  }
+  float psum[2] = {0.f, 0.f};
+#pragma unroll
+  for (int nt = 0; nt < BS / 8; ++nt) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float p = exp2f(s[nt][e] - muse[e >> 1]);
+      s[nt][e] = p;
+      psum[e >> 1] += p;
+    }
+  }
+  st.l[0] = st.l[0] * alpha[0] + psum[0];
+  st.l[1] = st.l[1] * alpha[1] + psum[1];
+
+  // P as A fragments: k-step ks covers tokens 16ks .. 16ks+15
+  uint32_t pa[BS / 16][4];
+#pragma unroll
+  for (int ks = 0; ks < BS / 16; ++ks) {
+    if (!FP8) {
+      pa[ks][0] = pack_bf16x2(s[2 * ks][0], s[2 * ks][1]);
+      pa[ks][1] = pack_bf16x2(s[2 * ks][2], s[2 * ks][3]);
+      pa[ks][2] = pack_bf16x2(s[2 * ks + 1][0], s[2 * ks + 1][1]);
+      pa[ks][3] = pack_bf16x2(s[2 * ks + 1][2], s[2 * ks + 1][3]);
+    } else {
+      pa[ks][0] = pack_f16x2(s[2 * ks][0], s[2 * ks][1]);
+      pa[ks][1] = pack_f16x2(s[2 * ks][2], s[2 * ks][3]);
+      pa[ks][2] = pack_f16x2(s[2 * ks + 1][0], s[2 * ks + 1][1]);
+      pa[ks][3] = pack_f16x2(s[2 * ks + 1][2], s[2 * ks + 1][3]);
+    }
+  }
+
+  // Rows of V past the sequence end may hold anything (even NaN); P is 0
+  // there but 0 * NaN is NaN, so clear them before the product.
+  if (valid < BS) {
+    uint8_t* vp = stage + Geo::kTensorBytes;
+    for (int idx = lane; idx < Geo::kTensorBytes / 16; idx += 32) {
+      const int row = (idx % (Geo::kRegionBytes / 16)) / 8;
+      if (row >= valid) reinterpret_cast<uint4*>(vp)[idx] = make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+  }
+
+  // ---- O = alpha * O + P . V ----
+  if (!FP8) {
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n) {
+      st.o[n][0] *= alpha[0];
+      st.o[n][1] *= alpha[0];
+      st.o[n][2] *= alpha[1];
+      st.o[n][3] *= alpha[1];
+    }
+#pragma unroll
+    for (int ks = 0; ks < BS / 16; ++ks) {
+      const int mi = lane >> 3;
+      const int row = ks * 16 + (mi & 1) * 8 + (lane & 7);
+#pragma unroll
+      for (int np = 0; np < D / 16; ++np) {
+        const int region = (np * 16) / 64;
+        const int chunk = ((np * 16) % 64) / 8 + (mi >> 1);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(vbase + region * Geo::kRegionBytes + swz128(row, chunk), b0, b1, b2, b3);
+        mma_bf16(st.o[2 * np], pa[ks], b0, b1);
+        mma_bf16(st.o[2 * np + 1], pa[ks], b2, b3);
+      }
+    }
+  } else {
+    // E4M3 V: the token pairs each lane needs come from two rows, so read 4
+    // bytes per row, interleave the rows byte by byte and convert pairs.
+    // Output column n of n-tile (4*blk + j) is d = 32*blk + 4*n + j.
+    const uint8_t* vrow = stage + Geo::kTensorBytes;
+#pragma unroll
+    for (int blk = 0; blk < D / 32; ++blk) {
+      float t[4][4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) t[j][0] = t[j][1] = t[j][2] = t[j][3] = 0.f;
+      const int off = 32 * blk + 4 * g;
+      const int chunk = off >> 4, within = off & 15;
+#pragma unroll
+      for (int ks = 0; ks < BS / 16; ++ks) {
+        const int r0 = ks * 16 + 2 * tig;
+        const uint32_t x0 = *reinterpret_cast<const uint32_t*>(vrow + swz128(r0, chunk) + within);
+        const uint32_t x1 = *reinterpret_cast<const uint32_t*>(vrow + swz128(r0 + 1, chunk) + within);
+        const uint32_t x2 = *reinterpret_cast<const uint32_t*>(vrow + swz128(r0 + 8, chunk) + within);
+        const uint32_t x3 = *reinterpret_cast<const uint32_t*>(vrow + swz128(r0 + 9, chunk) + within);
+        const uint32_t lo01 = __byte_perm(x0, x1, 0x5140), hi01 = __byte_perm(x0, x1, 0x7362);
+        const uint32_t lo23 = __byte_perm(x2, x3, 0x5140), hi23 = __byte_perm(x2, x3, 0x7362);
+        mma_f16(t[0], pa[ks], e4m3x2_to_f16x2(lo01), e4m3x2_to_f16x2(lo23));
+        mma_f16(t[1], pa[ks], e4m3x2_to_f16x2(lo01 >> 16), e4m3x2_to_f16x2(lo23 >> 16));
+        mma_f16(t[2], pa[ks], e4m3x2_to_f16x2(hi01), e4m3x2_to_f16x2(hi23));
+        mma_f16(t[3], pa[ks], e4m3x2_to_f16x2(hi01 >> 16), e4m3x2_to_f16x2(hi23 >> 16));
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float* o = st.o[4 * blk + j];
+        o[0] = fmaf(vscale, t[j][0], o[0] * alpha[0]);
+        o[1] = fmaf(vscale, t[j][1], o[1] * alpha[0]);
+        o[2] = fmaf(vscale, t[j][2], o[2] * alpha[1]);
+        o[3] = fmaf(vscale, t[j][3], o[3] * alpha[1]);
+      }
+    }
+  }
+}
+
+// Column (head_dim index) of C-fragment element (n-tile n, column c in 0..7).
+template <int D, bool FP8>
+__device__ __forceinline__ int mma_out_col(int n, int c) {
+  if (!FP8) return 8 * n + c;
+  return 32 * (n >> 2) + 4 * c + (n & 3);
+}
+
+template <int D, int BS, bool FP8>
+__device__ __forceinline__ void mma_finish(MmaState<D, BS, FP8>& st, const DecodeParams& p,
+                                           int b, int kvh, int pidx, int nparts, int lane) {
+  const int g = lane >> 2, tig = lane & 3;
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    st.l[r] += __shfl_xor_sync(kFull, st.l[r], 1);
+    st.l[r] += __shfl_xor_sync(kFull, st.l[r], 2);
+  }
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int row = g + 8 * r;
+    if (row >= p.G) continue;
+    const int h = kvh * p.G + row;
+    if (nparts == 1) {
+      const float inv = st.l[r] > 0.f ? 1.f / st.l[r] : 0.f;
+      __nv_bfloat16* o = p.out + (static_cast<size_t>(b) * p.Hq + h) * D;
+#pragma unroll
+      for (int n = 0; n < D / 8; ++n) {
+        const float v0 = st.o[n][2 * r] * inv, v1 = st.o[n][2 * r + 1] * inv;
+        if (!FP8) {
+          *reinterpret_cast<__nv_bfloat162*>(o + 8 * n + 2 * tig) = __floats2bfloat162_rn(v0, v1);
+        } else {
+          o[mma_out_col<D, FP8>(n, 2 * tig)] = __float2bfloat16_rn(v0);
+          o[mma_out_col<D, FP8>(n, 2 * tig + 1)] = __float2bfloat16_rn(v1);
+        }
+      }
+    } else {
+      const size_t slot = (static_cast<size_t>(b) * p.Hq + h) * p.pmax + pidx;
+      float* o = p.part_o + slot * D;
+#pragma unroll
+      for (int n = 0; n < D / 8; ++n) {
+        if (!FP8) {
+          *reinterpret_cast<float2*>(o + 8 * n + 2 * tig) = make_float2(st.o[n][2 * r], st.o[n][2 * r + 1]);
+        } else {
+          o[mma_out_col<D, FP8>(n, 2 * tig)] = st.o[n][2 * r];
+          o[mma_out_col<D, FP8>(n, 2 * tig + 1)] = st.o[n][2 * r + 1];
+        }
+      }
+      if (tig == 0) *reinterpret_cast<float2*>(p.part_ml + 2 * slot) = make_float2(st.m[r], st.l[r]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// FFMA back-end (fp32 CUDA cores); GT = heads per KV group (compile time)
+// ---------------------------------------------------------------------------
+// QK lane layout: lane = 8 * tl + dl; token rows 4i + tl, head_dim slice
+// [dl * D/8, (dl+1) * D/8).  PV lane layout: lane owns D/32 consecutive d.
+template <int D, int BS, bool FP8, int GT>
+struct FfmaState {
+  float q[GT][D / 8];
+  float o[GT][D / 32];
+  float m[GT];
+  float l[GT];
+};
+
+template <int D, int BS, bool FP8, int GT>
+__device__ __forceinline__ void ffma_load_q(FfmaState<D, BS, FP8, GT>& st,
+                                            const __nv_bfloat16* qg, int lane) {
+  const int dl = lane & 7;
+#pragma unroll
+  for (int h = 0; h < GT; ++h) {
+    const uint4* src = reinterpret_cast<const uint4*>(qg + static_cast<size_t>(h) * D + dl * (D / 8));
+#pragma unroll
+    for (int c = 0; c < D / 64; ++c) {
+      const uint4 w = src[c];
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        st.q[h][8 * c + 2 * i] = bf16lo_to_f32(ws[i]);
+        st.q[h][8 * c + 2 * i + 1] = bf16hi_to_f32(ws[i]);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < D / 32; ++j) st.o[h][j] = 0.f;
+    st.m[h] = -INFINITY;
+    st.l[h] = 0.f;
+  }
+}
+
+// D/8 consecutive K values of token row `row`, starting at d = dl * D/8.
+template <int D, int BS, bool FP8>
+__device__ __forceinline__ void ffma_load_k(const uint8_t* kp, int row, int dl, float (&kf)[D / 8]) {
+  using Geo = PageGeom<D, BS, FP8>;
+  if constexpr (!FP8) {
+#pragma unroll
+    for (int c = 0; c < D / 64; ++c) {
+      const int d0 = dl * (D / 8) + 8 * c;
+      const int region = d0 / 64, chunk = (d0 % 64) / 8;
+      const uint4 w = *reinterpret_cast<const uint4*>(kp + region * Geo::kRegionBytes + swz128(row, chunk));
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        kf[8 * c + 2 * i] = bf16lo_to_f32(ws[i]);
+        kf[8 * c + 2 * i + 1] = bf16hi_to_f32(ws[i]);
+      }
+    }
+  } else {
+    static_assert(D == 128, "E4M3 pages need head_dim 128");
+    // D/8 = 16 bytes = one chunk
+    const uint4 w = *reinterpret_cast<const uint4*>(kp + swz128(row, dl));
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t h01 = e4m3x2_to_f16x2(ws[i] & 0xffffu);
+      const uint32_t h23 = e4m3x2_to_f16x2(ws[i] >> 16);
+      const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+      const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+      kf[4 * i] = f01.x;
+      kf[4 * i + 1] = f01.y;
+      kf[4 * i + 2] = f23.x;
+      kf[4 * i + 3] = f23.y;
+    }
+  }
+}
+
+// D/32 consecutive V values of token row `row`, starting at d = lane * D/32.
+template <int D, int BS, bool FP8>
+__device__ __forceinline__ void ffma_load_v(const uint8_t* vp, int row, int lane, float (&vf)[D / 32]) {
+  using Geo = PageGeom<D, BS, FP8>;
+  const int d0 = lane * (D / 32);
+  if constexpr (!FP8) {
+    const int region = d0 / 64, chunk = (d0 % 64) / 8, within = (d0 % 8) * 2;
+    const uint8_t* src = vp + region * Geo::kRegionBytes + swz128(row, chunk) + within;
+    if constexpr (D / 32 == 4) {
+      const uint2 w = *reinterpret_cast<const uint2*>(src);
+      vf[0] = bf16lo_to_f32(w.x);
+      vf[1] = bf16hi_to_f32(w.x);
+      vf[2] = bf16lo_to_f32(w.y);
+      vf[3] = bf16hi_to_f32(w.y);
+    } else {
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(src);
+      vf[0] = bf16lo_to_f32(w);
+      vf[1] = bf16hi_to_f32(w);
+    }
+  } else {
+    static_assert(D / 32 == 4, "E4M3 pages need head_dim 128");
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(vp + swz128(row, d0 >> 4) + (d0 & 15));
+    const uint32_t h01 = e4m3x2_to_f16x2(w & 0xffffu);
+    const uint32_t h23 = e4m3x2_to_f16x2(w >> 16);
+    const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+    const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+    vf[0] = f01.x;
+    vf[1] = f01.y;
+    vf[2] = f23.x;
+    vf[3] = f23.y;
+  }
+}
+
+template <int D, int BS, bool FP8, int GT>
+__device__ __forceinline__ void ffma_page(FfmaState<D, BS, FP8, GT>& st, uint8_t* stage, int valid,
+                                          float sl, float vscale, float* pbuf, int lane) {
+  using Geo = PageGeom<D, BS, FP8>;
+  const int tl = lane >> 3, dl = lane & 7;
+  const uint8_t* kp = stage;
+  const uint8_t* vp = stage + Geo::kTensorBytes;
+  float s[BS / 4][GT];
+#pragma unroll
+  for (int i = 0; i < BS / 4; ++i) {
+    const int row = 4 * i + tl;
+    float kf[D / 8];
+    ffma_load_k<D, BS, FP8>(kp, row, dl, kf);
+#pragma unroll
+    for (int h = 0; h < GT; ++h) {
+      float acc = 0.f;
+#pragma unroll
+      for (int j = 0; j < D / 8; ++j) acc = fmaf(st.q[h][j], kf[j], acc);
+      acc += __shfl_xor_sync(kFull, acc, 1);
+      acc += __shfl_xor_sync(kFull, acc, 2);
+      acc += __shfl_xor_sync(kFull, acc, 4);
+      s[i][h] = (row < valid) ? acc * sl : -INFINITY;
+    }
+  }
+  float alpha[GT];
+#pragma unroll
+  for (int h = 0; h < GT; ++h) {
+    float mx = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < BS / 4; ++i) mx = fmaxf(mx, s[i][h]);
+    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
+    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
+    const float mnew = fmaxf(st.m[h], mx);
+    const float muse = (mnew == -INFINITY) ? 0.f : mnew;
+    alpha[h] = exp2f(st.m[h] - muse);
+    st.m[h] = mnew;
+    float ps = 0.f;
+#pragma unroll
+    for (int i = 0; i < BS / 4; ++i) {
+      const float pv = exp2f(s[i][h] - muse);
+      s[i][h] = pv;
+      ps += pv;
+    }
+    st.l[h] = st.l[h] * alpha[h] + ps;
+  }
+  if (dl == 0) {
+#pragma unroll
+    for (int i = 0; i < BS / 4; ++i)
+#pragma unroll
+      for (int h = 0; h < GT; ++h) pbuf[(4 * i + tl) * GT + h] = s[i][h] * vscale;
+  }
+  __syncwarp();
+#pragma unroll
+  for (int h = 0; h < GT; ++h)
+#pragma unroll
+    for (int j = 0; j < D / 32; ++j) st.o[h][j] *= alpha[h];
+#pragma unroll 4
+  for (int t = 0; t < valid; ++t) {
+    float vf[D / 32];
+    ffma_load_v<D, BS, FP8>(vp, t, lane, vf);
+    float pv[GT];
+#pragma unroll
+    for (int h = 0; h < GT; ++h) pv[h] = pbuf[t * GT + h];
+#pragma unroll
+    for (int h = 0; h < GT; ++h)
+#pragma unroll
+      for (int j = 0; j < D / 32; ++j) st.o[h][j] = fmaf(pv[h], vf[j], st.o[h][j]);
+  }
+}
+
+template <int D, int BS, bool FP8, int GT>
+__device__ __forceinline__ void ffma_finish(FfmaState<D, BS, FP8, GT>& st, const DecodeParams& p,
+                                            int b, int kvh, int pidx, int nparts, int lane) {
+#pragma unroll
+  for (int h = 0; h < GT; ++h) {
+    float lt = st.l[h];
+    lt += __shfl_xor_sync(kFull, lt, 8);
+    lt += __shfl_xor_sync(kFull, lt, 16);
+    const int hq = kvh * GT + h;
+    if (nparts == 1) {
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
+      __nv_bfloat16* o = p.out + (static_cast<size_t>(b) * p.Hq + hq) * D + lane * (D / 32);
+#pragma unroll
+      for (int j = 0; j < D / 32; j += 2)
+        *reinterpret_cast<__nv_bfloat162*>(o + j) = __floats2bfloat162_rn(st.o[h][j] * inv, st.o[h][j + 1] * inv);
+    } else {
+      const size_t slot = (static_cast<size_t>(b) * p.Hq + hq) * p.pmax + pidx;
+      float* o = p.part_o + slot * D + lane * (D / 32);
+#pragma unroll
+      for (int j = 0; j < D / 32; j += 2) *reinterpret_cast<float2*>(o + j) = make_float2(st.o[h][j], st.o[h][j + 1]);
+      if (lane == 0) *reinterpret_cast<float2*>(p.part_ml + 2 * slot) = make_float2(st.m[h], lt);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// the kernel
+// ---------------------------------------------------------------------------
+template <int D, int BS, bool FP8, int MATH, int GT>
+__global__ void __launch_bounds__(256, 1)
+    paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
+                        const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
+  using Geo = PageGeom<D, BS, FP8>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
+  const int R = p.stages;
+  uint8_t* ring = smem + static_cast<size_t>(warp) * R * Geo::kStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(nwarps) * R * Geo::kStageBytes) + warp * 8;
+  float* pbuf = reinterpret_cast<float*>(smem + static_cast<size_t>(nwarps) * R * Geo::kStageBytes +
+                                         nwarps * 8 * sizeof(uint64_t)) + warp * BS * 16;
+
+  if (lane == 0) {
+    for (int s = 0; s < R; ++s) mbar_init(&bars[s], 1);
+    fence_mbar_init();
+    if (warp == 0) {
+      prefetch_tensormap(&kmap);
+      prefetch_tensormap(&vmap);
+    }
+  }
+  __syncwarp();
+  const uint64_t policy = l2_policy_evict_first();
+
+  const int total_units = p.unit_start[p.B] * p.Hkv;
+  uint32_t it = 0;  // pages this warp has consumed (stage = it % R, phase = (it / R) & 1)
+  const int ppu_tokens = p.ppu * BS;
+
+  for (;;) {
+    int u = 0;
+    if (lane == 0) u = atomicAdd(p.work_counter, 1);
+    u = __shfl_sync(kFull, u, 0);
+    if (u >= total_units) break;
+    const int part = u / p.Hkv;
+    const int kvh = u - part * p.Hkv;
+    // sequence owning global partition `part`: largest b with unit_start[b] <= part
+    int lo = 0, hi = p.B;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(p.unit_start + mid) <= part) lo = mid; else hi = mid;
+    }
+    const int b = lo;
+    const int pidx = part - __ldg(p.unit_start + b);
+    const int nparts = __ldg(p.unit_start + b + 1) - __ldg(p.unit_start + b);
+    const int ctx = __ldg(p.ctx_eff + b);
+    const int t0 = pidx * ppu_tokens;
+    const int t1 = min(ctx, t0 + ppu_tokens);
+    const int npages = (t1 - t0 + BS - 1) / BS;
+    const int* trow = p.block_tables + static_cast<size_t>(b) * p.MB + t0 / BS;
+
+    // physical ids of this unit's pages: lane i holds pages i and i + 32
+    int e0 = 0, e1 = 0;
+    bool bad0 = false, bad1 = false;
+    if (lane < npages) {
+      e0 = __ldg(trow + lane);
+      if (static_cast<unsigned>(e0) >= static_cast<unsigned>(p.NB)) { bad0 = true; e0 = 0; }
+    }
+    if (lane + 32 < npages) {
+      e1 = __ldg(trow + lane + 32);
+      if (static_cast<unsigned>(e1) >= static_cast<unsigned>(p.NB)) { bad1 = true; e1 = 0; }
+    }
+    const uint32_t badm0 = __ballot_sync(kFull, bad0), badm1 = __ballot_sync(kFull, bad1);
+    if (lane == 0 && (badm0 | badm1)) atomicOr(p.err, PKV_DEVERR_BLOCK_ID);
+    float ks0 = 1.f, ks1 = 1.f, vs0 = 1.f, vs1 = 1.f;
+    if (FP8) {
+      if (lane < npages) {
+        ks0 = __ldg(p.k_scale + static_cast<size_t>(e0) * p.Hkv + kvh);
+        vs0 = __ldg(p.v_scale + static_cast<size_t>(e0) * p.Hkv + kvh);
+      }
+      if (lane + 32 < npages) {
+        ks1 = __ldg(p.k_scale + static_cast<size_t>(e1) * p.Hkv + kvh);
+        vs1 = __ldg(p.v_scale + static_cast<size_t>(e1) * p.Hkv + kvh);
+      }
+    }
+
+    auto issue = [&](int j, uint32_t slot_it) {
+      const int phys = (j < 32) ? __shfl_sync(kFull, e0, j & 31) : __shfl_sync(kFull, e1, j & 31);
+      if (lane == 0) {
+        const int s = static_cast<int>(slot_it % static_cast<uint32_t>(R));
+        uint8_t* st = ring + static_cast<size_t>(s) * Geo::kStageBytes;
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(&bars[s], Geo::kStageBytes);
+        const int row = p.row_base + (phys * p.Hkv + kvh) * BS;
+#pragma unroll
+        for (int r = 0; r < Geo::kRegions; ++r)
+          tma_load_2d(st + r * Geo::kRegionBytes, &kmap, &bars[s], r * Geo::kBoxInner, row, policy);
+#pragma unroll
+        for (int r = 0; r < Geo::kRegions; ++r)
+          tma_load_2d(st + Geo::kTensorBytes + r * Geo::kRegionBytes, &vmap, &bars[s],
+                      r * Geo::kBoxInner, row, policy);
+      }
+    };
+
+    const int pre = min(R, npages);
+    for (int j = 0; j < pre; ++j) issue(j, it + j);
+    int issued = pre;  // pages of this unit handed to the copy engine
+    int consumed = 0;
+
+    const __nv_bfloat16* qg = p.q + (static_cast<size_t>(b) * p.Hq + kvh * p.G) * D;
+    bool timed_out = false;
+    if (MATH == PKV_MATH_MMA) {
+      MmaState<D, BS, FP8> st;
+      mma_load_q<D, BS, FP8>(st, qg, p.G, lane);
+      for (int j = 0; j < npages; ++j) {
+        const uint32_t s = it % static_cast<uint32_t>(R);
+        const bool landed = mbar_wait_bounded(&bars[s], (it / R) & 1u, kWaitLimitNs);
+        if (!__all_sync(kFull, landed)) { timed_out = true; break; }
+        const bool bad = (j < 32) ? ((badm0 >> (j & 31)) & 1u) : ((badm1 >> (j & 31)) & 1u);
+        const int valid = bad ? 0 : min(BS, t1 - (t0 + j * BS));
+        float ksc = 1.f, vsc = 1.f;
+        if (FP8) {
+          ksc = (j < 32) ? __shfl_sync(kFull, ks0, j & 31) : __shfl_sync(kFull, ks1, j & 31);
+          vsc = (j < 32) ? __shfl_sync(kFull, vs0, j & 31) : __shfl_sync(kFull, vs1, j & 31);
+        }
+        mma_page<D, BS, FP8>(st, ring + static_cast<size_t>(s) * Geo::kStageBytes, valid,
+                             p.scale_log2 * ksc, vsc, lane);
+        fence_proxy_async_smem();  // this lane's reads of the stage precede the refill
+        __syncwarp();
+        if (j + R < npages) { issue(j + R, it + R); ++issued; }
+        ++it;
+        ++consumed;
+      }
+      if (!timed_out) mma_finish<D, BS, FP8>(st, p, b, kvh, pidx, nparts, lane);
+    } else {
+      FfmaState<D, BS, FP8, (GT > 0 ? GT : 1)> st;
+      ffma_load_q<D, BS, FP8, (GT > 0 ? GT : 1)>(st, qg, lane);
+      for (int j = 0; j < npages; ++j) {
+        const uint32_t s = it % static_cast<uint32_t>(R);
+        const bool landed = mbar_wait_bounded(&bars[s], (it / R) & 1u, kWaitLimitNs);
+        if (!__all_sync(kFull, landed)) { timed_out = true; break; }
+        const bool bad = (j < 32) ? ((badm0 >> (j & 31)) & 1u) : ((badm1 >> (j & 31)) & 1u);
+        const int valid = bad ? 0 : min(BS, t1 - (t0 + j * BS));
+        float ksc = 1.f, vsc = 1.f;
+        if (FP8) {
+          ksc = (j < 32) ? __shfl_sync(kFull, ks0, j & 31) : __shfl_sync(kFull, ks1, j & 31);
+          vsc = (j < 32) ? __shfl_sync(kFull, vs0, j & 31) : __shfl_sync(kFull, vs1, j & 31);
+        }
+        ffma_page<D, BS, FP8, (GT > 0 ? GT : 1)>(st, ring + static_cast<size_t>(s) * Geo::kStageBytes,
+                                                 valid, p.scale_log2 * ksc, vsc, pbuf, lane);
+        fence_proxy_async_smem();  // this lane's reads of the stage precede the refill
+        __syncwarp();
+        if (j + R < npages) { issue(j + R, it + R); ++issued; }
+        ++it;
+        ++consumed;
+      }
+      if (!timed_out) ffma_finish<D, BS, FP8, (GT > 0 ? GT : 1)>(st, p, b, kvh, pidx, nparts, lane);
+    }
+    if (timed_out) {
+      // Record the failure, give copies still in flight a bounded chance to
+      // land (the stage memory stays owned by this CTA meanwhile), and stop.
+      if (lane == 0) atomicOr(p.err, PKV_DEVERR_TIMEOUT);
+      for (int k = 1; k < issued - consumed; ++k) {
+        const uint32_t q = it + static_cast<uint32_t>(k);
+        mbar_wait_bounded(&bars[q % static_cast<uint32_t>(R)], (q / R) & 1u, kWaitLimitNs / 16);
+      }
+      return;
+    }
+  }
+}
+
+}  // namespace pkv

@@ -1,0 +1,402 @@
+// C ABI of the library (see include/pkv.h): host-side validation, tensor-map
+// encoding, launch configuration and the sticky device error word.
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include <cudaTypedefs.h>
+
+#include "pkv_internal.h"
+
+namespace {
+
+// Sticky device error word (PKV_DEVERR_* bits), one per device.
+__device__ unsigned int g_pkv_device_error;
+
+thread_local std::string t_last_error;
+
+void set_error(const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+}
+
+pkv_status fail(pkv_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return st;
+}
+
+pkv_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(PKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  std::atomic<int> ready{0};
+  unsigned* err_word = nullptr;
+  int num_sms = 0;
+};
+DeviceInfo g_devices[kMaxDevices];
+std::mutex g_dev_mutex;
+
+// Per-device facts, resolved once with that device current.
+pkv_status device_info(DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(PKV_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  DeviceInfo& d = g_devices[dev];
+  if (!d.ready.load(std::memory_order_acquire)) {
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    if (!d.ready.load(std::memory_order_relaxed)) {
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_pkv_device_error);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(device error word)");
+      int sms = 0;
+      e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
+      d.err_word = static_cast<unsigned*>(p);
+      d.num_sms = sms;
+      d.ready.store(1, std::memory_order_release);
+    }
+  }
+  *out = &d;
+  return PKV_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+pkv_status tensor_map_encoder(PFN_cuTensorMapEncodeTiled_v12000* fn) {
+  std::call_once(g_encode_once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  if (g_encode == nullptr) return fail(PKV_ERR_CUDA, "driver has no cuTensorMapEncodeTiled");
+  *fn = g_encode;
+  return PKV_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool env_flag(const char* name) {
+  const char* v = std::getenv(name);
+  return v != nullptr && v[0] != '\0' && std::strcmp(v, "0") != 0;
+}
+
+int env_int(const char* name, int dflt) {
+  const char* v = std::getenv(name);
+  if (v == nullptr || v[0] == '\0') return dflt;
+  return std::atoi(v);
+}
+
+pkv_status check_cache_desc(const pkv_cache_desc* c) {
+  if (c == nullptr) return fail(PKV_ERR_INVALID_ARG, "cache descriptor is NULL");
+  if (c->num_slots < 1 || c->num_blocks < 1 || c->num_kv_heads < 1)
+    return fail(PKV_ERR_INVALID_ARG, "cache: slots, blocks and KV heads must be >= 1");
+  if (c->dtype != PKV_KV_BF16 && c->dtype != PKV_KV_FP8_E4M3)
+    return fail(PKV_ERR_INVALID_ARG, "cache: unknown dtype %d", c->dtype);
+  if (c->block_size != 16 && c->block_size != 32)
+    return fail(PKV_ERR_UNSUPPORTED, "cache: block_size %d (supported: 16, 32)", c->block_size);
+  if (c->dtype == PKV_KV_BF16 && c->head_dim != 64 && c->head_dim != 128)
+    return fail(PKV_ERR_UNSUPPORTED, "cache: head_dim %d (bf16 supports 64, 128)", c->head_dim);
+  if (c->dtype == PKV_KV_FP8_E4M3 && c->head_dim != 128)
+    return fail(PKV_ERR_UNSUPPORTED, "cache: head_dim %d (E4M3 supports 128)", c->head_dim);
+  const long long rows = static_cast<long long>(c->num_slots) * c->num_blocks * c->num_kv_heads *
+                         c->block_size;
+  if (rows >= (1LL << 31)) return fail(PKV_ERR_UNSUPPORTED, "cache has %lld rows (limit 2^31)", rows);
+  return PKV_OK;
+}
+
+pkv_status encode_cache_map(CUtensorMap* map, const void* base, const pkv_cache_desc* c) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+  pkv_status st = tensor_map_encoder(&enc);
+  if (st != PKV_OK) return st;
+  const bool fp8 = c->dtype == PKV_KV_FP8_E4M3;
+  const int elem = fp8 ? 1 : 2;
+  const cuuint64_t rows = static_cast<cuuint64_t>(c->num_slots) * c->num_blocks * c->num_kv_heads *
+                          c->block_size;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(c->head_dim), rows};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(c->head_dim) * elem};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / elem), static_cast<cuuint32_t>(c->block_size)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+  return PKV_OK;
+}
+
+// Host copies of device tables for PKV_VALIDATE.
+template <typename T>
+pkv_status fetch(std::vector<T>& dst, const T* src, size_t n, cudaStream_t stream) {
+  dst.resize(n);
+  if (n == 0) return PKV_OK;
+  cudaError_t e = cudaMemcpyAsync(dst.data(), src, n * sizeof(T), cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, "PKV_VALIDATE copy");
+  return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t pkv_abi_version(void) { return PKV_ABI_VERSION; }
+
+const char* pkv_status_string(pkv_status s) {
+  switch (s) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_INVALID_ARG: return "invalid argument";
+    case PKV_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case PKV_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case PKV_ERR_CUDA: return "CUDA error";
+    case PKV_ERR_DEVICE_INDEX: return "device reported an out-of-range index";
+    case PKV_ERR_WORKSPACE: return "workspace missing or too small";
+  }
+  return "unknown status";
+}
+
+const char* pkv_last_error_message(void) { return t_last_error.c_str(); }
+
+pkv_status pkv_kv_append(const pkv_cache_desc* cache, int32_t slot, const void* k, const void* v,
+                         const int64_t* slot_mapping, int32_t num_tokens, void* k_cache,
+                         void* v_cache, const float* k_scale, const float* v_scale, void* stream) {
+  pkv_status st = check_cache_desc(cache);
+  if (st != PKV_OK) return st;
+  if (slot < 0 || slot >= cache->num_slots)
+    return fail(PKV_ERR_INVALID_ARG, "slot %d outside [0, %d)", slot, cache->num_slots);
+  if (num_tokens < 0) return fail(PKV_ERR_INVALID_ARG, "num_tokens %d < 0", num_tokens);
+  if (num_tokens == 0) return PKV_OK;
+  const bool fp8 = cache->dtype == PKV_KV_FP8_E4M3;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache)
+    return fail(PKV_ERR_INVALID_ARG, "NULL tensor pointer");
+  if (fp8 && (!k_scale || !v_scale)) return fail(PKV_ERR_INVALID_ARG, "E4M3 cache needs k_scale and v_scale");
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache))
+    return fail(PKV_ERR_ALIGNMENT, "k, v and caches must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(slot_mapping) & 7u) != 0)
+    return fail(PKV_ERR_ALIGNMENT, "slot_mapping must be 8-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != PKV_OK) return st;
+  const long long nslots = static_cast<long long>(cache->num_blocks) * cache->block_size;
+  if (env_flag("PKV_VALIDATE")) {
+    std::vector<int64_t> sm;
+    if ((st = fetch(sm, slot_mapping, static_cast<size_t>(num_tokens), s)) != PKV_OK) return st;
+    std::vector<int64_t> seen;
+    for (int i = 0; i < num_tokens; ++i) {
+      if (sm[i] < -1 || sm[i] >= nslots)
+        return fail(PKV_ERR_INVALID_ARG, "slot_mapping[%d] = %lld outside [-1, %lld)", i,
+                    static_cast<long long>(sm[i]), nslots);
+      if (sm[i] >= 0) seen.push_back(sm[i]);
+    }
+    std::sort(seen.begin(), seen.end());
+    if (std::adjacent_find(seen.begin(), seen.end()) != seen.end())
+      return fail(PKV_ERR_INVALID_ARG, "slot_mapping has duplicate slots");
+  }
+  const size_t page_elems = static_cast<size_t>(cache->num_kv_heads) * cache->block_size * cache->head_dim;
+  const size_t slot_elems = page_elems * cache->num_blocks;
+  const size_t elem = fp8 ? 1 : 2;
+  uint8_t* kb = static_cast<uint8_t*>(k_cache) + static_cast<size_t>(slot) * slot_elems * elem;
+  uint8_t* vb = static_cast<uint8_t*>(v_cache) + static_cast<size_t>(slot) * slot_elems * elem;
+  const size_t scale_off = static_cast<size_t>(slot) * cache->num_blocks * cache->num_kv_heads;
+  cudaError_t e = pkv::launch_kv_append(fp8, k, v, slot_mapping, num_tokens, cache->num_kv_heads,
+                                        cache->head_dim, cache->block_size, nslots, kb, vb,
+                                        fp8 ? k_scale + scale_off : nullptr,
+                                        fp8 ? v_scale + scale_off : nullptr, dev->err_word, s);
+  if (e != cudaSuccess) return cuda_fail(e, "kv_append launch");
+  return PKV_OK;
+}
+
+// Resolve options into a full launch configuration (no device work).
+static pkv_status resolve_decode(const pkv_cache_desc* c, int32_t batch, int32_t Hq, int32_t MB,
+                                 const pkv_decode_opts* opts, int num_sms, pkv::DecodeLaunch* L) {
+  pkv_status st = check_cache_desc(c);
+  if (st != PKV_OK) return st;
+  if (batch < 0) return fail(PKV_ERR_INVALID_ARG, "batch %d < 0", batch);
+  if (MB < 1) return fail(PKV_ERR_INVALID_ARG, "max_blocks_per_seq %d < 1", MB);
+  if (Hq < 1 || Hq % c->num_kv_heads != 0)
+    return fail(PKV_ERR_INVALID_ARG, "num_q_heads %d is not a multiple of num_kv_heads %d", Hq,
+                c->num_kv_heads);
+  if (static_cast<long long>(MB) * c->block_size >= (1LL << 31))
+    return fail(PKV_ERR_UNSUPPORTED, "max_blocks_per_seq too large");
+  const int G = Hq / c->num_kv_heads;
+  pkv_decode_opts o{};
+  if (opts) o = *opts;
+  int math = o.math != 0 ? o.math : env_int("PKV_DECODE_MATH", PKV_MATH_AUTO);
+  if (math == PKV_MATH_AUTO) math = PKV_MATH_MMA;
+  if (math == PKV_MATH_MMA && G > 16)
+    return fail(PKV_ERR_UNSUPPORTED, "G = %d query heads per KV head (mma supports <= 16)", G);
+  if (math == PKV_MATH_FFMA && G != 1 && G != 2 && G != 4 && G != 8)
+    return fail(PKV_ERR_UNSUPPORTED, "G = %d query heads per KV head (ffma supports 1, 2, 4, 8)", G);
+  if (math != PKV_MATH_MMA && math != PKV_MATH_FFMA) return fail(PKV_ERR_INVALID_ARG, "math %d", math);
+  const bool fp8 = c->dtype == PKV_KV_FP8_E4M3;
+  const size_t stage_bytes = static_cast<size_t>(2) * c->block_size * c->head_dim * (fp8 ? 1 : 2);
+  int warps = o.warps_per_cta != 0 ? o.warps_per_cta : env_int("PKV_DECODE_WARPS", 4);
+  int stages = o.stages != 0 ? o.stages : env_int("PKV_DECODE_STAGES", 0);
+  if (stages == 0) stages = static_cast<int>(std::clamp<size_t>((48u << 10) / stage_bytes, 3, 8));
+  if (warps < 1 || warps > 8) return fail(PKV_ERR_INVALID_ARG, "warps_per_cta %d outside 1..8", warps);
+  if (stages < 2 || stages > 8) return fail(PKV_ERR_INVALID_ARG, "stages %d outside 2..8", stages);
+  const size_t smem = pkv::decode_smem_bytes(fp8, c->head_dim, c->block_size, warps, stages);
+  if (smem > 227u * 1024u)
+    return fail(PKV_ERR_INVALID_ARG, "warps x stages need %zu bytes of shared memory", smem);
+  int ppu = o.partition_blocks != 0 ? o.partition_blocks : env_int("PKV_DECODE_PARTITION_BLOCKS", 0);
+  if (ppu == 0) {
+    // enough units for every warp of a full persistent grid to take several
+    const long long pages = static_cast<long long>(std::max(batch, 1)) * c->num_kv_heads * MB;
+    const int ctas_per_sm = std::max(1, static_cast<int>((228u * 1024u) / (smem + 1024)));
+    const long long warps_total = static_cast<long long>(num_sms) * ctas_per_sm * warps;
+    const long long want = pages / std::max(1LL, 4 * warps_total);
+    ppu = static_cast<int>(std::clamp<long long>(want, 8, 64));
+  }
+  if (ppu < 1 || ppu > 64) return fail(PKV_ERR_INVALID_ARG, "partition_blocks %d outside 1..64", ppu);
+  ppu = std::min(ppu, MB);
+  *L = pkv::DecodeLaunch{};
+  L->B = batch;
+  L->Hq = Hq;
+  L->Hkv = c->num_kv_heads;
+  L->G = G;
+  L->MB = MB;
+  L->NB = c->num_blocks;
+  L->bs = c->block_size;
+  L->D = c->head_dim;
+  L->kv_fp8 = fp8;
+  L->ppu = ppu;
+  L->pmax = (MB + ppu - 1) / ppu;
+  L->math = math;
+  L->warps = warps;
+  L->stages = stages;
+  L->num_sms = num_sms;
+  return PKV_OK;
+}
+
+size_t pkv_decode_workspace_bytes(const pkv_cache_desc* cache, int32_t batch, int32_t num_q_heads,
+                                  int32_t max_blocks_per_seq, const pkv_decode_opts* opts) {
+  pkv::DecodeLaunch L;
+  // The partition size (and so the workspace) must not depend on the device
+  // the call later runs on: size with the largest SM count this build targets.
+  if (resolve_decode(cache, batch, num_q_heads, max_blocks_per_seq, opts, 152, &L) != PKV_OK) return 0;
+  return pkv::workspace_layout(L.B, L.Hq, L.D, L.pmax).total;
+}
+
+pkv_status pkv_paged_decode(const pkv_cache_desc* cache, const void* q, int32_t batch,
+                            int32_t num_q_heads, const void* k_cache, const void* v_cache,
+                            const float* k_scale, const float* v_scale,
+                            const int32_t* block_tables, int32_t max_blocks_per_seq,
+                            const int32_t* context_lens, const int32_t* kv_group_ptr,
+                            int32_t num_layers, int32_t layer, float scale, void* out,
+                            void* workspace, size_t workspace_bytes, const pkv_decode_opts* opts,
+                            void* stream) {
+  pkv::DecodeLaunch L;
+  pkv_status st = resolve_decode(cache, batch, num_q_heads, max_blocks_per_seq, opts, 152, &L);
+  if (st != PKV_OK) return st;
+  if (kv_group_ptr == nullptr || num_layers < 1 || layer < 0 || layer >= num_layers)
+    return fail(PKV_ERR_INVALID_ARG, "layer %d / num_layers %d / kv_group_ptr", layer, num_layers);
+  const int32_t slot = kv_group_ptr[layer];
+  if (slot < 0 || slot >= cache->num_slots)
+    return fail(PKV_ERR_INVALID_ARG, "kv_group_ptr[%d] = %d outside [0, %d)", layer, slot, cache->num_slots);
+  if (!std::isfinite(scale)) return fail(PKV_ERR_INVALID_ARG, "scale is not finite");
+  if (batch == 0) return PKV_OK;
+  const bool fp8 = cache->dtype == PKV_KV_FP8_E4M3;
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+    return fail(PKV_ERR_INVALID_ARG, "NULL tensor pointer");
+  if (fp8 && (!k_scale || !v_scale)) return fail(PKV_ERR_INVALID_ARG, "E4M3 cache needs k_scale and v_scale");
+  if (!aligned16(q) || !aligned16(out) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(workspace))
+    return fail(PKV_ERR_ALIGNMENT, "q, out, caches and workspace must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u))
+    return fail(PKV_ERR_ALIGNMENT, "block_tables and context_lens must be 4-byte aligned");
+  const size_t qbytes = static_cast<size_t>(batch) * num_q_heads * cache->head_dim * 2;
+  const uintptr_t qa = reinterpret_cast<uintptr_t>(q), oa = reinterpret_cast<uintptr_t>(out);
+  if (qa < oa + qbytes && oa < qa + qbytes) return fail(PKV_ERR_INVALID_ARG, "out overlaps q");
+  const pkv::WorkspaceLayout wl = pkv::workspace_layout(L.B, L.Hq, L.D, L.pmax);
+  if (workspace == nullptr || workspace_bytes < wl.total)
+    return fail(PKV_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu", wl.total, workspace_bytes);
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != PKV_OK) return st;
+  L.num_sms = dev->num_sms;
+
+  if (env_flag("PKV_VALIDATE")) {
+    std::vector<int32_t> ctx, bt;
+    if ((st = fetch(ctx, context_lens, static_cast<size_t>(batch), s)) != PKV_OK) return st;
+    if ((st = fetch(bt, block_tables, static_cast<size_t>(batch) * max_blocks_per_seq, s)) != PKV_OK) return st;
+    for (int b = 0; b < batch; ++b) {
+      if (ctx[b] < 0 || static_cast<long long>(ctx[b]) > static_cast<long long>(max_blocks_per_seq) * cache->block_size)
+        return fail(PKV_ERR_INVALID_ARG, "context_lens[%d] = %d out of range", b, ctx[b]);
+      for (int j = 0; j < (ctx[b] + cache->block_size - 1) / cache->block_size; ++j) {
+        const int32_t blk = bt[static_cast<size_t>(b) * max_blocks_per_seq + j];
+        if (blk < 0 || blk >= cache->num_blocks)
+          return fail(PKV_ERR_INVALID_ARG, "block_tables[%d][%d] = %d outside [0, %d)", b, j, blk,
+                      cache->num_blocks);
+      }
+    }
+  }
+
+  if ((st = encode_cache_map(&L.kmap, k_cache, cache)) != PKV_OK) return st;
+  if ((st = encode_cache_map(&L.vmap, v_cache, cache)) != PKV_OK) return st;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  L.q = q;
+  L.out = out;
+  L.block_tables = block_tables;
+  L.context_lens = context_lens;
+  const size_t scale_off = static_cast<size_t>(slot) * cache->num_blocks * cache->num_kv_heads;
+  L.k_scale = fp8 ? k_scale + scale_off : nullptr;
+  L.v_scale = fp8 ? v_scale + scale_off : nullptr;
+  L.work_counter = reinterpret_cast<int32_t*>(ws + wl.counter);
+  L.unit_start = reinterpret_cast<int32_t*>(ws + wl.unit_start);
+  L.ctx_eff = reinterpret_cast<int32_t*>(ws + wl.ctx_eff);
+  L.part_ml = reinterpret_cast<float*>(ws + wl.part_ml);
+  L.part_o = reinterpret_cast<float*>(ws + wl.part_o);
+  L.err = dev->err_word;
+  L.row_base = static_cast<int>(static_cast<long long>(slot) * cache->num_blocks * cache->num_kv_heads *
+                                cache->block_size);
+  L.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  L.stream = s;
+  int launched = 0;
+  cudaError_t e = pkv::launch_decode(L, &launched);
+  if (e != cudaSuccess) return cuda_fail(e, "paged_decode launch");
+  return PKV_OK;
+}
+
+pkv_status pkv_read_device_error(uint32_t* flags, void* stream) {
+  if (flags == nullptr) return fail(PKV_ERR_INVALID_ARG, "flags is NULL");
+  DeviceInfo* dev = nullptr;
+  pkv_status st = device_info(&dev);
+  if (st != PKV_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned host = 0;
+  cudaError_t e = cudaMemcpyAsync(&host, dev->err_word, sizeof host, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(dev->err_word, 0, sizeof host, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+  *flags = host;
+  if (host != 0) {
+    set_error("device error word 0x%x", host);
+    return PKV_ERR_DEVICE_INDEX;
+  }
+  return PKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,65 @@
+// Host-side plumbing shared by the library's translation units (not part of
+// the public ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "pkv.h"
+
+namespace pkv {
+
+// Everything one decode launch needs, resolved and validated by the API layer.
+struct DecodeLaunch {
+  const void* q;
+  void* out;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  const float* k_scale;  // already offset to the selected slot (E4M3 only)
+  const float* v_scale;
+  int32_t* work_counter;  // workspace: dynamic work queue head
+  int32_t* unit_start;    // workspace: [B+1] prefix of partitions per sequence
+  int32_t* ctx_eff;       // workspace: [B] validated context lengths
+  float* part_ml;         // workspace: [B][Hq][pmax][2] (running max, sum)
+  float* part_o;          // workspace: [B][Hq][pmax][D]
+  unsigned* err;          // device error word
+  int B, Hq, Hkv, G, MB, NB, bs, D;
+  int kv_fp8;
+  int pmax;  // max partitions of a sequence (ceil(MB / ppu))
+  int ppu;   // pages (blocks) per partition
+  int row_base;  // first tensor-map row of the selected slot
+  float scale_log2;
+  int math;    // PKV_MATH_FFMA or PKV_MATH_MMA (resolved)
+  int warps;   // per CTA
+  int stages;  // per warp
+  CUtensorMap kmap, vmap;
+  cudaStream_t stream;
+  int num_sms;
+};
+
+// Workspace layout for one decode call.
+struct WorkspaceLayout {
+  size_t counter, unit_start, ctx_eff, part_ml, part_o, total;
+};
+WorkspaceLayout workspace_layout(int B, int Hq, int D, int pmax);
+
+// Shared memory per CTA of the decode kernel.
+size_t decode_smem_bytes(int kv_fp8, int D, int bs, int warps, int stages);
+
+// Launch planner + decode (+ merge when pmax > 1).  Returns cudaSuccess or
+// the first launch error.
+cudaError_t launch_decode(const DecodeLaunch& L, int* launched_kernels);
+
+// Decode kernel occupancy (CTAs per SM) for a configuration.
+int decode_ctas_per_sm(const DecodeLaunch& L, size_t smem);
+
+// KV append.
+cudaError_t launch_kv_append(int kv_fp8, const void* k, const void* v,
+                             const int64_t* slot_mapping, int N, int Hkv, int D, int bs,
+                             int64_t nslots, void* k_base, void* v_base, const float* ks_base,
+                             const float* vs_base, unsigned* err, cudaStream_t stream);
+
+}  // namespace pkv

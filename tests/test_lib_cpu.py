@@ -1,0 +1,122 @@
+"""CPU-side checks of the C ABI: the library builds, loads, exports every
+function the header declares, and the host-only entry points validate their
+arguments (no GPU needed: these paths return before touching CUDA)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_cache_274_gb300 as pkv
+from paged_kv_cache_274_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pkv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return pkv.load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(pkv_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_api():
+    names = declared_functions()
+    for n in ("pkv_kv_append", "pkv_paged_decode", "pkv_decode_workspace_bytes",
+              "pkv_read_device_error", "pkv_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), f"{n} declared in pkv.h but not exported"
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.pkv_abi_version() == 1
+    assert lib.pkv_status_string(0) == b"ok"
+    assert b"aligned" in lib.pkv_status_string(3)
+
+
+def _desc(**kw):
+    d = dict(num_slots=1, num_blocks=100, block_size=16, num_kv_heads=8, head_dim=128, dtype=0)
+    d.update(kw)
+    return pkv.CacheDesc(**d)
+
+
+def test_workspace_bytes_host_only(lib):
+    d = _desc()
+    n1 = lib.pkv_decode_workspace_bytes(ctypes.byref(d), 64, 32, 256, None)
+    assert n1 > 0
+    # one partition per sequence: no split-K partials
+    opts = pkv.decode_opts(partition_blocks=64)
+    small = lib.pkv_decode_workspace_bytes(ctypes.byref(d), 4, 32, 64, ctypes.byref(opts))
+    assert 0 < small < 4096
+    # more partitions need more partial storage
+    o8 = pkv.decode_opts(partition_blocks=8)
+    o32 = pkv.decode_opts(partition_blocks=32)
+    assert (lib.pkv_decode_workspace_bytes(ctypes.byref(d), 64, 32, 256, ctypes.byref(o8)) >
+            lib.pkv_decode_workspace_bytes(ctypes.byref(d), 64, 32, 256, ctypes.byref(o32)))
+
+
+@pytest.mark.parametrize("bad", [
+    dict(block_size=8), dict(head_dim=96), dict(dtype=1, head_dim=64), dict(num_kv_heads=0),
+    dict(dtype=7), dict(num_blocks=0)])
+def test_bad_cache_descriptors_rejected(lib, bad):
+    d = _desc(**bad)
+    assert lib.pkv_decode_workspace_bytes(ctypes.byref(d), 4, 32, 16, None) == 0
+    st = lib.pkv_kv_append(ctypes.byref(d), 0, None, None, None, 4, None, None, None, None, None)
+    assert st in (1, 2)
+
+
+def test_bad_head_grouping_rejected(lib):
+    d = _desc()
+    assert lib.pkv_decode_workspace_bytes(ctypes.byref(d), 4, 12, 16, None) == 0   # 12 % 8 != 0
+    ffma = pkv.decode_opts(math=pkv.MATH_FFMA)
+    d1 = _desc(num_kv_heads=1)
+    assert lib.pkv_decode_workspace_bytes(ctypes.byref(d1), 4, 16, 16, ctypes.byref(ffma)) == 0
+    assert lib.pkv_decode_workspace_bytes(ctypes.byref(d1), 4, 16, 16, None) > 0   # mma: G = 16 ok
+    assert lib.pkv_decode_workspace_bytes(ctypes.byref(d1), 4, 32, 16, None) == 0  # G = 32
+
+
+def test_append_argument_checks(lib):
+    d = _desc()
+    # slot outside the cache slots
+    assert lib.pkv_kv_append(ctypes.byref(d), 1, None, None, None, 1, None, None, None, None, None) == 1
+    # zero tokens is a no-op
+    assert lib.pkv_kv_append(ctypes.byref(d), 0, None, None, None, 0, None, None, None, None, None) == 0
+    # null pointers
+    assert lib.pkv_kv_append(ctypes.byref(d), 0, None, None, None, 3, None, None, None, None, None) == 1
+    # misaligned pointers (never dereferenced: the check comes first)
+    p = ctypes.c_void_p(0x1008)
+    assert lib.pkv_kv_append(ctypes.byref(d), 0, p, p, ctypes.c_void_p(0x2000), 3, p, p, None,
+                             None, None) == 3
+    # E4M3 cache without scales
+    d8 = _desc(dtype=1)
+    a = ctypes.c_void_p(0x1000)
+    assert lib.pkv_kv_append(ctypes.byref(d8), 0, a, a, a, 3, a, a, None, None, None) == 1
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    import importlib
+    monkeypatch.setattr(pkv, "_lib", None)
+    monkeypatch.setattr(pkv, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(pkv.PkvError):
+        pkv.load()
+    importlib.reload(pkv)
+
+
+def test_product_path_does_not_import_oracle():
+    pkg = os.path.join(ROOT, "paged_kv_cache_274_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "pkv_oracle" not in text, f
