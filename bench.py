@@ -1,0 +1,527 @@
+"""Benchmark: paged decode over a paged KV cache on GB300.
+
+One step = one pass of the whole hot path over one batch:
+  llama8b_layer (default): kv_append of each sequence's newest token, then
+      paged_decode of 64 sequences x 32 query heads at context 4096
+      (8 KV heads, head_dim 128, block 16, bf16) -- 1 GiB of KV read;
+  long_b4_32k / long_b1_128k: paged_decode, 64 q / 8 KV heads, block 32;
+  mixed_prefix: 256 sequences, log-uniform lengths, shared prefix blocks;
+  fp8_shared: four layer calls that read one E4M3 cache (shared-with pointer).
+
+Metric: KV bytes read per step / step time (GB/s, 1e9), with % of the
+measured HBM peak and decode steps/s beside it.  Inputs (>= 512 MiB of KV)
+are larger than L2, so L2 is not flushed between steps.
+
+`--impl reference` times the CPU float64 oracle on a bounded sample of the
+same workload instead (the only place besides the cpu_baseline leg where
+this script runs the oracle).
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import io
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode KV-read GB/s and % of GB300 HBM peak; decode steps/s"
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0
+WORKLOADS = ("llama8b_layer", "long_b4_32k", "long_b1_128k", "mixed_prefix", "fp8_shared", "tiny")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", choices=WORKLOADS, default="llama8b_layer")
+    ap.add_argument("--math", choices=("auto", "mma", "ffma"), default="auto")
+    ap.add_argument("--partition-blocks", type=int, default=0)
+    ap.add_argument("--warps", type=int, default=0)
+    ap.add_argument("--stages", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target CPU time of the oracle sample")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# environment: ranks, peaks, clocks, profile summaries
+# ---------------------------------------------------------------------------
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.text = ""
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.text, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        rows = []
+        for r in csv.reader(io.StringIO(getattr(self, "text", "") or "")):
+            if len(r) < 9:
+                continue
+            try:
+                rows.append([x.strip() for x in r])
+            except Exception:
+                pass
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def profile_traffic(workload):
+    """Per-launch DRAM bytes of the decode kernel from the committed ncu
+    summary, if it was taken on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", f"paged_decode_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
+    h = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    if not m or not h:
+        return None
+    from paged_kv_cache_274_gb300 import _build
+    if h.group(1) != _build.source_digest():
+        return None
+    return int(m.group(1))
+
+
+# ---------------------------------------------------------------------------
+# workloads (inputs resident in HBM before timing starts)
+# ---------------------------------------------------------------------------
+def structure(name):
+    """Block tables, lengths, queries, append slots (no cache contents)."""
+    from workloads import gen
+    if name == "llama8b_layer":
+        return gen.llama8b_layer_case(fill=False)
+    if name.startswith("long_"):
+        return gen.long_context_case(name[len("long_"):], fill=False)
+    if name == "mixed_prefix":
+        return gen.mixed_prefix_case(fill=False)
+    if name == "fp8_shared":
+        return gen.fp8_shared_case(fill=False)
+    return gen.tiny_case()
+
+
+def kv_bytes_of(c, seqs=None, layers=None):
+    """Algorithmic KV bytes one decode call reads: every real token's K and V
+    row of its KV heads (no tail padding), plus per-page E4M3 scales."""
+    elem = 1 if c.kv_dtype == "fp8" else 2
+    idx = range(c.B) if seqs is None else seqs
+    ctx = np.asarray(c.context_lens, dtype=np.int64)[list(idx)]
+    b = int(ctx.sum()) * 2 * c.Hkv * c.D * elem
+    if c.kv_dtype == "fp8":
+        b += int(((ctx + c.bs - 1) // c.bs).sum()) * 2 * c.Hkv * 4
+    n_layers = len(layers) if layers is not None else c.L
+    return b * n_layers
+
+
+class DeviceWorkload:
+    def __init__(self, name, rank, opts_kw):
+        import paged_kv_cache_274_gb300 as pkv
+        self.pkv = pkv
+        self.name = name
+        self.c = c = structure(name)
+        dev = torch.device("cuda", torch.cuda.current_device())
+        self.dev = dev
+        shape = (c.S, c.NB, c.Hkv, c.bs, c.D)
+        g = torch.Generator(device=dev)
+        g.manual_seed(7919 * (rank + 1) + len(name))
+        if c.kv_dtype == "fp8":
+            self.k = torch.empty(shape, dtype=torch.uint8, device=dev)
+            self.v = torch.empty(shape, dtype=torch.uint8, device=dev)
+            self.ks = torch.empty(shape[:3], dtype=torch.float32, device=dev)
+            self.vs = torch.empty(shape[:3], dtype=torch.float32, device=dev)
+            self._fill_fp8(g)
+        else:
+            self.k = torch.randn(shape, generator=g, device=dev, dtype=torch.bfloat16)
+            self.v = torch.randn(shape, generator=g, device=dev, dtype=torch.bfloat16)
+            self.ks = self.vs = None
+        self.q = torch.from_numpy(c.q).view(torch.bfloat16).to(dev)          # [L][B][Hq][D]
+        self.bt = torch.from_numpy(c.block_tables).to(dev)
+        self.cl = torch.from_numpy(c.context_lens).to(dev)
+        self.out = torch.empty((c.L, c.B, c.Hq, c.D), dtype=torch.bfloat16, device=dev)
+        self.append = c.k_new is not None
+        if self.append:
+            self.k_new = torch.from_numpy(c.k_new).view(torch.bfloat16).to(dev)
+            self.v_new = torch.from_numpy(c.v_new).view(torch.bfloat16).to(dev)
+            self.slots = torch.from_numpy(c.slot_mapping).to(dev)
+        self.opts_kw = opts_kw
+        self.opts = pkv.decode_opts(**opts_kw)
+        self.ws = pkv.new_decode_workspace(self.k, c.B, c.Hq, c.MB, self.opts)
+        self.plan = pkv.decode_plan(self.k, c.B, c.Hq, c.MB, self.opts)
+        self.layers = list(range(c.L))
+        self.kv_bytes = kv_bytes_of(c)
+        self.launches_per_step = (1 if self.append else 0) + len(self.layers) * self.plan["kernels_per_call"]
+        torch.cuda.synchronize()
+
+    def _fill_fp8(self, g):
+        """E4M3 cache from bf16 N(0,1) data through the library's own append,
+        with per-(block, KV head) scales amax / 448 chosen by the caller."""
+        c, pkv = self.c, self.pkv
+        chunk = 2048  # blocks per append call
+        for b0 in range(0, c.NB, chunk):
+            nb = min(chunk, c.NB - b0)
+            toks = []
+            for sc in (self.ks, self.vs):
+                src = torch.randn((nb, c.Hkv, c.bs, c.D), generator=g, device=self.dev, dtype=torch.bfloat16)
+                amax = src.float().abs().amax(dim=(2, 3))
+                s = amax / 448.0
+                s[amax == 0] = 1.0
+                sc[0, b0:b0 + nb] = s
+                toks.append(src.permute(0, 2, 1, 3).reshape(nb * c.bs, c.Hkv, c.D).contiguous())
+            slots = torch.arange(b0 * c.bs, (b0 + nb) * c.bs, device=self.dev, dtype=torch.int64)
+            pkv.kv_append(toks[0], toks[1], slots, self.k, self.v, self.ks, self.vs)
+        torch.cuda.synchronize()
+
+    def step(self, events=None):
+        """One decode step; `events`: optional list of (start, end) per layer call."""
+        pkv, c = self.pkv, self.c
+        if self.append:
+            pkv.kv_append(self.k_new, self.v_new, self.slots, self.k, self.v)
+        for i, layer in enumerate(self.layers):
+            opts = self.opts
+            if events is not None:
+                opts = pkv.decode_opts(**self.opts_kw, event_start=events[i][0], event_end=events[i][1])
+            pkv.paged_decode(self.q[layer], self.k, self.v, self.bt, self.cl, c.kv_group_ptr.tolist(),
+                             layer, c.scale, out=self.out[layer], workspace=self.ws,
+                             k_scale=self.ks, v_scale=self.vs, opts=opts)
+
+
+# ---------------------------------------------------------------------------
+# timing
+# ---------------------------------------------------------------------------
+def time_device(w, steps, warmup, world):
+    """Device-resident inputs: K timed steps between CUDA events on the
+    launching stream; the decode kernel itself is bracketed by events the
+    library records around it."""
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        w.step()
+    torch.cuda.synchronize()
+    def made_event():
+        ev = torch.cuda.Event(enable_timing=True)
+        ev.record(stream)   # torch creates the CUDA event lazily, on first record
+        return ev
+    kev = [[(made_event(), made_event()) for _ in w.layers] for _ in range(steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        start.record(stream)
+        for i in range(steps):
+            w.step(events=kev[i])
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    total_ms = start.elapsed_time(end)
+    kernel_ms = [a.elapsed_time(b) for evs in kev for (a, b) in evs]
+    return total_ms, kernel_ms, clk.summary()
+
+
+def time_e2e(w, steps, warmup, world):
+    """Through the public API from pinned host buffers: each step copies its
+    inputs host->device (queries, new tokens and slots, block tables,
+    lengths), runs the step, and copies the outputs device->host."""
+    c = w.c
+    host = {"q": w.q.cpu().pin_memory(), "bt": w.bt.cpu().pin_memory(), "cl": w.cl.cpu().pin_memory()}
+    if w.append:
+        host.update(k_new=w.k_new.cpu().pin_memory(), v_new=w.v_new.cpu().pin_memory(),
+                    slots=w.slots.cpu().pin_memory())
+    out_host = torch.empty(w.out.shape, dtype=w.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def one():
+        w.q.copy_(host["q"], non_blocking=True)
+        w.bt.copy_(host["bt"], non_blocking=True)
+        w.cl.copy_(host["cl"], non_blocking=True)
+        if w.append:
+            w.k_new.copy_(host["k_new"], non_blocking=True)
+            w.v_new.copy_(host["v_new"], non_blocking=True)
+            w.slots.copy_(host["slots"], non_blocking=True)
+        w.step()
+        out_host.copy_(w.out, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    barrier(world)
+    stream = torch.cuda.current_stream()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    start.record(stream)
+    for _ in range(steps):
+        one()
+    end.record(stream)
+    torch.cuda.synchronize()
+    wall_ms = (time.perf_counter() - t0) * 1e3
+    barrier(world)
+    return max(start.elapsed_time(end), wall_ms), h2d, d2h
+
+
+def oracle_sample(name, target_s):
+    """Time the CPU oracle (as it stands) on a bounded sample of the workload:
+    the first n sequences of one decode call, all query heads, layer 0.
+    Returns (GB/s, seconds, threads, description)."""
+    import oracle
+    from workloads import normal_bf16_bits
+    c = structure(name)
+    shape = (c.S, c.NB, c.Hkv, c.bs, c.D)
+    fp8 = c.kv_dtype == "fp8"
+    dt = np.uint8 if fp8 else np.uint16
+    k = np.zeros(shape, dtype=dt)
+    v = np.zeros(shape, dtype=dt)
+    ks = vs = None
+    if fp8:
+        ks = np.ones(shape[:3], np.float32)
+        vs = np.ones(shape[:3], np.float32)
+    rng = np.random.Generator(np.random.PCG64(11))
+    order = list(range(c.B))
+    filled = set()
+
+    def fill(upto):
+        for b in order[:upto]:
+            if b in filled:
+                continue
+            n = (int(c.context_lens[b]) + c.bs - 1) // c.bs
+            blks = c.block_tables[b, :n]
+            for arr, seed in ((k, 2), (v, 3)):
+                if fp8:
+                    arr[0, blks] = rng.integers(0, 0x7E, size=(n,) + shape[2:], dtype=np.uint8)
+                else:
+                    arr[0, blks] = normal_bf16_bits(1000 * seed + b, (n,) + shape[2:])
+            filled.add(b)
+
+    def run(nseq):
+        fill(nseq)
+        pairs = np.array([(b, h) for b in order[:nseq] for h in range(c.Hq)], np.int32)
+        t0 = time.perf_counter()
+        oracle.paged_decode(c.q[0], k, v, c.block_tables, c.context_lens, c.kv_group_ptr, 0, c.scale,
+                            k_scale=ks, v_scale=vs, pairs=pairs)
+        return time.perf_counter() - t0
+
+    t1 = run(1)
+    nseq = int(min(c.B, max(1, math.floor(target_s / max(t1, 1e-6)))))
+    secs = run(nseq) if nseq > 1 else t1
+    reps = 1
+    while secs * (reps + 1) / reps < target_s and secs / reps < target_s / 2 and reps < 64:
+        secs += run(nseq)
+        reps += 1
+    nbytes = kv_bytes_of(c, seqs=order[:nseq], layers=[0]) * reps
+    desc = (f"{name}: sequences 0..{nseq - 1} of {c.B} (all {c.Hq} query heads, one layer call), "
+            f"{reps} repetition(s), {nbytes / 1e9:.3f} GB of KV")
+    return nbytes / secs / 1e9, secs, oracle.num_threads(), desc
+
+
+# ---------------------------------------------------------------------------
+# main
+# ---------------------------------------------------------------------------
+def config_of(name, c, extra=None):
+    cfg = {"workload": name, "batch": c.B, "q_heads": c.Hq, "kv_heads": c.Hkv, "head_dim": c.D,
+           "block_size": c.bs, "kv_dtype": c.kv_dtype, "layer_calls_per_step": c.L,
+           "context_lens": ("uniform %d" % int(c.context_lens[0]) if len(set(c.context_lens.tolist())) == 1
+                            else "mixed %d..%d (mean %.0f)" % (int(c.context_lens.min()),
+                                                                int(c.context_lens.max()),
+                                                                float(c.context_lens.mean()))),
+           "pool_blocks": c.NB, "l2": "inputs larger than L2 (129 MB); no flush between steps"}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    c = structure(args.workload)
+    per_step_s = min(2.0, max(0.2, 150.0 / max(1, args.steps + args.warmup)))
+    samples = []
+    for i in range(args.warmup + args.steps):
+        gbs, secs, threads, desc = oracle_sample(args.workload, per_step_s)
+        if i >= args.warmup:
+            samples.append((gbs, secs))
+    value = statistics.median(g for g, _ in samples)
+    line = {"metric": METRIC, "value": value, "unit": "GB/s", "impl": "reference", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * statistics.median(s for _, s in samples),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_of(args.workload, c),
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world):
+    import paged_kv_cache_274_gb300 as pkv
+    pkv.load()   # fails loudly if the CUDA library is missing
+    opts_kw = dict(partition_blocks=args.partition_blocks,
+                   math={"auto": pkv.MATH_AUTO, "mma": pkv.MATH_MMA, "ffma": pkv.MATH_FFMA}[args.math],
+                   warps=args.warps, stages=args.stages)
+    w = DeviceWorkload(args.workload, rank, opts_kw)
+    c = w.c
+    total_ms, kernel_ms, clocks = time_device(w, args.steps, args.warmup, world)
+    assert pkv.read_device_error() == 0, "device error word set during the benchmark"
+    ms = max_over_ranks(total_ms / args.steps, world)
+    kv_total = sum_over_ranks(float(w.kv_bytes), world)
+    value = kv_total / (ms * 1e-3) / 1e9
+    peak, peak_kind = hbm_peak()
+    per_call_bytes = kv_bytes_of(c, layers=[0])
+    k_ms = statistics.mean(kernel_ms)
+    achieved = per_call_bytes / (k_ms * 1e-3) / 1e9
+    e2e = None
+    if not args.no_e2e:
+        e_ms, h2d, d2h = time_e2e(w, max(5, args.steps // 2), max(3, args.warmup), world)
+        e_ms = max_over_ranks(e_ms / max(5, args.steps // 2), world)
+        e2e = {"value": kv_total / (e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e_ms,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        gbs, secs, threads, desc = oracle_sample(args.workload, args.cpu_seconds)
+        cpu = {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": desc,
+               "seconds": secs}
+    if rank == 0:
+        plan = w.plan
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "fp8-e4m3 kv, f16 mma, fp32 accumulate" if c.kv_dtype == "fp8"
+            else "bf16 kv, bf16 mma, fp32 accumulate",
+            "data": "synthetic (seeded N(0,1) K/V/q, seeded block permutations)",
+            "config": config_of(args.workload, c, {
+                "parallelism": "replicas" if world > 1 else "single GPU",
+                "math": {1: "ffma", 2: "mma"}[plan["math"]],
+                "partition_blocks": plan["partition_blocks"], "max_partitions": plan["max_partitions"],
+                "warps_per_cta": plan["warps_per_cta"], "stages": plan["stages"]}),
+            "kv_bytes_per_step": w.kv_bytes,
+            "decode_steps_per_s": 1e3 / ms,
+            "pct_of_hbm_peak": 100.0 * value / peak,
+            "pct_of_nominal_8tbs": 100.0 * value / 8000.0,
+            "roofline": {"bound": "hbm", "kernel": "paged_decode_kernel", "achieved": achieved,
+                         "peak": peak, "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                         if peak_kind == "measured" else "fallback 6.8 TB/s",
+                         "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": profile_traffic(args.workload),
+                         "algorithmic_bytes_per_launch": per_call_bytes,
+                         "kernel_ms_mean": k_ms, "kernel_ms_median": statistics.median(kernel_ms)},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": w.launches_per_step * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        run_reference(args, rank, int(os.environ.get("WORLD_SIZE", "1")))
+        return
+    rank, world, _ = dist_setup(args.gpus)
+    try:
+        run_ours(args, rank, world)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -97,6 +97,11 @@ typedef struct {
   int32_t math;             /* pkv_decode_math */
   int32_t warps_per_cta;    /* 1..8 (0 = auto) */
   int32_t stages;           /* pages in each warp's copy ring, 2..8 (0 = auto) */
+  /* Optional cudaEvent_t handles (NULL = none) that the library records on
+   * the stream immediately before and after the decode kernel itself (not
+   * the planner or the merge), for timing that one kernel. */
+  void* event_decode_start;
+  void* event_decode_end;
 } pkv_decode_opts;
 
 /*
@@ -125,14 +130,36 @@ pkv_status pkv_kv_append(const pkv_cache_desc* cache, int32_t slot,
 
 /*
  * Bytes of device workspace pkv_paged_decode needs for these sizes (0 on a
- * bad argument).  The workspace holds the split-K partials and a small work
- * queue header; it must be zero-filled once before its first use, and each
- * call leaves the header ready for the next call on the same stream.  Calls
- * that run at the same time need separate workspaces.
+ * bad argument).  The workspace holds the split-K partials, the per-call
+ * plan (partition prefix sums, validated context lengths) and a work-queue
+ * counter.  It needs no initialisation: each call's planner kernel writes
+ * every field before the decode reads it.  Calls that may run at the same
+ * time (different streams) need separate workspaces.
  */
 size_t pkv_decode_workspace_bytes(const pkv_cache_desc* cache, int32_t batch,
                                   int32_t num_q_heads, int32_t max_blocks_per_seq,
                                   const pkv_decode_opts* opts);
+
+/* The launch plan pkv_paged_decode would use for these sizes and options. */
+typedef struct {
+  int32_t partition_blocks;  /* blocks per split-K partition */
+  int32_t max_partitions;    /* partitions of a max_blocks_per_seq-block sequence */
+  int32_t math;              /* resolved pkv_decode_math */
+  int32_t warps_per_cta;
+  int32_t stages;
+  int32_t kernels_per_call;  /* planner + decode (+ merge when max_partitions > 1) */
+  size_t workspace_bytes;
+  size_t smem_bytes_per_cta;
+} pkv_decode_plan;
+
+/*
+ * Resolve the options of a decode call without launching anything (host
+ * only).  Same argument checks as pkv_paged_decode's shape checks; *plan is
+ * written on PKV_OK.
+ */
+pkv_status pkv_decode_describe(const pkv_cache_desc* cache, int32_t batch, int32_t num_q_heads,
+                               int32_t max_blocks_per_seq, const pkv_decode_opts* opts,
+                               pkv_decode_plan* plan);
 
 /*
  * Single-token decode attention over the paged cache, one query token per

@@ -194,7 +194,7 @@ def paged_decode(q_bits, k_cache, v_cache, block_tables, context_lens, kv_group_
     ks = _c(k_scale, np.float32) if fp8 else None
     vs = _c(v_scale, np.float32) if fp8 else None
     out = np.full((B, Hq, D), np.nan if pairs is not None else 0.0, dtype=np.float64)
-    pr = None if pairs is None else _c(pairs, np.int32).reshape(-1, 2)
+    pr = None if pairs is None else np.unique(_c(pairs, np.int32).reshape(-1, 2), axis=0)
     rc = _load(lib).pkv_oracle_paged_decode(
         _ptr(q), B, Hq, _ptr(kc), _ptr(vc), int(fp8), _ptr(ks), _ptr(vs),
         S, NB, Hkv, bs, D, _ptr(bt), int(bt.shape[1]), _ptr(cl), _ptr(gp), int(gp.shape[0]),

@@ -207,8 +207,8 @@ static double cache_value(const void* cache, int32_t fp8, const float* scales,
  *   block_tables int32 [B][MB]; context_lens int32 [B]
  *   kv_group_ptr int32 [L]: cache slot read by layer l (shared-with pointer)
  *   out          double [B][Hq][D]
- *   pairs        optional int32 [npairs][2] list of (b, h) to compute (the
- *                others are left untouched); NULL computes every pair.
+ *   pairs        optional int32 [npairs][2] list of distinct (b, h) to compute
+ *                (the others are left untouched); NULL computes every pair.
  * For each (b, h) with n = context_lens[b] tokens (n == 0 gives zeros):
  *   K_t = K[slot][table[b][t / bs]][h / G][t % bs][:], t = 0 .. n-1 (V alike)
  *   s_t = double(scale) * sum_d double(q[b][h][d]) * K_t[d]
@@ -247,6 +247,7 @@ int pkv_oracle_paged_decode(const uint16_t* q, int32_t B, int32_t Hq,
 #endif
   {
     double* s = (double*)malloc(sizeof(double) * (size_t)(maxn > 0 ? maxn : 1));
+    double* acc = (double*)malloc(sizeof(double) * (size_t)D);
 #ifdef _OPENMP
 #pragma omp for schedule(dynamic, 1)
 #endif
@@ -257,8 +258,11 @@ int pkv_oracle_paged_decode(const uint16_t* q, int32_t B, int32_t Hq,
       int32_t n = context_lens[b];
       double* o = out + ((int64_t)b * Hq + h) * D;
       const uint16_t* qv = q + ((int64_t)b * Hq + h) * D;
-      for (int32_t d = 0; d < D; ++d) o[d] = 0.0;
-      if (n == 0) continue;
+      for (int32_t d = 0; d < D; ++d) acc[d] = 0.0;
+      if (n == 0) {
+        for (int32_t d = 0; d < D; ++d) o[d] = 0.0;
+        continue;
+      }
       /* logits over the gathered logical sequence */
       double smax = -INFINITY;
       for (int32_t t = 0; t < n; ++t) {
@@ -281,9 +285,12 @@ int pkv_oracle_paged_decode(const uint16_t* q, int32_t B, int32_t Hq,
         int64_t page = ((int64_t)slot * NB + blk) * Hkv + g;
         double p = s[t] / z;
         for (int32_t d = 0; d < D; ++d)
-          o[d] += p * cache_value(v_cache, fp8, v_scale, page, bs, D, t % bs, d);
+          acc[d] += p * cache_value(v_cache, fp8, v_scale, page, bs, D, t % bs, d);
       }
+      /* the row is stored once, so a (b, h) listed twice cannot interleave */
+      for (int32_t d = 0; d < D; ++d) o[d] = acc[d];
     }
+    free(acc);
     free(s);
   }
   return ORACLE_OK;

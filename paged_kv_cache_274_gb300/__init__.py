@@ -49,7 +49,15 @@ class CacheDesc(ctypes.Structure):
 
 class DecodeOpts(ctypes.Structure):
     _fields_ = [("partition_blocks", ctypes.c_int32), ("math", ctypes.c_int32),
-                ("warps_per_cta", ctypes.c_int32), ("stages", ctypes.c_int32)]
+                ("warps_per_cta", ctypes.c_int32), ("stages", ctypes.c_int32),
+                ("event_decode_start", ctypes.c_void_p), ("event_decode_end", ctypes.c_void_p)]
+
+
+class DecodePlan(ctypes.Structure):
+    _fields_ = [("partition_blocks", ctypes.c_int32), ("max_partitions", ctypes.c_int32),
+                ("math", ctypes.c_int32), ("warps_per_cta", ctypes.c_int32),
+                ("stages", ctypes.c_int32), ("kernels_per_call", ctypes.c_int32),
+                ("workspace_bytes", ctypes.c_size_t), ("smem_bytes_per_cta", ctypes.c_size_t)]
 
 
 _lib = None
@@ -76,6 +84,8 @@ def load() -> ctypes.CDLL:
         lib.pkv_kv_append.argtypes = [pdesc, i32, P, P, P, i32, P, P, P, P, P]
         lib.pkv_decode_workspace_bytes.restype = sz
         lib.pkv_decode_workspace_bytes.argtypes = [pdesc, i32, i32, i32, popts]
+        lib.pkv_decode_describe.restype = ctypes.c_int
+        lib.pkv_decode_describe.argtypes = [pdesc, i32, i32, i32, popts, ctypes.POINTER(DecodePlan)]
         lib.pkv_paged_decode.restype = ctypes.c_int
         lib.pkv_paged_decode.argtypes = [pdesc, P, i32, i32, P, P, P, P, P, i32, P, P, i32, i32,
                                          f32, P, P, sz, popts, P]
@@ -155,8 +165,13 @@ def kv_append(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
 
 
 def decode_opts(partition_blocks: int = 0, math: int = MATH_AUTO, warps: int = 0,
-                stages: int = 0) -> DecodeOpts:
-    return DecodeOpts(int(partition_blocks), int(math), int(warps), int(stages))
+                stages: int = 0, event_start=None, event_end=None) -> DecodeOpts:
+    """Options of :func:`paged_decode`.  ``event_start`` / ``event_end``:
+    optional torch.cuda.Event objects recorded around the decode kernel."""
+    def handle(ev):
+        return None if ev is None else ctypes.c_void_p(ev.cuda_event)
+    return DecodeOpts(int(partition_blocks), int(math), int(warps), int(stages),
+                      handle(event_start), handle(event_end))
 
 
 def decode_workspace_bytes(k_cache: torch.Tensor, batch: int, num_q_heads: int,
@@ -168,6 +183,18 @@ def decode_workspace_bytes(k_cache: torch.Tensor, batch: int, num_q_heads: int,
     if n == 0:
         raise PkvError(1, "bad arguments for the decode workspace")
     return int(n)
+
+
+def decode_plan(k_cache: torch.Tensor, batch: int, num_q_heads: int, max_blocks_per_seq: int,
+                opts: Optional[DecodeOpts] = None) -> dict:
+    """The resolved launch plan of a decode call (host only, nothing launched)."""
+    desc = cache_desc(k_cache)
+    plan = DecodePlan()
+    _check(load().pkv_decode_describe(ctypes.byref(desc), int(batch), int(num_q_heads),
+                                      int(max_blocks_per_seq),
+                                      ctypes.byref(opts) if opts is not None else None,
+                                      ctypes.byref(plan)))
+    return {f: getattr(plan, f) for f, _ in DecodePlan._fields_}
 
 
 def new_decode_workspace(k_cache: torch.Tensor, batch: int, num_q_heads: int,

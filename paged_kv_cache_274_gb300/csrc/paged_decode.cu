@@ -240,8 +240,10 @@ cudaError_t launch_decode(const DecodeLaunch& L, int* launched) {
   p.scale_log2 = L.scale_log2;
   CUtensorMap kmap = L.kmap, vmap = L.vmap;
   void* args[] = {&kmap, &vmap, &p};
+  if (L.ev_start != nullptr && (e = cudaEventRecord(L.ev_start, L.stream)) != cudaSuccess) return e;
   e = cudaLaunchKernel(fn, dim3(static_cast<unsigned>(grid)), dim3(L.warps * 32), args, smem, L.stream);
   if (e != cudaSuccess) return e;
+  if (L.ev_end != nullptr && (e = cudaEventRecord(L.ev_end, L.stream)) != cudaSuccess) return e;
   *launched += 1;
 
   // 3. merge (only when some sequence can span more than one partition)

@@ -300,6 +300,24 @@ size_t pkv_decode_workspace_bytes(const pkv_cache_desc* cache, int32_t batch, in
   return pkv::workspace_layout(L.B, L.Hq, L.D, L.pmax).total;
 }
 
+pkv_status pkv_decode_describe(const pkv_cache_desc* cache, int32_t batch, int32_t num_q_heads,
+                               int32_t max_blocks_per_seq, const pkv_decode_opts* opts,
+                               pkv_decode_plan* plan) {
+  if (plan == nullptr) return fail(PKV_ERR_INVALID_ARG, "plan is NULL");
+  pkv::DecodeLaunch L;
+  pkv_status st = resolve_decode(cache, batch, num_q_heads, max_blocks_per_seq, opts, 152, &L);
+  if (st != PKV_OK) return st;
+  plan->partition_blocks = L.ppu;
+  plan->max_partitions = L.pmax;
+  plan->math = L.math;
+  plan->warps_per_cta = L.warps;
+  plan->stages = L.stages;
+  plan->kernels_per_call = L.pmax > 1 ? 3 : 2;
+  plan->workspace_bytes = pkv::workspace_layout(L.B, L.Hq, L.D, L.pmax).total;
+  plan->smem_bytes_per_cta = pkv::decode_smem_bytes(L.kv_fp8, L.D, L.bs, L.warps, L.stages);
+  return PKV_OK;
+}
+
 pkv_status pkv_paged_decode(const pkv_cache_desc* cache, const void* q, int32_t batch,
                             int32_t num_q_heads, const void* k_cache, const void* v_cache,
                             const float* k_scale, const float* v_scale,
@@ -374,6 +392,10 @@ pkv_status pkv_paged_decode(const pkv_cache_desc* cache, const void* q, int32_t 
                                 cache->block_size);
   L.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   L.stream = s;
+  if (opts != nullptr) {
+    L.ev_start = static_cast<cudaEvent_t>(opts->event_decode_start);
+    L.ev_end = static_cast<cudaEvent_t>(opts->event_decode_end);
+  }
   int launched = 0;
   cudaError_t e = pkv::launch_decode(L, &launched);
   if (e != cudaSuccess) return cuda_fail(e, "paged_decode launch");

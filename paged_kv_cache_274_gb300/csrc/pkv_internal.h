@@ -38,6 +38,7 @@ struct DecodeLaunch {
   CUtensorMap kmap, vmap;
   cudaStream_t stream;
   int num_sms;
+  cudaEvent_t ev_start, ev_end;  // optional, recorded around the decode kernel
 };
 
 // Workspace layout for one decode call.

@@ -375,3 +375,16 @@ def test_planted_mistakes(name, old, new, tmp_path):
         except (AssertionError, ValueError):
             failed.append(pin.__name__)
     assert failed, f"no pin caught the planted mistake {name}"
+
+
+def test_sampled_pairs_with_repeats_match_full_run():
+    # a (b, h) listed more than once must give the same row as a full run
+    Hq, Hkv, D, bs, lens = 8, 2, 64, 16, [300, 41, 77]
+    ks, vs = dense_bf16_seqs(110, lens, Hkv, D)
+    kc, vc, bt, ctx, _ = paged_from_dense(ks, vs, bs, seed=111)
+    q = normal_bf16_bits(112, (3, Hq, D))
+    full = oracle.paged_decode(q, kc, vc, bt, ctx, [0], 0, 0.125)
+    pairs = np.array([[0, 1]] * 16 + [[2, 7], [0, 1], [1, 0]] * 8, dtype=np.int32)
+    part = oracle.paged_decode(q, kc, vc, bt, ctx, [0], 0, 0.125, pairs=pairs)
+    for b, h in pairs:
+        assert np.array_equal(part[b, h], full[b, h])

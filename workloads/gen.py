@@ -100,8 +100,8 @@ class DecodeCase:
     kv_group_ptr: np.ndarray           # int32 [L]
     scale: float                       # exactly representable in float32
     q: np.ndarray                      # uint16 [L][B][Hq][D]
-    k_src: np.ndarray                  # uint16 [S][NB][Hkv][bs][D]
-    v_src: np.ndarray                  # uint16 [S][NB][Hkv][bs][D]
+    k_src: Optional[np.ndarray]        # uint16 [S][NB][Hkv][bs][D] (None: structure only)
+    v_src: Optional[np.ndarray]
     k_scale: Optional[np.ndarray] = None   # float32 [S][NB][Hkv] (fp8 only)
     v_scale: Optional[np.ndarray] = None
     # optional append step: new tokens written before the decode
@@ -160,8 +160,8 @@ def _queries(cfg: int, L: int, B: int, Hq: int, D: int) -> np.ndarray:
 
 def _cache(cfg: int, S: int, NB: int, Hkv: int, bs: int, D: int, fill: bool):
     shape = (S, NB, Hkv, bs, D)
-    if not fill:
-        return np.zeros(shape, np.uint16), np.zeros(shape, np.uint16)
+    if not fill:   # structure only (block tables, lengths, queries)
+        return None, None
     return normal_bf16_bits(1000 * cfg + 2, shape), normal_bf16_bits(1000 * cfg + 3, shape)
 
 
