@@ -204,6 +204,44 @@ pkv_status pkv_paged_decode(const pkv_cache_desc* cache,
                             void* workspace, size_t workspace_bytes,
                             const pkv_decode_opts* opts, void* stream);
 
+/* Size of the library's built-in decode workspace (see below). */
+#define PKV_STATIC_WORKSPACE_MAX_BYTES ((size_t)16 << 20)
+
+/*
+ * pkv_paged_decode without a caller workspace.  The web pages have no
+ * counterpart to this call; it exists for callers that cannot allocate
+ * device memory at the point where they decode: code running where
+ * cudaMalloc is off limits (an allocator-free runtime, a plugin handed
+ * only its input and output buffers, a host that owns every allocation).
+ *
+ * The scratch the decode needs (split-K partials, the per-call plan, the
+ * work-queue counter) lives instead in one static device array of
+ * PKV_STATIC_WORKSPACE_MAX_BYTES bytes that every GPU which loads the
+ * library holds until the process exits.  Arguments and results are those of
+ * pkv_paged_decode; q, caches, tables and out are still the caller's.
+ *   - A request whose workspace (pkv_decode_workspace_bytes) would exceed
+ *     the array returns PKV_ERR_WORKSPACE and launches nothing; larger
+ *     opts->partition_blocks means fewer split-K partials.
+ *   - The first call on a device looks up that device's copy of the array
+ *     (cudaGetSymbolAddress, with the device current); make that first call
+ *     before any stream capture on the device.
+ *   - The call allocates nothing (no cudaMalloc / cudaFree).  Every call on
+ *     a device shares the one array and it keeps the previous call's
+ *     contents; each call's planner kernel rewrites everything the decode
+ *     reads, so nothing needs clearing by the caller.  Calls that can run at
+ *     the same time on the GPU (e.g. on different streams) race on the array.
+ */
+pkv_status pkv_paged_decode_static_workspace(const pkv_cache_desc* cache,
+                                             const void* q, int32_t batch, int32_t num_q_heads,
+                                             const void* k_cache, const void* v_cache,
+                                             const float* k_scale, const float* v_scale,
+                                             const int32_t* block_tables,
+                                             int32_t max_blocks_per_seq,
+                                             const int32_t* context_lens,
+                                             const int32_t* kv_group_ptr, int32_t num_layers,
+                                             int32_t layer, float scale, void* out,
+                                             const pkv_decode_opts* opts, void* stream);
+
 /*
  * Synchronise `stream`, copy the current device's sticky error word into
  * *flags (PKV_DEVERR_* bits) and clear it.  Returns PKV_ERR_DEVICE_INDEX if

@@ -89,6 +89,9 @@ def load() -> ctypes.CDLL:
         lib.pkv_paged_decode.restype = ctypes.c_int
         lib.pkv_paged_decode.argtypes = [pdesc, P, i32, i32, P, P, P, P, P, i32, P, P, i32, i32,
                                          f32, P, P, sz, popts, P]
+        lib.pkv_paged_decode_static_workspace.restype = ctypes.c_int
+        lib.pkv_paged_decode_static_workspace.argtypes = [pdesc, P, i32, i32, P, P, P, P, P, i32, P,
+                                                          P, i32, i32, f32, P, popts, P]
         lib.pkv_read_device_error.restype = ctypes.c_int
         lib.pkv_read_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), P]
         lib.pkv_status_string.restype = ctypes.c_char_p
@@ -237,6 +240,39 @@ def paged_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
         ctypes.byref(desc), _ptr(q), B, Hq, _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
         _ptr(v_scale), _ptr(block_tables), MB, _ptr(context_lens), gp, len(kv_group_ptr),
         int(layer), float(scale), _ptr(out), _ptr(workspace), int(workspace.numel()),
+        ctypes.byref(opts) if opts is not None else None, _stream_handle(stream)))
+    return out
+
+
+STATIC_WORKSPACE_MAX_BYTES = 16 << 20
+
+
+def paged_decode_static_workspace(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                  block_tables: torch.Tensor, context_lens: torch.Tensor,
+                                  kv_group_ptr: Sequence[int] = (0,), layer: int = 0,
+                                  scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                                  k_scale: Optional[torch.Tensor] = None,
+                                  v_scale: Optional[torch.Tensor] = None,
+                                  opts: Optional[DecodeOpts] = None, stream=None) -> torch.Tensor:
+    """:func:`paged_decode` for callers that cannot allocate a workspace: the
+    library's built-in static device array serves as scratch (at most
+    STATIC_WORKSPACE_MAX_BYTES; calls that overlap on the GPU race on it).
+    ``out`` must be passed in by a caller that cannot allocate."""
+    desc = cache_desc(k_cache)
+    _need_cuda("q", q, torch.bfloat16)
+    _need_cuda("block_tables", block_tables, torch.int32)
+    _need_cuda("context_lens", context_lens, torch.int32)
+    B, Hq, D = (int(x) for x in q.shape)
+    if out is None:
+        out = torch.empty_like(q)
+    _need_cuda("out", out, torch.bfloat16)
+    gp = (ctypes.c_int32 * len(kv_group_ptr))(*[int(x) for x in kv_group_ptr])
+    if scale is None:
+        scale = D ** -0.5
+    _check(load().pkv_paged_decode_static_workspace(
+        ctypes.byref(desc), _ptr(q), B, Hq, _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+        _ptr(v_scale), _ptr(block_tables), int(block_tables.shape[1]), _ptr(context_lens), gp,
+        len(kv_group_ptr), int(layer), float(scale), _ptr(out),
         ctypes.byref(opts) if opts is not None else None, _stream_handle(stream)))
     return out
 

@@ -161,6 +161,10 @@ pkv_status fetch(std::vector<T>& dst, const T* src, size_t n, cudaStream_t strea
 
 }  // namespace
 
+namespace pkv {
+void set_last_error_message(const char* msg) { t_last_error = msg; }
+}  // namespace pkv
+
 extern "C" {
 
 int32_t pkv_abi_version(void) { return PKV_ABI_VERSION; }

@@ -57,6 +57,9 @@ cudaError_t launch_decode(const DecodeLaunch& L, int* launched_kernels);
 // Decode kernel occupancy (CTAs per SM) for a configuration.
 int decode_ctas_per_sm(const DecodeLaunch& L, size_t smem);
 
+// Replace the calling thread's pkv_last_error_message() text.
+void set_last_error_message(const char* msg);
+
 // KV append.
 cudaError_t launch_kv_append(int kv_fp8, const void* k, const void* v,
                              const int64_t* slot_mapping, int N, int Hkv, int D, int bs,
