@@ -99,7 +99,8 @@ typedef struct {
   int32_t stages;           /* pages in each warp's copy ring, 2..8 (0 = auto) */
   /* Optional cudaEvent_t handles (NULL = none) that the library records on
    * the stream immediately before and after the decode kernel itself (not
-   * the planner or the merge), for timing that one kernel. */
+   * the planner), for timing that one kernel.  Recording the start event
+   * between the two kernels keeps them from overlapping. */
   void* event_decode_start;
   void* event_decode_end;
 } pkv_decode_opts;
@@ -147,7 +148,7 @@ typedef struct {
   int32_t math;              /* resolved pkv_decode_math */
   int32_t warps_per_cta;
   int32_t stages;
-  int32_t kernels_per_call;  /* planner + decode (+ merge when max_partitions > 1) */
+  int32_t kernels_per_call;  /* planner + decode (+ merge above 4 partitions) */
   size_t workspace_bytes;
   size_t smem_bytes_per_cta;
 } pkv_decode_plan;
@@ -190,8 +191,11 @@ pkv_status pkv_decode_describe(const pkv_cache_desc* cache, int32_t batch, int32
  * Accumulation is fp32; out is rounded to bf16 (round to nearest even).
  * The reduction order depends only on logical token positions and the
  * partition size, never on which physical blocks hold the tokens.
- * Launches up to three kernels: a planner, the decode, and (when some
- * sequence spans more than one partition) the split-K merge.
+ * Launches a planner and the decode kernel.  Sequences split into at most 4
+ * partitions are merged by the decode warp that finishes last; with more
+ * partitions a third kernel merges the partials.  Both kernels (and pkv_kv_append's) use programmatic dependent
+ * launch: each may be scheduled while the previous kernel on the stream
+ * drains, and waits for it before reading memory (PKV_PDL=0 turns this off).
  */
 pkv_status pkv_paged_decode(const pkv_cache_desc* cache,
                             const void* q, int32_t batch, int32_t num_q_heads,

@@ -7,7 +7,12 @@ namespace pkv {
 
 template <int D, int BS, bool FP8>
 const void* decode_kernel_for(int math, int gt) {
-  if (math == PKV_MATH_MMA) return reinterpret_cast<const void*>(&paged_decode_kernel<D, BS, FP8, PKV_MATH_MMA, 0>);
+  if (math == PKV_MATH_MMA) {
+    // GT = 8: at most 8 heads per group (half tiles); 16: up to 16
+    if (gt <= 8) return reinterpret_cast<const void*>(&paged_decode_kernel<D, BS, FP8, PKV_MATH_MMA, 8>);
+    if (gt <= 16) return reinterpret_cast<const void*>(&paged_decode_kernel<D, BS, FP8, PKV_MATH_MMA, 16>);
+    return nullptr;
+  }
   if (math != PKV_MATH_FFMA) return nullptr;
   switch (gt) {
     case 1: return reinterpret_cast<const void*>(&paged_decode_kernel<D, BS, FP8, PKV_MATH_FFMA, 1>);

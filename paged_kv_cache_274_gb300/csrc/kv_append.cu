@@ -23,6 +23,8 @@ __global__ void __launch_bounds__(256)
                      int64_t nslots, uint8_t* __restrict__ kc, uint8_t* __restrict__ vc,
                      const float* __restrict__ ks, const float* __restrict__ vs,
                      unsigned* __restrict__ err) {
+  pdl_trigger();
+  pdl_wait();  // inputs may come from the previous kernel on the stream
   const int chunks_per_row = D / 8;
   const int64_t per_tensor = static_cast<int64_t>(N) * Hkv * chunks_per_row;
   const int64_t total = 2 * per_tensor;
@@ -75,15 +77,19 @@ cudaError_t launch_kv_append(int kv_fp8, const void* k, const void* v,
   const int64_t total = 2LL * N * Hkv * (D / 8);
   const int threads = 256;
   const int64_t blocks = std::min<int64_t>((total + threads - 1) / threads, 1 << 16);
-  if (kv_fp8)
-    kv_append_kernel<true><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-        static_cast<const uint4*>(k), static_cast<const uint4*>(v), slot_mapping, N, Hkv, D, bs,
-        nslots, static_cast<uint8_t*>(k_base), static_cast<uint8_t*>(v_base), ks_base, vs_base, err);
-  else
-    kv_append_kernel<false><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-        static_cast<const uint4*>(k), static_cast<const uint4*>(v), slot_mapping, N, Hkv, D, bs,
-        nslots, static_cast<uint8_t*>(k_base), static_cast<uint8_t*>(v_base), ks_base, vs_base, err);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(threads);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  auto kernel = kv_fp8 ? kv_append_kernel<true> : kv_append_kernel<false>;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<const uint4*>(k), static_cast<const uint4*>(v),
+                            slot_mapping, N, Hkv, D, bs, nslots, static_cast<uint8_t*>(k_base),
+                            static_cast<uint8_t*>(v_base), ks_base, vs_base, err);
 }
 
 }  // namespace pkv

@@ -1,13 +1,20 @@
-// Planner and split-K merge kernels, and the host-side launch sequence of a
-// paged decode (planner -> decode -> merge).
+// Planner and merge kernels and the host-side launch sequence of a paged
+// decode (planner -> decode [-> merge when sequences span many partitions]).
 //
 // Split-K ("flash-decoding"): a long sequence is cut into partitions of
 // `ppu` blocks that different warps process at the same time; each writes
-// its running max m_p (log2 domain), sum l_p and unnormalised output O_p.
-// The merge takes M = max_p m_p and returns
-//   out = sum_p 2^(m_p - M) O_p / sum_p 2^(m_p - M) l_p,
-// which is the softmax over the union of the partitions' tokens.
+// its running max m_p (log2 domain), sum l_p and unnormalised output O_p,
+// and the warp that finishes a (sequence, KV head) last combines them.
+//
+// Both kernels are launched with programmatic dependent launch, so each can
+// be scheduled while its predecessor on the stream drains; each waits for
+// that predecessor (griddepcontrol.wait) before reading any global memory.
 #include <algorithm>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <tuple>
+#include <vector>
 
 #include "paged_decode.cuh"
 #include "pkv_internal.h"
@@ -22,16 +29,24 @@ const void* decode_kernel_fp8_d128(int bs, int math, int gt);
 // ---------------------------------------------------------------------------
 // planner: one CTA validates context lengths, counts each sequence's
 // partitions, prefix-sums them into unit_start, resets the work queue and
-// writes zeros for sequences that attend to nothing.
+// the split-K arrival counters, and writes zeros for sequences that attend
+// to nothing.
 // ---------------------------------------------------------------------------
 constexpr int kPlanThreads = 1024;
 
+// Sequences of at most this many partitions are merged inside the decode
+// kernel by the warp that finishes last; longer ones by merge_kernel (the
+// in-kernel merge is serial per (sequence, KV head) and lands in the tail).
+constexpr int kFusedMergeMaxParts = 4;
+
 __global__ void __launch_bounds__(kPlanThreads)
-    plan_kernel(const int32_t* __restrict__ context_lens, int B, int max_ctx, int tokens_per_part,
-                int32_t* work_counter, int32_t* unit_start, int32_t* ctx_eff,
-                __nv_bfloat16* out, int row_elems /* Hq * D */, unsigned* err) {
+    plan_kernel(const int32_t* __restrict__ context_lens, int B, int Hkv, int max_ctx,
+                int tokens_per_part, int32_t* work_counter, int32_t* unit_start, int32_t* ctx_eff,
+                int32_t* arrive, __nv_bfloat16* out, int row_elems /* Hq * D */, unsigned* err) {
   __shared__ int warp_tot[kPlanThreads / 32];
   __shared__ int carry_s;
+  pdl_trigger();
+  pdl_wait();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) carry_s = 0;
   __syncthreads();
@@ -77,6 +92,7 @@ __global__ void __launch_bounds__(kPlanThreads)
     unit_start[B] = carry_s;
     *work_counter = 0;
   }
+  for (int i = tid; i < B * Hkv; i += kPlanThreads) arrive[i] = 0;
   if (__syncthreads_or(bad_any) && tid == 0) atomicOr(err, PKV_DEVERR_CONTEXT_LEN);
   // zeros for inactive sequences (one warp per sequence)
   for (int b = warp; b < B; b += kPlanThreads / 32) {
@@ -87,53 +103,86 @@ __global__ void __launch_bounds__(kPlanThreads)
 }
 
 // ---------------------------------------------------------------------------
-// merge: one warp per (sequence, query head) with more than one partition
+// merge kernel (many partitions): one CTA per (sequence, query head); its
+// threads split head_dim (4 values each) and the partitions, stage the
+// partition weights in shared memory and reduce across partition groups.
+//   out = sum_p 2^(m_p - M) O_p / sum_p 2^(m_p - M) l_p,  M = max_p m_p.
 // ---------------------------------------------------------------------------
+constexpr int kMergeThreads = 256;
+
 template <int D>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kMergeThreads)
     merge_kernel(const float* __restrict__ part_ml, const float* __restrict__ part_o,
-                 const int32_t* __restrict__ unit_start, int B, int Hq, int pmax,
+                 const int32_t* __restrict__ unit_start, int Hq, int pmax,
                  __nv_bfloat16* __restrict__ out) {
-  const int lane = threadIdx.x & 31;
-  const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (gw >= B * Hq) return;
-  const int b = gw / Hq;
+  constexpr int kDG = D / 4;                  // threads along head_dim
+  constexpr int kPG = kMergeThreads / kDG;    // partition groups
+  extern __shared__ float4 wsm4[];           // [pmax] weights (padded to 4), then [kPG][D] sums
+  float* wsm = reinterpret_cast<float*>(wsm4);
+  __shared__ float red[kMergeThreads / 32];
+  __shared__ float bcast;
+  pdl_trigger();
+  pdl_wait();
+  const int bh = blockIdx.x;
+  const int b = bh / Hq;
   const int P = unit_start[b + 1] - unit_start[b];
-  if (P < 2) return;
-  const size_t base = static_cast<size_t>(gw) * pmax;
-  float M = -INFINITY;
-  for (int i = lane; i < P; i += 32) M = fmaxf(M, part_ml[2 * (base + i)]);
+  if (P < 2) return;  // written by the decode kernel (or zero-filled by the planner)
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const size_t base = static_cast<size_t>(bh) * pmax;
+  float mloc = -INFINITY;
+  for (int i = tid; i < P; i += kMergeThreads) mloc = fmaxf(mloc, part_ml[2 * (base + i)]);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
-  constexpr int kPer = D / 32;
-  float acc[kPer];
-#pragma unroll
-  for (int j = 0; j < kPer; ++j) acc[j] = 0.f;
-  float L = 0.f;
-  if (M != -INFINITY) {
-    for (int i = 0; i < P; ++i) {
-      const float2 ml = *reinterpret_cast<const float2*>(part_ml + 2 * (base + i));
-      const float w = exp2f(ml.x - M);  // 0 for an empty partition (m = -inf)
-      L = fmaf(w, ml.y, L);
-      const float* src = part_o + (base + i) * D + lane * kPer;
-      if constexpr (kPer == 4) {
-        const float4 v = *reinterpret_cast<const float4*>(src);
-        acc[0] = fmaf(w, v.x, acc[0]);
-        acc[1] = fmaf(w, v.y, acc[1]);
-        acc[2] = fmaf(w, v.z, acc[2]);
-        acc[3] = fmaf(w, v.w, acc[3]);
-      } else {
-        const float2 v = *reinterpret_cast<const float2*>(src);
-        acc[0] = fmaf(w, v.x, acc[0]);
-        acc[1] = fmaf(w, v.y, acc[1]);
-      }
-    }
+  for (int o = 16; o > 0; o >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(kFull, mloc, o));
+  if (lane == 0) red[warp] = mloc;
+  __syncthreads();
+  if (tid == 0) {
+    float m = -INFINITY;
+    for (int w = 0; w < kMergeThreads / 32; ++w) m = fmaxf(m, red[w]);
+    bcast = m;
   }
-  const float inv = L > 0.f ? 1.f / L : 0.f;
-  __nv_bfloat16* o = out + static_cast<size_t>(gw) * D + lane * kPer;
+  __syncthreads();
+  const float M = bcast;
+  float lloc = 0.f;
+  for (int i = tid; i < P; i += kMergeThreads) {
+    const float2 ml = *reinterpret_cast<const float2*>(part_ml + 2 * (base + i));
+    const float w = (M == -INFINITY) ? 0.f : exp2f(ml.x - M);
+    wsm[i] = w;
+    lloc = fmaf(w, ml.y, lloc);
+  }
 #pragma unroll
-  for (int j = 0; j < kPer; j += 2)
-    *reinterpret_cast<__nv_bfloat162*>(o + j) = __floats2bfloat162_rn(acc[j] * inv, acc[j + 1] * inv);
+  for (int o = 16; o > 0; o >>= 1) lloc += __shfl_xor_sync(kFull, lloc, o);
+  __syncthreads();  // red[] reuse and wsm[] complete
+  if (lane == 0) red[warp] = lloc;
+  const int dg = tid % kDG, pg = tid / kDG;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+  for (int i = pg; i < P; i += kPG) {
+    const float w = wsm[i];
+    const float4 v = *reinterpret_cast<const float4*>(part_o + (base + i) * D + 4 * dg);
+    acc.x = fmaf(w, v.x, acc.x);
+    acc.y = fmaf(w, v.y, acc.y);
+    acc.z = fmaf(w, v.z, acc.z);
+    acc.w = fmaf(w, v.w, acc.w);
+  }
+  float* sums = wsm + ((pmax + 3) & ~3);  // 16-byte aligned for the float4 stores
+  *reinterpret_cast<float4*>(sums + pg * D + 4 * dg) = acc;
+  __syncthreads();
+  if (tid < kDG) {
+    float L = 0.f;
+    for (int w = 0; w < kMergeThreads / 32; ++w) L += red[w];
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int g = 0; g < kPG; ++g) {
+      const float4 v = *reinterpret_cast<const float4*>(sums + g * D + 4 * tid);
+      t.x += v.x;
+      t.y += v.y;
+      t.z += v.z;
+      t.w += v.w;
+    }
+    __nv_bfloat16* o = out + static_cast<size_t>(bh) * D + 4 * tid;
+    *reinterpret_cast<__nv_bfloat162*>(o) = __floats2bfloat162_rn(t.x * inv, t.y * inv);
+    *reinterpret_cast<__nv_bfloat162*>(o + 2) = __floats2bfloat162_rn(t.z * inv, t.w * inv);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -141,7 +190,7 @@ __global__ void __launch_bounds__(256)
 // ---------------------------------------------------------------------------
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-WorkspaceLayout workspace_layout(int B, int Hq, int D, int pmax) {
+WorkspaceLayout workspace_layout(int B, int Hq, int Hkv, int D, int pmax) {
   WorkspaceLayout w{};
   size_t off = 0;
   w.counter = off;
@@ -150,6 +199,8 @@ WorkspaceLayout workspace_layout(int B, int Hq, int D, int pmax) {
   off = align_up(off + sizeof(int32_t) * (static_cast<size_t>(B) + 1), 256);
   w.ctx_eff = off;
   off = align_up(off + sizeof(int32_t) * static_cast<size_t>(B), 256);
+  w.arrive = off;
+  off = align_up(off + sizeof(int32_t) * static_cast<size_t>(B) * Hkv, 256);
   const size_t parts = pmax > 1 ? static_cast<size_t>(B) * Hq * pmax : 0;
   w.part_ml = off;
   off = align_up(off + sizeof(float) * 2 * parts, 256);
@@ -171,45 +222,99 @@ size_t decode_smem_bytes(int kv_fp8, int D, int bs, int warps, int stages) {
                   : decode_smem_layout_bytes<128, 32, false>(warps, stages);
 }
 
-static const void* pick_kernel(const DecodeLaunch& L) {
-  const int gt = (L.math == PKV_MATH_FFMA) ? L.G : 0;
-  if (L.kv_fp8) return decode_kernel_fp8_d128(L.bs, L.math, gt);
-  if (L.D == 64) return decode_kernel_bf16_d64(L.bs, L.math, gt);
-  return decode_kernel_bf16_d128(L.bs, L.math, gt);
+static const void* pick_kernel(int kv_fp8, int D, int bs, int math, int G) {
+  const int gt = G;
+  if (kv_fp8) return decode_kernel_fp8_d128(bs, math, gt);
+  if (D == 64) return decode_kernel_bf16_d64(bs, math, gt);
+  return decode_kernel_bf16_d128(bs, math, gt);
+}
+
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("PKV_PDL");
+    return v == nullptr || std::strcmp(v, "0") != 0;
+  }();
+  return on;
+}
+
+// CTAs of the decode kernel that fit on one SM, per (device, kernel, shape);
+// also raises the kernel's dynamic shared memory limit the first time.
+static cudaError_t ctas_per_sm(const void* fn, int threads, size_t smem, int* out) {
+  struct Entry {
+    int dev;
+    const void* fn;
+    int threads;
+    size_t smem;
+    int n;
+  };
+  static std::mutex mu;
+  static std::vector<Entry> cache;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (const Entry& x : cache)
+      if (x.dev == dev && x.fn == fn && x.threads == threads && x.smem == smem) {
+        *out = x.n;
+        return cudaSuccess;
+      }
+  }
+  // Raise the kernel's limit to the device's opt-in maximum (not to this
+  // request), so a cached entry never leaves a smaller limit behind.
+  int optin = 0;
+  e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e != cudaSuccess) return e;
+  if (smem > static_cast<size_t>(optin)) return cudaErrorInvalidValue;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+  if (e != cudaSuccess) return e;
+  int n = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, smem);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  cache.push_back(Entry{dev, fn, threads, smem, n});
+  *out = n;
+  return cudaSuccess;
 }
 
 int decode_ctas_per_sm(const DecodeLaunch& L, size_t smem) {
-  const void* fn = pick_kernel(L);
-  if (fn == nullptr) return 0;
-  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
-      cudaSuccess)
-    return 0;
+  const void* fn = pick_kernel(L.kv_fp8, L.D, L.bs, L.math, L.G);
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, L.warps * 32, smem) != cudaSuccess) return 0;
+  if (fn == nullptr || ctas_per_sm(fn, L.warps * 32, smem, &n) != cudaSuccess) return 0;
   return n;
 }
 
 cudaError_t launch_decode(const DecodeLaunch& L, int* launched) {
   *launched = 0;
-  const void* fn = pick_kernel(L);
+  const void* fn = pick_kernel(L.kv_fp8, L.D, L.bs, L.math, L.G);
   if (fn == nullptr) return cudaErrorInvalidDeviceFunction;
   const size_t smem = decode_smem_bytes(L.kv_fp8, L.D, L.bs, L.warps, L.stages);
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-
-  // 1. planner
-  plan_kernel<<<1, kPlanThreads, 0, L.stream>>>(L.context_lens, L.B, L.MB * L.bs, L.ppu * L.bs,
-                                                L.work_counter, L.unit_start, L.ctx_eff,
-                                                static_cast<__nv_bfloat16*>(L.out), L.Hq * L.D, L.err);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  *launched += 1;
-
-  // 2. decode: persistent grid, at most one warp per possible unit
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, L.warps * 32, smem);
+  cudaError_t e = ctas_per_sm(fn, L.warps * 32, smem, &per_sm);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
+
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+
+  // 1. planner
+  {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(kPlanThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = L.stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, plan_kernel, L.context_lens, L.B, L.Hkv, L.MB * L.bs, L.ppu * L.bs,
+                           L.work_counter, L.unit_start, L.ctx_eff, L.arrive,
+                           static_cast<__nv_bfloat16*>(L.out), L.Hq * L.D, L.err);
+    if (e != cudaSuccess) return e;
+    *launched += 1;
+  }
+
+  // 2. decode: persistent grid, at most one warp per possible unit
   const long long max_units = static_cast<long long>(L.B) * L.Hkv * L.pmax;
   long long grid = static_cast<long long>(L.num_sms) * per_sm;
   grid = std::min(grid, (max_units + L.warps - 1) / L.warps);
@@ -226,6 +331,7 @@ cudaError_t launch_decode(const DecodeLaunch& L, int* launched) {
   p.ctx_eff = L.ctx_eff;
   p.part_ml = L.part_ml;
   p.part_o = L.part_o;
+  p.arrive = L.arrive;
   p.err = L.err;
   p.B = L.B;
   p.Hq = L.Hq;
@@ -236,27 +342,46 @@ cudaError_t launch_decode(const DecodeLaunch& L, int* launched) {
   p.pmax = L.pmax;
   p.ppu = L.ppu;
   p.stages = L.stages;
+  p.fused_merge = (L.pmax <= kFusedMergeMaxParts) ? 1 : 0;
   p.row_base = L.row_base;
   p.scale_log2 = L.scale_log2;
   CUtensorMap kmap = L.kmap, vmap = L.vmap;
   void* args[] = {&kmap, &vmap, &p};
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(L.warps * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = L.stream;
+  // An event recorded between the planner and the decode would sit between
+  // them on the stream; launch without the overlap attribute then.
+  cfg.attrs = attr;
+  cfg.numAttrs = (L.ev_start == nullptr) ? 1 : 0;
   if (L.ev_start != nullptr && (e = cudaEventRecord(L.ev_start, L.stream)) != cudaSuccess) return e;
-  e = cudaLaunchKernel(fn, dim3(static_cast<unsigned>(grid)), dim3(L.warps * 32), args, smem, L.stream);
+  e = cudaLaunchKernelExC(&cfg, fn, args);
   if (e != cudaSuccess) return e;
   if (L.ev_end != nullptr && (e = cudaEventRecord(L.ev_end, L.stream)) != cudaSuccess) return e;
   *launched += 1;
 
-  // 3. merge (only when some sequence can span more than one partition)
-  if (L.pmax > 1) {
-    const int warps_total = L.B * L.Hq;
-    const int blocks = (warps_total + 7) / 8;
+  // 3. merge kernel when sequences may span many partitions
+  if (!p.fused_merge) {
+    cudaLaunchConfig_t mc{};
+    mc.gridDim = dim3(static_cast<unsigned>(L.B * L.Hq));
+    mc.blockDim = dim3(kMergeThreads);
+    const int pg = kMergeThreads / (L.D / 4);
+    mc.dynamicSmemBytes =
+        sizeof(float) * ((static_cast<size_t>(L.pmax) + 3) / 4 * 4 + static_cast<size_t>(pg) * L.D);
+    mc.stream = L.stream;
+    mc.attrs = attr;
+    mc.numAttrs = (L.ev_end == nullptr) ? 1 : 0;
     if (L.D == 64)
-      merge_kernel<64><<<blocks, 256, 0, L.stream>>>(L.part_ml, L.part_o, L.unit_start, L.B, L.Hq,
-                                                     L.pmax, static_cast<__nv_bfloat16*>(L.out));
+      e = cudaLaunchKernelEx(&mc, merge_kernel<64>, static_cast<const float*>(L.part_ml),
+                             static_cast<const float*>(L.part_o), static_cast<const int32_t*>(L.unit_start),
+                             L.Hq, L.pmax, static_cast<__nv_bfloat16*>(L.out));
     else
-      merge_kernel<128><<<blocks, 256, 0, L.stream>>>(L.part_ml, L.part_o, L.unit_start, L.B, L.Hq,
-                                                      L.pmax, static_cast<__nv_bfloat16*>(L.out));
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+      e = cudaLaunchKernelEx(&mc, merge_kernel<128>, static_cast<const float*>(L.part_ml),
+                             static_cast<const float*>(L.part_o), static_cast<const int32_t*>(L.unit_start),
+                             L.Hq, L.pmax, static_cast<__nv_bfloat16*>(L.out));
+    if (e != cudaSuccess) return e;
     *launched += 1;
   }
   return cudaSuccess;

@@ -24,8 +24,10 @@
 //     K/V page read (GQA reuse).  Online softmax in the log2 domain with
 //     fp32 state; the reduction order depends only on logical positions.
 //   * A unit that covers its whole sequence writes the bf16 output; other
-//     units write (max, sum, unnormalised output) partials that the merge
-//     kernel combines (flash-decoding split-K).
+//     units write (max, sum, unnormalised output) partials (flash-decoding
+//     split-K).  With few partitions per sequence the warp that completes
+//     the last partition of a (sequence, KV head) merges them in place; with
+//     many, a separate merge kernel spreads that work over the GPU.
 //   * Two math back-ends share the pipeline: MMA (mma.sync m16n8k16 with the
 //     group's heads on M, tokens on N for q.K^T, and head_dim on N, tokens
 //     on K for P.V) and FFMA (fp32 CUDA-core dot products).
@@ -48,8 +50,10 @@ struct DecodeParams {
   const int32_t* ctx_eff;
   float* part_ml;
   float* part_o;
+  int32_t* arrive;  // [B][Hkv] partitions finished so far (zeroed by the planner)
   unsigned* err;
   int B, Hq, Hkv, G, MB, NB, pmax, ppu, stages;
+  int fused_merge;  // 1: the last warp of a (sequence, KV head) merges; 0: the merge kernel does
   int row_base;
   float scale_log2;
 };
@@ -79,27 +83,45 @@ __host__ __device__ constexpr size_t decode_smem_layout_bytes(int warps, int sta
 // ---------------------------------------------------------------------------
 // MMA back-end state and page step
 // ---------------------------------------------------------------------------
-template <int D, int BS, bool FP8>
+// m16n8k16 tiles with the group's heads on M.  HI = false: at most 8 heads,
+// rows 8..15 of every tile are zero and only rows 0..7 are carried (half the
+// registers); HI = true: up to 16 heads, both row halves carried.
+// Fragment arrays hold {row g k-lo, row g k-hi, row g+8 k-lo, row g+8 k-hi}
+// (A operands) and {row g c0, c1, row g+8 c0, c1} (C/D).
+template <int D, int BS, bool FP8, bool HI>
 struct MmaState {
-  uint32_t qa[D / 16][4];  // A fragments of q (rows = heads of the group)
-  float o[D / 8][4];       // C fragments of the output (rows = heads, cols = d)
-  float m[2];              // running max of rows g and g+8 (log2 domain)
-  float l[2];              // this lane's share of the running sums
+  static constexpr int kR = HI ? 2 : 1;
+  uint32_t qa[D / 16][2 * kR];  // q as A fragments, one entry per k-step of 16 d
+  float o[D / 8][2 * kR];       // output accumulators, one entry per 8 columns of d
+  float m[kR];                  // running max of rows g (and g+8), log2 domain
+  float l[kR];                  // this lane's share of the running sums
 };
 
-template <int D, int BS, bool FP8>
-__device__ __forceinline__ void mma_load_q(MmaState<D, BS, FP8>& st, const __nv_bfloat16* qg,
+template <bool FP8, bool HI, int N>
+__device__ __forceinline__ void mma_rows(float (&d)[N], const uint32_t (&a)[N], uint32_t b0,
+                                         uint32_t b1) {
+  if constexpr (HI) {
+    const uint32_t full[4] = {a[0], a[2], a[1], a[3]};
+    if constexpr (FP8) mma_f16(d, full, b0, b1); else mma_bf16(d, full, b0, b1);
+  } else {
+    if constexpr (FP8) mma_f16_lo(d, a[0], a[1], b0, b1); else mma_bf16_lo(d, a[0], a[1], b0, b1);
+  }
+}
+
+template <int D, int BS, bool FP8, bool HI>
+__device__ __forceinline__ void mma_load_q(MmaState<D, BS, FP8, HI>& st, const __nv_bfloat16* qg,
                                            int G, int lane) {
+  constexpr int kR = HI ? 2 : 1;
   const int g = lane >> 2, tig = lane & 3;
 #pragma unroll
   for (int s = 0; s < D / 16; ++s) {
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
+    for (int half = 0; half < kR; ++half) {
       const int row = g + 8 * half;
       uint32_t lo = 0, hi = 0;
       if (row < G) {
         const __nv_bfloat16* qr = qg + static_cast<size_t>(row) * D;
-        if (!FP8) {
+        if constexpr (!FP8) {
           // k = 2tig, 2tig+1 -> d = 16s + 2tig (+1); k + 8 -> d + 8
           lo = *reinterpret_cast<const uint32_t*>(qr + 16 * s + 2 * tig);
           hi = *reinterpret_cast<const uint32_t*>(qr + 16 * s + 8 + 2 * tig);
@@ -112,41 +134,51 @@ __device__ __forceinline__ void mma_load_q(MmaState<D, BS, FP8>& st, const __nv_
           hi = pack_f16x2(bf16lo_to_f32(w1), bf16hi_to_f32(w1));
         }
       }
-      st.qa[s][half] = lo;       // a0a1 (row g) / a2a3 (row g+8)
-      st.qa[s][2 + half] = hi;   // a4a5 (row g) / a6a7 (row g+8)
+      st.qa[s][2 * half] = lo;
+      st.qa[s][2 * half + 1] = hi;
     }
   }
 #pragma unroll
-  for (int n = 0; n < D / 8; ++n) st.o[n][0] = st.o[n][1] = st.o[n][2] = st.o[n][3] = 0.f;
-  st.m[0] = st.m[1] = -INFINITY;
-  st.l[0] = st.l[1] = 0.f;
+  for (int n = 0; n < D / 8; ++n)
+#pragma unroll
+    for (int e = 0; e < 2 * kR; ++e) st.o[n][e] = 0.f;
+#pragma unroll
+  for (int r = 0; r < kR; ++r) {
+    st.m[r] = -INFINITY;
+    st.l[r] = 0.f;
+  }
 }
 
 // One page (BS tokens) of the online softmax with tensor-core tiles.
-// `valid` = tokens of the page that belong to the sequence (0..BS).
-template <int D, int BS, bool FP8>
-__device__ __forceinline__ void mma_page(MmaState<D, BS, FP8>& st, uint8_t* stage, int valid,
+// `valid` = tokens of the page that belong to the sequence (0..BS); `sl` =
+// softmax scale * log2(e) (* the page's K scale for E4M3); `vscale` = the
+// page's V scale (E4M3 only).
+template <int D, int BS, bool FP8, bool HI>
+__device__ __forceinline__ void mma_page(MmaState<D, BS, FP8, HI>& st, uint8_t* stage, int valid,
                                          float sl, float vscale, int lane) {
   using Geo = PageGeom<D, BS, FP8>;
+  constexpr int kR = HI ? 2 : 1;
+  constexpr int kC = 2 * kR;
   const int g = lane >> 2, tig = lane & 3;
   const uint32_t kbase = smem_addr(stage);
   const uint32_t vbase = kbase + Geo::kTensorBytes;
 
   // ---- S = q . K^T  (rows = heads, cols = tokens) ----
-  float s[BS / 8][4];
+  float s[BS / 8][kC];
 #pragma unroll
   for (int nt = 0; nt < BS / 8; ++nt) {
-    s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+    for (int e = 0; e < kC; ++e) s[nt][e] = 0.f;
     const int row = nt * 8 + (lane & 7);
-    if (!FP8) {
+    if constexpr (!FP8) {
 #pragma unroll
       for (int kk = 0; kk < D / 32; ++kk) {
         const int region = kk >> 1;
         const int chunk = (kk & 1) * 4 + (lane >> 3);
         uint32_t b0, b1, b2, b3;
         ldsm_x4(kbase + region * Geo::kRegionBytes + swz128(row, chunk), b0, b1, b2, b3);
-        mma_bf16(s[nt], st.qa[2 * kk], b0, b1);
-        mma_bf16(s[nt], st.qa[2 * kk + 1], b2, b3);
+        mma_rows<FP8, HI>(s[nt], st.qa[2 * kk], b0, b1);
+        mma_rows<FP8, HI>(s[nt], st.qa[2 * kk + 1], b2, b3);
       }
     } else {
 #pragma unroll
@@ -154,71 +186,90 @@ __device__ __forceinline__ void mma_page(MmaState<D, BS, FP8>& st, uint8_t* stag
         uint32_t r[4];
         ldsm_x4(kbase + swz128(row, c4 * 4 + (lane >> 3)), r[0], r[1], r[2], r[3]);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint32_t b0 = e4m3x2_to_f16x2(r[i] & 0xffffu);
-          const uint32_t b1 = e4m3x2_to_f16x2(r[i] >> 16);
-          mma_f16(s[nt], st.qa[c4 * 4 + i], b0, b1);
-        }
+        for (int i = 0; i < 4; ++i)
+          mma_rows<FP8, HI>(s[nt], st.qa[c4 * 4 + i], e4m3x2_to_f16x2(r[i] & 0xffffu),
+                            e4m3x2_to_f16x2(r[i] >> 16));
       }
     }
   }
 
   // ---- online softmax (log2 domain) ----
-  float mx[2] = {-INFINITY, -INFINITY};
+  const bool partial = valid < BS;  // warp-uniform: only a sequence's last page
+  float mx[kR];
 #pragma unroll
-  for (int nt = 0; nt < BS / 8; ++nt) {
+  for (int r = 0; r < kR; ++r) mx[r] = -INFINITY;
+  if (partial) {
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int tok = nt * 8 + 2 * tig + (e & 1);
-      float v = s[nt][e] * sl;
-      if (tok >= valid) v = -INFINITY;
-      s[nt][e] = v;
-      mx[e >> 1] = fmaxf(mx[e >> 1], v);
-    }
+    for (int nt = 0; nt < BS / 8; ++nt)
+#pragma unroll
+      for (int e = 0; e < kC; ++e) {
+        const int tok = nt * 8 + 2 * tig + (e & 1);
+        const float v = (tok < valid) ? s[nt][e] * sl : -INFINITY;
+        s[nt][e] = v;
+        mx[e >> 1] = fmaxf(mx[e >> 1], v);
+      }
+  } else {
+#pragma unroll
+    for (int nt = 0; nt < BS / 8; ++nt)
+#pragma unroll
+      for (int e = 0; e < kC; ++e) {
+        const float v = s[nt][e] * sl;
+        s[nt][e] = v;
+        mx[e >> 1] = fmaxf(mx[e >> 1], v);
+      }
   }
-  float alpha[2], muse[2];
+  float alpha[kR], muse[kR];
+  bool changed = false;
 #pragma unroll
-  for (int r = 0; r < 2; ++r) {
+  for (int r = 0; r < kR; ++r) {
     mx[r] = fmaxf(mx[r], __shfl_xor_sync(kFull, mx[r], 1));
     mx[r] = fmaxf(mx[r], __shfl_xor_sync(kFull, mx[r], 2));
     const float mnew = fmaxf(st.m[r], mx[r]);
     muse[r] = (mnew == -INFINITY) ? 0.f : mnew;
-    alpha[r] = exp2f(st.m[r] - muse[r]);
+    alpha[r] = ex2_approx(st.m[r] - muse[r]);
+    changed |= (mnew != st.m[r]);
     st.m[r] = mnew;
   }
-  float psum[2] = {0.f, 0.f};
+  float psum[kR];
 #pragma unroll
-  for (int nt = 0; nt < BS / 8; ++nt) {
+  for (int r = 0; r < kR; ++r) psum[r] = 0.f;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float p = exp2f(s[nt][e] - muse[e >> 1]);
-      s[nt][e] = p;
-      psum[e >> 1] += p;
+  for (int nt = 0; nt < BS / 8; ++nt)
+#pragma unroll
+    for (int e = 0; e < kC; ++e) {
+      const float pv = ex2_approx(s[nt][e] - muse[e >> 1]);
+      s[nt][e] = pv;
+      psum[e >> 1] += pv;
     }
+#pragma unroll
+  for (int r = 0; r < kR; ++r) st.l[r] = fmaf(st.l[r], alpha[r], psum[r]);
+  // Rescale O only when some row's running max moved (rare after the first
+  // pages); alpha is exactly 1 for rows whose max did not move.
+  if (__any_sync(kFull, changed)) {
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n)
+#pragma unroll
+      for (int e = 0; e < kC; ++e) st.o[n][e] *= alpha[e >> 1];
   }
-  st.l[0] = st.l[0] * alpha[0] + psum[0];
-  st.l[1] = st.l[1] * alpha[1] + psum[1];
 
-  // P as A fragments: k-step ks covers tokens 16ks .. 16ks+15
-  uint32_t pa[BS / 16][4];
+  // P as A fragments: k-step ks covers tokens 16ks .. 16ks+15 (n-tiles 2ks, 2ks+1)
+  uint32_t pa[BS / 16][kC];
 #pragma unroll
-  for (int ks = 0; ks < BS / 16; ++ks) {
-    if (!FP8) {
-      pa[ks][0] = pack_bf16x2(s[2 * ks][0], s[2 * ks][1]);
-      pa[ks][1] = pack_bf16x2(s[2 * ks][2], s[2 * ks][3]);
-      pa[ks][2] = pack_bf16x2(s[2 * ks + 1][0], s[2 * ks + 1][1]);
-      pa[ks][3] = pack_bf16x2(s[2 * ks + 1][2], s[2 * ks + 1][3]);
-    } else {
-      pa[ks][0] = pack_f16x2(s[2 * ks][0], s[2 * ks][1]);
-      pa[ks][1] = pack_f16x2(s[2 * ks][2], s[2 * ks][3]);
-      pa[ks][2] = pack_f16x2(s[2 * ks + 1][0], s[2 * ks + 1][1]);
-      pa[ks][3] = pack_f16x2(s[2 * ks + 1][2], s[2 * ks + 1][3]);
-    }
-  }
+  for (int ks = 0; ks < BS / 16; ++ks)
+#pragma unroll
+    for (int r = 0; r < kR; ++r)
+#pragma unroll
+      for (int kh = 0; kh < 2; ++kh) {
+        const float* src = s[2 * ks + kh];
+        if constexpr (!FP8)
+          pa[ks][2 * r + kh] = pack_bf16x2(src[2 * r], src[2 * r + 1]);
+        else
+          pa[ks][2 * r + kh] = pack_f16x2(src[2 * r], src[2 * r + 1]);
+      }
 
   // Rows of V past the sequence end may hold anything (even NaN); P is 0
   // there but 0 * NaN is NaN, so clear them before the product.
-  if (valid < BS) {
+  if (partial) {
     uint8_t* vp = stage + Geo::kTensorBytes;
     for (int idx = lane; idx < Geo::kTensorBytes / 16; idx += 32) {
       const int row = (idx % (Geo::kRegionBytes / 16)) / 8;
@@ -228,15 +279,8 @@ __device__ __forceinline__ void mma_page(MmaState<D, BS, FP8>& st, uint8_t* stag
     __syncwarp();
   }
 
-  // ---- O = alpha * O + P . V ----
-  if (!FP8) {
-#pragma unroll
-    for (int n = 0; n < D / 8; ++n) {
-      st.o[n][0] *= alpha[0];
-      st.o[n][1] *= alpha[0];
-      st.o[n][2] *= alpha[1];
-      st.o[n][3] *= alpha[1];
-    }
+  // ---- O += P . V ----
+  if constexpr (!FP8) {
 #pragma unroll
     for (int ks = 0; ks < BS / 16; ++ks) {
       const int mi = lane >> 3;
@@ -247,8 +291,8 @@ __device__ __forceinline__ void mma_page(MmaState<D, BS, FP8>& st, uint8_t* stag
         const int chunk = ((np * 16) % 64) / 8 + (mi >> 1);
         uint32_t b0, b1, b2, b3;
         ldsm_x4_t(vbase + region * Geo::kRegionBytes + swz128(row, chunk), b0, b1, b2, b3);
-        mma_bf16(st.o[2 * np], pa[ks], b0, b1);
-        mma_bf16(st.o[2 * np + 1], pa[ks], b2, b3);
+        mma_rows<FP8, HI>(st.o[2 * np], pa[ks], b0, b1);
+        mma_rows<FP8, HI>(st.o[2 * np + 1], pa[ks], b2, b3);
       }
     }
   } else {
@@ -258,11 +302,13 @@ __device__ __forceinline__ void mma_page(MmaState<D, BS, FP8>& st, uint8_t* stag
     const uint8_t* vrow = stage + Geo::kTensorBytes;
 #pragma unroll
     for (int blk = 0; blk < D / 32; ++blk) {
-      float t[4][4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) t[j][0] = t[j][1] = t[j][2] = t[j][3] = 0.f;
       const int off = 32 * blk + 4 * g;
       const int chunk = off >> 4, within = off & 15;
+      float t[4][kC];  // this page's P . V8 for n-tiles 4*blk .. 4*blk+3
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int e = 0; e < kC; ++e) t[j][e] = 0.f;
 #pragma unroll
       for (int ks = 0; ks < BS / 16; ++ks) {
         const int r0 = ks * 16 + 2 * tig;
@@ -272,19 +318,16 @@ __device__ __forceinline__ void mma_page(MmaState<D, BS, FP8>& st, uint8_t* stag
         const uint32_t x3 = *reinterpret_cast<const uint32_t*>(vrow + swz128(r0 + 9, chunk) + within);
         const uint32_t lo01 = __byte_perm(x0, x1, 0x5140), hi01 = __byte_perm(x0, x1, 0x7362);
         const uint32_t lo23 = __byte_perm(x2, x3, 0x5140), hi23 = __byte_perm(x2, x3, 0x7362);
-        mma_f16(t[0], pa[ks], e4m3x2_to_f16x2(lo01), e4m3x2_to_f16x2(lo23));
-        mma_f16(t[1], pa[ks], e4m3x2_to_f16x2(lo01 >> 16), e4m3x2_to_f16x2(lo23 >> 16));
-        mma_f16(t[2], pa[ks], e4m3x2_to_f16x2(hi01), e4m3x2_to_f16x2(hi23));
-        mma_f16(t[3], pa[ks], e4m3x2_to_f16x2(hi01 >> 16), e4m3x2_to_f16x2(hi23 >> 16));
+        mma_rows<FP8, HI>(t[0], pa[ks], e4m3x2_to_f16x2(lo01), e4m3x2_to_f16x2(lo23));
+        mma_rows<FP8, HI>(t[1], pa[ks], e4m3x2_to_f16x2(lo01 >> 16), e4m3x2_to_f16x2(lo23 >> 16));
+        mma_rows<FP8, HI>(t[2], pa[ks], e4m3x2_to_f16x2(hi01), e4m3x2_to_f16x2(hi23));
+        mma_rows<FP8, HI>(t[3], pa[ks], e4m3x2_to_f16x2(hi01 >> 16), e4m3x2_to_f16x2(hi23 >> 16));
       }
+      // the page's V scale applies to its whole product, in fp32
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        float* o = st.o[4 * blk + j];
-        o[0] = fmaf(vscale, t[j][0], o[0] * alpha[0]);
-        o[1] = fmaf(vscale, t[j][1], o[1] * alpha[0]);
-        o[2] = fmaf(vscale, t[j][2], o[2] * alpha[1]);
-        o[3] = fmaf(vscale, t[j][3], o[3] * alpha[1]);
-      }
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int e = 0; e < kC; ++e) st.o[4 * blk + j][e] = fmaf(vscale, t[j][e], st.o[4 * blk + j][e]);
     }
   }
 }
@@ -296,17 +339,18 @@ __device__ __forceinline__ int mma_out_col(int n, int c) {
   return 32 * (n >> 2) + 4 * c + (n & 3);
 }
 
-template <int D, int BS, bool FP8>
-__device__ __forceinline__ void mma_finish(MmaState<D, BS, FP8>& st, const DecodeParams& p,
+template <int D, int BS, bool FP8, bool HI>
+__device__ __forceinline__ void mma_finish(MmaState<D, BS, FP8, HI>& st, const DecodeParams& p,
                                            int b, int kvh, int pidx, int nparts, int lane) {
+  constexpr int kR = HI ? 2 : 1;
   const int g = lane >> 2, tig = lane & 3;
 #pragma unroll
-  for (int r = 0; r < 2; ++r) {
+  for (int r = 0; r < kR; ++r) {
     st.l[r] += __shfl_xor_sync(kFull, st.l[r], 1);
     st.l[r] += __shfl_xor_sync(kFull, st.l[r], 2);
   }
 #pragma unroll
-  for (int r = 0; r < 2; ++r) {
+  for (int r = 0; r < kR; ++r) {
     const int row = g + 8 * r;
     if (row >= p.G) continue;
     const int h = kvh * p.G + row;
@@ -316,7 +360,7 @@ __device__ __forceinline__ void mma_finish(MmaState<D, BS, FP8>& st, const Decod
 #pragma unroll
       for (int n = 0; n < D / 8; ++n) {
         const float v0 = st.o[n][2 * r] * inv, v1 = st.o[n][2 * r + 1] * inv;
-        if (!FP8) {
+        if constexpr (!FP8) {
           *reinterpret_cast<__nv_bfloat162*>(o + 8 * n + 2 * tig) = __floats2bfloat162_rn(v0, v1);
         } else {
           o[mma_out_col<D, FP8>(n, 2 * tig)] = __float2bfloat16_rn(v0);
@@ -328,11 +372,12 @@ __device__ __forceinline__ void mma_finish(MmaState<D, BS, FP8>& st, const Decod
       float* o = p.part_o + slot * D;
 #pragma unroll
       for (int n = 0; n < D / 8; ++n) {
-        if (!FP8) {
-          *reinterpret_cast<float2*>(o + 8 * n + 2 * tig) = make_float2(st.o[n][2 * r], st.o[n][2 * r + 1]);
+        const float v0 = st.o[n][2 * r], v1 = st.o[n][2 * r + 1];
+        if constexpr (!FP8) {
+          *reinterpret_cast<float2*>(o + 8 * n + 2 * tig) = make_float2(v0, v1);
         } else {
-          o[mma_out_col<D, FP8>(n, 2 * tig)] = st.o[n][2 * r];
-          o[mma_out_col<D, FP8>(n, 2 * tig + 1)] = st.o[n][2 * r + 1];
+          o[mma_out_col<D, FP8>(n, 2 * tig)] = v0;
+          o[mma_out_col<D, FP8>(n, 2 * tig + 1)] = v1;
         }
       }
       if (tig == 0) *reinterpret_cast<float2*>(p.part_ml + 2 * slot) = make_float2(st.m[r], st.l[r]);
@@ -542,6 +587,65 @@ __device__ __forceinline__ void ffma_finish(FfmaState<D, BS, FP8, GT>& st, const
 }
 
 // ---------------------------------------------------------------------------
+// split-K merge, done by the warp that finishes a (sequence, KV head) last
+// ---------------------------------------------------------------------------
+// With partials (m_p, l_p, O_p) of partitions p of one head, M = max_p m_p:
+//   out = sum_p 2^(m_p - M) O_p / sum_p 2^(m_p - M) l_p,
+// the softmax over the union of the partitions' tokens.  An empty partition
+// (m = -inf) has weight 0.
+template <int D>
+__device__ __forceinline__ void arrive_and_merge(const DecodeParams& p, int b, int kvh, int nparts,
+                                                 int lane) {
+  // publish this warp's partials, then count the partition as done
+  __threadfence();
+  __syncwarp();
+  int prev = 0;
+  if (lane == 0) prev = atomicAdd(p.arrive + b * p.Hkv + kvh, 1);
+  prev = __shfl_sync(kFull, prev, 0);
+  if (prev != nparts - 1) return;
+  __threadfence();  // the other partitions' partials are visible from here on
+  constexpr int kPer = D / 32;
+  for (int r = 0; r < p.G; ++r) {
+    const int h = kvh * p.G + r;
+    const size_t base = (static_cast<size_t>(b) * p.Hq + h) * p.pmax;
+    float M = -INFINITY;
+    for (int i = lane; i < nparts; i += 32) M = fmaxf(M, __ldcg(p.part_ml + 2 * (base + i)));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+    float acc[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) acc[j] = 0.f;
+    float L = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll 4
+      for (int i = 0; i < nparts; ++i) {
+        const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml + 2 * (base + i)));
+        const float w = exp2f(ml.x - M);
+        L = fmaf(w, ml.y, L);
+        const float* src = p.part_o + (base + i) * D + lane * kPer;
+        if constexpr (kPer == 4) {
+          const float4 v = __ldcg(reinterpret_cast<const float4*>(src));
+          acc[0] = fmaf(w, v.x, acc[0]);
+          acc[1] = fmaf(w, v.y, acc[1]);
+          acc[2] = fmaf(w, v.z, acc[2]);
+          acc[3] = fmaf(w, v.w, acc[3]);
+        } else {
+          const float2 v = __ldcg(reinterpret_cast<const float2*>(src));
+          acc[0] = fmaf(w, v.x, acc[0]);
+          acc[1] = fmaf(w, v.y, acc[1]);
+        }
+      }
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    __nv_bfloat16* o = p.out + (static_cast<size_t>(b) * p.Hq + h) * D + lane * kPer;
+#pragma unroll
+    for (int j = 0; j < kPer; j += 2)
+      *reinterpret_cast<__nv_bfloat162*>(o + j) = __floats2bfloat162_rn(acc[j] * inv, acc[j + 1] * inv);
+  }
+  if (lane == 0) p.arrive[b * p.Hkv + kvh] = 0;  // ready for the next call on this workspace
+}
+
+// ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
 template <int D, int BS, bool FP8, int MATH, int GT>
@@ -571,6 +675,8 @@ __global__ void __launch_bounds__(256, 1)
   }
   __syncwarp();
   const uint64_t policy = l2_policy_evict_first();
+  pdl_trigger();
+  pdl_wait();  // the planner's output and every input are complete from here on
 
   const int total_units = p.unit_start[p.B] * p.Hkv;
   uint32_t it = 0;  // pages this warp has consumed (stage = it % R, phase = (it / R) & 1)
@@ -649,8 +755,9 @@ __global__ void __launch_bounds__(256, 1)
     const __nv_bfloat16* qg = p.q + (static_cast<size_t>(b) * p.Hq + kvh * p.G) * D;
     bool timed_out = false;
     if (MATH == PKV_MATH_MMA) {
-      MmaState<D, BS, FP8> st;
-      mma_load_q<D, BS, FP8>(st, qg, p.G, lane);
+      constexpr bool kHi = GT > 8;
+      MmaState<D, BS, FP8, kHi> st;
+      mma_load_q<D, BS, FP8, kHi>(st, qg, p.G, lane);
       for (int j = 0; j < npages; ++j) {
         const uint32_t s = it % static_cast<uint32_t>(R);
         const bool landed = mbar_wait_bounded(&bars[s], (it / R) & 1u, kWaitLimitNs);
@@ -662,15 +769,18 @@ __global__ void __launch_bounds__(256, 1)
           ksc = (j < 32) ? __shfl_sync(kFull, ks0, j & 31) : __shfl_sync(kFull, ks1, j & 31);
           vsc = (j < 32) ? __shfl_sync(kFull, vs0, j & 31) : __shfl_sync(kFull, vs1, j & 31);
         }
-        mma_page<D, BS, FP8>(st, ring + static_cast<size_t>(s) * Geo::kStageBytes, valid,
-                             p.scale_log2 * ksc, vsc, lane);
+        mma_page<D, BS, FP8, kHi>(st, ring + static_cast<size_t>(s) * Geo::kStageBytes, valid,
+                                  p.scale_log2 * ksc, vsc, lane);
         fence_proxy_async_smem();  // this lane's reads of the stage precede the refill
         __syncwarp();
         if (j + R < npages) { issue(j + R, it + R); ++issued; }
         ++it;
         ++consumed;
       }
-      if (!timed_out) mma_finish<D, BS, FP8>(st, p, b, kvh, pidx, nparts, lane);
+      if (!timed_out) {
+        mma_finish<D, BS, FP8, kHi>(st, p, b, kvh, pidx, nparts, lane);
+        if (nparts > 1 && p.fused_merge) arrive_and_merge<D>(p, b, kvh, nparts, lane);
+      }
     } else {
       FfmaState<D, BS, FP8, (GT > 0 ? GT : 1)> st;
       ffma_load_q<D, BS, FP8, (GT > 0 ? GT : 1)>(st, qg, lane);
@@ -693,7 +803,10 @@ __global__ void __launch_bounds__(256, 1)
         ++it;
         ++consumed;
       }
-      if (!timed_out) ffma_finish<D, BS, FP8, (GT > 0 ? GT : 1)>(st, p, b, kvh, pidx, nparts, lane);
+      if (!timed_out) {
+        ffma_finish<D, BS, FP8, (GT > 0 ? GT : 1)>(st, p, b, kvh, pidx, nparts, lane);
+        if (nparts > 1 && p.fused_merge) arrive_and_merge<D>(p, b, kvh, nparts, lane);
+      }
     }
     if (timed_out) {
       // Record the failure, give copies still in flight a bounded chance to

@@ -257,9 +257,12 @@ static pkv_status resolve_decode(const pkv_cache_desc* c, int32_t batch, int32_t
   if (math != PKV_MATH_MMA && math != PKV_MATH_FFMA) return fail(PKV_ERR_INVALID_ARG, "math %d", math);
   const bool fp8 = c->dtype == PKV_KV_FP8_E4M3;
   const size_t stage_bytes = static_cast<size_t>(2) * c->block_size * c->head_dim * (fp8 ? 1 : 2);
+  // Defaults measured on GB300: 4 warps per CTA with shallow (2-stage)
+  // rings give several CTAs, i.e. 8+ streaming warps, per SM; deeper rings
+  // only cost occupancy.
   int warps = o.warps_per_cta != 0 ? o.warps_per_cta : env_int("PKV_DECODE_WARPS", 4);
   int stages = o.stages != 0 ? o.stages : env_int("PKV_DECODE_STAGES", 0);
-  if (stages == 0) stages = static_cast<int>(std::clamp<size_t>((48u << 10) / stage_bytes, 3, 8));
+  if (stages == 0) stages = stage_bytes >= (8u << 10) ? 2 : 3;
   if (warps < 1 || warps > 8) return fail(PKV_ERR_INVALID_ARG, "warps_per_cta %d outside 1..8", warps);
   if (stages < 2 || stages > 8) return fail(PKV_ERR_INVALID_ARG, "stages %d outside 2..8", stages);
   const size_t smem = pkv::decode_smem_bytes(fp8, c->head_dim, c->block_size, warps, stages);
@@ -267,15 +270,36 @@ static pkv_status resolve_decode(const pkv_cache_desc* c, int32_t batch, int32_t
     return fail(PKV_ERR_INVALID_ARG, "warps x stages need %zu bytes of shared memory", smem);
   int ppu = o.partition_blocks != 0 ? o.partition_blocks : env_int("PKV_DECODE_PARTITION_BLOCKS", 0);
   if (ppu == 0) {
-    // enough units for every warp of a full persistent grid to take several
-    const long long pages = static_cast<long long>(std::max(batch, 1)) * c->num_kv_heads * MB;
-    const int ctas_per_sm = std::max(1, static_cast<int>((228u * 1024u) / (smem + 1024)));
-    const long long warps_total = static_cast<long long>(num_sms) * ctas_per_sm * warps;
-    const long long want = pages / std::max(1LL, 4 * warps_total);
-    ppu = static_cast<int>(std::clamp<long long>(want, 8, 64));
+    // The decode is a persistent grid of W streaming warps pulling units of
+    // work; its time follows how full the last round of units is.  Estimate
+    // W from shared memory and about 200 registers a thread, count units for
+    // the longest allowed context, take 64-block partitions when one round
+    // holds every unit, else the size of {32, 16, 8} whose last round is
+    // fullest (a larger size unless a smaller one is clearly better).
+    const long long ctas_smem = std::max<long long>(1, (228LL * 1024) / static_cast<long long>(smem + 1024));
+    const long long ctas_regs = std::max<long long>(1, 65536LL / (warps * 32LL * 200));
+    const long long W = static_cast<long long>(num_sms) * std::min(ctas_smem, ctas_regs) * warps;
+    auto units = [&](int pp) {
+      return static_cast<long long>(std::max(batch, 1)) * c->num_kv_heads * ((MB + pp - 1) / pp);
+    };
+    if (units(64) <= W) {
+      ppu = 64;
+    } else {
+      double best = -1.0;
+      for (int pp : {32, 16, 8}) {
+        const double r = static_cast<double>(units(pp)) / static_cast<double>(W);
+        const double eff = r / std::ceil(r);
+        if (eff > best + 0.05) {
+          best = eff;
+          ppu = pp;
+        }
+      }
+    }
   }
   if (ppu < 1 || ppu > 64) return fail(PKV_ERR_INVALID_ARG, "partition_blocks %d outside 1..64", ppu);
   ppu = std::min(ppu, MB);
+  if ((MB + ppu - 1) / ppu > 8192)
+    return fail(PKV_ERR_UNSUPPORTED, "more than 8192 partitions per sequence; raise partition_blocks");
   *L = pkv::DecodeLaunch{};
   L->B = batch;
   L->Hq = Hq;
@@ -301,7 +325,7 @@ size_t pkv_decode_workspace_bytes(const pkv_cache_desc* cache, int32_t batch, in
   // The partition size (and so the workspace) must not depend on the device
   // the call later runs on: size with the largest SM count this build targets.
   if (resolve_decode(cache, batch, num_q_heads, max_blocks_per_seq, opts, 152, &L) != PKV_OK) return 0;
-  return pkv::workspace_layout(L.B, L.Hq, L.D, L.pmax).total;
+  return pkv::workspace_layout(L.B, L.Hq, L.Hkv, L.D, L.pmax).total;
 }
 
 pkv_status pkv_decode_describe(const pkv_cache_desc* cache, int32_t batch, int32_t num_q_heads,
@@ -316,8 +340,8 @@ pkv_status pkv_decode_describe(const pkv_cache_desc* cache, int32_t batch, int32
   plan->math = L.math;
   plan->warps_per_cta = L.warps;
   plan->stages = L.stages;
-  plan->kernels_per_call = L.pmax > 1 ? 3 : 2;
-  plan->workspace_bytes = pkv::workspace_layout(L.B, L.Hq, L.D, L.pmax).total;
+  plan->kernels_per_call = L.pmax > 4 ? 3 : 2;  // the merge kernel runs above 4 partitions
+  plan->workspace_bytes = pkv::workspace_layout(L.B, L.Hq, L.Hkv, L.D, L.pmax).total;
   plan->smem_bytes_per_cta = pkv::decode_smem_bytes(L.kv_fp8, L.D, L.bs, L.warps, L.stages);
   return PKV_OK;
 }
@@ -351,7 +375,7 @@ pkv_status pkv_paged_decode(const pkv_cache_desc* cache, const void* q, int32_t 
   const size_t qbytes = static_cast<size_t>(batch) * num_q_heads * cache->head_dim * 2;
   const uintptr_t qa = reinterpret_cast<uintptr_t>(q), oa = reinterpret_cast<uintptr_t>(out);
   if (qa < oa + qbytes && oa < qa + qbytes) return fail(PKV_ERR_INVALID_ARG, "out overlaps q");
-  const pkv::WorkspaceLayout wl = pkv::workspace_layout(L.B, L.Hq, L.D, L.pmax);
+  const pkv::WorkspaceLayout wl = pkv::workspace_layout(L.B, L.Hq, L.Hkv, L.D, L.pmax);
   if (workspace == nullptr || workspace_bytes < wl.total)
     return fail(PKV_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu", wl.total, workspace_bytes);
 
@@ -389,6 +413,7 @@ pkv_status pkv_paged_decode(const pkv_cache_desc* cache, const void* q, int32_t 
   L.work_counter = reinterpret_cast<int32_t*>(ws + wl.counter);
   L.unit_start = reinterpret_cast<int32_t*>(ws + wl.unit_start);
   L.ctx_eff = reinterpret_cast<int32_t*>(ws + wl.ctx_eff);
+  L.arrive = reinterpret_cast<int32_t*>(ws + wl.arrive);
   L.part_ml = reinterpret_cast<float*>(ws + wl.part_ml);
   L.part_o = reinterpret_cast<float*>(ws + wl.part_o);
   L.err = dev->err_word;

@@ -28,6 +28,16 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialisation attribute may start before the previous kernel on the
+// stream has finished; it must call pdl_wait() before touching memory that
+// kernel writes.  pdl_trigger() lets the next such kernel start launching.
+// Both are no-ops for kernels launched without the attribute.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
@@ -141,6 +151,40 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], u
       "{%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Variants for tiles whose rows 8..15 of A are zero (at most 8 heads in the
+// group): only the lower half of C/D is carried; the upper half is fed zeros
+// and its results are discarded.  a0 = A(row g, k 2t..2t+1), a2 = A(row g,
+// k 2t+8..2t+9).
+__device__ __forceinline__ void mma_bf16_lo(float (&d)[2], uint32_t a0, uint32_t a2, uint32_t b0,
+                                            uint32_t b1) {
+  float u0, u1;  // rows 8..15 of D: zeros, discarded
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%5}, "
+      "{%7,%8}, {%0,%1,%9,%9};"
+      : "+f"(d[0]), "+f"(d[1]), "=f"(u0), "=f"(u1)
+      : "r"(a0), "r"(0u), "r"(a2), "r"(b0), "r"(b1), "f"(0.f));
+  asm volatile("" ::"f"(u0), "f"(u1));  // consumed here; emits nothing
+}
+
+__device__ __forceinline__ void mma_f16_lo(float (&d)[2], uint32_t a0, uint32_t a2, uint32_t b0,
+                                           uint32_t b1) {
+  float u0, u1;
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%5}, "
+      "{%7,%8}, {%0,%1,%9,%9};"
+      : "+f"(d[0]), "+f"(d[1]), "=f"(u0), "=f"(u1)
+      : "r"(a0), "r"(0u), "r"(a2), "r"(b0), "r"(b1), "f"(0.f));
+  asm volatile("" ::"f"(u0), "f"(u1));  // consumed here; emits nothing
+}
+
+// 2^x with the SFU's approximate exponential (relative error about 2^-22;
+// results below 2^-126 flush to zero, -inf gives 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // ---------------------------------------------------------------------------

@@ -23,6 +23,7 @@ struct DecodeLaunch {
   int32_t* work_counter;  // workspace: dynamic work queue head
   int32_t* unit_start;    // workspace: [B+1] prefix of partitions per sequence
   int32_t* ctx_eff;       // workspace: [B] validated context lengths
+  int32_t* arrive;        // workspace: [B][Hkv] split-K partitions finished
   float* part_ml;         // workspace: [B][Hq][pmax][2] (running max, sum)
   float* part_o;          // workspace: [B][Hq][pmax][D]
   unsigned* err;          // device error word
@@ -43,14 +44,17 @@ struct DecodeLaunch {
 
 // Workspace layout for one decode call.
 struct WorkspaceLayout {
-  size_t counter, unit_start, ctx_eff, part_ml, part_o, total;
+  size_t counter, unit_start, ctx_eff, arrive, part_ml, part_o, total;
 };
-WorkspaceLayout workspace_layout(int B, int Hq, int D, int pmax);
+WorkspaceLayout workspace_layout(int B, int Hq, int Hkv, int D, int pmax);
+
+// Programmatic dependent launch on (default) or off (PKV_PDL=0).
+bool pdl_enabled();
 
 // Shared memory per CTA of the decode kernel.
 size_t decode_smem_bytes(int kv_fp8, int D, int bs, int warps, int stages);
 
-// Launch planner + decode (+ merge when pmax > 1).  Returns cudaSuccess or
+// Launch planner + decode (the decode merges split-K partials itself).  Returns cudaSuccess or
 // the first launch error.
 cudaError_t launch_decode(const DecodeLaunch& L, int* launched_kernels);
 

@@ -221,3 +221,23 @@ def test_host_argument_errors():
     with pytest.raises(pkv.PkvError) as ei:       # out aliases q
         pkv.paged_decode(dc.q[0], dc.k, dc.v, dc.bt, dc.cl, [0], 0, out=dc.q[0])
     assert ei.value.status == 1
+
+
+@pytest.mark.parametrize("math", ["mma", "ffma"])
+def test_fp8_scales_spanning_orders_of_magnitude(math):
+    # per-page E4M3 scales spread over three decades within one sequence
+    # (V pages scaled by 1e-3 .. 1, K pages by 0.1 .. 3); values stay O(1),
+    # the range the tolerance is written for.  The oracle dequantises the
+    # same bytes.
+    from workloads import bf16_bits_to_f32, bf16_bits_from_f32, fp8_tile_scales
+    c = random_case(23, 3, 16, 4, 128, 32, [600, 333, 64], kv_dtype="fp8")
+    rng = np.random.Generator(np.random.PCG64(24))
+    fv = (10.0 ** rng.uniform(-3, 0, size=(1, c.NB, 1, 1, 1))).astype(np.float32)
+    fk = rng.uniform(0.1, 3.0, size=(1, c.NB, 1, 1, 1)).astype(np.float32)
+    c.k_src = bf16_bits_from_f32(bf16_bits_to_f32(c.k_src) * fk)
+    c.v_src = bf16_bits_from_f32(bf16_bits_to_f32(c.v_src) * fv)
+    c.k_scale = fp8_tile_scales(c.k_src)
+    c.v_scale = fp8_tile_scales(c.v_src)
+    for ppu in (0, 3):
+        got, want, _, _ = _run(c, math, ppu)
+        assert_close(got, want, f"fp8 wide scales {math} ppu{ppu}")
