@@ -149,6 +149,17 @@ __device__ __forceinline__ void mma_load_q(MmaState<D, BS, FP8, HI>& st, const _
   }
 }
 
+// Token held in column `r` (0..7) of q.K^T n-tile `nt`.  bf16 pages use the
+// natural order.  E4M3 pages permute tokens inside each 16-token k-step so
+// that P's k-slots (2t, 2t+1) and (2t+8, 2t+9) are tokens 4t, 4t+1 and
+// 4t+2, 4t+3: the token quads that the byte-transposing ldmatrix hands each
+// lane of the V operand.
+template <bool FP8>
+__device__ __forceinline__ int qk_token(int nt, int r) {
+  if constexpr (!FP8) return nt * 8 + r;
+  return 16 * (nt >> 1) + 4 * (r >> 1) + 2 * (nt & 1) + (r & 1);
+}
+
 // One page (BS tokens) of the online softmax with tensor-core tiles.
 // `valid` = tokens of the page that belong to the sequence (0..BS); `sl` =
 // softmax scale * log2(e) (* the page's K scale for E4M3); `vscale` = the
@@ -159,7 +170,7 @@ __device__ __forceinline__ void mma_page(MmaState<D, BS, FP8, HI>& st, uint8_t* 
   using Geo = PageGeom<D, BS, FP8>;
   constexpr int kR = HI ? 2 : 1;
   constexpr int kC = 2 * kR;
-  const int g = lane >> 2, tig = lane & 3;
+  const int tig = lane & 3;
   const uint32_t kbase = smem_addr(stage);
   const uint32_t vbase = kbase + Geo::kTensorBytes;
 
@@ -169,7 +180,7 @@ __device__ __forceinline__ void mma_page(MmaState<D, BS, FP8, HI>& st, uint8_t* 
   for (int nt = 0; nt < BS / 8; ++nt) {
 #pragma unroll
     for (int e = 0; e < kC; ++e) s[nt][e] = 0.f;
-    const int row = nt * 8 + (lane & 7);
+    const int row = qk_token<FP8>(nt, lane & 7);
     if constexpr (!FP8) {
 #pragma unroll
       for (int kk = 0; kk < D / 32; ++kk) {
@@ -186,9 +197,11 @@ __device__ __forceinline__ void mma_page(MmaState<D, BS, FP8, HI>& st, uint8_t* 
         uint32_t r[4];
         ldsm_x4(kbase + swz128(row, c4 * 4 + (lane >> 3)), r[0], r[1], r[2], r[3]);
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          mma_rows<FP8, HI>(s[nt], st.qa[c4 * 4 + i], e4m3x2_to_f16x2(r[i] & 0xffffu),
-                            e4m3x2_to_f16x2(r[i] >> 16));
+        for (int i = 0; i < 4; ++i) {
+          uint32_t b0, b1;
+          e4m3x4_to_f16x2x2(r[i], b0, b1);
+          mma_rows<FP8, HI>(s[nt], st.qa[c4 * 4 + i], b0, b1);
+        }
       }
     }
   }
@@ -203,7 +216,7 @@ __device__ __forceinline__ void mma_page(MmaState<D, BS, FP8, HI>& st, uint8_t* 
     for (int nt = 0; nt < BS / 8; ++nt)
 #pragma unroll
       for (int e = 0; e < kC; ++e) {
-        const int tok = nt * 8 + 2 * tig + (e & 1);
+        const int tok = qk_token<FP8>(nt, 2 * tig + (e & 1));
         const float v = (tok < valid) ? s[nt][e] * sl : -INFINITY;
         s[nt][e] = v;
         mx[e >> 1] = fmaxf(mx[e >> 1], v);
@@ -296,47 +309,34 @@ __device__ __forceinline__ void mma_page(MmaState<D, BS, FP8, HI>& st, uint8_t* 
       }
     }
   } else {
-    // E4M3 V: the token pairs each lane needs come from two rows, so read 4
-    // bytes per row, interleave the rows byte by byte and convert pairs.
-    // Output column n of n-tile (4*blk + j) is d = 32*blk + 4*n + j.
-    const uint8_t* vrow = stage + Geo::kTensorBytes;
+    // E4M3 V: a byte-transposing ldmatrix gives each lane four consecutive
+    // tokens of one column (the quads P's k-slots were arranged for), which
+    // convert to two f16x2 B registers; two 16-column chunks per load.
 #pragma unroll
-    for (int blk = 0; blk < D / 32; ++blk) {
-      const int off = 32 * blk + 4 * g;
-      const int chunk = off >> 4, within = off & 15;
-      float t[4][kC];  // this page's P . V8 for n-tiles 4*blk .. 4*blk+3
+    for (int cp = 0; cp < D / 32; ++cp) {
+      float t[4][kC];  // this page's P . V8 for n-tiles 4*cp .. 4*cp+3
 #pragma unroll
       for (int j = 0; j < 4; ++j)
 #pragma unroll
         for (int e = 0; e < kC; ++e) t[j][e] = 0.f;
 #pragma unroll
       for (int ks = 0; ks < BS / 16; ++ks) {
-        const int r0 = ks * 16 + 2 * tig;
-        const uint32_t x0 = *reinterpret_cast<const uint32_t*>(vrow + swz128(r0, chunk) + within);
-        const uint32_t x1 = *reinterpret_cast<const uint32_t*>(vrow + swz128(r0 + 1, chunk) + within);
-        const uint32_t x2 = *reinterpret_cast<const uint32_t*>(vrow + swz128(r0 + 8, chunk) + within);
-        const uint32_t x3 = *reinterpret_cast<const uint32_t*>(vrow + swz128(r0 + 9, chunk) + within);
-        const uint32_t lo01 = __byte_perm(x0, x1, 0x5140), hi01 = __byte_perm(x0, x1, 0x7362);
-        const uint32_t lo23 = __byte_perm(x2, x3, 0x5140), hi23 = __byte_perm(x2, x3, 0x7362);
-        mma_rows<FP8, HI>(t[0], pa[ks], e4m3x2_to_f16x2(lo01), e4m3x2_to_f16x2(lo23));
-        mma_rows<FP8, HI>(t[1], pa[ks], e4m3x2_to_f16x2(lo01 >> 16), e4m3x2_to_f16x2(lo23 >> 16));
-        mma_rows<FP8, HI>(t[2], pa[ks], e4m3x2_to_f16x2(hi01), e4m3x2_to_f16x2(hi23));
-        mma_rows<FP8, HI>(t[3], pa[ks], e4m3x2_to_f16x2(hi01 >> 16), e4m3x2_to_f16x2(hi23 >> 16));
+        uint32_t q[4];
+        ldsm_x2_t_b8(vbase + swz128(ks * 16 + (lane & 15), 2 * cp + (lane >> 4)), q[0], q[1], q[2], q[3]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t b0, b1;
+          e4m3x4_to_f16x2x2(q[j], b0, b1);
+          mma_rows<FP8, HI>(t[j], pa[ks], b0, b1);
+        }
       }
       // the page's V scale applies to its whole product, in fp32
 #pragma unroll
       for (int j = 0; j < 4; ++j)
 #pragma unroll
-        for (int e = 0; e < kC; ++e) st.o[4 * blk + j][e] = fmaf(vscale, t[j][e], st.o[4 * blk + j][e]);
+        for (int e = 0; e < kC; ++e) st.o[4 * cp + j][e] = fmaf(vscale, t[j][e], st.o[4 * cp + j][e]);
     }
   }
-}
-
-// Column (head_dim index) of C-fragment element (n-tile n, column c in 0..7).
-template <int D, bool FP8>
-__device__ __forceinline__ int mma_out_col(int n, int c) {
-  if (!FP8) return 8 * n + c;
-  return 32 * (n >> 2) + 4 * c + (n & 3);
 }
 
 template <int D, int BS, bool FP8, bool HI>
@@ -358,28 +358,15 @@ __device__ __forceinline__ void mma_finish(MmaState<D, BS, FP8, HI>& st, const D
       const float inv = st.l[r] > 0.f ? 1.f / st.l[r] : 0.f;
       __nv_bfloat16* o = p.out + (static_cast<size_t>(b) * p.Hq + h) * D;
 #pragma unroll
-      for (int n = 0; n < D / 8; ++n) {
-        const float v0 = st.o[n][2 * r] * inv, v1 = st.o[n][2 * r + 1] * inv;
-        if constexpr (!FP8) {
-          *reinterpret_cast<__nv_bfloat162*>(o + 8 * n + 2 * tig) = __floats2bfloat162_rn(v0, v1);
-        } else {
-          o[mma_out_col<D, FP8>(n, 2 * tig)] = __float2bfloat16_rn(v0);
-          o[mma_out_col<D, FP8>(n, 2 * tig + 1)] = __float2bfloat16_rn(v1);
-        }
-      }
+      for (int n = 0; n < D / 8; ++n)
+        *reinterpret_cast<__nv_bfloat162*>(o + 8 * n + 2 * tig) =
+            __floats2bfloat162_rn(st.o[n][2 * r] * inv, st.o[n][2 * r + 1] * inv);
     } else {
       const size_t slot = (static_cast<size_t>(b) * p.Hq + h) * p.pmax + pidx;
       float* o = p.part_o + slot * D;
 #pragma unroll
-      for (int n = 0; n < D / 8; ++n) {
-        const float v0 = st.o[n][2 * r], v1 = st.o[n][2 * r + 1];
-        if constexpr (!FP8) {
-          *reinterpret_cast<float2*>(o + 8 * n + 2 * tig) = make_float2(v0, v1);
-        } else {
-          o[mma_out_col<D, FP8>(n, 2 * tig)] = v0;
-          o[mma_out_col<D, FP8>(n, 2 * tig + 1)] = v1;
-        }
-      }
+      for (int n = 0; n < D / 8; ++n)
+        *reinterpret_cast<float2*>(o + 8 * n + 2 * tig) = make_float2(st.o[n][2 * r], st.o[n][2 * r + 1]);
       if (tig == 0) *reinterpret_cast<float2*>(p.part_ml + 2 * slot) = make_float2(st.m[r], st.l[r]);
     }
   }
@@ -446,8 +433,8 @@ __device__ __forceinline__ void ffma_load_k(const uint8_t* kp, int row, int dl, 
     const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const uint32_t h01 = e4m3x2_to_f16x2(ws[i] & 0xffffu);
-      const uint32_t h23 = e4m3x2_to_f16x2(ws[i] >> 16);
+      uint32_t h01, h23;
+      e4m3x4_to_f16x2x2(ws[i], h01, h23);
       const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
       const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
       kf[4 * i] = f01.x;
@@ -480,8 +467,8 @@ __device__ __forceinline__ void ffma_load_v(const uint8_t* vp, int row, int lane
   } else {
     static_assert(D / 32 == 4, "E4M3 pages need head_dim 128");
     const uint32_t w = *reinterpret_cast<const uint32_t*>(vp + swz128(row, d0 >> 4) + (d0 & 15));
-    const uint32_t h01 = e4m3x2_to_f16x2(w & 0xffffu);
-    const uint32_t h23 = e4m3x2_to_f16x2(w >> 16);
+    uint32_t h01, h23;
+    e4m3x4_to_f16x2x2(w, h01, h23);
     const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
     const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
     vf[0] = f01.x;

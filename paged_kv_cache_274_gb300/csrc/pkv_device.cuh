@@ -133,6 +133,17 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
                : "r"(addr));
 }
 
+// Two 16x16-byte tiles, transposed: lanes 0-15 give the row addresses of
+// tile 0, lanes 16-31 those of tile 1.  Lane 4g + t receives, per tile, the
+// bytes of rows 4t..4t+3 in column g (first register) and in column g + 8
+// (second register).
+__device__ __forceinline__ void ldsm_x2_t_b8(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                             uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m16n16.x2.trans.shared.b8 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
 // D = A(16x16, row) * B(16x8, col) + D, bf16 inputs, fp32 accumulate.
 __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1) {
@@ -200,11 +211,18 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Two E4M3 codes (low byte = first element) -> f16x2 (exact).
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t pair16) {
-  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(pair16 & 0xffffu),
-                                             __NV_E4M3);
-  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+// Four E4M3 codes (byte i = element i) -> two f16x2 words: lo = elements
+// (0, 1), hi = elements (2, 3).  The 32-bit word is split into its 16-bit
+// halves and each half converted by the hardware (exact).
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t x, uint32_t& lo, uint32_t& hi) {
+  asm("{\n"
+      " .reg .b16 l, h;\n"
+      " mov.b32 {l, h}, %2;\n"
+      " cvt.rn.f16x2.e4m3x2 %0, l;\n"
+      " cvt.rn.f16x2.e4m3x2 %1, h;\n"
+      "}\n"
+      : "=r"(lo), "=r"(hi)
+      : "r"(x));
 }
 
 // bf16 pair in a 32-bit word -> two floats (exact).
