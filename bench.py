@@ -83,22 +83,36 @@ def barrier(world):
         dist.barrier()
 
 
+def _reduce_device():
+    import torch.distributed as dist
+    return "cuda" if dist.get_backend() == "nccl" else "cpu"
+
+
 def max_over_ranks(x, world):
+    """Largest value over ranks (a step time: the slowest replica sets it)."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=_reduce_device())
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
 
 def sum_over_ranks(x, world):
+    """Sum over ranks (bytes every replica processed)."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=_reduce_device())
     dist.all_reduce(t, op=dist.ReduceOp.SUM)
     return float(t.item())
+
+
+def whole_job_gbs(bytes_per_rank, ms_per_rank, world):
+    """Weak-scaling throughput: all ranks' bytes over the slowest rank's time."""
+    total = sum_over_ranks(float(bytes_per_rank), world)
+    ms = max_over_ranks(float(ms_per_rank), world)
+    return total / (ms * 1e-3) / 1e9, ms, total
 
 
 def hbm_peak():
@@ -464,9 +478,7 @@ def run_ours(args, rank, world):
     c = w.c
     total_ms, kernel_ms, clocks = time_device(w, args.steps, args.warmup, world)
     assert pkv.read_device_error() == 0, "device error word set during the benchmark"
-    ms = max_over_ranks(total_ms / args.steps, world)
-    kv_total = sum_over_ranks(float(w.kv_bytes), world)
-    value = kv_total / (ms * 1e-3) / 1e9
+    value, ms, kv_total = whole_job_gbs(w.kv_bytes, total_ms / args.steps, world)
     peak, peak_kind = hbm_peak()
     per_call_bytes = kv_bytes_of(c, layers=[0])
     k_ms = statistics.mean(kernel_ms)

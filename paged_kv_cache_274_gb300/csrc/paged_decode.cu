@@ -103,12 +103,13 @@ __global__ void __launch_bounds__(kPlanThreads)
 }
 
 // ---------------------------------------------------------------------------
-// merge kernel (many partitions): one CTA per (sequence, query head); its
-// threads split head_dim (4 values each) and the partitions, stage the
-// partition weights in shared memory and reduce across partition groups.
+// merge kernel (many partitions): one CTA per (sequence, query head); thread
+// (pg, dg) owns 4 columns of head_dim and partitions pg, pg + kPG, ...  It
+// folds its partitions in one pass with a running maximum, then the kPG
+// partial results are combined through shared memory:
 //   out = sum_p 2^(m_p - M) O_p / sum_p 2^(m_p - M) l_p,  M = max_p m_p.
 // ---------------------------------------------------------------------------
-constexpr int kMergeThreads = 256;
+constexpr int kMergeThreads = 128;
 
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads)
@@ -117,72 +118,59 @@ __global__ void __launch_bounds__(kMergeThreads)
                  __nv_bfloat16* __restrict__ out) {
   constexpr int kDG = D / 4;                  // threads along head_dim
   constexpr int kPG = kMergeThreads / kDG;    // partition groups
-  extern __shared__ float4 wsm4[];           // [pmax] weights (padded to 4), then [kPG][D] sums
-  float* wsm = reinterpret_cast<float*>(wsm4);
-  __shared__ float red[kMergeThreads / 32];
-  __shared__ float bcast;
+  __shared__ float4 s_acc[kPG][kDG];
+  __shared__ float s_m[kPG][kDG], s_l[kPG][kDG];
   pdl_trigger();
   pdl_wait();
   const int bh = blockIdx.x;
   const int b = bh / Hq;
   const int P = unit_start[b + 1] - unit_start[b];
   if (P < 2) return;  // written by the decode kernel (or zero-filled by the planner)
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const size_t base = static_cast<size_t>(bh) * pmax;
-  float mloc = -INFINITY;
-  for (int i = tid; i < P; i += kMergeThreads) mloc = fmaxf(mloc, part_ml[2 * (base + i)]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(kFull, mloc, o));
-  if (lane == 0) red[warp] = mloc;
-  __syncthreads();
-  if (tid == 0) {
-    float m = -INFINITY;
-    for (int w = 0; w < kMergeThreads / 32; ++w) m = fmaxf(m, red[w]);
-    bcast = m;
-  }
-  __syncthreads();
-  const float M = bcast;
-  float lloc = 0.f;
-  for (int i = tid; i < P; i += kMergeThreads) {
-    const float2 ml = *reinterpret_cast<const float2*>(part_ml + 2 * (base + i));
-    const float w = (M == -INFINITY) ? 0.f : exp2f(ml.x - M);
-    wsm[i] = w;
-    lloc = fmaf(w, ml.y, lloc);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) lloc += __shfl_xor_sync(kFull, lloc, o);
-  __syncthreads();  // red[] reuse and wsm[] complete
-  if (lane == 0) red[warp] = lloc;
+  const int tid = threadIdx.x;
   const int dg = tid % kDG, pg = tid / kDG;
+  const size_t base = static_cast<size_t>(bh) * pmax;
+  float m = -INFINITY, l = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
+#pragma unroll 2
   for (int i = pg; i < P; i += kPG) {
-    const float w = wsm[i];
+    const float2 ml = *reinterpret_cast<const float2*>(part_ml + 2 * (base + i));
     const float4 v = *reinterpret_cast<const float4*>(part_o + (base + i) * D + 4 * dg);
-    acc.x = fmaf(w, v.x, acc.x);
-    acc.y = fmaf(w, v.y, acc.y);
-    acc.z = fmaf(w, v.z, acc.z);
-    acc.w = fmaf(w, v.w, acc.w);
+    const float mn = fmaxf(m, ml.x);
+    if (mn == -INFINITY) continue;  // nothing but empty partitions so far
+    const float a = exp2f(m - mn), w = exp2f(ml.x - mn);
+    l = fmaf(l, a, w * ml.y);
+    acc.x = fmaf(acc.x, a, w * v.x);
+    acc.y = fmaf(acc.y, a, w * v.y);
+    acc.z = fmaf(acc.z, a, w * v.z);
+    acc.w = fmaf(acc.w, a, w * v.w);
+    m = mn;
   }
-  float* sums = wsm + ((pmax + 3) & ~3);  // 16-byte aligned for the float4 stores
-  *reinterpret_cast<float4*>(sums + pg * D + 4 * dg) = acc;
+  s_acc[pg][dg] = acc;
+  s_m[pg][dg] = m;
+  s_l[pg][dg] = l;
   __syncthreads();
-  if (tid < kDG) {
-    float L = 0.f;
-    for (int w = 0; w < kMergeThreads / 32; ++w) L += red[w];
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (pg != 0) return;
+  float M = -INFINITY;
+#pragma unroll
+  for (int g = 0; g < kPG; ++g) M = fmaxf(M, s_m[g][dg]);
+  float L = 0.f;
+  float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (M != -INFINITY) {
+#pragma unroll
     for (int g = 0; g < kPG; ++g) {
-      const float4 v = *reinterpret_cast<const float4*>(sums + g * D + 4 * tid);
-      t.x += v.x;
-      t.y += v.y;
-      t.z += v.z;
-      t.w += v.w;
+      const float w = exp2f(s_m[g][dg] - M);  // 0 for a group with only empty partitions
+      const float4 v = s_acc[g][dg];
+      L = fmaf(w, s_l[g][dg], L);
+      t.x = fmaf(w, v.x, t.x);
+      t.y = fmaf(w, v.y, t.y);
+      t.z = fmaf(w, v.z, t.z);
+      t.w = fmaf(w, v.w, t.w);
     }
-    __nv_bfloat16* o = out + static_cast<size_t>(bh) * D + 4 * tid;
-    *reinterpret_cast<__nv_bfloat162*>(o) = __floats2bfloat162_rn(t.x * inv, t.y * inv);
-    *reinterpret_cast<__nv_bfloat162*>(o + 2) = __floats2bfloat162_rn(t.z * inv, t.w * inv);
   }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  __nv_bfloat16* o = out + static_cast<size_t>(bh) * D + 4 * dg;
+  *reinterpret_cast<__nv_bfloat162*>(o) = __floats2bfloat162_rn(t.x * inv, t.y * inv);
+  *reinterpret_cast<__nv_bfloat162*>(o + 2) = __floats2bfloat162_rn(t.z * inv, t.w * inv);
 }
 
 // ---------------------------------------------------------------------------
@@ -367,9 +355,7 @@ cudaError_t launch_decode(const DecodeLaunch& L, int* launched) {
     cudaLaunchConfig_t mc{};
     mc.gridDim = dim3(static_cast<unsigned>(L.B * L.Hq));
     mc.blockDim = dim3(kMergeThreads);
-    const int pg = kMergeThreads / (L.D / 4);
-    mc.dynamicSmemBytes =
-        sizeof(float) * ((static_cast<size_t>(L.pmax) + 3) / 4 * 4 + static_cast<size_t>(pg) * L.D);
+    mc.dynamicSmemBytes = 0;
     mc.stream = L.stream;
     mc.attrs = attr;
     mc.numAttrs = (L.ev_end == nullptr) ? 1 : 0;

@@ -298,8 +298,8 @@ static pkv_status resolve_decode(const pkv_cache_desc* c, int32_t batch, int32_t
   }
   if (ppu < 1 || ppu > 64) return fail(PKV_ERR_INVALID_ARG, "partition_blocks %d outside 1..64", ppu);
   ppu = std::min(ppu, MB);
-  if ((MB + ppu - 1) / ppu > 8192)
-    return fail(PKV_ERR_UNSUPPORTED, "more than 8192 partitions per sequence; raise partition_blocks");
+  if ((MB + ppu - 1) / ppu > 65536)
+    return fail(PKV_ERR_UNSUPPORTED, "more than 65536 partitions per sequence; raise partition_blocks");
   *L = pkv::DecodeLaunch{};
   L->B = batch;
   L->Hq = Hq;
