@@ -40,7 +40,8 @@ if ROOT not in sys.path:
 METRIC = "paged decode KV-read GB/s and % of GB300 HBM peak; decode steps/s"
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0
-WORKLOADS = ("llama8b_layer", "long_b4_32k", "long_b1_128k", "mixed_prefix", "fp8_shared", "tiny")
+WORKLOADS = ("llama8b_layer", "long_b4_32k", "long_b1_128k", "mixed_prefix", "fp8_shared", "tiny",
+             "copy_blocks")
 
 
 def parse_args():
@@ -298,6 +299,42 @@ class DeviceWorkload:
                              k_scale=self.ks, v_scale=self.vs, opts=opts)
 
 
+class CopyWorkload:
+    """Block copy (copy-on-write / swap): 4096 random blocks of the
+    Llama-3.1-8B layer pool (8 KV heads x 16 tokens x 128 x bf16, K and V:
+    64 KiB a block) to 4096 other blocks of the same pool, HBM to HBM.
+    Bytes per step = read + write = 2 x 4096 x 64 KiB."""
+
+    def __init__(self, rank):
+        import paged_kv_cache_274_gb300 as pkv
+        self.pkv = pkv
+        self.c = c = structure("llama8b_layer")
+        dev = torch.device("cuda", torch.cuda.current_device())
+        g = torch.Generator(device=dev)
+        g.manual_seed(104729 * (rank + 1))
+        shape = (c.NB, c.Hkv, c.bs, c.D)
+        self.k = torch.randn(shape, generator=g, device=dev, dtype=torch.bfloat16)
+        self.v = torch.randn(shape, generator=g, device=dev, dtype=torch.bfloat16)
+        rng = np.random.Generator(np.random.PCG64(1000 * 6 + 9))
+        ids = rng.permutation(c.NB)[:8192]
+        self.pairs = torch.from_numpy(np.stack([ids[:4096], ids[4096:]], axis=1).astype(np.int32)).to(dev)
+        block = c.Hkv * c.bs * c.D * 2 * 2
+        self.kv_bytes = 2 * 4096 * block
+        self.layers = [0]
+        self.append = False
+        self.plan = {"kernels_per_call": 1, "math": 0, "partition_blocks": 0, "max_partitions": 0,
+                     "warps_per_cta": 8, "stages": 0}
+        self.launches_per_step = 1
+        torch.cuda.synchronize()
+
+    def step(self, events=None):
+        if events is not None:
+            events[0][0].record()
+        self.pkv.copy_blocks(self.k, self.v, self.k, self.v, self.pairs)
+        if events is not None:
+            events[0][1].record()
+
+
 # ---------------------------------------------------------------------------
 # timing
 # ---------------------------------------------------------------------------
@@ -474,44 +511,47 @@ def run_ours(args, rank, world):
     opts_kw = dict(partition_blocks=args.partition_blocks,
                    math={"auto": pkv.MATH_AUTO, "mma": pkv.MATH_MMA, "ffma": pkv.MATH_FFMA}[args.math],
                    warps=args.warps, stages=args.stages)
-    w = DeviceWorkload(args.workload, rank, opts_kw)
+    copy = args.workload == "copy_blocks"
+    w = CopyWorkload(rank) if copy else DeviceWorkload(args.workload, rank, opts_kw)
     c = w.c
     total_ms, kernel_ms, clocks = time_device(w, args.steps, args.warmup, world)
     assert pkv.read_device_error() == 0, "device error word set during the benchmark"
     value, ms, kv_total = whole_job_gbs(w.kv_bytes, total_ms / args.steps, world)
     peak, peak_kind = hbm_peak()
-    per_call_bytes = kv_bytes_of(c, layers=[0])
+    per_call_bytes = w.kv_bytes if copy else kv_bytes_of(c, layers=[0])
     k_ms = statistics.mean(kernel_ms)
     achieved = per_call_bytes / (k_ms * 1e-3) / 1e9
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not copy:
         e_ms, h2d, d2h = time_e2e(w, max(5, args.steps // 2), max(3, args.warmup), world)
         e_ms = max_over_ranks(e_ms / max(5, args.steps // 2), world)
         e2e = {"value": kv_total / (e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e_ms,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not copy:
         gbs, secs, threads, desc = oracle_sample(args.workload, args.cpu_seconds)
         cpu = {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": desc,
                "seconds": secs}
     if rank == 0:
         plan = w.plan
         line = {
-            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "metric": "paged KV block copy GB/s (read + write bytes)" if copy else METRIC,
+            "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "fp8-e4m3 kv, f16 mma, fp32 accumulate" if c.kv_dtype == "fp8"
             else "bf16 kv, bf16 mma, fp32 accumulate",
             "data": "synthetic (seeded N(0,1) K/V/q, seeded block permutations)",
             "config": config_of(args.workload, c, {
                 "parallelism": "replicas" if world > 1 else "single GPU",
-                "math": {1: "ffma", 2: "mma"}[plan["math"]],
+                "math": {0: "-", 1: "ffma", 2: "mma"}[plan["math"]],
                 "partition_blocks": plan["partition_blocks"], "max_partitions": plan["max_partitions"],
                 "warps_per_cta": plan["warps_per_cta"], "stages": plan["stages"]}),
             "kv_bytes_per_step": w.kv_bytes,
             "decode_steps_per_s": 1e3 / ms,
             "pct_of_hbm_peak": 100.0 * value / peak,
             "pct_of_nominal_8tbs": 100.0 * value / 8000.0,
-            "roofline": {"bound": "hbm", "kernel": "paged_decode_kernel", "achieved": achieved,
+            "roofline": {"bound": "hbm", "kernel": "copy_blocks_kernel" if copy else "paged_decode_kernel",
+                         "achieved": achieved,
                          "peak": peak, "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                          if peak_kind == "measured" else "fallback 6.8 TB/s",
                          "unit": "GB/s", "frac": achieved / peak,

@@ -247,6 +247,37 @@ pkv_status pkv_paged_decode_static_workspace(const pkv_cache_desc* cache,
                                              const pkv_decode_opts* opts, void* stream);
 
 /*
+ * Copy whole physical blocks between two block pools of the same page shape
+ * (`cache` gives bs, Hkv, D and dtype; num_slots and num_blocks are not
+ * used).  For each pair i, block src_ids[i] of the source pool is copied to
+ * block dst_ids[i] of the destination pool: every KV head's K and V page
+ * and, for E4M3 pools, its K and V scales.
+ * Sources: [BW] "PagedAttention" (block sharing: a sequence that appends
+ * into a shared block first needs its own copy) and "KV-Cache Engineering:
+ * The Memory Wall of LLM Serving", "Lever 5: Offloading" and "When the cache
+ * fills" (moving a sequence's blocks to host memory and back).
+ *
+ *   src_k, src_v     source pool, [src_num_blocks][Hkv][bs][D]: device memory,
+ *                    or host memory the GPU can address (pinned memory; on
+ *                    systems with a coherent CPU-GPU interconnect any host
+ *                    memory).  Point them at the first block of a cache slot.
+ *   dst_k, dst_v     destination pool, [dst_num_blocks][Hkv][bs][D], same rules.
+ *   src/dst_k_scale, src/dst_v_scale  fp32 [num_blocks][Hkv], E4M3 pools only.
+ *   block_pairs      device int32 [count][2]: (src id, dst id).  Ids outside
+ *                    their pool set PKV_DEVERR_BLOCK_ID and the pair is
+ *                    skipped.  Two pairs with the same destination, or a
+ *                    destination that is also a source of the same call:
+ *                    unspecified result (validate mode rejects the first).
+ * Bytes move unchanged (bit-exact).  One kernel launch (none when count == 0).
+ */
+pkv_status pkv_copy_blocks(const pkv_cache_desc* cache,
+                           const void* src_k, const void* src_v, const float* src_k_scale,
+                           const float* src_v_scale, int32_t src_num_blocks,
+                           void* dst_k, void* dst_v, float* dst_k_scale, float* dst_v_scale,
+                           int32_t dst_num_blocks, const int32_t* block_pairs, int32_t count,
+                           void* stream);
+
+/*
  * Synchronise `stream`, copy the current device's sticky error word into
  * *flags (PKV_DEVERR_* bits) and clear it.  Returns PKV_ERR_DEVICE_INDEX if
  * it was non-zero, PKV_OK if it was zero.

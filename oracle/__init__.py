@@ -76,6 +76,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.pkv_oracle_paged_decode.argtypes = [P, i32, i32, P, P, i32, P, P,
                                             i32, i32, i32, i32, i32,
                                             P, i32, P, P, i32, i32, f32, P, P, i32]
+    lib.pkv_oracle_copy_blocks.restype = ctypes.c_int
+    lib.pkv_oracle_copy_blocks.argtypes = [P, P, P, P, i32, P, P, P, P, i32, P, i32, i64, i32]
     lib.pkv_oracle_num_threads.restype = ctypes.c_int
     lib.pkv_oracle_num_threads.argtypes = []
     return lib
@@ -203,3 +205,19 @@ def paged_decode(q_bits, k_cache, v_cache, block_tables, context_lens, kv_group_
     if rc != ORACLE_OK:
         raise ValueError(f"oracle paged_decode status {rc}")
     return out
+
+
+def copy_blocks(src_k, src_v, dst_k, dst_v, pairs, src_k_scale=None, src_v_scale=None,
+                dst_k_scale=None, dst_v_scale=None, lib=None) -> int:
+    """In-place block copy between pools [NB][Hkv][bs][D] (numpy, any dtype),
+    pairs (src, dst) applied in order.  Returns the oracle status."""
+    pr = _c(pairs, np.int32).reshape(-1, 2)
+    for a in (src_k, src_v, dst_k, dst_v):
+        assert a.flags.c_contiguous
+    nb_bytes = int(np.prod(src_k.shape[1:])) * src_k.dtype.itemsize
+    fp8 = src_k_scale is not None
+    hkv = int(src_k.shape[1])
+    return int(_load(lib).pkv_oracle_copy_blocks(
+        _ptr(src_k), _ptr(src_v), _ptr(src_k_scale), _ptr(src_v_scale), int(src_k.shape[0]),
+        _ptr(dst_k), _ptr(dst_v), _ptr(dst_k_scale), _ptr(dst_v_scale), int(dst_k.shape[0]),
+        _ptr(pr), int(pr.shape[0]), nb_bytes, hkv if fp8 else 0))

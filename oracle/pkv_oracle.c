@@ -296,6 +296,36 @@ int pkv_oracle_paged_decode(const uint16_t* q, int32_t B, int32_t Hq,
   return ORACLE_OK;
 }
 
+/* ------------------------------------------------------------------------ */
+/* Block copy between two pools (copy-on-write of a shared block; moving a  */
+/* sequence's blocks to host memory and back)                               */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Pools are [num_blocks][block_bytes] for K and V (and [num_blocks][Hkv]
+ * fp32 scales for E4M3 pools, NULL otherwise).  Pairs are applied in order:
+ * dst[pairs[i][1]] = src[pairs[i][0]].  Returns ORACLE_BAD_BLOCK (copying
+ * nothing) if an id is out of range.
+ */
+int pkv_oracle_copy_blocks(const uint8_t* src_k, const uint8_t* src_v, const float* src_ks,
+                           const float* src_vs, int32_t src_nb, uint8_t* dst_k, uint8_t* dst_v,
+                           float* dst_ks, float* dst_vs, int32_t dst_nb, const int32_t* pairs,
+                           int32_t count, int64_t block_bytes, int32_t scales_per_block) {
+  for (int32_t i = 0; i < count; ++i)
+    if (pairs[2 * i] < 0 || pairs[2 * i] >= src_nb || pairs[2 * i + 1] < 0 || pairs[2 * i + 1] >= dst_nb)
+      return ORACLE_BAD_BLOCK;
+  for (int32_t i = 0; i < count; ++i) {
+    const int64_t s = pairs[2 * i], d = pairs[2 * i + 1];
+    memcpy(dst_k + d * block_bytes, src_k + s * block_bytes, (size_t)block_bytes);
+    memcpy(dst_v + d * block_bytes, src_v + s * block_bytes, (size_t)block_bytes);
+    if (src_ks != NULL) {
+      memcpy(dst_ks + d * scales_per_block, src_ks + s * scales_per_block, sizeof(float) * (size_t)scales_per_block);
+      memcpy(dst_vs + d * scales_per_block, src_vs + s * scales_per_block, sizeof(float) * (size_t)scales_per_block);
+    }
+  }
+  return ORACLE_OK;
+}
+
 /* Number of threads the OpenMP runtime would use (1 without OpenMP). */
 int pkv_oracle_num_threads(void) {
 #ifdef _OPENMP

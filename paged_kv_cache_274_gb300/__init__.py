@@ -92,6 +92,8 @@ def load() -> ctypes.CDLL:
         lib.pkv_paged_decode_static_workspace.restype = ctypes.c_int
         lib.pkv_paged_decode_static_workspace.argtypes = [pdesc, P, i32, i32, P, P, P, P, P, i32, P,
                                                           P, i32, i32, f32, P, popts, P]
+        lib.pkv_copy_blocks.restype = ctypes.c_int
+        lib.pkv_copy_blocks.argtypes = [pdesc, P, P, P, P, i32, P, P, P, P, i32, P, i32, P]
         lib.pkv_read_device_error.restype = ctypes.c_int
         lib.pkv_read_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), P]
         lib.pkv_status_string.restype = ctypes.c_char_p
@@ -242,6 +244,30 @@ def paged_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
         int(layer), float(scale), _ptr(out), _ptr(workspace), int(workspace.numel()),
         ctypes.byref(opts) if opts is not None else None, _stream_handle(stream)))
     return out
+
+
+def copy_blocks(src_k: torch.Tensor, src_v: torch.Tensor, dst_k: torch.Tensor,
+                dst_v: torch.Tensor, block_pairs: torch.Tensor,
+                src_k_scale: Optional[torch.Tensor] = None, src_v_scale: Optional[torch.Tensor] = None,
+                dst_k_scale: Optional[torch.Tensor] = None, dst_v_scale: Optional[torch.Tensor] = None,
+                stream=None) -> None:
+    """Copy blocks ``block_pairs[i] = (src, dst)`` (device int32 [n][2]) from
+    one pool ``[NB][Hkv][bs][D]`` to another.  Pools may live in device
+    memory or in pinned host memory (``tensor.pin_memory()``)."""
+    for n, t in (("src_k", src_k), ("src_v", src_v), ("dst_k", dst_k), ("dst_v", dst_v)):
+        if t.dim() != 4 or not t.is_contiguous():
+            raise PkvError(1, f"{n} must be a contiguous [NB][Hkv][bs][D] tensor")
+        if not (t.is_cuda or t.is_pinned()):
+            raise PkvError(1, f"{n} must be a CUDA tensor or pinned host memory")
+    if src_k.shape[1:] != dst_k.shape[1:] or src_k.dtype != dst_k.dtype:
+        raise PkvError(1, "source and destination pages differ in shape or dtype")
+    _need_cuda("block_pairs", block_pairs, torch.int32)
+    desc = cache_desc(src_k.unsqueeze(0))
+    n = int(block_pairs.shape[0])
+    _check(load().pkv_copy_blocks(
+        ctypes.byref(desc), _ptr(src_k), _ptr(src_v), _ptr(src_k_scale), _ptr(src_v_scale),
+        int(src_k.shape[0]), _ptr(dst_k), _ptr(dst_v), _ptr(dst_k_scale), _ptr(dst_v_scale),
+        int(dst_k.shape[0]), _ptr(block_pairs), n, _stream_handle(stream)))
 
 
 STATIC_WORKSPACE_MAX_BYTES = 16 << 20

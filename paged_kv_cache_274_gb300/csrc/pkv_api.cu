@@ -431,6 +431,53 @@ pkv_status pkv_paged_decode(const pkv_cache_desc* cache, const void* q, int32_t 
   return PKV_OK;
 }
 
+pkv_status pkv_copy_blocks(const pkv_cache_desc* cache, const void* src_k, const void* src_v,
+                           const float* src_k_scale, const float* src_v_scale, int32_t src_num_blocks,
+                           void* dst_k, void* dst_v, float* dst_k_scale, float* dst_v_scale,
+                           int32_t dst_num_blocks, const int32_t* block_pairs, int32_t count,
+                           void* stream) {
+  pkv_status st = check_cache_desc(cache);
+  if (st != PKV_OK) return st;
+  if (count < 0 || src_num_blocks < 1 || dst_num_blocks < 1)
+    return fail(PKV_ERR_INVALID_ARG, "count %d, src_num_blocks %d, dst_num_blocks %d", count,
+                src_num_blocks, dst_num_blocks);
+  if (count == 0) return PKV_OK;
+  const bool fp8 = cache->dtype == PKV_KV_FP8_E4M3;
+  if (!src_k || !src_v || !dst_k || !dst_v || !block_pairs)
+    return fail(PKV_ERR_INVALID_ARG, "NULL pointer");
+  if (fp8 && (!src_k_scale || !src_v_scale || !dst_k_scale || !dst_v_scale))
+    return fail(PKV_ERR_INVALID_ARG, "E4M3 pools need source and destination scales");
+  if (!aligned16(src_k) || !aligned16(src_v) || !aligned16(dst_k) || !aligned16(dst_v))
+    return fail(PKV_ERR_ALIGNMENT, "pools must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(block_pairs) & 3u) != 0)
+    return fail(PKV_ERR_ALIGNMENT, "block_pairs must be 4-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != PKV_OK) return st;
+  if (env_flag("PKV_VALIDATE")) {
+    std::vector<int32_t> pr;
+    if ((st = fetch(pr, block_pairs, static_cast<size_t>(count) * 2, s)) != PKV_OK) return st;
+    std::vector<int32_t> dsts;
+    for (int i = 0; i < count; ++i) {
+      if (pr[2 * i] < 0 || pr[2 * i] >= src_num_blocks || pr[2 * i + 1] < 0 || pr[2 * i + 1] >= dst_num_blocks)
+        return fail(PKV_ERR_INVALID_ARG, "block_pairs[%d] = (%d, %d) out of range", i, pr[2 * i], pr[2 * i + 1]);
+      dsts.push_back(pr[2 * i + 1]);
+    }
+    std::sort(dsts.begin(), dsts.end());
+    if (std::adjacent_find(dsts.begin(), dsts.end()) != dsts.end())
+      return fail(PKV_ERR_INVALID_ARG, "block_pairs has a repeated destination");
+  }
+  const int64_t block_bytes = static_cast<int64_t>(cache->num_kv_heads) * cache->block_size *
+                              cache->head_dim * (fp8 ? 1 : 2);
+  cudaError_t e = pkv::launch_copy_blocks(src_k, src_v, fp8 ? src_k_scale : nullptr,
+                                          fp8 ? src_v_scale : nullptr, src_num_blocks, dst_k, dst_v,
+                                          fp8 ? dst_k_scale : nullptr, fp8 ? dst_v_scale : nullptr,
+                                          dst_num_blocks, block_pairs, count, block_bytes,
+                                          cache->num_kv_heads, dev->num_sms, dev->err_word, s);
+  if (e != cudaSuccess) return cuda_fail(e, "copy_blocks launch");
+  return PKV_OK;
+}
+
 pkv_status pkv_read_device_error(uint32_t* flags, void* stream) {
   if (flags == nullptr) return fail(PKV_ERR_INVALID_ARG, "flags is NULL");
   DeviceInfo* dev = nullptr;

@@ -70,4 +70,11 @@ cudaError_t launch_kv_append(int kv_fp8, const void* k, const void* v,
                              int64_t nslots, void* k_base, void* v_base, const float* ks_base,
                              const float* vs_base, unsigned* err, cudaStream_t stream);
 
+// Block copy between two pools of the same page shape.
+cudaError_t launch_copy_blocks(const void* src_k, const void* src_v, const float* src_ks,
+                               const float* src_vs, int src_nb, void* dst_k, void* dst_v,
+                               float* dst_ks, float* dst_vs, int dst_nb, const int32_t* pairs,
+                               int count, int64_t block_bytes, int scales_per_block,
+                               int num_sms, unsigned* err, cudaStream_t stream);
+
 }  // namespace pkv

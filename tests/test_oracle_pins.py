@@ -321,11 +321,35 @@ def pin_append_fp8(lib=None):
             assert np.array_equal(vc[0, blk, h, off], torch_f32_to_e4m3(qv))
 
 
+def pin_copy_blocks(lib=None):
+    # every destination block equals its source block; nothing else moves;
+    # copying back restores the source pool
+    rng = np.random.Generator(np.random.PCG64(120))
+    shape_a, shape_b = (11, 2, 16, 64), (7, 2, 16, 64)
+    ak = rng.integers(0, 1 << 16, size=shape_a, dtype=np.uint16)
+    av = rng.integers(0, 1 << 16, size=shape_a, dtype=np.uint16)
+    bk = rng.integers(0, 1 << 16, size=shape_b, dtype=np.uint16)
+    bv = rng.integers(0, 1 << 16, size=shape_b, dtype=np.uint16)
+    pairs = np.array([[3, 0], [9, 5], [0, 2], [10, 6]], np.int32)
+    bk0, bv0 = bk.copy(), bv.copy()
+    assert oracle.copy_blocks(ak, av, bk, bv, pairs, lib=lib) == 0
+    for s_, d_ in pairs:
+        assert np.array_equal(bk[d_], ak[s_]) and np.array_equal(bv[d_], av[s_])
+    untouched = [i for i in range(shape_b[0]) if i not in set(pairs[:, 1])]
+    assert np.array_equal(bk[untouched], bk0[untouched]) and np.array_equal(bv[untouched], bv0[untouched])
+    ak2, av2 = ak.copy(), av.copy()
+    ak2[pairs[:, 0]] = 0
+    av2[pairs[:, 0]] = 0
+    assert oracle.copy_blocks(bk, bv, ak2, av2, pairs[:, ::-1].copy(), lib=lib) == 0
+    assert np.array_equal(ak2, ak) and np.array_equal(av2, av)
+    assert oracle.copy_blocks(ak, av, bk, bv, np.array([[11, 0]], np.int32), lib=lib) == oracle.ORACLE_BAD_BLOCK
+
+
 PINS = [pin_sdpa_bf16, pin_large_logits, pin_closed_forms, pin_permutation_invariance,
         pin_shared_prefix, pin_poisoned_unused, pin_gqa_equals_repeated_mha,
         pin_shared_with_pointer, pin_sdpa_fp8, pin_bad_inputs_rejected,
         pin_e4m3_decode_all_codes, pin_e4m3_encode_matches_library, pin_e4m3_scaled_quantize,
-        pin_append_scatter, pin_append_fp8]
+        pin_append_scatter, pin_append_fp8, pin_copy_blocks]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -353,6 +377,8 @@ MUTANTS = [
     ("e4m3_wrong_bias", "mag = ldexp(1.0 + (double)mantissa / 8.0, exponent - 7);",
      "mag = ldexp(1.0 + (double)mantissa / 8.0, exponent - 6);"),
     ("e4m3_ties_up", "else code = (lo % 2 == 0) ? lo : lo + 1;", "else code = lo + 1;"),
+    ("copy_wrong_source", "memcpy(dst_k + d * block_bytes, src_k + s * block_bytes",
+     "memcpy(dst_k + d * block_bytes, src_k + d * block_bytes"),
     ("append_wrong_offset", "int64_t blk = s / bs, off = s % bs;", "int64_t blk = s / bs, off = (s + 1) % bs;"),
 ]
 
