@@ -6,7 +6,8 @@ One step = one pass of the whole hot path over one batch:
       (8 KV heads, head_dim 128, block 16, bf16) -- 1 GiB of KV read;
   long_b4_32k / long_b1_128k: paged_decode, 64 q / 8 KV heads, block 32;
   mixed_prefix: 256 sequences, log-uniform lengths, shared prefix blocks;
-  fp8_shared: four layer calls that read one E4M3 cache (shared-with pointer).
+  fp8_shared: four layer calls that read one E4M3 cache (shared-with pointer);
+  int8_shared: the same with an INT8 cache, per-page (scale, zero) pairs.
 
 Metric: KV bytes read per step / step time (GB/s, 1e9), with % of the
 measured HBM peak and decode steps/s beside it.  Inputs (>= 512 MiB of KV)
@@ -40,8 +41,8 @@ if ROOT not in sys.path:
 METRIC = "paged decode KV-read GB/s and % of GB300 HBM peak; decode steps/s"
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0
-WORKLOADS = ("llama8b_layer", "long_b4_32k", "long_b1_128k", "mixed_prefix", "fp8_shared", "tiny",
-             "copy_blocks")
+WORKLOADS = ("llama8b_layer", "long_b4_32k", "long_b1_128k", "mixed_prefix", "fp8_shared",
+             "int8_shared", "tiny", "copy_blocks")
 
 
 def parse_args():
@@ -211,18 +212,23 @@ def structure(name):
         return gen.mixed_prefix_case(fill=False)
     if name == "fp8_shared":
         return gen.fp8_shared_case(fill=False)
+    if name == "int8_shared":
+        return gen.fp8_shared_case(fill=False, kv_dtype="int8a")
     return gen.tiny_case()
 
 
 def kv_bytes_of(c, seqs=None, layers=None):
     """Algorithmic KV bytes one decode call reads: every real token's K and V
-    row of its KV heads (no tail padding), plus per-page E4M3 scales."""
-    elem = 1 if c.kv_dtype == "fp8" else 2
+    row of its KV heads (no tail padding), plus per-page E4M3 scales or
+    INT8 (scale, zero) pairs."""
+    one_byte = c.kv_dtype != "bf16"
+    elem = 1 if one_byte else 2
     idx = range(c.B) if seqs is None else seqs
     ctx = np.asarray(c.context_lens, dtype=np.int64)[list(idx)]
     b = int(ctx.sum()) * 2 * c.Hkv * c.D * elem
-    if c.kv_dtype == "fp8":
-        b += int(((ctx + c.bs - 1) // c.bs).sum()) * 2 * c.Hkv * 4
+    if one_byte:
+        per_page = 4 if c.kv_dtype == "fp8" else 8
+        b += int(((ctx + c.bs - 1) // c.bs).sum()) * 2 * c.Hkv * per_page
     n_layers = len(layers) if layers is not None else c.L
     return b * n_layers
 
@@ -244,6 +250,12 @@ class DeviceWorkload:
             self.ks = torch.empty(shape[:3], dtype=torch.float32, device=dev)
             self.vs = torch.empty(shape[:3], dtype=torch.float32, device=dev)
             self._fill_fp8(g)
+        elif c.kv_dtype.startswith("int8"):
+            self.k = torch.empty(shape, dtype=torch.int8, device=dev)
+            self.v = torch.empty(shape, dtype=torch.int8, device=dev)
+            self.ks = torch.empty(shape[:3] + (2,), dtype=torch.float32, device=dev)
+            self.vs = torch.empty(shape[:3] + (2,), dtype=torch.float32, device=dev)
+            self._fill_int8(g)
         else:
             self.k = torch.randn(shape, generator=g, device=dev, dtype=torch.bfloat16)
             self.v = torch.randn(shape, generator=g, device=dev, dtype=torch.bfloat16)
@@ -280,6 +292,28 @@ class DeviceWorkload:
                 s = amax / 448.0
                 s[amax == 0] = 1.0
                 sc[0, b0:b0 + nb] = s
+                toks.append(src.permute(0, 2, 1, 3).reshape(nb * c.bs, c.Hkv, c.D).contiguous())
+            slots = torch.arange(b0 * c.bs, (b0 + nb) * c.bs, device=self.dev, dtype=torch.int64)
+            pkv.kv_append(toks[0], toks[1], slots, self.k, self.v, self.ks, self.vs)
+        torch.cuda.synchronize()
+
+    def _fill_int8(self, g):
+        """INT8 cache from bf16 N(0,1) data through the library's append, with
+        asymmetric per-(block, KV head) parameters: scale (max - min) / 255,
+        zero point round(-128 - min / scale)."""
+        c, pkv = self.c, self.pkv
+        chunk = 2048
+        for b0 in range(0, c.NB, chunk):
+            nb = min(chunk, c.NB - b0)
+            toks = []
+            for prm in (self.ks, self.vs):
+                src = torch.randn((nb, c.Hkv, c.bs, c.D), generator=g, device=self.dev, dtype=torch.bfloat16)
+                lo = src.float().amin(dim=(2, 3))
+                hi = src.float().amax(dim=(2, 3))
+                s = (hi - lo) / 255.0
+                s[s == 0] = 1.0
+                prm[0, b0:b0 + nb, :, 0] = s
+                prm[0, b0:b0 + nb, :, 1] = torch.round(-128.0 - lo / s).clamp(-128, 127)
                 toks.append(src.permute(0, 2, 1, 3).reshape(nb * c.bs, c.Hkv, c.D).contiguous())
             slots = torch.arange(b0 * c.bs, (b0 + nb) * c.bs, device=self.dev, dtype=torch.int64)
             pkv.kv_append(toks[0], toks[1], slots, self.k, self.v, self.ks, self.vs)
@@ -422,13 +456,19 @@ def oracle_sample(name, target_s):
     c = structure(name)
     shape = (c.S, c.NB, c.Hkv, c.bs, c.D)
     fp8 = c.kv_dtype == "fp8"
-    dt = np.uint8 if fp8 else np.uint16
+    int8 = c.kv_dtype.startswith("int8")
+    dt = np.uint8 if fp8 else np.int8 if int8 else np.uint16
     k = np.zeros(shape, dtype=dt)
     v = np.zeros(shape, dtype=dt)
     ks = vs = None
     if fp8:
         ks = np.ones(shape[:3], np.float32)
         vs = np.ones(shape[:3], np.float32)
+    if int8:
+        ks = np.zeros(shape[:3] + (2,), np.float32)
+        ks[..., 0] = 0.02
+        ks[..., 1] = 3.0
+        vs = ks.copy()
     rng = np.random.Generator(np.random.PCG64(11))
     order = list(range(c.B))
     filled = set()
@@ -442,6 +482,8 @@ def oracle_sample(name, target_s):
             for arr, seed in ((k, 2), (v, 3)):
                 if fp8:
                     arr[0, blks] = rng.integers(0, 0x7E, size=(n,) + shape[2:], dtype=np.uint8)
+                elif int8:
+                    arr[0, blks] = rng.integers(-128, 128, size=(n,) + shape[2:], dtype=np.int8)
                 else:
                     arr[0, blks] = normal_bf16_bits(1000 * seed + b, (n,) + shape[2:])
             filled.add(b)
@@ -538,8 +580,9 @@ def run_ours(args, rank, world):
             "metric": "paged KV block copy GB/s (read + write bytes)" if copy else METRIC,
             "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "fp8-e4m3 kv, f16 mma, fp32 accumulate" if c.kv_dtype == "fp8"
-            else "bf16 kv, bf16 mma, fp32 accumulate",
+            "vs_baseline": None, "dtype": {"fp8": "fp8-e4m3 kv, f16 mma, fp32 accumulate",
+                                           "bf16": "bf16 kv, bf16 mma, fp32 accumulate"}.get(
+                c.kv_dtype, "int8 kv (scale, zero per page), f16 mma, fp32 accumulate"),
             "data": "synthetic (seeded N(0,1) K/V/q, seeded block permutations)",
             "config": config_of(args.workload, c, {
                 "parallelism": "replicas" if world > 1 else "single GPU",

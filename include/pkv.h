@@ -19,11 +19,21 @@
  * is the library's choice):
  *   k_cache, v_cache  [S][NB][Hkv][bs][D]   S cache slots (layer groups),
  *                     NB physical blocks, Hkv KV heads, bs tokens per block,
- *                     D head_dim.  Element type bf16 or FP8 E4M3 (1 byte).
+ *                     D head_dim.  Element type bf16, FP8 E4M3 or INT8
+ *                     (1 byte).
  *                     One (slot, block, KV head) page is a contiguous
  *                     bs*D run.
- *   k_scale, v_scale  fp32 [S][NB][Hkv]     E4M3 caches only: one scale per
- *                     page; stored value = e4m3(x / scale).
+ *   k_scale, v_scale  E4M3 caches: fp32 [S][NB][Hkv], one scale per page;
+ *                     stored value = e4m3(x / scale).
+ *                     INT8 caches: fp32 [S][NB][Hkv][2], (scale, zero point)
+ *                     per page, the zero point an integer in [-128, 127];
+ *                     stored value q = clamp(rne(x / scale) + zero, lo, 127)
+ *                     with lo = -127 when zero == 0 (symmetric) and -128
+ *                     otherwise; value read back = (q - zero) * scale.
+ *                     Alignment: 4 bytes (E4M3) or 8 bytes (INT8), else
+ *                     PKV_ERR_ALIGNMENT.
+ *                     Source: [BW] "INT8 KV cache" (symmetric or asymmetric
+ *                     quantisation with a scale and zero point).
  *   q, out            bf16 [B][Hq][D]       one query token per sequence.
  *   block_tables      int32 [B][MB]         logical block j of sequence b is
  *                     physical block block_tables[b*MB + j].
@@ -59,13 +69,13 @@ typedef enum {
   PKV_OK = 0,
   PKV_ERR_INVALID_ARG = 1,   /* null pointer, bad size, bad index argument */
   PKV_ERR_UNSUPPORTED = 2,   /* shape or dtype this build has no kernel for */
-  PKV_ERR_ALIGNMENT = 3,     /* a tensor is not 16-byte aligned */
+  PKV_ERR_ALIGNMENT = 3,     /* a tensor is not aligned as its call requires */
   PKV_ERR_CUDA = 4,          /* a CUDA runtime/driver call or launch failed */
   PKV_ERR_DEVICE_INDEX = 5,  /* the device error word was non-zero */
   PKV_ERR_WORKSPACE = 6      /* workspace missing or smaller than required */
 } pkv_status;
 
-typedef enum { PKV_KV_BF16 = 0, PKV_KV_FP8_E4M3 = 1 } pkv_kv_dtype;
+typedef enum { PKV_KV_BF16 = 0, PKV_KV_FP8_E4M3 = 1, PKV_KV_INT8 = 2 } pkv_kv_dtype;
 
 /* Bits of the device error word. */
 #define PKV_DEVERR_BLOCK_ID 0x1u     /* block table entry outside [0, NB) */
@@ -74,7 +84,7 @@ typedef enum { PKV_KV_BF16 = 0, PKV_KV_FP8_E4M3 = 1 } pkv_kv_dtype;
 #define PKV_DEVERR_TIMEOUT 0x8u      /* a bounded wait on a copy gave up */
 
 /* Shape of one paged cache (both K and V).  Supported: block_size 16 or 32;
- * head_dim 64 or 128 for bf16, 128 for E4M3. */
+ * head_dim 64 or 128 for bf16, 128 for E4M3 and INT8. */
 typedef struct {
   int32_t num_slots;    /* S: independent caches (layer groups) */
   int32_t num_blocks;   /* NB: physical blocks per slot */
@@ -88,7 +98,7 @@ typedef struct {
 typedef enum {
   PKV_MATH_AUTO = 0, /* the library picks (tensor-core mma when supported) */
   PKV_MATH_FFMA = 1, /* fp32 CUDA-core FMAs; G must be 1, 2, 4 or 8 */
-  PKV_MATH_MMA = 2   /* mma.sync tiles (bf16, or f16 for E4M3); G <= 16 */
+  PKV_MATH_MMA = 2   /* mma.sync tiles (bf16, or f16 for one-byte caches); G <= 16 */
 } pkv_decode_math;
 
 /* Tuning knobs of pkv_paged_decode; a NULL pointer or zero fields = auto. */
@@ -119,9 +129,11 @@ typedef struct {
  *                PKV_DEVERR_SLOT and skip the token.  Two tokens with the
  *                same slot in one call: unspecified which one lands.
  *   k_cache, v_cache  device, written in place.
- *   k_scale, v_scale  device fp32 [S][NB][Hkv], E4M3 caches only (may be NULL
- *                for bf16): stored byte = e4m3_rn_satfinite(float(x) / scale),
- *                IEEE binary32 division.  bf16 caches receive the bits as is.
+ *   k_scale, v_scale  device, E4M3 and INT8 caches only (may be NULL for
+ *                bf16), layouts as above: E4M3 byte =
+ *                e4m3_rn_satfinite(float(x) / scale); INT8 byte = clamp(rne(
+ *                float(x) / scale) + zero, lo, 127).  The division is IEEE
+ *                binary32.  bf16 caches receive the bits as is.
  * Returns PKV_OK after launching one kernel (none when N == 0).
  */
 pkv_status pkv_kv_append(const pkv_cache_desc* cache, int32_t slot,
@@ -177,7 +189,7 @@ pkv_status pkv_decode_describe(const pkv_cache_desc* cache, int32_t batch, int32
  *
  *   q              device bf16 [B][Hq][D].
  *   k/v_cache      device [S][NB][Hkv][bs][D] as described by `cache`.
- *   k/v_scale      device fp32 [S][NB][Hkv], E4M3 only (NULL for bf16).
+ *   k/v_scale      device, E4M3 / INT8 only (NULL for bf16), layouts as above.
  *   block_tables   device int32 [B][max_blocks_per_seq]; entries past a
  *                  sequence's last block are never read.
  *   context_lens   device int32 [B].
@@ -251,7 +263,7 @@ pkv_status pkv_paged_decode_static_workspace(const pkv_cache_desc* cache,
  * (`cache` gives bs, Hkv, D and dtype; num_slots and num_blocks are not
  * used).  For each pair i, block src_ids[i] of the source pool is copied to
  * block dst_ids[i] of the destination pool: every KV head's K and V page
- * and, for E4M3 pools, its K and V scales.
+ * and, for E4M3 and INT8 pools, its K and V page parameters.
  * Sources: [BW] "PagedAttention" (block sharing: a sequence that appends
  * into a shared block first needs its own copy) and "KV-Cache Engineering:
  * The Memory Wall of LLM Serving", "Lever 5: Offloading" and "When the cache
@@ -262,7 +274,8 @@ pkv_status pkv_paged_decode_static_workspace(const pkv_cache_desc* cache,
  *                    systems with a coherent CPU-GPU interconnect any host
  *                    memory).  Point them at the first block of a cache slot.
  *   dst_k, dst_v     destination pool, [dst_num_blocks][Hkv][bs][D], same rules.
- *   src/dst_k_scale, src/dst_v_scale  fp32 [num_blocks][Hkv], E4M3 pools only.
+ *   src/dst_k_scale, src/dst_v_scale  fp32 [num_blocks][Hkv] (E4M3) or
+ *                    [num_blocks][Hkv][2] (INT8, (scale, zero)); NULL for bf16.
  *   block_pairs      device int32 [count][2]: (src id, dst id).  Ids outside
  *                    their pool set PKV_DEVERR_BLOCK_ID and the pair is
  *                    skipped.  Two pairs with the same destination, or a

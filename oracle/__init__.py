@@ -76,6 +76,10 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.pkv_oracle_paged_decode.argtypes = [P, i32, i32, P, P, i32, P, P,
                                             i32, i32, i32, i32, i32,
                                             P, i32, P, P, i32, i32, f32, P, P, i32]
+    lib.pkv_oracle_int8_encode.restype = ctypes.c_int8
+    lib.pkv_oracle_int8_encode.argtypes = [f32, f32, f32]
+    lib.pkv_oracle_int8_decode.restype = ctypes.c_double
+    lib.pkv_oracle_int8_decode.argtypes = [ctypes.c_int8, f32, f32]
     lib.pkv_oracle_copy_blocks.restype = ctypes.c_int
     lib.pkv_oracle_copy_blocks.argtypes = [P, P, P, P, i32, P, P, P, P, i32, P, i32, i64, i32]
     lib.pkv_oracle_num_threads.restype = ctypes.c_int
@@ -96,6 +100,12 @@ def _load(lib: Optional[ctypes.CDLL] = None) -> ctypes.CDLL:
         if _lib is None:
             _lib = _bind(ctypes.CDLL(build()))
     return _lib
+
+
+def _kind(cache: np.ndarray) -> int:
+    """Element kind of a cache array: 0 bf16 bits (uint16), 1 E4M3 codes
+    (uint8), 2 INT8 codes (int8)."""
+    return {np.dtype(np.uint16): 0, np.dtype(np.uint8): 1, np.dtype(np.int8): 2}[cache.dtype]
 
 
 def _ptr(a: Optional[np.ndarray]):
@@ -161,9 +171,11 @@ def kv_append(k_new, v_new, slot_mapping, k_cache: np.ndarray, v_cache: np.ndarr
               k_scale=None, v_scale=None, slot: int = 0, lib=None) -> int:
     """In-place scatter of new tokens into ``k_cache``/``v_cache`` (numpy).
 
-    Caches are ``[S][NB][Hkv][bs][D]`` uint16 (bf16 bits) or uint8 (E4M3).
+    Caches are ``[S][NB][Hkv][bs][D]`` uint16 (bf16 bits), uint8 (E4M3) or
+    int8 (INT8; scales then [S][NB][Hkv][2] = (scale, zero)).
     Returns the oracle status (0 = ok)."""
-    fp8 = k_cache.dtype == np.uint8
+    kind = _kind(k_cache)
+    fp8 = kind != 0
     S, NB, Hkv, bs, D = k_cache.shape
     kn = _c(k_new, np.uint16)
     vn = _c(v_new, np.uint16)
@@ -173,7 +185,7 @@ def kv_append(k_new, v_new, slot_mapping, k_cache: np.ndarray, v_cache: np.ndarr
     vs = _c(v_scale, np.float32) if fp8 else None
     return int(_load(lib).pkv_oracle_kv_append(
         _ptr(kn), _ptr(vn), _ptr(sm), int(sm.shape[0]), _ptr(k_cache), _ptr(v_cache),
-        int(fp8), _ptr(ks), _ptr(vs), S, NB, Hkv, bs, D, int(slot)))
+        kind, _ptr(ks), _ptr(vs), S, NB, Hkv, bs, D, int(slot)))
 
 
 def paged_decode(q_bits, k_cache, v_cache, block_tables, context_lens, kv_group_ptr,
@@ -185,7 +197,8 @@ def paged_decode(q_bits, k_cache, v_cache, block_tables, context_lens, kv_group_
     of the result are NaN.  Raises ValueError on an oracle status != 0."""
     q = _c(q_bits, np.uint16)
     B, Hq, D = q.shape
-    fp8 = k_cache.dtype == np.uint8
+    kind = _kind(k_cache)
+    fp8 = kind != 0
     kc = _c(k_cache, k_cache.dtype)
     vc = _c(v_cache, v_cache.dtype)
     S, NB, Hkv, bs, Dc = kc.shape
@@ -198,7 +211,7 @@ def paged_decode(q_bits, k_cache, v_cache, block_tables, context_lens, kv_group_
     out = np.full((B, Hq, D), np.nan if pairs is not None else 0.0, dtype=np.float64)
     pr = None if pairs is None else np.unique(_c(pairs, np.int32).reshape(-1, 2), axis=0)
     rc = _load(lib).pkv_oracle_paged_decode(
-        _ptr(q), B, Hq, _ptr(kc), _ptr(vc), int(fp8), _ptr(ks), _ptr(vs),
+        _ptr(q), B, Hq, _ptr(kc), _ptr(vc), kind, _ptr(ks), _ptr(vs),
         S, NB, Hkv, bs, D, _ptr(bt), int(bt.shape[1]), _ptr(cl), _ptr(gp), int(gp.shape[0]),
         int(layer), float(np.float32(scale)), _ptr(out), _ptr(pr),
         0 if pr is None else int(pr.shape[0]))
@@ -216,8 +229,32 @@ def copy_blocks(src_k, src_v, dst_k, dst_v, pairs, src_k_scale=None, src_v_scale
         assert a.flags.c_contiguous
     nb_bytes = int(np.prod(src_k.shape[1:])) * src_k.dtype.itemsize
     fp8 = src_k_scale is not None
-    hkv = int(src_k.shape[1])
+    hkv = int(src_k.shape[1]) * (2 if src_k.dtype == np.int8 else 1)
     return int(_load(lib).pkv_oracle_copy_blocks(
         _ptr(src_k), _ptr(src_v), _ptr(src_k_scale), _ptr(src_v_scale), int(src_k.shape[0]),
         _ptr(dst_k), _ptr(dst_v), _ptr(dst_k_scale), _ptr(dst_v_scale), int(dst_k.shape[0]),
         _ptr(pr), int(pr.shape[0]), nb_bytes, hkv if fp8 else 0))
+
+
+def int8_encode(x: float, scale: float, zero: float = 0.0, lib=None) -> int:
+    return int(_load(lib).pkv_oracle_int8_encode(float(np.float32(x)), float(np.float32(scale)),
+                                                  float(np.float32(zero))))
+
+
+def int8_decode(q: int, scale: float, zero: float = 0.0, lib=None) -> float:
+    return float(_load(lib).pkv_oracle_int8_decode(int(q), float(np.float32(scale)), float(np.float32(zero))))
+
+
+def int8_quantize_cache(src_bits: np.ndarray, params: np.ndarray) -> np.ndarray:
+    """INT8 cache [S][NB][Hkv][bs][D] from bf16 source and [S][NB][Hkv][2]
+    (scale, zero) page parameters, through the oracle's append of every row."""
+    S, NB, Hkv, bs, D = src_bits.shape
+    out = np.zeros(src_bits.shape, dtype=np.int8)
+    other = np.zeros(src_bits.shape, dtype=np.int8)
+    tok = np.ascontiguousarray(np.transpose(src_bits, (0, 1, 3, 2, 4)))  # [S][NB][bs][Hkv][D]
+    for s_ in range(S):
+        rows = tok[s_].reshape(NB * bs, Hkv, D)
+        slots = np.arange(NB * bs, dtype=np.int64)
+        rc = kv_append(rows, rows, slots, out, other, params, params, slot=s_)
+        assert rc == 0
+    return out

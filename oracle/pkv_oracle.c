@@ -141,6 +141,29 @@ void pkv_oracle_e4m3_quantize_array(const uint16_t* x_bf16, const float* scale_p
 }
 
 /* ------------------------------------------------------------------------ */
+/* INT8 codec ("KV Cache Engineering ...", "INT8 KV cache": symmetric or     */
+/* asymmetric integer quantisation with a scale and a zero point)           */
+/* ------------------------------------------------------------------------ */
+
+/* Code of x: q = rne(x / scale) + zero, clamped to [lo, 127] with lo = -127
+ * for a symmetric page (zero == 0) and -128 otherwise; x / scale in IEEE
+ * binary32; NaN gives the zero point. */
+int8_t pkv_oracle_int8_encode(float x, float scale, float zero) {
+  volatile float t = x / scale;
+  if (isnan(t)) return (int8_t)zero;
+  double q = nearbyint((double)t) + (double)zero; /* default rounding: to nearest, ties to even */
+  double lo = (zero == 0.0f) ? -127.0 : -128.0;
+  if (q < lo) q = lo;
+  if (q > 127.0) q = 127.0;
+  return (int8_t)q;
+}
+
+/* Value of a code: (q - zero) * scale. */
+double pkv_oracle_int8_decode(int8_t q, float scale, float zero) {
+  return ((double)q - (double)zero) * (double)scale;
+}
+
+/* ------------------------------------------------------------------------ */
 /* KV append: write each new token's K and V into its physical slot         */
 /* ------------------------------------------------------------------------ */
 
@@ -153,7 +176,7 @@ void pkv_oracle_e4m3_quantize_array(const uint16_t* x_bf16, const float* scale_p
  */
 int pkv_oracle_kv_append(const uint16_t* k_new, const uint16_t* v_new,
                          const int64_t* slot_mapping, int32_t N,
-                         void* k_cache, void* v_cache, int32_t fp8,
+                         void* k_cache, void* v_cache, int32_t kind /* 0 bf16, 1 E4M3, 2 INT8 */,
                          const float* k_scale, const float* v_scale,
                          int32_t S, int32_t NB, int32_t Hkv, int32_t bs, int32_t D,
                          int32_t slot) {
@@ -170,9 +193,17 @@ int pkv_oracle_kv_append(const uint16_t* k_new, const uint16_t* v_new,
       int64_t src = ((int64_t)i * Hkv + h) * D;
       int64_t page = (((int64_t)slot * NB + blk) * Hkv + h);
       int64_t dst = (page * bs + off) * D;
-      if (!fp8) {
+      if (kind == 0) {
         memcpy((uint16_t*)k_cache + dst, k_new + src, (size_t)D * 2);
         memcpy((uint16_t*)v_cache + dst, v_new + src, (size_t)D * 2);
+      } else if (kind == 2) {
+        /* scales are (scale, zero) pairs per page */
+        float ks = k_scale[2 * page], kz = k_scale[2 * page + 1];
+        float vs = v_scale[2 * page], vz = v_scale[2 * page + 1];
+        for (int32_t d = 0; d < D; ++d) {
+          ((int8_t*)k_cache)[dst + d] = pkv_oracle_int8_encode(bf16_bits_to_float(k_new[src + d]), ks, kz);
+          ((int8_t*)v_cache)[dst + d] = pkv_oracle_int8_encode(bf16_bits_to_float(v_new[src + d]), vs, vz);
+        }
       } else {
         float ks = k_scale[page], vs = v_scale[page];
         for (int32_t d = 0; d < D; ++d) {
@@ -191,19 +222,21 @@ int pkv_oracle_kv_append(const uint16_t* k_new, const uint16_t* v_new,
 /* Paged decode attention                                                   */
 /* ------------------------------------------------------------------------ */
 
-/* Value of cache element (slot, blk, g, row, d), dequantised for E4M3. */
-static double cache_value(const void* cache, int32_t fp8, const float* scales,
+/* Value of cache element (slot, blk, g, row, d), dequantised for E4M3
+ * (code * scale) and INT8 ((code - zero) * scale). */
+static double cache_value(const void* cache, int32_t kind, const float* scales,
                           int64_t page, int32_t bs, int32_t D, int32_t row, int32_t d) {
   int64_t idx = (page * bs + row) * D + d;
-  if (!fp8) return bf16_bits_to_double(((const uint16_t*)cache)[idx]);
+  if (kind == 0) return bf16_bits_to_double(((const uint16_t*)cache)[idx]);
+  if (kind == 2) return pkv_oracle_int8_decode(((const int8_t*)cache)[idx], scales[2 * page], scales[2 * page + 1]);
   return pkv_oracle_e4m3_decode(((const uint8_t*)cache)[idx]) * (double)scales[page];
 }
 
 /*
  * One decode step for one layer.
  *   q            bf16 bits [B][Hq][D]
- *   k/v_cache    [S][NB][Hkv][bs][D], bf16 bits or E4M3 codes (fp8 != 0)
- *   k/v_scale    fp32 [S][NB][Hkv] (E4M3 only)
+ *   k/v_cache    [S][NB][Hkv][bs][D], bf16 bits, E4M3 codes or INT8 codes
+ *   k/v_scale    fp32 [S][NB][Hkv] (E4M3) or [S][NB][Hkv][2] (INT8: scale, zero)
  *   block_tables int32 [B][MB]; context_lens int32 [B]
  *   kv_group_ptr int32 [L]: cache slot read by layer l (shared-with pointer)
  *   out          double [B][Hq][D]
@@ -217,7 +250,8 @@ static double cache_value(const void* cache, int32_t fp8, const float* scales,
  * read or a context length is out of range (nothing is read out of bounds).
  */
 int pkv_oracle_paged_decode(const uint16_t* q, int32_t B, int32_t Hq,
-                            const void* k_cache, const void* v_cache, int32_t fp8,
+                            const void* k_cache, const void* v_cache,
+                            int32_t fp8 /* element kind: 0 bf16, 1 E4M3, 2 INT8 */,
                             const float* k_scale, const float* v_scale,
                             int32_t S, int32_t NB, int32_t Hkv, int32_t bs, int32_t D,
                             const int32_t* block_tables, int32_t MB,

@@ -30,7 +30,7 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libpkv.so")
 PKV_OK = 0
 STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "alignment", 4: "cuda",
                 5: "device index error", 6: "workspace"}
-KV_BF16, KV_FP8_E4M3 = 0, 1
+KV_BF16, KV_FP8_E4M3, KV_INT8 = 0, 1, 2
 MATH_AUTO, MATH_FFMA, MATH_MMA = 0, 1, 2
 DEVERR_BLOCK_ID, DEVERR_SLOT, DEVERR_CONTEXT_LEN, DEVERR_TIMEOUT = 1, 2, 4, 8
 
@@ -132,6 +132,16 @@ def _need_cuda(name: str, t: torch.Tensor, dtype=None):
         raise PkvError(1, f"{name} must be {dtype}, got {t.dtype}")
 
 
+def _need_page_params(desc: CacheDesc, t: Optional[torch.Tensor], name: str):
+    """E4M3: fp32 [S][NB][Hkv]; INT8: fp32 [S][NB][Hkv][2] (scale, zero)."""
+    _need_cuda(name, t, torch.float32)
+    want = (desc.num_slots, desc.num_blocks, desc.num_kv_heads)
+    if desc.dtype == KV_INT8:
+        want = want + (2,)
+    if tuple(t.shape) != want:
+        raise PkvError(1, f"{name} must have shape {list(want)}")
+
+
 def cache_desc(k_cache: torch.Tensor) -> CacheDesc:
     """Descriptor of a [S][NB][Hkv][bs][D] cache tensor (bf16, or uint8 = E4M3)."""
     if k_cache.dim() != 5:
@@ -140,8 +150,10 @@ def cache_desc(k_cache: torch.Tensor) -> CacheDesc:
         dt = KV_BF16
     elif k_cache.dtype == torch.uint8:
         dt = KV_FP8_E4M3
+    elif k_cache.dtype == torch.int8:
+        dt = KV_INT8
     else:
-        raise PkvError(1, f"cache dtype {k_cache.dtype} (bfloat16 or uint8 E4M3 codes)")
+        raise PkvError(1, f"cache dtype {k_cache.dtype} (bfloat16, uint8 E4M3 codes or int8)")
     S, NB, Hkv, bs, D = (int(x) for x in k_cache.shape)
     return CacheDesc(S, NB, bs, Hkv, D, dt)
 
@@ -161,9 +173,9 @@ def kv_append(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
     N = int(slot_mapping.shape[0])
     if k.shape != (N, desc.num_kv_heads, desc.head_dim) or v.shape != k.shape:
         raise PkvError(1, f"k/v must be [{N}][{desc.num_kv_heads}][{desc.head_dim}]")
-    if desc.dtype == KV_FP8_E4M3:
-        _need_cuda("k_scale", k_scale, torch.float32)
-        _need_cuda("v_scale", v_scale, torch.float32)
+    if desc.dtype != KV_BF16:
+        _need_page_params(desc, k_scale, "k_scale")
+        _need_page_params(desc, v_scale, "v_scale")
     _check(load().pkv_kv_append(ctypes.byref(desc), int(slot), _ptr(k), _ptr(v), _ptr(slot_mapping),
                                 N, _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
                                 _stream_handle(stream)))
@@ -230,9 +242,9 @@ def paged_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
     if out is None:
         out = torch.empty_like(q)
     _need_cuda("out", out, torch.bfloat16)
-    if desc.dtype == KV_FP8_E4M3:
-        _need_cuda("k_scale", k_scale, torch.float32)
-        _need_cuda("v_scale", v_scale, torch.float32)
+    if desc.dtype != KV_BF16:
+        _need_page_params(desc, k_scale, "k_scale")
+        _need_page_params(desc, v_scale, "v_scale")
     if workspace is None:
         workspace = new_decode_workspace(k_cache, B, Hq, MB, opts)
     gp = (ctypes.c_int32 * len(kv_group_ptr))(*[int(x) for x in kv_group_ptr])

@@ -1,5 +1,5 @@
-// Block copy: whole physical blocks (all KV heads, K and V, and the E4M3
-// scales) from one block pool to another, by (source id, destination id)
+// Block copy: whole physical blocks (all KV heads, K and V, and the
+// page parameters of one-byte caches) from one block pool to another, by (source id, destination id)
 // pairs.  Used for copy-on-write of a shared block before a sequence appends
 // into it, and for moving a sequence's blocks between HBM and host memory.
 //

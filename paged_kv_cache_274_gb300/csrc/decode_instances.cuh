@@ -5,20 +5,20 @@
 
 namespace pkv {
 
-template <int D, int BS, bool FP8>
+template <int D, int BS, bool FP8, bool I8 = false>
 const void* decode_kernel_for(int math, int gt) {
   if (math == PKV_MATH_MMA) {
     // GT = 8: at most 8 heads per group (half tiles); 16: up to 16
-    if (gt <= 8) return reinterpret_cast<const void*>(&paged_decode_kernel<D, BS, FP8, PKV_MATH_MMA, 8>);
-    if (gt <= 16) return reinterpret_cast<const void*>(&paged_decode_kernel<D, BS, FP8, PKV_MATH_MMA, 16>);
+    if (gt <= 8) return reinterpret_cast<const void*>(&paged_decode_kernel<D, BS, FP8, PKV_MATH_MMA, 8, I8>);
+    if (gt <= 16) return reinterpret_cast<const void*>(&paged_decode_kernel<D, BS, FP8, PKV_MATH_MMA, 16, I8>);
     return nullptr;
   }
   if (math != PKV_MATH_FFMA) return nullptr;
   switch (gt) {
-    case 1: return reinterpret_cast<const void*>(&paged_decode_kernel<D, BS, FP8, PKV_MATH_FFMA, 1>);
-    case 2: return reinterpret_cast<const void*>(&paged_decode_kernel<D, BS, FP8, PKV_MATH_FFMA, 2>);
-    case 4: return reinterpret_cast<const void*>(&paged_decode_kernel<D, BS, FP8, PKV_MATH_FFMA, 4>);
-    case 8: return reinterpret_cast<const void*>(&paged_decode_kernel<D, BS, FP8, PKV_MATH_FFMA, 8>);
+    case 1: return reinterpret_cast<const void*>(&paged_decode_kernel<D, BS, FP8, PKV_MATH_FFMA, 1, I8>);
+    case 2: return reinterpret_cast<const void*>(&paged_decode_kernel<D, BS, FP8, PKV_MATH_FFMA, 2, I8>);
+    case 4: return reinterpret_cast<const void*>(&paged_decode_kernel<D, BS, FP8, PKV_MATH_FFMA, 4, I8>);
+    case 8: return reinterpret_cast<const void*>(&paged_decode_kernel<D, BS, FP8, PKV_MATH_FFMA, 8, I8>);
     default: return nullptr;
   }
 }

@@ -6,9 +6,12 @@
 // later steps) and "Continuous Batching" (a growing sequence takes a free
 // block when it needs one; the caller's slot mapping says which).
 //
-// One thread moves one 16-byte chunk: 8 bf16 values, or (E4M3 caches) 8
-// values quantised to 8 bytes with e4m3_rn_satfinite(float(x) / scale),
-// the division in IEEE binary32 and the page's scale.
+// One thread moves one 16-byte chunk: 8 bf16 values, or 8 values quantised
+// to 8 bytes with the page's parameters, the division in IEEE binary32:
+//   E4M3: e4m3_rn_satfinite(float(x) / scale)
+//   INT8: clamp(rne(float(x) / scale) + zero, lo, 127), lo = -127 for a
+//         symmetric page (zero == 0) else -128; NaN stores the zero point
+//         ([BW] "INT8 KV cache").
 #include <algorithm>
 
 #include "pkv_device.cuh"
@@ -16,7 +19,15 @@
 
 namespace pkv {
 
-template <bool FP8>
+__device__ __forceinline__ uint32_t int8_code(float x, float scale, float zero) {
+  const float t = __fdiv_rn(x, scale);
+  if (isnan(t)) return static_cast<uint32_t>(static_cast<int>(zero)) & 0xffu;
+  const float lo = (zero == 0.f) ? -127.f : -128.f;
+  const float q = fminf(fmaxf(rintf(t) + zero, lo), 127.f);
+  return static_cast<uint32_t>(static_cast<int>(q)) & 0xffu;
+}
+
+template <int KV>  // pkv_kv_dtype
 __global__ void __launch_bounds__(256)
     kv_append_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
                      const int64_t* __restrict__ slot_mapping, int N, int Hkv, int D, int bs,
@@ -46,8 +57,19 @@ __global__ void __launch_bounds__(256)
     const int64_t page = blk * Hkv + h;
     const int64_t dst_elem = (page * bs + off) * D + 8 * c;
     const uint4 w = __ldg((is_v ? v : k) + th * chunks_per_row + c);
-    if (!FP8) {
+    if constexpr (KV == PKV_KV_BF16) {
       *reinterpret_cast<uint4*>((is_v ? vc : kc) + 2 * dst_elem) = w;
+    } else if constexpr (KV == PKV_KV_INT8) {
+      const float2 sz = __ldg(reinterpret_cast<const float2*>(is_v ? vs : ks) + page);
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+      uint32_t outw[2] = {0u, 0u};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t lo = int8_code(bf16lo_to_f32(ws[j]), sz.x, sz.y);
+        const uint32_t hi = int8_code(bf16hi_to_f32(ws[j]), sz.x, sz.y);
+        outw[j >> 1] |= (lo | (hi << 8)) << (16 * (j & 1));
+      }
+      *reinterpret_cast<uint2*>((is_v ? vc : kc) + dst_elem) = make_uint2(outw[0], outw[1]);
     } else {
       const float scale = __ldg((is_v ? vs : ks) + page);
       const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
@@ -70,7 +92,7 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-cudaError_t launch_kv_append(int kv_fp8, const void* k, const void* v,
+cudaError_t launch_kv_append(int kv_dtype, const void* k, const void* v,
                              const int64_t* slot_mapping, int N, int Hkv, int D, int bs,
                              int64_t nslots, void* k_base, void* v_base, const float* ks_base,
                              const float* vs_base, unsigned* err, cudaStream_t stream) {
@@ -86,7 +108,9 @@ cudaError_t launch_kv_append(int kv_fp8, const void* k, const void* v,
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  auto kernel = kv_fp8 ? kv_append_kernel<true> : kv_append_kernel<false>;
+  auto kernel = kv_dtype == PKV_KV_INT8        ? kv_append_kernel<PKV_KV_INT8>
+                : kv_dtype == PKV_KV_FP8_E4M3 ? kv_append_kernel<PKV_KV_FP8_E4M3>
+                                              : kv_append_kernel<PKV_KV_BF16>;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<const uint4*>(k), static_cast<const uint4*>(v),
                             slot_mapping, N, Hkv, D, bs, nslots, static_cast<uint8_t*>(k_base),
                             static_cast<uint8_t*>(v_base), ks_base, vs_base, err);

@@ -25,6 +25,7 @@ namespace pkv {
 const void* decode_kernel_bf16_d64(int bs, int math, int gt);
 const void* decode_kernel_bf16_d128(int bs, int math, int gt);
 const void* decode_kernel_fp8_d128(int bs, int math, int gt);
+const void* decode_kernel_int8_d128(int bs, int math, int gt);
 
 // ---------------------------------------------------------------------------
 // planner: one CTA validates context lengths, counts each sequence's
@@ -210,9 +211,10 @@ size_t decode_smem_bytes(int kv_fp8, int D, int bs, int warps, int stages) {
                   : decode_smem_layout_bytes<128, 32, false>(warps, stages);
 }
 
-static const void* pick_kernel(int kv_fp8, int D, int bs, int math, int G) {
+static const void* pick_kernel(int kv_dtype, int D, int bs, int math, int G) {
   const int gt = G;
-  if (kv_fp8) return decode_kernel_fp8_d128(bs, math, gt);
+  if (kv_dtype == PKV_KV_INT8) return decode_kernel_int8_d128(bs, math, gt);
+  if (kv_dtype == PKV_KV_FP8_E4M3) return decode_kernel_fp8_d128(bs, math, gt);
   if (D == 64) return decode_kernel_bf16_d64(bs, math, gt);
   return decode_kernel_bf16_d128(bs, math, gt);
 }
@@ -266,7 +268,7 @@ static cudaError_t ctas_per_sm(const void* fn, int threads, size_t smem, int* ou
 }
 
 int decode_ctas_per_sm(const DecodeLaunch& L, size_t smem) {
-  const void* fn = pick_kernel(L.kv_fp8, L.D, L.bs, L.math, L.G);
+  const void* fn = pick_kernel(L.kv_dtype, L.D, L.bs, L.math, L.G);
   int n = 0;
   if (fn == nullptr || ctas_per_sm(fn, L.warps * 32, smem, &n) != cudaSuccess) return 0;
   return n;
@@ -274,7 +276,7 @@ int decode_ctas_per_sm(const DecodeLaunch& L, size_t smem) {
 
 cudaError_t launch_decode(const DecodeLaunch& L, int* launched) {
   *launched = 0;
-  const void* fn = pick_kernel(L.kv_fp8, L.D, L.bs, L.math, L.G);
+  const void* fn = pick_kernel(L.kv_dtype, L.D, L.bs, L.math, L.G);
   if (fn == nullptr) return cudaErrorInvalidDeviceFunction;
   const size_t smem = decode_smem_bytes(L.kv_fp8, L.D, L.bs, L.warps, L.stages);
   int per_sm = 0;

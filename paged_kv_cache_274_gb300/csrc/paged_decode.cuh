@@ -5,7 +5,8 @@
 // and Why" (the new query attends over every cached K,V), "PagedAttention"
 // (the kernel reaches physical blocks through the per-sequence block table;
 // only the last block is partly filled), "Attention Variants" (GQA: a group
-// of query heads shares one K/V head), "FP8 KV cache" (dequantise on read),
+// of query heads shares one K/V head), "FP8 KV cache" and "INT8 KV cache"
+// (dequantise on read),
 // "Two Costs: Capacity and Bandwidth" (every step streams the whole cache,
 // so the kernel is bound by HBM bandwidth).
 //
@@ -160,13 +161,21 @@ __device__ __forceinline__ int qk_token(int nt, int r) {
   return 16 * (nt >> 1) + 4 * (r >> 1) + 2 * (nt & 1) + (r & 1);
 }
 
+// Four one-byte codes -> two f16x2 words (exact): E4M3 by hardware
+// conversion, INT8 as code - zero (zc from int8_zero_const).
+template <bool I8>
+__device__ __forceinline__ void bytes4_to_f16x2x2(uint32_t x, uint32_t zc, uint32_t& lo, uint32_t& hi) {
+  if constexpr (I8) int8x4_to_f16x2x2(x, zc, lo, hi); else e4m3x4_to_f16x2x2(x, lo, hi);
+}
+
 // One page (BS tokens) of the online softmax with tensor-core tiles.
 // `valid` = tokens of the page that belong to the sequence (0..BS); `sl` =
 // softmax scale * log2(e) (* the page's K scale for E4M3); `vscale` = the
 // page's V scale (E4M3 only).
-template <int D, int BS, bool FP8, bool HI>
+template <int D, int BS, bool FP8, bool HI, bool I8>
 __device__ __forceinline__ void mma_page(MmaState<D, BS, FP8, HI>& st, uint8_t* stage, int valid,
-                                         float sl, float vscale, int lane) {
+                                         float sl, float vscale, uint32_t kzc, uint32_t vzc,
+                                         int lane) {
   using Geo = PageGeom<D, BS, FP8>;
   constexpr int kR = HI ? 2 : 1;
   constexpr int kC = 2 * kR;
@@ -199,7 +208,7 @@ __device__ __forceinline__ void mma_page(MmaState<D, BS, FP8, HI>& st, uint8_t* 
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           uint32_t b0, b1;
-          e4m3x4_to_f16x2x2(r[i], b0, b1);
+          bytes4_to_f16x2x2<I8>(r[i], kzc, b0, b1);
           mma_rows<FP8, HI>(s[nt], st.qa[c4 * 4 + i], b0, b1);
         }
       }
@@ -326,7 +335,7 @@ __device__ __forceinline__ void mma_page(MmaState<D, BS, FP8, HI>& st, uint8_t* 
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           uint32_t b0, b1;
-          e4m3x4_to_f16x2x2(q[j], b0, b1);
+          bytes4_to_f16x2x2<I8>(q[j], vzc, b0, b1);
           mma_rows<FP8, HI>(t[j], pa[ks], b0, b1);
         }
       }
@@ -410,8 +419,9 @@ __device__ __forceinline__ void ffma_load_q(FfmaState<D, BS, FP8, GT>& st,
 }
 
 // D/8 consecutive K values of token row `row`, starting at d = dl * D/8.
-template <int D, int BS, bool FP8>
-__device__ __forceinline__ void ffma_load_k(const uint8_t* kp, int row, int dl, float (&kf)[D / 8]) {
+template <int D, int BS, bool FP8, bool I8>
+__device__ __forceinline__ void ffma_load_k(const uint8_t* kp, int row, int dl, uint32_t zc,
+                                            float (&kf)[D / 8]) {
   using Geo = PageGeom<D, BS, FP8>;
   if constexpr (!FP8) {
 #pragma unroll
@@ -434,7 +444,7 @@ __device__ __forceinline__ void ffma_load_k(const uint8_t* kp, int row, int dl, 
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       uint32_t h01, h23;
-      e4m3x4_to_f16x2x2(ws[i], h01, h23);
+      bytes4_to_f16x2x2<I8>(ws[i], zc, h01, h23);
       const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
       const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
       kf[4 * i] = f01.x;
@@ -446,8 +456,9 @@ __device__ __forceinline__ void ffma_load_k(const uint8_t* kp, int row, int dl, 
 }
 
 // D/32 consecutive V values of token row `row`, starting at d = lane * D/32.
-template <int D, int BS, bool FP8>
-__device__ __forceinline__ void ffma_load_v(const uint8_t* vp, int row, int lane, float (&vf)[D / 32]) {
+template <int D, int BS, bool FP8, bool I8>
+__device__ __forceinline__ void ffma_load_v(const uint8_t* vp, int row, int lane, uint32_t zc,
+                                            float (&vf)[D / 32]) {
   using Geo = PageGeom<D, BS, FP8>;
   const int d0 = lane * (D / 32);
   if constexpr (!FP8) {
@@ -468,7 +479,7 @@ __device__ __forceinline__ void ffma_load_v(const uint8_t* vp, int row, int lane
     static_assert(D / 32 == 4, "E4M3 pages need head_dim 128");
     const uint32_t w = *reinterpret_cast<const uint32_t*>(vp + swz128(row, d0 >> 4) + (d0 & 15));
     uint32_t h01, h23;
-    e4m3x4_to_f16x2x2(w, h01, h23);
+    bytes4_to_f16x2x2<I8>(w, zc, h01, h23);
     const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
     const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
     vf[0] = f01.x;
@@ -478,9 +489,10 @@ __device__ __forceinline__ void ffma_load_v(const uint8_t* vp, int row, int lane
   }
 }
 
-template <int D, int BS, bool FP8, int GT>
+template <int D, int BS, bool FP8, int GT, bool I8>
 __device__ __forceinline__ void ffma_page(FfmaState<D, BS, FP8, GT>& st, uint8_t* stage, int valid,
-                                          float sl, float vscale, float* pbuf, int lane) {
+                                          float sl, float vscale, uint32_t kzc, uint32_t vzc,
+                                          float* pbuf, int lane) {
   using Geo = PageGeom<D, BS, FP8>;
   const int tl = lane >> 3, dl = lane & 7;
   const uint8_t* kp = stage;
@@ -490,7 +502,7 @@ __device__ __forceinline__ void ffma_page(FfmaState<D, BS, FP8, GT>& st, uint8_t
   for (int i = 0; i < BS / 4; ++i) {
     const int row = 4 * i + tl;
     float kf[D / 8];
-    ffma_load_k<D, BS, FP8>(kp, row, dl, kf);
+    ffma_load_k<D, BS, FP8, I8>(kp, row, dl, kzc, kf);
 #pragma unroll
     for (int h = 0; h < GT; ++h) {
       float acc = 0.f;
@@ -537,7 +549,7 @@ __device__ __forceinline__ void ffma_page(FfmaState<D, BS, FP8, GT>& st, uint8_t
 #pragma unroll 4
   for (int t = 0; t < valid; ++t) {
     float vf[D / 32];
-    ffma_load_v<D, BS, FP8>(vp, t, lane, vf);
+    ffma_load_v<D, BS, FP8, I8>(vp, t, lane, vzc, vf);
     float pv[GT];
 #pragma unroll
     for (int h = 0; h < GT; ++h) pv[h] = pbuf[t * GT + h];
@@ -635,7 +647,7 @@ __device__ __forceinline__ void arrive_and_merge(const DecodeParams& p, int b, i
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-template <int D, int BS, bool FP8, int MATH, int GT>
+template <int D, int BS, bool FP8, int MATH, int GT, bool I8 = false>
 __global__ void __launch_bounds__(256, 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
@@ -704,8 +716,10 @@ __global__ void __launch_bounds__(256, 1)
     }
     const uint32_t badm0 = __ballot_sync(kFull, bad0), badm1 = __ballot_sync(kFull, bad1);
     if (lane == 0 && (badm0 | badm1)) atomicOr(p.err, PKV_DEVERR_BLOCK_ID);
+    // per-page dequantisation parameters (E4M3: scale; INT8: scale, zero)
     float ks0 = 1.f, ks1 = 1.f, vs0 = 1.f, vs1 = 1.f;
-    if (FP8) {
+    float kz0 = 0.f, kz1 = 0.f, vz0 = 0.f, vz1 = 0.f;
+    if (FP8 && !I8) {
       if (lane < npages) {
         ks0 = __ldg(p.k_scale + static_cast<size_t>(e0) * p.Hkv + kvh);
         vs0 = __ldg(p.v_scale + static_cast<size_t>(e0) * p.Hkv + kvh);
@@ -713,6 +727,19 @@ __global__ void __launch_bounds__(256, 1)
       if (lane + 32 < npages) {
         ks1 = __ldg(p.k_scale + static_cast<size_t>(e1) * p.Hkv + kvh);
         vs1 = __ldg(p.v_scale + static_cast<size_t>(e1) * p.Hkv + kvh);
+      }
+    } else if (I8) {
+      const float2* kp2 = reinterpret_cast<const float2*>(p.k_scale);
+      const float2* vp2 = reinterpret_cast<const float2*>(p.v_scale);
+      if (lane < npages) {
+        const float2 a = __ldg(kp2 + static_cast<size_t>(e0) * p.Hkv + kvh);
+        const float2 c = __ldg(vp2 + static_cast<size_t>(e0) * p.Hkv + kvh);
+        ks0 = a.x; kz0 = a.y; vs0 = c.x; vz0 = c.y;
+      }
+      if (lane + 32 < npages) {
+        const float2 a = __ldg(kp2 + static_cast<size_t>(e1) * p.Hkv + kvh);
+        const float2 c = __ldg(vp2 + static_cast<size_t>(e1) * p.Hkv + kvh);
+        ks1 = a.x; kz1 = a.y; vs1 = c.x; vz1 = c.y;
       }
     }
 
@@ -752,12 +779,17 @@ __global__ void __launch_bounds__(256, 1)
         const bool bad = (j < 32) ? ((badm0 >> (j & 31)) & 1u) : ((badm1 >> (j & 31)) & 1u);
         const int valid = bad ? 0 : min(BS, t1 - (t0 + j * BS));
         float ksc = 1.f, vsc = 1.f;
+        uint32_t kzc = 0u, vzc = 0u;
         if (FP8) {
           ksc = (j < 32) ? __shfl_sync(kFull, ks0, j & 31) : __shfl_sync(kFull, ks1, j & 31);
           vsc = (j < 32) ? __shfl_sync(kFull, vs0, j & 31) : __shfl_sync(kFull, vs1, j & 31);
         }
-        mma_page<D, BS, FP8, kHi>(st, ring + static_cast<size_t>(s) * Geo::kStageBytes, valid,
-                                  p.scale_log2 * ksc, vsc, lane);
+        if (I8) {
+          kzc = int8_zero_const((j < 32) ? __shfl_sync(kFull, kz0, j & 31) : __shfl_sync(kFull, kz1, j & 31));
+          vzc = int8_zero_const((j < 32) ? __shfl_sync(kFull, vz0, j & 31) : __shfl_sync(kFull, vz1, j & 31));
+        }
+        mma_page<D, BS, FP8, kHi, I8>(st, ring + static_cast<size_t>(s) * Geo::kStageBytes, valid,
+                                      p.scale_log2 * ksc, vsc, kzc, vzc, lane);
         fence_proxy_async_smem();  // this lane's reads of the stage precede the refill
         __syncwarp();
         if (j + R < npages) { issue(j + R, it + R); ++issued; }
@@ -778,12 +810,17 @@ __global__ void __launch_bounds__(256, 1)
         const bool bad = (j < 32) ? ((badm0 >> (j & 31)) & 1u) : ((badm1 >> (j & 31)) & 1u);
         const int valid = bad ? 0 : min(BS, t1 - (t0 + j * BS));
         float ksc = 1.f, vsc = 1.f;
+        uint32_t kzc = 0u, vzc = 0u;
         if (FP8) {
           ksc = (j < 32) ? __shfl_sync(kFull, ks0, j & 31) : __shfl_sync(kFull, ks1, j & 31);
           vsc = (j < 32) ? __shfl_sync(kFull, vs0, j & 31) : __shfl_sync(kFull, vs1, j & 31);
         }
-        ffma_page<D, BS, FP8, (GT > 0 ? GT : 1)>(st, ring + static_cast<size_t>(s) * Geo::kStageBytes,
-                                                 valid, p.scale_log2 * ksc, vsc, pbuf, lane);
+        if (I8) {
+          kzc = int8_zero_const((j < 32) ? __shfl_sync(kFull, kz0, j & 31) : __shfl_sync(kFull, kz1, j & 31));
+          vzc = int8_zero_const((j < 32) ? __shfl_sync(kFull, vz0, j & 31) : __shfl_sync(kFull, vz1, j & 31));
+        }
+        ffma_page<D, BS, FP8, (GT > 0 ? GT : 1), I8>(st, ring + static_cast<size_t>(s) * Geo::kStageBytes,
+                                                     valid, p.scale_log2 * ksc, vsc, kzc, vzc, pbuf, lane);
         fence_proxy_async_smem();  // this lane's reads of the stage precede the refill
         __syncwarp();
         if (j + R < npages) { issue(j + R, it + R); ++issued; }

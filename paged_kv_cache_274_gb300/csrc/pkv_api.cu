@@ -99,6 +99,12 @@ pkv_status tensor_map_encoder(PFN_cuTensorMapEncodeTiled_v12000* fn) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// page parameters: E4M3 scales are read as floats, INT8 (scale, zero) pairs as float2
+bool scales_aligned(int dtype, const void* a, const void* b) {
+  const uintptr_t m = dtype == PKV_KV_INT8 ? 7u : 3u;
+  return ((reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(b)) & m) == 0;
+}
+
 bool env_flag(const char* name) {
   const char* v = std::getenv(name);
   return v != nullptr && v[0] != '\0' && std::strcmp(v, "0") != 0;
@@ -114,14 +120,14 @@ pkv_status check_cache_desc(const pkv_cache_desc* c) {
   if (c == nullptr) return fail(PKV_ERR_INVALID_ARG, "cache descriptor is NULL");
   if (c->num_slots < 1 || c->num_blocks < 1 || c->num_kv_heads < 1)
     return fail(PKV_ERR_INVALID_ARG, "cache: slots, blocks and KV heads must be >= 1");
-  if (c->dtype != PKV_KV_BF16 && c->dtype != PKV_KV_FP8_E4M3)
+  if (c->dtype != PKV_KV_BF16 && c->dtype != PKV_KV_FP8_E4M3 && c->dtype != PKV_KV_INT8)
     return fail(PKV_ERR_INVALID_ARG, "cache: unknown dtype %d", c->dtype);
   if (c->block_size != 16 && c->block_size != 32)
     return fail(PKV_ERR_UNSUPPORTED, "cache: block_size %d (supported: 16, 32)", c->block_size);
   if (c->dtype == PKV_KV_BF16 && c->head_dim != 64 && c->head_dim != 128)
     return fail(PKV_ERR_UNSUPPORTED, "cache: head_dim %d (bf16 supports 64, 128)", c->head_dim);
-  if (c->dtype == PKV_KV_FP8_E4M3 && c->head_dim != 128)
-    return fail(PKV_ERR_UNSUPPORTED, "cache: head_dim %d (E4M3 supports 128)", c->head_dim);
+  if (c->dtype != PKV_KV_BF16 && c->head_dim != 128)
+    return fail(PKV_ERR_UNSUPPORTED, "cache: head_dim %d (E4M3 and INT8 support 128)", c->head_dim);
   const long long rows = static_cast<long long>(c->num_slots) * c->num_blocks * c->num_kv_heads *
                          c->block_size;
   if (rows >= (1LL << 31)) return fail(PKV_ERR_UNSUPPORTED, "cache has %lld rows (limit 2^31)", rows);
@@ -132,7 +138,7 @@ pkv_status encode_cache_map(CUtensorMap* map, const void* base, const pkv_cache_
   PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
   pkv_status st = tensor_map_encoder(&enc);
   if (st != PKV_OK) return st;
-  const bool fp8 = c->dtype == PKV_KV_FP8_E4M3;
+  const bool fp8 = c->dtype != PKV_KV_BF16;  // one-byte elements
   const int elem = fp8 ? 1 : 2;
   const cuuint64_t rows = static_cast<cuuint64_t>(c->num_slots) * c->num_blocks * c->num_kv_heads *
                           c->block_size;
@@ -193,10 +199,12 @@ pkv_status pkv_kv_append(const pkv_cache_desc* cache, int32_t slot, const void* 
     return fail(PKV_ERR_INVALID_ARG, "slot %d outside [0, %d)", slot, cache->num_slots);
   if (num_tokens < 0) return fail(PKV_ERR_INVALID_ARG, "num_tokens %d < 0", num_tokens);
   if (num_tokens == 0) return PKV_OK;
-  const bool fp8 = cache->dtype == PKV_KV_FP8_E4M3;
+  const bool fp8 = cache->dtype != PKV_KV_BF16;  // one-byte elements (E4M3 or INT8)
   if (!k || !v || !slot_mapping || !k_cache || !v_cache)
     return fail(PKV_ERR_INVALID_ARG, "NULL tensor pointer");
-  if (fp8 && (!k_scale || !v_scale)) return fail(PKV_ERR_INVALID_ARG, "E4M3 cache needs k_scale and v_scale");
+  if (fp8 && (!k_scale || !v_scale)) return fail(PKV_ERR_INVALID_ARG, "E4M3 and INT8 caches need k_scale and v_scale");
+  if (fp8 && !scales_aligned(cache->dtype, k_scale, v_scale))
+    return fail(PKV_ERR_ALIGNMENT, "k_scale and v_scale must be 4-byte (E4M3) or 8-byte (INT8) aligned");
   if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache))
     return fail(PKV_ERR_ALIGNMENT, "k, v and caches must be 16-byte aligned");
   if ((reinterpret_cast<uintptr_t>(slot_mapping) & 7u) != 0)
@@ -224,8 +232,9 @@ pkv_status pkv_kv_append(const pkv_cache_desc* cache, int32_t slot, const void* 
   const size_t elem = fp8 ? 1 : 2;
   uint8_t* kb = static_cast<uint8_t*>(k_cache) + static_cast<size_t>(slot) * slot_elems * elem;
   uint8_t* vb = static_cast<uint8_t*>(v_cache) + static_cast<size_t>(slot) * slot_elems * elem;
-  const size_t scale_off = static_cast<size_t>(slot) * cache->num_blocks * cache->num_kv_heads;
-  cudaError_t e = pkv::launch_kv_append(fp8, k, v, slot_mapping, num_tokens, cache->num_kv_heads,
+  const size_t scale_off = static_cast<size_t>(slot) * cache->num_blocks * cache->num_kv_heads *
+                           (cache->dtype == PKV_KV_INT8 ? 2 : 1);
+  cudaError_t e = pkv::launch_kv_append(cache->dtype, k, v, slot_mapping, num_tokens, cache->num_kv_heads,
                                         cache->head_dim, cache->block_size, nslots, kb, vb,
                                         fp8 ? k_scale + scale_off : nullptr,
                                         fp8 ? v_scale + scale_off : nullptr, dev->err_word, s);
@@ -255,7 +264,7 @@ static pkv_status resolve_decode(const pkv_cache_desc* c, int32_t batch, int32_t
   if (math == PKV_MATH_FFMA && G != 1 && G != 2 && G != 4 && G != 8)
     return fail(PKV_ERR_UNSUPPORTED, "G = %d query heads per KV head (ffma supports 1, 2, 4, 8)", G);
   if (math != PKV_MATH_MMA && math != PKV_MATH_FFMA) return fail(PKV_ERR_INVALID_ARG, "math %d", math);
-  const bool fp8 = c->dtype == PKV_KV_FP8_E4M3;
+  const bool fp8 = c->dtype != PKV_KV_BF16;  // one-byte elements
   const size_t stage_bytes = static_cast<size_t>(2) * c->block_size * c->head_dim * (fp8 ? 1 : 2);
   // Defaults measured on GB300: 4 warps per CTA with shallow (2-stage)
   // rings give several CTAs, i.e. 8+ streaming warps, per SM; deeper rings
@@ -310,6 +319,7 @@ static pkv_status resolve_decode(const pkv_cache_desc* c, int32_t batch, int32_t
   L->bs = c->block_size;
   L->D = c->head_dim;
   L->kv_fp8 = fp8;
+  L->kv_dtype = c->dtype;
   L->ppu = ppu;
   L->pmax = (MB + ppu - 1) / ppu;
   L->math = math;
@@ -364,10 +374,12 @@ pkv_status pkv_paged_decode(const pkv_cache_desc* cache, const void* q, int32_t 
     return fail(PKV_ERR_INVALID_ARG, "kv_group_ptr[%d] = %d outside [0, %d)", layer, slot, cache->num_slots);
   if (!std::isfinite(scale)) return fail(PKV_ERR_INVALID_ARG, "scale is not finite");
   if (batch == 0) return PKV_OK;
-  const bool fp8 = cache->dtype == PKV_KV_FP8_E4M3;
+  const bool fp8 = cache->dtype != PKV_KV_BF16;  // one-byte elements (E4M3 or INT8)
   if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
     return fail(PKV_ERR_INVALID_ARG, "NULL tensor pointer");
-  if (fp8 && (!k_scale || !v_scale)) return fail(PKV_ERR_INVALID_ARG, "E4M3 cache needs k_scale and v_scale");
+  if (fp8 && (!k_scale || !v_scale)) return fail(PKV_ERR_INVALID_ARG, "E4M3 and INT8 caches need k_scale and v_scale");
+  if (fp8 && !scales_aligned(cache->dtype, k_scale, v_scale))
+    return fail(PKV_ERR_ALIGNMENT, "k_scale and v_scale must be 4-byte (E4M3) or 8-byte (INT8) aligned");
   if (!aligned16(q) || !aligned16(out) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(workspace))
     return fail(PKV_ERR_ALIGNMENT, "q, out, caches and workspace must be 16-byte aligned");
   if ((reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u))
@@ -407,7 +419,8 @@ pkv_status pkv_paged_decode(const pkv_cache_desc* cache, const void* q, int32_t 
   L.out = out;
   L.block_tables = block_tables;
   L.context_lens = context_lens;
-  const size_t scale_off = static_cast<size_t>(slot) * cache->num_blocks * cache->num_kv_heads;
+  const size_t scale_off = static_cast<size_t>(slot) * cache->num_blocks * cache->num_kv_heads *
+                           (cache->dtype == PKV_KV_INT8 ? 2 : 1);
   L.k_scale = fp8 ? k_scale + scale_off : nullptr;
   L.v_scale = fp8 ? v_scale + scale_off : nullptr;
   L.work_counter = reinterpret_cast<int32_t*>(ws + wl.counter);
@@ -442,11 +455,14 @@ pkv_status pkv_copy_blocks(const pkv_cache_desc* cache, const void* src_k, const
     return fail(PKV_ERR_INVALID_ARG, "count %d, src_num_blocks %d, dst_num_blocks %d", count,
                 src_num_blocks, dst_num_blocks);
   if (count == 0) return PKV_OK;
-  const bool fp8 = cache->dtype == PKV_KV_FP8_E4M3;
+  const bool fp8 = cache->dtype != PKV_KV_BF16;  // one-byte elements (E4M3 or INT8)
   if (!src_k || !src_v || !dst_k || !dst_v || !block_pairs)
     return fail(PKV_ERR_INVALID_ARG, "NULL pointer");
   if (fp8 && (!src_k_scale || !src_v_scale || !dst_k_scale || !dst_v_scale))
-    return fail(PKV_ERR_INVALID_ARG, "E4M3 pools need source and destination scales");
+    return fail(PKV_ERR_INVALID_ARG, "E4M3 and INT8 pools need source and destination scales");
+  if (fp8 && (!scales_aligned(cache->dtype, src_k_scale, src_v_scale) ||
+              !scales_aligned(cache->dtype, dst_k_scale, dst_v_scale)))
+    return fail(PKV_ERR_ALIGNMENT, "scales must be 4-byte (E4M3) or 8-byte (INT8) aligned");
   if (!aligned16(src_k) || !aligned16(src_v) || !aligned16(dst_k) || !aligned16(dst_v))
     return fail(PKV_ERR_ALIGNMENT, "pools must be 16-byte aligned");
   if ((reinterpret_cast<uintptr_t>(block_pairs) & 3u) != 0)
@@ -473,7 +489,8 @@ pkv_status pkv_copy_blocks(const pkv_cache_desc* cache, const void* src_k, const
                                           fp8 ? src_v_scale : nullptr, src_num_blocks, dst_k, dst_v,
                                           fp8 ? dst_k_scale : nullptr, fp8 ? dst_v_scale : nullptr,
                                           dst_num_blocks, block_pairs, count, block_bytes,
-                                          cache->num_kv_heads, dev->num_sms, dev->err_word, s);
+                                          cache->num_kv_heads * (cache->dtype == PKV_KV_INT8 ? 2 : 1),
+                                          dev->num_sms, dev->err_word, s);
   if (e != cudaSuccess) return cuda_fail(e, "copy_blocks launch");
   return PKV_OK;
 }

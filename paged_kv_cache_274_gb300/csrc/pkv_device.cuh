@@ -225,6 +225,30 @@ __device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t x, uint32_t& lo, uint
       : "r"(x));
 }
 
+// Four INT8 codes (byte i = element i) -> two f16x2 words holding
+// (code - zero): lo = elements (0, 1), hi = elements (2, 3).  Flipping the
+// sign bit gives code + 128 in 0..255; that byte placed under the f16
+// exponent of 1024 (high byte 0x64) is the f16 value 1024 + code + 128, and
+// subtracting zc = f16x2(1152 + zero) leaves code - zero.  Every value here
+// is an integer of magnitude <= 2048, so all of it is exact in f16.
+__device__ __forceinline__ void int8x4_to_f16x2x2(uint32_t x, uint32_t zc, uint32_t& lo, uint32_t& hi) {
+  const uint32_t y = x ^ 0x80808080u;
+  const uint32_t l = __byte_perm(y, 0x64646464u, 0x4140);
+  const uint32_t h = __byte_perm(y, 0x64646464u, 0x4342);
+  const __half2 z = *reinterpret_cast<const __half2*>(&zc);
+  const __half2 lh = __hsub2(*reinterpret_cast<const __half2*>(&l), z);
+  const __half2 hh = __hsub2(*reinterpret_cast<const __half2*>(&h), z);
+  lo = *reinterpret_cast<const uint32_t*>(&lh);
+  hi = *reinterpret_cast<const uint32_t*>(&hh);
+}
+
+// f16x2 constant (1152 + zero, 1152 + zero) for int8x4_to_f16x2x2.
+__device__ __forceinline__ uint32_t int8_zero_const(float zero) {
+  const __half h = __float2half_rn(1152.f + zero);
+  const uint16_t b = *reinterpret_cast<const uint16_t*>(&h);
+  return static_cast<uint32_t>(b) | (static_cast<uint32_t>(b) << 16);
+}
+
 // bf16 pair in a 32-bit word -> two floats (exact).
 __device__ __forceinline__ float bf16lo_to_f32(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi_to_f32(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }

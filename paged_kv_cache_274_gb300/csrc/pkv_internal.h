@@ -28,7 +28,8 @@ struct DecodeLaunch {
   float* part_o;          // workspace: [B][Hq][pmax][D]
   unsigned* err;          // device error word
   int B, Hq, Hkv, G, MB, NB, bs, D;
-  int kv_fp8;
+  int kv_fp8;    // one-byte elements (E4M3 or INT8)
+  int kv_dtype;  // pkv_kv_dtype
   int pmax;  // max partitions of a sequence (ceil(MB / ppu))
   int ppu;   // pages (blocks) per partition
   int row_base;  // first tensor-map row of the selected slot
@@ -65,7 +66,7 @@ int decode_ctas_per_sm(const DecodeLaunch& L, size_t smem);
 void set_last_error_message(const char* msg);
 
 // KV append.
-cudaError_t launch_kv_append(int kv_fp8, const void* k, const void* v,
+cudaError_t launch_kv_append(int kv_dtype, const void* k, const void* v,
                              const int64_t* slot_mapping, int N, int Hkv, int D, int bs,
                              int64_t nslots, void* k_base, void* v_base, const float* ks_base,
                              const float* vs_base, unsigned* err, cudaStream_t stream);

@@ -33,7 +33,14 @@ class DeviceCase:
 
     def __init__(self, c: DecodeCase):
         self.c = c
-        if c.kv_dtype == "fp8":
+        if c.kv_dtype in ("int8", "int8a"):
+            self.k_host = oracle.int8_quantize_cache(c.k_src, c.k_scale)
+            self.v_host = oracle.int8_quantize_cache(c.v_src, c.v_scale)
+            self.k = to_dev(self.k_host)
+            self.v = to_dev(self.v_host)
+            self.ks = to_dev(c.k_scale)
+            self.vs = to_dev(c.v_scale)
+        elif c.kv_dtype == "fp8":
             self.k_host = oracle.quantize_cache(c.k_src, c.k_scale)
             self.v_host = oracle.quantize_cache(c.v_src, c.v_scale)
             self.k = to_dev(self.k_host)

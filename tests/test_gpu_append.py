@@ -18,6 +18,9 @@ def _caches(shape, dtype, seed):
     if dtype == "bf16":
         k = rng.integers(0, 1 << 16, size=shape, dtype=np.uint16)
         v = rng.integers(0, 1 << 16, size=shape, dtype=np.uint16)
+    elif dtype == "int8":
+        k = rng.integers(-128, 128, size=shape, dtype=np.int8)
+        v = rng.integers(-128, 128, size=shape, dtype=np.int8)
     else:
         k = rng.integers(0, 256, size=shape, dtype=np.uint8)
         v = rng.integers(0, 256, size=shape, dtype=np.uint8)
@@ -28,18 +31,42 @@ def _dev_cache(a):
     return to_dev_bf16(a) if a.dtype == np.uint16 else to_dev(a)
 
 
+@pytest.mark.parametrize("scale,zero", [(1.0, 0.0), (0.031, 0.0), (0.02, -17.0), (1e-3, 5.0), (250.0, 127.0)])
+def test_int8_quantisation_every_bf16_pattern(scale, zero):
+    # all 65536 bf16 bit patterns (NaN included) through the INT8 append,
+    # against the oracle's encoder
+    Hkv, D, bs = 1, 128, 32
+    N = (1 << 16) // D
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16).reshape(N, Hkv, D)
+    NB = N // bs
+    shape = (1, NB, Hkv, bs, D)
+    kd = torch.zeros(shape, dtype=torch.int8, device=DEV)
+    vd = torch.zeros(shape, dtype=torch.int8, device=DEV)
+    prm = np.zeros((1, NB, Hkv, 2), dtype=np.float32)
+    prm[..., 0] = scale
+    prm[..., 1] = zero
+    slots = np.arange(N, dtype=np.int64)
+    pkv.kv_append(to_dev_bf16(bits), to_dev_bf16(bits), to_dev(slots), kd, vd, to_dev(prm), to_dev(prm))
+    torch.cuda.synchronize()
+    ko = np.zeros(shape, np.int8)
+    vo = np.zeros(shape, np.int8)
+    assert oracle.kv_append(bits, bits, slots, ko, vo, prm, prm) == 0
+    assert np.array_equal(kd.cpu().numpy(), ko)
+    assert np.array_equal(vd.cpu().numpy(), vo)
+
+
 def _host(t):
     if t.dtype == torch.bfloat16:
         return t.view(torch.int16).cpu().numpy().view(np.uint16)
     return t.cpu().numpy()
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp8", "int8"])
 @pytest.mark.parametrize("D,bs", [(64, 16), (128, 16), (128, 32)])
 @pytest.mark.parametrize("slot", [0, 1])
 def test_append_bit_exact(dtype, D, bs, slot):
-    if dtype == "fp8" and D != 128:
-        pytest.skip("E4M3 cache needs head_dim 128")
+    if dtype != "bf16" and D != 128:
+        pytest.skip("one-byte caches need head_dim 128")
     S, NB, Hkv, N = 2, 37, 4, 64
     shape = (S, NB, Hkv, bs, D)
     k, v = _caches(shape, dtype, 1 + D + bs)       # random canary bytes everywhere
@@ -53,6 +80,11 @@ def test_append_bit_exact(dtype, D, bs, slot):
     if dtype == "fp8":
         ks = rng.uniform(0.002, 0.03, size=(S, NB, Hkv)).astype(np.float32)
         vs = rng.uniform(0.002, 0.03, size=(S, NB, Hkv)).astype(np.float32)
+    elif dtype == "int8":
+        # half the pages symmetric (zero 0), half with a zero point
+        z = np.where(rng.random((S, NB, Hkv)) < 0.5, 0, rng.integers(-30, 31, size=(S, NB, Hkv)))
+        ks = np.stack([rng.uniform(0.01, 0.05, size=(S, NB, Hkv)), z], axis=-1).astype(np.float32)
+        vs = np.stack([rng.uniform(0.01, 0.05, size=(S, NB, Hkv)), z[..., ::-1]], axis=-1).astype(np.float32)
     kd, vd = _dev_cache(k), _dev_cache(v)
     pkv.kv_append(to_dev_bf16(kn), to_dev_bf16(vn), to_dev(slots), kd, vd,
                   None if ks is None else to_dev(ks), None if vs is None else to_dev(vs), slot=slot)

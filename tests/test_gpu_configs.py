@@ -106,3 +106,14 @@ def test_fp8_shared_four_layers():
         torch.cuda.synchronize()
         assert pkv.read_device_error() == 0
         _check_sampled(dc, out, layer, 12, 10 + layer, f"fp8 layer {layer}")
+
+
+def test_int8_shared_two_layers():
+    # the same workload with an asymmetric INT8 cache
+    c = fp8_shared_case(kv_dtype="int8a", L=2)
+    dc = DeviceCase(c)
+    for layer in range(c.L):
+        out = dc.decode(layer=layer)
+        torch.cuda.synchronize()
+        assert pkv.read_device_error() == 0
+        _check_sampled(dc, out, layer, 12, 20 + layer, f"int8 layer {layer}")

@@ -1,5 +1,6 @@
 """GPU block copy against the oracle's copy: bit-exact, between device pools,
-to and from pinned host memory, with E4M3 scales; plus copy-on-write of a
+to and from pinned host memory, with E4M3 scales and INT8 (scale, zero)
+pairs; plus copy-on-write of a
 shared prefix block followed by an append and a decode."""
 import numpy as np
 import pytest
@@ -18,8 +19,10 @@ def _pools(seed, nb, shape, dtype):
     if dtype == "bf16":
         return (rng.integers(0, 1 << 16, size=(nb,) + shape, dtype=np.uint16),
                 rng.integers(0, 1 << 16, size=(nb,) + shape, dtype=np.uint16))
-    return (rng.integers(0, 256, size=(nb,) + shape, dtype=np.uint8),
-            rng.integers(0, 256, size=(nb,) + shape, dtype=np.uint8))
+    dt = np.uint8 if dtype == "fp8" else np.int8
+    lo, hi = (0, 256) if dtype == "fp8" else (-128, 128)
+    return (rng.integers(lo, hi, size=(nb,) + shape, dtype=dt),
+            rng.integers(lo, hi, size=(nb,) + shape, dtype=dt))
 
 
 def _tensor(a, where):
@@ -38,7 +41,8 @@ def _host(t):
     return t.numpy()
 
 
-@pytest.mark.parametrize("dtype,shape", [("bf16", (8, 16, 128)), ("bf16", (2, 32, 64)), ("fp8", (8, 32, 128))])
+@pytest.mark.parametrize("dtype,shape", [("bf16", (8, 16, 128)), ("bf16", (2, 32, 64)), ("fp8", (8, 32, 128)),
+                                         ("int8", (4, 16, 128))])
 @pytest.mark.parametrize("src_where,dst_where", [("device", "device"), ("device", "host"), ("host", "device")])
 def test_copy_bit_exact(dtype, shape, src_where, dst_where):
     src_nb, dst_nb, n = 40, 25, 17
@@ -48,9 +52,10 @@ def test_copy_bit_exact(dtype, shape, src_where, dst_where):
     pairs = np.stack([rng.choice(src_nb, n, replace=False), rng.choice(dst_nb, n, replace=False)],
                      axis=1).astype(np.int32)
     scales = {}
-    if dtype == "fp8":
+    if dtype != "bf16":
+        per_page = (shape[0],) if dtype == "fp8" else (shape[0], 2)
         for name, nb in (("sks", src_nb), ("svs", src_nb), ("dks", dst_nb), ("dvs", dst_nb)):
-            scales[name] = rng.uniform(0.01, 1.0, size=(nb, shape[0])).astype(np.float32)
+            scales[name] = rng.uniform(0.01, 1.0, size=(nb,) + per_page).astype(np.float32)
     t_sk, t_sv = _tensor(sk, src_where), _tensor(sv, src_where)
     t_dk, t_dv = _tensor(dk, dst_where), _tensor(dv, dst_where)
     ts = {k: (v := _tensor(a, "device" if k[0] == "s" and src_where == "device" or
@@ -62,7 +67,7 @@ def test_copy_bit_exact(dtype, shape, src_where, dst_where):
     args = [scales.get("sks"), scales.get("svs"), scales.get("dks"), scales.get("dvs")]
     assert oracle.copy_blocks(sk, sv, dk, dv, pairs, *args) == 0
     assert np.array_equal(_host(t_dk), dk) and np.array_equal(_host(t_dv), dv)
-    if dtype == "fp8":
+    if dtype != "bf16":
         assert np.array_equal(_host(ts["dks"]), scales["dks"])
         assert np.array_equal(_host(ts["dvs"]), scales["dvs"])
 

@@ -37,6 +37,7 @@ SWEEP = [  # (D, bs, Hq, Hkv, dtype)
     (64, 16, 8, 2, "bf16"), (64, 32, 4, 4, "bf16"), (128, 16, 32, 8, "bf16"),
     (128, 32, 64, 8, "bf16"), (128, 16, 8, 1, "bf16"), (128, 32, 16, 2, "bf16"),
     (128, 32, 32, 8, "fp8"), (128, 16, 8, 2, "fp8"), (128, 32, 8, 8, "fp8"),
+    (128, 32, 32, 8, "int8"), (128, 16, 8, 2, "int8a"), (128, 32, 16, 1, "int8a"),
 ]
 LENS = [1, 15, 16, 17, 100, 257, 0, 513, 1031]
 
@@ -48,7 +49,7 @@ def test_random_sweep(D, bs, Hq, Hkv, dtype, math, ppu):
     G = Hq // Hkv
     if math == "ffma" and G not in (1, 2, 4, 8):
         pytest.skip("ffma supports G in {1, 2, 4, 8}")
-    seed = D * 1000 + bs * 10 + Hq + 7 * Hkv + (50000 if dtype == "fp8" else 0)
+    seed = D * 1000 + bs * 10 + Hq + 7 * Hkv + {"bf16": 0, "fp8": 50000, "int8": 60000, "int8a": 70000}[dtype]
     c = random_case(seed, len(LENS), Hq, Hkv, D, bs, LENS, kv_dtype=dtype, poison=True)
     got, want, _, _ = _run(c, math, ppu)
     assert_close(got, want, f"D{D} bs{bs} G{G} {dtype} {math} ppu{ppu}")
@@ -73,7 +74,7 @@ def test_head_groupings(math, G):
 
 
 @pytest.mark.parametrize("math", ["mma", "ffma"])
-@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp8", "int8a"])
 def test_single_token_is_v_exactly(math, dtype):
     # one token: softmax weight 1, the output is bf16(V_0) bit for bit
     c = random_case(5, 3, 8, 2, 128, 32, [1, 1, 1], kv_dtype=dtype)
@@ -83,7 +84,7 @@ def test_single_token_is_v_exactly(math, dtype):
         want_bits = bf16_bits_from_f32(want.astype(np.float32))
         assert np.array_equal(bits, want_bits)
     else:
-        # E4M3: scale * code is rounded to fp32 before the bf16 output
+        # one-byte caches: the dequantised value is rounded to fp32 first
         assert_close(got, want, "single token fp8")
 
 
@@ -138,7 +139,7 @@ def test_split_matches_single_pass(math):
     assert_close(split, single, "split vs single")
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp8", "int8"])
 def test_shared_with_pointer(dtype):
     # two cache slots; layers 0..3 read slots [1, 0, 1, 1]
     c = random_case(14, 3, 16, 4, 128, 32, [40, 200, 77], kv_dtype=dtype, S=2,

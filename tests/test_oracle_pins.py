@@ -345,11 +345,58 @@ def pin_copy_blocks(lib=None):
     assert oracle.copy_blocks(ak, av, bk, bv, np.array([[11, 0]], np.int32), lib=lib) == oracle.ORACLE_BAD_BLOCK
 
 
+def pin_int8_codec(lib=None):
+    # reference: numpy's IEEE float32 division and round-half-even rint,
+    # plus the clamp and the NaN rule; closed forms for ties and range ends
+    rng = np.random.Generator(np.random.PCG64(130))
+    xs = np.concatenate([rng.standard_normal(400).astype(np.float32) * 3,
+                         np.array([0.0, -0.0, 1e30, -1e30], np.float32)])
+    for scale, zero in ((0.031, 0.0), (0.5, 0.0), (0.02, -17.0), (0.2, 100.0), (1.0, -128.0)):
+        sc, z = np.float32(scale), np.float32(zero)
+        lo = -127.0 if zero == 0 else -128.0
+        want = np.clip(np.rint(xs / sc) + z, lo, 127).astype(np.int64)
+        got = np.array([oracle.int8_encode(x, scale, zero, lib=lib) for x in xs])
+        assert np.array_equal(got, want), (scale, zero)
+        assert oracle.int8_encode(float("nan"), scale, zero, lib=lib) == int(zero)
+    # ties go to the even integer; exact multiples are exact; decode is (q - z) s
+    assert [oracle.int8_encode(v, 1.0, lib=lib) for v in (0.5, 1.5, 2.5, -2.5, 7.0)] == [0, 2, 2, -2, 7]
+    assert oracle.int8_encode(-500.0, 1.0, 0.0, lib=lib) == -127
+    assert oracle.int8_encode(-500.0, 1.0, 5.0, lib=lib) == -128
+    for q in (-128, -1, 0, 1, 127):
+        assert oracle.int8_decode(q, 0.25, 3.0, lib=lib) == (q - 3) * 0.25
+
+
+def pin_sdpa_int8(lib=None):
+    # INT8 pages with (scale, zero) per (block, KV head): the reference is
+    # SDPA over (code - zero) * scale computed here in float64
+    Hq, Hkv, D, bs, lens = 8, 2, 128, 16, [70, 31]
+    rng = np.random.Generator(np.random.PCG64(131))
+    codes = [rng.integers(-128, 128, size=(n, Hkv, D), dtype=np.int8) for n in lens]
+    vcodes = [rng.integers(-128, 128, size=(n, Hkv, D), dtype=np.int8) for n in lens]
+    kc, vc, bt, ctx, pl = paged_from_dense(codes, vcodes, bs, seed=132)
+    NB = kc.shape[1]
+    kp = np.stack([rng.uniform(0.001, 0.05, size=(1, NB, Hkv)),
+                   rng.integers(-20, 21, size=(1, NB, Hkv))], axis=-1).astype(np.float32)
+    vp = np.stack([rng.uniform(0.001, 0.05, size=(1, NB, Hkv)),
+                   rng.integers(-20, 21, size=(1, NB, Hkv))], axis=-1).astype(np.float32)
+    q = normal_bf16_bits(133, (2, Hq, D))
+    got = oracle.paged_decode(q, kc, vc, bt, ctx, [0], 0, 0.0883883, k_scale=kp, v_scale=vp, lib=lib)
+    kd, vd = [], []
+    for b, n in enumerate(lens):
+        blk = np.array([pl[b][t // bs] for t in range(n)])
+        ks, kz = kp[0, blk, :, 0][:, :, None].astype(np.float64), kp[0, blk, :, 1][:, :, None].astype(np.float64)
+        vs, vz = vp[0, blk, :, 0][:, :, None].astype(np.float64), vp[0, blk, :, 1][:, :, None].astype(np.float64)
+        kd.append((codes[b].astype(np.float64) - kz) * ks)
+        vd.append((vcodes[b].astype(np.float64) - vz) * vs)
+    want = sdpa_reference(q, kd, vd, 0.0883883)
+    np.testing.assert_allclose(got, want, rtol=TOL, atol=TOL)
+
+
 PINS = [pin_sdpa_bf16, pin_large_logits, pin_closed_forms, pin_permutation_invariance,
         pin_shared_prefix, pin_poisoned_unused, pin_gqa_equals_repeated_mha,
         pin_shared_with_pointer, pin_sdpa_fp8, pin_bad_inputs_rejected,
         pin_e4m3_decode_all_codes, pin_e4m3_encode_matches_library, pin_e4m3_scaled_quantize,
-        pin_append_scatter, pin_append_fp8, pin_copy_blocks]
+        pin_append_scatter, pin_append_fp8, pin_copy_blocks, pin_int8_codec, pin_sdpa_int8]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -379,6 +426,11 @@ MUTANTS = [
     ("e4m3_ties_up", "else code = (lo % 2 == 0) ? lo : lo + 1;", "else code = lo + 1;"),
     ("copy_wrong_source", "memcpy(dst_k + d * block_bytes, src_k + s * block_bytes",
      "memcpy(dst_k + d * block_bytes, src_k + d * block_bytes"),
+    ("int8_rounds_down", "double q = nearbyint((double)t) + (double)zero;",
+     "double q = floor((double)t) + (double)zero;"),
+    ("int8_zero_sign", "return ((double)q - (double)zero) * (double)scale;",
+     "return ((double)q + (double)zero) * (double)scale;"),
+    ("int8_symmetric_clamp", "double lo = (zero == 0.0f) ? -127.0 : -128.0;", "double lo = -128.0;"),
     ("append_wrong_offset", "int64_t blk = s / bs, off = s % bs;", "int64_t blk = s / bs, off = (s + 1) % bs;"),
 ]
 

@@ -11,6 +11,7 @@ from .gen import (  # noqa: F401
     bf16_bits_to_f32,
     normal_bf16_bits,
     fp8_tile_scales,
+    int8_tile_params,
     tiny_case,
     llama8b_layer_case,
     mixed_prefix_case,

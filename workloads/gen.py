@@ -81,6 +81,34 @@ def fp8_tile_scales(src_bits: np.ndarray) -> np.ndarray:
     return out
 
 
+def int8_tile_params(src_bits: np.ndarray, symmetric: bool) -> np.ndarray:
+    """Caller-side INT8 page parameters, float32 [S][NB][Hkv][2] = (scale, zero).
+
+    Symmetric: scale = amax(|tile|) / 127, zero = 0.  Asymmetric: scale =
+    (max - min) / 255 and zero = rint(-128 - min / scale) clamped to
+    [-128, 127].  A constant tile gets scale 1.  float32 arithmetic."""
+    S, NB, Hkv = src_bits.shape[:3]
+    out = np.empty((S * NB * Hkv, 2), dtype=np.float32)
+    flat = src_bits.reshape(S * NB * Hkv, -1)
+    step = 1 << 14
+    for s in range(0, flat.shape[0], step):
+        f = bf16_bits_to_f32(flat[s:s + step])
+        if symmetric:
+            amax = np.abs(f).max(axis=1).astype(np.float32)
+            sc = (amax / np.float32(127.0)).astype(np.float32)
+            sc[amax == 0] = np.float32(1.0)
+            zero = np.zeros_like(sc)
+        else:
+            lo = f.min(axis=1).astype(np.float32)
+            hi = f.max(axis=1).astype(np.float32)
+            sc = ((hi - lo) / np.float32(255.0)).astype(np.float32)
+            sc[hi == lo] = np.float32(1.0)
+            zero = np.clip(np.rint(np.float32(-128.0) - lo / sc), -128, 127).astype(np.float32)
+        out[s:s + step, 0] = sc
+        out[s:s + step, 1] = zero
+    return out.reshape(S, NB, Hkv, 2)
+
+
 # ---------------------------------------------------------------------------
 # case container
 # ---------------------------------------------------------------------------
@@ -94,7 +122,7 @@ class DecodeCase:
     bs: int
     S: int
     NB: int
-    kv_dtype: str                      # "bf16" or "fp8"
+    kv_dtype: str                      # "bf16", "fp8", "int8" (symmetric) or "int8a" (asymmetric)
     context_lens: np.ndarray           # int32 [B]
     block_tables: np.ndarray           # int32 [B][MB]
     kv_group_ptr: np.ndarray           # int32 [L]
@@ -102,7 +130,7 @@ class DecodeCase:
     q: np.ndarray                      # uint16 [L][B][Hq][D]
     k_src: Optional[np.ndarray]        # uint16 [S][NB][Hkv][bs][D] (None: structure only)
     v_src: Optional[np.ndarray]
-    k_scale: Optional[np.ndarray] = None   # float32 [S][NB][Hkv] (fp8 only)
+    k_scale: Optional[np.ndarray] = None   # float32 [S][NB][Hkv] (fp8) or [S][NB][Hkv][2] (int8)
     v_scale: Optional[np.ndarray] = None
     # optional append step: new tokens written before the decode
     k_new: Optional[np.ndarray] = None     # uint16 [N][Hkv][D]
@@ -166,9 +194,15 @@ def _cache(cfg: int, S: int, NB: int, Hkv: int, bs: int, D: int, fill: bool):
 
 
 def _finish_fp8(case: DecodeCase) -> DecodeCase:
+    """Page parameters for one-byte caches: "fp8" (E4M3 scales), "int8"
+    (symmetric INT8) and "int8a" (asymmetric INT8)."""
     if case.kv_dtype == "fp8":
         case.k_scale = fp8_tile_scales(case.k_src)
         case.v_scale = fp8_tile_scales(case.v_src)
+    elif case.kv_dtype in ("int8", "int8a"):
+        sym = case.kv_dtype == "int8"
+        case.k_scale = int8_tile_params(case.k_src, sym)
+        case.v_scale = int8_tile_params(case.v_src, sym)
     return case
 
 
@@ -289,10 +323,12 @@ def long_context_case(variant: str = "b4_32k", fill: bool = True) -> DecodeCase:
                       np.zeros(1, np.int32), _scale_for(D), _queries(cfg, 1, B, Hq, D), k, v)
 
 
-def fp8_shared_case(fill: bool = True, B: int = 128, ctx_len: int = 8192, L: int = 4) -> DecodeCase:
+def fp8_shared_case(fill: bool = True, B: int = 128, ctx_len: int = 8192, L: int = 4,
+                    kv_dtype: str = "fp8") -> DecodeCase:
     """FP8 KV cache with cross-layer sharing: L layers whose shared-with
     pointers all name cache slot 0; B 128, 32 q / 8 KV heads, D 128, bs 32,
-    context 8192; per-(block, KV head) fp32 scales from the bf16 N(0,1) data."""
+    context 8192; per-(block, KV head) fp32 scales from the bf16 N(0,1) data.
+    kv_dtype "int8" / "int8a" gives the same workload with an INT8 cache."""
     cfg, Hq, Hkv, D, bs = 5, 32, 8, 128, 32
     per_seq = ctx_len // bs
     NB = B * per_seq
@@ -300,7 +336,7 @@ def fp8_shared_case(fill: bool = True, B: int = 128, ctx_len: int = 8192, L: int
     tables = _tables_from_counts([per_seq] * B, phys, per_seq)
     ctx = np.full(B, ctx_len, dtype=np.int32)
     k, v = _cache(cfg, 1, NB, Hkv, bs, D, fill)
-    c = DecodeCase("fp8_shared", B, Hq, Hkv, D, bs, 1, NB, "fp8", ctx, tables,
+    c = DecodeCase(kv_dtype + "_shared", B, Hq, Hkv, D, bs, 1, NB, kv_dtype, ctx, tables,
                    np.zeros(L, np.int32), _scale_for(D), _queries(cfg, L, B, Hq, D), k, v)
     return _finish_fp8(c) if fill else c
 
