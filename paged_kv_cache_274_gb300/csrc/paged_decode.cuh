@@ -96,7 +96,12 @@ struct MmaState {
   float o[D / 8][2 * kR];       // output accumulators, one entry per 8 columns of d
   float m[kR];                  // running max of rows g (and g+8), log2 domain
   float l[kR];                  // this lane's share of the running sums
+  // INT8 pages enter the products as 1152 + code (see int8x4_to_f16x2x2_biased):
+  float qs[kR];    // sum over d of the f16 query row, for removing the K bias
+  float corr[kR];  // V bias carried by every column of o (same rescaling as o)
 };
+
+constexpr uint32_t kOnesF16x2 = 0x3C003C00u;  // f16x2 (1, 1)
 
 template <bool FP8, bool HI, int N>
 __device__ __forceinline__ void mma_rows(float (&d)[N], const uint32_t (&a)[N], uint32_t b0,
@@ -168,14 +173,49 @@ __device__ __forceinline__ void bytes4_to_f16x2x2(uint32_t x, uint32_t zc, uint3
   if constexpr (I8) int8x4_to_f16x2x2(x, zc, lo, hi); else e4m3x4_to_f16x2x2(x, lo, hi);
 }
 
+// Tensor-core back-end form: INT8 codes stay biased by 1152 + zero and the
+// bias is removed per row after the products (one subtraction per score and
+// per output column instead of one per cache element).
+template <bool I8>
+__device__ __forceinline__ void bytes4_to_f16x2x2_mma(uint32_t x, uint32_t& lo, uint32_t& hi) {
+  if constexpr (I8) int8x4_to_f16x2x2_biased(x, lo, hi); else e4m3x4_to_f16x2x2(x, lo, hi);
+}
+
+// INT8: qs = sum over d of each head's f16 query row (q . 1 on the tensor
+// cores, fp32 accumulation), and the V bias accumulator cleared.
+template <int D, int BS, bool FP8, bool HI>
+__device__ __forceinline__ void mma_int8_prepare(MmaState<D, BS, FP8, HI>& st) {
+  constexpr int kR = HI ? 2 : 1;
+  float acc[2 * kR];
+#pragma unroll
+  for (int e = 0; e < 2 * kR; ++e) acc[e] = 0.f;
+#pragma unroll
+  for (int s = 0; s < D / 16; ++s) mma_rows<FP8, HI>(acc, st.qa[s], kOnesF16x2, kOnesF16x2);
+#pragma unroll
+  for (int r = 0; r < kR; ++r) {
+    st.qs[r] = acc[2 * r];
+    st.corr[r] = 0.f;
+  }
+}
+
+// INT8: remove the V bias from every output column (once per work unit).
+template <int D, int BS, bool FP8, bool HI>
+__device__ __forceinline__ void mma_int8_unbias(MmaState<D, BS, FP8, HI>& st) {
+  constexpr int kR = HI ? 2 : 1;
+#pragma unroll
+  for (int n = 0; n < D / 8; ++n)
+#pragma unroll
+    for (int e = 0; e < 2 * kR; ++e) st.o[n][e] -= st.corr[e >> 1];
+}
+
 // One page (BS tokens) of the online softmax with tensor-core tiles.
 // `valid` = tokens of the page that belong to the sequence (0..BS); `sl` =
-// softmax scale * log2(e) (* the page's K scale for E4M3); `vscale` = the
-// page's V scale (E4M3 only).
+// softmax scale * log2(e) (* the page's K scale for one-byte pages);
+// `vscale` = the page's V scale (one-byte pages); `kc`, `vc` = the page's
+// INT8 biases 1152 + zero of K and V.
 template <int D, int BS, bool FP8, bool HI, bool I8>
 __device__ __forceinline__ void mma_page(MmaState<D, BS, FP8, HI>& st, uint8_t* stage, int valid,
-                                         float sl, float vscale, uint32_t kzc, uint32_t vzc,
-                                         int lane) {
+                                         float sl, float vscale, float kc, float vc, int lane) {
   using Geo = PageGeom<D, BS, FP8>;
   constexpr int kR = HI ? 2 : 1;
   constexpr int kC = 2 * kR;
@@ -208,7 +248,7 @@ __device__ __forceinline__ void mma_page(MmaState<D, BS, FP8, HI>& st, uint8_t* 
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           uint32_t b0, b1;
-          bytes4_to_f16x2x2<I8>(r[i], kzc, b0, b1);
+          bytes4_to_f16x2x2_mma<I8>(r[i], b0, b1);
           mma_rows<FP8, HI>(s[nt], st.qa[c4 * 4 + i], b0, b1);
         }
       }
@@ -217,6 +257,10 @@ __device__ __forceinline__ void mma_page(MmaState<D, BS, FP8, HI>& st, uint8_t* 
 
   // ---- online softmax (log2 domain) ----
   const bool partial = valid < BS;  // warp-uniform: only a sequence's last page
+  // INT8: q . (K' - kc) = q . K' - kc * qs, folded into the scaling
+  float kb[kR];
+#pragma unroll
+  for (int r = 0; r < kR; ++r) kb[r] = I8 ? -kc * st.qs[r] * sl : 0.f;
   float mx[kR];
 #pragma unroll
   for (int r = 0; r < kR; ++r) mx[r] = -INFINITY;
@@ -226,7 +270,7 @@ __device__ __forceinline__ void mma_page(MmaState<D, BS, FP8, HI>& st, uint8_t* 
 #pragma unroll
       for (int e = 0; e < kC; ++e) {
         const int tok = qk_token<FP8>(nt, 2 * tig + (e & 1));
-        const float v = (tok < valid) ? s[nt][e] * sl : -INFINITY;
+        const float v = (tok < valid) ? fmaf(s[nt][e], sl, kb[e >> 1]) : -INFINITY;
         s[nt][e] = v;
         mx[e >> 1] = fmaxf(mx[e >> 1], v);
       }
@@ -235,7 +279,7 @@ __device__ __forceinline__ void mma_page(MmaState<D, BS, FP8, HI>& st, uint8_t* 
     for (int nt = 0; nt < BS / 8; ++nt)
 #pragma unroll
       for (int e = 0; e < kC; ++e) {
-        const float v = s[nt][e] * sl;
+        const float v = fmaf(s[nt][e], sl, kb[e >> 1]);
         s[nt][e] = v;
         mx[e >> 1] = fmaxf(mx[e >> 1], v);
       }
@@ -272,6 +316,10 @@ __device__ __forceinline__ void mma_page(MmaState<D, BS, FP8, HI>& st, uint8_t* 
     for (int n = 0; n < D / 8; ++n)
 #pragma unroll
       for (int e = 0; e < kC; ++e) st.o[n][e] *= alpha[e >> 1];
+    if constexpr (I8) {
+#pragma unroll
+      for (int r = 0; r < kR; ++r) st.corr[r] *= alpha[r];
+    }
   }
 
   // P as A fragments: k-step ks covers tokens 16ks .. 16ks+15 (n-tiles 2ks, 2ks+1)
@@ -289,9 +337,22 @@ __device__ __forceinline__ void mma_page(MmaState<D, BS, FP8, HI>& st, uint8_t* 
           pa[ks][2 * r + kh] = pack_f16x2(src[2 * r], src[2 * r + 1]);
       }
 
-  // Rows of V past the sequence end may hold anything (even NaN); P is 0
-  // there but 0 * NaN is NaN, so clear them before the product.
-  if (partial) {
+  // INT8: P . (V' - vc) = P . V' - vc * sum(P), with sum(P) taken over the
+  // same f16 P (P . 1 on the tensor cores) and applied to o at the end
+  if constexpr (I8) {
+    float ps[kC];
+#pragma unroll
+    for (int e = 0; e < kC; ++e) ps[e] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < BS / 16; ++ks) mma_rows<FP8, HI>(ps, pa[ks], kOnesF16x2, kOnesF16x2);
+#pragma unroll
+    for (int r = 0; r < kR; ++r) st.corr[r] = fmaf(vscale * vc, ps[2 * r], st.corr[r]);
+  }
+
+  // Rows of V past the sequence end may hold anything (E4M3 and bf16: even
+  // NaN); P is 0 there but 0 * NaN is NaN, so clear them before the product.
+  // Every INT8 byte is a finite value.
+  if (!I8 && partial) {
     uint8_t* vp = stage + Geo::kTensorBytes;
     for (int idx = lane; idx < Geo::kTensorBytes / 16; idx += 32) {
       const int row = (idx % (Geo::kRegionBytes / 16)) / 8;
@@ -335,7 +396,7 @@ __device__ __forceinline__ void mma_page(MmaState<D, BS, FP8, HI>& st, uint8_t* 
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           uint32_t b0, b1;
-          bytes4_to_f16x2x2<I8>(q[j], vzc, b0, b1);
+          bytes4_to_f16x2x2_mma<I8>(q[j], b0, b1);
           mma_rows<FP8, HI>(t[j], pa[ks], b0, b1);
         }
       }
@@ -772,24 +833,24 @@ __global__ void __launch_bounds__(256, 1)
       constexpr bool kHi = GT > 8;
       MmaState<D, BS, FP8, kHi> st;
       mma_load_q<D, BS, FP8, kHi>(st, qg, p.G, lane);
+      if constexpr (I8) mma_int8_prepare(st);
       for (int j = 0; j < npages; ++j) {
         const uint32_t s = it % static_cast<uint32_t>(R);
         const bool landed = mbar_wait_bounded(&bars[s], (it / R) & 1u, kWaitLimitNs);
         if (!__all_sync(kFull, landed)) { timed_out = true; break; }
         const bool bad = (j < 32) ? ((badm0 >> (j & 31)) & 1u) : ((badm1 >> (j & 31)) & 1u);
         const int valid = bad ? 0 : min(BS, t1 - (t0 + j * BS));
-        float ksc = 1.f, vsc = 1.f;
-        uint32_t kzc = 0u, vzc = 0u;
+        float ksc = 1.f, vsc = 1.f, kc = 0.f, vc = 0.f;
         if (FP8) {
           ksc = (j < 32) ? __shfl_sync(kFull, ks0, j & 31) : __shfl_sync(kFull, ks1, j & 31);
           vsc = (j < 32) ? __shfl_sync(kFull, vs0, j & 31) : __shfl_sync(kFull, vs1, j & 31);
         }
         if (I8) {
-          kzc = int8_zero_const((j < 32) ? __shfl_sync(kFull, kz0, j & 31) : __shfl_sync(kFull, kz1, j & 31));
-          vzc = int8_zero_const((j < 32) ? __shfl_sync(kFull, vz0, j & 31) : __shfl_sync(kFull, vz1, j & 31));
+          kc = kInt8Bias + ((j < 32) ? __shfl_sync(kFull, kz0, j & 31) : __shfl_sync(kFull, kz1, j & 31));
+          vc = kInt8Bias + ((j < 32) ? __shfl_sync(kFull, vz0, j & 31) : __shfl_sync(kFull, vz1, j & 31));
         }
         mma_page<D, BS, FP8, kHi, I8>(st, ring + static_cast<size_t>(s) * Geo::kStageBytes, valid,
-                                      p.scale_log2 * ksc, vsc, kzc, vzc, lane);
+                                      p.scale_log2 * ksc, vsc, kc, vc, lane);
         fence_proxy_async_smem();  // this lane's reads of the stage precede the refill
         __syncwarp();
         if (j + R < npages) { issue(j + R, it + R); ++issued; }
@@ -797,6 +858,7 @@ __global__ void __launch_bounds__(256, 1)
         ++consumed;
       }
       if (!timed_out) {
+        if constexpr (I8) mma_int8_unbias(st);
         mma_finish<D, BS, FP8, kHi>(st, p, b, kvh, pidx, nparts, lane);
         if (nparts > 1 && p.fused_merge) arrive_and_merge<D>(p, b, kvh, nparts, lane);
       }

@@ -242,6 +242,19 @@ __device__ __forceinline__ void int8x4_to_f16x2x2(uint32_t x, uint32_t zc, uint3
   hi = *reinterpret_cast<const uint32_t*>(&hh);
 }
 
+// Four INT8 codes -> two f16x2 words holding 1152 + code (exact): the same
+// sign flip and exponent placement as int8x4_to_f16x2x2 without the
+// subtraction, for callers that remove the constant 1152 + zero after the
+// product (it is the same for every element of a page).
+__device__ __forceinline__ void int8x4_to_f16x2x2_biased(uint32_t x, uint32_t& lo, uint32_t& hi) {
+  const uint32_t y = x ^ 0x80808080u;
+  lo = __byte_perm(y, 0x64646464u, 0x4140);
+  hi = __byte_perm(y, 0x64646464u, 0x4342);
+}
+
+// Bias of int8x4_to_f16x2x2_biased: the f16 value of code 0 before the flip.
+constexpr float kInt8Bias = 1152.f;
+
 // f16x2 constant (1152 + zero, 1152 + zero) for int8x4_to_f16x2x2.
 __device__ __forceinline__ uint32_t int8_zero_const(float zero) {
   const __half h = __float2half_rn(1152.f + zero);
