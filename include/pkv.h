@@ -63,7 +63,7 @@
 extern "C" {
 #endif
 
-#define PKV_ABI_VERSION 1
+#define PKV_ABI_VERSION 2
 
 typedef enum {
   PKV_OK = 0,
@@ -163,6 +163,8 @@ typedef struct {
   int32_t kernels_per_call;  /* planner + decode (+ merge above 4 partitions) */
   size_t workspace_bytes;
   size_t smem_bytes_per_cta;
+  int32_t query_tokens_per_tile; /* multi-token queries: tokens per row tile (1 for T = 1) */
+  int32_t row_tiles;             /* row tiles per (sequence, KV head): each reads the pages */
 } pkv_decode_plan;
 
 /*
@@ -219,6 +221,54 @@ pkv_status pkv_paged_decode(const pkv_cache_desc* cache,
                             float scale, void* out,
                             void* workspace, size_t workspace_bytes,
                             const pkv_decode_opts* opts, void* stream);
+
+/* Largest number of query tokens per sequence of pkv_paged_decode_multi. */
+#define PKV_MAX_QUERY_TOKENS 128
+
+/*
+ * Decode with T >= 1 new query tokens per sequence (T = 1 is
+ * pkv_paged_decode): the verification step of speculative decoding, where
+ * the target model checks T proposed tokens in one pass over the shared
+ * cache ([PC] "How does speculative decoding interact with KV-cache
+ * compression?"), and small prefill chunks over a paged cache ([BW]
+ * "Continuous Batching", chunked prefill).  The T new tokens' K and V must
+ * already be in the cache as the last T of the context_lens[b] tokens;
+ * query token t (0..T-1) sits at position n - T + t (n = context_lens[b])
+ * and attends causally to positions 0 .. n - T + t:
+ *   out[b][t][h][:] = sum_j softmax_j(scale * q[b][t][h] . K_j) V_j,
+ *   j = 0 .. n - T + t.
+ * Rows with no position to attend to (n - T + t < 0, including n = 0) get
+ * zeros.
+ *
+ *   q, out         device bf16 [B][T][Hq][D] (must not overlap).
+ *   workspace      pkv_decode_multi_workspace_bytes() bytes.
+ *   everything else as in pkv_paged_decode.
+ * The tensor-core back-end only (PKV_MATH_FFMA with T > 1 gives
+ * PKV_ERR_UNSUPPORTED).  The (query token, head) rows of one KV head form
+ * row tiles of at most 16 rows (whole query tokens per tile); each tile is
+ * a separate stream over the pages, so G * T <= 16 reads the cache once.
+ */
+pkv_status pkv_paged_decode_multi(const pkv_cache_desc* cache,
+                                  const void* q, int32_t batch, int32_t num_query_tokens,
+                                  int32_t num_q_heads,
+                                  const void* k_cache, const void* v_cache,
+                                  const float* k_scale, const float* v_scale,
+                                  const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                  const int32_t* context_lens,
+                                  const int32_t* kv_group_ptr, int32_t num_layers, int32_t layer,
+                                  float scale, void* out,
+                                  void* workspace, size_t workspace_bytes,
+                                  const pkv_decode_opts* opts, void* stream);
+
+/* Workspace bytes and launch plan of pkv_paged_decode_multi (0 / an error
+ * status for invalid arguments), as for the single-token calls. */
+size_t pkv_decode_multi_workspace_bytes(const pkv_cache_desc* cache, int32_t batch,
+                                        int32_t num_query_tokens, int32_t num_q_heads,
+                                        int32_t max_blocks_per_seq, const pkv_decode_opts* opts);
+pkv_status pkv_decode_multi_describe(const pkv_cache_desc* cache, int32_t batch,
+                                     int32_t num_query_tokens, int32_t num_q_heads,
+                                     int32_t max_blocks_per_seq, const pkv_decode_opts* opts,
+                                     pkv_decode_plan* plan);
 
 /* Size of the library's built-in decode workspace (see below). */
 #define PKV_STATIC_WORKSPACE_MAX_BYTES ((size_t)16 << 20)

@@ -76,6 +76,10 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.pkv_oracle_paged_decode.argtypes = [P, i32, i32, P, P, i32, P, P,
                                             i32, i32, i32, i32, i32,
                                             P, i32, P, P, i32, i32, f32, P, P, i32]
+    lib.pkv_oracle_paged_decode_multi.restype = ctypes.c_int
+    lib.pkv_oracle_paged_decode_multi.argtypes = [P, i32, i32, i32, P, P, i32, P, P,
+                                                  i32, i32, i32, i32, i32,
+                                                  P, i32, P, P, i32, i32, f32, P, P, i32]
     lib.pkv_oracle_int8_encode.restype = ctypes.c_int8
     lib.pkv_oracle_int8_encode.argtypes = [f32, f32, f32]
     lib.pkv_oracle_int8_decode.restype = ctypes.c_double
@@ -217,6 +221,41 @@ def paged_decode(q_bits, k_cache, v_cache, block_tables, context_lens, kv_group_
         0 if pr is None else int(pr.shape[0]))
     if rc != ORACLE_OK:
         raise ValueError(f"oracle paged_decode status {rc}")
+    return out
+
+
+def paged_decode_multi(q_bits, k_cache, v_cache, block_tables, context_lens, kv_group_ptr,
+                       layer: int, scale: float, k_scale=None, v_scale=None,
+                       rows=None, lib=None) -> np.ndarray:
+    """float64 [B][T][Hq][D] output of a T-token query step (query token t of
+    sequence b attends to its first context_lens[b] - T + t + 1 cached
+    tokens; see pkv_oracle.c).  ``rows``: optional int array [n][3] of
+    (b, t, h) to compute; other entries of the result are NaN."""
+    q = _c(q_bits, np.uint16)
+    B, T, Hq, D = q.shape
+    kind = _kind(k_cache)
+    fp8 = kind != 0
+    kc = _c(k_cache, k_cache.dtype)
+    vc = _c(v_cache, v_cache.dtype)
+    S, NB, Hkv, bs, Dc = kc.shape
+    assert Dc == D
+    bt = _c(block_tables, np.int32)
+    cl = _c(context_lens, np.int32)
+    gp = _c(kv_group_ptr, np.int32)
+    ks = _c(k_scale, np.float32) if fp8 else None
+    vs = _c(v_scale, np.float32) if fp8 else None
+    out = np.full((B, T, Hq, D), np.nan if rows is not None else 0.0, dtype=np.float64)
+    pr = None
+    if rows is not None:
+        r = np.asarray(rows, dtype=np.int64).reshape(-1, 3)
+        pr = np.unique(np.stack([r[:, 0], r[:, 1] * Hq + r[:, 2]], axis=1).astype(np.int32), axis=0)
+    rc = _load(lib).pkv_oracle_paged_decode_multi(
+        _ptr(q), B, T, Hq, _ptr(kc), _ptr(vc), kind, _ptr(ks), _ptr(vs),
+        S, NB, Hkv, bs, D, _ptr(bt), int(bt.shape[1]), _ptr(cl), _ptr(gp), int(gp.shape[0]),
+        int(layer), float(np.float32(scale)), _ptr(out), _ptr(pr),
+        0 if pr is None else int(pr.shape[0]))
+    if rc != ORACLE_OK:
+        raise ValueError(f"oracle paged_decode_multi status {rc}")
     return out
 
 

@@ -233,33 +233,43 @@ static double cache_value(const void* cache, int32_t kind, const float* scales,
 }
 
 /*
- * One decode step for one layer.
- *   q            bf16 bits [B][Hq][D]
+ * One decode step for one layer, T >= 1 new query tokens per sequence.
+ *   q            bf16 bits [B][T][Hq][D]
  *   k/v_cache    [S][NB][Hkv][bs][D], bf16 bits, E4M3 codes or INT8 codes
  *   k/v_scale    fp32 [S][NB][Hkv] (E4M3) or [S][NB][Hkv][2] (INT8: scale, zero)
  *   block_tables int32 [B][MB]; context_lens int32 [B]
  *   kv_group_ptr int32 [L]: cache slot read by layer l (shared-with pointer)
- *   out          double [B][Hq][D]
- *   pairs        optional int32 [npairs][2] list of distinct (b, h) to compute
- *                (the others are left untouched); NULL computes every pair.
- * For each (b, h) with n = context_lens[b] tokens (n == 0 gives zeros):
- *   K_t = K[slot][table[b][t / bs]][h / G][t % bs][:], t = 0 .. n-1 (V alike)
- *   s_t = double(scale) * sum_d double(q[b][h][d]) * K_t[d]
- *   out = sum_t exp(s_t - max s) V_t / sum_t exp(s_t - max s)
+ *   out          double [B][T][Hq][D]
+ *   pairs        optional int32 [npairs][2] list of distinct (b, r), r = t*Hq + h,
+ *                to compute (the others are left untouched); NULL computes all.
+ * The T new tokens are the last T of the n = context_lens[b] cached tokens
+ * (already appended): query token t sits at position n - T + t and attends
+ * to positions 0 .. n - T + t (causal among the new tokens).  Row (b, t, h)
+ * with m = n - T + t + 1 keys (m <= 0 gives zeros):
+ *   K_j = K[slot][table[b][j / bs]][h / G][j % bs][:], j = 0 .. m-1 (V alike)
+ *   s_j = double(scale) * sum_d double(q[b][t][h][d]) * K_j[d]
+ *   out = sum_j exp(s_j - max s) V_j / sum_j exp(s_j - max s)
+ * T = 1 is single-token decode.  Sources: "KV Cache Engineering:
+ * PagedAttention, Continuous Batching, Attention Variants, and the Bandwidth
+ * Wall", "What the KV Cache Stores and Why" and "PagedAttention"; the T > 1
+ * reading follows "KV-Cache Engineering: Paged Attention, Prefix Cache,
+ * Disaggregation (2026)", speculative decoding (the target checks the
+ * draft's proposed tokens in one parallel pass over the shared cache).
  * Returns ORACLE_BAD_BLOCK / ORACLE_BAD_CTX if a table entry that would be
  * read or a context length is out of range (nothing is read out of bounds).
  */
-int pkv_oracle_paged_decode(const uint16_t* q, int32_t B, int32_t Hq,
-                            const void* k_cache, const void* v_cache,
-                            int32_t fp8 /* element kind: 0 bf16, 1 E4M3, 2 INT8 */,
-                            const float* k_scale, const float* v_scale,
-                            int32_t S, int32_t NB, int32_t Hkv, int32_t bs, int32_t D,
-                            const int32_t* block_tables, int32_t MB,
-                            const int32_t* context_lens,
-                            const int32_t* kv_group_ptr, int32_t L, int32_t layer,
-                            float scale, double* out,
-                            const int32_t* pairs, int32_t npairs) {
-  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || bs <= 0 || D <= 0 || MB <= 0) return ORACLE_BAD_ARG;
+int pkv_oracle_paged_decode_multi(const uint16_t* q, int32_t B, int32_t T, int32_t Hq,
+                                  const void* k_cache, const void* v_cache,
+                                  int32_t fp8 /* element kind: 0 bf16, 1 E4M3, 2 INT8 */,
+                                  const float* k_scale, const float* v_scale,
+                                  int32_t S, int32_t NB, int32_t Hkv, int32_t bs, int32_t D,
+                                  const int32_t* block_tables, int32_t MB,
+                                  const int32_t* context_lens,
+                                  const int32_t* kv_group_ptr, int32_t L, int32_t layer,
+                                  float scale, double* out,
+                                  const int32_t* pairs, int32_t npairs) {
+  if (B < 0 || T <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || bs <= 0 || D <= 0 || MB <= 0)
+    return ORACLE_BAD_ARG;
   if (layer < 0 || layer >= L) return ORACLE_BAD_ARG;
   const int32_t slot = kv_group_ptr[layer];
   if (slot < 0 || slot >= S) return ORACLE_BAD_ARG;
@@ -272,7 +282,8 @@ int pkv_oracle_paged_decode(const uint16_t* q, int32_t B, int32_t Hq,
       if (blk < 0 || blk >= NB) return ORACLE_BAD_BLOCK;
     }
   }
-  const int64_t total = (pairs != NULL) ? npairs : (int64_t)B * Hq;
+  const int32_t rows = T * Hq; /* query rows per sequence */
+  const int64_t total = (pairs != NULL) ? npairs : (int64_t)B * rows;
   int32_t maxn = 0;
   for (int32_t b = 0; b < B; ++b) if (context_lens[b] > maxn) maxn = context_lens[b];
 
@@ -286,48 +297,64 @@ int pkv_oracle_paged_decode(const uint16_t* q, int32_t B, int32_t Hq,
 #pragma omp for schedule(dynamic, 1)
 #endif
     for (int64_t w = 0; w < total; ++w) {
-      int32_t b = (pairs != NULL) ? pairs[2 * w] : (int32_t)(w / Hq);
-      int32_t h = (pairs != NULL) ? pairs[2 * w + 1] : (int32_t)(w % Hq);
+      int32_t b = (pairs != NULL) ? pairs[2 * w] : (int32_t)(w / rows);
+      int32_t r = (pairs != NULL) ? pairs[2 * w + 1] : (int32_t)(w % rows);
+      int32_t t = r / Hq, h = r % Hq;
       int32_t g = h / G;
-      int32_t n = context_lens[b];
-      double* o = out + ((int64_t)b * Hq + h) * D;
-      const uint16_t* qv = q + ((int64_t)b * Hq + h) * D;
+      int32_t m = context_lens[b] - T + t + 1; /* keys this query token sees */
+      double* o = out + ((int64_t)b * rows + r) * D;
+      const uint16_t* qv = q + ((int64_t)b * rows + r) * D;
       for (int32_t d = 0; d < D; ++d) acc[d] = 0.0;
-      if (n == 0) {
+      if (m <= 0) {
         for (int32_t d = 0; d < D; ++d) o[d] = 0.0;
         continue;
       }
       /* logits over the gathered logical sequence */
       double smax = -INFINITY;
-      for (int32_t t = 0; t < n; ++t) {
-        int32_t blk = block_tables[(int64_t)b * MB + t / bs];
+      for (int32_t j = 0; j < m; ++j) {
+        int32_t blk = block_tables[(int64_t)b * MB + j / bs];
         int64_t page = ((int64_t)slot * NB + blk) * Hkv + g;
         double dot = 0.0;
         for (int32_t d = 0; d < D; ++d)
-          dot += bf16_bits_to_double(qv[d]) * cache_value(k_cache, fp8, k_scale, page, bs, D, t % bs, d);
-        s[t] = (double)scale * dot;
-        if (s[t] > smax) smax = s[t];
+          dot += bf16_bits_to_double(qv[d]) * cache_value(k_cache, fp8, k_scale, page, bs, D, j % bs, d);
+        s[j] = (double)scale * dot;
+        if (s[j] > smax) smax = s[j];
       }
       /* softmax weights and the weighted sum of values */
       double z = 0.0;
-      for (int32_t t = 0; t < n; ++t) {
-        s[t] = exp(s[t] - smax);
-        z += s[t];
+      for (int32_t j = 0; j < m; ++j) {
+        s[j] = exp(s[j] - smax);
+        z += s[j];
       }
-      for (int32_t t = 0; t < n; ++t) {
-        int32_t blk = block_tables[(int64_t)b * MB + t / bs];
+      for (int32_t j = 0; j < m; ++j) {
+        int32_t blk = block_tables[(int64_t)b * MB + j / bs];
         int64_t page = ((int64_t)slot * NB + blk) * Hkv + g;
-        double p = s[t] / z;
+        double p = s[j] / z;
         for (int32_t d = 0; d < D; ++d)
-          acc[d] += p * cache_value(v_cache, fp8, v_scale, page, bs, D, t % bs, d);
+          acc[d] += p * cache_value(v_cache, fp8, v_scale, page, bs, D, j % bs, d);
       }
-      /* the row is stored once, so a (b, h) listed twice cannot interleave */
+      /* the row is stored once, so a (b, r) listed twice cannot interleave */
       for (int32_t d = 0; d < D; ++d) o[d] = acc[d];
     }
     free(acc);
     free(s);
   }
   return ORACLE_OK;
+}
+
+/* Single-token decode: T = 1, pairs are (b, h). */
+int pkv_oracle_paged_decode(const uint16_t* q, int32_t B, int32_t Hq,
+                            const void* k_cache, const void* v_cache, int32_t fp8,
+                            const float* k_scale, const float* v_scale,
+                            int32_t S, int32_t NB, int32_t Hkv, int32_t bs, int32_t D,
+                            const int32_t* block_tables, int32_t MB,
+                            const int32_t* context_lens,
+                            const int32_t* kv_group_ptr, int32_t L, int32_t layer,
+                            float scale, double* out,
+                            const int32_t* pairs, int32_t npairs) {
+  return pkv_oracle_paged_decode_multi(q, B, 1, Hq, k_cache, v_cache, fp8, k_scale, v_scale, S, NB,
+                                       Hkv, bs, D, block_tables, MB, context_lens, kv_group_ptr, L,
+                                       layer, scale, out, pairs, npairs);
 }
 
 /* ------------------------------------------------------------------------ */

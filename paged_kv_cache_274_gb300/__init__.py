@@ -57,7 +57,11 @@ class DecodePlan(ctypes.Structure):
     _fields_ = [("partition_blocks", ctypes.c_int32), ("max_partitions", ctypes.c_int32),
                 ("math", ctypes.c_int32), ("warps_per_cta", ctypes.c_int32),
                 ("stages", ctypes.c_int32), ("kernels_per_call", ctypes.c_int32),
-                ("workspace_bytes", ctypes.c_size_t), ("smem_bytes_per_cta", ctypes.c_size_t)]
+                ("workspace_bytes", ctypes.c_size_t), ("smem_bytes_per_cta", ctypes.c_size_t),
+                ("query_tokens_per_tile", ctypes.c_int32), ("row_tiles", ctypes.c_int32)]
+
+MAX_QUERY_TOKENS = 128
+ABI_VERSION = 2
 
 
 _lib = None
@@ -89,6 +93,14 @@ def load() -> ctypes.CDLL:
         lib.pkv_paged_decode.restype = ctypes.c_int
         lib.pkv_paged_decode.argtypes = [pdesc, P, i32, i32, P, P, P, P, P, i32, P, P, i32, i32,
                                          f32, P, P, sz, popts, P]
+        lib.pkv_decode_multi_workspace_bytes.restype = sz
+        lib.pkv_decode_multi_workspace_bytes.argtypes = [pdesc, i32, i32, i32, i32, popts]
+        lib.pkv_decode_multi_describe.restype = ctypes.c_int
+        lib.pkv_decode_multi_describe.argtypes = [pdesc, i32, i32, i32, i32, popts,
+                                                  ctypes.POINTER(DecodePlan)]
+        lib.pkv_paged_decode_multi.restype = ctypes.c_int
+        lib.pkv_paged_decode_multi.argtypes = [pdesc, P, i32, i32, i32, P, P, P, P, P, i32, P, P, i32,
+                                               i32, f32, P, P, sz, popts, P]
         lib.pkv_paged_decode_static_workspace.restype = ctypes.c_int
         lib.pkv_paged_decode_static_workspace.argtypes = [pdesc, P, i32, i32, P, P, P, P, P, i32, P,
                                                           P, i32, i32, f32, P, popts, P]
@@ -102,6 +114,9 @@ def load() -> ctypes.CDLL:
         lib.pkv_last_error_message.argtypes = []
         lib.pkv_abi_version.restype = ctypes.c_int32
         lib.pkv_abi_version.argtypes = []
+        if lib.pkv_abi_version() != ABI_VERSION:
+            raise RuntimeError(f"{LIB_PATH} has ABI version {lib.pkv_abi_version()}, "
+                               f"this binding needs {ABI_VERSION}: rebuild")
         _lib = lib
         return lib
 
@@ -192,32 +207,35 @@ def decode_opts(partition_blocks: int = 0, math: int = MATH_AUTO, warps: int = 0
 
 
 def decode_workspace_bytes(k_cache: torch.Tensor, batch: int, num_q_heads: int,
-                           max_blocks_per_seq: int, opts: Optional[DecodeOpts] = None) -> int:
+                           max_blocks_per_seq: int, opts: Optional[DecodeOpts] = None,
+                           query_tokens: int = 1) -> int:
     desc = cache_desc(k_cache)
-    n = load().pkv_decode_workspace_bytes(ctypes.byref(desc), int(batch), int(num_q_heads),
-                                          int(max_blocks_per_seq),
-                                          ctypes.byref(opts) if opts is not None else None)
+    n = load().pkv_decode_multi_workspace_bytes(ctypes.byref(desc), int(batch), int(query_tokens),
+                                                int(num_q_heads), int(max_blocks_per_seq),
+                                                ctypes.byref(opts) if opts is not None else None)
     if n == 0:
         raise PkvError(1, "bad arguments for the decode workspace")
     return int(n)
 
 
 def decode_plan(k_cache: torch.Tensor, batch: int, num_q_heads: int, max_blocks_per_seq: int,
-                opts: Optional[DecodeOpts] = None) -> dict:
+                opts: Optional[DecodeOpts] = None, query_tokens: int = 1) -> dict:
     """The resolved launch plan of a decode call (host only, nothing launched)."""
     desc = cache_desc(k_cache)
     plan = DecodePlan()
-    _check(load().pkv_decode_describe(ctypes.byref(desc), int(batch), int(num_q_heads),
-                                      int(max_blocks_per_seq),
-                                      ctypes.byref(opts) if opts is not None else None,
-                                      ctypes.byref(plan)))
+    _check(load().pkv_decode_multi_describe(ctypes.byref(desc), int(batch), int(query_tokens),
+                                            int(num_q_heads), int(max_blocks_per_seq),
+                                            ctypes.byref(opts) if opts is not None else None,
+                                            ctypes.byref(plan)))
     return {f: getattr(plan, f) for f, _ in DecodePlan._fields_}
 
 
 def new_decode_workspace(k_cache: torch.Tensor, batch: int, num_q_heads: int,
-                         max_blocks_per_seq: int, opts: Optional[DecodeOpts] = None) -> torch.Tensor:
-    """Zero-filled device workspace for :func:`paged_decode`."""
-    n = decode_workspace_bytes(k_cache, batch, num_q_heads, max_blocks_per_seq, opts)
+                         max_blocks_per_seq: int, opts: Optional[DecodeOpts] = None,
+                         query_tokens: int = 1) -> torch.Tensor:
+    """Zero-filled device workspace for :func:`paged_decode` (or, with
+    ``query_tokens`` T, :func:`paged_decode_multi`)."""
+    n = decode_workspace_bytes(k_cache, batch, num_q_heads, max_blocks_per_seq, opts, query_tokens)
     return torch.zeros(n, dtype=torch.uint8, device=k_cache.device)
 
 
@@ -252,6 +270,47 @@ def paged_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
         scale = D ** -0.5
     _check(load().pkv_paged_decode(
         ctypes.byref(desc), _ptr(q), B, Hq, _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+        _ptr(v_scale), _ptr(block_tables), MB, _ptr(context_lens), gp, len(kv_group_ptr),
+        int(layer), float(scale), _ptr(out), _ptr(workspace), int(workspace.numel()),
+        ctypes.byref(opts) if opts is not None else None, _stream_handle(stream)))
+    return out
+
+
+def paged_decode_multi(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                       block_tables: torch.Tensor, context_lens: torch.Tensor,
+                       kv_group_ptr: Sequence[int] = (0,), layer: int = 0,
+                       scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                       workspace: Optional[torch.Tensor] = None,
+                       k_scale: Optional[torch.Tensor] = None, v_scale: Optional[torch.Tensor] = None,
+                       opts: Optional[DecodeOpts] = None, stream=None) -> torch.Tensor:
+    """T new query tokens per sequence, q [B][T][Hq][D] (bf16), already
+    appended as the last T cached tokens; token t attends causally to the
+    first context_lens[b] - T + t + 1 tokens.  Returns out [B][T][Hq][D]."""
+    desc = cache_desc(k_cache)
+    _need_cuda("q", q, torch.bfloat16)
+    _need_cuda("k_cache", k_cache)
+    _need_cuda("v_cache", v_cache, k_cache.dtype)
+    _need_cuda("block_tables", block_tables, torch.int32)
+    _need_cuda("context_lens", context_lens, torch.int32)
+    if q.dim() != 4:
+        raise PkvError(1, "q must be [B][T][Hq][D]")
+    B, T, Hq, D = (int(x) for x in q.shape)
+    if D != desc.head_dim or block_tables.dim() != 2 or block_tables.shape[0] != B:
+        raise PkvError(1, "q / block_tables shapes do not match the cache")
+    MB = int(block_tables.shape[1])
+    if out is None:
+        out = torch.empty_like(q)
+    _need_cuda("out", out, torch.bfloat16)
+    if desc.dtype != KV_BF16:
+        _need_page_params(desc, k_scale, "k_scale")
+        _need_page_params(desc, v_scale, "v_scale")
+    if workspace is None:
+        workspace = new_decode_workspace(k_cache, B, Hq, MB, opts, T)
+    gp = (ctypes.c_int32 * len(kv_group_ptr))(*[int(x) for x in kv_group_ptr])
+    if scale is None:
+        scale = D ** -0.5
+    _check(load().pkv_paged_decode_multi(
+        ctypes.byref(desc), _ptr(q), B, T, Hq, _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
         _ptr(v_scale), _ptr(block_tables), MB, _ptr(context_lens), gp, len(kv_group_ptr),
         int(layer), float(scale), _ptr(out), _ptr(workspace), int(workspace.numel()),
         ctypes.byref(opts) if opts is not None else None, _stream_handle(stream)))

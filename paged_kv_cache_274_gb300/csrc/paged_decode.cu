@@ -26,6 +26,8 @@ const void* decode_kernel_bf16_d64(int bs, int math, int gt);
 const void* decode_kernel_bf16_d128(int bs, int math, int gt);
 const void* decode_kernel_fp8_d128(int bs, int math, int gt);
 const void* decode_kernel_int8_d128(int bs, int math, int gt);
+const void* decode_kernel_mt_bf16(int D, int bs, int gt);
+const void* decode_kernel_mt_1byte(int kv_dtype, int bs, int gt);
 
 // ---------------------------------------------------------------------------
 // planner: one CTA validates context lengths, counts each sequence's
@@ -41,9 +43,10 @@ constexpr int kPlanThreads = 1024;
 constexpr int kFusedMergeMaxParts = 4;
 
 __global__ void __launch_bounds__(kPlanThreads)
-    plan_kernel(const int32_t* __restrict__ context_lens, int B, int Hkv, int max_ctx,
-                int tokens_per_part, int32_t* work_counter, int32_t* unit_start, int32_t* ctx_eff,
-                int32_t* arrive, __nv_bfloat16* out, int row_elems /* Hq * D */, unsigned* err) {
+    plan_kernel(const int32_t* __restrict__ context_lens, int B, int num_arrive /* B * Hkv * NT */,
+                int max_ctx, int tokens_per_part, int32_t* work_counter, int32_t* unit_start,
+                int32_t* ctx_eff, int32_t* arrive, __nv_bfloat16* out,
+                int row_elems /* T * Hq * D */, unsigned* err) {
   __shared__ int warp_tot[kPlanThreads / 32];
   __shared__ int carry_s;
   pdl_trigger();
@@ -93,7 +96,7 @@ __global__ void __launch_bounds__(kPlanThreads)
     unit_start[B] = carry_s;
     *work_counter = 0;
   }
-  for (int i = tid; i < B * Hkv; i += kPlanThreads) arrive[i] = 0;
+  for (int i = tid; i < num_arrive; i += kPlanThreads) arrive[i] = 0;
   if (__syncthreads_or(bad_any) && tid == 0) atomicOr(err, PKV_DEVERR_CONTEXT_LEN);
   // zeros for inactive sequences (one warp per sequence)
   for (int b = warp; b < B; b += kPlanThreads / 32) {
@@ -104,7 +107,8 @@ __global__ void __launch_bounds__(kPlanThreads)
 }
 
 // ---------------------------------------------------------------------------
-// merge kernel (many partitions): one CTA per (sequence, query head); thread
+// merge kernel (many partitions): one CTA per (sequence, query token, query
+// head) row; thread
 // (pg, dg) owns 4 columns of head_dim and partitions pg, pg + kPG, ...  It
 // folds its partitions in one pass with a running maximum, then the kPG
 // partial results are combined through shared memory:
@@ -115,16 +119,16 @@ constexpr int kMergeThreads = 128;
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads)
     merge_kernel(const float* __restrict__ part_ml, const float* __restrict__ part_o,
-                 const int32_t* __restrict__ unit_start, int Hq, int pmax,
-                 __nv_bfloat16* __restrict__ out) {
+                 const int32_t* __restrict__ unit_start, int rows_per_seq /* T * Hq */,
+                 int pmax, __nv_bfloat16* __restrict__ out) {
   constexpr int kDG = D / 4;                  // threads along head_dim
   constexpr int kPG = kMergeThreads / kDG;    // partition groups
   __shared__ float4 s_acc[kPG][kDG];
   __shared__ float s_m[kPG][kDG], s_l[kPG][kDG];
   pdl_trigger();
   pdl_wait();
-  const int bh = blockIdx.x;
-  const int b = bh / Hq;
+  const int bh = blockIdx.x;  // row (b * T + t) * Hq + h
+  const int b = bh / rows_per_seq;
   const int P = unit_start[b + 1] - unit_start[b];
   if (P < 2) return;  // written by the decode kernel (or zero-filled by the planner)
   const int tid = threadIdx.x;
@@ -179,7 +183,7 @@ __global__ void __launch_bounds__(kMergeThreads)
 // ---------------------------------------------------------------------------
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-WorkspaceLayout workspace_layout(int B, int Hq, int Hkv, int D, int pmax) {
+WorkspaceLayout workspace_layout(int B, int T, int Hq, int Hkv, int NT, int D, int pmax) {
   WorkspaceLayout w{};
   size_t off = 0;
   w.counter = off;
@@ -189,8 +193,8 @@ WorkspaceLayout workspace_layout(int B, int Hq, int Hkv, int D, int pmax) {
   w.ctx_eff = off;
   off = align_up(off + sizeof(int32_t) * static_cast<size_t>(B), 256);
   w.arrive = off;
-  off = align_up(off + sizeof(int32_t) * static_cast<size_t>(B) * Hkv, 256);
-  const size_t parts = pmax > 1 ? static_cast<size_t>(B) * Hq * pmax : 0;
+  off = align_up(off + sizeof(int32_t) * static_cast<size_t>(B) * Hkv * NT, 256);
+  const size_t parts = pmax > 1 ? static_cast<size_t>(B) * T * Hq * pmax : 0;
   w.part_ml = off;
   off = align_up(off + sizeof(float) * 2 * parts, 256);
   w.part_o = off;
@@ -211,8 +215,12 @@ size_t decode_smem_bytes(int kv_fp8, int D, int bs, int warps, int stages) {
                   : decode_smem_layout_bytes<128, 32, false>(warps, stages);
 }
 
-static const void* pick_kernel(int kv_dtype, int D, int bs, int math, int G) {
-  const int gt = G;
+// gt: query rows per tile; mt: multi-token kernel (T > 1).
+static const void* pick_kernel(int kv_dtype, int D, int bs, int math, int gt, bool mt) {
+  if (mt) {
+    if (math != PKV_MATH_MMA) return nullptr;
+    return kv_dtype == PKV_KV_BF16 ? decode_kernel_mt_bf16(D, bs, gt) : decode_kernel_mt_1byte(kv_dtype, bs, gt);
+  }
   if (kv_dtype == PKV_KV_INT8) return decode_kernel_int8_d128(bs, math, gt);
   if (kv_dtype == PKV_KV_FP8_E4M3) return decode_kernel_fp8_d128(bs, math, gt);
   if (D == 64) return decode_kernel_bf16_d64(bs, math, gt);
@@ -268,7 +276,7 @@ static cudaError_t ctas_per_sm(const void* fn, int threads, size_t smem, int* ou
 }
 
 int decode_ctas_per_sm(const DecodeLaunch& L, size_t smem) {
-  const void* fn = pick_kernel(L.kv_dtype, L.D, L.bs, L.math, L.G);
+  const void* fn = pick_kernel(L.kv_dtype, L.D, L.bs, L.math, L.G * L.Tt, L.T > 1);
   int n = 0;
   if (fn == nullptr || ctas_per_sm(fn, L.warps * 32, smem, &n) != cudaSuccess) return 0;
   return n;
@@ -276,7 +284,7 @@ int decode_ctas_per_sm(const DecodeLaunch& L, size_t smem) {
 
 cudaError_t launch_decode(const DecodeLaunch& L, int* launched) {
   *launched = 0;
-  const void* fn = pick_kernel(L.kv_dtype, L.D, L.bs, L.math, L.G);
+  const void* fn = pick_kernel(L.kv_dtype, L.D, L.bs, L.math, L.G * L.Tt, L.T > 1);
   if (fn == nullptr) return cudaErrorInvalidDeviceFunction;
   const size_t smem = decode_smem_bytes(L.kv_fp8, L.D, L.bs, L.warps, L.stages);
   int per_sm = 0;
@@ -297,15 +305,15 @@ cudaError_t launch_decode(const DecodeLaunch& L, int* launched) {
     cfg.stream = L.stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, plan_kernel, L.context_lens, L.B, L.Hkv, L.MB * L.bs, L.ppu * L.bs,
-                           L.work_counter, L.unit_start, L.ctx_eff, L.arrive,
-                           static_cast<__nv_bfloat16*>(L.out), L.Hq * L.D, L.err);
+    e = cudaLaunchKernelEx(&cfg, plan_kernel, L.context_lens, L.B, L.B * L.Hkv * L.NT, L.MB * L.bs,
+                           L.ppu * L.bs, L.work_counter, L.unit_start, L.ctx_eff, L.arrive,
+                           static_cast<__nv_bfloat16*>(L.out), L.T * L.Hq * L.D, L.err);
     if (e != cudaSuccess) return e;
     *launched += 1;
   }
 
   // 2. decode: persistent grid, at most one warp per possible unit
-  const long long max_units = static_cast<long long>(L.B) * L.Hkv * L.pmax;
+  const long long max_units = static_cast<long long>(L.B) * L.Hkv * L.NT * L.pmax;
   long long grid = static_cast<long long>(L.num_sms) * per_sm;
   grid = std::min(grid, (max_units + L.warps - 1) / L.warps);
   grid = std::max(grid, 1LL);
@@ -327,6 +335,9 @@ cudaError_t launch_decode(const DecodeLaunch& L, int* launched) {
   p.Hq = L.Hq;
   p.Hkv = L.Hkv;
   p.G = L.G;
+  p.T = L.T;
+  p.Tt = L.Tt;
+  p.NT = L.NT;
   p.MB = L.MB;
   p.NB = L.NB;
   p.pmax = L.pmax;
@@ -355,7 +366,7 @@ cudaError_t launch_decode(const DecodeLaunch& L, int* launched) {
   // 3. merge kernel when sequences may span many partitions
   if (!p.fused_merge) {
     cudaLaunchConfig_t mc{};
-    mc.gridDim = dim3(static_cast<unsigned>(L.B * L.Hq));
+    mc.gridDim = dim3(static_cast<unsigned>(L.B * L.T * L.Hq));
     mc.blockDim = dim3(kMergeThreads);
     mc.dynamicSmemBytes = 0;
     mc.stream = L.stream;
@@ -364,11 +375,11 @@ cudaError_t launch_decode(const DecodeLaunch& L, int* launched) {
     if (L.D == 64)
       e = cudaLaunchKernelEx(&mc, merge_kernel<64>, static_cast<const float*>(L.part_ml),
                              static_cast<const float*>(L.part_o), static_cast<const int32_t*>(L.unit_start),
-                             L.Hq, L.pmax, static_cast<__nv_bfloat16*>(L.out));
+                             L.T * L.Hq, L.pmax, static_cast<__nv_bfloat16*>(L.out));
     else
       e = cudaLaunchKernelEx(&mc, merge_kernel<128>, static_cast<const float*>(L.part_ml),
                              static_cast<const float*>(L.part_o), static_cast<const int32_t*>(L.unit_start),
-                             L.Hq, L.pmax, static_cast<__nv_bfloat16*>(L.out));
+                             L.T * L.Hq, L.pmax, static_cast<__nv_bfloat16*>(L.out));
     if (e != cudaSuccess) return e;
     *launched += 1;
   }

@@ -10,9 +10,15 @@
 // "Two Costs: Capacity and Bandwidth" (every step streams the whole cache,
 // so the kernel is bound by HBM bandwidth).
 //
+// Multi-token queries: T >= 1 new query tokens per sequence (speculative
+// decoding's verification step, "KV-Cache Engineering: Paged Attention,
+// Prefix Cache, Disaggregation (2026)"), already appended as the last T
+// cached tokens; query token t attends to positions 0 .. ctx - T + t.
+//
 // Structure
-//   * Work unit = (sequence b, KV head, partition p): a run of up to `ppu`
-//     consecutive logical blocks.  Units are handed out one at a time from a
+//   * Work unit = (sequence b, KV head, row tile, partition p): a run of up
+//     to `ppu` consecutive logical blocks.  A row tile is up to 16 query
+//     rows (query token, head of the group); T = 1 has one tile of G rows.  Units are handed out one at a time from a
 //     global counter to warps of a persistent grid (each warp is an
 //     independent streamer: no cross-warp synchronisation).
 //   * Each warp owns a ring of `stages` shared-memory stages.  Lane 0 reads
@@ -54,10 +60,29 @@ struct DecodeParams {
   int32_t* arrive;  // [B][Hkv] partitions finished so far (zeroed by the planner)
   unsigned* err;
   int B, Hq, Hkv, G, MB, NB, pmax, ppu, stages;
+  int T, Tt, NT;  // query tokens per sequence, per row tile; row tiles
   int fused_merge;  // 1: the last warp of a (sequence, KV head) merges; 0: the merge kernel does
   int row_base;
   float scale_log2;
 };
+
+// Query row `row` (0..15) of row tile `tile` of KV head `kvh`: query token
+// t = tile * Tt + row / G, query head h = kvh * G + row % G.  False for rows
+// past the tile's tokens.  The row's offset in q, out and the partials is
+// (b * T + t) * Hq + h.  MT = false: single-token kernels (T = 1, one tile).
+template <bool MT>
+__device__ __forceinline__ bool tile_row(const DecodeParams& p, int kvh, int tile, int row, int& t,
+                                         int& h) {
+  if constexpr (!MT) {
+    t = 0;
+    h = kvh * p.G + row;
+    return row < p.G;
+  }
+  const int tl = row / p.G;
+  t = tile * p.Tt + tl;
+  h = kvh * p.G + (row - tl * p.G);
+  return tl < p.Tt && t < p.T;
+}
 
 template <int D, int BS, bool FP8>
 struct PageGeom {
@@ -114,19 +139,26 @@ __device__ __forceinline__ void mma_rows(float (&d)[N], const uint32_t (&a)[N], 
   }
 }
 
-template <int D, int BS, bool FP8, bool HI>
-__device__ __forceinline__ void mma_load_q(MmaState<D, BS, FP8, HI>& st, const __nv_bfloat16* qg,
-                                           int G, int lane) {
+template <int D, int BS, bool FP8, bool HI, bool MT>
+__device__ __forceinline__ void mma_load_q(MmaState<D, BS, FP8, HI>& st, const DecodeParams& p,
+                                           int b, int kvh, int tile, int lane) {
   constexpr int kR = HI ? 2 : 1;
   const int g = lane >> 2, tig = lane & 3;
+  const __nv_bfloat16* qrow[kR];
+#pragma unroll
+  for (int half = 0; half < kR; ++half) {
+    int t, h;
+    qrow[half] = tile_row<MT>(p, kvh, tile, g + 8 * half, t, h)
+                     ? p.q + (static_cast<size_t>(b * p.T + t) * p.Hq + h) * D
+                     : nullptr;
+  }
 #pragma unroll
   for (int s = 0; s < D / 16; ++s) {
 #pragma unroll
     for (int half = 0; half < kR; ++half) {
-      const int row = g + 8 * half;
       uint32_t lo = 0, hi = 0;
-      if (row < G) {
-        const __nv_bfloat16* qr = qg + static_cast<size_t>(row) * D;
+      if (qrow[half] != nullptr) {
+        const __nv_bfloat16* qr = qrow[half];
         if constexpr (!FP8) {
           // k = 2tig, 2tig+1 -> d = 16s + 2tig (+1); k + 8 -> d + 8
           lo = *reinterpret_cast<const uint32_t*>(qr + 16 * s + 2 * tig);
@@ -209,13 +241,17 @@ __device__ __forceinline__ void mma_int8_unbias(MmaState<D, BS, FP8, HI>& st) {
 }
 
 // One page (BS tokens) of the online softmax with tensor-core tiles.
-// `valid` = tokens of the page that belong to the sequence (0..BS); `sl` =
+// `valid` = tokens of the page that belong to the sequence (0..BS); `rv[r]`
+// = tokens of the page that query row g + 8r attends to (<= valid; below it
+// for the earlier tokens of a multi-token query); `partial` = some row of
+// the tile attends to fewer than BS tokens of the page (warp-uniform); `sl` =
 // softmax scale * log2(e) (* the page's K scale for one-byte pages);
 // `vscale` = the page's V scale (one-byte pages); `kc`, `vc` = the page's
 // INT8 biases 1152 + zero of K and V.
 template <int D, int BS, bool FP8, bool HI, bool I8>
 __device__ __forceinline__ void mma_page(MmaState<D, BS, FP8, HI>& st, uint8_t* stage, int valid,
-                                         float sl, float vscale, float kc, float vc, int lane) {
+                                         const int (&rv)[HI ? 2 : 1], bool partial, float sl,
+                                         float vscale, float kc, float vc, int lane) {
   using Geo = PageGeom<D, BS, FP8>;
   constexpr int kR = HI ? 2 : 1;
   constexpr int kC = 2 * kR;
@@ -256,7 +292,6 @@ __device__ __forceinline__ void mma_page(MmaState<D, BS, FP8, HI>& st, uint8_t* 
   }
 
   // ---- online softmax (log2 domain) ----
-  const bool partial = valid < BS;  // warp-uniform: only a sequence's last page
   // INT8: q . (K' - kc) = q . K' - kc * qs, folded into the scaling
   float kb[kR];
 #pragma unroll
@@ -270,7 +305,7 @@ __device__ __forceinline__ void mma_page(MmaState<D, BS, FP8, HI>& st, uint8_t* 
 #pragma unroll
       for (int e = 0; e < kC; ++e) {
         const int tok = qk_token<FP8>(nt, 2 * tig + (e & 1));
-        const float v = (tok < valid) ? fmaf(s[nt][e], sl, kb[e >> 1]) : -INFINITY;
+        const float v = (tok < rv[e >> 1]) ? fmaf(s[nt][e], sl, kb[e >> 1]) : -INFINITY;
         s[nt][e] = v;
         mx[e >> 1] = fmaxf(mx[e >> 1], v);
       }
@@ -352,7 +387,7 @@ __device__ __forceinline__ void mma_page(MmaState<D, BS, FP8, HI>& st, uint8_t* 
   // Rows of V past the sequence end may hold anything (E4M3 and bf16: even
   // NaN); P is 0 there but 0 * NaN is NaN, so clear them before the product.
   // Every INT8 byte is a finite value.
-  if (!I8 && partial) {
+  if (!I8 && valid < BS) {
     uint8_t* vp = stage + Geo::kTensorBytes;
     for (int idx = lane; idx < Geo::kTensorBytes / 16; idx += 32) {
       const int row = (idx % (Geo::kRegionBytes / 16)) / 8;
@@ -409,9 +444,9 @@ __device__ __forceinline__ void mma_page(MmaState<D, BS, FP8, HI>& st, uint8_t* 
   }
 }
 
-template <int D, int BS, bool FP8, bool HI>
+template <int D, int BS, bool FP8, bool HI, bool MT>
 __device__ __forceinline__ void mma_finish(MmaState<D, BS, FP8, HI>& st, const DecodeParams& p,
-                                           int b, int kvh, int pidx, int nparts, int lane) {
+                                           int b, int kvh, int tile, int pidx, int nparts, int lane) {
   constexpr int kR = HI ? 2 : 1;
   const int g = lane >> 2, tig = lane & 3;
 #pragma unroll
@@ -421,18 +456,18 @@ __device__ __forceinline__ void mma_finish(MmaState<D, BS, FP8, HI>& st, const D
   }
 #pragma unroll
   for (int r = 0; r < kR; ++r) {
-    const int row = g + 8 * r;
-    if (row >= p.G) continue;
-    const int h = kvh * p.G + row;
+    int t, h;
+    if (!tile_row<MT>(p, kvh, tile, g + 8 * r, t, h)) continue;
+    const size_t qrow = static_cast<size_t>(b * p.T + t) * p.Hq + h;
     if (nparts == 1) {
       const float inv = st.l[r] > 0.f ? 1.f / st.l[r] : 0.f;
-      __nv_bfloat16* o = p.out + (static_cast<size_t>(b) * p.Hq + h) * D;
+      __nv_bfloat16* o = p.out + qrow * D;
 #pragma unroll
       for (int n = 0; n < D / 8; ++n)
         *reinterpret_cast<__nv_bfloat162*>(o + 8 * n + 2 * tig) =
             __floats2bfloat162_rn(st.o[n][2 * r] * inv, st.o[n][2 * r + 1] * inv);
     } else {
-      const size_t slot = (static_cast<size_t>(b) * p.Hq + h) * p.pmax + pidx;
+      const size_t slot = qrow * p.pmax + pidx;
       float* o = p.part_o + slot * D;
 #pragma unroll
       for (int n = 0; n < D / 8; ++n)
@@ -653,21 +688,24 @@ __device__ __forceinline__ void ffma_finish(FfmaState<D, BS, FP8, GT>& st, const
 //   out = sum_p 2^(m_p - M) O_p / sum_p 2^(m_p - M) l_p,
 // the softmax over the union of the partitions' tokens.  An empty partition
 // (m = -inf) has weight 0.
-template <int D>
-__device__ __forceinline__ void arrive_and_merge(const DecodeParams& p, int b, int kvh, int nparts,
-                                                 int lane) {
+template <int D, bool MT>
+__device__ __forceinline__ void arrive_and_merge(const DecodeParams& p, int b, int kvh, int tile,
+                                                 int nparts, int lane) {
   // publish this warp's partials, then count the partition as done
   __threadfence();
   __syncwarp();
+  int* counter = p.arrive + (MT ? (b * p.Hkv + kvh) * p.NT + tile : b * p.Hkv + kvh);
   int prev = 0;
-  if (lane == 0) prev = atomicAdd(p.arrive + b * p.Hkv + kvh, 1);
+  if (lane == 0) prev = atomicAdd(counter, 1);
   prev = __shfl_sync(kFull, prev, 0);
   if (prev != nparts - 1) return;
   __threadfence();  // the other partitions' partials are visible from here on
   constexpr int kPer = D / 32;
-  for (int r = 0; r < p.G; ++r) {
-    const int h = kvh * p.G + r;
-    const size_t base = (static_cast<size_t>(b) * p.Hq + h) * p.pmax;
+  for (int r = 0; r < (MT ? p.G * p.Tt : p.G); ++r) {
+    int t, h;
+    if (!tile_row<MT>(p, kvh, tile, r, t, h)) break;
+    const size_t qrow = static_cast<size_t>(b * p.T + t) * p.Hq + h;
+    const size_t base = qrow * p.pmax;
     float M = -INFINITY;
     for (int i = lane; i < nparts; i += 32) M = fmaxf(M, __ldcg(p.part_ml + 2 * (base + i)));
 #pragma unroll
@@ -697,18 +735,20 @@ __device__ __forceinline__ void arrive_and_merge(const DecodeParams& p, int b, i
       }
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
-    __nv_bfloat16* o = p.out + (static_cast<size_t>(b) * p.Hq + h) * D + lane * kPer;
+    __nv_bfloat16* o = p.out + qrow * D + lane * kPer;
 #pragma unroll
     for (int j = 0; j < kPer; j += 2)
       *reinterpret_cast<__nv_bfloat162*>(o + j) = __floats2bfloat162_rn(acc[j] * inv, acc[j + 1] * inv);
   }
-  if (lane == 0) p.arrive[b * p.Hkv + kvh] = 0;  // ready for the next call on this workspace
+  if (lane == 0) *counter = 0;  // ready for the next call on this workspace
 }
 
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-template <int D, int BS, bool FP8, int MATH, int GT, bool I8 = false>
+// MT: multi-token queries (T >= 1, row tiles, per-row causal limits);
+// false: single-token kernels, T = 1 only.
+template <int D, int BS, bool FP8, int MATH, int GT, bool I8 = false, bool MT = false>
 __global__ void __launch_bounds__(256, 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
@@ -734,11 +774,14 @@ __global__ void __launch_bounds__(256, 1)
     }
   }
   __syncwarp();
-  const uint64_t policy = l2_policy_evict_first();
+  // Pages are read once, except by the row tiles of one (sequence, KV head,
+  // partition), which are adjacent units: keep those lines in L2 then.
+  const uint64_t policy = (MT && p.NT > 1) ? l2_policy_evict_normal() : l2_policy_evict_first();
   pdl_trigger();
   pdl_wait();  // the planner's output and every input are complete from here on
 
-  const int total_units = p.unit_start[p.B] * p.Hkv;
+  const int units_per_part = MT ? p.Hkv * p.NT : p.Hkv;
+  const int total_units = p.unit_start[p.B] * units_per_part;
   uint32_t it = 0;  // pages this warp has consumed (stage = it % R, phase = (it / R) & 1)
   const int ppu_tokens = p.ppu * BS;
 
@@ -747,8 +790,10 @@ __global__ void __launch_bounds__(256, 1)
     if (lane == 0) u = atomicAdd(p.work_counter, 1);
     u = __shfl_sync(kFull, u, 0);
     if (u >= total_units) break;
-    const int part = u / p.Hkv;
-    const int kvh = u - part * p.Hkv;
+    const int part = u / units_per_part;
+    const int rem = u - part * units_per_part;
+    const int kvh = MT ? rem / p.NT : rem;
+    const int tile = MT ? rem - kvh * p.NT : 0;
     // sequence owning global partition `part`: largest b with unit_start[b] <= part
     int lo = 0, hi = p.B;
     while (hi - lo > 1) {
@@ -827,13 +872,23 @@ __global__ void __launch_bounds__(256, 1)
     int issued = pre;  // pages of this unit handed to the copy engine
     int consumed = 0;
 
-    const __nv_bfloat16* qg = p.q + (static_cast<size_t>(b) * p.Hq + kvh * p.G) * D;
     bool timed_out = false;
     if (MATH == PKV_MATH_MMA) {
       constexpr bool kHi = GT > 8;
+      constexpr int kR = kHi ? 2 : 1;
       MmaState<D, BS, FP8, kHi> st;
-      mma_load_q<D, BS, FP8, kHi>(st, qg, p.G, lane);
+      mma_load_q<D, BS, FP8, kHi, MT>(st, p, b, kvh, tile, lane);
       if constexpr (I8) mma_int8_prepare(st);
+      // causal limits: query row g + 8r attends to positions < lim[r];
+      // lim_min is the smallest over the tile (T = 1: both are ctx)
+      int lim[kR];
+#pragma unroll
+      for (int r = 0; r < kR; ++r) {
+        int t, h;
+        tile_row<MT>(p, kvh, tile, (lane >> 2) + 8 * r, t, h);
+        lim[r] = MT ? ctx - p.T + 1 + min(t, p.T - 1) : ctx;
+      }
+      const int lim_min = MT ? ctx - p.T + 1 + tile * p.Tt : ctx;
       for (int j = 0; j < npages; ++j) {
         const uint32_t s = it % static_cast<uint32_t>(R);
         const bool landed = mbar_wait_bounded(&bars[s], (it / R) & 1u, kWaitLimitNs);
@@ -849,8 +904,13 @@ __global__ void __launch_bounds__(256, 1)
           kc = kInt8Bias + ((j < 32) ? __shfl_sync(kFull, kz0, j & 31) : __shfl_sync(kFull, kz1, j & 31));
           vc = kInt8Bias + ((j < 32) ? __shfl_sync(kFull, vz0, j & 31) : __shfl_sync(kFull, vz1, j & 31));
         }
-        mma_page<D, BS, FP8, kHi, I8>(st, ring + static_cast<size_t>(s) * Geo::kStageBytes, valid,
-                                      p.scale_log2 * ksc, vsc, kc, vc, lane);
+        const int pos0 = t0 + j * BS;
+        int rv[kR];
+#pragma unroll
+        for (int r = 0; r < kR; ++r) rv[r] = MT ? min(valid, lim[r] - pos0) : valid;
+        const bool partial = MT ? (valid < BS || lim_min - pos0 < BS) : valid < BS;
+        mma_page<D, BS, FP8, kHi, I8>(st, ring + static_cast<size_t>(s) * Geo::kStageBytes, valid, rv,
+                                      partial, p.scale_log2 * ksc, vsc, kc, vc, lane);
         fence_proxy_async_smem();  // this lane's reads of the stage precede the refill
         __syncwarp();
         if (j + R < npages) { issue(j + R, it + R); ++issued; }
@@ -859,10 +919,12 @@ __global__ void __launch_bounds__(256, 1)
       }
       if (!timed_out) {
         if constexpr (I8) mma_int8_unbias(st);
-        mma_finish<D, BS, FP8, kHi>(st, p, b, kvh, pidx, nparts, lane);
-        if (nparts > 1 && p.fused_merge) arrive_and_merge<D>(p, b, kvh, nparts, lane);
+        mma_finish<D, BS, FP8, kHi, MT>(st, p, b, kvh, tile, pidx, nparts, lane);
+        if (nparts > 1 && p.fused_merge) arrive_and_merge<D, MT>(p, b, kvh, tile, nparts, lane);
       }
     } else {
+      // single-token queries only (the host rejects T > 1 here)
+      const __nv_bfloat16* qg = p.q + (static_cast<size_t>(b) * p.Hq + kvh * p.G) * D;
       FfmaState<D, BS, FP8, (GT > 0 ? GT : 1)> st;
       ffma_load_q<D, BS, FP8, (GT > 0 ? GT : 1)>(st, qg, lane);
       for (int j = 0; j < npages; ++j) {
@@ -891,7 +953,7 @@ __global__ void __launch_bounds__(256, 1)
       }
       if (!timed_out) {
         ffma_finish<D, BS, FP8, (GT > 0 ? GT : 1)>(st, p, b, kvh, pidx, nparts, lane);
-        if (nparts > 1 && p.fused_merge) arrive_and_merge<D>(p, b, kvh, nparts, lane);
+        if (nparts > 1 && p.fused_merge) arrive_and_merge<D, false>(p, b, kvh, 0, nparts, lane);
       }
     }
     if (timed_out) {

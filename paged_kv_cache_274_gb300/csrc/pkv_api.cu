@@ -243,11 +243,14 @@ pkv_status pkv_kv_append(const pkv_cache_desc* cache, int32_t slot, const void* 
 }
 
 // Resolve options into a full launch configuration (no device work).
-static pkv_status resolve_decode(const pkv_cache_desc* c, int32_t batch, int32_t Hq, int32_t MB,
-                                 const pkv_decode_opts* opts, int num_sms, pkv::DecodeLaunch* L) {
+static pkv_status resolve_decode(const pkv_cache_desc* c, int32_t batch, int32_t T, int32_t Hq,
+                                 int32_t MB, const pkv_decode_opts* opts, int num_sms,
+                                 pkv::DecodeLaunch* L) {
   pkv_status st = check_cache_desc(c);
   if (st != PKV_OK) return st;
   if (batch < 0) return fail(PKV_ERR_INVALID_ARG, "batch %d < 0", batch);
+  if (T < 1 || T > PKV_MAX_QUERY_TOKENS)
+    return fail(PKV_ERR_INVALID_ARG, "num_query_tokens %d outside 1..%d", T, PKV_MAX_QUERY_TOKENS);
   if (MB < 1) return fail(PKV_ERR_INVALID_ARG, "max_blocks_per_seq %d < 1", MB);
   if (Hq < 1 || Hq % c->num_kv_heads != 0)
     return fail(PKV_ERR_INVALID_ARG, "num_q_heads %d is not a multiple of num_kv_heads %d", Hq,
@@ -264,6 +267,13 @@ static pkv_status resolve_decode(const pkv_cache_desc* c, int32_t batch, int32_t
   if (math == PKV_MATH_FFMA && G != 1 && G != 2 && G != 4 && G != 8)
     return fail(PKV_ERR_UNSUPPORTED, "G = %d query heads per KV head (ffma supports 1, 2, 4, 8)", G);
   if (math != PKV_MATH_MMA && math != PKV_MATH_FFMA) return fail(PKV_ERR_INVALID_ARG, "math %d", math);
+  if (math == PKV_MATH_FFMA && T > 1)
+    return fail(PKV_ERR_UNSUPPORTED, "multi-token queries need the mma back-end");
+  if (static_cast<long long>(batch) * T * Hq * c->head_dim >= (1LL << 31))
+    return fail(PKV_ERR_UNSUPPORTED, "batch x query tokens x heads x head_dim too large");
+  // row tiles of at most 16 (query token, head) rows: whole query tokens per tile
+  const int Tt = std::max(1, std::min(T, 16 / G));
+  const int NT = (T + Tt - 1) / Tt;
   const bool fp8 = c->dtype != PKV_KV_BF16;  // one-byte elements
   const size_t stage_bytes = static_cast<size_t>(2) * c->block_size * c->head_dim * (fp8 ? 1 : 2);
   // Defaults measured on GB300: 4 warps per CTA with shallow (2-stage)
@@ -289,7 +299,7 @@ static pkv_status resolve_decode(const pkv_cache_desc* c, int32_t batch, int32_t
     const long long ctas_regs = std::max<long long>(1, 65536LL / (warps * 32LL * 200));
     const long long W = static_cast<long long>(num_sms) * std::min(ctas_smem, ctas_regs) * warps;
     auto units = [&](int pp) {
-      return static_cast<long long>(std::max(batch, 1)) * c->num_kv_heads * ((MB + pp - 1) / pp);
+      return static_cast<long long>(std::max(batch, 1)) * c->num_kv_heads * NT * ((MB + pp - 1) / pp);
     };
     if (units(64) <= W) {
       ppu = 64;
@@ -314,6 +324,9 @@ static pkv_status resolve_decode(const pkv_cache_desc* c, int32_t batch, int32_t
   L->Hq = Hq;
   L->Hkv = c->num_kv_heads;
   L->G = G;
+  L->T = T;
+  L->Tt = Tt;
+  L->NT = NT;
   L->MB = MB;
   L->NB = c->num_blocks;
   L->bs = c->block_size;
@@ -329,21 +342,35 @@ static pkv_status resolve_decode(const pkv_cache_desc* c, int32_t batch, int32_t
   return PKV_OK;
 }
 
-size_t pkv_decode_workspace_bytes(const pkv_cache_desc* cache, int32_t batch, int32_t num_q_heads,
-                                  int32_t max_blocks_per_seq, const pkv_decode_opts* opts) {
+static pkv::WorkspaceLayout layout_of(const pkv::DecodeLaunch& L) {
+  return pkv::workspace_layout(L.B, L.T, L.Hq, L.Hkv, L.NT, L.D, L.pmax);
+}
+
+size_t pkv_decode_multi_workspace_bytes(const pkv_cache_desc* cache, int32_t batch,
+                                        int32_t num_query_tokens, int32_t num_q_heads,
+                                        int32_t max_blocks_per_seq, const pkv_decode_opts* opts) {
   pkv::DecodeLaunch L;
   // The partition size (and so the workspace) must not depend on the device
   // the call later runs on: size with the largest SM count this build targets.
-  if (resolve_decode(cache, batch, num_q_heads, max_blocks_per_seq, opts, 152, &L) != PKV_OK) return 0;
-  return pkv::workspace_layout(L.B, L.Hq, L.Hkv, L.D, L.pmax).total;
+  if (resolve_decode(cache, batch, num_query_tokens, num_q_heads, max_blocks_per_seq, opts, 152, &L) !=
+      PKV_OK)
+    return 0;
+  return layout_of(L).total;
 }
 
-pkv_status pkv_decode_describe(const pkv_cache_desc* cache, int32_t batch, int32_t num_q_heads,
-                               int32_t max_blocks_per_seq, const pkv_decode_opts* opts,
-                               pkv_decode_plan* plan) {
+size_t pkv_decode_workspace_bytes(const pkv_cache_desc* cache, int32_t batch, int32_t num_q_heads,
+                                  int32_t max_blocks_per_seq, const pkv_decode_opts* opts) {
+  return pkv_decode_multi_workspace_bytes(cache, batch, 1, num_q_heads, max_blocks_per_seq, opts);
+}
+
+pkv_status pkv_decode_multi_describe(const pkv_cache_desc* cache, int32_t batch,
+                                     int32_t num_query_tokens, int32_t num_q_heads,
+                                     int32_t max_blocks_per_seq, const pkv_decode_opts* opts,
+                                     pkv_decode_plan* plan) {
   if (plan == nullptr) return fail(PKV_ERR_INVALID_ARG, "plan is NULL");
   pkv::DecodeLaunch L;
-  pkv_status st = resolve_decode(cache, batch, num_q_heads, max_blocks_per_seq, opts, 152, &L);
+  pkv_status st = resolve_decode(cache, batch, num_query_tokens, num_q_heads, max_blocks_per_seq, opts,
+                                 152, &L);
   if (st != PKV_OK) return st;
   plan->partition_blocks = L.ppu;
   plan->max_partitions = L.pmax;
@@ -351,21 +378,30 @@ pkv_status pkv_decode_describe(const pkv_cache_desc* cache, int32_t batch, int32
   plan->warps_per_cta = L.warps;
   plan->stages = L.stages;
   plan->kernels_per_call = L.pmax > 4 ? 3 : 2;  // the merge kernel runs above 4 partitions
-  plan->workspace_bytes = pkv::workspace_layout(L.B, L.Hq, L.Hkv, L.D, L.pmax).total;
+  plan->workspace_bytes = layout_of(L).total;
   plan->smem_bytes_per_cta = pkv::decode_smem_bytes(L.kv_fp8, L.D, L.bs, L.warps, L.stages);
+  plan->query_tokens_per_tile = L.Tt;
+  plan->row_tiles = L.NT;
   return PKV_OK;
 }
 
-pkv_status pkv_paged_decode(const pkv_cache_desc* cache, const void* q, int32_t batch,
-                            int32_t num_q_heads, const void* k_cache, const void* v_cache,
-                            const float* k_scale, const float* v_scale,
-                            const int32_t* block_tables, int32_t max_blocks_per_seq,
-                            const int32_t* context_lens, const int32_t* kv_group_ptr,
-                            int32_t num_layers, int32_t layer, float scale, void* out,
-                            void* workspace, size_t workspace_bytes, const pkv_decode_opts* opts,
-                            void* stream) {
+pkv_status pkv_decode_describe(const pkv_cache_desc* cache, int32_t batch, int32_t num_q_heads,
+                               int32_t max_blocks_per_seq, const pkv_decode_opts* opts,
+                               pkv_decode_plan* plan) {
+  return pkv_decode_multi_describe(cache, batch, 1, num_q_heads, max_blocks_per_seq, opts, plan);
+}
+
+pkv_status pkv_paged_decode_multi(const pkv_cache_desc* cache, const void* q, int32_t batch,
+                                  int32_t num_query_tokens, int32_t num_q_heads, const void* k_cache,
+                                  const void* v_cache, const float* k_scale, const float* v_scale,
+                                  const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                  const int32_t* context_lens, const int32_t* kv_group_ptr,
+                                  int32_t num_layers, int32_t layer, float scale, void* out,
+                                  void* workspace, size_t workspace_bytes,
+                                  const pkv_decode_opts* opts, void* stream) {
   pkv::DecodeLaunch L;
-  pkv_status st = resolve_decode(cache, batch, num_q_heads, max_blocks_per_seq, opts, 152, &L);
+  pkv_status st = resolve_decode(cache, batch, num_query_tokens, num_q_heads, max_blocks_per_seq, opts,
+                                 152, &L);
   if (st != PKV_OK) return st;
   if (kv_group_ptr == nullptr || num_layers < 1 || layer < 0 || layer >= num_layers)
     return fail(PKV_ERR_INVALID_ARG, "layer %d / num_layers %d / kv_group_ptr", layer, num_layers);
@@ -384,10 +420,10 @@ pkv_status pkv_paged_decode(const pkv_cache_desc* cache, const void* q, int32_t 
     return fail(PKV_ERR_ALIGNMENT, "q, out, caches and workspace must be 16-byte aligned");
   if ((reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u))
     return fail(PKV_ERR_ALIGNMENT, "block_tables and context_lens must be 4-byte aligned");
-  const size_t qbytes = static_cast<size_t>(batch) * num_q_heads * cache->head_dim * 2;
+  const size_t qbytes = static_cast<size_t>(batch) * num_query_tokens * num_q_heads * cache->head_dim * 2;
   const uintptr_t qa = reinterpret_cast<uintptr_t>(q), oa = reinterpret_cast<uintptr_t>(out);
   if (qa < oa + qbytes && oa < qa + qbytes) return fail(PKV_ERR_INVALID_ARG, "out overlaps q");
-  const pkv::WorkspaceLayout wl = pkv::workspace_layout(L.B, L.Hq, L.Hkv, L.D, L.pmax);
+  const pkv::WorkspaceLayout wl = layout_of(L);
   if (workspace == nullptr || workspace_bytes < wl.total)
     return fail(PKV_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu", wl.total, workspace_bytes);
 
@@ -442,6 +478,20 @@ pkv_status pkv_paged_decode(const pkv_cache_desc* cache, const void* q, int32_t 
   cudaError_t e = pkv::launch_decode(L, &launched);
   if (e != cudaSuccess) return cuda_fail(e, "paged_decode launch");
   return PKV_OK;
+}
+
+pkv_status pkv_paged_decode(const pkv_cache_desc* cache, const void* q, int32_t batch,
+                            int32_t num_q_heads, const void* k_cache, const void* v_cache,
+                            const float* k_scale, const float* v_scale,
+                            const int32_t* block_tables, int32_t max_blocks_per_seq,
+                            const int32_t* context_lens, const int32_t* kv_group_ptr,
+                            int32_t num_layers, int32_t layer, float scale, void* out,
+                            void* workspace, size_t workspace_bytes, const pkv_decode_opts* opts,
+                            void* stream) {
+  return pkv_paged_decode_multi(cache, q, batch, 1, num_q_heads, k_cache, v_cache, k_scale, v_scale,
+                                block_tables, max_blocks_per_seq, context_lens, kv_group_ptr,
+                                num_layers, layer, scale, out, workspace, workspace_bytes, opts,
+                                stream);
 }
 
 pkv_status pkv_copy_blocks(const pkv_cache_desc* cache, const void* src_k, const void* src_v,

@@ -23,11 +23,14 @@ struct DecodeLaunch {
   int32_t* work_counter;  // workspace: dynamic work queue head
   int32_t* unit_start;    // workspace: [B+1] prefix of partitions per sequence
   int32_t* ctx_eff;       // workspace: [B] validated context lengths
-  int32_t* arrive;        // workspace: [B][Hkv] split-K partitions finished
-  float* part_ml;         // workspace: [B][Hq][pmax][2] (running max, sum)
-  float* part_o;          // workspace: [B][Hq][pmax][D]
+  int32_t* arrive;        // workspace: [B][Hkv][NT] split-K partitions finished
+  float* part_ml;         // workspace: [B][T][Hq][pmax][2] (running max, sum)
+  float* part_o;          // workspace: [B][T][Hq][pmax][D]
   unsigned* err;          // device error word
   int B, Hq, Hkv, G, MB, NB, bs, D;
+  int T;   // query tokens per sequence (1: single-token decode)
+  int Tt;  // query tokens per row tile (G * Tt <= 16 rows)
+  int NT;  // row tiles per (sequence, KV head): ceil(T / Tt)
   int kv_fp8;    // one-byte elements (E4M3 or INT8)
   int kv_dtype;  // pkv_kv_dtype
   int pmax;  // max partitions of a sequence (ceil(MB / ppu))
@@ -47,7 +50,7 @@ struct DecodeLaunch {
 struct WorkspaceLayout {
   size_t counter, unit_start, ctx_eff, arrive, part_ml, part_o, total;
 };
-WorkspaceLayout workspace_layout(int B, int Hq, int Hkv, int D, int pmax);
+WorkspaceLayout workspace_layout(int B, int T, int Hq, int Hkv, int NT, int D, int pmax);
 
 // Programmatic dependent launch on (default) or off (PKV_PDL=0).
 bool pdl_enabled();

@@ -73,6 +73,36 @@ def sdpa_reference(q_bits, k_vals, v_vals, scale):
     return out
 
 
+def sdpa_causal_tail_reference(q_bits, k_vals, v_vals, scale):
+    """float64 torch SDPA for T new query tokens per sequence.
+
+    q_bits: bf16 bits [B][T][Hq][D]; k_vals[b], v_vals[b]: float64 [n][Hkv][D]
+    whose last T rows are the new tokens' keys and values.  The query tokens
+    are placed at the last T positions of a square causal problem over all n
+    positions (the earlier positions get zero queries, and their rows are
+    dropped), so token t sees positions 0 .. n - T + t.  Rows whose position
+    would be negative (n < T) are zero."""
+    q = bf16_bits_to_f32(q_bits).astype(np.float64)
+    B, T, Hq, D = q.shape
+    out = np.zeros((B, T, Hq, D), dtype=np.float64)
+    for b in range(B):
+        n = k_vals[b].shape[0]
+        if n == 0:
+            continue
+        Hkv = k_vals[b].shape[1]
+        take = min(T, n)  # the last `take` query tokens have a position
+        qf = np.zeros((n, Hq, D))
+        qf[n - take:] = q[b, T - take:]
+        qt = torch.from_numpy(np.ascontiguousarray(np.transpose(qf, (1, 0, 2)))).reshape(1, Hq, n, D)
+        kt = torch.from_numpy(np.ascontiguousarray(np.transpose(k_vals[b], (1, 0, 2)))).reshape(1, Hkv, n, D)
+        vt = torch.from_numpy(np.ascontiguousarray(np.transpose(v_vals[b], (1, 0, 2)))).reshape(1, Hkv, n, D)
+        o = torch.nn.functional.scaled_dot_product_attention(
+            qt, kt, vt, scale=float(np.float32(scale)), is_causal=True, enable_gqa=(Hkv != Hq))
+        o = o.reshape(Hq, n, D).numpy()
+        out[b, T - take:] = np.transpose(o[:, n - take:], (1, 0, 2))
+    return out
+
+
 def torch_e4m3_to_f64(codes):
     """Library decode of E4M3 codes (torch float8_e4m3fn) to float64."""
     t = torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8))

@@ -1,0 +1,143 @@
+"""GPU multi-token query decode (T new tokens per sequence, causal among
+them) against the oracle: sweeps over head grouping x T (one and several row
+tiles), block sizes, cache dtypes, split-K partition sizes, contexts shorter
+than T; the T = 1 case against the single-token call; each query token
+against a single-token decode of the truncated context (bitwise); and the
+speculative-decoding flow (append T tokens, then verify them)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_274_gb300 as pkv
+from workloads import normal_bf16_bits, random_case
+from tests._gpu import DEV, DeviceCase, assert_close, bf16_dev_to_f64, to_dev, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+def _q(seed, B, T, Hq, D):
+    return normal_bf16_bits(seed, (B, T, Hq, D))
+
+
+def _run(dc, qbits, ppu=0, layer=0):
+    c = dc.c
+    opts = pkv.decode_opts(partition_blocks=ppu)
+    out = pkv.paged_decode_multi(to_dev_bf16(qbits), dc.k, dc.v, dc.bt, dc.cl, c.kv_group_ptr.tolist(),
+                                 layer, c.scale, k_scale=dc.ks, v_scale=dc.vs, opts=opts)
+    torch.cuda.synchronize()
+    assert pkv.read_device_error() == 0
+    return out
+
+
+def _oracle(dc, qbits, layer=0):
+    c = dc.c
+    return oracle.paged_decode_multi(qbits, dc.k_host, dc.v_host, c.block_tables, c.context_lens,
+                                     c.kv_group_ptr, layer, c.scale, k_scale=c.k_scale, v_scale=c.v_scale)
+
+
+SWEEP = [  # (D, bs, Hq, Hkv, T, dtype, lens)
+    (128, 16, 32, 8, 2, "bf16", [1, 2, 3, 17, 300, 33]),     # G 4: 8 rows, one tile
+    (128, 16, 32, 8, 4, "bf16", [4, 5, 16, 100, 1000]),       # 16 rows, one tile
+    (128, 16, 32, 8, 8, "bf16", [3, 8, 9, 64, 700]),          # two tiles; a context below T
+    (128, 32, 32, 8, 5, "bf16", [5, 31, 32, 33, 513]),        # ragged last tile
+    (64, 16, 8, 8, 16, "bf16", [16, 17, 40, 200]),            # MHA: 16 tokens in one tile
+    (64, 32, 8, 8, 20, "bf16", [19, 20, 21, 333]),            # two tiles of 16 and 4 tokens
+    (128, 16, 16, 1, 3, "bf16", [3, 50, 129]),                # MQA G 16: one token per tile
+    (128, 32, 64, 8, 2, "bf16", [2, 77, 260]),                # G 8
+    (128, 32, 32, 8, 4, "fp8", [4, 70, 300]),
+    (128, 16, 32, 8, 8, "fp8", [8, 20, 129]),
+    (128, 32, 32, 8, 4, "int8a", [4, 70, 300]),
+    (128, 16, 16, 4, 6, "int8", [6, 33, 250]),
+]
+
+
+@pytest.mark.parametrize("D,bs,Hq,Hkv,T,dtype,lens", SWEEP)
+@pytest.mark.parametrize("ppu", [0, 1, 3])
+def test_multi_token_sweep(D, bs, Hq, Hkv, T, dtype, lens, ppu):
+    seed = D + 3 * bs + 7 * Hq + 11 * Hkv + 13 * T + len(lens)
+    c = random_case(seed, len(lens), Hq, Hkv, D, bs, lens, kv_dtype=dtype)
+    dc = DeviceCase(c)
+    q = _q(seed + 1, c.B, T, Hq, D)
+    got = bf16_dev_to_f64(_run(dc, q, ppu))
+    want = _oracle(dc, q)
+    assert_close(got, want, f"T={T} {dtype} ppu={ppu}")
+
+
+def test_one_token_is_the_single_token_call():
+    c = random_case(71, 4, 32, 8, 128, 16, [1, 40, 300, 0])
+    dc = DeviceCase(c)
+    q = _q(72, c.B, 1, 32, 128)
+    multi = _run(dc, q)
+    single = pkv.paged_decode(to_dev_bf16(q[:, 0]), dc.k, dc.v, dc.bt, dc.cl, [0], 0, c.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(multi[:, 0], single)
+
+
+@pytest.mark.parametrize("Hq,Hkv,T", [(32, 8, 4), (32, 8, 8), (8, 8, 5)])
+def test_each_token_equals_truncated_single_token_decode(Hq, Hkv, T):
+    # query token t over context n is a single-token decode over n - T + t + 1
+    # tokens: same tiles per row, same masking, same partitions -> same bits
+    lens = [T + 3, 100, 257]
+    c = random_case(80 + T, len(lens), Hq, Hkv, 128, 16, lens)
+    dc = DeviceCase(c)
+    q = _q(81 + T, c.B, T, Hq, 128)
+    opts = pkv.decode_opts(partition_blocks=4)
+    multi = pkv.paged_decode_multi(to_dev_bf16(q), dc.k, dc.v, dc.bt, dc.cl, [0], 0, c.scale, opts=opts)
+    for t in range(T):
+        cl = to_dev((c.context_lens - T + t + 1).astype(np.int32))
+        single = pkv.paged_decode(to_dev_bf16(np.ascontiguousarray(q[:, t])), dc.k, dc.v, dc.bt, cl, [0], 0,
+                                  c.scale, opts=opts)
+        torch.cuda.synchronize()
+        assert torch.equal(multi[:, t], single), f"token {t}"
+
+
+def test_contexts_shorter_than_t_give_zero_rows():
+    T = 6
+    c = random_case(90, 4, 8, 2, 64, 16, [0, 2, 5, 6])
+    dc = DeviceCase(c)
+    q = _q(91, c.B, T, 8, 64)
+    got = bf16_dev_to_f64(_run(dc, q))
+    want = _oracle(dc, q)
+    assert_close(got, want, "short contexts")
+    assert np.all(got[0] == 0) and np.all(got[1, :4] == 0) and np.all(got[2, :1] == 0)
+
+
+def test_poisoned_tails_do_not_leak():
+    c = random_case(95, 3, 32, 8, 128, 16, [7, 33, 100], poison=True)
+    dc = DeviceCase(c)
+    q = _q(96, c.B, 4, 32, 128)
+    got = bf16_dev_to_f64(_run(dc, q, ppu=2))
+    assert_close(got, _oracle(dc, q), "poisoned")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8", "int8a"])
+def test_speculative_verify_flow(dtype):
+    # a step that appends T draft tokens per sequence, then scores them
+    T, Hq, Hkv, D, bs = 4, 32, 8, 128, 16
+    before = np.array([60, 15, 200], np.int32)
+    c = random_case(100, 3, Hq, Hkv, D, bs, (before + T).tolist(), kv_dtype=dtype, spare_blocks=2)
+    dc = DeviceCase(c)
+    # the draft tokens' K/V: the rows at positions before[b] .. before[b] + T - 1
+    slots = np.array([c.block_tables[b, p // bs] * bs + p % bs
+                      for b in range(c.B) for p in range(before[b], before[b] + T)], np.int64)
+    kn = normal_bf16_bits(101, (len(slots), Hkv, D))
+    vn = normal_bf16_bits(102, (len(slots), Hkv, D))
+    pkv.kv_append(to_dev_bf16(kn), to_dev_bf16(vn), to_dev(slots), dc.k, dc.v, dc.ks, dc.vs)
+    q = _q(103, c.B, T, Hq, D)
+    got = bf16_dev_to_f64(_run(dc, q))
+    ko, vo = dc.k_host.copy(), dc.v_host.copy()
+    assert oracle.kv_append(kn, vn, slots, ko, vo, c.k_scale, c.v_scale) == 0
+    assert np.array_equal(dc.k.cpu().numpy().view(ko.dtype) if dtype != "bf16" else
+                          dc.k.view(torch.int16).cpu().numpy().view(np.uint16), ko)
+    want = oracle.paged_decode_multi(q, ko, vo, c.block_tables, c.context_lens, c.kv_group_ptr, 0,
+                                     c.scale, k_scale=c.k_scale, v_scale=c.v_scale)
+    assert_close(got, want, f"verify {dtype}")
+
+
+def test_ffma_rejects_multi_token():
+    c = random_case(110, 2, 8, 2, 64, 16, [10, 20])
+    dc = DeviceCase(c)
+    q = to_dev_bf16(_q(111, 2, 2, 8, 64))
+    with pytest.raises(pkv.PkvError):
+        pkv.paged_decode_multi(q, dc.k, dc.v, dc.bt, dc.cl, opts=pkv.decode_opts(math=pkv.MATH_FFMA))

@@ -39,7 +39,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.pkv_abi_version() == 1
+    assert lib.pkv_abi_version() == 2
     assert lib.pkv_status_string(0) == b"ok"
     assert b"aligned" in lib.pkv_status_string(3)
 
@@ -104,12 +104,11 @@ def test_append_argument_checks(lib):
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
-    import importlib
+    # monkeypatch puts the loaded library and its path back afterwards
     monkeypatch.setattr(pkv, "_lib", None)
     monkeypatch.setattr(pkv, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(pkv.PkvError):
         pkv.load()
-    importlib.reload(pkv)
 
 
 def test_product_path_does_not_import_oracle():
@@ -120,3 +119,41 @@ def test_product_path_does_not_import_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "pkv_oracle" not in text, f
+
+
+def _plan(lib, d, B, T, Hq, MB, opts=None):
+    plan = pkv.DecodePlan()
+    st = lib.pkv_decode_multi_describe(ctypes.byref(d), B, T, Hq, MB,
+                                       ctypes.byref(opts) if opts is not None else None,
+                                       ctypes.byref(plan))
+    return st, plan
+
+
+@pytest.mark.parametrize("Hq,Hkv,T,tokens_per_tile,tiles", [
+    (32, 8, 1, 1, 1), (32, 8, 4, 4, 1), (32, 8, 8, 4, 2), (32, 8, 5, 4, 2),
+    (16, 1, 3, 1, 3), (8, 8, 16, 16, 1), (8, 8, 17, 16, 2), (24, 8, 6, 5, 2)])
+def test_multi_token_row_tiles(lib, Hq, Hkv, T, tokens_per_tile, tiles):
+    # (query token, head) rows form tiles of at most 16 rows, whole tokens each
+    d = _desc(num_kv_heads=Hkv)
+    st, plan = _plan(lib, d, 8, T, Hq, 64)
+    assert st == 0
+    assert (plan.query_tokens_per_tile, plan.row_tiles) == (tokens_per_tile, tiles)
+    assert (Hq // Hkv) * plan.query_tokens_per_tile <= 16
+
+
+def test_multi_token_arguments(lib):
+    d = _desc()
+    assert _plan(lib, d, 8, 0, 32, 64)[0] == 1                       # T = 0
+    assert _plan(lib, d, 8, pkv.MAX_QUERY_TOKENS + 1, 32, 64)[0] == 1
+    assert _plan(lib, d, 8, 2, 32, 64, pkv.decode_opts(math=pkv.MATH_FFMA))[0] == 2  # mma only
+    assert _plan(lib, d, 8, 1, 32, 64, pkv.decode_opts(math=pkv.MATH_FFMA))[0] == 0
+    # T = 1 is the single-token call
+    one = pkv.DecodePlan()
+    assert lib.pkv_decode_describe(ctypes.byref(d), 8, 32, 64, None, ctypes.byref(one)) == 0
+    st, multi = _plan(lib, d, 8, 1, 32, 64)
+    assert st == 0 and bytes(one) == bytes(multi)
+    # partial storage grows with the query rows
+    o = pkv.decode_opts(partition_blocks=8)
+    w1 = lib.pkv_decode_multi_workspace_bytes(ctypes.byref(d), 8, 1, 32, 64, ctypes.byref(o))
+    w4 = lib.pkv_decode_multi_workspace_bytes(ctypes.byref(d), 8, 4, 32, 64, ctypes.byref(o))
+    assert w4 > 3 * w1 > 0

@@ -24,8 +24,8 @@ import pytest
 
 import oracle
 from workloads import bf16_bits_from_f32, bf16_bits_to_f32, normal_bf16_bits
-from tests._paged import (dense_bf16_seqs, paged_from_dense, sdpa_reference,
-                          torch_e4m3_to_f64, torch_f32_to_e4m3)
+from tests._paged import (dense_bf16_seqs, paged_from_dense, sdpa_causal_tail_reference,
+                          sdpa_reference, torch_e4m3_to_f64, torch_f32_to_e4m3)
 
 TOL = 1e-12
 
@@ -392,11 +392,35 @@ def pin_sdpa_int8(lib=None):
     np.testing.assert_allclose(got, want, rtol=TOL, atol=TOL)
 
 
+def pin_multi_token_causal(lib=None):
+    # T new query tokens per sequence against torch's causal SDPA on the dense
+    # sequence (bottom-right aligned: the new tokens are the last T positions)
+    configs = [  # (T, Hq, Hkv, D, bs, lens)
+        (2, 8, 2, 64, 16, [37, 100, 2]),
+        (4, 4, 4, 64, 16, [1, 16, 17, 3]),   # lengths below T: leading rows are zero
+        (3, 8, 1, 128, 32, [33, 64, 5]),
+        (5, 16, 4, 128, 16, [48, 250]),
+        (1, 8, 2, 64, 16, [20, 9]),
+    ]
+    for i, (T, Hq, Hkv, D, bs, lens) in enumerate(configs):
+        ks, vs = dense_bf16_seqs(400 + i, lens, Hkv, D)
+        kc, vc, bt, ctx, _ = paged_from_dense(ks, vs, bs, seed=500 + i)
+        q = normal_bf16_bits(600 + i, (len(lens), T, Hq, D))
+        scale = float(np.float32(1 / np.sqrt(D)))
+        got = oracle.paged_decode_multi(q, kc, vc, bt, ctx, [0], 0, scale, lib=lib)
+        want = sdpa_causal_tail_reference(q, [_f64(k) for k in ks], [_f64(v) for v in vs], scale)
+        np.testing.assert_allclose(got, want, rtol=TOL, atol=TOL, err_msg=f"config {i}")
+        if T == 1:  # the single-token entry point is the T = 1 case
+            one = oracle.paged_decode(q[:, 0], kc, vc, bt, ctx, [0], 0, scale, lib=lib)
+            np.testing.assert_array_equal(one, got[:, 0])
+
+
 PINS = [pin_sdpa_bf16, pin_large_logits, pin_closed_forms, pin_permutation_invariance,
         pin_shared_prefix, pin_poisoned_unused, pin_gqa_equals_repeated_mha,
         pin_shared_with_pointer, pin_sdpa_fp8, pin_bad_inputs_rejected,
         pin_e4m3_decode_all_codes, pin_e4m3_encode_matches_library, pin_e4m3_scaled_quantize,
-        pin_append_scatter, pin_append_fp8, pin_copy_blocks, pin_int8_codec, pin_sdpa_int8]
+        pin_append_scatter, pin_append_fp8, pin_copy_blocks, pin_int8_codec, pin_sdpa_int8,
+        pin_multi_token_causal]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -408,13 +432,13 @@ def test_pin(pin):
 # planted mistakes: each must make at least one pin fail
 # ---------------------------------------------------------------------------
 MUTANTS = [
-    ("gather_wrong_block", "block_tables[(int64_t)b * MB + t / bs];\n        int64_t page",
-     "block_tables[(int64_t)b * MB + (t / bs) / 2];\n        int64_t page"),
+    ("gather_wrong_block", "block_tables[(int64_t)b * MB + j / bs];\n        int64_t page",
+     "block_tables[(int64_t)b * MB + (j / bs) / 2];\n        int64_t page"),
     ("gqa_strided_heads", "int32_t g = h / G;", "int32_t g = h % Hkv;"),
-    ("scale_dropped", "s[t] = (double)scale * dot;", "s[t] = dot;"),
-    ("no_max_subtraction", "s[t] = exp(s[t] - smax);", "s[t] = exp(s[t]);"),
-    ("no_normalisation", "double p = s[t] / z;", "double p = s[t];"),
-    ("rows_reversed", "page, bs, D, t % bs, d)", "page, bs, D, bs - 1 - t % bs, d)"),
+    ("scale_dropped", "s[j] = (double)scale * dot;", "s[j] = dot;"),
+    ("no_max_subtraction", "s[j] = exp(s[j] - smax);", "s[j] = exp(s[j]);"),
+    ("no_normalisation", "double p = s[j] / z;", "double p = s[j];"),
+    ("rows_reversed", "page, bs, D, j % bs, d)", "page, bs, D, bs - 1 - j % bs, d)"),
     ("last_dim_dropped", "for (int32_t d = 0; d < D; ++d)\n          dot +=",
      "for (int32_t d = 0; d < D - 1; ++d)\n          dot +="),
     ("v_from_k_cache", "cache_value(v_cache, fp8, v_scale", "cache_value(k_cache, fp8, k_scale"),
@@ -431,6 +455,10 @@ MUTANTS = [
     ("int8_zero_sign", "return ((double)q - (double)zero) * (double)scale;",
      "return ((double)q + (double)zero) * (double)scale;"),
     ("int8_symmetric_clamp", "double lo = (zero == 0.0f) ? -127.0 : -128.0;", "double lo = -128.0;"),
+    ("causal_off_by_one", "int32_t m = context_lens[b] - T + t + 1;",
+     "int32_t m = context_lens[b] - T + t;"),
+    ("causal_ignored", "int32_t m = context_lens[b] - T + t + 1;", "int32_t m = context_lens[b];"),
+    ("query_token_order", "int32_t t = r / Hq, h = r % Hq;", "int32_t t = (T - 1) - r / Hq, h = r % Hq;"),
     ("append_wrong_offset", "int64_t blk = s / bs, off = s % bs;", "int64_t blk = s / bs, off = (s + 1) % bs;"),
 ]
 
