@@ -7,7 +7,9 @@ One step = one pass of the whole hot path over one batch:
   long_b4_32k / long_b1_128k: paged_decode, 64 q / 8 KV heads, block 32;
   mixed_prefix: 256 sequences, log-uniform lengths, shared prefix blocks;
   fp8_shared: four layer calls that read one E4M3 cache (shared-with pointer);
-  int8_shared: the same with an INT8 cache, per-page (scale, zero) pairs.
+  int8_shared: the same with an INT8 cache, per-page (scale, zero) pairs;
+  spec_verify_t4: the Llama-8B layer scoring 4 draft tokens per sequence
+      (append 4 tokens, then one multi-token decode, causal among them).
 
 Metric: KV bytes read per step / step time (GB/s, 1e9), with % of the
 measured HBM peak and decode steps/s beside it.  Inputs (>= 512 MiB of KV)
@@ -42,7 +44,12 @@ METRIC = "paged decode KV-read GB/s and % of GB300 HBM peak; decode steps/s"
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0
 WORKLOADS = ("llama8b_layer", "long_b4_32k", "long_b1_128k", "mixed_prefix", "fp8_shared",
-             "int8_shared", "tiny", "copy_blocks")
+             "int8_shared", "spec_verify_t4", "spec_verify_t8", "tiny", "copy_blocks")
+
+
+def query_tokens_of(name):
+    """Query tokens per sequence of a workload (1: single-token decode)."""
+    return int(name[len("spec_verify_t"):]) if name.startswith("spec_verify_t") else 1
 
 
 def parse_args():
@@ -183,7 +190,8 @@ class ClockSampler:
 def profile_traffic(workload):
     """Per-launch DRAM bytes of the decode kernel from the committed ncu
     summary, if it was taken on the current kernel sources; else None."""
-    path = os.path.join(ROOT, "profiles", f"paged_decode_{workload}.md")
+    name = "copy_blocks_llama8b_pool" if workload == "copy_blocks" else f"paged_decode_{workload}"
+    path = os.path.join(ROOT, "profiles", f"{name}.md")
     try:
         text = open(path).read()
     except OSError:
@@ -204,7 +212,7 @@ def profile_traffic(workload):
 def structure(name):
     """Block tables, lengths, queries, append slots (no cache contents)."""
     from workloads import gen
-    if name == "llama8b_layer":
+    if name == "llama8b_layer" or name.startswith("spec_verify_t"):
         return gen.llama8b_layer_case(fill=False)
     if name.startswith("long_"):
         return gen.long_context_case(name[len("long_"):], fill=False)
@@ -331,6 +339,44 @@ class DeviceWorkload:
             pkv.paged_decode(self.q[layer], self.k, self.v, self.bt, self.cl, c.kv_group_ptr.tolist(),
                              layer, c.scale, out=self.out[layer], workspace=self.ws,
                              k_scale=self.ks, v_scale=self.vs, opts=opts)
+
+
+class VerifyWorkload(DeviceWorkload):
+    """Speculative-decoding verification on the Llama-3.1-8B decode layer:
+    each step appends T draft tokens per sequence (positions ctx-T .. ctx-1)
+    and scores them with one multi-token decode (64 sequences x T query
+    tokens x 32 heads over context 4096; the T x 4 rows of a KV head share
+    one read of its pages)."""
+
+    def __init__(self, name, rank, opts_kw):
+        super().__init__(name, rank, opts_kw)
+        c, pkv, dev = self.c, self.pkv, self.dev
+        self.T = T = query_tokens_of(name)
+        g = torch.Generator(device=dev)
+        g.manual_seed(15485863 * (rank + 1) + T)
+        self.q = torch.randn((c.L, c.B, T, c.Hq, c.D), generator=g, device=dev, dtype=torch.bfloat16)
+        self.out = torch.empty_like(self.q)
+        pos = c.context_lens.astype(np.int64)[:, None] - T + np.arange(T)[None, :]
+        blk = c.block_tables[np.arange(c.B)[:, None], pos // c.bs].astype(np.int64)
+        self.slots = torch.from_numpy((blk * c.bs + pos % c.bs).reshape(-1)).to(dev)
+        self.k_new = torch.randn((c.B * T, c.Hkv, c.D), generator=g, device=dev, dtype=torch.bfloat16)
+        self.v_new = torch.randn((c.B * T, c.Hkv, c.D), generator=g, device=dev, dtype=torch.bfloat16)
+        self.append = True
+        self.ws = pkv.new_decode_workspace(self.k, c.B, c.Hq, c.MB, self.opts, T)
+        self.plan = pkv.decode_plan(self.k, c.B, c.Hq, c.MB, self.opts, T)
+        self.launches_per_step = 1 + len(self.layers) * self.plan["kernels_per_call"]
+        torch.cuda.synchronize()
+
+    def step(self, events=None):
+        pkv, c = self.pkv, self.c
+        pkv.kv_append(self.k_new, self.v_new, self.slots, self.k, self.v, self.ks, self.vs)
+        for i, layer in enumerate(self.layers):
+            opts = self.opts
+            if events is not None:
+                opts = pkv.decode_opts(**self.opts_kw, event_start=events[i][0], event_end=events[i][1])
+            pkv.paged_decode_multi(self.q[layer], self.k, self.v, self.bt, self.cl, c.kv_group_ptr.tolist(),
+                                   layer, c.scale, out=self.out[layer], workspace=self.ws,
+                                   k_scale=self.ks, v_scale=self.vs, opts=opts)
 
 
 class CopyWorkload:
@@ -488,12 +534,20 @@ def oracle_sample(name, target_s):
                     arr[0, blks] = normal_bf16_bits(1000 * seed + b, (n,) + shape[2:])
             filled.add(b)
 
+    T = query_tokens_of(name)
+    qm = normal_bf16_bits(17, (c.B, T, c.Hq, c.D)) if T > 1 else None
+
     def run(nseq):
         fill(nseq)
-        pairs = np.array([(b, h) for b in order[:nseq] for h in range(c.Hq)], np.int32)
         t0 = time.perf_counter()
-        oracle.paged_decode(c.q[0], k, v, c.block_tables, c.context_lens, c.kv_group_ptr, 0, c.scale,
-                            k_scale=ks, v_scale=vs, pairs=pairs)
+        if T > 1:
+            rows = np.array([(b, t, h) for b in order[:nseq] for t in range(T) for h in range(c.Hq)])
+            oracle.paged_decode_multi(qm, k, v, c.block_tables, c.context_lens, c.kv_group_ptr, 0,
+                                      c.scale, k_scale=ks, v_scale=vs, rows=rows)
+        else:
+            pairs = np.array([(b, h) for b in order[:nseq] for h in range(c.Hq)], np.int32)
+            oracle.paged_decode(c.q[0], k, v, c.block_tables, c.context_lens, c.kv_group_ptr, 0,
+                                c.scale, k_scale=ks, v_scale=vs, pairs=pairs)
         return time.perf_counter() - t0
 
     t1 = run(1)
@@ -504,7 +558,8 @@ def oracle_sample(name, target_s):
         secs += run(nseq)
         reps += 1
     nbytes = kv_bytes_of(c, seqs=order[:nseq], layers=[0]) * reps
-    desc = (f"{name}: sequences 0..{nseq - 1} of {c.B} (all {c.Hq} query heads, one layer call), "
+    desc = (f"{name}: sequences 0..{nseq - 1} of {c.B} (all {c.Hq} query heads"
+            f"{f' x {T} query tokens' if T > 1 else ''}, one layer call), "
             f"{reps} repetition(s), {nbytes / 1e9:.3f} GB of KV")
     return nbytes / secs / 1e9, secs, oracle.num_threads(), desc
 
@@ -520,6 +575,8 @@ def config_of(name, c, extra=None):
                                                                 int(c.context_lens.max()),
                                                                 float(c.context_lens.mean()))),
            "pool_blocks": c.NB, "l2": "inputs larger than L2 (129 MB); no flush between steps"}
+    if query_tokens_of(name) > 1:
+        cfg["query_tokens_per_seq"] = query_tokens_of(name)
     if extra:
         cfg.update(extra)
     return cfg
@@ -554,7 +611,12 @@ def run_ours(args, rank, world):
                    math={"auto": pkv.MATH_AUTO, "mma": pkv.MATH_MMA, "ffma": pkv.MATH_FFMA}[args.math],
                    warps=args.warps, stages=args.stages)
     copy = args.workload == "copy_blocks"
-    w = CopyWorkload(rank) if copy else DeviceWorkload(args.workload, rank, opts_kw)
+    if copy:
+        w = CopyWorkload(rank)
+    elif query_tokens_of(args.workload) > 1:
+        w = VerifyWorkload(args.workload, rank, opts_kw)
+    else:
+        w = DeviceWorkload(args.workload, rank, opts_kw)
     c = w.c
     total_ms, kernel_ms, clocks = time_device(w, args.steps, args.warmup, world)
     assert pkv.read_device_error() == 0, "device error word set during the benchmark"
