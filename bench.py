@@ -187,10 +187,12 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
-def profile_traffic(workload):
-    """Per-launch DRAM bytes of the decode kernel from the committed ncu
+def profile_traffic(workload, math="mma"):
+    """Per-launch DRAM bytes of the workload's kernel from the committed ncu
     summary, if it was taken on the current kernel sources; else None."""
     name = "copy_blocks_llama8b_pool" if workload == "copy_blocks" else f"paged_decode_{workload}"
+    if math == "ffma":
+        name += "_ffma"
     path = os.path.join(ROOT, "profiles", f"{name}.md")
     try:
         text = open(path).read()
@@ -201,7 +203,7 @@ def profile_traffic(workload):
     if not m or not h:
         return None
     from paged_kv_cache_274_gb300 import _build
-    if h.group(1) != _build.source_digest():
+    if h.group(1) != _build.kernel_digest():
         return None
     return int(m.group(1))
 
@@ -660,7 +662,7 @@ def run_ours(args, rank, world):
                          "peak": peak, "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                          if peak_kind == "measured" else "fallback 6.8 TB/s",
                          "unit": "GB/s", "frac": achieved / peak,
-                         "traffic": profile_traffic(args.workload),
+                         "traffic": profile_traffic(args.workload, {1: "ffma", 2: "mma"}.get(plan["math"], "mma")),
                          "algorithmic_bytes_per_launch": per_call_bytes,
                          "kernel_ms_mean": k_ms, "kernel_ms_median": statistics.median(kernel_ms)},
             "cpu_baseline": cpu,

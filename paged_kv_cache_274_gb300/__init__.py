@@ -114,6 +114,23 @@ def load() -> ctypes.CDLL:
         lib.pkv_last_error_message.argtypes = []
         lib.pkv_abi_version.restype = ctypes.c_int32
         lib.pkv_abi_version.argtypes = []
+        i64 = ctypes.c_int64
+        pi32 = ctypes.POINTER(ctypes.c_int32)
+        pi64 = ctypes.POINTER(ctypes.c_int64)
+        lib.pkv_prefix_block_hashes.restype = ctypes.c_int
+        lib.pkv_prefix_block_hashes.argtypes = [i32, P, i64, P]
+        lib.pkv_prefix_cache_create.restype = ctypes.c_int
+        lib.pkv_prefix_cache_create.argtypes = [i32, i32, ctypes.POINTER(ctypes.c_void_p)]
+        lib.pkv_prefix_cache_destroy.restype = ctypes.c_int
+        lib.pkv_prefix_cache_destroy.argtypes = [P]
+        lib.pkv_prefix_cache_match.restype = ctypes.c_int
+        lib.pkv_prefix_cache_match.argtypes = [P, i32, P, i64, P, i32, pi32]
+        lib.pkv_prefix_cache_insert.restype = ctypes.c_int
+        lib.pkv_prefix_cache_insert.argtypes = [P, i32, P, i64, P, i32, pi32]
+        lib.pkv_prefix_cache_erase.restype = ctypes.c_int
+        lib.pkv_prefix_cache_erase.argtypes = [P, i32, P, i32, pi32]
+        lib.pkv_prefix_cache_stats.restype = ctypes.c_int
+        lib.pkv_prefix_cache_stats.argtypes = [P, i32, pi64, pi64, pi64]
         if lib.pkv_abi_version() != ABI_VERSION:
             raise RuntimeError(f"{LIB_PATH} has ABI version {lib.pkv_abi_version()}, "
                                f"this binding needs {ABI_VERSION}: rebuild")
@@ -386,3 +403,70 @@ def read_device_error(stream=None) -> int:
 def build(force: bool = False) -> str:
     from . import _build
     return _build.build(force=force)
+
+
+# ---------------------------------------------------------------------------
+# prefix cache (host only; include/pkv_prefix.h)
+# ---------------------------------------------------------------------------
+def _i32_array(values) -> "ctypes.Array":
+    vals = [int(v) for v in values]
+    return (ctypes.c_int32 * max(1, len(vals)))(*vals)
+
+
+def prefix_block_hashes(tokens: Sequence[int], block_size: int) -> list:
+    """Cumulative FNV-1a-64 hash of every full block of a token sequence."""
+    n = len(tokens)
+    nb = n // int(block_size) if block_size > 0 else 0
+    out = (ctypes.c_uint64 * max(1, nb))()
+    _check(load().pkv_prefix_block_hashes(int(block_size), _i32_array(tokens), n, out))
+    return [int(out[j]) for j in range(nb)]
+
+
+class PrefixCache:
+    """Host index from block content to physical block, per layer group:
+    ``match`` walks a request's full blocks and returns the physical blocks of
+    its cached prefix; ``insert`` registers a sequence's full blocks; ``erase``
+    forgets freed blocks."""
+
+    def __init__(self, block_size: int, num_groups: int = 1):
+        self._lib = load()
+        h = ctypes.c_void_p()
+        _check(self._lib.pkv_prefix_cache_create(int(block_size), int(num_groups), ctypes.byref(h)))
+        self._h = h
+        self.block_size = int(block_size)
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            self._lib.pkv_prefix_cache_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        self.close()
+
+    def match(self, tokens: Sequence[int], group: int = 0, max_blocks: Optional[int] = None) -> list:
+        nb = len(tokens) // self.block_size
+        cap = nb if max_blocks is None else min(nb, int(max_blocks))
+        ids = (ctypes.c_int32 * max(1, cap))()
+        n = ctypes.c_int32(0)
+        _check(self._lib.pkv_prefix_cache_match(self._h, int(group), _i32_array(tokens), len(tokens), ids,
+                                                 cap, ctypes.byref(n)))
+        return [int(ids[j]) for j in range(n.value)]
+
+    def insert(self, tokens: Sequence[int], block_ids: Sequence[int], group: int = 0) -> int:
+        n = ctypes.c_int32(0)
+        _check(self._lib.pkv_prefix_cache_insert(self._h, int(group), _i32_array(tokens), len(tokens),
+                                                  _i32_array(block_ids), len(block_ids), ctypes.byref(n)))
+        return n.value
+
+    def erase(self, block_ids: Sequence[int], group: int = 0) -> int:
+        n = ctypes.c_int32(0)
+        _check(self._lib.pkv_prefix_cache_erase(self._h, int(group), _i32_array(block_ids), len(block_ids),
+                                                 ctypes.byref(n)))
+        return n.value
+
+    def stats(self, group: int = 0):
+        """(entries, lookups, hits) of one group."""
+        e, l, h = ctypes.c_int64(0), ctypes.c_int64(0), ctypes.c_int64(0)
+        _check(self._lib.pkv_prefix_cache_stats(self._h, int(group), ctypes.byref(e), ctypes.byref(l),
+                                                 ctypes.byref(h)))
+        return e.value, l.value, h.value

@@ -1,4 +1,5 @@
-"""Compile the CUDA library in-tree: csrc/*.cu -> _lib/libpkv.so (sm_103a only).
+"""Compile the library in-tree: csrc/*.cu (+ host-only csrc/*.cpp) ->
+_lib/libpkv.so (sm_103a only).
 
 Each translation unit is compiled in its own nvcc process (in parallel), then
 linked with ``nvcc -shared`` (static CUDA runtime).  No cmake, no torch
@@ -31,7 +32,7 @@ def _nvcc() -> str:
 
 
 def _sources():
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
 
 
 def source_digest() -> str:
@@ -42,6 +43,18 @@ def source_digest() -> str:
         if os.path.isfile(f):
             h.update(os.path.basename(f).encode())
             h.update(open(f, "rb").read())
+    return h.hexdigest()
+
+
+def kernel_digest() -> str:
+    """sha256 over the GPU-side sources (csrc/*.cu, *.cuh, *.h): what a
+    profile of the kernels was taken on.  Host-only .cpp files and the
+    public headers' prose are not part of it."""
+    h = hashlib.sha256()
+    files = sorted(f for ext in ("*.cu", "*.cuh", "*.h") for f in glob.glob(os.path.join(CSRC, ext)))
+    for f in files:
+        h.update(os.path.basename(f).encode())
+        h.update(open(f, "rb").read())
     return h.hexdigest()
 
 
@@ -60,7 +73,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     objs = []
 
     def compile_one(src):
-        obj = os.path.join(OUT_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(OUT_DIR, os.path.splitext(os.path.basename(src))[0] + ".o")
         cmd = [nvcc] + common + ["-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:

@@ -21,7 +21,8 @@ def lib():
 
 
 def declared_functions():
-    src = open(HEADER).read()
+    src = "".join(open(os.path.join(ROOT, "include", f)).read()
+                  for f in sorted(os.listdir(os.path.join(ROOT, "include"))) if f.endswith(".h"))
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(pkv_\w+)\s*\(", src, flags=re.M)))
 
@@ -29,7 +30,8 @@ def declared_functions():
 def test_header_declares_api():
     names = declared_functions()
     for n in ("pkv_kv_append", "pkv_paged_decode", "pkv_decode_workspace_bytes",
-              "pkv_read_device_error", "pkv_status_string"):
+              "pkv_read_device_error", "pkv_status_string", "pkv_paged_decode_multi",
+              "pkv_copy_blocks", "pkv_prefix_cache_match"):
         assert n in names
 
 
