@@ -108,13 +108,17 @@ __global__ void __launch_bounds__(kPlanThreads)
 
 // ---------------------------------------------------------------------------
 // merge kernel (many partitions): one CTA per (sequence, query token, query
-// head) row; thread
-// (pg, dg) owns 4 columns of head_dim and partitions pg, pg + kPG, ...  It
-// folds its partitions in one pass with a running maximum, then the kPG
-// partial results are combined through shared memory:
-//   out = sum_p 2^(m_p - M) O_p / sum_p 2^(m_p - M) l_p,  M = max_p m_p.
+// head) row, in two phases so that no load waits on another:
+//   1. M = max_p m_p over the row's partitions (all threads, strided);
+//   2. thread (pg, dg) owns 4 columns of head_dim and partitions pg, pg + kPG,
+//      ...; with M known every weight 2^(m_p - M) is final, so its loads are
+//      independent and are issued four partitions at a time;
+// then the kPG partial sums are added through shared memory:
+//   out = sum_p 2^(m_p - M) O_p / sum_p 2^(m_p - M) l_p.
+// Empty partitions (m = -inf) have weight 0; a row whose partitions are all
+// empty gets zeros.
 // ---------------------------------------------------------------------------
-constexpr int kMergeThreads = 128;
+constexpr int kMergeThreads = 256;
 
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads)
@@ -123,8 +127,10 @@ __global__ void __launch_bounds__(kMergeThreads)
                  int pmax, __nv_bfloat16* __restrict__ out) {
   constexpr int kDG = D / 4;                  // threads along head_dim
   constexpr int kPG = kMergeThreads / kDG;    // partition groups
+  constexpr int kBatch = 4;                   // partitions in flight per thread
   __shared__ float4 s_acc[kPG][kDG];
-  __shared__ float s_m[kPG][kDG], s_l[kPG][kDG];
+  __shared__ float s_l[kPG][kDG];
+  __shared__ float s_max[kMergeThreads / 32];
   pdl_trigger();
   pdl_wait();
   const int bh = blockIdx.x;  // row (b * T + t) * Hq + h
@@ -132,50 +138,127 @@ __global__ void __launch_bounds__(kMergeThreads)
   const int P = unit_start[b + 1] - unit_start[b];
   if (P < 2) return;  // written by the decode kernel (or zero-filled by the planner)
   const int tid = threadIdx.x;
-  const int dg = tid % kDG, pg = tid / kDG;
   const size_t base = static_cast<size_t>(bh) * pmax;
-  float m = -INFINITY, l = 0.f;
+  const float2* ml = reinterpret_cast<const float2*>(part_ml) + base;
+
+  // 1. row maximum
+  float M = -INFINITY;
+  for (int i = tid; i < P; i += kMergeThreads) M = fmaxf(M, ml[i].x);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+  if ((tid & 31) == 0) s_max[tid >> 5] = M;
+  __syncthreads();
+  M = s_max[0];
+#pragma unroll
+  for (int w = 1; w < kMergeThreads / 32; ++w) M = fmaxf(M, s_max[w]);
+
+  // 2. weighted sums, four independent partitions at a time
+  const int dg = tid % kDG, pg = tid / kDG;
+  float L = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 2
-  for (int i = pg; i < P; i += kPG) {
-    const float2 ml = *reinterpret_cast<const float2*>(part_ml + 2 * (base + i));
-    const float4 v = *reinterpret_cast<const float4*>(part_o + (base + i) * D + 4 * dg);
-    const float mn = fmaxf(m, ml.x);
-    if (mn == -INFINITY) continue;  // nothing but empty partitions so far
-    const float a = exp2f(m - mn), w = exp2f(ml.x - mn);
-    l = fmaf(l, a, w * ml.y);
-    acc.x = fmaf(acc.x, a, w * v.x);
-    acc.y = fmaf(acc.y, a, w * v.y);
-    acc.z = fmaf(acc.z, a, w * v.z);
-    acc.w = fmaf(acc.w, a, w * v.w);
-    m = mn;
+  if (M != -INFINITY) {
+    const float* ob = part_o + base * D + 4 * dg;
+    for (int i0 = pg; i0 < P; i0 += kPG * kBatch) {
+      float2 m[kBatch];
+      float4 v[kBatch];
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const int i = i0 + k * kPG;
+        if (i < P) {
+          m[k] = ml[i];
+          v[k] = *reinterpret_cast<const float4*>(ob + static_cast<size_t>(i) * D);
+        } else {
+          m[k] = make_float2(-INFINITY, 0.f);
+          v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const float w = exp2f(m[k].x - M);  // 0 for an empty partition or a missing one
+        L = fmaf(w, m[k].y, L);
+        acc.x = fmaf(w, v[k].x, acc.x);
+        acc.y = fmaf(w, v[k].y, acc.y);
+        acc.z = fmaf(w, v[k].z, acc.z);
+        acc.w = fmaf(w, v[k].w, acc.w);
+      }
+    }
   }
   s_acc[pg][dg] = acc;
-  s_m[pg][dg] = m;
-  s_l[pg][dg] = l;
+  s_l[pg][dg] = L;
   __syncthreads();
   if (pg != 0) return;
-  float M = -INFINITY;
 #pragma unroll
-  for (int g = 0; g < kPG; ++g) M = fmaxf(M, s_m[g][dg]);
-  float L = 0.f;
-  float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (M != -INFINITY) {
-#pragma unroll
-    for (int g = 0; g < kPG; ++g) {
-      const float w = exp2f(s_m[g][dg] - M);  // 0 for a group with only empty partitions
-      const float4 v = s_acc[g][dg];
-      L = fmaf(w, s_l[g][dg], L);
-      t.x = fmaf(w, v.x, t.x);
-      t.y = fmaf(w, v.y, t.y);
-      t.z = fmaf(w, v.z, t.z);
-      t.w = fmaf(w, v.w, t.w);
-    }
+  for (int g = 1; g < kPG; ++g) {
+    const float4 a = s_acc[g][dg];
+    acc.x += a.x;
+    acc.y += a.y;
+    acc.z += a.z;
+    acc.w += a.w;
+    L += s_l[g][dg];
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
   __nv_bfloat16* o = out + static_cast<size_t>(bh) * D + 4 * dg;
-  *reinterpret_cast<__nv_bfloat162*>(o) = __floats2bfloat162_rn(t.x * inv, t.y * inv);
-  *reinterpret_cast<__nv_bfloat162*>(o + 2) = __floats2bfloat162_rn(t.z * inv, t.w * inv);
+  *reinterpret_cast<__nv_bfloat162*>(o) = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+  *reinterpret_cast<__nv_bfloat162*>(o + 2) = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+}
+
+// ---------------------------------------------------------------------------
+// merge for rows of at most 32 partitions: one warp per row, 2 rows per CTA.
+// Lane p loads partition p's (m, l); the warp reduces M and L; then every
+// lane loads its D/32 columns of all partitions at once (independent loads)
+// and weights them with 2^(m_p - M) taken from lane p.
+// ---------------------------------------------------------------------------
+constexpr int kMergeRowsPerCta = 2;
+constexpr int kMergeWarpMaxParts = 32;
+
+template <int D>
+__global__ void __launch_bounds__(kMergeRowsPerCta * 32)
+    merge_rows_kernel(const float* __restrict__ part_ml, const float* __restrict__ part_o,
+                      const int32_t* __restrict__ unit_start, int rows_per_seq /* T * Hq */,
+                      int pmax, int num_rows, __nv_bfloat16* __restrict__ out) {
+  constexpr int kPer = D / 32;  // columns per lane
+  pdl_trigger();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * kMergeRowsPerCta + (threadIdx.x >> 5);  // (b * T + t) * Hq + h
+  if (row >= num_rows) return;
+  const int b = row / rows_per_seq;
+  const int P = unit_start[b + 1] - unit_start[b];
+  if (P < 2) return;  // written by the decode kernel (or zero-filled by the planner)
+  const size_t base = static_cast<size_t>(row) * pmax;
+  const float2 mine = lane < P ? reinterpret_cast<const float2*>(part_ml)[base + lane]
+                               : make_float2(-INFINITY, 0.f);
+  float M = mine.x;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+  const float w = (M == -INFINITY) ? 0.f : exp2f(mine.x - M);  // 0 past P and for empty partitions
+  float L = w * mine.y;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(kFull, L, o);
+  float acc[kPer];
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) acc[j] = 0.f;
+  const float* ob = part_o + base * D + lane * kPer;
+#pragma unroll 16
+  for (int p = 0; p < P; ++p) {
+    const float wp = __shfl_sync(kFull, w, p);
+    if constexpr (kPer == 4) {
+      const float4 v = *reinterpret_cast<const float4*>(ob + static_cast<size_t>(p) * D);
+      acc[0] = fmaf(wp, v.x, acc[0]);
+      acc[1] = fmaf(wp, v.y, acc[1]);
+      acc[2] = fmaf(wp, v.z, acc[2]);
+      acc[3] = fmaf(wp, v.w, acc[3]);
+    } else {
+      const float2 v = *reinterpret_cast<const float2*>(ob + static_cast<size_t>(p) * D);
+      acc[0] = fmaf(wp, v.x, acc[0]);
+      acc[1] = fmaf(wp, v.y, acc[1]);
+    }
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  __nv_bfloat16* o = out + static_cast<size_t>(row) * D + lane * kPer;
+#pragma unroll
+  for (int j = 0; j < kPer; j += 2)
+    *reinterpret_cast<__nv_bfloat162*>(o + j) = __floats2bfloat162_rn(acc[j] * inv, acc[j + 1] * inv);
 }
 
 // ---------------------------------------------------------------------------
@@ -363,23 +446,29 @@ cudaError_t launch_decode(const DecodeLaunch& L, int* launched) {
   if (L.ev_end != nullptr && (e = cudaEventRecord(L.ev_end, L.stream)) != cudaSuccess) return e;
   *launched += 1;
 
-  // 3. merge kernel when sequences may span many partitions
+  // 3. merge kernel when sequences may span many partitions: a warp per row
+  //    up to 32 partitions, a CTA per row beyond
   if (!p.fused_merge) {
+    const int rows = L.B * L.T * L.Hq;
+    const bool by_warp = L.pmax <= kMergeWarpMaxParts;
     cudaLaunchConfig_t mc{};
-    mc.gridDim = dim3(static_cast<unsigned>(L.B * L.T * L.Hq));
-    mc.blockDim = dim3(kMergeThreads);
+    mc.gridDim = dim3(static_cast<unsigned>(by_warp ? (rows + kMergeRowsPerCta - 1) / kMergeRowsPerCta : rows));
+    mc.blockDim = dim3(by_warp ? kMergeRowsPerCta * 32 : kMergeThreads);
     mc.dynamicSmemBytes = 0;
     mc.stream = L.stream;
     mc.attrs = attr;
     mc.numAttrs = (L.ev_end == nullptr) ? 1 : 0;
-    if (L.D == 64)
-      e = cudaLaunchKernelEx(&mc, merge_kernel<64>, static_cast<const float*>(L.part_ml),
-                             static_cast<const float*>(L.part_o), static_cast<const int32_t*>(L.unit_start),
-                             L.T * L.Hq, L.pmax, static_cast<__nv_bfloat16*>(L.out));
+    const float* pml = static_cast<const float*>(L.part_ml);
+    const float* po = static_cast<const float*>(L.part_o);
+    const int32_t* us = static_cast<const int32_t*>(L.unit_start);
+    __nv_bfloat16* o = static_cast<__nv_bfloat16*>(L.out);
+    const int rps = L.T * L.Hq;
+    if (by_warp)
+      e = L.D == 64 ? cudaLaunchKernelEx(&mc, merge_rows_kernel<64>, pml, po, us, rps, L.pmax, rows, o)
+                    : cudaLaunchKernelEx(&mc, merge_rows_kernel<128>, pml, po, us, rps, L.pmax, rows, o);
     else
-      e = cudaLaunchKernelEx(&mc, merge_kernel<128>, static_cast<const float*>(L.part_ml),
-                             static_cast<const float*>(L.part_o), static_cast<const int32_t*>(L.unit_start),
-                             L.T * L.Hq, L.pmax, static_cast<__nv_bfloat16*>(L.out));
+      e = L.D == 64 ? cudaLaunchKernelEx(&mc, merge_kernel<64>, pml, po, us, rps, L.pmax, o)
+                    : cudaLaunchKernelEx(&mc, merge_kernel<128>, pml, po, us, rps, L.pmax, o);
     if (e != cudaSuccess) return e;
     *launched += 1;
   }
