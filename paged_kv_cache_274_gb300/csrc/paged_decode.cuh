@@ -744,6 +744,73 @@ __device__ __forceinline__ void arrive_and_merge(const DecodeParams& p, int b, i
 }
 
 // ---------------------------------------------------------------------------
+// a unit's pages: physical ids, bad-id masks and dequantisation parameters;
+// lane i holds pages i and i + 32 (a unit has at most 64 pages)
+// ---------------------------------------------------------------------------
+struct UnitPages {
+  int e0, e1;
+  uint32_t badm0, badm1;
+  float ks0, ks1, vs0, vs1;  // E4M3 / INT8 scales (1 for bf16)
+  float kz0, kz1, vz0, vz1;  // INT8 zero points (0 otherwise)
+};
+
+template <bool FP8, bool I8>
+__device__ __forceinline__ UnitPages load_unit_pages(const DecodeParams& p, int kvh, const int* trow,
+                                                     int npages, int lane) {
+  UnitPages u;
+  u.e0 = 0;
+  u.e1 = 0;
+  bool bad0 = false, bad1 = false;
+  if (lane < npages) {
+    u.e0 = __ldg(trow + lane);
+    if (static_cast<unsigned>(u.e0) >= static_cast<unsigned>(p.NB)) { bad0 = true; u.e0 = 0; }
+  }
+  if (lane + 32 < npages) {
+    u.e1 = __ldg(trow + lane + 32);
+    if (static_cast<unsigned>(u.e1) >= static_cast<unsigned>(p.NB)) { bad1 = true; u.e1 = 0; }
+  }
+  u.badm0 = __ballot_sync(kFull, bad0);
+  u.badm1 = __ballot_sync(kFull, bad1);
+  u.ks0 = u.ks1 = u.vs0 = u.vs1 = 1.f;
+  u.kz0 = u.kz1 = u.vz0 = u.vz1 = 0.f;
+  if (FP8 && !I8) {
+    if (lane < npages) {
+      u.ks0 = __ldg(p.k_scale + static_cast<size_t>(u.e0) * p.Hkv + kvh);
+      u.vs0 = __ldg(p.v_scale + static_cast<size_t>(u.e0) * p.Hkv + kvh);
+    }
+    if (lane + 32 < npages) {
+      u.ks1 = __ldg(p.k_scale + static_cast<size_t>(u.e1) * p.Hkv + kvh);
+      u.vs1 = __ldg(p.v_scale + static_cast<size_t>(u.e1) * p.Hkv + kvh);
+    }
+  } else if (I8) {
+    const float2* kp2 = reinterpret_cast<const float2*>(p.k_scale);
+    const float2* vp2 = reinterpret_cast<const float2*>(p.v_scale);
+    if (lane < npages) {
+      const float2 a = __ldg(kp2 + static_cast<size_t>(u.e0) * p.Hkv + kvh);
+      const float2 c = __ldg(vp2 + static_cast<size_t>(u.e0) * p.Hkv + kvh);
+      u.ks0 = a.x; u.kz0 = a.y; u.vs0 = c.x; u.vz0 = c.y;
+    }
+    if (lane + 32 < npages) {
+      const float2 a = __ldg(kp2 + static_cast<size_t>(u.e1) * p.Hkv + kvh);
+      const float2 c = __ldg(vp2 + static_cast<size_t>(u.e1) * p.Hkv + kvh);
+      u.ks1 = a.x; u.kz1 = a.y; u.vs1 = c.x; u.vz1 = c.y;
+    }
+  }
+  return u;
+}
+
+// Page j's value of a per-lane pair (lane j holds pages j, j + 32); warp-wide.
+__device__ __forceinline__ float unit_pick(float v0, float v1, int j) {
+  return (j < 32) ? __shfl_sync(kFull, v0, j & 31) : __shfl_sync(kFull, v1, j & 31);
+}
+__device__ __forceinline__ int unit_pick(int v0, int v1, int j) {
+  return (j < 32) ? __shfl_sync(kFull, v0, j & 31) : __shfl_sync(kFull, v1, j & 31);
+}
+__device__ __forceinline__ bool unit_bad(const UnitPages& u, int j) {
+  return (j < 32) ? ((u.badm0 >> (j & 31)) & 1u) : ((u.badm1 >> (j & 31)) & 1u);
+}
+
+// ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
 // MT: multi-token queries (T >= 1, row tiles, per-row causal limits);
@@ -809,48 +876,11 @@ __global__ void __launch_bounds__(256, 1)
     const int npages = (t1 - t0 + BS - 1) / BS;
     const int* trow = p.block_tables + static_cast<size_t>(b) * p.MB + t0 / BS;
 
-    // physical ids of this unit's pages: lane i holds pages i and i + 32
-    int e0 = 0, e1 = 0;
-    bool bad0 = false, bad1 = false;
-    if (lane < npages) {
-      e0 = __ldg(trow + lane);
-      if (static_cast<unsigned>(e0) >= static_cast<unsigned>(p.NB)) { bad0 = true; e0 = 0; }
-    }
-    if (lane + 32 < npages) {
-      e1 = __ldg(trow + lane + 32);
-      if (static_cast<unsigned>(e1) >= static_cast<unsigned>(p.NB)) { bad1 = true; e1 = 0; }
-    }
-    const uint32_t badm0 = __ballot_sync(kFull, bad0), badm1 = __ballot_sync(kFull, bad1);
-    if (lane == 0 && (badm0 | badm1)) atomicOr(p.err, PKV_DEVERR_BLOCK_ID);
-    // per-page dequantisation parameters (E4M3: scale; INT8: scale, zero)
-    float ks0 = 1.f, ks1 = 1.f, vs0 = 1.f, vs1 = 1.f;
-    float kz0 = 0.f, kz1 = 0.f, vz0 = 0.f, vz1 = 0.f;
-    if (FP8 && !I8) {
-      if (lane < npages) {
-        ks0 = __ldg(p.k_scale + static_cast<size_t>(e0) * p.Hkv + kvh);
-        vs0 = __ldg(p.v_scale + static_cast<size_t>(e0) * p.Hkv + kvh);
-      }
-      if (lane + 32 < npages) {
-        ks1 = __ldg(p.k_scale + static_cast<size_t>(e1) * p.Hkv + kvh);
-        vs1 = __ldg(p.v_scale + static_cast<size_t>(e1) * p.Hkv + kvh);
-      }
-    } else if (I8) {
-      const float2* kp2 = reinterpret_cast<const float2*>(p.k_scale);
-      const float2* vp2 = reinterpret_cast<const float2*>(p.v_scale);
-      if (lane < npages) {
-        const float2 a = __ldg(kp2 + static_cast<size_t>(e0) * p.Hkv + kvh);
-        const float2 c = __ldg(vp2 + static_cast<size_t>(e0) * p.Hkv + kvh);
-        ks0 = a.x; kz0 = a.y; vs0 = c.x; vz0 = c.y;
-      }
-      if (lane + 32 < npages) {
-        const float2 a = __ldg(kp2 + static_cast<size_t>(e1) * p.Hkv + kvh);
-        const float2 c = __ldg(vp2 + static_cast<size_t>(e1) * p.Hkv + kvh);
-        ks1 = a.x; kz1 = a.y; vs1 = c.x; vz1 = c.y;
-      }
-    }
+    const UnitPages up = load_unit_pages<FP8, I8>(p, kvh, trow, npages, lane);
+    if (lane == 0 && (up.badm0 | up.badm1)) atomicOr(p.err, PKV_DEVERR_BLOCK_ID);
 
     auto issue = [&](int j, uint32_t slot_it) {
-      const int phys = (j < 32) ? __shfl_sync(kFull, e0, j & 31) : __shfl_sync(kFull, e1, j & 31);
+      const int phys = unit_pick(up.e0, up.e1, j);
       if (lane == 0) {
         const int s = static_cast<int>(slot_it % static_cast<uint32_t>(R));
         uint8_t* st = ring + static_cast<size_t>(s) * Geo::kStageBytes;
@@ -893,16 +923,15 @@ __global__ void __launch_bounds__(256, 1)
         const uint32_t s = it % static_cast<uint32_t>(R);
         const bool landed = mbar_wait_bounded(&bars[s], (it / R) & 1u, kWaitLimitNs);
         if (!__all_sync(kFull, landed)) { timed_out = true; break; }
-        const bool bad = (j < 32) ? ((badm0 >> (j & 31)) & 1u) : ((badm1 >> (j & 31)) & 1u);
-        const int valid = bad ? 0 : min(BS, t1 - (t0 + j * BS));
+        const int valid = unit_bad(up, j) ? 0 : min(BS, t1 - (t0 + j * BS));
         float ksc = 1.f, vsc = 1.f, kc = 0.f, vc = 0.f;
         if (FP8) {
-          ksc = (j < 32) ? __shfl_sync(kFull, ks0, j & 31) : __shfl_sync(kFull, ks1, j & 31);
-          vsc = (j < 32) ? __shfl_sync(kFull, vs0, j & 31) : __shfl_sync(kFull, vs1, j & 31);
+          ksc = unit_pick(up.ks0, up.ks1, j);
+          vsc = unit_pick(up.vs0, up.vs1, j);
         }
         if (I8) {
-          kc = kInt8Bias + ((j < 32) ? __shfl_sync(kFull, kz0, j & 31) : __shfl_sync(kFull, kz1, j & 31));
-          vc = kInt8Bias + ((j < 32) ? __shfl_sync(kFull, vz0, j & 31) : __shfl_sync(kFull, vz1, j & 31));
+          kc = kInt8Bias + unit_pick(up.kz0, up.kz1, j);
+          vc = kInt8Bias + unit_pick(up.vz0, up.vz1, j);
         }
         const int pos0 = t0 + j * BS;
         int rv[kR];
@@ -931,17 +960,16 @@ __global__ void __launch_bounds__(256, 1)
         const uint32_t s = it % static_cast<uint32_t>(R);
         const bool landed = mbar_wait_bounded(&bars[s], (it / R) & 1u, kWaitLimitNs);
         if (!__all_sync(kFull, landed)) { timed_out = true; break; }
-        const bool bad = (j < 32) ? ((badm0 >> (j & 31)) & 1u) : ((badm1 >> (j & 31)) & 1u);
-        const int valid = bad ? 0 : min(BS, t1 - (t0 + j * BS));
+        const int valid = unit_bad(up, j) ? 0 : min(BS, t1 - (t0 + j * BS));
         float ksc = 1.f, vsc = 1.f;
         uint32_t kzc = 0u, vzc = 0u;
         if (FP8) {
-          ksc = (j < 32) ? __shfl_sync(kFull, ks0, j & 31) : __shfl_sync(kFull, ks1, j & 31);
-          vsc = (j < 32) ? __shfl_sync(kFull, vs0, j & 31) : __shfl_sync(kFull, vs1, j & 31);
+          ksc = unit_pick(up.ks0, up.ks1, j);
+          vsc = unit_pick(up.vs0, up.vs1, j);
         }
         if (I8) {
-          kzc = int8_zero_const((j < 32) ? __shfl_sync(kFull, kz0, j & 31) : __shfl_sync(kFull, kz1, j & 31));
-          vzc = int8_zero_const((j < 32) ? __shfl_sync(kFull, vz0, j & 31) : __shfl_sync(kFull, vz1, j & 31));
+          kzc = int8_zero_const(unit_pick(up.kz0, up.kz1, j));
+          vzc = int8_zero_const(unit_pick(up.vz0, up.vz1, j));
         }
         ffma_page<D, BS, FP8, (GT > 0 ? GT : 1), I8>(st, ring + static_cast<size_t>(s) * Geo::kStageBytes,
                                                      valid, p.scale_log2 * ksc, vsc, kzc, vzc, pbuf, lane);

@@ -141,3 +141,21 @@ def test_ffma_rejects_multi_token():
     q = to_dev_bf16(_q(111, 2, 2, 8, 64))
     with pytest.raises(pkv.PkvError):
         pkv.paged_decode_multi(q, dc.k, dc.v, dc.bt, dc.cl, opts=pkv.decode_opts(math=pkv.MATH_FFMA))
+
+
+@pytest.mark.parametrize("stages", [2, 3, 6])
+@pytest.mark.parametrize("T,Hq,Hkv", [(8, 32, 8), (16, 32, 8), (3, 16, 1)])
+def test_multi_tile_ring_depths(stages, T, Hq, Hkv):
+    # several row tiles per KV head, each its own stream over the pages, at
+    # every ring depth, over many units and partitions
+    lens = [T + 1, 300, 611, 64]
+    c = random_case(120 + T + stages, len(lens), Hq, Hkv, 128, 16, lens, poison=True)
+    dc = DeviceCase(c)
+    q = _q(121 + T, c.B, T, Hq, 128)
+    plan = pkv.decode_plan(dc.k, c.B, Hq, c.MB, pkv.decode_opts(stages=stages), T)
+    assert plan["row_tiles"] > 1 and plan["stages"] == stages
+    out = pkv.paged_decode_multi(to_dev_bf16(q), dc.k, dc.v, dc.bt, dc.cl, [0], 0, c.scale,
+                                 opts=pkv.decode_opts(stages=stages, partition_blocks=5))
+    torch.cuda.synchronize()
+    assert pkv.read_device_error() == 0
+    assert_close(bf16_dev_to_f64(out), _oracle(dc, q), f"T={T} stages={stages}")
