@@ -1,8 +1,9 @@
 """Benchmark: paged decode over a paged KV cache on GB300.
 
 One step = one pass of the whole hot path over one batch:
-  llama8b_layer (default): kv_append of each sequence's newest token, then
-      paged_decode of 64 sequences x 32 query heads at context 4096
+  llama8b_layer (default): the append of each sequence's newest token and
+      the decode of 64 sequences x 32 query heads at context 4096, in one
+      append_and_decode call
       (8 KV heads, head_dim 128, block 16, bf16) -- 1 GiB of KV read;
   long_b4_32k / long_b1_128k: paged_decode, 64 q / 8 KV heads, block 32;
   mixed_prefix: 256 sequences, log-uniform lengths, shared prefix blocks;
@@ -285,7 +286,7 @@ class DeviceWorkload:
         self.plan = pkv.decode_plan(self.k, c.B, c.Hq, c.MB, self.opts)
         self.layers = list(range(c.L))
         self.kv_bytes = kv_bytes_of(c)
-        self.launches_per_step = (1 if self.append else 0) + len(self.layers) * self.plan["kernels_per_call"]
+        self.launches_per_step = len(self.layers) * self.plan["kernels_per_call"]
         torch.cuda.synchronize()
 
     def _fill_fp8(self, g):
@@ -330,17 +331,20 @@ class DeviceWorkload:
         torch.cuda.synchronize()
 
     def step(self, events=None):
-        """One decode step; `events`: optional list of (start, end) per layer call."""
+        """One decode step; `events`: optional list of (start, end) per layer
+        call.  The step's append rides in the first layer call's planner
+        launch (append_and_decode)."""
         pkv, c = self.pkv, self.c
-        if self.append:
-            pkv.kv_append(self.k_new, self.v_new, self.slots, self.k, self.v)
         for i, layer in enumerate(self.layers):
             opts = self.opts
             if events is not None:
                 opts = pkv.decode_opts(**self.opts_kw, event_start=events[i][0], event_end=events[i][1])
-            pkv.paged_decode(self.q[layer], self.k, self.v, self.bt, self.cl, c.kv_group_ptr.tolist(),
-                             layer, c.scale, out=self.out[layer], workspace=self.ws,
-                             k_scale=self.ks, v_scale=self.vs, opts=opts)
+            args = (self.q[layer], self.k, self.v, self.bt, self.cl, c.kv_group_ptr.tolist(), layer, c.scale)
+            kw = dict(out=self.out[layer], workspace=self.ws, k_scale=self.ks, v_scale=self.vs, opts=opts)
+            if self.append and i == 0:
+                pkv.append_and_decode(self.k_new, self.v_new, self.slots, *args, **kw)
+            else:
+                pkv.paged_decode(*args, **kw)
 
 
 class VerifyWorkload(DeviceWorkload):
@@ -366,19 +370,18 @@ class VerifyWorkload(DeviceWorkload):
         self.append = True
         self.ws = pkv.new_decode_workspace(self.k, c.B, c.Hq, c.MB, self.opts, T)
         self.plan = pkv.decode_plan(self.k, c.B, c.Hq, c.MB, self.opts, T)
-        self.launches_per_step = 1 + len(self.layers) * self.plan["kernels_per_call"]
+        self.launches_per_step = len(self.layers) * self.plan["kernels_per_call"]
         torch.cuda.synchronize()
 
     def step(self, events=None):
         pkv, c = self.pkv, self.c
-        pkv.kv_append(self.k_new, self.v_new, self.slots, self.k, self.v, self.ks, self.vs)
         for i, layer in enumerate(self.layers):
             opts = self.opts
             if events is not None:
                 opts = pkv.decode_opts(**self.opts_kw, event_start=events[i][0], event_end=events[i][1])
-            pkv.paged_decode_multi(self.q[layer], self.k, self.v, self.bt, self.cl, c.kv_group_ptr.tolist(),
-                                   layer, c.scale, out=self.out[layer], workspace=self.ws,
-                                   k_scale=self.ks, v_scale=self.vs, opts=opts)
+            pkv.append_and_decode(self.k_new, self.v_new, self.slots, self.q[layer], self.k, self.v, self.bt,
+                                  self.cl, c.kv_group_ptr.tolist(), layer, c.scale, out=self.out[layer],
+                                  workspace=self.ws, k_scale=self.ks, v_scale=self.vs, opts=opts)
 
 
 class CopyWorkload:
@@ -455,45 +458,76 @@ def time_device(w, steps, warmup, world):
 
 
 def time_e2e(w, steps, warmup, world):
-    """Through the public API from pinned host memory: each step copies its
-    inputs (queries, new tokens and slots, block tables, lengths) host->device
-    as one packed staging buffer, runs the step, and copies the outputs
-    device->host.  The step's device tensors are views into the device copy
-    of that buffer."""
+    """Through the public API from pinned host memory, pipelined as a serving
+    loop would be: each step's inputs (queries, new tokens and slots, block
+    tables, lengths) go host->device as one packed staging buffer on a copy
+    stream while the previous step computes, and each step's output goes
+    device->host on a second copy stream while the next step computes (two
+    streams, so that no upload queues behind a download).  Staging
+    and output buffers are double-buffered; events order every copy against
+    the compute that produces or consumes it.  The timed region spans the
+    first upload to the last download."""
     names = ["q", "bt", "cl"] + (["k_new", "v_new", "slots"] if w.append else [])
     tensors = [getattr(w, n) for n in names]
     offs, off = [], 0
     for t in tensors:
         offs.append(off)
         off += (t.numel() * t.element_size() + 255) // 256 * 256
-    dev_blob = torch.empty(off, dtype=torch.uint8, device=w.dev)
     host_blob = torch.empty(off, dtype=torch.uint8).pin_memory()
+    dev_blobs = [torch.empty(off, dtype=torch.uint8, device=w.dev) for _ in range(2)]
+    views = [{}, {}]
     for n, t, o in zip(names, tensors, offs):
         nbytes = t.numel() * t.element_size()
-        view = dev_blob[o:o + nbytes].view(t.dtype).view(t.shape)
-        view.copy_(t)
-        host_blob[o:o + nbytes].copy_(view.view(torch.uint8).reshape(-1).cpu())
-        setattr(w, n, view)
+        for k in range(2):
+            v = dev_blobs[k][o:o + nbytes].view(t.dtype).view(t.shape)
+            v.copy_(t)
+            views[k][n] = v
+        host_blob[o:o + nbytes].copy_(views[0][n].view(torch.uint8).reshape(-1).cpu())
+    outs = [w.out, torch.empty_like(w.out)]
     out_host = torch.empty(w.out.shape, dtype=w.out.dtype).pin_memory()
     h2d = off
     d2h = out_host.numel() * out_host.element_size()
+    compute = torch.cuda.current_stream()
+    up = torch.cuda.Stream(device=w.dev)     # host -> device (next step's inputs)
+    down = torch.cuda.Stream(device=w.dev)   # device -> host (previous step's output)
+    ev_in = [torch.cuda.Event() for _ in range(2)]     # inputs of buffer k uploaded
+    ev_used = [torch.cuda.Event() for _ in range(2)]   # step on buffer k done (inputs read, out written)
+    ev_out = [torch.cuda.Event() for _ in range(2)]    # out of buffer k downloaded
+    for k in range(2):
+        for e in (ev_used[k], ev_out[k]):
+            e.record(compute)
 
-    def one():
-        dev_blob.copy_(host_blob, non_blocking=True)
-        w.step()
-        out_host.copy_(w.out, non_blocking=True)
+    def run(n):
+        for i in range(n):
+            k = i % 2
+            with torch.cuda.stream(up):
+                up.wait_event(ev_used[k])               # buffer k no longer read by step i-2
+                dev_blobs[k].copy_(host_blob, non_blocking=True)
+                ev_in[k].record(up)
+            compute.wait_event(ev_in[k])
+            compute.wait_event(ev_out[k])               # out buffer k downloaded (step i-2)
+            for n_, v in views[k].items():
+                setattr(w, n_, v)
+            w.out = outs[k]
+            w.step()
+            ev_used[k].record(compute)
+            with torch.cuda.stream(down):
+                down.wait_event(ev_used[k])
+                out_host.copy_(outs[k], non_blocking=True)
+                ev_out[k].record(down)
 
-    for _ in range(warmup):
-        one()
+    run(warmup)
     torch.cuda.synchronize()
     barrier(world)
-    stream = torch.cuda.current_stream()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0 = time.perf_counter()
-    start.record(stream)
-    for _ in range(steps):
-        one()
-    end.record(stream)
+    start.record(compute)
+    up.wait_event(start)
+    down.wait_event(start)
+    run(steps)
+    compute.wait_stream(up)
+    compute.wait_stream(down)
+    end.record(compute)
     torch.cuda.synchronize()
     wall_ms = (time.perf_counter() - t0) * 1e3
     barrier(world)
@@ -673,7 +707,7 @@ def run_ours(args, rank, world):
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": w.launches_per_step * args.steps,
-            "gpu_launches_note": "kernels of the headline loop (kv_append, planner, decode per layer call)",
+            "gpu_launches_note": "kernels of the headline loop per layer call: planner (with the step's append on extra CTAs), decode, merge when more than 4 partitions",
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

@@ -260,6 +260,35 @@ pkv_status pkv_paged_decode_multi(const pkv_cache_desc* cache,
                                   void* workspace, size_t workspace_bytes,
                                   const pkv_decode_opts* opts, void* stream);
 
+/*
+ * One decode step in one call: append the step's new tokens into cache slot
+ * kv_group_ptr[layer] (exactly pkv_kv_append with that slot), then decode
+ * (exactly pkv_paged_decode_multi; num_query_tokens = 1 is pkv_paged_decode).
+ * The append runs on extra CTAs of the decode's planner launch, so the step
+ * costs one launch less and the append and the planning overlap.
+ * Sources: [BW] "What the KV Cache Stores and Why" (a step stores the new
+ * token's K,V, then attends over the whole cache).
+ *
+ *   k_new, v_new, slot_mapping, num_new_tokens   as pkv_kv_append's k, v,
+ *                  slot_mapping, num_tokens (0: no append).
+ *   everything else as in pkv_paged_decode_multi; k_cache and v_cache are
+ *                  written (the append) before they are read.
+ * Same results, bit for bit, as the two separate calls.
+ */
+pkv_status pkv_append_and_decode(const pkv_cache_desc* cache,
+                                 const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                                 int32_t num_new_tokens,
+                                 const void* q, int32_t batch, int32_t num_query_tokens,
+                                 int32_t num_q_heads,
+                                 void* k_cache, void* v_cache,
+                                 const float* k_scale, const float* v_scale,
+                                 const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                 const int32_t* context_lens,
+                                 const int32_t* kv_group_ptr, int32_t num_layers, int32_t layer,
+                                 float scale, void* out,
+                                 void* workspace, size_t workspace_bytes,
+                                 const pkv_decode_opts* opts, void* stream);
+
 /* Workspace bytes and launch plan of pkv_paged_decode_multi (0 / an error
  * status for invalid arguments), as for the single-token calls. */
 size_t pkv_decode_multi_workspace_bytes(const pkv_cache_desc* cache, int32_t batch,

@@ -101,6 +101,9 @@ def load() -> ctypes.CDLL:
         lib.pkv_paged_decode_multi.restype = ctypes.c_int
         lib.pkv_paged_decode_multi.argtypes = [pdesc, P, i32, i32, i32, P, P, P, P, P, i32, P, P, i32,
                                                i32, f32, P, P, sz, popts, P]
+        lib.pkv_append_and_decode.restype = ctypes.c_int
+        lib.pkv_append_and_decode.argtypes = [pdesc, P, P, P, i32, P, i32, i32, i32, P, P, P, P, P, i32, P,
+                                              P, i32, i32, f32, P, P, sz, popts, P]
         lib.pkv_paged_decode_static_workspace.restype = ctypes.c_int
         lib.pkv_paged_decode_static_workspace.argtypes = [pdesc, P, i32, i32, P, P, P, P, P, i32, P,
                                                           P, i32, i32, f32, P, popts, P]
@@ -331,6 +334,57 @@ def paged_decode_multi(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Te
         _ptr(v_scale), _ptr(block_tables), MB, _ptr(context_lens), gp, len(kv_group_ptr),
         int(layer), float(scale), _ptr(out), _ptr(workspace), int(workspace.numel()),
         ctypes.byref(opts) if opts is not None else None, _stream_handle(stream)))
+    return out
+
+
+def append_and_decode(k_new: torch.Tensor, v_new: torch.Tensor, slot_mapping: torch.Tensor,
+                      q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                      block_tables: torch.Tensor, context_lens: torch.Tensor,
+                      kv_group_ptr: Sequence[int] = (0,), layer: int = 0,
+                      scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                      workspace: Optional[torch.Tensor] = None,
+                      k_scale: Optional[torch.Tensor] = None, v_scale: Optional[torch.Tensor] = None,
+                      opts: Optional[DecodeOpts] = None, stream=None) -> torch.Tensor:
+    """One step in one call: :func:`kv_append` of k_new / v_new [N][Hkv][D]
+    at ``slot_mapping`` into cache slot ``kv_group_ptr[layer]``, then
+    :func:`paged_decode` (q [B][Hq][D]) or :func:`paged_decode_multi`
+    (q [B][T][Hq][D]).  Returns out, shaped like q."""
+    desc = cache_desc(k_cache)
+    for n, t, dt in (("k_new", k_new, torch.bfloat16), ("v_new", v_new, torch.bfloat16),
+                     ("slot_mapping", slot_mapping, torch.int64), ("q", q, torch.bfloat16),
+                     ("block_tables", block_tables, torch.int32), ("context_lens", context_lens, torch.int32)):
+        _need_cuda(n, t, dt)
+    _need_cuda("k_cache", k_cache)
+    _need_cuda("v_cache", v_cache, k_cache.dtype)
+    if q.dim() == 3:
+        B, Hq, D = (int(x) for x in q.shape)
+        T = 1
+    elif q.dim() == 4:
+        B, T, Hq, D = (int(x) for x in q.shape)
+    else:
+        raise PkvError(1, "q must be [B][Hq][D] or [B][T][Hq][D]")
+    if D != desc.head_dim or block_tables.dim() != 2 or block_tables.shape[0] != B:
+        raise PkvError(1, "q / block_tables shapes do not match the cache")
+    N = int(slot_mapping.numel())
+    if k_new.shape != (N, desc.num_kv_heads, desc.head_dim) or v_new.shape != k_new.shape:
+        raise PkvError(1, "k_new / v_new must be [N][Hkv][D] with N = len(slot_mapping)")
+    MB = int(block_tables.shape[1])
+    if out is None:
+        out = torch.empty_like(q)
+    _need_cuda("out", out, torch.bfloat16)
+    if desc.dtype != KV_BF16:
+        _need_page_params(desc, k_scale, "k_scale")
+        _need_page_params(desc, v_scale, "v_scale")
+    if workspace is None:
+        workspace = new_decode_workspace(k_cache, B, Hq, MB, opts, T)
+    gp = (ctypes.c_int32 * len(kv_group_ptr))(*[int(x) for x in kv_group_ptr])
+    if scale is None:
+        scale = D ** -0.5
+    _check(load().pkv_append_and_decode(
+        ctypes.byref(desc), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), N, _ptr(q), B, T, Hq,
+        _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_tables), MB,
+        _ptr(context_lens), gp, len(kv_group_ptr), int(layer), float(scale), _ptr(out), _ptr(workspace),
+        int(workspace.numel()), ctypes.byref(opts) if opts is not None else None, _stream_handle(stream)))
     return out
 
 

@@ -16,6 +16,7 @@
 #include <tuple>
 #include <vector>
 
+#include "kv_append.cuh"
 #include "paged_decode.cuh"
 #include "pkv_internal.h"
 
@@ -42,15 +43,25 @@ constexpr int kPlanThreads = 1024;
 // in-kernel merge is serial per (sequence, KV head) and lands in the tail).
 constexpr int kFusedMergeMaxParts = 4;
 
+// KV >= 0: CTAs 1.. of the same launch first run a KV append of that kind
+// (pkv_kv_dtype), so that a decode step's append and plan cost one launch.
+template <int KV>
 __global__ void __launch_bounds__(kPlanThreads)
     plan_kernel(const int32_t* __restrict__ context_lens, int B, int num_arrive /* B * Hkv * NT */,
                 int max_ctx, int tokens_per_part, int32_t* work_counter, int32_t* unit_start,
                 int32_t* ctx_eff, int32_t* arrive, __nv_bfloat16* out,
-                int row_elems /* T * Hq * D */, unsigned* err) {
+                int row_elems /* T * Hq * D */, unsigned* err, const AppendArgs app) {
   __shared__ int warp_tot[kPlanThreads / 32];
   __shared__ int carry_s;
   pdl_trigger();
   pdl_wait();
+  if constexpr (KV >= 0) {
+    if (blockIdx.x > 0) {  // block-uniform: these CTAs never reach the planner's barriers
+      append_chunks<KV>(app, (blockIdx.x - 1) * static_cast<int64_t>(blockDim.x) + threadIdx.x,
+                        static_cast<int64_t>(gridDim.x - 1) * blockDim.x);
+      return;
+    }
+  }
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) carry_s = 0;
   __syncthreads();
@@ -379,18 +390,29 @@ cudaError_t launch_decode(const DecodeLaunch& L, int* launched) {
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
 
-  // 1. planner
+  // 1. planner (with the step's KV append on extra CTAs when one is given)
   {
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(1);
+    long long append_blocks = 0;
+    if (L.append != nullptr) {
+      const long long total = 2LL * L.append->N * L.append->Hkv * (L.append->D / 8);
+      append_blocks = std::min<long long>((total + kPlanThreads - 1) / kPlanThreads, 1 << 16);
+    }
+    cfg.gridDim = dim3(static_cast<unsigned>(1 + append_blocks));
     cfg.blockDim = dim3(kPlanThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = L.stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, plan_kernel, L.context_lens, L.B, L.B * L.Hkv * L.NT, L.MB * L.bs,
+    const AppendArgs none{};
+    const AppendArgs& app = L.append != nullptr ? *L.append : none;
+    auto plan = L.append == nullptr                ? plan_kernel<-1>
+                : L.append_kind == PKV_KV_INT8      ? plan_kernel<PKV_KV_INT8>
+                : L.append_kind == PKV_KV_FP8_E4M3  ? plan_kernel<PKV_KV_FP8_E4M3>
+                                                    : plan_kernel<PKV_KV_BF16>;
+    e = cudaLaunchKernelEx(&cfg, plan, L.context_lens, L.B, L.B * L.Hkv * L.NT, L.MB * L.bs,
                            L.ppu * L.bs, L.work_counter, L.unit_start, L.ctx_eff, L.arrive,
-                           static_cast<__nv_bfloat16*>(L.out), L.T * L.Hq * L.D, L.err);
+                           static_cast<__nv_bfloat16*>(L.out), L.T * L.Hq * L.D, L.err, app);
     if (e != cudaSuccess) return e;
     *launched += 1;
   }

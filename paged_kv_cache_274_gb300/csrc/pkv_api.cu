@@ -190,15 +190,17 @@ const char* pkv_status_string(pkv_status s) {
 
 const char* pkv_last_error_message(void) { return t_last_error.c_str(); }
 
-pkv_status pkv_kv_append(const pkv_cache_desc* cache, int32_t slot, const void* k, const void* v,
-                         const int64_t* slot_mapping, int32_t num_tokens, void* k_cache,
-                         void* v_cache, const float* k_scale, const float* v_scale, void* stream) {
-  pkv_status st = check_cache_desc(cache);
-  if (st != PKV_OK) return st;
+}  // extern "C"
+
+// Validate a KV append into cache slot `slot` and resolve its launch
+// arguments; *a is left untouched unless PKV_OK.  num_tokens >= 1.
+static pkv_status prepare_append(const pkv_cache_desc* cache, int32_t slot, const void* k, const void* v,
+                                 const int64_t* slot_mapping, int32_t num_tokens, void* k_cache,
+                                 void* v_cache, const float* k_scale, const float* v_scale,
+                                 cudaStream_t s, DeviceInfo* dev, pkv::AppendArgs* a) {
+  pkv_status st;
   if (slot < 0 || slot >= cache->num_slots)
     return fail(PKV_ERR_INVALID_ARG, "slot %d outside [0, %d)", slot, cache->num_slots);
-  if (num_tokens < 0) return fail(PKV_ERR_INVALID_ARG, "num_tokens %d < 0", num_tokens);
-  if (num_tokens == 0) return PKV_OK;
   const bool fp8 = cache->dtype != PKV_KV_BF16;  // one-byte elements (E4M3 or INT8)
   if (!k || !v || !slot_mapping || !k_cache || !v_cache)
     return fail(PKV_ERR_INVALID_ARG, "NULL tensor pointer");
@@ -209,9 +211,6 @@ pkv_status pkv_kv_append(const pkv_cache_desc* cache, int32_t slot, const void* 
     return fail(PKV_ERR_ALIGNMENT, "k, v and caches must be 16-byte aligned");
   if ((reinterpret_cast<uintptr_t>(slot_mapping) & 7u) != 0)
     return fail(PKV_ERR_ALIGNMENT, "slot_mapping must be 8-byte aligned");
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  DeviceInfo* dev = nullptr;
-  if ((st = device_info(&dev)) != PKV_OK) return st;
   const long long nslots = static_cast<long long>(cache->num_blocks) * cache->block_size;
   if (env_flag("PKV_VALIDATE")) {
     std::vector<int64_t> sm;
@@ -230,14 +229,53 @@ pkv_status pkv_kv_append(const pkv_cache_desc* cache, int32_t slot, const void* 
   const size_t page_elems = static_cast<size_t>(cache->num_kv_heads) * cache->block_size * cache->head_dim;
   const size_t slot_elems = page_elems * cache->num_blocks;
   const size_t elem = fp8 ? 1 : 2;
-  uint8_t* kb = static_cast<uint8_t*>(k_cache) + static_cast<size_t>(slot) * slot_elems * elem;
-  uint8_t* vb = static_cast<uint8_t*>(v_cache) + static_cast<size_t>(slot) * slot_elems * elem;
   const size_t scale_off = static_cast<size_t>(slot) * cache->num_blocks * cache->num_kv_heads *
                            (cache->dtype == PKV_KV_INT8 ? 2 : 1);
-  cudaError_t e = pkv::launch_kv_append(cache->dtype, k, v, slot_mapping, num_tokens, cache->num_kv_heads,
-                                        cache->head_dim, cache->block_size, nslots, kb, vb,
-                                        fp8 ? k_scale + scale_off : nullptr,
-                                        fp8 ? v_scale + scale_off : nullptr, dev->err_word, s);
+  a->k = static_cast<const uint4*>(k);
+  a->v = static_cast<const uint4*>(v);
+  a->slot_mapping = slot_mapping;
+  a->N = num_tokens;
+  a->Hkv = cache->num_kv_heads;
+  a->D = cache->head_dim;
+  a->bs = cache->block_size;
+  a->nslots = nslots;
+  a->kc = static_cast<uint8_t*>(k_cache) + static_cast<size_t>(slot) * slot_elems * elem;
+  a->vc = static_cast<uint8_t*>(v_cache) + static_cast<size_t>(slot) * slot_elems * elem;
+  a->ks = fp8 ? k_scale + scale_off : nullptr;
+  a->vs = fp8 ? v_scale + scale_off : nullptr;
+  a->err = dev->err_word;
+  return PKV_OK;
+}
+
+extern "C" {
+
+pkv_status pkv_kv_append(const pkv_cache_desc* cache, int32_t slot, const void* k, const void* v,
+                         const int64_t* slot_mapping, int32_t num_tokens, void* k_cache,
+                         void* v_cache, const float* k_scale, const float* v_scale, void* stream) {
+  pkv_status st = check_cache_desc(cache);
+  if (st != PKV_OK) return st;
+  if (slot < 0 || slot >= cache->num_slots)
+    return fail(PKV_ERR_INVALID_ARG, "slot %d outside [0, %d)", slot, cache->num_slots);
+  if (num_tokens < 0) return fail(PKV_ERR_INVALID_ARG, "num_tokens %d < 0", num_tokens);
+  if (num_tokens == 0) return PKV_OK;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache)
+    return fail(PKV_ERR_INVALID_ARG, "NULL tensor pointer");
+  const bool fp8 = cache->dtype != PKV_KV_BF16;
+  if (fp8 && (!k_scale || !v_scale)) return fail(PKV_ERR_INVALID_ARG, "E4M3 and INT8 caches need k_scale and v_scale");
+  if (fp8 && !scales_aligned(cache->dtype, k_scale, v_scale))
+    return fail(PKV_ERR_ALIGNMENT, "k_scale and v_scale must be 4-byte (E4M3) or 8-byte (INT8) aligned");
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache))
+    return fail(PKV_ERR_ALIGNMENT, "k, v and caches must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(slot_mapping) & 7u) != 0)
+    return fail(PKV_ERR_ALIGNMENT, "slot_mapping must be 8-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != PKV_OK) return st;
+  pkv::AppendArgs a{};
+  if ((st = prepare_append(cache, slot, k, v, slot_mapping, num_tokens, k_cache, v_cache, k_scale, v_scale, s,
+                           dev, &a)) != PKV_OK)
+    return st;
+  cudaError_t e = pkv::launch_kv_append(cache->dtype, a, s);
   if (e != cudaSuccess) return cuda_fail(e, "kv_append launch");
   return PKV_OK;
 }
@@ -395,14 +433,24 @@ pkv_status pkv_decode_describe(const pkv_cache_desc* cache, int32_t batch, int32
   return pkv_decode_multi_describe(cache, batch, 1, num_q_heads, max_blocks_per_seq, opts, plan);
 }
 
-pkv_status pkv_paged_decode_multi(const pkv_cache_desc* cache, const void* q, int32_t batch,
-                                  int32_t num_query_tokens, int32_t num_q_heads, const void* k_cache,
-                                  const void* v_cache, const float* k_scale, const float* v_scale,
-                                  const int32_t* block_tables, int32_t max_blocks_per_seq,
-                                  const int32_t* context_lens, const int32_t* kv_group_ptr,
-                                  int32_t num_layers, int32_t layer, float scale, void* out,
-                                  void* workspace, size_t workspace_bytes,
-                                  const pkv_decode_opts* opts, void* stream) {
+}  // extern "C"
+
+// The new tokens of a fused append-and-decode call.
+struct AppendRequest {
+  const void* k;
+  const void* v;
+  const int64_t* slot_mapping;
+  int32_t num_tokens;
+};
+
+static pkv_status decode_call(const pkv_cache_desc* cache, const void* q, int32_t batch,
+                              int32_t num_query_tokens, int32_t num_q_heads, const void* k_cache,
+                              const void* v_cache, const float* k_scale, const float* v_scale,
+                              const int32_t* block_tables, int32_t max_blocks_per_seq,
+                              const int32_t* context_lens, const int32_t* kv_group_ptr,
+                              int32_t num_layers, int32_t layer, float scale, void* out,
+                              void* workspace, size_t workspace_bytes,
+                              const pkv_decode_opts* opts, void* stream, const AppendRequest* req) {
   pkv::DecodeLaunch L;
   pkv_status st = resolve_decode(cache, batch, num_query_tokens, num_q_heads, max_blocks_per_seq, opts,
                                  152, &L);
@@ -413,7 +461,11 @@ pkv_status pkv_paged_decode_multi(const pkv_cache_desc* cache, const void* q, in
   if (slot < 0 || slot >= cache->num_slots)
     return fail(PKV_ERR_INVALID_ARG, "kv_group_ptr[%d] = %d outside [0, %d)", layer, slot, cache->num_slots);
   if (!std::isfinite(scale)) return fail(PKV_ERR_INVALID_ARG, "scale is not finite");
-  if (batch == 0) return PKV_OK;
+  if (batch == 0) {  // nothing to decode: only the append, if any
+    if (req == nullptr || req->num_tokens == 0) return PKV_OK;
+    return pkv_kv_append(cache, slot, req->k, req->v, req->slot_mapping, req->num_tokens,
+                         const_cast<void*>(k_cache), const_cast<void*>(v_cache), k_scale, v_scale, stream);
+  }
   const bool fp8 = cache->dtype != PKV_KV_BF16;  // one-byte elements (E4M3 or INT8)
   if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
     return fail(PKV_ERR_INVALID_ARG, "NULL tensor pointer");
@@ -478,10 +530,50 @@ pkv_status pkv_paged_decode_multi(const pkv_cache_desc* cache, const void* q, in
     L.ev_start = static_cast<cudaEvent_t>(opts->event_decode_start);
     L.ev_end = static_cast<cudaEvent_t>(opts->event_decode_end);
   }
+  pkv::AppendArgs app{};
+  if (req != nullptr && req->num_tokens > 0) {
+    if ((st = prepare_append(cache, slot, req->k, req->v, req->slot_mapping, req->num_tokens,
+                             const_cast<void*>(k_cache), const_cast<void*>(v_cache), k_scale, v_scale, s,
+                             dev, &app)) != PKV_OK)
+      return st;
+    L.append = &app;
+    L.append_kind = cache->dtype;
+  }
   int launched = 0;
   cudaError_t e = pkv::launch_decode(L, &launched);
   if (e != cudaSuccess) return cuda_fail(e, "paged_decode launch");
   return PKV_OK;
+}
+
+extern "C" {
+
+pkv_status pkv_paged_decode_multi(const pkv_cache_desc* cache, const void* q, int32_t batch,
+                                  int32_t num_query_tokens, int32_t num_q_heads, const void* k_cache,
+                                  const void* v_cache, const float* k_scale, const float* v_scale,
+                                  const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                  const int32_t* context_lens, const int32_t* kv_group_ptr,
+                                  int32_t num_layers, int32_t layer, float scale, void* out,
+                                  void* workspace, size_t workspace_bytes,
+                                  const pkv_decode_opts* opts, void* stream) {
+  return decode_call(cache, q, batch, num_query_tokens, num_q_heads, k_cache, v_cache, k_scale, v_scale,
+                     block_tables, max_blocks_per_seq, context_lens, kv_group_ptr, num_layers, layer, scale,
+                     out, workspace, workspace_bytes, opts, stream, nullptr);
+}
+
+pkv_status pkv_append_and_decode(const pkv_cache_desc* cache, const void* k_new, const void* v_new,
+                                 const int64_t* slot_mapping, int32_t num_new_tokens, const void* q,
+                                 int32_t batch, int32_t num_query_tokens, int32_t num_q_heads,
+                                 void* k_cache, void* v_cache, const float* k_scale, const float* v_scale,
+                                 const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                 const int32_t* context_lens, const int32_t* kv_group_ptr,
+                                 int32_t num_layers, int32_t layer, float scale, void* out,
+                                 void* workspace, size_t workspace_bytes, const pkv_decode_opts* opts,
+                                 void* stream) {
+  if (num_new_tokens < 0) return fail(PKV_ERR_INVALID_ARG, "num_new_tokens %d < 0", num_new_tokens);
+  const AppendRequest req{k_new, v_new, slot_mapping, num_new_tokens};
+  return decode_call(cache, q, batch, num_query_tokens, num_q_heads, k_cache, v_cache, k_scale, v_scale,
+                     block_tables, max_blocks_per_seq, context_lens, kv_group_ptr, num_layers, layer, scale,
+                     out, workspace, workspace_bytes, opts, stream, &req);
 }
 
 pkv_status pkv_paged_decode(const pkv_cache_desc* cache, const void* q, int32_t batch,

@@ -12,6 +12,21 @@
 
 namespace pkv {
 
+// One KV append, resolved and validated by the API layer: rows of N tokens
+// [N][Hkv][D] bf16 into the selected cache slot's pages.
+struct AppendArgs {
+  const uint4* k;
+  const uint4* v;
+  const int64_t* slot_mapping;
+  int N, Hkv, D, bs;
+  int64_t nslots;
+  uint8_t* kc;  // the slot's K pages
+  uint8_t* vc;
+  const float* ks;  // the slot's page parameters (one-byte caches)
+  const float* vs;
+  unsigned* err;
+};
+
 // Everything one decode launch needs, resolved and validated by the API layer.
 struct DecodeLaunch {
   const void* q;
@@ -44,6 +59,8 @@ struct DecodeLaunch {
   cudaStream_t stream;
   int num_sms;
   cudaEvent_t ev_start, ev_end;  // optional, recorded around the decode kernel
+  const AppendArgs* append;  // optional: append run by the planner launch (the decode sees it)
+  int append_kind;           // pkv_kv_dtype of that append
 };
 
 // Workspace layout for one decode call.
@@ -69,10 +86,7 @@ int decode_ctas_per_sm(const DecodeLaunch& L, size_t smem);
 void set_last_error_message(const char* msg);
 
 // KV append.
-cudaError_t launch_kv_append(int kv_dtype, const void* k, const void* v,
-                             const int64_t* slot_mapping, int N, int Hkv, int D, int bs,
-                             int64_t nslots, void* k_base, void* v_base, const float* ks_base,
-                             const float* vs_base, unsigned* err, cudaStream_t stream);
+cudaError_t launch_kv_append(int kv_dtype, const AppendArgs& a, cudaStream_t stream);
 
 // Block copy between two pools of the same page shape.
 cudaError_t launch_copy_blocks(const void* src_k, const void* src_v, const float* src_ks,
