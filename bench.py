@@ -60,7 +60,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", choices=WORKLOADS, default="llama8b_layer")
-    ap.add_argument("--math", choices=("auto", "mma", "ffma"), default="auto")
+    ap.add_argument("--math", choices=("auto", "mma", "ffma", "tc"), default="auto")
     ap.add_argument("--partition-blocks", type=int, default=0)
     ap.add_argument("--warps", type=int, default=0)
     ap.add_argument("--stages", type=int, default=0)
@@ -192,8 +192,8 @@ def profile_traffic(workload, math="mma"):
     """Per-launch DRAM bytes of the workload's kernel from the committed ncu
     summary, if it was taken on the current kernel sources; else None."""
     name = "copy_blocks_llama8b_pool" if workload == "copy_blocks" else f"paged_decode_{workload}"
-    if math == "ffma":
-        name += "_ffma"
+    if math in ("ffma", "tc"):
+        name += "_" + math
     path = os.path.join(ROOT, "profiles", f"{name}.md")
     try:
         text = open(path).read()
@@ -649,7 +649,7 @@ def run_ours(args, rank, world):
     import paged_kv_cache_274_gb300 as pkv
     pkv.load()   # fails loudly if the CUDA library is missing
     opts_kw = dict(partition_blocks=args.partition_blocks,
-                   math={"auto": pkv.MATH_AUTO, "mma": pkv.MATH_MMA, "ffma": pkv.MATH_FFMA}[args.math],
+                   math={"auto": pkv.MATH_AUTO, "mma": pkv.MATH_MMA, "ffma": pkv.MATH_FFMA, "tc": pkv.MATH_TC}[args.math],
                    warps=args.warps, stages=args.stages)
     copy = args.workload == "copy_blocks"
     if copy:
@@ -689,19 +689,20 @@ def run_ours(args, rank, world):
             "data": "synthetic (seeded N(0,1) K/V/q, seeded block permutations)",
             "config": config_of(args.workload, c, {
                 "parallelism": "replicas" if world > 1 else "single GPU",
-                "math": {0: "-", 1: "ffma", 2: "mma"}[plan["math"]],
+                "math": {0: "-", 1: "ffma", 2: "mma", 3: "tcgen05"}[plan["math"]],
                 "partition_blocks": plan["partition_blocks"], "max_partitions": plan["max_partitions"],
                 "warps_per_cta": plan["warps_per_cta"], "stages": plan["stages"]}),
             "kv_bytes_per_step": w.kv_bytes,
             "decode_steps_per_s": 1e3 / ms,
             "pct_of_hbm_peak": 100.0 * value / peak,
             "pct_of_nominal_8tbs": 100.0 * value / 8000.0,
-            "roofline": {"bound": "hbm", "kernel": "copy_blocks_kernel" if copy else "paged_decode_kernel",
+            "roofline": {"bound": "hbm", "kernel": "copy_blocks_kernel" if copy else
+                         ("paged_decode_tc_kernel" if plan["math"] == 3 else "paged_decode_kernel"),
                          "achieved": achieved,
                          "peak": peak, "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                          if peak_kind == "measured" else "fallback 6.8 TB/s",
                          "unit": "GB/s", "frac": achieved / peak,
-                         "traffic": profile_traffic(args.workload, {1: "ffma", 2: "mma"}.get(plan["math"], "mma")),
+                         "traffic": profile_traffic(args.workload, {1: "ffma", 2: "mma", 3: "tc"}.get(plan["math"], "mma")),
                          "algorithmic_bytes_per_launch": per_call_bytes,
                          "kernel_ms_mean": k_ms, "kernel_ms_median": statistics.median(kernel_ms)},
             "cpu_baseline": cpu,

@@ -31,7 +31,7 @@ PKV_OK = 0
 STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "alignment", 4: "cuda",
                 5: "device index error", 6: "workspace"}
 KV_BF16, KV_FP8_E4M3, KV_INT8 = 0, 1, 2
-MATH_AUTO, MATH_FFMA, MATH_MMA = 0, 1, 2
+MATH_AUTO, MATH_FFMA, MATH_MMA, MATH_TC = 0, 1, 2, 3
 DEVERR_BLOCK_ID, DEVERR_SLOT, DEVERR_CONTEXT_LEN, DEVERR_TIMEOUT = 1, 2, 4, 8
 
 

@@ -18,6 +18,7 @@
 
 #include "kv_append.cuh"
 #include "paged_decode.cuh"
+#include "paged_decode_tc.cuh"
 #include "pkv_internal.h"
 
 namespace pkv {
@@ -29,6 +30,7 @@ const void* decode_kernel_fp8_d128(int bs, int math, int gt);
 const void* decode_kernel_int8_d128(int bs, int math, int gt);
 const void* decode_kernel_mt_bf16(int D, int bs, int gt);
 const void* decode_kernel_mt_1byte(int kv_dtype, int bs, int gt);
+const void* decode_kernel_tc(int bs);
 
 // ---------------------------------------------------------------------------
 // planner: one CTA validates context lengths, counts each sequence's
@@ -297,7 +299,8 @@ WorkspaceLayout workspace_layout(int B, int T, int Hq, int Hkv, int NT, int D, i
   return w;
 }
 
-size_t decode_smem_bytes(int kv_fp8, int D, int bs, int warps, int stages) {
+size_t decode_smem_bytes(int kv_fp8, int D, int bs, int warps, int stages, int tc) {
+  if (tc) return tc_smem_layout_bytes();
   if (kv_fp8) {
     return bs == 16 ? decode_smem_layout_bytes<128, 16, true>(warps, stages)
                     : decode_smem_layout_bytes<128, 32, true>(warps, stages);
@@ -311,6 +314,7 @@ size_t decode_smem_bytes(int kv_fp8, int D, int bs, int warps, int stages) {
 
 // gt: query rows per tile; mt: multi-token kernel (T > 1).
 static const void* pick_kernel(int kv_dtype, int D, int bs, int math, int gt, bool mt) {
+  if (math == PKV_MATH_TC) return (kv_dtype == PKV_KV_BF16 && D == 128) ? decode_kernel_tc(bs) : nullptr;
   if (mt) {
     if (math != PKV_MATH_MMA) return nullptr;
     return kv_dtype == PKV_KV_BF16 ? decode_kernel_mt_bf16(D, bs, gt) : decode_kernel_mt_1byte(kv_dtype, bs, gt);
@@ -380,7 +384,7 @@ cudaError_t launch_decode(const DecodeLaunch& L, int* launched) {
   *launched = 0;
   const void* fn = pick_kernel(L.kv_dtype, L.D, L.bs, L.math, L.G * L.Tt, L.T > 1);
   if (fn == nullptr) return cudaErrorInvalidDeviceFunction;
-  const size_t smem = decode_smem_bytes(L.kv_fp8, L.D, L.bs, L.warps, L.stages);
+  const size_t smem = decode_smem_bytes(L.kv_fp8, L.D, L.bs, L.warps, L.stages, L.tc);
   int per_sm = 0;
   cudaError_t e = ctas_per_sm(fn, L.warps * 32, smem, &per_sm);
   if (e != cudaSuccess) return e;
@@ -448,7 +452,8 @@ cudaError_t launch_decode(const DecodeLaunch& L, int* launched) {
   p.pmax = L.pmax;
   p.ppu = L.ppu;
   p.stages = L.stages;
-  p.fused_merge = (L.pmax <= kFusedMergeMaxParts) ? 1 : 0;
+  // the tcgen05 kernel leaves every split-K merge to the merge kernels
+  p.fused_merge = (!L.tc && L.pmax <= kFusedMergeMaxParts) ? 1 : 0;
   p.row_base = L.row_base;
   p.scale_log2 = L.scale_log2;
   CUtensorMap kmap = L.kmap, vmap = L.vmap;
@@ -470,7 +475,7 @@ cudaError_t launch_decode(const DecodeLaunch& L, int* launched) {
 
   // 3. merge kernel when sequences may span many partitions: a warp per row
   //    up to 32 partitions, a CTA per row beyond
-  if (!p.fused_merge) {
+  if (!p.fused_merge && L.pmax > 1) {
     const int rows = L.B * L.T * L.Hq;
     const bool by_warp = L.pmax <= kMergeWarpMaxParts;
     cudaLaunchConfig_t mc{};

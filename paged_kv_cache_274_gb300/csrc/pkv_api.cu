@@ -299,30 +299,38 @@ static pkv_status resolve_decode(const pkv_cache_desc* c, int32_t batch, int32_t
   pkv_decode_opts o{};
   if (opts) o = *opts;
   int math = o.math != 0 ? o.math : env_int("PKV_DECODE_MATH", PKV_MATH_AUTO);
-  if (math == PKV_MATH_AUTO) math = PKV_MATH_MMA;
+  // tcgen05 tiles: multi-token calls on bf16 caches with head_dim 128
+  const bool tc_ok = c->dtype == PKV_KV_BF16 && c->head_dim == 128 && T > 1 && G <= 128;
+  if (math == PKV_MATH_AUTO) math = (tc_ok && static_cast<long long>(T) * G > 16) ? PKV_MATH_TC : PKV_MATH_MMA;
+  if (math == PKV_MATH_TC && !tc_ok)
+    return fail(PKV_ERR_UNSUPPORTED, "tcgen05 tiles need T > 1, a bf16 cache, head_dim 128 and G <= 128");
   if (math == PKV_MATH_MMA && G > 16)
     return fail(PKV_ERR_UNSUPPORTED, "G = %d query heads per KV head (mma supports <= 16)", G);
   if (math == PKV_MATH_FFMA && G != 1 && G != 2 && G != 4 && G != 8)
     return fail(PKV_ERR_UNSUPPORTED, "G = %d query heads per KV head (ffma supports 1, 2, 4, 8)", G);
-  if (math != PKV_MATH_MMA && math != PKV_MATH_FFMA) return fail(PKV_ERR_INVALID_ARG, "math %d", math);
+  if (math != PKV_MATH_MMA && math != PKV_MATH_FFMA && math != PKV_MATH_TC)
+    return fail(PKV_ERR_INVALID_ARG, "math %d", math);
+  const bool tc = math == PKV_MATH_TC;
   if (math == PKV_MATH_FFMA && T > 1)
     return fail(PKV_ERR_UNSUPPORTED, "multi-token queries need the mma back-end");
   if (static_cast<long long>(batch) * T * Hq * c->head_dim >= (1LL << 31))
     return fail(PKV_ERR_UNSUPPORTED, "batch x query tokens x heads x head_dim too large");
-  // row tiles of at most 16 (query token, head) rows: whole query tokens per tile
-  const int Tt = std::max(1, std::min(T, 16 / G));
+  // row tiles of at most 16 (mma.sync) or 128 (tcgen05) (query token, head)
+  // rows: whole query tokens per tile
+  const int Tt = std::max(1, std::min(T, (tc ? 128 : 16) / G));
   const int NT = (T + Tt - 1) / Tt;
   const bool fp8 = c->dtype != PKV_KV_BF16;  // one-byte elements
   const size_t stage_bytes = static_cast<size_t>(2) * c->block_size * c->head_dim * (fp8 ? 1 : 2);
   // Defaults measured on GB300: 4 warps per CTA with shallow (2-stage)
   // rings give several CTAs, i.e. 8+ streaming warps, per SM; deeper rings
   // only cost occupancy.
-  int warps = o.warps_per_cta != 0 ? o.warps_per_cta : env_int("PKV_DECODE_WARPS", 4);
-  int stages = o.stages != 0 ? o.stages : env_int("PKV_DECODE_STAGES", 0);
+  // (the tcgen05 kernel has a fixed shape: 4 warps, a 3-stage ring)
+  int warps = tc ? 4 : (o.warps_per_cta != 0 ? o.warps_per_cta : env_int("PKV_DECODE_WARPS", 4));
+  int stages = tc ? 3 : (o.stages != 0 ? o.stages : env_int("PKV_DECODE_STAGES", 0));
   if (stages == 0) stages = stage_bytes >= (8u << 10) ? 2 : 3;
   if (warps < 1 || warps > 8) return fail(PKV_ERR_INVALID_ARG, "warps_per_cta %d outside 1..8", warps);
   if (stages < 2 || stages > 8) return fail(PKV_ERR_INVALID_ARG, "stages %d outside 2..8", stages);
-  const size_t smem = pkv::decode_smem_bytes(fp8, c->head_dim, c->block_size, warps, stages);
+  const size_t smem = pkv::decode_smem_bytes(fp8, c->head_dim, c->block_size, warps, stages, tc);
   if (smem > 227u * 1024u)
     return fail(PKV_ERR_INVALID_ARG, "warps x stages need %zu bytes of shared memory", smem);
   int ppu = o.partition_blocks != 0 ? o.partition_blocks : env_int("PKV_DECODE_PARTITION_BLOCKS", 0);
@@ -335,7 +343,9 @@ static pkv_status resolve_decode(const pkv_cache_desc* c, int32_t batch, int32_t
     // fullest (a larger size unless a smaller one is clearly better).
     const long long ctas_smem = std::max<long long>(1, (228LL * 1024) / static_cast<long long>(smem + 1024));
     const long long ctas_regs = std::max<long long>(1, 65536LL / (warps * 32LL * 200));
-    const long long W = static_cast<long long>(num_sms) * std::min(ctas_smem, ctas_regs) * warps;
+    // streams: warps of the mma.sync kernels; CTAs of the tcgen05 kernel
+    // (two per SM: their accumulators fill the SM's tensor memory)
+    const long long W = tc ? 2LL * num_sms : static_cast<long long>(num_sms) * std::min(ctas_smem, ctas_regs) * warps;
     auto units = [&](int pp) {
       return static_cast<long long>(std::max(batch, 1)) * c->num_kv_heads * NT * ((MB + pp - 1) / pp);
     };
@@ -369,6 +379,7 @@ static pkv_status resolve_decode(const pkv_cache_desc* c, int32_t batch, int32_t
   L->T = T;
   L->Tt = Tt;
   L->NT = NT;
+  L->tc = tc ? 1 : 0;
   L->MB = MB;
   L->NB = c->num_blocks;
   L->bs = c->block_size;
@@ -419,9 +430,10 @@ pkv_status pkv_decode_multi_describe(const pkv_cache_desc* cache, int32_t batch,
   plan->math = L.math;
   plan->warps_per_cta = L.warps;
   plan->stages = L.stages;
-  plan->kernels_per_call = L.pmax > 4 ? 3 : 2;  // the merge kernel runs above 4 partitions
+  // the merge kernel runs above 4 partitions (tcgen05 kernel: above 1)
+  plan->kernels_per_call = L.pmax > (L.tc ? 1 : 4) ? 3 : 2;
   plan->workspace_bytes = layout_of(L).total;
-  plan->smem_bytes_per_cta = pkv::decode_smem_bytes(L.kv_fp8, L.D, L.bs, L.warps, L.stages);
+  plan->smem_bytes_per_cta = pkv::decode_smem_bytes(L.kv_fp8, L.D, L.bs, L.warps, L.stages, L.tc);
   plan->query_tokens_per_tile = L.Tt;
   plan->row_tiles = L.NT;
   return PKV_OK;

@@ -46,6 +46,7 @@ struct DecodeLaunch {
   int T;   // query tokens per sequence (1: single-token decode)
   int Tt;  // query tokens per row tile (G * Tt <= 16 rows)
   int NT;  // row tiles per (sequence, KV head): ceil(T / Tt)
+  int tc;  // 1: tcgen05 kernel (128-row tiles, math PKV_MATH_TC)
   int kv_fp8;    // one-byte elements (E4M3 or INT8)
   int kv_dtype;  // pkv_kv_dtype
   int pmax;  // max partitions of a sequence (ceil(MB / ppu))
@@ -73,7 +74,7 @@ WorkspaceLayout workspace_layout(int B, int T, int Hq, int Hkv, int NT, int D, i
 bool pdl_enabled();
 
 // Shared memory per CTA of the decode kernel.
-size_t decode_smem_bytes(int kv_fp8, int D, int bs, int warps, int stages);
+size_t decode_smem_bytes(int kv_fp8, int D, int bs, int warps, int stages, int tc);
 
 // Launch planner + decode (the decode merges split-K partials itself).  Returns cudaSuccess or
 // the first launch error.

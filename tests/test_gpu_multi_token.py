@@ -82,7 +82,7 @@ def test_each_token_equals_truncated_single_token_decode(Hq, Hkv, T):
     c = random_case(80 + T, len(lens), Hq, Hkv, 128, 16, lens)
     dc = DeviceCase(c)
     q = _q(81 + T, c.B, T, Hq, 128)
-    opts = pkv.decode_opts(partition_blocks=4)
+    opts = pkv.decode_opts(partition_blocks=4, math=pkv.MATH_MMA)  # the same mma.sync kernels
     multi = pkv.paged_decode_multi(to_dev_bf16(q), dc.k, dc.v, dc.bt, dc.cl, [0], 0, c.scale, opts=opts)
     for t in range(T):
         cl = to_dev((c.context_lens - T + t + 1).astype(np.int32))
@@ -152,10 +152,91 @@ def test_multi_tile_ring_depths(stages, T, Hq, Hkv):
     c = random_case(120 + T + stages, len(lens), Hq, Hkv, 128, 16, lens, poison=True)
     dc = DeviceCase(c)
     q = _q(121 + T, c.B, T, Hq, 128)
-    plan = pkv.decode_plan(dc.k, c.B, Hq, c.MB, pkv.decode_opts(stages=stages), T)
+    opts = pkv.decode_opts(stages=stages, partition_blocks=5, math=pkv.MATH_MMA)
+    plan = pkv.decode_plan(dc.k, c.B, Hq, c.MB, opts, T)
     assert plan["row_tiles"] > 1 and plan["stages"] == stages
-    out = pkv.paged_decode_multi(to_dev_bf16(q), dc.k, dc.v, dc.bt, dc.cl, [0], 0, c.scale,
-                                 opts=pkv.decode_opts(stages=stages, partition_blocks=5))
+    out = pkv.paged_decode_multi(to_dev_bf16(q), dc.k, dc.v, dc.bt, dc.cl, [0], 0, c.scale, opts=opts)
     torch.cuda.synchronize()
     assert pkv.read_device_error() == 0
     assert_close(bf16_dev_to_f64(out), _oracle(dc, q), f"T={T} stages={stages}")
+
+
+# ---------------------------------------------------------------------------
+# tcgen05 tiles (128 query rows, TMEM accumulators)
+# ---------------------------------------------------------------------------
+TC_SWEEP = [  # (bs, Hq, Hkv, T, lens)
+    (16, 32, 8, 8, [1, 9, 40, 300, 1000]),      # G 4: 32 rows of 128; a context below T
+    (32, 32, 8, 5, [5, 31, 32, 33, 513]),       # bs 32: one page per step
+    (16, 16, 1, 3, [3, 50, 129]),               # G 16
+    (16, 8, 8, 20, [19, 20, 21, 333]),          # MHA, 20 rows
+    (16, 32, 8, 33, [40, 100, 260]),            # two tiles (32 + 1 tokens)
+    (16, 64, 8, 128, [130, 300]),               # G 8: eight tiles, a prefill chunk
+    (32, 16, 2, 17, [17, 64, 65, 700]),
+]
+
+
+def _tc_opts(ppu=0):
+    return pkv.decode_opts(partition_blocks=ppu, math=pkv.MATH_TC)
+
+
+@pytest.mark.parametrize("bs,Hq,Hkv,T,lens", TC_SWEEP)
+@pytest.mark.parametrize("ppu", [0, 1, 3, 7])
+def test_tc_sweep(bs, Hq, Hkv, T, lens, ppu):
+    seed = 900 + 3 * bs + 7 * Hq + 11 * Hkv + 13 * T
+    c = random_case(seed, len(lens), Hq, Hkv, 128, bs, lens, poison=True)
+    dc = DeviceCase(c)
+    q = _q(seed + 1, c.B, T, Hq, 128)
+    plan = pkv.decode_plan(dc.k, c.B, Hq, c.MB, _tc_opts(ppu), T)
+    assert plan["math"] == pkv.MATH_TC
+    out = pkv.paged_decode_multi(to_dev_bf16(q), dc.k, dc.v, dc.bt, dc.cl, [0], 0, c.scale, opts=_tc_opts(ppu))
+    torch.cuda.synchronize()
+    assert pkv.read_device_error() == 0
+    assert_close(bf16_dev_to_f64(out), _oracle(dc, q), f"tc T={T} G={Hq // Hkv} bs={bs} ppu={ppu}")
+
+
+@pytest.mark.parametrize("value_scale", [1.0, 4.0])
+def test_tc_large_logits_and_auto_choice(value_scale):
+    # logits of order +-100 make the lazy running maximum rescale O often
+    c = random_case(950, 3, 32, 8, 128, 16, [64, 500, 1200], value_scale=value_scale)
+    dc = DeviceCase(c)
+    q = _q(951, c.B, 8, 32, 128)
+    assert pkv.decode_plan(dc.k, c.B, 32, c.MB, None, 8)["math"] == pkv.MATH_TC   # auto picks tcgen05
+    tc = pkv.paged_decode_multi(to_dev_bf16(q), dc.k, dc.v, dc.bt, dc.cl, [0], 0, c.scale)
+    mma = pkv.paged_decode_multi(to_dev_bf16(q), dc.k, dc.v, dc.bt, dc.cl, [0], 0, c.scale,
+                                 opts=pkv.decode_opts(math=pkv.MATH_MMA))
+    torch.cuda.synchronize()
+    want = _oracle(dc, q)
+    assert_close(bf16_dev_to_f64(tc), want, "tc")
+    assert_close(bf16_dev_to_f64(mma), want, "mma")
+
+
+def test_tc_speculative_verify_flow():
+    T, Hq, Hkv, D, bs = 8, 32, 8, 128, 16
+    before = np.array([60, 15, 200, 1000], np.int32)
+    c = random_case(960, 4, Hq, Hkv, D, bs, (before + T).tolist(), spare_blocks=2)
+    dc = DeviceCase(c)
+    slots = np.array([c.block_tables[b, p // bs] * bs + p % bs
+                      for b in range(c.B) for p in range(before[b], before[b] + T)], np.int64)
+    kn = normal_bf16_bits(961, (len(slots), Hkv, D))
+    vn = normal_bf16_bits(962, (len(slots), Hkv, D))
+    q = _q(963, c.B, T, Hq, D)
+    got = pkv.append_and_decode(to_dev_bf16(kn), to_dev_bf16(vn), to_dev(slots), to_dev_bf16(q), dc.k, dc.v,
+                                dc.bt, dc.cl, [0], 0, c.scale)
+    torch.cuda.synchronize()
+    assert pkv.read_device_error() == 0
+    ko, vo = dc.k_host.copy(), dc.v_host.copy()
+    assert oracle.kv_append(kn, vn, slots, ko, vo) == 0
+    want = oracle.paged_decode_multi(q, ko, vo, c.block_tables, c.context_lens, c.kv_group_ptr, 0, c.scale)
+    assert_close(bf16_dev_to_f64(got), want, "tc verify")
+
+
+def test_tc_unsupported_shapes_rejected():
+    c8 = random_case(970, 2, 32, 8, 128, 16, [40, 50], kv_dtype="fp8")
+    d8 = DeviceCase(c8)
+    q = to_dev_bf16(_q(971, 2, 8, 32, 128))
+    with pytest.raises(pkv.PkvError):
+        pkv.paged_decode_multi(q, d8.k, d8.v, d8.bt, d8.cl, k_scale=d8.ks, v_scale=d8.vs, opts=_tc_opts())
+    c = random_case(972, 2, 32, 8, 128, 16, [40, 50])
+    dc = DeviceCase(c)
+    with pytest.raises(pkv.PkvError):   # T = 1
+        pkv.paged_decode_multi(to_dev_bf16(_q(973, 2, 1, 32, 128)), dc.k, dc.v, dc.bt, dc.cl, opts=_tc_opts())

@@ -135,12 +135,34 @@ def _plan(lib, d, B, T, Hq, MB, opts=None):
     (32, 8, 1, 1, 1), (32, 8, 4, 4, 1), (32, 8, 8, 4, 2), (32, 8, 5, 4, 2),
     (16, 1, 3, 1, 3), (8, 8, 16, 16, 1), (8, 8, 17, 16, 2), (24, 8, 6, 5, 2)])
 def test_multi_token_row_tiles(lib, Hq, Hkv, T, tokens_per_tile, tiles):
-    # (query token, head) rows form tiles of at most 16 rows, whole tokens each
+    # mma.sync: (query token, head) rows form tiles of at most 16 rows, whole tokens each
     d = _desc(num_kv_heads=Hkv)
-    st, plan = _plan(lib, d, 8, T, Hq, 64)
+    st, plan = _plan(lib, d, 8, T, Hq, 64, pkv.decode_opts(math=pkv.MATH_MMA))
     assert st == 0
     assert (plan.query_tokens_per_tile, plan.row_tiles) == (tokens_per_tile, tiles)
     assert (Hq // Hkv) * plan.query_tokens_per_tile <= 16
+
+
+@pytest.mark.parametrize("Hq,Hkv,T,math,tokens_per_tile,tiles", [
+    (32, 8, 4, 2, 4, 1),        # 16 rows: auto keeps mma.sync
+    (32, 8, 8, 3, 8, 1),        # 32 rows: auto picks tcgen05 (128-row tiles)
+    (32, 8, 33, 3, 32, 2),
+    (16, 1, 9, 3, 8, 2),        # G 16: 8 tokens per 128-row tile
+    (8, 8, 128, 3, 128, 1),     # MHA: 128 tokens in one tile
+    (64, 8, 2, 2, 2, 1)])       # G 8, 16 rows
+def test_auto_back_end_and_tiles(lib, Hq, Hkv, T, math, tokens_per_tile, tiles):
+    d = _desc(num_kv_heads=Hkv)
+    st, plan = _plan(lib, d, 8, T, Hq, 64)
+    assert st == 0 and plan.math == math
+    assert (plan.query_tokens_per_tile, plan.row_tiles) == (tokens_per_tile, tiles)
+
+
+def test_tc_argument_checks(lib):
+    tc = pkv.decode_opts(math=pkv.MATH_TC)
+    assert _plan(lib, _desc(), 8, 1, 32, 64, tc)[0] == 2                  # T = 1
+    assert _plan(lib, _desc(dtype=1), 8, 4, 32, 64, tc)[0] == 2           # E4M3 cache
+    assert _plan(lib, _desc(head_dim=64), 8, 4, 32, 64, tc)[0] == 2       # head_dim 64
+    assert _plan(lib, _desc(), 8, 4, 32, 64, tc)[0] == 0
 
 
 def test_multi_token_arguments(lib):
