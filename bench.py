@@ -45,7 +45,8 @@ METRIC = "paged decode KV-read GB/s and % of GB300 HBM peak; decode steps/s"
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0
 WORKLOADS = ("llama8b_layer", "long_b4_32k", "long_b1_128k", "mixed_prefix", "fp8_shared",
-             "int8_shared", "spec_verify_t4", "spec_verify_t8", "spec_verify_t16", "tiny", "copy_blocks")
+             "int8_shared", "spec_verify_t4", "spec_verify_t8", "spec_verify_t16", "spec_verify_t32",
+             "spec_verify_t64", "spec_verify_t128", "tiny", "copy_blocks")
 
 
 def query_tokens_of(name):
@@ -282,8 +283,9 @@ class DeviceWorkload:
             self.slots = torch.from_numpy(c.slot_mapping).to(dev)
         self.opts_kw = opts_kw
         self.opts = pkv.decode_opts(**opts_kw)
-        self.ws = pkv.new_decode_workspace(self.k, c.B, c.Hq, c.MB, self.opts)
-        self.plan = pkv.decode_plan(self.k, c.B, c.Hq, c.MB, self.opts)
+        T = query_tokens_of(name)
+        self.ws = pkv.new_decode_workspace(self.k, c.B, c.Hq, c.MB, self.opts, T)
+        self.plan = pkv.decode_plan(self.k, c.B, c.Hq, c.MB, self.opts, T)
         self.layers = list(range(c.L))
         self.kv_bytes = kv_bytes_of(c)
         self.launches_per_step = len(self.layers) * self.plan["kernels_per_call"]
@@ -368,8 +370,6 @@ class VerifyWorkload(DeviceWorkload):
         self.k_new = torch.randn((c.B * T, c.Hkv, c.D), generator=g, device=dev, dtype=torch.bfloat16)
         self.v_new = torch.randn((c.B * T, c.Hkv, c.D), generator=g, device=dev, dtype=torch.bfloat16)
         self.append = True
-        self.ws = pkv.new_decode_workspace(self.k, c.B, c.Hq, c.MB, self.opts, T)
-        self.plan = pkv.decode_plan(self.k, c.B, c.Hq, c.MB, self.opts, T)
         self.launches_per_step = len(self.layers) * self.plan["kernels_per_call"]
         torch.cuda.synchronize()
 

@@ -423,8 +423,12 @@ cudaError_t launch_decode(const DecodeLaunch& L, int* launched) {
 
   // 2. decode: persistent grid, at most one warp per possible unit
   const long long max_units = static_cast<long long>(L.B) * L.Hkv * L.NT * L.pmax;
+  // The tcgen05 kernel holds 256 of an SM's 512 TMEM columns: two CTAs per SM
+  // (the occupancy query does not see the tensor memory and may say one).
+  if (L.tc) per_sm = 2;
   long long grid = static_cast<long long>(L.num_sms) * per_sm;
-  grid = std::min(grid, (max_units + L.warps - 1) / L.warps);
+  // a warp of the mma.sync kernels, a CTA of the tcgen05 kernel, per unit
+  grid = std::min(grid, L.tc ? max_units : (max_units + L.warps - 1) / L.warps);
   grid = std::max(grid, 1LL);
 
   DecodeParams p{};

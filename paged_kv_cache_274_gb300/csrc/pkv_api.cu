@@ -301,7 +301,10 @@ static pkv_status resolve_decode(const pkv_cache_desc* c, int32_t batch, int32_t
   int math = o.math != 0 ? o.math : env_int("PKV_DECODE_MATH", PKV_MATH_AUTO);
   // tcgen05 tiles: multi-token calls on bf16 caches with head_dim 128
   const bool tc_ok = c->dtype == PKV_KV_BF16 && c->head_dim == 128 && T > 1 && G <= 128;
-  if (math == PKV_MATH_AUTO) math = (tc_ok && static_cast<long long>(T) * G > 16) ? PKV_MATH_TC : PKV_MATH_MMA;
+  // measured on GB300 (Llama-8B layer, G 4): mma.sync tiles are faster up to
+  // 32 rows per KV head (235 vs 300 us at 8 tokens), tcgen05 tiles from 64
+  // rows on (320 vs 453 us at 16 tokens, 1386 vs 3430 us at 128)
+  if (math == PKV_MATH_AUTO) math = (tc_ok && static_cast<long long>(T) * G > 32) ? PKV_MATH_TC : PKV_MATH_MMA;
   if (math == PKV_MATH_TC && !tc_ok)
     return fail(PKV_ERR_UNSUPPORTED, "tcgen05 tiles need T > 1, a bf16 cache, head_dim 128 and G <= 128");
   if (math == PKV_MATH_MMA && G > 16)
@@ -324,8 +327,9 @@ static pkv_status resolve_decode(const pkv_cache_desc* c, int32_t batch, int32_t
   // Defaults measured on GB300: 4 warps per CTA with shallow (2-stage)
   // rings give several CTAs, i.e. 8+ streaming warps, per SM; deeper rings
   // only cost occupancy.
-  // (the tcgen05 kernel has a fixed shape: 4 warps, a 3-stage ring)
-  int warps = tc ? 4 : (o.warps_per_cta != 0 ? o.warps_per_cta : env_int("PKV_DECODE_WARPS", 4));
+  // (the tcgen05 kernel has a fixed shape: 4 compute warps, an MMA warp and a
+  // copy warp, a 3-stage ring)
+  int warps = tc ? 6 : (o.warps_per_cta != 0 ? o.warps_per_cta : env_int("PKV_DECODE_WARPS", 4));
   int stages = tc ? 3 : (o.stages != 0 ? o.stages : env_int("PKV_DECODE_STAGES", 0));
   if (stages == 0) stages = stage_bytes >= (8u << 10) ? 2 : 3;
   if (warps < 1 || warps > 8) return fail(PKV_ERR_INVALID_ARG, "warps_per_cta %d outside 1..8", warps);

@@ -199,8 +199,8 @@ def test_tc_large_logits_and_auto_choice(value_scale):
     # logits of order +-100 make the lazy running maximum rescale O often
     c = random_case(950, 3, 32, 8, 128, 16, [64, 500, 1200], value_scale=value_scale)
     dc = DeviceCase(c)
-    q = _q(951, c.B, 8, 32, 128)
-    assert pkv.decode_plan(dc.k, c.B, 32, c.MB, None, 8)["math"] == pkv.MATH_TC   # auto picks tcgen05
+    q = _q(951, c.B, 16, 32, 128)
+    assert pkv.decode_plan(dc.k, c.B, 32, c.MB, None, 16)["math"] == pkv.MATH_TC   # auto picks tcgen05
     tc = pkv.paged_decode_multi(to_dev_bf16(q), dc.k, dc.v, dc.bt, dc.cl, [0], 0, c.scale)
     mma = pkv.paged_decode_multi(to_dev_bf16(q), dc.k, dc.v, dc.bt, dc.cl, [0], 0, c.scale,
                                  opts=pkv.decode_opts(math=pkv.MATH_MMA))
