@@ -51,7 +51,7 @@ template <int KV>
 __global__ void __launch_bounds__(kPlanThreads)
     plan_kernel(const int32_t* __restrict__ context_lens, int B, int num_arrive /* B * Hkv * NT */,
                 int max_ctx, int tokens_per_part, int32_t* work_counter, int32_t* unit_start,
-                int32_t* ctx_eff, int32_t* arrive, __nv_bfloat16* out,
+                int32_t* ctx_eff, int32_t* part_seq, int32_t* arrive, __nv_bfloat16* out,
                 int row_elems /* T * Hq * D */, unsigned* err, const AppendArgs app) {
   __shared__ int warp_tot[kPlanThreads / 32];
   __shared__ int carry_s;
@@ -111,6 +111,10 @@ __global__ void __launch_bounds__(kPlanThreads)
   }
   for (int i = tid; i < num_arrive; i += kPlanThreads) arrive[i] = 0;
   if (__syncthreads_or(bad_any) && tid == 0) atomicOr(err, PKV_DEVERR_CONTEXT_LEN);
+  // the sequence of every global partition (one warp per sequence), so that
+  // a decode unit finds its sequence with one load
+  for (int b = warp; b < B; b += kPlanThreads / 32)
+    for (int q = unit_start[b] + lane; q < unit_start[b + 1]; q += 32) part_seq[q] = b;
   // zeros for inactive sequences (one warp per sequence)
   for (int b = warp; b < B; b += kPlanThreads / 32) {
     if (ctx_eff[b] != 0) continue;
@@ -288,6 +292,8 @@ WorkspaceLayout workspace_layout(int B, int T, int Hq, int Hkv, int NT, int D, i
   off = align_up(off + sizeof(int32_t) * (static_cast<size_t>(B) + 1), 256);
   w.ctx_eff = off;
   off = align_up(off + sizeof(int32_t) * static_cast<size_t>(B), 256);
+  w.part_seq = off;
+  off = align_up(off + sizeof(int32_t) * static_cast<size_t>(B) * pmax, 256);
   w.arrive = off;
   off = align_up(off + sizeof(int32_t) * static_cast<size_t>(B) * Hkv * NT, 256);
   const size_t parts = pmax > 1 ? static_cast<size_t>(B) * T * Hq * pmax : 0;
@@ -415,7 +421,7 @@ cudaError_t launch_decode(const DecodeLaunch& L, int* launched) {
                 : L.append_kind == PKV_KV_FP8_E4M3  ? plan_kernel<PKV_KV_FP8_E4M3>
                                                     : plan_kernel<PKV_KV_BF16>;
     e = cudaLaunchKernelEx(&cfg, plan, L.context_lens, L.B, L.B * L.Hkv * L.NT, L.MB * L.bs,
-                           L.ppu * L.bs, L.work_counter, L.unit_start, L.ctx_eff, L.arrive,
+                           L.ppu * L.bs, L.work_counter, L.unit_start, L.ctx_eff, L.part_seq, L.arrive,
                            static_cast<__nv_bfloat16*>(L.out), L.T * L.Hq * L.D, L.err, app);
     if (e != cudaSuccess) return e;
     *launched += 1;
@@ -440,6 +446,7 @@ cudaError_t launch_decode(const DecodeLaunch& L, int* launched) {
   p.work_counter = L.work_counter;
   p.unit_start = L.unit_start;
   p.ctx_eff = L.ctx_eff;
+  p.part_seq = L.part_seq;
   p.part_ml = L.part_ml;
   p.part_o = L.part_o;
   p.arrive = L.arrive;

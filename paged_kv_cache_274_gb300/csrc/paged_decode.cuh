@@ -55,6 +55,7 @@ struct DecodeParams {
   int32_t* work_counter;
   const int32_t* unit_start;
   const int32_t* ctx_eff;
+  const int32_t* part_seq;  // sequence of each global partition (written by the planner)
   float* part_ml;
   float* part_o;
   int32_t* arrive;  // [B][Hkv] partitions finished so far (zeroed by the planner)
@@ -861,13 +862,7 @@ __global__ void __launch_bounds__(256, 1)
     const int rem = u - part * units_per_part;
     const int kvh = MT ? rem / p.NT : rem;
     const int tile = MT ? rem - kvh * p.NT : 0;
-    // sequence owning global partition `part`: largest b with unit_start[b] <= part
-    int lo = 0, hi = p.B;
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (__ldg(p.unit_start + mid) <= part) lo = mid; else hi = mid;
-    }
-    const int b = lo;
+    const int b = __ldg(p.part_seq + part);  // the sequence owning global partition `part`
     const int pidx = part - __ldg(p.unit_start + b);
     const int nparts = __ldg(p.unit_start + b + 1) - __ldg(p.unit_start + b);
     const int ctx = __ldg(p.ctx_eff + b);

@@ -145,12 +145,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int rem = u - part * units_per_part;
     const int kvh = rem / p.NT;
     const int tile = rem - kvh * p.NT;
-    int lo = 0, hi = p.B;
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (__ldg(p.unit_start + mid) <= part) lo = mid; else hi = mid;
-    }
-    const int b = lo;
+    const int b = __ldg(p.part_seq + part);  // the sequence owning global partition `part`
     const int pidx = part - __ldg(p.unit_start + b);
     const int nparts = __ldg(p.unit_start + b + 1) - __ldg(p.unit_start + b);
     const int ctx = __ldg(p.ctx_eff + b);
@@ -191,34 +186,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     if (producer) {
       // step j's K and V pages into stage (g0 + j) % 3, once P . V of the step
-      // that last used the stage (g0 + j - 3) is done
-      if (lane == 0) {
-        for (int j = 0; j < nsteps; ++j) {
-          const uint32_t g = g0 + j;
-          if (g >= kTcStages &&
-              !mbar_wait_spin(&o_done[g % kTcStages], ((g - kTcStages) / kTcStages) & 1u, kWaitLimitNs)) {
-            timed_out = true;
-            break;
-          }
-          uint8_t* st = sm + TcLayout::kStages + (g % kTcStages) * TcLayout::kStage;
-          uint64_t* bar = &full[g % kTcStages];
-          const int np = min(PPI, npages - j * PPI);
+      // that last used the stage (g0 + j - 3) is done; lane 4q + 2h + kv issues
+      // the copy of half h of K (kv 0) or V (kv 1) of the step's page q
+      for (int j = 0; j < nsteps; ++j) {
+        const uint32_t g = g0 + j;
+        int ok = 1;
+        if (lane == 0 && g >= kTcStages)
+          ok = mbar_wait_spin(&o_done[g % kTcStages], ((g - kTcStages) / kTcStages) & 1u, kWaitLimitNs) ? 1 : 0;
+        if (!__shfl_sync(kFull, ok, 0)) {
+          timed_out = true;
+          break;
+        }
+        uint8_t* st = sm + TcLayout::kStages + (g % kTcStages) * TcLayout::kStage;
+        uint64_t* bar = &full[g % kTcStages];
+        const int np = min(PPI, npages - j * PPI);
+        if (lane == 0) {
           fence_proxy_async_smem();
           mbar_arrive_expect_tx(bar, static_cast<uint32_t>(np) * 4u * 64u * BS * 2u);
-          for (int q = 0; q < np; ++q) {
-            const int row = p.row_base + (pages[j * PPI + q] * p.Hkv + kvh) * BS;
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              tma_load_2d(st + half * TcLayout::kRegion + q * BS * 128, &kmap, bar, half * 64, row, policy);
-              tma_load_2d(st + TcLayout::kTile + half * TcLayout::kRegion + q * BS * 128, &vmap, bar, half * 64,
-                          row, policy);
-            }
-          }
         }
-        // every copy of this unit lands before the unit ends
-        const uint32_t gl = g0 + nsteps - 1;
-        if (!timed_out && !mbar_wait_bounded(&full[gl % kTcStages], (gl / kTcStages) & 1u, kWaitLimitNs))
-          timed_out = true;
+        __syncwarp();
+        if (lane < 4 * np) {
+          const int q = lane >> 2, half = (lane >> 1) & 1, kv = lane & 1;
+          const int row = p.row_base + (pages[j * PPI + q] * p.Hkv + kvh) * BS;
+          tma_load_2d(st + kv * TcLayout::kTile + half * TcLayout::kRegion + q * BS * 128, kv ? &vmap : &kmap, bar,
+                      half * 64, row, policy);
+        }
       }
       __syncwarp();
     } else if (mma_warp) {
@@ -294,13 +286,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int nrow = lim - pos0;
         const uint32_t rmask =
             row_ok ? (vmask & (nrow >= kTcTokens ? ~0u : (nrow <= 0 ? 0u : ((1u << nrow) - 1u)))) : 0u;
-        float sc[kTcTokens];
+        // masked maximum of the scaled scores, then p = 2^(s * scale - m)
         float smax = -INFINITY;
 #pragma unroll
-        for (int k = 0; k < kTcTokens; ++k) {
-          sc[k] = ((rmask >> k) & 1u) ? __uint_as_float(sv[k]) * p.scale_log2 : -INFINITY;
-          smax = fmaxf(smax, sc[k]);
-        }
+        for (int k = 0; k < kTcTokens; ++k)
+          if ((rmask >> k) & 1u) smax = fmaxf(smax, __uint_as_float(sv[k]) * p.scale_log2);
         const float mnew = fmaxf(m, smax);
         const bool grow = (m == -INFINITY) ? (mnew != -INFINITY) : (mnew > m + 8.f);
         float factor = 1.f;
@@ -309,12 +299,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           l *= factor;
           m = mnew;
         }
+        const float neg_m = (m == -INFINITY) ? 0.f : -m;
         uint32_t pw[kTcTokens / 2];
         float psum = 0.f;
 #pragma unroll
         for (int k = 0; k < kTcTokens; k += 2) {
-          const float p0 = (m == -INFINITY) ? 0.f : ex2_approx(sc[k] - m);
-          const float p1 = (m == -INFINITY) ? 0.f : ex2_approx(sc[k + 1] - m);
+          const float p0 = ((rmask >> k) & 1u) ? ex2_approx(fmaf(__uint_as_float(sv[k]), p.scale_log2, neg_m)) : 0.f;
+          const float p1 =
+              ((rmask >> (k + 1)) & 1u) ? ex2_approx(fmaf(__uint_as_float(sv[k + 1]), p.scale_log2, neg_m)) : 0.f;
           psum += p0 + p1;
           pw[k / 2] = pack_bf16x2(p0, p1);
         }
@@ -335,14 +327,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           tc_wait_st();
         }
-        // P row -> buffer g % 2 (K-major core matrices), free once P . V(g - 2) is done
-        if (j >= 2 && !mbar_wait_spin(&o_done[(g - 2) % kTcStages], ((g - 2) / kTcStages) & 1u, kWaitLimitNs))
-          timed_out = true;
-        uint8_t* pbuf = sm + TcLayout::kP + (g & 1u) * TcLayout::kPBuf;
-#pragma unroll
-        for (int k8 = 0; k8 < kTcTokens / 8; ++k8)
-          *reinterpret_cast<uint4*>(pbuf + tc_core_off(tid, k8)) =
-              make_uint4(pw[4 * k8], pw[4 * k8 + 1], pw[4 * k8 + 2], pw[4 * k8 + 3]);
         // V^T -> the stage's K area (K is spent once S is done): warp w moves
         // the 8x8 blocks of d-chunks 4w .. 4w+3 with ldmatrix from the swizzled
         // page and a transposing stmatrix.  Rows of tokens outside the
@@ -376,6 +360,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             stsm_x4_t(k_addr + tc_core_off(8 * dc + (lane & 7), q), r0, r1, r2, r3);
           }
         }
+        // P row -> buffer g % 2 (K-major core matrices), free once P . V(g - 2) is done
+        if (j >= 2 && !mbar_wait_spin(&o_done[(g - 2) % kTcStages], ((g - 2) / kTcStages) & 1u, kWaitLimitNs))
+          timed_out = true;
+        uint8_t* pbuf = sm + TcLayout::kP + (g & 1u) * TcLayout::kPBuf;
+#pragma unroll
+        for (int k8 = 0; k8 < kTcTokens / 8; ++k8)
+          *reinterpret_cast<uint4*>(pbuf + tc_core_off(tid, k8)) =
+              make_uint4(pw[4 * k8], pw[4 * k8 + 1], pw[4 * k8 + 2], pw[4 * k8 + 3]);
         fence_proxy_async_smem();  // P and V^T are read by the tensor cores
         tc_fence_before_sync();
         mbar_arrive(&p_ready[g & 1u]);

@@ -357,7 +357,9 @@ static pkv_status resolve_decode(const pkv_cache_desc* c, int32_t batch, int32_t
     // rows each, so they stay at 32 or 64 blocks (measured on the 4- and
     // 8-token verify steps: 32 beats 16 by 4-10% in the kernel).
     const std::vector<int> sizes = T > 1 ? std::vector<int>{32, 64} : std::vector<int>{32, 16, 8};
-    if (units(64) <= W) {
+    // the tcgen05 kernel's per-unit start-up and partial writes make 64-block
+    // units the fastest at every size measured (10-20% over 32)
+    if (tc || units(64) <= W) {
       ppu = 64;
     } else {
       double best = -1.0;
@@ -534,6 +536,7 @@ static pkv_status decode_call(const pkv_cache_desc* cache, const void* q, int32_
   L.work_counter = reinterpret_cast<int32_t*>(ws + wl.counter);
   L.unit_start = reinterpret_cast<int32_t*>(ws + wl.unit_start);
   L.ctx_eff = reinterpret_cast<int32_t*>(ws + wl.ctx_eff);
+  L.part_seq = reinterpret_cast<int32_t*>(ws + wl.part_seq);
   L.arrive = reinterpret_cast<int32_t*>(ws + wl.arrive);
   L.part_ml = reinterpret_cast<float*>(ws + wl.part_ml);
   L.part_o = reinterpret_cast<float*>(ws + wl.part_o);

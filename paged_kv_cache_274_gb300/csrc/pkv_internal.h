@@ -38,6 +38,7 @@ struct DecodeLaunch {
   int32_t* work_counter;  // workspace: dynamic work queue head
   int32_t* unit_start;    // workspace: [B+1] prefix of partitions per sequence
   int32_t* ctx_eff;       // workspace: [B] validated context lengths
+  int32_t* part_seq;      // workspace: [B * pmax] sequence of each global partition
   int32_t* arrive;        // workspace: [B][Hkv][NT] split-K partitions finished
   float* part_ml;         // workspace: [B][T][Hq][pmax][2] (running max, sum)
   float* part_o;          // workspace: [B][T][Hq][pmax][D]
@@ -66,7 +67,7 @@ struct DecodeLaunch {
 
 // Workspace layout for one decode call.
 struct WorkspaceLayout {
-  size_t counter, unit_start, ctx_eff, arrive, part_ml, part_o, total;
+  size_t counter, unit_start, ctx_eff, part_seq, arrive, part_ml, part_o, total;
 };
 WorkspaceLayout workspace_layout(int B, int T, int Hq, int Hkv, int NT, int D, int pmax);
 
