@@ -62,7 +62,8 @@ struct TcLayout {  // byte offsets from the 1024-aligned shared-memory base
   static constexpr uint32_t kBars = kP + 2 * kPBuf;
   // full[3], s_done[2], p_ready[2], o_done[3]
   static constexpr uint32_t kMisc = kBars + 8 * (kTcStages + 2 + 2 + 3);  // TMEM base, unit
-  static constexpr uint32_t kPages = kMisc + 16;              // int32 physical ids of the unit's pages
+  static constexpr uint32_t kDesc = kMisc + 16;               // 2 x 8 int32: unit descriptors
+  static constexpr uint32_t kPages = kDesc + 64;              // int32 physical ids of the unit's pages
   static constexpr uint32_t kBad = kPages + 64 * 4;           // uint8 bad-id flags
   static constexpr uint32_t kEnd = kBad + 64;
 };
@@ -93,7 +94,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* p_ready = s_done + 2;                                       // [2] P(g), V^T(g) in smem
   uint64_t* o_done = p_ready + 2;                                       // [3] P . V(g) done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + TcLayout::kMisc);
-  volatile int* unit_slot = reinterpret_cast<volatile int*>(sm + TcLayout::kMisc + 4);
+  volatile int* desc = reinterpret_cast<volatile int*>(sm + TcLayout::kDesc);  // [2][8]
   int* pages = reinterpret_cast<int*>(sm + TcLayout::kPages);
   uint8_t* bad = sm + TcLayout::kBad;
   const int tid = threadIdx.x;
@@ -135,20 +136,40 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint32_t g0 = 0;  // global index of the current unit's first step
   bool timed_out = false;
 
+  // One thread takes the next unit from the counter and looks up its
+  // sequence, partition index, partition count and length into descriptor
+  // slot `k` (u >= total_units: no more work); done one unit ahead, so that
+  // these dependent loads overlap the current unit.
+  auto fetch_unit = [&](int k) {
+    volatile int* d = desc + 8 * k;
+    const int u = atomicAdd(p.work_counter, 1);
+    d[0] = u;
+    if (u < total_units) {
+      const int part = u / units_per_part;
+      const int b = __ldg(p.part_seq + part);
+      const int us = __ldg(p.unit_start + b);
+      d[1] = b;
+      d[2] = part - us;
+      d[3] = __ldg(p.unit_start + b + 1) - us;
+      d[4] = __ldg(p.ctx_eff + b);
+    }
+  };
+  if (tid == 0) fetch_unit(0);
+  int cur = 0;
+
   for (;;) {
-    if (tid == 0) *unit_slot = atomicAdd(p.work_counter, 1);
-    __syncthreads();
-    const int u = *unit_slot;
-    __syncthreads();
+    __syncthreads();  // descriptor `cur` is in place
+    const volatile int* d = desc + 8 * cur;
+    const int u = d[0];
     if (u >= total_units) break;
     const int part = u / units_per_part;
     const int rem = u - part * units_per_part;
     const int kvh = rem / p.NT;
     const int tile = rem - kvh * p.NT;
-    const int b = __ldg(p.part_seq + part);  // the sequence owning global partition `part`
-    const int pidx = part - __ldg(p.unit_start + b);
-    const int nparts = __ldg(p.unit_start + b + 1) - __ldg(p.unit_start + b);
-    const int ctx = __ldg(p.ctx_eff + b);
+    const int b = d[1];
+    const int pidx = d[2];
+    const int nparts = d[3];
+    const int ctx = d[4];
     const int t0 = pidx * ppu_tokens;
     const int t1 = min(ctx, t0 + ppu_tokens);
     const int npages = (t1 - t0 + BS - 1) / BS;  // 1 .. 64
@@ -187,8 +208,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (producer) {
       // step j's K and V pages into stage (g0 + j) % 3, once P . V of the step
       // that last used the stage (g0 + j - 3) is done; lane 4q + 2h + kv issues
-      // the copy of half h of K (kv 0) or V (kv 1) of the step's page q
+      // the copy of half h of K (kv 0) or V (kv 1) of the step's page q.
+      // After the first copies are on their way, lane 0 fetches the next unit.
       for (int j = 0; j < nsteps; ++j) {
+        if (j == kTcStages && lane == 0) fetch_unit(cur ^ 1);
         const uint32_t g = g0 + j;
         int ok = 1;
         if (lane == 0 && g >= kTcStages)
@@ -212,6 +235,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                       half * 64, row, policy);
         }
       }
+      if (nsteps <= kTcStages && lane == 0 && !timed_out) fetch_unit(cur ^ 1);
       __syncwarp();
     } else if (mma_warp) {
       if (lane == 0) {
@@ -412,6 +436,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     }
     g0 += static_cast<uint32_t>(nsteps);
+    cur ^= 1;
     tc_fence_before_sync();
     if (__syncthreads_or(timed_out)) {  // the unit is done in every role
       timed_out = true;
