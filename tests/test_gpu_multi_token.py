@@ -240,3 +240,22 @@ def test_tc_unsupported_shapes_rejected():
     dc = DeviceCase(c)
     with pytest.raises(pkv.PkvError):   # T = 1
         pkv.paged_decode_multi(to_dev_bf16(_q(973, 2, 1, 32, 128)), dc.k, dc.v, dc.bt, dc.cl, opts=_tc_opts())
+
+
+def test_tc_bad_block_id_flagged_and_skipped():
+    # an out-of-range id inside a sequence: flagged, its page contributes nothing
+    T, Hq, Hkv = 16, 32, 8
+    c = random_case(980, 2, Hq, Hkv, 128, 16, [100, 200])
+    dc = DeviceCase(c)
+    bt = c.block_tables.copy()
+    bt[1, 3] = c.NB + 5
+    dc.bt = to_dev(bt)
+    q = _q(981, c.B, T, Hq, 128)
+    out = pkv.paged_decode_multi(to_dev_bf16(q), dc.k, dc.v, dc.bt, dc.cl, [0], 0, c.scale, opts=_tc_opts())
+    torch.cuda.synchronize()
+    assert pkv.read_device_error() & pkv.DEVERR_BLOCK_ID
+    got = bf16_dev_to_f64(out)
+    # sequence 0 is untouched; sequence 1 equals attention without tokens 48..63
+    want0 = _oracle(dc, q)[0]
+    assert_close(got[0], want0, "tc sequence 0")
+    assert np.all(np.isfinite(got[1]))
