@@ -327,9 +327,9 @@ static pkv_status resolve_decode(const pkv_cache_desc* c, int32_t batch, int32_t
   // Defaults measured on GB300: 4 warps per CTA with shallow (2-stage)
   // rings give several CTAs, i.e. 8+ streaming warps, per SM; deeper rings
   // only cost occupancy.
-  // (the tcgen05 kernel has a fixed shape: 4 compute warps, an MMA warp and a
-  // copy warp, a 3-stage ring)
-  int warps = tc ? 6 : (o.warps_per_cta != 0 ? o.warps_per_cta : env_int("PKV_DECODE_WARPS", 4));
+  // (the tcgen05 kernel has a fixed shape: 4 compute warps, an MMA warp and
+  // two copy warps (K, V), 3-stage rings)
+  int warps = tc ? 7 : (o.warps_per_cta != 0 ? o.warps_per_cta : env_int("PKV_DECODE_WARPS", 4));
   int stages = tc ? 3 : (o.stages != 0 ? o.stages : env_int("PKV_DECODE_STAGES", 0));
   if (stages == 0) stages = stage_bytes >= (8u << 10) ? 2 : 3;
   if (warps < 1 || warps > 8) return fail(PKV_ERR_INVALID_ARG, "warps_per_cta %d outside 1..8", warps);

@@ -96,26 +96,33 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
-// Same, spinning on the non-blocking test instead of the potentially
-// suspending try_wait: for phases that complete within a microsecond (tensor
-// core products), where a suspended thread would wake up late.
+// Non-blocking test of phase `parity`.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n"
+      " .reg .pred p;\n"
+      " mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Same as mbar_wait_bounded, spinning on the non-blocking test instead of the
+// potentially suspending try_wait: for phases that complete within a
+// microsecond (tensor core products), where a suspended thread would wake up
+// late.  The clock is read only once the phase is found open, so a phase that
+// has already completed costs one test.
 __device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_test_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
 #pragma unroll 1
-    for (int i = 0; i < 64; ++i) {
-      uint32_t ok;
-      asm volatile(
-          "{\n"
-          " .reg .pred p;\n"
-          " mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-          " selp.u32 %0, 1, 0, p;\n"
-          "}\n"
-          : "=r"(ok)
-          : "r"(smem_addr(bar)), "r"(parity)
-          : "memory");
-      if (ok) return true;
-    }
+    for (int i = 0; i < 64; ++i)
+      if (mbar_test_wait(bar, parity)) return true;
     if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
@@ -327,10 +334,11 @@ __device__ __forceinline__ uint64_t tc_smem_desc(uint32_t saddr, uint32_t lbo, u
   return d;
 }
 
-// Instruction descriptor, kind::f16: bf16 A and B (both K-major), f32 D, M x N.
-__host__ __device__ constexpr uint32_t tc_idesc_bf16_f32(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
-         (static_cast<uint32_t>(M >> 4) << 24);
+// Instruction descriptor, kind::f16: bf16 A and B, f32 D, M x N; A K-major,
+// B K-major or (b_mn_major, bit 16) MN-major.
+__host__ __device__ constexpr uint32_t tc_idesc_bf16_f32(int M, int N, bool b_mn_major = false) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn_major ? (1u << 16) : 0u) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 // D[tmem] (+)= A[smem] . B[smem]^T; issued by one thread.
@@ -340,6 +348,16 @@ __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, ui
       "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u));
+}
+
+// D[tmem] (+)= A[tmem] . B[smem]^T: A read from tensor memory (row i of A in
+// lane i, two bf16 per 32-bit column, K along the columns); one thread.
+__device__ __forceinline__ void tc_mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                               bool accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u));
 }
 
 // The MMAs this thread issued so far arrive on `bar` when complete.
