@@ -154,6 +154,28 @@ pkv_status encode_cache_map(CUtensorMap* map, const void* base, const pkv_cache_
   return PKV_OK;
 }
 
+// Store map of the split-K partial outputs part_o [B][T][Hq][pmax][D] fp32
+// for the tcgen05 kernel: a box of 32 columns x one partition x the G heads of
+// a KV head x the Tt query tokens of a row tile (128-byte rows, swizzled as
+// the kernel stages them); the token dimension clips a ragged last tile.
+pkv_status encode_partial_map(CUtensorMap* map, void* part_o, int B, int T, int Hq, int pmax, int D, int G,
+                              int Tt) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+  pkv_status st = tensor_map_encoder(&enc);
+  if (st != PKV_OK) return st;
+  const cuuint64_t row = static_cast<cuuint64_t>(D) * sizeof(float);
+  cuuint64_t dims[5] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(pmax), static_cast<cuuint64_t>(Hq),
+                        static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[4] = {row, row * pmax, row * pmax * Hq, row * pmax * Hq * T};
+  cuuint32_t box[5] = {32, 1, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(Tt), 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, part_o, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled (partials) failed (%d)", static_cast<int>(r));
+  return PKV_OK;
+}
+
 // Host copies of device tables for PKV_VALIDATE.
 template <typename T>
 pkv_status fetch(std::vector<T>& dst, const T* src, size_t n, cudaStream_t stream) {
@@ -328,9 +350,9 @@ static pkv_status resolve_decode(const pkv_cache_desc* c, int32_t batch, int32_t
   // rings give several CTAs, i.e. 8+ streaming warps, per SM; deeper rings
   // only cost occupancy.
   // (the tcgen05 kernel has a fixed shape: 4 compute warps, an MMA warp and
-  // two copy warps (K, V), 3-stage rings)
+  // two copy warps, a 4-stage K ring and a 2-stage V ring of 64 tokens)
   int warps = tc ? 7 : (o.warps_per_cta != 0 ? o.warps_per_cta : env_int("PKV_DECODE_WARPS", 4));
-  int stages = tc ? 3 : (o.stages != 0 ? o.stages : env_int("PKV_DECODE_STAGES", 0));
+  int stages = tc ? 4 : (o.stages != 0 ? o.stages : env_int("PKV_DECODE_STAGES", 0));
   if (stages == 0) stages = stage_bytes >= (8u << 10) ? 2 : 3;
   if (warps < 1 || warps > 8) return fail(PKV_ERR_INVALID_ARG, "warps_per_cta %d outside 1..8", warps);
   if (stages < 2 || stages > 8) return fail(PKV_ERR_INVALID_ARG, "stages %d outside 2..8", stages);
@@ -540,6 +562,9 @@ static pkv_status decode_call(const pkv_cache_desc* cache, const void* q, int32_
   L.arrive = reinterpret_cast<int32_t*>(ws + wl.arrive);
   L.part_ml = reinterpret_cast<float*>(ws + wl.part_ml);
   L.part_o = reinterpret_cast<float*>(ws + wl.part_o);
+  if (L.tc && L.pmax > 1 &&
+      (st = encode_partial_map(&L.omap, L.part_o, batch, L.T, L.Hq, L.pmax, L.D, L.G, L.Tt)) != PKV_OK)
+    return st;
   L.err = dev->err_word;
   L.row_base = static_cast<int>(static_cast<long long>(slot) * cache->num_blocks * cache->num_kv_heads *
                                 cache->block_size);

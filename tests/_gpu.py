@@ -69,11 +69,11 @@ class DeviceCase:
                                    k_scale=c.k_scale, v_scale=c.v_scale, pairs=pairs)
 
 
-def assert_close(got: np.ndarray, want: np.ndarray, what: str = ""):
+def assert_close(got: np.ndarray, want: np.ndarray, what: str = "", atol: float = ATOL):
     assert got.shape == want.shape
     assert np.all(np.isfinite(got)), f"{what}: non-finite GPU output"
     err = np.abs(got - want)
-    bound = ATOL + RTOL * np.abs(want)
+    bound = atol + RTOL * np.abs(want)
     bad = err > bound
     if bad.any():
         idx = np.argwhere(bad)[:5]

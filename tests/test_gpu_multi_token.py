@@ -11,7 +11,7 @@ import torch
 import oracle
 import paged_kv_cache_274_gb300 as pkv
 from workloads import normal_bf16_bits, random_case
-from tests._gpu import DEV, DeviceCase, assert_close, bf16_dev_to_f64, to_dev, to_dev_bf16
+from tests._gpu import ATOL, DEV, DeviceCase, assert_close, bf16_dev_to_f64, to_dev, to_dev_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -206,8 +206,14 @@ def test_tc_large_logits_and_auto_choice(value_scale):
                                  opts=pkv.decode_opts(math=pkv.MATH_MMA))
     torch.cuda.synchronize()
     want = _oracle(dc, q)
-    assert_close(bf16_dev_to_f64(tc), want, "tc")
-    assert_close(bf16_dev_to_f64(mma), want, "mma")
+    # Both back-ends round the attention weights P to bf16 (unit roundoff
+    # 2^-8) before P . V, so the numerator's error is up to 2^-8 sum_k w_k |V_k|
+    # <= 2^-8 max|V|, which the unit-scale ATOL does not cover once the values
+    # are scaled up (outputs near 0 by cancellation have no relative slack).
+    v = bf16_dev_to_f64(dc.v)
+    atol = ATOL + 2.0 ** -8 * float(np.abs(v).max())
+    assert_close(bf16_dev_to_f64(tc), want, "tc", atol=atol)
+    assert_close(bf16_dev_to_f64(mma), want, "mma", atol=atol)
 
 
 def test_tc_speculative_verify_flow():
