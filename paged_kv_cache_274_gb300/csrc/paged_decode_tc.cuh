@@ -66,8 +66,9 @@ struct TcLayout {  // byte offsets from the 1024-aligned shared-memory base
   static constexpr uint32_t kV = kK + kTcKStages * kTile;    // V ring
   static constexpr uint32_t kBars = kV + kTcVStages * kTile;
   // full_k[4], kp_free[4], full_v[2], v_free[2], s_done, s_free, p_ready,
-  // q_ready, slot_full[2], slot_free[2], stg_done, stg_full, stg_free
-  static constexpr int kNumBars = 2 * kTcKStages + 2 * kTcVStages + 4 + 4 + 3;
+  // q_ready, slot_full[2], slot_free[2], stg_done, stg_full, stg_free,
+  // o_ready, mma_drain
+  static constexpr int kNumBars = 2 * kTcKStages + 2 * kTcVStages + 4 + 4 + 5;
   static constexpr uint32_t kMisc = kBars + 8 * kNumBars;    // TMEM base
   static constexpr uint32_t kSlots = kMisc + 16;             // 2 unit slots
   static constexpr uint32_t kSlotPages = 32;                 // after 8 int32 of descriptor
@@ -129,8 +130,9 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   // Barrier phases are counted over the CTA's lifetime: by the global step
   // index g (K stage and full_k[] / kp_free[] by g % 4, V stage and full_v[] /
   // v_free[] by g % 2, s_done / s_free / p_ready once per step) or by the
-  // unit index i (slot_full[] / slot_free[] by i % 2, q_ready and stg_done
-  // once per unit) or by the split-K output chunk (stg_full / stg_free).
+  // unit index i (slot_full[] / slot_free[] by i % 2, q_ready and o_ready
+  // once per unit, stg_done once per unit written directly) or by the
+  // split-K output chunk (stg_full once, stg_free twice per unit).
   // Every barrier completes one phase per use, and no waiter can fall two
   // phases behind (each next use of a barrier depends on the wait).
   uint64_t* full_k = reinterpret_cast<uint64_t*>(sm + TcLayout::kBars);  // [4] K(g) landed
@@ -145,7 +147,9 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   uint64_t* slot_free = slot_full + 2;        // [2] unit slot released by every reader
   uint64_t* stg_done = slot_free + 2;         // the compute warps are done staging a unit's output
   uint64_t* stg_full = stg_done + 1;          // split-K partials: 32 columns of the tile staged
-  uint64_t* stg_free = stg_full + 1;          // split-K partials: their store has read the staging
+  uint64_t* stg_free = stg_full + 1;          // split-K partials: a store has read its staging buffer
+  uint64_t* o_ready = stg_free + 1;           // a unit's last P . V done: O final, its K and V stages idle
+  uint64_t* mma_drain = o_ready + 1;          // after a timeout: every product issued is done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + TcLayout::kMisc);
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -174,6 +178,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     mbar_init(stg_done, kTcComputeWarps);
     mbar_init(stg_full, kTcComputeWarps);
     mbar_init(stg_free, 1);
+    mbar_init(o_ready, 1);
+    mbar_init(mma_drain, 1);
     fence_mbar_init();
     prefetch_tensormap(&kmap);
     prefetch_tensormap(&vmap);
@@ -395,137 +401,121 @@ __global__ void __launch_bounds__(kTcThreads, 2)
           const uint64_t bdesc = tc_smem_desc(v_addr + kk * 2048, TcLayout::kRegion, 1024, 2);
           tc_mma_bf16(tmem + kTcOCol, a, bdesc, kIdescO, !first || kk > 0);
         }
-        // the K stage of a unit's last step is released by the compute warps,
-        // who stage the unit's output there
-        if (!last) tc_commit(&kp_free[g % kTcKStages]);
-        tc_commit(&v_free[g % kTcVStages]);
+        // the K and V stages of a unit's last step are released by the
+        // compute warps, who stage the unit's output there
+        if (last) {
+          tc_commit(o_ready);
+        } else {
+          tc_commit(&kp_free[g % kTcKStages]);
+          tc_commit(&v_free[g % kTcVStages]);
+        }
         pv_end = g + 1;
         return true;
       };
       bool ok = mbar_wait_bounded(&slot_full[0], 0, kWaitLimitNs);
-      TcUnit cur = read_unit(0);
-      if (ok && cur.u < total_units) ok = mbar_wait_spin(q_ready, 0, kWaitLimitNs) && issue_s(0);
+      bool more = ok && slot_desc(0)[0] < total_units;
+      int nsteps = more ? read_unit(0).nsteps : 0;
+      if (more) ok = mbar_wait_spin(q_ready, 0, kWaitLimitNs) && issue_s(0);
       uint32_t g0 = 0;
-      for (int i = 0; ok && cur.u < total_units; ++i) {
-        TcUnit nxt;
-        nxt.u = total_units;
-        for (int j = 0; ok && j < cur.nsteps; ++j) {
+      for (int i = 0; ok && more; ++i) {
+        int next_steps = 0;
+        for (int j = 0; ok && j < nsteps; ++j) {
           const uint32_t g = g0 + j;
-          if (j + 1 < cur.nsteps) {
-            ok = issue_s(g + 1);
-          } else {  // the next unit's first S, once its query tile is in TMEM
-            ok = mbar_wait_bounded(&slot_full[(i + 1) & 1], ((i + 1) >> 1) & 1u, kWaitLimitNs);
-            if (ok) {
-              nxt = read_unit((i + 1) & 1);
-              if (nxt.u < total_units) ok = mbar_wait_spin(q_ready, (i + 1) & 1u, kWaitLimitNs) && issue_s(g + 1);
+          if (j + 1 < nsteps) {  // S one step ahead, then P . V
+            ok = issue_s(g + 1) && issue_pv(g, j == 0, false);
+          } else {  // the unit's last P . V, then the next unit's first S once its query tile is in TMEM
+            ok = issue_pv(g, j == 0, true) &&
+                 mbar_wait_bounded(&slot_full[(i + 1) & 1], ((i + 1) >> 1) & 1u, kWaitLimitNs);
+            more = ok && slot_desc((i + 1) & 1)[0] < total_units;
+            if (more) {
+              next_steps = read_unit((i + 1) & 1).nsteps;
+              ok = mbar_wait_spin(q_ready, (i + 1) & 1u, kWaitLimitNs) && issue_s(g + 1);
             }
           }
-          if (ok) ok = issue_pv(g, j == 0, j + 1 == cur.nsteps);
         }
         if (!ok) break;
         mbar_arrive(&slot_free[i & 1]);
-        g0 += static_cast<uint32_t>(cur.nsteps);
-        cur = nxt;
+        g0 += static_cast<uint32_t>(nsteps);
+        nsteps = next_steps;
       }
       if (!ok) timed_out = true;
     }
     __syncwarp();
   } else {
     // compute warps: thread tid owns row tid of the tile
-    // this row of unit U's query tile -> its TMEM lane, then q_ready
-    auto put_query = [&](const TcUnit& U) {
+    // this row of unit U's query tile: loads (in flight until used), then
+    // into its TMEM lane, then q_ready
+    auto load_query = [&](const TcUnit& U, int half, uint4 (&qv)[8]) {  // d 64 half .. +63
       int t = 0, h = 0;
       const bool ok = tile_row<true>(p, U.kvh, U.tile, tid, t, h);
-      const uint4* src = reinterpret_cast<const uint4*>(p.q + (static_cast<size_t>(U.b * p.T + t) * p.Hq + h) * D);
+      const uint4* src = reinterpret_cast<const uint4*>(p.q + (static_cast<size_t>(U.b * p.T + t) * p.Hq + h) * D) + 8 * half;
 #pragma unroll
+      for (int c = 0; c < 8; ++c) qv[c] = ok ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+    };
+    auto store_query = [&](int half, const uint4 (&qv)[8]) {
+      uint32_t w[32];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        w[4 * c] = qv[c].x;
+        w[4 * c + 1] = qv[c].y;
+        w[4 * c + 2] = qv[c].z;
+        w[4 * c + 3] = qv[c].w;
+      }
+      tc_st32(t_lane + kTcQCol + 32 * half, w);
+    };
+    const float c = p.scale_log2;
+    uint32_t ndirect = 0, nchunk = 0, nfree = 0;  // phases of stg_done, stg_full, stg_free
+    // The unit stays in its slot until these warps release it, so only what
+    // the steps need is kept in registers; the rest is read again for the
+    // output.
+    bool ok = warp_wait(&slot_full[0], 0, true);
+    bool more = ok && slot_desc(0)[0] < total_units;
+    if (more) {
+      const TcUnit U = read_unit(0);
       for (int half = 0; half < 2; ++half) {
-        uint32_t qv[32];
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint4 w = ok ? __ldg(src + 8 * half + c) : make_uint4(0, 0, 0, 0);
-          qv[4 * c] = w.x;
-          qv[4 * c + 1] = w.y;
-          qv[4 * c + 2] = w.z;
-          qv[4 * c + 3] = w.w;
-        }
-        tc_st32(t_lane + kTcQCol + 32 * half, qv);
+        uint4 qv[8];
+        load_query(U, half, qv);
+        store_query(half, qv);
       }
       tc_wait_st();
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(q_ready);
-    };
-    const float c = p.scale_log2;
-    uint32_t ndirect = 0, nchunk = 0;  // units written directly, split-K output chunks stored
-    bool ok = warp_wait(&slot_full[0], 0, true);
-    TcUnit cur = read_unit(0);
-    if (ok && cur.u < total_units) put_query(cur);
+    }
     uint32_t g0 = 0;
-    for (int i = 0; ok && cur.u < total_units; ++i) {
-      int t = 0, h = 0;
-      const bool row_ok = tile_row<true>(p, cur.kvh, cur.tile, tid, t, h);
-      const size_t qrow = static_cast<size_t>(cur.b * p.T + t) * p.Hq + h;
-      const int lim = cur.ctx - p.T + 1 + t;  // keys of this row: positions < lim
-      const volatile uint8_t* bad = slot_bad(i & 1);
-      TcUnit nxt;
-      nxt.u = total_units;
+    for (int i = 0; more; ++i) {
+      const int k = i & 1;
+      int nsteps, t0, t1, lim;  // steps, token range, keys of this row: positions < lim
+      bool row_ok;
+      {
+        const TcUnit U = read_unit(k);
+        int t = 0, h = 0;
+        row_ok = tile_row<true>(p, U.kvh, U.tile, tid, t, h);
+        nsteps = U.nsteps;
+        t0 = U.t0;
+        t1 = U.t1;
+        lim = U.ctx - p.T + 1 + t;
+      }
+      const volatile uint8_t* bad = slot_bad(k);
+      bool has_next = false;
       float m = -INFINITY, l = 0.f;  // log2-domain running max (lazy) and sum of this row
-      for (int j = 0; j < cur.nsteps; ++j) {
-        const uint32_t g = g0 + j;
-        if (!mbar_wait_spin(s_done, g & 1u, kWaitLimitNs)) timed_out = true;
-        if (__any_sync(kFull, timed_out)) {  // warp-uniform exit (the loads below are collective)
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        if (j + 1 == cur.nsteps) {
-          // the unit's last S is done, so the next unit's query tile can take
-          // its TMEM columns (before this step's scores occupy the registers)
-          if (!warp_wait(&slot_full[(i + 1) & 1], ((i + 1) >> 1) & 1u, true)) {
-            ok = false;
-            break;
-          }
-          nxt = read_unit((i + 1) & 1);
-          if (nxt.u < total_units) put_query(nxt);
-        }
-        uint32_t sv[kTcTokens];
-        tc_ld32(t_lane + kTcSCol, *reinterpret_cast<uint32_t(*)[32]>(sv));
-        tc_ld32(t_lane + kTcSCol + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
-        tc_wait_ld();
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(s_free);  // the slot may take S(g + 1)
 
-        // tokens of this step that belong to the sequence (and to a valid
-        // page), then those this row attends to (its causal limit)
-        const int pos0 = cur.t0 + j * kTcTokens;
-        const int nvalid = cur.t1 - pos0;
-        uint64_t vmask = nvalid >= kTcTokens ? ~0ull : ((1ull << nvalid) - 1ull);
+      // tokens of step j that belong to the sequence (and to a valid page),
+      // then those this row attends to (its causal limit)
+      auto step_masks = [&](int j, uint64_t& vmask, uint64_t& rmask) {
+        const int pos0 = t0 + j * kTcTokens;
+        const int nvalid = t1 - pos0;
+        vmask = nvalid >= kTcTokens ? ~0ull : ((1ull << nvalid) - 1ull);
 #pragma unroll
         for (int q = 0; q < PPI; ++q)
           if (bad[j * PPI + q]) vmask &= ~(((1ull << BS) - 1ull) << (q * BS));
         const int nrow = lim - pos0;
-        const uint64_t rmask =
-            row_ok ? (vmask & (nrow >= kTcTokens ? ~0ull : (nrow <= 0 ? 0ull : ((1ull << nrow) - 1ull)))) : 0ull;
-        // masked maximum of the scaled scores (the extremum of the raw ones
-        // times the scale), then p = 2^(s * scale - m); a step whose tokens
-        // are all this row's (all but a unit's last steps) takes branch-free
-        // code
-        const bool all = rmask == ~0ull;
-        float ext;
-        if (all) {
-          ext = c >= 0.f ? tree_max64(sv) : -tree_max64_neg(sv);
-        } else if (c >= 0.f) {
-          ext = -INFINITY;
-#pragma unroll
-          for (int k = 0; k < kTcTokens; ++k)
-            if ((rmask >> k) & 1ull) ext = fmaxf(ext, __uint_as_float(sv[k]));
-        } else {
-          ext = INFINITY;
-#pragma unroll
-          for (int k = 0; k < kTcTokens; ++k)
-            if ((rmask >> k) & 1ull) ext = fminf(ext, __uint_as_float(sv[k]));
-        }
+        rmask = row_ok ? (vmask & (nrow >= kTcTokens ? ~0ull : (nrow <= 0 ? 0ull : ((1ull << nrow) - 1ull)))) : 0ull;
+      };
+      // the step's masked extremum of the raw scores -> running maximum; a
+      // row whose maximum grew by more than 2^8 rescales l and (once
+      // P . V(g - 1) is done) its O in TMEM.  False on timeout.
+      auto update_max = [&](float ext, uint64_t rmask, uint32_t g, int j) -> bool {
         const float smax = rmask != 0ull ? ext * c : -INFINITY;
         const float mnew = fmaxf(m, smax);
         const bool grow = (m == -INFINITY) ? (mnew != -INFINITY) : (mnew > m + 8.f);
@@ -535,7 +525,6 @@ __global__ void __launch_bounds__(kTcThreads, 2)
           l *= factor;
           m = mnew;
         }
-        // a row whose maximum grew: scale its O (TMEM) once P . V(g - 1) is done
         if (j > 0 && __any_sync(kFull, grow)) {
           if (!mbar_wait_spin(&v_free[(g - 1) % kTcVStages], ((g - 1) / kTcVStages) & 1u, kWaitLimitNs))
             timed_out = true;
@@ -551,54 +540,124 @@ __global__ void __launch_bounds__(kTcThreads, 2)
           }
           tc_wait_st();
         }
-        // V rows of tokens outside the sequence (or of a bad page) may hold
-        // anything (even NaN) and P is 0 there: once V(g) has landed, thread
-        // (warp w, lane l) clears 16-byte d-chunks 4w .. 4w+3 of token rows l
-        // and l + 32.
-        if (vmask != ~0ull) {
-          if (!mbar_wait_bounded(&full_v[g % kTcVStages], (g / kTcVStages) & 1u, kWaitLimitNs)) timed_out = true;
-          if (__any_sync(kFull, timed_out)) {
-            ok = false;
-            break;
-          }
-          uint8_t* vb = sm + TcLayout::kV + (g % kTcVStages) * TcLayout::kTile;
+        return !__any_sync(kFull, timed_out);
+      };
+      // V rows of tokens outside the sequence (or of a bad page) may hold
+      // anything (even NaN) and P is 0 there: once V(g) has landed, thread
+      // (warp w, lane l) clears 16-byte d-chunks 4w .. 4w+3 of token rows l
+      // and l + 32.  False on timeout.
+      auto clear_stale_v = [&](uint64_t vmask, uint32_t g) -> bool {
+        if (vmask == ~0ull) return true;
+        if (!mbar_wait_bounded(&full_v[g % kTcVStages], (g / kTcVStages) & 1u, kWaitLimitNs)) timed_out = true;
+        if (__any_sync(kFull, timed_out)) return false;
+        uint8_t* vb = sm + TcLayout::kV + (g % kTcVStages) * TcLayout::kTile;
 #pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            const int k = lane + 32 * r;  // token row
+        for (int r = 0; r < 2; ++r) {
+          const int tk = lane + 32 * r;  // token row
 #pragma unroll
-            for (int i4 = 0; i4 < 4; ++i4) {
-              const int dc = 4 * warp + i4;  // 16-byte d-chunk
-              if (!((vmask >> k) & 1ull))
-                *reinterpret_cast<uint4*>(vb + (dc >> 3) * TcLayout::kRegion + k * 128 +
-                                          (((dc & 7) ^ (k & 7)) << 4)) = make_uint4(0, 0, 0, 0);
-            }
+          for (int i4 = 0; i4 < 4; ++i4) {
+            const int dc = 4 * warp + i4;  // 16-byte d-chunk
+            if (!((vmask >> tk) & 1ull))
+              *reinterpret_cast<uint4*>(vb + (dc >> 3) * TcLayout::kRegion + tk * 128 +
+                                        (((dc & 7) ^ (tk & 7)) << 4)) = make_uint4(0, 0, 0, 0);
           }
         }
-        // P row -> the step's K stage (K-major core matrices), 8 tokens at a time
+        return true;
+      };
+      // 32 scores (bit patterns) -> P (bf16, 8 tokens per 16-byte store) at
+      // token columns 32 half .. +31 of the step's K stage; returns their sum
+      auto write_p = [&](const uint32_t (&sc)[32], uint32_t hm, bool all32, uint8_t* pbuf, int half) -> float {
         const float neg_m = (m == -INFINITY) ? 0.f : -m;
-        uint8_t* pbuf = sm + TcLayout::kK + (g % kTcKStages) * TcLayout::kTile;
         float psum = 0.f;
 #pragma unroll
-        for (int k8 = 0; k8 < kTcTokens / 8; ++k8) {
+        for (int k8 = 0; k8 < 4; ++k8) {
           uint32_t pw[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int k = 8 * k8 + 2 * e;
-            float p0 = ex2_approx(fmaf(__uint_as_float(sv[k]), c, neg_m));
-            float p1 = ex2_approx(fmaf(__uint_as_float(sv[k + 1]), c, neg_m));
-            if (!all) {
-              p0 = ((rmask >> k) & 1ull) ? p0 : 0.f;
-              p1 = ((rmask >> (k + 1)) & 1ull) ? p1 : 0.f;
+            const int kk = 8 * k8 + 2 * e;
+            float p0 = ex2_approx(fmaf(__uint_as_float(sc[kk]), c, neg_m));
+            float p1 = ex2_approx(fmaf(__uint_as_float(sc[kk + 1]), c, neg_m));
+            if (!all32) {
+              p0 = ((hm >> kk) & 1u) ? p0 : 0.f;
+              p1 = ((hm >> (kk + 1)) & 1u) ? p1 : 0.f;
             }
             psum += p0 + p1;
             pw[e] = pack_bf16x2(p0, p1);
           }
-          *reinterpret_cast<uint4*>(pbuf + tc_p_off(tid, k8)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+          *reinterpret_cast<uint4*>(pbuf + tc_p_off(tid, 4 * half + k8)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
         }
-        l += psum;
+        return psum;
+      };
+      auto finish_step = [&]() {
         fence_proxy_async_smem();  // P and the cleared V rows are read by the tensor cores
         tc_fence_before_sync();
         mbar_arrive(p_ready);
+      };
+
+      for (int j = 0; j < nsteps; ++j) {
+        const uint32_t g = g0 + j;
+        if (!mbar_wait_spin(s_done, g & 1u, kWaitLimitNs)) timed_out = true;
+        if (__any_sync(kFull, timed_out)) {  // warp-uniform exit (the loads below are collective)
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        if (j + 1 == nsteps) {
+          // the unit's last S is done, so the next unit's query tile can take
+          // its TMEM columns (before this step's scores occupy the registers)
+          if (!warp_wait(&slot_full[k ^ 1], ((i + 1) >> 1) & 1u, true)) {
+            ok = false;
+            break;
+          }
+          has_next = slot_desc(k ^ 1)[0] < total_units;
+          if (has_next) {
+            const TcUnit U = read_unit(k ^ 1);
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half) {
+              uint4 qv[8];
+              load_query(U, half, qv);
+              store_query(half, qv);
+            }
+            tc_wait_st();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(q_ready);
+          }
+        }
+        uint32_t sv[kTcTokens];
+        tc_ld32(t_lane + kTcSCol, *reinterpret_cast<uint32_t(*)[32]>(sv));
+        tc_ld32(t_lane + kTcSCol + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+        tc_wait_ld();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_free);  // the slot may take S(g + 1)
+        uint64_t vmask, rmask;
+        step_masks(j, vmask, rmask);
+        // masked extremum of the raw scores (maximum for a non-negative
+        // scale); a step whose tokens are all this row's takes branch-free code
+        const bool all = rmask == ~0ull;
+        float ext;
+        if (all) {
+          ext = c >= 0.f ? tree_max64(sv) : -tree_max64_neg(sv);
+        } else if (c >= 0.f) {
+          ext = -INFINITY;
+#pragma unroll
+          for (int kk = 0; kk < kTcTokens; ++kk)
+            if ((rmask >> kk) & 1ull) ext = fmaxf(ext, __uint_as_float(sv[kk]));
+        } else {
+          ext = INFINITY;
+#pragma unroll
+          for (int kk = 0; kk < kTcTokens; ++kk)
+            if ((rmask >> kk) & 1ull) ext = fminf(ext, __uint_as_float(sv[kk]));
+        }
+        if (!update_max(ext, rmask, g, j) || !clear_stale_v(vmask, g)) {
+          ok = false;
+          break;
+        }
+        uint8_t* pbuf = sm + TcLayout::kK + (g % kTcKStages) * TcLayout::kTile;
+        l += write_p(*reinterpret_cast<const uint32_t(*)[32]>(sv), static_cast<uint32_t>(rmask), all, pbuf, 0) +
+             write_p(*reinterpret_cast<const uint32_t(*)[32]>(sv + 32), static_cast<uint32_t>(rmask >> 32), all, pbuf, 1);
+        finish_step();
       }
       if (!ok || __any_sync(kFull, timed_out)) {
         ok = false;
@@ -608,18 +667,26 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       // 32 columns at a time in the last step's K stage (P . V is done with
       // it), so that the global stores write whole lines; every lane loads
       // (tcgen05.ld is warp-collective), rows without a query token write nothing
-      const uint32_t gl = g0 + cur.nsteps - 1;
-      if (!mbar_wait_spin(&v_free[gl % kTcVStages], (gl / kTcVStages) & 1u, kWaitLimitNs)) timed_out = true;
+      const uint32_t gl = g0 + nsteps - 1;
+      if (!mbar_wait_spin(o_ready, i & 1u, kWaitLimitNs)) timed_out = true;
       if (__any_sync(kFull, timed_out)) {
         ok = false;
         break;
       }
       tc_fence_after_sync();
-      const bool direct = cur.nparts == 1;
+      const TcUnit U = read_unit(k);
+      size_t qrow;
+      {
+        int t = 0, h = 0;
+        tile_row<true>(p, U.kvh, U.tile, tid, t, h);
+        qrow = static_cast<size_t>(U.b * p.T + t) * p.Hq + h;
+      }
+      const bool direct = U.nparts == 1;
       uint8_t* stg_base = sm + TcLayout::kK + (gl % kTcKStages) * TcLayout::kTile;  // [128 rows][128 B]
       if (direct) {
         // bf16 output: warp w stages its rows 32 columns at a time and
         // writes them back as 64-byte row pieces
+        if (tid == 0) mbar_arrive(&v_free[gl % kTcVStages]);  // not used for staging here
         const float osc = l > 0.f ? 1.f / l : 0.f;
         const long long orow = static_cast<long long>(qrow);
         uint8_t* stg = stg_base + warp * 4096;
@@ -662,43 +729,55 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         // split-K partials (m, l, unnormalised O): the tile's rows are staged
         // 32 columns at a time (row r at r * 128 bytes, 16-byte chunks
         // XOR-swizzled by r % 8, as the store map's 128-byte swizzle reads
-        // them) and thread 0 stores each chunk with one tensor-map store
+        // them), alternately in the last step's K and V stages, and thread 0
+        // stores each chunk with one tensor-map store; a buffer is restaged
+        // once the store before has read it
+        uint8_t* vbuf = sm + TcLayout::kV + (gl % kTcVStages) * TcLayout::kTile;
 #pragma unroll 1
-        for (int cc = 0; cc < D; cc += 32, ++nchunk) {
+        for (int k = 0; k < D / 32; ++k, ++nchunk) {
+          const int cc = 32 * k;
           uint32_t ov[32];
           tc_ld32(t_lane + kTcOCol + cc, ov);
           tc_wait_ld();
-          if (nchunk > 0 && !warp_wait(stg_free, (nchunk - 1) & 1u, false)) {  // the last store read the staging
+          if (k >= 2 && !warp_wait(stg_free, (nfree + k - 2) & 1u, false)) {
             timed_out = true;
             break;
           }
+          uint8_t* buf = (k & 1) ? vbuf : stg_base;
 #pragma unroll
           for (int c4 = 0; c4 < 8; ++c4)
-            *reinterpret_cast<uint4*>(stg_base + tid * 128 + ((c4 ^ (tid & 7)) << 4)) =
+            *reinterpret_cast<uint4*>(buf + tid * 128 + ((c4 ^ (tid & 7)) << 4)) =
                 make_uint4(ov[4 * c4], ov[4 * c4 + 1], ov[4 * c4 + 2], ov[4 * c4 + 3]);
           fence_proxy_async_smem();  // read by the tensor-map store
           __syncwarp();
           if (lane == 0) mbar_arrive(stg_full);
           if (tid == 0) {
             if (mbar_wait_spin(stg_full, nchunk & 1u, kWaitLimitNs)) {
-              tma_store_5d(&omap, stg_base, cc, cur.pidx, cur.kvh * p.G, cur.tile * p.Tt, cur.b);
+              tma_store_5d(&omap, buf, cc, U.pidx, U.kvh * p.G, U.tile * p.Tt, U.b);
               bulk_commit();
-              bulk_wait_read_all();
-              mbar_arrive(stg_free);
+              if (k == 1 || k == 2) {  // the store of chunk k - 1 has read its buffer
+                bulk_wait_read_but1();
+                mbar_arrive(stg_free);
+              }
             } else {
               timed_out = true;
             }
           }
         }
-        if (row_ok) *reinterpret_cast<float2*>(p.part_ml + 2 * (qrow * p.pmax + cur.pidx)) = make_float2(m, l);
-        // the last store has read the staging: the stage goes back to the K copy warp
-        if (tid == 0 && !timed_out) mbar_arrive(&kp_free[gl % kTcKStages]);
+        nfree += 2;
+        if (row_ok) *reinterpret_cast<float2*>(p.part_ml + 2 * (qrow * p.pmax + U.pidx)) = make_float2(m, l);
+        // both stages go back to the copy warps once the last stores have read them
+        if (tid == 0 && !timed_out) {
+          bulk_wait_read_all();
+          mbar_arrive(&kp_free[gl % kTcKStages]);
+          mbar_arrive(&v_free[gl % kTcVStages]);
+        }
       }
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&slot_free[i & 1]);
-      g0 += static_cast<uint32_t>(cur.nsteps);
-      cur = nxt;
+      g0 += static_cast<uint32_t>(nsteps);
+      more = ok && has_next;
     }
     if (!ok) timed_out = true;
   }
@@ -716,10 +795,9 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     if (vcopy && lane == 0)
       for (uint32_t g = copies_end > kTcVStages ? copies_end - kTcVStages : 0; g < copies_end; ++g)
         mbar_wait_bounded(&full_v[g % kTcVStages], (g / kTcVStages) & 1u, kWaitLimitNs / 16);
-    if (mma_warp && lane == 0) {
-      if (s_end > 0) mbar_wait_bounded(s_done, (s_end - 1) & 1u, kWaitLimitNs / 16);
-      if (pv_end > 0)
-        mbar_wait_bounded(&v_free[(pv_end - 1) % kTcVStages], ((pv_end - 1) / kTcVStages) & 1u, kWaitLimitNs / 16);
+    if (mma_warp && lane == 0 && (s_end > 0 || pv_end > 0)) {  // one commit covers every product issued
+      tc_commit(mma_drain);
+      mbar_wait_bounded(mma_drain, 0, kWaitLimitNs / 16);
     }
   }
   if (tid == 0) bulk_wait_all();  // the partials' stores are written before the CTA retires
