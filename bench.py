@@ -42,6 +42,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "paged decode KV-read GB/s and % of GB300 HBM peak; decode steps/s"
+FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0
 WORKLOADS = ("llama8b_layer", "long_b4_32k", "long_b1_128k", "mixed_prefix", "fp8_shared",
@@ -134,6 +135,26 @@ def hbm_peak():
         return v, "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def tensor_peak():
+    """Dense bf16 (= f16) tensor-core TFLOP/s: the burst figure, for a kernel
+    timed on its own."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def attention_flops_of(c, T):
+    """Algorithmic FLOPs of one call: 2 D for q.k and 2 D for p.v per
+    (query row, attended key); query token t of a sequence with context
+    length L attends to its first L - T + 1 + t keys."""
+    ctx = np.asarray(c.context_lens, dtype=np.int64)
+    keys = int((T * ctx - T * (T - 1) // 2).sum())
+    return 4 * c.D * c.Hq * keys
 
 
 class ClockSampler:
@@ -677,6 +698,21 @@ def run_ours(args, rank, world):
         gbs, secs, threads, desc = oracle_sample(args.workload, args.cpu_seconds)
         cpu = {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": desc,
                "seconds": secs}
+    # The dominant roof: HBM bytes or tensor-core FLOPs (multi-token calls
+    # with many query rows per KV head do ~4 D T G flops per K/V byte pair).
+    tpeak, tpeak_kind = tensor_peak()
+    flops = 0 if copy else attention_flops_of(c, query_tokens_of(args.workload))
+    tflops = flops / (k_ms * 1e-3) / 1e12
+    hbm = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+           "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback 6.8 TB/s"}
+    tensor = {"bound": "tensor", "achieved": tflops, "peak": tpeak, "unit": "TFLOP/s", "frac": tflops / tpeak,
+              "peak_kind": f"{tpeak_kind} (MEASURED_PEAKS.json bf16_tflops, burst)" if tpeak_kind == "measured"
+              else "fallback 1.9 PFLOP/s bf16"}
+    t_hbm = per_call_bytes / (peak * 1e9)
+    t_tensor = flops / (tpeak * 1e12)
+    bound_fields = dict(tensor if t_tensor > t_hbm else hbm)
+    bound_fields.update({"hbm_frac": hbm["frac"], "tensor_frac": tensor["frac"],
+                         "algorithmic_flops_per_launch": flops})
     if rank == 0:
         plan = w.plan
         line = {
@@ -696,12 +732,8 @@ def run_ours(args, rank, world):
             "decode_steps_per_s": 1e3 / ms,
             "pct_of_hbm_peak": 100.0 * value / peak,
             "pct_of_nominal_8tbs": 100.0 * value / 8000.0,
-            "roofline": {"bound": "hbm", "kernel": "copy_blocks_kernel" if copy else
+            "roofline": {**bound_fields, "kernel": "copy_blocks_kernel" if copy else
                          ("paged_decode_tc_kernel" if plan["math"] == 3 else "paged_decode_kernel"),
-                         "achieved": achieved,
-                         "peak": peak, "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
-                         if peak_kind == "measured" else "fallback 6.8 TB/s",
-                         "unit": "GB/s", "frac": achieved / peak,
                          "traffic": profile_traffic(args.workload, {1: "ffma", 2: "mma", 3: "tc"}.get(plan["math"], "mma")),
                          "algorithmic_bytes_per_launch": per_call_bytes,
                          "kernel_ms_mean": k_ms, "kernel_ms_median": statistics.median(kernel_ms)},

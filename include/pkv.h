@@ -97,7 +97,7 @@ typedef struct {
 /* How the decode computes its dot products. */
 typedef enum {
   PKV_MATH_AUTO = 0, /* the library picks: TC for multi-token bf16 calls with more
-                        than 32 query rows per KV head and head_dim 128, else MMA */
+                        than 16 query rows per KV head and head_dim 128, else MMA */
   PKV_MATH_FFMA = 1, /* fp32 CUDA-core FMAs; G must be 1, 2, 4 or 8; T = 1 */
   PKV_MATH_MMA = 2,  /* mma.sync tiles of up to 16 rows (bf16, or f16 for one-byte
                         caches); G <= 16 */

@@ -145,7 +145,7 @@ def test_multi_token_row_tiles(lib, Hq, Hkv, T, tokens_per_tile, tiles):
 
 @pytest.mark.parametrize("Hq,Hkv,T,math,tokens_per_tile,tiles", [
     (32, 8, 4, 2, 4, 1),        # 16 rows: auto keeps mma.sync
-    (32, 8, 8, 2, 4, 2),        # 32 rows: auto keeps mma.sync (two 16-row tiles)
+    (32, 8, 8, 3, 8, 1),        # 32 rows: auto picks tcgen05 (one 128-row tile)
     (32, 8, 16, 3, 16, 1),      # 64 rows: auto picks tcgen05 (128-row tiles)
     (32, 8, 33, 3, 32, 2),
     (16, 1, 9, 3, 8, 2),        # G 16: 8 tokens per 128-row tile
