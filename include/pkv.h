@@ -108,7 +108,8 @@ typedef enum {
 
 /* Tuning knobs of pkv_paged_decode; a NULL pointer or zero fields = auto. */
 typedef struct {
-  int32_t partition_blocks; /* blocks per split-K partition, 1..64 (0 = auto) */
+  int32_t partition_blocks; /* blocks per split-K partition, 1..64 (0 = auto; auto may
+                               take 128 or 256 for PKV_MATH_TC) */
   int32_t math;             /* pkv_decode_math */
   int32_t warps_per_cta;    /* 1..8 (0 = auto) */
   int32_t stages;           /* pages in each warp's copy ring, 2..8 (0 = auto) */

@@ -467,9 +467,9 @@ cudaError_t launch_decode(const DecodeLaunch& L, int* launched) {
   p.fused_merge = (!L.tc && L.pmax <= kFusedMergeMaxParts) ? 1 : 0;
   p.row_base = L.row_base;
   p.scale_log2 = L.scale_log2;
-  CUtensorMap kmap = L.kmap, vmap = L.vmap, omap = L.omap;
+  CUtensorMap kmap = L.kmap, vmap = L.vmap, pmap = L.pmap, omap = L.omap;
   void* args_mma[] = {&kmap, &vmap, &p};
-  void* args_tc[] = {&kmap, &vmap, &omap, &p};  // + the partial-output store map
+  void* args_tc[] = {&kmap, &vmap, &pmap, &omap, &p};  // + the partial and output store maps
   void** args = L.tc ? args_tc : args_mma;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));

@@ -51,7 +51,7 @@ constexpr int kTcRows = 128;        // query rows per tile (MMA M)
 constexpr int kTcTokens = 64;       // tokens per step (N of S)
 constexpr int kTcKStages = 4;       // K ring; a stage holds K(g), then P(g)
 constexpr int kTcVStages = 2;       // V ring
-constexpr int kTcMaxPages = 64;     // pages of a unit (the planner's partition length for this kernel)
+constexpr int kTcMaxPages = 256;    // pages of a unit (the planner's partition length for this kernel)
 constexpr int kTcComputeWarps = 4;  // one row of the tile per thread
 constexpr int kTcThreads = 32 * (kTcComputeWarps + 3);  // + MMA warp + K copy warp + V copy warp
 constexpr uint32_t kTcCols = 256;   // TMEM columns: S at 0, Q at 64, O at 128
@@ -66,9 +66,9 @@ struct TcLayout {  // byte offsets from the 1024-aligned shared-memory base
   static constexpr uint32_t kV = kK + kTcKStages * kTile;    // V ring
   static constexpr uint32_t kBars = kV + kTcVStages * kTile;
   // full_k[4], kp_free[4], full_v[2], v_free[2], s_done, s_free, p_ready,
-  // q_ready, slot_full[2], slot_free[2], stg_done, stg_full, stg_free,
-  // o_ready, mma_drain
-  static constexpr int kNumBars = 2 * kTcKStages + 2 * kTcVStages + 4 + 4 + 5;
+  // q_ready, slot_full[2], slot_free[2], stg_full, stg_free, o_ready,
+  // mma_drain
+  static constexpr int kNumBars = 2 * kTcKStages + 2 * kTcVStages + 4 + 4 + 4;
   static constexpr uint32_t kMisc = kBars + 8 * kNumBars;    // TMEM base
   static constexpr uint32_t kSlots = kMisc + 16;             // 2 unit slots
   static constexpr uint32_t kSlotPages = 32;                 // after 8 int32 of descriptor
@@ -119,7 +119,8 @@ template <int BS>
 __global__ void __launch_bounds__(kTcThreads, 2)
     paged_decode_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                            const __grid_constant__ CUtensorMap vmap,
-                           const __grid_constant__ CUtensorMap omap,  // split-K partials (unused otherwise)
+                           const __grid_constant__ CUtensorMap pmap,  // split-K partials (pmax > 1)
+                           const __grid_constant__ CUtensorMap omap,  // bf16 output
                            const DecodeParams p) {
   constexpr int D = 128;
   constexpr int PPI = kTcTokens / BS;  // pages per step
@@ -131,8 +132,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   // index g (K stage and full_k[] / kp_free[] by g % 4, V stage and full_v[] /
   // v_free[] by g % 2, s_done / s_free / p_ready once per step) or by the
   // unit index i (slot_full[] / slot_free[] by i % 2, q_ready and o_ready
-  // once per unit, stg_done once per unit written directly) or by the
-  // split-K output chunk (stg_full once, stg_free twice per unit).
+  // once per unit) or by the output chunks (stg_full once per chunk, stg_free
+  // twice per split-K unit).
   // Every barrier completes one phase per use, and no waiter can fall two
   // phases behind (each next use of a barrier depends on the wait).
   uint64_t* full_k = reinterpret_cast<uint64_t*>(sm + TcLayout::kBars);  // [4] K(g) landed
@@ -145,8 +146,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   uint64_t* q_ready = p_ready + 1;            // the unit's query tile in TMEM
   uint64_t* slot_full = q_ready + 1;          // [2] unit slot written
   uint64_t* slot_free = slot_full + 2;        // [2] unit slot released by every reader
-  uint64_t* stg_done = slot_free + 2;         // the compute warps are done staging a unit's output
-  uint64_t* stg_full = stg_done + 1;          // split-K partials: 32 columns of the tile staged
+  uint64_t* stg_full = slot_free + 2;         // a chunk of the unit's output staged by every compute warp
   uint64_t* stg_free = stg_full + 1;          // split-K partials: a store has read its staging buffer
   uint64_t* o_ready = stg_free + 1;           // a unit's last P . V done: O final, its K and V stages idle
   uint64_t* mma_drain = o_ready + 1;          // after a timeout: every product issued is done
@@ -175,7 +175,6 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       mbar_init(&slot_full[s], 1);
       mbar_init(&slot_free[s], kTcComputeWarps + 2);  // compute warps, MMA warp, V copy warp
     }
-    mbar_init(stg_done, kTcComputeWarps);
     mbar_init(stg_full, kTcComputeWarps);
     mbar_init(stg_free, 1);
     mbar_init(o_ready, 1);
@@ -183,7 +182,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     fence_mbar_init();
     prefetch_tensormap(&kmap);
     prefetch_tensormap(&vmap);
-    if (p.pmax > 1) prefetch_tensormap(&omap);
+    if (p.pmax > 1) prefetch_tensormap(&pmap);
+    prefetch_tensormap(&omap);
   }
   if (warp == 0) tc_alloc(tmem_slot, kTcCols);
   tc_fence_before_sync();
@@ -226,7 +226,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     U.tile = rem - U.kvh * p.NT;
     U.t0 = U.pidx * ppu_tokens;
     U.t1 = min(U.ctx, U.t0 + ppu_tokens);
-    U.npages = (U.t1 - U.t0 + BS - 1) / BS;  // 1 .. 64
+    U.npages = (U.t1 - U.t0 + BS - 1) / BS;  // 1 .. kTcMaxPages
     U.nsteps = (U.npages + PPI - 1) / PPI;
     return U;
   };
@@ -276,7 +276,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         const int rem = u - (u / units_per_part) * units_per_part;
         kvh = rem / p.NT;
         const int t0 = pidx * ppu_tokens;
-        const int npages = (min(ctx, t0 + ppu_tokens) - t0 + BS - 1) / BS;
+        const int npages = (min(ctx, t0 + ppu_tokens) - t0 + BS - 1) / BS;  // 1 .. kTcMaxPages
         nsteps = (npages + PPI - 1) / PPI;
         const int* trow = p.block_tables + static_cast<size_t>(b) * p.MB + t0 / BS;
         volatile int* pg = reinterpret_cast<volatile int*>(sm + TcLayout::kSlots + k * TcLayout::kSlot + TcLayout::kSlotPages);
@@ -464,7 +464,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       tc_st32(t_lane + kTcQCol + 32 * half, w);
     };
     const float c = p.scale_log2;
-    uint32_t ndirect = 0, nchunk = 0, nfree = 0;  // phases of stg_done, stg_full, stg_free
+    uint32_t nchunk = 0, nfree = 0;  // phases of stg_full, stg_free
     // The unit stays in its slot until these warps release it, so only what
     // the steps need is kept in registers; the rest is read again for the
     // output.
@@ -663,10 +663,10 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         ok = false;
         break;
       }
-      // the unit's last P . V, then the output: each warp stages its 32 rows
-      // 32 columns at a time in the last step's K stage (P . V is done with
-      // it), so that the global stores write whole lines; every lane loads
-      // (tcgen05.ld is warp-collective), rows without a query token write nothing
+      // the unit's last P . V, then the output, staged in the last step's K
+      // and V stages (P . V is done with them) and written by tensor-map
+      // stores; every lane loads (tcgen05.ld is warp-collective), and the
+      // store box holds only the tile's query rows (tokens past T clipped)
       const uint32_t gl = g0 + nsteps - 1;
       if (!mbar_wait_spin(o_ready, i & 1u, kWaitLimitNs)) timed_out = true;
       if (__any_sync(kFull, timed_out)) {
@@ -684,47 +684,46 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       const bool direct = U.nparts == 1;
       uint8_t* stg_base = sm + TcLayout::kK + (gl % kTcKStages) * TcLayout::kTile;  // [128 rows][128 B]
       if (direct) {
-        // bf16 output: warp w stages its rows 32 columns at a time and
-        // writes them back as 64-byte row pieces
-        if (tid == 0) mbar_arrive(&v_free[gl % kTcVStages]);  // not used for staging here
+        // bf16 output (O / l): two chunks of 64 columns as 128-byte rows of
+        // bf16, staged in the last step's K and V stages (16-byte chunks
+        // XOR-swizzled by row, as the output map's 128-byte swizzle reads
+        // them) and written by thread 0 with one tensor-map store each
         const float osc = l > 0.f ? 1.f / l : 0.f;
-        const long long orow = static_cast<long long>(qrow);
-        uint8_t* stg = stg_base + warp * 4096;
+        uint8_t* vbuf = sm + TcLayout::kV + (gl % kTcVStages) * TcLayout::kTile;
 #pragma unroll 1
-        for (int cc = 0; cc < D; cc += 32) {
-          uint32_t ov[32];
-          tc_ld32(t_lane + kTcOCol + cc, ov);
-          tc_wait_ld();
+        for (int k2 = 0; k2 < 2; ++k2, ++nchunk) {
+          uint8_t* buf = k2 ? vbuf : stg_base;
+#pragma unroll 1
+          for (int hh = 0; hh < 2; ++hh) {  // 32 columns at a time
+            uint32_t ov[32];
+            tc_ld32(t_lane + kTcOCol + 64 * k2 + 32 * hh, ov);
+            tc_wait_ld();
 #pragma unroll
-          for (int c4 = 0; c4 < 8; ++c4)  // 16-byte chunks, XOR-swizzled by row
-            *reinterpret_cast<float4*>(stg + lane * 128 + ((c4 ^ (lane & 7)) << 4)) =
-                make_float4(__uint_as_float(ov[4 * c4]) * osc, __uint_as_float(ov[4 * c4 + 1]) * osc,
-                            __uint_as_float(ov[4 * c4 + 2]) * osc, __uint_as_float(ov[4 * c4 + 3]) * osc);
-          __syncwarp();
-#pragma unroll
-          for (int it = 0; it < 4; ++it) {  // lane: row 8 it + lane / 4, columns 8 (lane % 4) .. +7
-            const int r = 8 * it + (lane >> 2), cp = lane & 3;
-            const float4 a = *reinterpret_cast<const float4*>(stg + r * 128 + (((2 * cp) ^ (r & 7)) << 4));
-            const float4 e = *reinterpret_cast<const float4*>(stg + r * 128 + (((2 * cp + 1) ^ (r & 7)) << 4));
-            const int rok = __shfl_sync(kFull, row_ok ? 1 : 0, r);
-            const long long rs = __shfl_sync(kFull, orow, r);
-            if (rok)
-              *reinterpret_cast<uint4*>(p.out + rs * D + cc + 8 * cp) =
-                  make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(e.x, e.y), pack_bf16x2(e.z, e.w));
+            for (int c4 = 0; c4 < 4; ++c4) {
+              const float* f = reinterpret_cast<const float*>(ov + 8 * c4);
+              *reinterpret_cast<uint4*>(buf + tid * 128 + (((4 * hh + c4) ^ (tid & 7)) << 4)) =
+                  make_uint4(pack_bf16x2(f[0] * osc, f[1] * osc), pack_bf16x2(f[2] * osc, f[3] * osc),
+                             pack_bf16x2(f[4] * osc, f[5] * osc), pack_bf16x2(f[6] * osc, f[7] * osc));
+            }
           }
-          __syncwarp();  // before the next columns overwrite the staging
+          fence_proxy_async_smem();  // read by the tensor-map store
+          __syncwarp();
+          if (lane == 0) mbar_arrive(stg_full);
+          if (tid == 0) {
+            if (mbar_wait_spin(stg_full, nchunk & 1u, kWaitLimitNs)) {
+              tma_store_4d(&omap, buf, 64 * k2, U.kvh * p.G, U.tile * p.Tt, U.b);
+              bulk_commit();
+            } else {
+              timed_out = true;
+            }
+          }
         }
-        // the stage goes back to the K copy warp once all four warps are done
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(stg_done);
-        if (tid == 0) {
-          if (mbar_wait_spin(stg_done, ndirect & 1u, kWaitLimitNs))
-            mbar_arrive(&kp_free[gl % kTcKStages]);
-          else
-            timed_out = true;
+        // both stages go back to the copy warps once the stores have read them
+        if (tid == 0 && !timed_out) {
+          bulk_wait_read_all();
+          mbar_arrive(&kp_free[gl % kTcKStages]);
+          mbar_arrive(&v_free[gl % kTcVStages]);
         }
-        ++ndirect;
       } else {
         // split-K partials (m, l, unnormalised O): the tile's rows are staged
         // 32 columns at a time (row r at r * 128 bytes, 16-byte chunks
@@ -753,7 +752,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
           if (lane == 0) mbar_arrive(stg_full);
           if (tid == 0) {
             if (mbar_wait_spin(stg_full, nchunk & 1u, kWaitLimitNs)) {
-              tma_store_5d(&omap, buf, cc, U.pidx, U.kvh * p.G, U.tile * p.Tt, U.b);
+              tma_store_5d(&pmap, buf, cc, U.pidx, U.kvh * p.G, U.tile * p.Tt, U.b);
               bulk_commit();
               if (k == 1 || k == 2) {  // the store of chunk k - 1 has read its buffer
                 bulk_wait_read_but1();

@@ -176,6 +176,26 @@ pkv_status encode_partial_map(CUtensorMap* map, void* part_o, int B, int T, int 
   return PKV_OK;
 }
 
+// Store map of the bf16 output out [B][T][Hq][D] for the tcgen05 kernel: a
+// box of 64 columns x the G heads of a KV head x the Tt query tokens of a row
+// tile (128-byte rows, swizzled as the kernel stages them).
+pkv_status encode_output_map(CUtensorMap* map, void* out, int B, int T, int Hq, int D, int G, int Tt) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+  pkv_status st = tensor_map_encoder(&enc);
+  if (st != PKV_OK) return st;
+  const cuuint64_t row = static_cast<cuuint64_t>(D) * 2;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hq), static_cast<cuuint64_t>(T),
+                        static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {row, row * Hq, row * Hq * T};
+  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(Tt), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, out, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled (output) failed (%d)", static_cast<int>(r));
+  return PKV_OK;
+}
+
 // Host copies of device tables for PKV_VALIDATE.
 template <typename T>
 pkv_status fetch(std::vector<T>& dst, const T* src, size_t n, cudaStream_t stream) {
@@ -361,6 +381,7 @@ static pkv_status resolve_decode(const pkv_cache_desc* c, int32_t batch, int32_t
   if (smem > 227u * 1024u)
     return fail(PKV_ERR_INVALID_ARG, "warps x stages need %zu bytes of shared memory", smem);
   int ppu = o.partition_blocks != 0 ? o.partition_blocks : env_int("PKV_DECODE_PARTITION_BLOCKS", 0);
+  if (ppu < 0 || ppu > 64) return fail(PKV_ERR_INVALID_ARG, "partition_blocks %d outside 1..64", ppu);
   if (ppu == 0) {
     // The decode is a persistent grid of W streaming warps pulling units of
     // work; its time follows how full the last round of units is.  Estimate
@@ -380,9 +401,23 @@ static pkv_status resolve_decode(const pkv_cache_desc* c, int32_t batch, int32_t
     // rows each, so they stay at 32 or 64 blocks (measured on the 4- and
     // 8-token verify steps: 32 beats 16 by 4-10% in the kernel).
     const std::vector<int> sizes = T > 1 ? std::vector<int>{32, 64} : std::vector<int>{32, 16, 8};
-    // the tcgen05 kernel's per-unit start-up and partial writes make 64-block
-    // units the fastest at every size measured (10-20% over 32)
-    if (tc || units(64) <= W) {
+    if (tc) {
+      // tcgen05 units cost their 64-token steps plus a start-up and write-out
+      // of about 6.5 steps (measured on GB300); rounds of 2 x SMs units:
+      // the size of {64, 128, 256} blocks with the least modelled time
+      // (long units also drop the split-K partials and the merge)
+      double best = 0.0;
+      for (int pp : {64, 128, 256}) {
+        const long long rounds = (units(pp) + W - 1) / W;
+        const double cost = static_cast<double>(rounds) *
+                            (static_cast<double>(pp) * c->block_size / 64.0 + 6.5);
+        if (best == 0.0 || cost < best) {
+          best = cost;
+          ppu = pp;
+        }
+        if (pp >= MB) break;  // one partition per sequence already
+      }
+    } else if (units(64) <= W) {
       ppu = 64;
     } else {
       double best = -1.0;
@@ -396,7 +431,6 @@ static pkv_status resolve_decode(const pkv_cache_desc* c, int32_t batch, int32_t
       }
     }
   }
-  if (ppu < 1 || ppu > 64) return fail(PKV_ERR_INVALID_ARG, "partition_blocks %d outside 1..64", ppu);
   ppu = std::min(ppu, MB);
   if ((MB + ppu - 1) / ppu > 65536)
     return fail(PKV_ERR_UNSUPPORTED, "more than 65536 partitions per sequence; raise partition_blocks");
@@ -564,8 +598,9 @@ static pkv_status decode_call(const pkv_cache_desc* cache, const void* q, int32_
   L.part_ml = reinterpret_cast<float*>(ws + wl.part_ml);
   L.part_o = reinterpret_cast<float*>(ws + wl.part_o);
   if (L.tc && L.pmax > 1 &&
-      (st = encode_partial_map(&L.omap, L.part_o, batch, L.T, L.Hq, L.pmax, L.D, L.G, L.Tt)) != PKV_OK)
+      (st = encode_partial_map(&L.pmap, L.part_o, batch, L.T, L.Hq, L.pmax, L.D, L.G, L.Tt)) != PKV_OK)
     return st;
+  if (L.tc && (st = encode_output_map(&L.omap, out, batch, L.T, L.Hq, L.D, L.G, L.Tt)) != PKV_OK) return st;
   L.err = dev->err_word;
   L.row_base = static_cast<int>(static_cast<long long>(slot) * cache->num_blocks * cache->num_kv_heads *
                                 cache->block_size);

@@ -58,7 +58,8 @@ struct DecodeLaunch {
   int warps;   // per CTA
   int stages;  // per warp
   CUtensorMap kmap, vmap;
-  CUtensorMap omap;  // tcgen05 kernel with split-K: store map of part_o ([B][T][Hq][pmax][D] fp32)
+  CUtensorMap pmap;  // tcgen05 kernel with split-K: store map of part_o ([B][T][Hq][pmax][D] fp32)
+  CUtensorMap omap;  // tcgen05 kernel: store map of out ([B][T][Hq][D] bf16)
   cudaStream_t stream;
   int num_sms;
   cudaEvent_t ev_start, ev_end;  // optional, recorded around the decode kernel
