@@ -8,9 +8,10 @@
 // sharing); "KV-Cache Engineering: The Memory Wall of LLM Serving" --
 // "Lever 5: Offloading", "When the cache fills" (swap to host memory).
 //
-// One CTA per pair; the threads stream a block's 16-byte chunks in order
-// (coalesced on both sides), four K and four V chunks in flight per thread.  Bandwidth-bound: 2 x block bytes moved
-// per pair (read + write).
+// A CTA copies one slice of a pair: kCopySliceChunks 16-byte chunks of K and
+// the same of V (4 KiB each), every load of a thread issued before its
+// stores, coalesced on both sides.  Small slices keep the last wave of CTAs
+// short.  Bandwidth-bound: 2 x block bytes moved per pair (read + write).
 #include <algorithm>
 
 #include "pkv_device.cuh"
@@ -18,7 +19,9 @@
 
 namespace pkv {
 
-constexpr int kCopyThreads = 256;
+constexpr int kCopyThreads = 128;
+constexpr int kCopySliceChunks = 256;                       // per tensor (K or V)
+constexpr int kCopyPerThread = kCopySliceChunks / kCopyThreads;  // 2
 
 __global__ void __launch_bounds__(kCopyThreads)
     copy_blocks_kernel(const uint4* __restrict__ src_k, const uint4* __restrict__ src_v,
@@ -29,39 +32,42 @@ __global__ void __launch_bounds__(kCopyThreads)
                        int scales_per_block, unsigned* __restrict__ err) {
   pdl_trigger();
   pdl_wait();
-  for (int i = blockIdx.x; i < count; i += gridDim.x) {
+  const int64_t slices = (chunks_per_block + kCopySliceChunks - 1) / kCopySliceChunks;
+  const int64_t items = static_cast<int64_t>(count) * slices;
+  for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
+    const int i = static_cast<int>(it / slices);
+    const int64_t slice = it - static_cast<int64_t>(i) * slices;
     const int s = pairs[2 * i], d = pairs[2 * i + 1];
     if (static_cast<unsigned>(s) >= static_cast<unsigned>(src_nb) ||
         static_cast<unsigned>(d) >= static_cast<unsigned>(dst_nb)) {
-      if (threadIdx.x == 0) atomicOr(err, PKV_DEVERR_BLOCK_ID);
+      if (threadIdx.x == 0 && slice == 0) atomicOr(err, PKV_DEVERR_BLOCK_ID);
       continue;
     }
-    const uint4* sk = src_k + static_cast<int64_t>(s) * chunks_per_block;
-    const uint4* sv = src_v + static_cast<int64_t>(s) * chunks_per_block;
-    uint4* dk = dst_k + static_cast<int64_t>(d) * chunks_per_block;
-    uint4* dv = dst_v + static_cast<int64_t>(d) * chunks_per_block;
-    // 4 chunks of K and 4 of V in flight per thread
-    int64_t c = threadIdx.x;
-    for (; c + 3 * kCopyThreads < chunks_per_block; c += 4 * kCopyThreads) {
-      uint4 a[4], b[4];
+    const int64_t base = slice * kCopySliceChunks;
+    const uint4* sk = src_k + static_cast<int64_t>(s) * chunks_per_block + base;
+    const uint4* sv = src_v + static_cast<int64_t>(s) * chunks_per_block + base;
+    uint4* dk = dst_k + static_cast<int64_t>(d) * chunks_per_block + base;
+    uint4* dv = dst_v + static_cast<int64_t>(d) * chunks_per_block + base;
+    const int64_t rest = chunks_per_block - base;
+    const int64_t n = rest < kCopySliceChunks ? rest : kCopySliceChunks;
+    uint4 a[kCopyPerThread], b[kCopyPerThread];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        a[u] = sk[c + u * kCopyThreads];
-        b[u] = sv[c + u * kCopyThreads];
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        dk[c + u * kCopyThreads] = a[u];
-        dv[c + u * kCopyThreads] = b[u];
+    for (int u = 0; u < kCopyPerThread; ++u) {
+      const int64_t c = threadIdx.x + u * kCopyThreads;
+      if (c < n) {
+        a[u] = sk[c];
+        b[u] = sv[c];
       }
     }
-    for (; c < chunks_per_block; c += kCopyThreads) {
-      const uint4 a = sk[c];
-      const uint4 b = sv[c];
-      dk[c] = a;
-      dv[c] = b;
+#pragma unroll
+    for (int u = 0; u < kCopyPerThread; ++u) {
+      const int64_t c = threadIdx.x + u * kCopyThreads;
+      if (c < n) {
+        dk[c] = a[u];
+        dv[c] = b[u];
+      }
     }
-    if (src_ks != nullptr) {
+    if (src_ks != nullptr && slice == 0) {
       for (int h = threadIdx.x; h < scales_per_block; h += kCopyThreads) {
         dst_ks[static_cast<int64_t>(d) * scales_per_block + h] = src_ks[static_cast<int64_t>(s) * scales_per_block + h];
         dst_vs[static_cast<int64_t>(d) * scales_per_block + h] = src_vs[static_cast<int64_t>(s) * scales_per_block + h];
@@ -75,9 +81,11 @@ cudaError_t launch_copy_blocks(const void* src_k, const void* src_v, const float
                                float* dst_ks, float* dst_vs, int dst_nb, const int32_t* pairs,
                                int count, int64_t block_bytes, int scales_per_block,
                                int num_sms, unsigned* err, cudaStream_t stream) {
-  // one CTA per pair (the hardware scheduler balances the tail); a grid-stride
-  // loop covers counts beyond the grid limit
-  const int grid = static_cast<int>(std::min<int64_t>(count, 1 << 30));
+  // one CTA per slice of a pair (the hardware scheduler balances the tail); a
+  // grid-stride loop covers counts beyond the grid limit
+  const int64_t chunks = block_bytes / 16;
+  const int64_t items = static_cast<int64_t>(count) * ((chunks + kCopySliceChunks - 1) / kCopySliceChunks);
+  const int grid = static_cast<int>(std::min<int64_t>(items, 1 << 30));
   (void)num_sms;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
