@@ -1,7 +1,8 @@
-"""The five workloads at full size, in the launch configuration the benchmark
-times (default options), compared with the oracle on sampled (sequence,
-head) outputs that it computes one by one; plus the invariants that hold at
-any size (aliased prefix == private copies, bitwise)."""
+"""The five workloads and the verify steps at full size, in the launch
+configuration the benchmark times (default options), compared with the
+oracle on sampled (sequence, head) or (sequence, token, head) outputs that it
+computes one by one; plus the invariants that hold at any size (aliased
+prefix == private copies, bitwise)."""
 import gc
 
 import numpy as np
@@ -11,7 +12,7 @@ import torch
 import oracle
 import paged_kv_cache_274_gb300 as pkv
 from workloads import (fp8_shared_case, llama8b_layer_case, long_context_case, mixed_prefix_case,
-                       tiny_case)
+                       normal_bf16_bits, tiny_case)
 from workloads.gen import unalias_prefix
 from tests._gpu import DeviceCase, assert_close, bf16_dev_to_f64, sample_pairs, to_dev, to_dev_bf16
 
@@ -58,6 +59,38 @@ def test_llama8b_layer_step():
     _check_sampled(dc, out, 0, 48, 2, "llama8b layer")
     out_ffma = dc.decode(opts=pkv.decode_opts(math=pkv.MATH_FFMA))
     _check_sampled(dc, out_ffma, 0, 16, 3, "llama8b layer (ffma)")
+
+
+@pytest.mark.parametrize("T", [4, 8, 32, 128])
+def test_spec_verify_full(T):
+    # the verify step the benchmark times: T draft tokens per sequence appended
+    # at the end of its context (4096 after the append), then one T-token
+    # decode with default options (mma.sync tiles for 16 rows per KV head,
+    # the tcgen05 kernel with long units above), sampled (sequence, token,
+    # head) rows against the oracle
+    c = llama8b_layer_case()
+    dc = DeviceCase(c)
+    pos = c.context_lens.astype(np.int64)[:, None] - T + np.arange(T)[None, :]
+    blk = c.block_tables[np.arange(c.B)[:, None], pos // c.bs].astype(np.int64)
+    slots = (blk * c.bs + pos % c.bs).reshape(-1)
+    kn = normal_bf16_bits(301 + T, (c.B * T, c.Hkv, c.D))
+    vn = normal_bf16_bits(302 + T, (c.B * T, c.Hkv, c.D))
+    q = normal_bf16_bits(303 + T, (c.B, T, c.Hq, c.D))
+    plan = pkv.decode_plan(dc.k, c.B, c.Hq, c.MB, None, T)
+    assert plan["math"] == (pkv.MATH_MMA if T * c.G <= 16 else pkv.MATH_TC)
+    out = pkv.append_and_decode(to_dev_bf16(kn), to_dev_bf16(vn), to_dev(slots), to_dev_bf16(q), dc.k, dc.v,
+                                dc.bt, dc.cl, c.kv_group_ptr.tolist(), 0, c.scale)
+    torch.cuda.synchronize()
+    assert pkv.read_device_error() == 0
+    assert oracle.kv_append(kn, vn, slots, dc.k_host, dc.v_host) == 0
+    rng = np.random.Generator(np.random.PCG64(304 + T))
+    rows = np.stack([rng.integers(0, c.B, 24), rng.integers(0, T, 24), rng.integers(0, c.Hq, 24)], axis=1)
+    rows[0], rows[-1] = (0, 0, 0), (c.B - 1, T - 1, c.Hq - 1)
+    want = oracle.paged_decode_multi(q, dc.k_host, dc.v_host, c.block_tables, c.context_lens, c.kv_group_ptr,
+                                     0, c.scale, rows=rows)
+    got = bf16_dev_to_f64(out)
+    b, t, h = rows[:, 0], rows[:, 1], rows[:, 2]
+    assert_close(got[b, t, h], want[b, t, h], f"verify T={T} ({plan['partition_blocks']}-block partitions)")
 
 
 def test_mixed_prefix_batch():
