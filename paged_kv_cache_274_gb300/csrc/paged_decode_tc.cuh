@@ -85,27 +85,34 @@ __device__ __forceinline__ uint32_t tc_p_off(int r, int k8) {
   return static_cast<uint32_t>((r >> 3) * 1024 + k8 * 128 + (r & 7) * 16);
 }
 
-// Maximum of 64 scores (bit patterns of floats) as a tree; the _neg form
-// gives the maximum of the negated scores (minus the minimum).
-__device__ __forceinline__ float tree_max64(const uint32_t (&v)[kTcTokens]) {
-  float t[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) t[i] = fmaxf(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-#pragma unroll
-  for (int w = 16; w >= 1; w >>= 1)
-#pragma unroll
-    for (int i = 0; i < w; ++i) t[i] = fmaxf(t[i], t[i + w]);
-  return t[0];
+// Three-input maximum and minimum (one instruction each on sm_103a).
+__device__ __forceinline__ float fmax3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
 }
-__device__ __forceinline__ float tree_max64_neg(const uint32_t (&v)[kTcTokens]) {
-  float t[32];
+__device__ __forceinline__ float fmin3f(float a, float b, float c) {
+  float r;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Maximum (kMax) or minimum of 64 scores (bit patterns of floats) as a tree
+// of three-input operations: 32 instructions, depth 5.
+template <bool kMax>
+__device__ __forceinline__ float tree_ext64(const uint32_t (&v)[kTcTokens]) {
+  auto op3 = [](float a, float b, float c) { return kMax ? fmax3f(a, b, c) : fmin3f(a, b, c); };
+  float t[22];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) t[i] = fmaxf(-__uint_as_float(v[2 * i]), -__uint_as_float(v[2 * i + 1]));
+  for (int i = 0; i < 21; ++i)
+    t[i] = op3(__uint_as_float(v[3 * i]), __uint_as_float(v[3 * i + 1]), __uint_as_float(v[3 * i + 2]));
+  t[21] = __uint_as_float(v[63]);
 #pragma unroll
-  for (int w = 16; w >= 1; w >>= 1)
-#pragma unroll
-    for (int i = 0; i < w; ++i) t[i] = fmaxf(t[i], t[i + w]);
-  return t[0];
+  for (int i = 0; i < 7; ++i) t[i] = op3(t[3 * i], t[3 * i + 1], t[3 * i + 2]);  // 22 -> 8
+  t[7] = t[21];
+  const float u0 = op3(t[0], t[1], t[2]), u1 = op3(t[3], t[4], t[5]);  // 8 -> 4
+  const float w = op3(u0, u1, t[6]);
+  return kMax ? fmaxf(w, t[7]) : fminf(w, t[7]);
 }
 
 // A unit as the descriptor slot holds it.
@@ -539,8 +546,9 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             tc_st32(t_lane + kTcOCol + cc, ov);
           }
           tc_wait_st();
+          return !__any_sync(kFull, timed_out);  // the only wait here
         }
-        return !__any_sync(kFull, timed_out);
+        return true;
       };
       // V rows of tokens outside the sequence (or of a bad page) may hold
       // anything (even NaN) and P is 0 there: once V(g) has landed, thread
@@ -596,6 +604,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
 
       for (int j = 0; j < nsteps; ++j) {
         const uint32_t g = g0 + j;
+        uint64_t vmask, rmask;
+        step_masks(j, vmask, rmask);  // independent of S: computed while it is on its way
         if (!mbar_wait_spin(s_done, g & 1u, kWaitLimitNs)) timed_out = true;
         if (__any_sync(kFull, timed_out)) {  // warp-uniform exit (the loads below are collective)
           ok = false;
@@ -631,14 +641,15 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(s_free);  // the slot may take S(g + 1)
-        uint64_t vmask, rmask;
-        step_masks(j, vmask, rmask);
         // masked extremum of the raw scores (maximum for a non-negative
         // scale); a step whose tokens are all this row's takes branch-free code
         const bool all = rmask == ~0ull;
         float ext;
         if (all) {
-          ext = c >= 0.f ? tree_max64(sv) : -tree_max64_neg(sv);
+          if (c >= 0.f)
+            ext = tree_ext64<true>(sv);
+          else
+            ext = tree_ext64<false>(sv);
         } else if (c >= 0.f) {
           ext = -INFINITY;
 #pragma unroll
