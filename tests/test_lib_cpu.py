@@ -182,3 +182,18 @@ def test_multi_token_arguments(lib):
     w1 = lib.pkv_decode_multi_workspace_bytes(ctypes.byref(d), 8, 1, 32, 64, ctypes.byref(o))
     w4 = lib.pkv_decode_multi_workspace_bytes(ctypes.byref(d), 8, 4, 32, 64, ctypes.byref(o))
     assert w4 > 3 * w1 > 0
+
+
+@pytest.mark.parametrize("B,MB,ppu", [
+    (64, 256, 256),   # 64 sequences x 8 KV heads of 4096 tokens: 512 whole-sequence units (2 rounds of 304)
+    (4, 256, 64),     # 4 sequences: 64-block units, 128 of them, one round
+    (64, 40, 40)])    # short contexts: one partition per sequence
+def test_tc_partition_length(lib, B, MB, ppu):
+    # the tcgen05 kernel's partition length: the size of {64, 128, 256}
+    # blocks with the least modelled time (rounds of 2 x 152 units x (64-token
+    # steps + 6.5)), capped at the table width; explicit sizes stay 1..64
+    st, plan = _plan(lib, _desc(num_blocks=20000), B, 32, 32, MB)
+    assert st == 0 and plan.math == pkv.MATH_TC
+    assert plan.partition_blocks == ppu
+    assert plan.max_partitions == (MB + ppu - 1) // ppu
+    assert _plan(lib, _desc(num_blocks=20000), B, 32, 32, MB, pkv.decode_opts(partition_blocks=128))[0] == 1
