@@ -65,10 +65,10 @@ struct TcLayout {  // byte offsets from the 1024-aligned shared-memory base
   static constexpr uint32_t kK = 0;                          // K ring
   static constexpr uint32_t kV = kK + kTcKStages * kTile;    // V ring
   static constexpr uint32_t kBars = kV + kTcVStages * kTile;
-  // full_k[4], kp_free[4], full_v[2], v_free[2], s_done, s_free, p_ready,
+  // full_k[4], kp_free[4], full_v[2], v_free[2], s_done, s_free, p_ready[4],
   // q_ready, slot_full[2], slot_free[2], stg_full, stg_free, o_ready,
   // mma_drain
-  static constexpr int kNumBars = 2 * kTcKStages + 2 * kTcVStages + 4 + 4 + 4;
+  static constexpr int kNumBars = 3 * kTcKStages + 2 * kTcVStages + 3 + 4 + 4;
   static constexpr uint32_t kMisc = kBars + 8 * kNumBars;    // TMEM base
   static constexpr uint32_t kSlots = kMisc + 16;             // 2 unit slots
   static constexpr uint32_t kSlotPages = 32;                 // after 8 int32 of descriptor
@@ -136,21 +136,24 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   uint8_t* sm = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   // Barrier phases are counted over the CTA's lifetime: by the global step
-  // index g (K stage and full_k[] / kp_free[] by g % 4, V stage and full_v[] /
-  // v_free[] by g % 2, s_done / s_free / p_ready once per step) or by the
-  // unit index i (slot_full[] / slot_free[] by i % 2, q_ready and o_ready
+  // index g (K stage and full_k[] / kp_free[] / p_ready[] by g % 4, V stage
+  // and full_v[] / v_free[] by g % 2, s_done / s_free once per step) or by
+  // the unit index i (slot_full[] / slot_free[] by i % 2, q_ready and o_ready
   // once per unit) or by the output chunks (stg_full once per chunk, stg_free
   // twice per split-K unit).
-  // Every barrier completes one phase per use, and no waiter can fall two
-  // phases behind (each next use of a barrier depends on the wait).
+  // Every barrier completes one phase per use, and a waiter is never two
+  // phases away from the phase it waits for (a parity wait cannot tell them
+  // apart): each next use of a barrier depends on the wait.  p_ready has one
+  // barrier per K stage for this reason: its next use, step g + 4, needs
+  // K(g + 4) in the stage, i.e. P . V(g) done.
   uint64_t* full_k = reinterpret_cast<uint64_t*>(sm + TcLayout::kBars);  // [4] K(g) landed
   uint64_t* kp_free = full_k + kTcKStages;    // [4] P . V(g) done: K stage (holding P(g)) free
   uint64_t* full_v = kp_free + kTcKStages;    // [2] V(g) landed
   uint64_t* v_free = full_v + kTcVStages;     // [2] P . V(g) done: V stage free, O quiescent
   uint64_t* s_done = v_free + kTcVStages;     // S(g) in TMEM
   uint64_t* s_free = s_done + 1;              // S(g) read by the compute warps
-  uint64_t* p_ready = s_free + 1;             // P(g) in shared memory
-  uint64_t* q_ready = p_ready + 1;            // the unit's query tile in TMEM
+  uint64_t* p_ready = s_free + 1;             // [4] P(g) in shared memory (its K stage)
+  uint64_t* q_ready = p_ready + kTcKStages;   // the unit's query tile in TMEM
   uint64_t* slot_full = q_ready + 1;          // [2] unit slot written
   uint64_t* slot_free = slot_full + 2;        // [2] unit slot released by every reader
   uint64_t* stg_full = slot_free + 2;         // a chunk of the unit's output staged by every compute warp
@@ -176,7 +179,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     }
     mbar_init(s_done, 1);
     mbar_init(s_free, kTcComputeWarps);  // one lane per compute warp
-    mbar_init(p_ready, 32 * kTcComputeWarps);
+    for (int s = 0; s < kTcKStages; ++s) mbar_init(&p_ready[s], 32 * kTcComputeWarps);
     mbar_init(q_ready, kTcComputeWarps);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&slot_full[s], 1);
@@ -397,7 +400,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       // holds it (64-d halves kRegion apart, 8-token groups 1024 B apart);
       // the commits release the stages (and let the compute warps read O)
       auto issue_pv = [&](uint32_t g, bool first, bool last) -> bool {
-        if (!mbar_wait_spin(p_ready, g & 1u, kWaitLimitNs)) return false;
+        if (!mbar_wait_spin(&p_ready[g % kTcKStages], (g / kTcKStages) & 1u, kWaitLimitNs)) return false;
         if (!mbar_wait_bounded(&full_v[g % kTcVStages], (g / kTcVStages) & 1u, kWaitLimitNs)) return false;
         const uint32_t pa = smem_addr(sm + TcLayout::kK + (g % kTcKStages) * TcLayout::kTile);
         const uint32_t v_addr = smem_addr(sm + TcLayout::kV + (g % kTcVStages) * TcLayout::kTile);
@@ -596,10 +599,10 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         }
         return psum;
       };
-      auto finish_step = [&]() {
+      auto finish_step = [&](uint32_t g) {
         fence_proxy_async_smem();  // P and the cleared V rows are read by the tensor cores
         tc_fence_before_sync();
-        mbar_arrive(p_ready);
+        mbar_arrive(&p_ready[g % kTcKStages]);
       };
 
       for (int j = 0; j < nsteps; ++j) {
@@ -668,7 +671,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         uint8_t* pbuf = sm + TcLayout::kK + (g % kTcKStages) * TcLayout::kTile;
         l += write_p(*reinterpret_cast<const uint32_t(*)[32]>(sv), static_cast<uint32_t>(rmask), all, pbuf, 0) +
              write_p(*reinterpret_cast<const uint32_t(*)[32]>(sv + 32), static_cast<uint32_t>(rmask >> 32), all, pbuf, 1);
-        finish_step();
+        finish_step(g);
       }
       if (!ok || __any_sync(kFull, timed_out)) {
         ok = false;
