@@ -66,6 +66,8 @@ def parse_args():
     ap.add_argument("--partition-blocks", type=int, default=0)
     ap.add_argument("--warps", type=int, default=0)
     ap.add_argument("--stages", type=int, default=0)
+    ap.add_argument("--graph", action="store_true",
+                    help="time replays of one step captured in a CUDA graph (launch-bound small steps)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -444,16 +446,31 @@ class CopyWorkload:
 # ---------------------------------------------------------------------------
 # timing
 # ---------------------------------------------------------------------------
-def time_device(w, steps, warmup, world):
+def time_device(w, steps, warmup, world, graph=False):
     """Device-resident inputs.  Loop 1 times K steps between CUDA events on
-    the launching stream (the headline).  Loop 2 repeats K steps with the
-    decode kernel bracketed by events the library records around it (the
-    roofline's kernel time; those events keep the planner and the decode
-    from overlapping, so loop 2 is not used for the step time)."""
+    the launching stream (the headline); with `graph`, one step is captured
+    in a CUDA graph after the warm-up and loop 1 replays it.  Loop 2 repeats
+    K eager steps with the decode kernel bracketed by events the library
+    records around it (the roofline's kernel time; those events keep the
+    planner and the decode from overlapping, so loop 2 is not used for the
+    step time)."""
     stream = torch.cuda.current_stream()
     for _ in range(warmup):
         w.step()
     torch.cuda.synchronize()
+    run_step = w.step
+    if graph:
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            w.step()
+        stream.wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            w.step()
+        g.replay()
+        torch.cuda.synchronize()
+        run_step = g.replay
 
     def made_event():
         ev = torch.cuda.Event(enable_timing=True)
@@ -466,7 +483,7 @@ def time_device(w, steps, warmup, world):
     with ClockSampler(torch.cuda.current_device()) as clk:
         start.record(stream)
         for _ in range(steps):
-            w.step()
+            run_step()
         end.record(stream)
         torch.cuda.synchronize()
         for i in range(steps):
@@ -680,7 +697,7 @@ def run_ours(args, rank, world):
     else:
         w = DeviceWorkload(args.workload, rank, opts_kw)
     c = w.c
-    total_ms, kernel_ms, clocks = time_device(w, args.steps, args.warmup, world)
+    total_ms, kernel_ms, clocks = time_device(w, args.steps, args.warmup, world, graph=args.graph)
     assert pkv.read_device_error() == 0, "device error word set during the benchmark"
     value, ms, kv_total = whole_job_gbs(w.kv_bytes, total_ms / args.steps, world)
     peak, peak_kind = hbm_peak()
@@ -725,6 +742,7 @@ def run_ours(args, rank, world):
             "data": "synthetic (seeded N(0,1) K/V/q, seeded block permutations)",
             "config": config_of(args.workload, c, {
                 "parallelism": "replicas" if world > 1 else "single GPU",
+                "step_launch": "CUDA graph replay" if args.graph else "eager calls (programmatic dependent launch)",
                 "math": {0: "-", 1: "ffma", 2: "mma", 3: "tcgen05"}[plan["math"]],
                 "partition_blocks": plan["partition_blocks"], "max_partitions": plan["max_partitions"],
                 "warps_per_cta": plan["warps_per_cta"], "stages": plan["stages"]}),
