@@ -16,6 +16,12 @@ Metric: KV bytes read per step / step time (GB/s, 1e9), with % of the
 measured HBM peak and decode steps/s beside it.  Inputs (>= 512 MiB of KV)
 are larger than L2, so L2 is not flushed between steps.
 
+Each step is issued through prepared library calls (the step's arguments
+checked and marshalled once, every kernel launched anew each step);
+`--eager-calls` uses the plain calls, `--graph` replays a captured step.
+The e2e leg adds the pinned-host uploads of each step's inputs and the
+download of its output, pipelined on two copy streams.
+
 `--impl reference` times the CPU float64 oracle on a bounded sample of the
 same workload instead (the only place besides the cpu_baseline leg where
 this script runs the oracle).
@@ -68,6 +74,9 @@ def parse_args():
     ap.add_argument("--stages", type=int, default=0)
     ap.add_argument("--graph", action="store_true",
                     help="time replays of one step captured in a CUDA graph (launch-bound small steps)")
+    ap.add_argument("--eager-calls", action="store_true",
+                    help="issue each step through the plain calls (argument checks and marshalling every "
+                         "step) instead of prepared calls")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -304,6 +313,7 @@ class DeviceWorkload:
             self.k_new = torch.from_numpy(c.k_new).view(torch.bfloat16).to(dev)
             self.v_new = torch.from_numpy(c.v_new).view(torch.bfloat16).to(dev)
             self.slots = torch.from_numpy(c.slot_mapping).to(dev)
+        self.append_every_layer = False
         self.opts_kw = opts_kw
         self.opts = pkv.decode_opts(**opts_kw)
         T = query_tokens_of(name)
@@ -313,6 +323,21 @@ class DeviceWorkload:
         self.kv_bytes = kv_bytes_of(c)
         self.launches_per_step = len(self.layers) * self.plan["kernels_per_call"]
         torch.cuda.synchronize()
+
+    def prepare(self, stream=None):
+        """The step as prepared library calls (one per layer), bound to the
+        tensors the workload holds now (and to `stream`, if given): what a
+        serving loop with fixed step buffers calls each step."""
+        pkv, c = self.pkv, self.c
+        calls = []
+        for i, layer in enumerate(self.layers):
+            app = self.append and (i == 0 or self.append_every_layer)
+            calls.append(pkv.PreparedDecode(
+                self.q[layer], self.k, self.v, self.bt, self.cl, c.kv_group_ptr.tolist(), layer, c.scale,
+                out=self.out[layer], workspace=self.ws, k_scale=self.ks, v_scale=self.vs, opts=self.opts,
+                k_new=self.k_new if app else None, v_new=self.v_new if app else None,
+                slot_mapping=self.slots if app else None, stream=stream))
+        return calls
 
     def _fill_fp8(self, g):
         """E4M3 cache from bf16 N(0,1) data through the library's own append,
@@ -393,6 +418,7 @@ class VerifyWorkload(DeviceWorkload):
         self.k_new = torch.randn((c.B * T, c.Hkv, c.D), generator=g, device=dev, dtype=torch.bfloat16)
         self.v_new = torch.randn((c.B * T, c.Hkv, c.D), generator=g, device=dev, dtype=torch.bfloat16)
         self.append = True
+        self.append_every_layer = True
         self.launches_per_step = len(self.layers) * self.plan["kernels_per_call"]
         torch.cuda.synchronize()
 
@@ -446,10 +472,23 @@ class CopyWorkload:
 # ---------------------------------------------------------------------------
 # timing
 # ---------------------------------------------------------------------------
-def time_device(w, steps, warmup, world, graph=False):
+def step_launch_mode(w, args):
+    if args.graph:
+        return "graph"
+    return "eager" if args.eager_calls or not hasattr(w, "prepare") else "prepared"
+
+
+STEP_LAUNCH_DESC = {"graph": "CUDA graph replay",
+                    "prepared": "prepared library calls (programmatic dependent launch)",
+                    "eager": "plain library calls (programmatic dependent launch)"}
+
+
+def time_device(w, steps, warmup, world, mode="eager"):
     """Device-resident inputs.  Loop 1 times K steps between CUDA events on
-    the launching stream (the headline); with `graph`, one step is captured
-    in a CUDA graph after the warm-up and loop 1 replays it.  Loop 2 repeats
+    the launching stream (the headline), issued as `mode` says: "eager",
+    the plain calls; "prepared", the step's prepared calls (arguments checked
+    and marshalled once, the kernels launched anew every step); "graph", one
+    step captured in a CUDA graph after the warm-up and replayed.  Loop 2 repeats
     K eager steps with the decode kernel bracketed by events the library
     records around it (the roofline's kernel time; those events keep the
     planner and the decode from overlapping, so loop 2 is not used for the
@@ -459,7 +498,14 @@ def time_device(w, steps, warmup, world, graph=False):
         w.step()
     torch.cuda.synchronize()
     run_step = w.step
-    if graph:
+    if mode == "prepared":
+        calls = w.prepare(stream)
+
+        def run_step():
+            for f in calls:
+                f()
+        run_step()
+    if mode == "graph":
         side = torch.cuda.Stream()
         side.wait_stream(stream)
         with torch.cuda.stream(side):
@@ -495,7 +541,7 @@ def time_device(w, steps, warmup, world, graph=False):
     return total_ms, kernel_ms, clk.summary()
 
 
-def time_e2e(w, steps, warmup, world):
+def time_e2e(w, steps, warmup, world, prepared=True):
     """Through the public API from pinned host memory, pipelined as a serving
     loop would be: each step's inputs (queries, new tokens and slots, block
     tables, lengths) go host->device as one packed staging buffer on a copy
@@ -503,7 +549,9 @@ def time_e2e(w, steps, warmup, world):
     device->host on a second copy stream while the next step computes (two
     streams, so that no upload queues behind a download).  Staging
     and output buffers are double-buffered; events order every copy against
-    the compute that produces or consumes it.  The timed region spans the
+    the compute that produces or consumes it.  With `prepared`, each buffer
+    set's step is prepared once and called every step; otherwise the plain
+    calls run with the buffers of the step.  The timed region spans the
     first upload to the last download."""
     names = ["q", "bt", "cl"] + (["k_new", "v_new", "slots"] if w.append else [])
     tensors = [getattr(w, n) for n in names]
@@ -535,24 +583,39 @@ def time_e2e(w, steps, warmup, world):
         for e in (ev_used[k], ev_out[k]):
             e.record(compute)
 
+    def bind(k):
+        for n_, v in views[k].items():
+            setattr(w, n_, v)
+        w.out = outs[k]
+    calls = []
+    if prepared:
+        for k in range(2):
+            bind(k)
+            calls.append(w.prepare(compute))
+    set_stream = torch.cuda.set_stream
+
     def run(n):
         for i in range(n):
-            k = i % 2
-            with torch.cuda.stream(up):
-                up.wait_event(ev_used[k])               # buffer k no longer read by step i-2
-                dev_blobs[k].copy_(host_blob, non_blocking=True)
-                ev_in[k].record(up)
+            k = i & 1
+            up.wait_event(ev_used[k])                   # buffer k no longer read by step i-2
+            set_stream(up)
+            dev_blobs[k].copy_(host_blob, non_blocking=True)
+            ev_in[k].record(up)
+            set_stream(compute)
             compute.wait_event(ev_in[k])
             compute.wait_event(ev_out[k])               # out buffer k downloaded (step i-2)
-            for n_, v in views[k].items():
-                setattr(w, n_, v)
-            w.out = outs[k]
-            w.step()
+            if prepared:
+                for f in calls[k]:
+                    f()
+            else:
+                bind(k)
+                w.step()
             ev_used[k].record(compute)
-            with torch.cuda.stream(down):
-                down.wait_event(ev_used[k])
-                out_host.copy_(outs[k], non_blocking=True)
-                ev_out[k].record(down)
+            down.wait_event(ev_used[k])
+            set_stream(down)
+            out_host.copy_(outs[k], non_blocking=True)
+            ev_out[k].record(down)
+            set_stream(compute)
 
     run(warmup)
     torch.cuda.synchronize()
@@ -697,7 +760,8 @@ def run_ours(args, rank, world):
     else:
         w = DeviceWorkload(args.workload, rank, opts_kw)
     c = w.c
-    total_ms, kernel_ms, clocks = time_device(w, args.steps, args.warmup, world, graph=args.graph)
+    mode = step_launch_mode(w, args)
+    total_ms, kernel_ms, clocks = time_device(w, args.steps, args.warmup, world, mode=mode)
     assert pkv.read_device_error() == 0, "device error word set during the benchmark"
     value, ms, kv_total = whole_job_gbs(w.kv_bytes, total_ms / args.steps, world)
     peak, peak_kind = hbm_peak()
@@ -706,9 +770,13 @@ def run_ours(args, rank, world):
     achieved = per_call_bytes / (k_ms * 1e-3) / 1e9
     e2e = None
     if not args.no_e2e and not copy:
-        e_ms, h2d, d2h = time_e2e(w, max(5, args.steps // 2), max(3, args.warmup), world)
-        e_ms = max_over_ranks(e_ms / max(5, args.steps // 2), world)
-        e2e = {"value": kv_total / (e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e_ms,
+        # enough steps that the pipeline's fill and drain (one upload, one
+        # download) weigh little: at least K, and at least ~50 ms of steps
+        e_steps = min(4000, max(args.steps, int(math.ceil(50.0 / (total_ms / args.steps)))))
+        e_ms, h2d, d2h = time_e2e(w, e_steps, max(3, args.warmup), world, prepared=mode != "eager")
+        e_ms = max_over_ranks(e_ms / e_steps, world)
+        e2e = {"value": kv_total / (e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e_ms, "steps": e_steps,
+               "step_launch": STEP_LAUNCH_DESC["eager" if mode == "eager" else "prepared"],
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not copy:
@@ -742,7 +810,7 @@ def run_ours(args, rank, world):
             "data": "synthetic (seeded N(0,1) K/V/q, seeded block permutations)",
             "config": config_of(args.workload, c, {
                 "parallelism": "replicas" if world > 1 else "single GPU",
-                "step_launch": "CUDA graph replay" if args.graph else "eager calls (programmatic dependent launch)",
+                "step_launch": STEP_LAUNCH_DESC[mode],
                 "math": {0: "-", 1: "ffma", 2: "mma", 3: "tcgen05"}[plan["math"]],
                 "partition_blocks": plan["partition_blocks"], "max_partitions": plan["max_partitions"],
                 "warps_per_cta": plan["warps_per_cta"], "stages": plan["stages"]}),

@@ -259,6 +259,65 @@ def new_decode_workspace(k_cache: torch.Tensor, batch: int, num_q_heads: int,
     return torch.zeros(n, dtype=torch.uint8, device=k_cache.device)
 
 
+def _marshal_decode(q, k_cache, v_cache, block_tables, context_lens, kv_group_ptr, layer, scale, out,
+                    workspace, k_scale, v_scale, opts, k_new=None, v_new=None, slot_mapping=None,
+                    want_dim=None):
+    """Check one decode call's arguments and turn them into the C call's
+    argument list (without the trailing stream).  Returns (function, args,
+    out, workspace)."""
+    desc = cache_desc(k_cache)
+    _need_cuda("q", q, torch.bfloat16)
+    _need_cuda("k_cache", k_cache)
+    _need_cuda("v_cache", v_cache, k_cache.dtype)
+    _need_cuda("block_tables", block_tables, torch.int32)
+    _need_cuda("context_lens", context_lens, torch.int32)
+    if want_dim is not None and q.dim() != want_dim:
+        raise PkvError(1, "q must be [B][Hq][D]" if want_dim == 3 else "q must be [B][T][Hq][D]")
+    if q.dim() == 3:
+        B, Hq, D = (int(x) for x in q.shape)
+        T = 1
+    elif q.dim() == 4:
+        B, T, Hq, D = (int(x) for x in q.shape)
+    else:
+        raise PkvError(1, "q must be [B][Hq][D] or [B][T][Hq][D]")
+    if D != desc.head_dim or block_tables.dim() != 2 or block_tables.shape[0] != B:
+        raise PkvError(1, "q / block_tables shapes do not match the cache")
+    append = k_new is not None or v_new is not None or slot_mapping is not None
+    if append:
+        _need_cuda("k_new", k_new, torch.bfloat16)
+        _need_cuda("v_new", v_new, torch.bfloat16)
+        _need_cuda("slot_mapping", slot_mapping, torch.int64)
+        N = int(slot_mapping.numel())
+        if k_new.shape != (N, desc.num_kv_heads, desc.head_dim) or v_new.shape != k_new.shape:
+            raise PkvError(1, "k_new / v_new must be [N][Hkv][D] with N = len(slot_mapping)")
+    MB = int(block_tables.shape[1])
+    if out is None:
+        out = torch.empty_like(q)
+    _need_cuda("out", out, torch.bfloat16)
+    if out.shape != q.shape:
+        raise PkvError(1, "out must be shaped like q")
+    if desc.dtype != KV_BF16:
+        _need_page_params(desc, k_scale, "k_scale")
+        _need_page_params(desc, v_scale, "v_scale")
+    if workspace is None:
+        workspace = new_decode_workspace(k_cache, B, Hq, MB, opts, T)
+    gp = (ctypes.c_int32 * len(kv_group_ptr))(*[int(x) for x in kv_group_ptr])
+    if scale is None:
+        scale = D ** -0.5
+    popts = ctypes.byref(opts) if opts is not None else None
+    tail = (_ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_tables), MB,
+            _ptr(context_lens), gp, len(kv_group_ptr), int(layer), float(scale), _ptr(out),
+            _ptr(workspace), int(workspace.numel()), popts)
+    lib = load()
+    if append:
+        return (lib.pkv_append_and_decode,
+                (ctypes.byref(desc), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), N, _ptr(q), B, T, Hq)
+                + tail, out, workspace)
+    if q.dim() == 4:
+        return lib.pkv_paged_decode_multi, (ctypes.byref(desc), _ptr(q), B, T, Hq) + tail, out, workspace
+    return lib.pkv_paged_decode, (ctypes.byref(desc), _ptr(q), B, Hq) + tail, out, workspace
+
+
 def paged_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                  block_tables: torch.Tensor, context_lens: torch.Tensor,
                  kv_group_ptr: Sequence[int] = (0,), layer: int = 0,
@@ -267,32 +326,9 @@ def paged_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                  k_scale: Optional[torch.Tensor] = None, v_scale: Optional[torch.Tensor] = None,
                  opts: Optional[DecodeOpts] = None, stream=None) -> torch.Tensor:
     """One decode step of one layer: returns out [B][Hq][D] (bf16)."""
-    desc = cache_desc(k_cache)
-    _need_cuda("q", q, torch.bfloat16)
-    _need_cuda("k_cache", k_cache)
-    _need_cuda("v_cache", v_cache, k_cache.dtype)
-    _need_cuda("block_tables", block_tables, torch.int32)
-    _need_cuda("context_lens", context_lens, torch.int32)
-    B, Hq, D = (int(x) for x in q.shape)
-    if D != desc.head_dim or block_tables.dim() != 2 or block_tables.shape[0] != B:
-        raise PkvError(1, "q / block_tables shapes do not match the cache")
-    MB = int(block_tables.shape[1])
-    if out is None:
-        out = torch.empty_like(q)
-    _need_cuda("out", out, torch.bfloat16)
-    if desc.dtype != KV_BF16:
-        _need_page_params(desc, k_scale, "k_scale")
-        _need_page_params(desc, v_scale, "v_scale")
-    if workspace is None:
-        workspace = new_decode_workspace(k_cache, B, Hq, MB, opts)
-    gp = (ctypes.c_int32 * len(kv_group_ptr))(*[int(x) for x in kv_group_ptr])
-    if scale is None:
-        scale = D ** -0.5
-    _check(load().pkv_paged_decode(
-        ctypes.byref(desc), _ptr(q), B, Hq, _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
-        _ptr(v_scale), _ptr(block_tables), MB, _ptr(context_lens), gp, len(kv_group_ptr),
-        int(layer), float(scale), _ptr(out), _ptr(workspace), int(workspace.numel()),
-        ctypes.byref(opts) if opts is not None else None, _stream_handle(stream)))
+    fn, args, out, _ = _marshal_decode(q, k_cache, v_cache, block_tables, context_lens, kv_group_ptr, layer,
+                                       scale, out, workspace, k_scale, v_scale, opts, want_dim=3)
+    _check(fn(*args, _stream_handle(stream)))
     return out
 
 
@@ -306,34 +342,9 @@ def paged_decode_multi(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Te
     """T new query tokens per sequence, q [B][T][Hq][D] (bf16), already
     appended as the last T cached tokens; token t attends causally to the
     first context_lens[b] - T + t + 1 tokens.  Returns out [B][T][Hq][D]."""
-    desc = cache_desc(k_cache)
-    _need_cuda("q", q, torch.bfloat16)
-    _need_cuda("k_cache", k_cache)
-    _need_cuda("v_cache", v_cache, k_cache.dtype)
-    _need_cuda("block_tables", block_tables, torch.int32)
-    _need_cuda("context_lens", context_lens, torch.int32)
-    if q.dim() != 4:
-        raise PkvError(1, "q must be [B][T][Hq][D]")
-    B, T, Hq, D = (int(x) for x in q.shape)
-    if D != desc.head_dim or block_tables.dim() != 2 or block_tables.shape[0] != B:
-        raise PkvError(1, "q / block_tables shapes do not match the cache")
-    MB = int(block_tables.shape[1])
-    if out is None:
-        out = torch.empty_like(q)
-    _need_cuda("out", out, torch.bfloat16)
-    if desc.dtype != KV_BF16:
-        _need_page_params(desc, k_scale, "k_scale")
-        _need_page_params(desc, v_scale, "v_scale")
-    if workspace is None:
-        workspace = new_decode_workspace(k_cache, B, Hq, MB, opts, T)
-    gp = (ctypes.c_int32 * len(kv_group_ptr))(*[int(x) for x in kv_group_ptr])
-    if scale is None:
-        scale = D ** -0.5
-    _check(load().pkv_paged_decode_multi(
-        ctypes.byref(desc), _ptr(q), B, T, Hq, _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
-        _ptr(v_scale), _ptr(block_tables), MB, _ptr(context_lens), gp, len(kv_group_ptr),
-        int(layer), float(scale), _ptr(out), _ptr(workspace), int(workspace.numel()),
-        ctypes.byref(opts) if opts is not None else None, _stream_handle(stream)))
+    fn, args, out, _ = _marshal_decode(q, k_cache, v_cache, block_tables, context_lens, kv_group_ptr, layer,
+                                       scale, out, workspace, k_scale, v_scale, opts, want_dim=4)
+    _check(fn(*args, _stream_handle(stream)))
     return out
 
 
@@ -349,43 +360,44 @@ def append_and_decode(k_new: torch.Tensor, v_new: torch.Tensor, slot_mapping: to
     at ``slot_mapping`` into cache slot ``kv_group_ptr[layer]``, then
     :func:`paged_decode` (q [B][Hq][D]) or :func:`paged_decode_multi`
     (q [B][T][Hq][D]).  Returns out, shaped like q."""
-    desc = cache_desc(k_cache)
-    for n, t, dt in (("k_new", k_new, torch.bfloat16), ("v_new", v_new, torch.bfloat16),
-                     ("slot_mapping", slot_mapping, torch.int64), ("q", q, torch.bfloat16),
-                     ("block_tables", block_tables, torch.int32), ("context_lens", context_lens, torch.int32)):
-        _need_cuda(n, t, dt)
-    _need_cuda("k_cache", k_cache)
-    _need_cuda("v_cache", v_cache, k_cache.dtype)
-    if q.dim() == 3:
-        B, Hq, D = (int(x) for x in q.shape)
-        T = 1
-    elif q.dim() == 4:
-        B, T, Hq, D = (int(x) for x in q.shape)
-    else:
-        raise PkvError(1, "q must be [B][Hq][D] or [B][T][Hq][D]")
-    if D != desc.head_dim or block_tables.dim() != 2 or block_tables.shape[0] != B:
-        raise PkvError(1, "q / block_tables shapes do not match the cache")
-    N = int(slot_mapping.numel())
-    if k_new.shape != (N, desc.num_kv_heads, desc.head_dim) or v_new.shape != k_new.shape:
-        raise PkvError(1, "k_new / v_new must be [N][Hkv][D] with N = len(slot_mapping)")
-    MB = int(block_tables.shape[1])
-    if out is None:
-        out = torch.empty_like(q)
-    _need_cuda("out", out, torch.bfloat16)
-    if desc.dtype != KV_BF16:
-        _need_page_params(desc, k_scale, "k_scale")
-        _need_page_params(desc, v_scale, "v_scale")
-    if workspace is None:
-        workspace = new_decode_workspace(k_cache, B, Hq, MB, opts, T)
-    gp = (ctypes.c_int32 * len(kv_group_ptr))(*[int(x) for x in kv_group_ptr])
-    if scale is None:
-        scale = D ** -0.5
-    _check(load().pkv_append_and_decode(
-        ctypes.byref(desc), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), N, _ptr(q), B, T, Hq,
-        _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_tables), MB,
-        _ptr(context_lens), gp, len(kv_group_ptr), int(layer), float(scale), _ptr(out), _ptr(workspace),
-        int(workspace.numel()), ctypes.byref(opts) if opts is not None else None, _stream_handle(stream)))
+    if k_new is None or v_new is None or slot_mapping is None:
+        raise PkvError(1, "k_new, v_new and slot_mapping are required")
+    fn, args, out, _ = _marshal_decode(q, k_cache, v_cache, block_tables, context_lens, kv_group_ptr, layer,
+                                       scale, out, workspace, k_scale, v_scale, opts, k_new, v_new,
+                                       slot_mapping)
+    _check(fn(*args, _stream_handle(stream)))
     return out
+
+
+class PreparedDecode:
+    """A decode call (:func:`paged_decode`, :func:`paged_decode_multi`, or
+    :func:`append_and_decode` when ``k_new`` / ``v_new`` / ``slot_mapping``
+    are given) whose arguments were checked and marshalled once.  Each call
+    of the object enqueues the same launch again, reading whatever the bound
+    tensors hold at that time: the pattern of a serving loop whose step
+    buffers stay in place (as under CUDA graph capture) and whose host cost
+    per step must stay small.  The object keeps every bound tensor alive.
+    ``stream``: the stream bound at preparation (default: the current stream
+    at each call); a call may override it."""
+
+    def __init__(self, q, k_cache, v_cache, block_tables, context_lens, kv_group_ptr=(0,), layer=0,
+                 scale=None, out=None, workspace=None, k_scale=None, v_scale=None, opts=None,
+                 k_new=None, v_new=None, slot_mapping=None, stream=None):
+        fn, args, out, workspace = _marshal_decode(q, k_cache, v_cache, block_tables, context_lens,
+                                                   kv_group_ptr, layer, scale, out, workspace, k_scale,
+                                                   v_scale, opts, k_new, v_new, slot_mapping)
+        self._fn, self._args = fn, args
+        self._keep = (q, k_cache, v_cache, block_tables, context_lens, k_scale, v_scale, opts, k_new,
+                      v_new, slot_mapping)
+        self.out, self.workspace = out, workspace
+        self._stream = None if stream is None else _stream_handle(stream)
+
+    def __call__(self, stream=None) -> torch.Tensor:
+        h = _stream_handle(stream) if (stream is not None or self._stream is None) else self._stream
+        st = self._fn(*self._args, h)
+        if st != PKV_OK:
+            _check(st)
+        return self.out
 
 
 def copy_blocks(src_k: torch.Tensor, src_v: torch.Tensor, dst_k: torch.Tensor,

@@ -6,6 +6,7 @@ import os
 import re
 
 import pytest
+import torch
 
 import paged_kv_cache_274_gb300 as pkv
 from paged_kv_cache_274_gb300 import _build
@@ -111,6 +112,18 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(pkv, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(pkv.PkvError):
         pkv.load()
+
+
+def test_binding_rejects_host_tensors():
+    # every call checks its tensors before anything is launched
+    kc = torch.zeros((1, 4, 2, 16, 64), dtype=torch.bfloat16)
+    q = torch.zeros((2, 8, 64), dtype=torch.bfloat16)
+    bt = torch.zeros((2, 4), dtype=torch.int32)
+    cl = torch.ones(2, dtype=torch.int32)
+    for call in (pkv.paged_decode, pkv.PreparedDecode):
+        with pytest.raises(pkv.PkvError) as ei:
+            call(q, kc, kc, bt, cl)
+        assert ei.value.status == 1 and "CUDA tensor" in str(ei.value)
 
 
 def test_product_path_does_not_import_oracle():
