@@ -541,6 +541,28 @@ def time_device(w, steps, warmup, world, mode="eager"):
     return total_ms, kernel_ms, clk.summary()
 
 
+def read_probe_gbs(nbytes=1 << 30, iters=10):
+    """The read-only HBM rate of this device: the library's read probe
+    streaming a 1 GiB buffer (larger than L2) once per launch, timed with
+    CUDA events around each launch after three warm-up launches."""
+    import paged_kv_cache_274_gb300 as pkv
+    buf = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    out = torch.zeros(1, dtype=torch.int64, device="cuda")
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        pkv.read_probe(buf, out)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+    torch.cuda.synchronize()
+    for a, b in evs:
+        a.record(stream)
+        pkv.read_probe(buf, out)
+        b.record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    del buf
+    return nbytes / (ms * 1e-3) / 1e9, ms
+
+
 def time_e2e(w, steps, warmup, world, prepared=True):
     """Through the public API from pinned host memory, pipelined as a serving
     loop would be: each step's inputs (queries, new tokens and slots, block
@@ -768,6 +790,7 @@ def run_ours(args, rank, world):
     per_call_bytes = w.kv_bytes if copy else kv_bytes_of(c, layers=[0])
     k_ms = statistics.mean(kernel_ms)
     achieved = per_call_bytes / (k_ms * 1e-3) / 1e9
+    probe_gbs, probe_ms = read_probe_gbs()
     e2e = None
     if not args.no_e2e and not copy:
         # enough steps that the pipeline's fill and drain (one upload, one
@@ -823,6 +846,11 @@ def run_ours(args, rank, world):
                          "traffic": profile_traffic(args.workload, {1: "ffma", 2: "mma", 3: "tc"}.get(plan["math"], "mma")),
                          "algorithmic_bytes_per_launch": per_call_bytes,
                          "kernel_ms_mean": k_ms, "kernel_ms_median": statistics.median(kernel_ms)},
+            "hbm_read_probe": {"gbs": probe_gbs, "ms": probe_ms, "bytes": 1 << 30, "kernel": "read_probe_kernel",
+                               "frac_of_copy_peak": probe_gbs / peak,
+                               "kernel_frac_of_read_probe": achieved / probe_gbs,
+                               "note": "read-only streaming rate of this device (the decode's own ceiling); "
+                                       "the roofline peak stays the measured copy rate"},
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": w.launches_per_step * args.steps,

@@ -108,8 +108,9 @@ typedef enum {
 
 /* Tuning knobs of pkv_paged_decode; a NULL pointer or zero fields = auto. */
 typedef struct {
-  int32_t partition_blocks; /* blocks per split-K partition, 1..64 (0 = auto; auto may
-                               take 128 or 256 for PKV_MATH_TC) */
+  int32_t partition_blocks; /* blocks per split-K partition, 1..64, or 1..256 for
+                               PKV_MATH_TC (0 = auto; auto may take 128 or 256 for
+                               PKV_MATH_TC) */
   int32_t math;             /* pkv_decode_math */
   int32_t warps_per_cta;    /* 1..8 (0 = auto) */
   int32_t stages;           /* pages in each warp's copy ring, 2..8 (0 = auto) */
@@ -374,6 +375,24 @@ pkv_status pkv_copy_blocks(const pkv_cache_desc* cache,
                            void* dst_k, void* dst_v, float* dst_k_scale, float* dst_v_scale,
                            int32_t dst_num_blocks, const int32_t* block_pairs, int32_t count,
                            void* stream);
+
+/*
+ * Read-only HBM probe, a measurement aid beside the decode (not part of it):
+ * one kernel launch on `stream` reads `bytes` bytes at `data` once, with
+ * 16-byte streaming loads, and adds the sum of their 32-bit words (unsigned,
+ * modulo 2^64) to *sum.  The decode reads its cache and writes almost
+ * nothing, so its ceiling is the read-only rate; this probe measures that
+ * rate on the same device ("KV Cache Engineering: PagedAttention, Continuous
+ * Batching, Attention Variants, and the Bandwidth Wall", "Two Costs:
+ * Capacity and Bandwidth").
+ *   data   device memory, 16-byte aligned, caller-owned, only read.
+ *   bytes  a multiple of 16 (0: nothing is launched).
+ *   sum    device uint64, 8-byte aligned, caller-owned; added to, not set.
+ * Errors: NULL pointers or a size that is not a multiple of 16 ->
+ * PKV_ERR_INVALID_ARG; misaligned pointers -> PKV_ERR_ALIGNMENT; a failed
+ * launch -> PKV_ERR_CUDA.
+ */
+pkv_status pkv_read_probe(const void* data, size_t bytes, uint64_t* sum, void* stream);
 
 /*
  * Synchronise `stream`, copy the current device's sticky error word into

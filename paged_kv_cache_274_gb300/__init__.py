@@ -109,6 +109,8 @@ def load() -> ctypes.CDLL:
                                                           P, i32, i32, f32, P, popts, P]
         lib.pkv_copy_blocks.restype = ctypes.c_int
         lib.pkv_copy_blocks.argtypes = [pdesc, P, P, P, P, i32, P, P, P, P, i32, P, i32, P]
+        lib.pkv_read_probe.restype = ctypes.c_int
+        lib.pkv_read_probe.argtypes = [P, sz, P, P]
         lib.pkv_read_device_error.restype = ctypes.c_int
         lib.pkv_read_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), P]
         lib.pkv_status_string.restype = ctypes.c_char_p
@@ -455,6 +457,21 @@ def paged_decode_static_workspace(q: torch.Tensor, k_cache: torch.Tensor, v_cach
         len(kv_group_ptr), int(layer), float(scale), _ptr(out),
         ctypes.byref(opts) if opts is not None else None, _stream_handle(stream)))
     return out
+
+
+def read_probe(data: torch.Tensor, sum_out: torch.Tensor, stream=None) -> torch.Tensor:
+    """Read-only HBM probe (a measurement aid, not part of the decode): one
+    launch streams the contiguous CUDA tensor ``data`` once and adds the
+    unsigned sum of its 32-bit words, modulo 2^64, to ``sum_out`` (a CUDA
+    int64 tensor of one element, holding the bits of a uint64)."""
+    if not isinstance(data, torch.Tensor) or not data.is_cuda or not data.is_contiguous():
+        raise PkvError(1, "data must be a contiguous CUDA tensor")
+    _need_cuda("sum_out", sum_out, torch.int64)
+    if sum_out.numel() != 1:
+        raise PkvError(1, "sum_out must hold one element")
+    _check(load().pkv_read_probe(_ptr(data), int(data.numel() * data.element_size()), _ptr(sum_out),
+                                 _stream_handle(stream)))
+    return sum_out
 
 
 def read_device_error(stream=None) -> int:

@@ -23,6 +23,8 @@
 
 namespace pkv {
 
+static_assert(kTcMaxPages == kTcUnitMaxPages, "the tcgen05 unit's page table");
+
 // Kernel tables of the instantiation units.
 const void* decode_kernel_bf16_d64(int bs, int math, int gt);
 const void* decode_kernel_bf16_d128(int bs, int math, int gt);

@@ -381,7 +381,10 @@ static pkv_status resolve_decode(const pkv_cache_desc* c, int32_t batch, int32_t
   if (smem > 227u * 1024u)
     return fail(PKV_ERR_INVALID_ARG, "warps x stages need %zu bytes of shared memory", smem);
   int ppu = o.partition_blocks != 0 ? o.partition_blocks : env_int("PKV_DECODE_PARTITION_BLOCKS", 0);
-  if (ppu < 0 || ppu > 64) return fail(PKV_ERR_INVALID_ARG, "partition_blocks %d outside 1..64", ppu);
+  // partitions of up to 64 blocks for the mma.sync kernels, up to a unit's
+  // page table for the tcgen05 kernel
+  const int ppu_max = tc ? pkv::kTcUnitMaxPages : 64;
+  if (ppu < 0 || ppu > ppu_max) return fail(PKV_ERR_INVALID_ARG, "partition_blocks %d outside 1..%d", ppu, ppu_max);
   if (ppu == 0) {
     // The decode is a persistent grid of W streaming warps pulling units of
     // work; its time follows how full the last round of units is.  Estimate
@@ -718,6 +721,21 @@ pkv_status pkv_copy_blocks(const pkv_cache_desc* cache, const void* src_k, const
                                           cache->num_kv_heads * (cache->dtype == PKV_KV_INT8 ? 2 : 1),
                                           dev->num_sms, dev->err_word, s);
   if (e != cudaSuccess) return cuda_fail(e, "copy_blocks launch");
+  return PKV_OK;
+}
+
+pkv_status pkv_read_probe(const void* data, size_t bytes, uint64_t* sum, void* stream) {
+  if (bytes == 0) return PKV_OK;  // nothing to read, nothing launched
+  if (data == nullptr || sum == nullptr) return fail(PKV_ERR_INVALID_ARG, "data or sum is NULL");
+  if (bytes % 16 != 0) return fail(PKV_ERR_INVALID_ARG, "bytes %zu is not a multiple of 16", bytes);
+  if (reinterpret_cast<uintptr_t>(data) % 16 != 0 || reinterpret_cast<uintptr_t>(sum) % 8 != 0)
+    return fail(PKV_ERR_ALIGNMENT, "data must be 16-byte and sum 8-byte aligned");
+  DeviceInfo* dev = nullptr;
+  pkv_status st = device_info(&dev);
+  if (st != PKV_OK) return st;
+  cudaError_t e = pkv::launch_read_probe(data, bytes, reinterpret_cast<unsigned long long*>(sum), dev->num_sms,
+                                         static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "read probe launch");
   return PKV_OK;
 }
 

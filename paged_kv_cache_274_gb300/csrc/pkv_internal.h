@@ -77,6 +77,8 @@ WorkspaceLayout workspace_layout(int B, int T, int Hq, int Hkv, int NT, int D, i
 bool pdl_enabled();
 
 // Shared memory per CTA of the decode kernel.
+// pages a tcgen05 work unit may span (its descriptor slot's page table)
+constexpr int kTcUnitMaxPages = 256;
 size_t decode_smem_bytes(int kv_fp8, int D, int bs, int warps, int stages, int tc);
 
 // Launch planner + decode (the decode merges split-K partials itself).  Returns cudaSuccess or
@@ -98,5 +100,10 @@ cudaError_t launch_copy_blocks(const void* src_k, const void* src_v, const float
                                float* dst_ks, float* dst_vs, int dst_nb, const int32_t* pairs,
                                int count, int64_t block_bytes, int scales_per_block,
                                int num_sms, unsigned* err, cudaStream_t stream);
+
+// Read-only probe: sums the 32-bit words of `bytes` bytes (a multiple of 16,
+// 16-byte aligned) into *sum; one launch of up to 8 CTAs per SM.
+cudaError_t launch_read_probe(const void* data, size_t bytes, unsigned long long* sum, int num_sms,
+                              cudaStream_t stream);
 
 }  // namespace pkv

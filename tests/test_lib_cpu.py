@@ -32,7 +32,7 @@ def test_header_declares_api():
     names = declared_functions()
     for n in ("pkv_kv_append", "pkv_paged_decode", "pkv_decode_workspace_bytes",
               "pkv_read_device_error", "pkv_status_string", "pkv_paged_decode_multi",
-              "pkv_copy_blocks", "pkv_prefix_cache_match"):
+              "pkv_copy_blocks", "pkv_prefix_cache_match", "pkv_read_probe"):
         assert n in names
 
 
@@ -204,9 +204,21 @@ def test_multi_token_arguments(lib):
 def test_tc_partition_length(lib, B, MB, ppu):
     # the tcgen05 kernel's partition length: the size of {64, 128, 256}
     # blocks with the least modelled time (rounds of 2 x 152 units x (64-token
-    # steps + 6.5)), capped at the table width; explicit sizes stay 1..64
+    # steps + 6.5)), capped at the table width; explicit sizes 1..256
     st, plan = _plan(lib, _desc(num_blocks=20000), B, 32, 32, MB)
     assert st == 0 and plan.math == pkv.MATH_TC
     assert plan.partition_blocks == ppu
     assert plan.max_partitions == (MB + ppu - 1) // ppu
-    assert _plan(lib, _desc(num_blocks=20000), B, 32, 32, MB, pkv.decode_opts(partition_blocks=128))[0] == 1
+    st, p128 = _plan(lib, _desc(num_blocks=20000), B, 32, 32, MB, pkv.decode_opts(partition_blocks=128))
+    assert st == 0 and p128.partition_blocks == min(128, MB)
+    assert _plan(lib, _desc(num_blocks=20000), B, 32, 32, MB, pkv.decode_opts(partition_blocks=257))[0] == 1
+
+
+def test_read_probe_argument_errors(lib):
+    # host checks come before any CUDA call
+    a = ctypes.c_void_p(0x1000)
+    assert lib.pkv_read_probe(None, 16, a, None) == 1
+    assert lib.pkv_read_probe(a, 16, None, None) == 1
+    assert lib.pkv_read_probe(a, 24, a, None) == 1          # not a multiple of 16
+    assert lib.pkv_read_probe(ctypes.c_void_p(0x1008), 16, a, None) == 3   # data not 16-byte aligned
+    assert lib.pkv_read_probe(a, 16, ctypes.c_void_p(0x1004), None) == 3   # sum not 8-byte aligned
