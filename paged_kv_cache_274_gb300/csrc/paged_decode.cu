@@ -32,7 +32,7 @@ const void* decode_kernel_fp8_d128(int bs, int math, int gt);
 const void* decode_kernel_int8_d128(int bs, int math, int gt);
 const void* decode_kernel_mt_bf16(int D, int bs, int gt);
 const void* decode_kernel_mt_1byte(int kv_dtype, int bs, int gt);
-const void* decode_kernel_tc(int bs);
+const void* decode_kernel_tc(int bs, bool rot);
 
 // ---------------------------------------------------------------------------
 // planner: one CTA validates context lengths, counts each sequence's
@@ -322,7 +322,8 @@ size_t decode_smem_bytes(int kv_fp8, int D, int bs, int warps, int stages, int t
 
 // gt: query rows per tile; mt: multi-token kernel (T > 1).
 static const void* pick_kernel(int kv_dtype, int D, int bs, int math, int gt, bool mt) {
-  if (math == PKV_MATH_TC) return (kv_dtype == PKV_KV_BF16 && D == 128) ? decode_kernel_tc(bs) : nullptr;
+  if (math == PKV_MATH_TC)
+    return (kv_dtype == PKV_KV_BF16 && D == 128) ? decode_kernel_tc(bs, gt <= kTcRotMaxRows) : nullptr;
   if (mt) {
     if (math != PKV_MATH_MMA) return nullptr;
     return kv_dtype == PKV_KV_BF16 ? decode_kernel_mt_bf16(D, bs, gt) : decode_kernel_mt_1byte(kv_dtype, bs, gt);

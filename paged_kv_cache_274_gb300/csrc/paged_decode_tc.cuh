@@ -36,6 +36,12 @@
 //     query rows into TMEM; at the end of the unit each thread reads its row
 //     of O and writes the bf16 output or the split-K partials (m, l, O) of
 //     the merge kernels.
+//   * Tiles with at most 96 query rows (kRot) place their rows in the
+//     highest TMEM lanes: thread tid owns tile row (tid - rot) mod 128 with
+//     rot = 128 - (rows rounded up to 32).  A warp all of whose rows are
+//     empty then skips the scores, the softmax and P (its rows of P and O are
+//     never stored): at T x G = 32, say, only warp 3 works, and warp 0, which
+//     shares its sub-partition with the MMA warp, stays idle.
 //
 // Units are (sequence, KV head, row tile, partition) from the planner's
 // counter; the merge kernel combines partitions.  Every wait is bounded; a
@@ -58,6 +64,7 @@ constexpr uint32_t kTcCols = 256;   // TMEM columns: S at 0, Q at 64, O at 128
 constexpr uint32_t kTcSCol = 0;     // S(g): 64 fp32 columns
 constexpr uint32_t kTcQCol = 64;    // query tile: 128 d as 64 columns of bf16 pairs
 constexpr uint32_t kTcOCol = 128;   // O: 128 fp32 columns
+constexpr int kTcRotMaxRows = 96;   // tiles of at most this many rows use the rotated-row instance
 
 struct TcLayout {  // byte offsets from the 1024-aligned shared-memory base
   static constexpr uint32_t kRegion = kTcTokens * 128;       // half (64 of 128 d) of a step's tile: 8 KiB
@@ -120,7 +127,7 @@ struct TcUnit {
   int u, b, pidx, nparts, ctx, kvh, tile, t0, t1, npages, nsteps;
 };
 
-template <int BS>
+template <int BS, bool kRot>
 // Two CTAs per SM: a sub-partition's 16384 registers hold four of the 14
 // warps at 128 registers a thread.
 __global__ void __launch_bounds__(kTcThreads, 2)
@@ -452,12 +459,17 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     }
     __syncwarp();
   } else {
-    // compute warps: thread tid owns row tid of the tile
+    // compute warps: thread tid owns row vrow of the tile (tid itself unless
+    // the rows are rotated into the highest lanes); a warp without rows
+    // (warp_dead) only keeps the barriers' counts and clears stale V rows
+    const int rot = kRot ? 128 - ((p.G * p.Tt + 31) & ~31) : 0;
+    const int vrow = kRot ? ((tid - rot) & 127) : tid;
+    const bool warp_dead = kRot && (32 * warp + 31) < rot;
     // this row of unit U's query tile: loads (in flight until used), then
     // into its TMEM lane, then q_ready
     auto load_query = [&](const TcUnit& U, int half, uint4 (&qv)[8]) {  // d 64 half .. +63
       int t = 0, h = 0;
-      const bool ok = tile_row<true>(p, U.kvh, U.tile, tid, t, h);
+      const bool ok = tile_row<true>(p, U.kvh, U.tile, vrow, t, h);
       const uint4* src = reinterpret_cast<const uint4*>(p.q + (static_cast<size_t>(U.b * p.T + t) * p.Hq + h) * D) + 8 * half;
 #pragma unroll
       for (int c = 0; c < 8; ++c) qv[c] = ok ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
@@ -500,7 +512,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       {
         const TcUnit U = read_unit(k);
         int t = 0, h = 0;
-        row_ok = tile_row<true>(p, U.kvh, U.tile, tid, t, h);
+        row_ok = tile_row<true>(p, U.kvh, U.tile, vrow, t, h);
         nsteps = U.nsteps;
         t0 = U.t0;
         t1 = U.t1;
@@ -609,7 +621,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         const uint32_t g = g0 + j;
         uint64_t vmask, rmask;
         step_masks(j, vmask, rmask);  // independent of S: computed while it is on its way
-        if (!mbar_wait_spin(s_done, g & 1u, kWaitLimitNs)) timed_out = true;
+        if (!mbar_wait_bounded(s_done, g & 1u, kWaitLimitNs)) timed_out = true;
         if (__any_sync(kFull, timed_out)) {  // warp-uniform exit (the loads below are collective)
           ok = false;
           break;
@@ -636,6 +648,16 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             __syncwarp();
             if (lane == 0) mbar_arrive(q_ready);
           }
+        }
+        if (warp_dead) {  // no scores to read: S(g + 1) may come at once
+          __syncwarp();
+          if (lane == 0) mbar_arrive(s_free);
+          if (!clear_stale_v(vmask, g)) {
+            ok = false;
+            break;
+          }
+          finish_step(g);
+          continue;
         }
         uint32_t sv[kTcTokens];
         tc_ld32(t_lane + kTcSCol, *reinterpret_cast<uint32_t(*)[32]>(sv));
@@ -682,7 +704,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       // stores; every lane loads (tcgen05.ld is warp-collective), and the
       // store box holds only the tile's query rows (tokens past T clipped)
       const uint32_t gl = g0 + nsteps - 1;
-      if (!mbar_wait_spin(o_ready, i & 1u, kWaitLimitNs)) timed_out = true;
+      if (!mbar_wait_bounded(o_ready, i & 1u, kWaitLimitNs)) timed_out = true;
       if (__any_sync(kFull, timed_out)) {
         ok = false;
         break;
@@ -692,7 +714,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       size_t qrow;
       {
         int t = 0, h = 0;
-        tile_row<true>(p, U.kvh, U.tile, tid, t, h);
+        tile_row<true>(p, U.kvh, U.tile, vrow, t, h);
         qrow = static_cast<size_t>(U.b * p.T + t) * p.Hq + h;
       }
       const bool direct = U.nparts == 1;
@@ -715,7 +737,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
 #pragma unroll
             for (int c4 = 0; c4 < 4; ++c4) {
               const float* f = reinterpret_cast<const float*>(ov + 8 * c4);
-              *reinterpret_cast<uint4*>(buf + tid * 128 + (((4 * hh + c4) ^ (tid & 7)) << 4)) =
+              *reinterpret_cast<uint4*>(buf + vrow * 128 + (((4 * hh + c4) ^ (vrow & 7)) << 4)) =
                   make_uint4(pack_bf16x2(f[0] * osc, f[1] * osc), pack_bf16x2(f[2] * osc, f[3] * osc),
                              pack_bf16x2(f[4] * osc, f[5] * osc), pack_bf16x2(f[6] * osc, f[7] * osc));
             }
@@ -759,7 +781,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
           uint8_t* buf = (k & 1) ? vbuf : stg_base;
 #pragma unroll
           for (int c4 = 0; c4 < 8; ++c4)
-            *reinterpret_cast<uint4*>(buf + tid * 128 + ((c4 ^ (tid & 7)) << 4)) =
+            *reinterpret_cast<uint4*>(buf + vrow * 128 + ((c4 ^ (vrow & 7)) << 4)) =
                 make_uint4(ov[4 * c4], ov[4 * c4 + 1], ov[4 * c4 + 2], ov[4 * c4 + 3]);
           fence_proxy_async_smem();  // read by the tensor-map store
           __syncwarp();
