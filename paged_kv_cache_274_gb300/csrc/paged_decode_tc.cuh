@@ -535,35 +535,38 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         rmask = row_ok ? (vmask & (nrow >= kTcTokens ? ~0ull : (nrow <= 0 ? 0ull : ((1ull << nrow) - 1ull)))) : 0ull;
       };
       // the step's masked extremum of the raw scores -> running maximum; a
-      // row whose maximum grew by more than 2^8 rescales l and (once
-      // P . V(g - 1) is done) its O in TMEM.  False on timeout.
-      auto update_max = [&](float ext, uint64_t rmask, uint32_t g, int j) -> bool {
+      // row whose maximum grew by more than 2^8 (grow) rescales l here and
+      // its O by the returned factor once P is written (rescale_o)
+      auto update_max = [&](float ext, uint64_t rmask, bool& grow) -> float {
         const float smax = rmask != 0ull ? ext * c : -INFINITY;
         const float mnew = fmaxf(m, smax);
-        const bool grow = (m == -INFINITY) ? (mnew != -INFINITY) : (mnew > m + 8.f);
+        grow = (m == -INFINITY) ? (mnew != -INFINITY) : (mnew > m + 8.f);
         float factor = 1.f;
         if (grow) {
           factor = (m == -INFINITY) ? 0.f : ex2_approx(m - mnew);
           l *= factor;
           m = mnew;
         }
-        if (j > 0 && __any_sync(kFull, grow)) {
-          if (!mbar_wait_spin(&v_free[(g - 1) % kTcVStages], ((g - 1) / kTcVStages) & 1u, kWaitLimitNs))
-            timed_out = true;
-          tc_fence_after_sync();
+        return factor;
+      };
+      // O *= factor in TMEM once P . V(g - 1) is done; after the step's P is
+      // written, so that the scores no longer hold registers.  False on
+      // timeout.
+      auto rescale_o = [&](float factor, uint32_t g) -> bool {
+        if (!mbar_wait_spin(&v_free[(g - 1) % kTcVStages], ((g - 1) / kTcVStages) & 1u, kWaitLimitNs))
+          timed_out = true;
+        tc_fence_after_sync();
 #pragma unroll 1
-          for (int cc = 0; cc < D; cc += 32) {
-            uint32_t ov[32];
-            tc_ld32(t_lane + kTcOCol + cc, ov);
-            tc_wait_ld();
+        for (int cc = 0; cc < D; cc += 32) {
+          uint32_t ov[32];
+          tc_ld32(t_lane + kTcOCol + cc, ov);
+          tc_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * factor);
-            tc_st32(t_lane + kTcOCol + cc, ov);
-          }
-          tc_wait_st();
-          return !__any_sync(kFull, timed_out);  // the only wait here
+          for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * factor);
+          tc_st32(t_lane + kTcOCol + cc, ov);
         }
-        return true;
+        tc_wait_st();
+        return !__any_sync(kFull, timed_out);  // the only wait here
       };
       // V rows of tokens outside the sequence (or of a bad page) may hold
       // anything (even NaN) and P is 0 there: once V(g) has landed, thread
@@ -686,13 +689,19 @@ __global__ void __launch_bounds__(kTcThreads, 2)
           for (int kk = 0; kk < kTcTokens; ++kk)
             if ((rmask >> kk) & 1ull) ext = fminf(ext, __uint_as_float(sv[kk]));
         }
-        if (!update_max(ext, rmask, g, j) || !clear_stale_v(vmask, g)) {
+        bool grow;
+        const float factor = update_max(ext, rmask, grow);
+        if (!clear_stale_v(vmask, g)) {
           ok = false;
           break;
         }
         uint8_t* pbuf = sm + TcLayout::kK + (g % kTcKStages) * TcLayout::kTile;
         l += write_p(*reinterpret_cast<const uint32_t(*)[32]>(sv), static_cast<uint32_t>(rmask), all, pbuf, 0) +
              write_p(*reinterpret_cast<const uint32_t(*)[32]>(sv + 32), static_cast<uint32_t>(rmask >> 32), all, pbuf, 1);
+        if (j > 0 && __any_sync(kFull, grow) && !rescale_o(factor, g)) {
+          ok = false;
+          break;
+        }
         finish_step(g);
       }
       if (!ok || __any_sync(kFull, timed_out)) {
