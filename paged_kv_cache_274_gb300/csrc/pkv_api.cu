@@ -409,11 +409,18 @@ static pkv_status resolve_decode(const pkv_cache_desc* c, int32_t batch, int32_t
       // of about 6.5 steps (measured on GB300); rounds of 2 x SMs units:
       // the size of {64, 128, 256} blocks with the least modelled time
       // (long units also drop the split-K partials and the merge)
+      // A sequence in several partitions also writes split-K partials that
+      // the merge kernel reads back: (query rows) x (D + 2) fp32 per unit,
+      // each way, at about 4 MB per modelled step (measured on GB300: the
+      // 64-token verify step with 128-block units ran 393 us against 345
+      // with whole-sequence units, whose kernel alone is 18 us slower).
+      const double partial_bytes = static_cast<double>(G) * Tt * (c->head_dim + 2) * 4.0;
       double best = 0.0;
       for (int pp : {64, 128, 256}) {
         const long long rounds = (units(pp) + W - 1) / W;
+        const double merge = pp < MB ? static_cast<double>(units(pp)) * partial_bytes * 2.0 / 4.0e6 : 0.0;
         const double cost = static_cast<double>(rounds) *
-                            (static_cast<double>(pp) * c->block_size / 64.0 + 6.5);
+                            (static_cast<double>(pp) * c->block_size / 64.0 + 6.5) + merge;
         if (best == 0.0 || cost < best) {
           best = cost;
           ppu = pp;
