@@ -222,3 +222,16 @@ def test_read_probe_argument_errors(lib):
     assert lib.pkv_read_probe(a, 24, a, None) == 1          # not a multiple of 16
     assert lib.pkv_read_probe(ctypes.c_void_p(0x1008), 16, a, None) == 3   # data not 16-byte aligned
     assert lib.pkv_read_probe(a, 16, ctypes.c_void_p(0x1004), None) == 3   # sum not 8-byte aligned
+
+
+@pytest.mark.parametrize("T,ppu", [(8, 256), (32, 256), (64, 256), (128, 256)])
+def test_tc_partition_length_counts_split_k(lib, T, ppu):
+    # the verify steps of the Llama-8B layer (64 sequences of 256 blocks):
+    # at T = 64 (two row tiles per KV head) 128-block units would take fewer
+    # modelled rounds (7 x 38.5 = 269.5 against 4 x 70.5 = 282), but each
+    # writes 128 rows x 130 fp32 of split-K partials that the merge reads back
+    # (2048 x 133 KB at 4 MB per step: +68), so whole sequences win
+    st, plan = _plan(lib, _desc(num_blocks=20000), 64, T, 32, 256)
+    assert st == 0 and plan.math == pkv.MATH_TC
+    assert plan.partition_blocks == ppu and plan.max_partitions == 1
+    assert plan.kernels_per_call == 2   # planner and decode: no merge launch
