@@ -11,6 +11,7 @@ import concurrent.futures as cf
 import glob
 import hashlib
 import os
+import re
 import shutil
 import subprocess
 import sys
@@ -46,15 +47,27 @@ def source_digest() -> str:
     return h.hexdigest()
 
 
-def kernel_digest() -> str:
-    """sha256 over the GPU-side sources (csrc/*.cu, *.cuh, *.h): what a
-    profile of the kernels was taken on.  Host-only .cpp files and the
-    public headers' prose are not part of it."""
+_BLOCK_COMMENT = re.compile(r"/\*.*?\*/", re.S)
+_LINE_COMMENT = re.compile(r"//[^\n]*")
+_SPACE = re.compile(r"\s+")
+
+
+def _code_only(text: str) -> str:
+    """Source text without comments, runs of white space collapsed."""
+    return _SPACE.sub(" ", _LINE_COMMENT.sub("", _BLOCK_COMMENT.sub(" ", text))).strip()
+
+
+def kernel_digest(csrc: str = CSRC) -> str:
+    """sha256 over the GPU-side sources (csrc/*.cu, *.cuh, *.h) with their
+    comments and white space left out: what a profile of the kernels was
+    taken on.  An edit to a comment keeps the digest; any change to the code
+    changes it.  Host-only .cpp files and the public headers' prose are not
+    part of it."""
     h = hashlib.sha256()
-    files = sorted(f for ext in ("*.cu", "*.cuh", "*.h") for f in glob.glob(os.path.join(CSRC, ext)))
+    files = sorted(f for ext in ("*.cu", "*.cuh", "*.h") for f in glob.glob(os.path.join(csrc, ext)))
     for f in files:
         h.update(os.path.basename(f).encode())
-        h.update(open(f, "rb").read())
+        h.update(_code_only(open(f, encoding="utf-8").read()).encode())
     return h.hexdigest()
 
 

@@ -23,12 +23,14 @@
 //     have P ready; four compute warps own the 128 rows.  The roles hand work
 //     over only through mbarriers, so copies, products and softmax of
 //     neighbouring steps and units overlap.
-//   * Thread r owns row r: it loads its 64 scores from TMEM (and tells the MMA
-//     warp that the S slot is free), masks them (sequence end, bad pages, the
-//     causal limit of its query token), and keeps the online softmax state in
-//     registers.  The running maximum is lazy: the output is rescaled only
-//     when a row's maximum grows by more than 2^8, so P stays below 256 and
-//     the rescale of O in TMEM is rare.  P goes as bf16 (K-major, no swizzle)
+//   * Each compute thread owns one row of the tile (thread r row r in full
+//     tiles; see partial tiles below): it loads its 64 scores from TMEM (and
+//     tells the MMA warp that the S slot is free), masks them (sequence end,
+//     bad pages, the causal limit of its query token), and keeps the online
+//     softmax state in registers.  The running maximum is lazy: the output is
+//     rescaled only when a row's maximum grows by more than 2^8, so P stays
+//     below 256 and the rescale of O in TMEM is rare; it runs after the
+//     step's P is written, when the scores no longer hold registers.  P goes as bf16 (K-major, no swizzle)
 //     into the step's K stage, which is dead once S is done.  V rows of
 //     tokens outside the sequence (or of a bad page) are cleared in the stage,
 //     as P is 0 there but the stale rows may hold NaN.

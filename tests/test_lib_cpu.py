@@ -235,3 +235,19 @@ def test_tc_partition_length_counts_split_k(lib, T, ppu):
     assert st == 0 and plan.math == pkv.MATH_TC
     assert plan.partition_blocks == ppu and plan.max_partitions == 1
     assert plan.kernels_per_call == 2   # planner and decode: no merge launch
+
+
+def test_kernel_digest_ignores_comments_only(tmp_path):
+    # profiles name the sources they were taken on by this digest: a comment
+    # edit keeps it, a code edit changes it
+    import shutil
+    d = tmp_path / "csrc"
+    shutil.copytree(os.path.join(ROOT, "paged_kv_cache_274_gb300", "csrc"), d)
+    base = _build.kernel_digest(str(d))
+    assert base == _build.kernel_digest()
+    f = d / "read_probe.cu"
+    src = f.read_text()
+    f.write_text(src.replace("// Read-only HBM probe", "// A read-only HBM probe", 1) + "\n/* a note */\n")
+    assert _build.kernel_digest(str(d)) == base
+    f.write_text(src.replace("kProbeUnroll = 4", "kProbeUnroll = 2", 1))
+    assert _build.kernel_digest(str(d)) != base
