@@ -113,9 +113,12 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
 
 // Same as mbar_wait_bounded, spinning on the non-blocking test instead of the
 // potentially suspending try_wait: for phases that complete within a
-// microsecond (tensor core products), where a suspended thread would wake up
-// late.  The clock is read only once the phase is found open, so a phase that
-// has already completed costs one test.
+// microsecond, where a suspended thread could wake up late.  A spinning warp
+// takes issue slots from the other warps of its sub-partition, so whole warps
+// that wait while others compute on the same sub-partition (the tcgen05
+// kernel's compute warps waiting for S) use mbar_wait_bounded.  The clock is
+// read only once the phase is found open, so a phase that has already
+// completed costs one test.
 __device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_test_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
