@@ -265,3 +265,24 @@ def test_tc_bad_block_id_flagged_and_skipped():
     want0 = _oracle(dc, q)[0]
     assert_close(got[0], want0, "tc sequence 0")
     assert np.all(np.isfinite(got[1]))
+
+
+@pytest.mark.parametrize("T,ppu", [(8, 0), (8, 1), (32, 0), (32, 1)])
+def test_tc_first_token_is_v0_exactly(T, ppu):
+    # context_lens == T: the first query token attends to position 0 alone,
+    # so its softmax weight is 1 and its output is bf16(V_0) bit for bit, in
+    # the rotated (T x G = 32) and the full-tile (128 rows) instance, with and
+    # without split-K partitions (a partition with no key of the row has
+    # weight 0 in the merge)
+    c = random_case(990 + T + ppu, 3, 32, 8, 128, 16, [T, T, T])
+    dc = DeviceCase(c)
+    q = _q(991 + T, c.B, T, 32, 128)
+    out = pkv.paged_decode_multi(to_dev_bf16(q), dc.k, dc.v, dc.bt, dc.cl, [0], 0, c.scale, opts=_tc_opts(ppu))
+    torch.cuda.synchronize()
+    assert pkv.read_device_error() == 0
+    got = out[:, 0].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)   # [B][Hq][D]
+    G = c.Hq // c.Hkv
+    for b in range(c.B):
+        blk = int(c.block_tables[b, 0])
+        for h in range(c.Hq):
+            assert np.array_equal(got[b, h], dc.v_host[0, blk, h // G, 0]), (b, h)
