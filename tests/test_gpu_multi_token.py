@@ -286,3 +286,49 @@ def test_tc_first_token_is_v0_exactly(T, ppu):
         blk = int(c.block_tables[b, 0])
         for h in range(c.Hq):
             assert np.array_equal(got[b, h], dc.v_host[0, blk, h // G, 0]), (b, h)
+
+
+@pytest.mark.parametrize("T", [8, 32])
+def test_tc_physical_permutation_bitwise_identical(T):
+    # the same logical sequences stored in two different block permutations
+    # give the same output bits: the order of every sum depends only on
+    # logical positions (and the partition length)
+    lens = [70, 300, 40, 129]
+    a = random_case(13 + T, 4, 32, 8, 128, 16, lens)
+    b = random_case(13 + T, 4, 32, 8, 128, 16, lens)
+    perm = np.random.Generator(np.random.PCG64(4)).permutation(a.NB)
+    inv = np.argsort(perm)
+    b.k_src = a.k_src[:, inv].copy()
+    b.v_src = a.v_src[:, inv].copy()
+    b.block_tables = np.where(a.block_tables >= 0, perm[np.maximum(a.block_tables, 0)], -1).astype(np.int32)
+    da, db = DeviceCase(a), DeviceCase(b)
+    q = to_dev_bf16(_q(14 + T, a.B, T, 32, 128))
+    for ppu in (0, 3):
+        oa = pkv.paged_decode_multi(q, da.k, da.v, da.bt, da.cl, [0], 0, a.scale, opts=_tc_opts(ppu))
+        ob = pkv.paged_decode_multi(q, db.k, db.v, db.bt, db.cl, [0], 0, b.scale, opts=_tc_opts(ppu))
+        torch.cuda.synchronize()
+        assert torch.equal(oa, ob), f"T={T} ppu={ppu}"
+
+
+@pytest.mark.parametrize("T", [8, 32])
+def test_tc_aliased_prefix_bitwise_identical(T):
+    # sequences 1 and 2 point at sequence 0's first 4 blocks instead of
+    # private copies holding the same tokens
+    lens = [100, 90, 80]
+    c = random_case(15 + T, 3, 32, 8, 128, 16, lens)
+    for s in (1, 2):
+        for j in range(4):
+            dst, src = c.block_tables[s, j], c.block_tables[0, j]
+            c.k_src[:, dst] = c.k_src[:, src]
+            c.v_src[:, dst] = c.v_src[:, src]
+    private = DeviceCase(c)
+    c2 = random_case(15 + T, 3, 32, 8, 128, 16, lens)
+    c2.k_src, c2.v_src = c.k_src.copy(), c.v_src.copy()
+    for s in (1, 2):
+        c2.block_tables[s, :4] = c.block_tables[0, :4]
+    shared = DeviceCase(c2)
+    q = to_dev_bf16(_q(16 + T, c.B, T, 32, 128))
+    op = pkv.paged_decode_multi(q, private.k, private.v, private.bt, private.cl, [0], 0, c.scale, opts=_tc_opts(2))
+    osh = pkv.paged_decode_multi(q, shared.k, shared.v, shared.bt, shared.cl, [0], 0, c2.scale, opts=_tc_opts(2))
+    torch.cuda.synchronize()
+    assert torch.equal(op, osh)
