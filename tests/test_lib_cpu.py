@@ -5,6 +5,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 import torch
 
@@ -251,3 +252,44 @@ def test_kernel_digest_ignores_comments_only(tmp_path):
     assert _build.kernel_digest(str(d)) == base
     f.write_text(src.replace("kProbeUnroll = 4", "kProbeUnroll = 2", 1))
     assert _build.kernel_digest(str(d)) != base
+
+
+def test_plans_are_consistent_over_random_shapes(lib):
+    # host planning only: for seeded random shapes every accepted plan covers
+    # the table with its partitions, tiles whole query tokens, fits shared
+    # memory, launches a merge exactly when a sequence can span more
+    # partitions than the decode merges itself, and sizes a workspace the
+    # library accepts
+    rng = np.random.Generator(np.random.PCG64(2024))
+    checked = 0
+    for _ in range(400):
+        D = int(rng.choice([64, 128]))
+        bs = int(rng.choice([16, 32]))
+        dtype = int(rng.choice([0, 1, 2])) if D == 128 else 0
+        Hkv = int(rng.choice([1, 2, 4, 8]))
+        G = int(rng.choice([1, 2, 4, 8, 16]))
+        T = int(rng.choice([1, 2, 4, 8, 16, 33, 64, 128]))
+        B = int(rng.integers(1, 300))
+        MB = int(rng.integers(1, 1200))
+        math = int(rng.choice([0, 1, 2, 3]))
+        ppu = int(rng.choice([0, 0, 1, 5, 64]))
+        d = _desc(num_blocks=50000, block_size=bs, num_kv_heads=Hkv, head_dim=D, dtype=dtype)
+        opts = pkv.decode_opts(partition_blocks=ppu, math=math)
+        st, plan = _plan(lib, d, B, T, G * Hkv, MB, opts)
+        if st != 0:
+            assert st in (1, 2)   # refused shapes: invalid argument or unsupported
+            continue
+        checked += 1
+        assert plan.math in (pkv.MATH_FFMA, pkv.MATH_MMA, pkv.MATH_TC)
+        assert plan.partition_blocks >= 1 and plan.partition_blocks * plan.max_partitions >= MB
+        assert (plan.max_partitions - 1) * plan.partition_blocks < MB
+        tt, nt = plan.query_tokens_per_tile, plan.row_tiles
+        assert 1 <= tt <= T and nt == (T + tt - 1) // tt
+        rows = 128 if plan.math == pkv.MATH_TC else 16
+        assert tt * G <= rows or tt == 1
+        assert plan.smem_bytes_per_cta <= 227 * 1024
+        fused = plan.math != pkv.MATH_TC and plan.max_partitions <= 4
+        assert plan.kernels_per_call == (3 if plan.max_partitions > 1 and not fused else 2)
+        n = lib.pkv_decode_multi_workspace_bytes(ctypes.byref(d), B, T, G * Hkv, MB, ctypes.byref(opts))
+        assert n == plan.workspace_bytes and n > 0
+    assert checked > 150
