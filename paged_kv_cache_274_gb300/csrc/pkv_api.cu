@@ -344,9 +344,9 @@ static pkv_status resolve_decode(const pkv_cache_desc* c, int32_t batch, int32_t
   // tcgen05 tiles: multi-token calls on bf16 caches with head_dim 128
   const bool tc_ok = c->dtype == PKV_KV_BF16 && c->head_dim == 128 && T > 1 && G <= 128;
   // measured on GB300 (Llama-8B layer, G 4): mma.sync tiles are faster up to
-  // 16 rows per KV head (171 us at 4 tokens, one tile), tcgen05 tiles from 32
-  // rows on (kernel 205 vs 234 us at 8 tokens, 208 vs 451 at 16, 733 vs 3402
-  // at 128)
+  // 16 rows per KV head (172 us at 4 tokens, one tile), tcgen05 tiles from 32
+  // rows on (kernel 173 vs 234 us at 8 tokens, 173 vs 451 at 16, 183 vs 865
+  // at 32, 583 vs 3402 at 128)
   if (math == PKV_MATH_AUTO) math = (tc_ok && static_cast<long long>(T) * G > 16) ? PKV_MATH_TC : PKV_MATH_MMA;
   if (math == PKV_MATH_TC && !tc_ok)
     return fail(PKV_ERR_UNSUPPORTED, "tcgen05 tiles need T > 1, a bf16 cache, head_dim 128 and G <= 128");
