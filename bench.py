@@ -34,6 +34,7 @@ import io
 import json
 import math
 import os
+import platform
 import re
 import statistics
 import subprocess
@@ -277,6 +278,48 @@ def kv_bytes_of(c, seqs=None, layers=None):
     return b * n_layers
 
 
+def unique_kv_bytes_of(c, layers=None):
+    """KV bytes one decode call must bring from HBM: each (physical block, KV
+    head) page once, however many sequences' tables alias it, with the rows
+    up to the most that any sequence reads from it (plus its page
+    parameters for one-byte caches).  Equal to kv_bytes_of when no block is
+    shared; smaller for the prefix-sharing batch, whose aliased prefix pages
+    are read by many sequences but stored once ("KV Cache Engineering:
+    PagedAttention, Continuous Batching, Attention Variants, and the
+    Bandwidth Wall", "PagedAttention": block sharing)."""
+    one_byte = c.kv_dtype != "bf16"
+    elem = 1 if one_byte else 2
+    rows = {}
+    for b in range(c.B):
+        n = int(c.context_lens[b])
+        for j in range((n + c.bs - 1) // c.bs):
+            blk = int(c.block_tables[b, j])
+            rows[blk] = max(rows.get(blk, 0), min(c.bs, n - j * c.bs))
+    nbytes = sum(rows.values()) * 2 * c.Hkv * c.D * elem
+    if one_byte:
+        nbytes += len(rows) * 2 * c.Hkv * (4 if c.kv_dtype == "fp8" else 8)
+    n_layers = len(layers) if layers is not None else c.L
+    return nbytes * n_layers
+
+
+def cpu_model():
+    """Host CPU model name (lscpu, else /proc/cpuinfo), for the CPU baseline."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu model")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
+
+
 class DeviceWorkload:
     def __init__(self, name, rank, opts_kw):
         import paged_kv_cache_274_gb300 as pkv
@@ -320,7 +363,8 @@ class DeviceWorkload:
         self.ws = pkv.new_decode_workspace(self.k, c.B, c.Hq, c.MB, self.opts, T)
         self.plan = pkv.decode_plan(self.k, c.B, c.Hq, c.MB, self.opts, T)
         self.layers = list(range(c.L))
-        self.kv_bytes = kv_bytes_of(c)
+        self.kv_bytes_logical = kv_bytes_of(c)
+        self.kv_bytes = unique_kv_bytes_of(c)
         self.launches_per_step = len(self.layers) * self.plan["kernels_per_call"]
         torch.cuda.synchronize()
 
@@ -453,7 +497,7 @@ class CopyWorkload:
         ids = rng.permutation(c.NB)[:8192]
         self.pairs = torch.from_numpy(np.stack([ids[:4096], ids[4096:]], axis=1).astype(np.int32)).to(dev)
         block = c.Hkv * c.bs * c.D * 2 * 2
-        self.kv_bytes = 2 * 4096 * block
+        self.kv_bytes = self.kv_bytes_logical = 2 * 4096 * block
         self.layers = [0]
         self.append = False
         self.plan = {"kernels_per_call": 1, "math": 0, "partition_blocks": 0, "max_partitions": 0,
@@ -763,7 +807,7 @@ def run_reference(args, rank, world):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": config_of(args.workload, c),
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
-                             "sample": desc},
+                             "sample": desc, "cpu_model": cpu_model(), "nproc": os.cpu_count()},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -786,8 +830,10 @@ def run_ours(args, rank, world):
     total_ms, kernel_ms, clocks = time_device(w, args.steps, args.warmup, world, mode=mode)
     assert pkv.read_device_error() == 0, "device error word set during the benchmark"
     value, ms, kv_total = whole_job_gbs(w.kv_bytes, total_ms / args.steps, world)
+    logical_total = sum_over_ranks(float(w.kv_bytes_logical), world)
     peak, peak_kind = hbm_peak()
-    per_call_bytes = w.kv_bytes if copy else kv_bytes_of(c, layers=[0])
+    per_call_bytes = w.kv_bytes if copy else unique_kv_bytes_of(c, layers=[0])
+    per_call_logical = w.kv_bytes_logical if copy else kv_bytes_of(c, layers=[0])
     k_ms = statistics.mean(kernel_ms)
     achieved = per_call_bytes / (k_ms * 1e-3) / 1e9
     probe_gbs, probe_ms = read_probe_gbs()
@@ -805,7 +851,7 @@ def run_ours(args, rank, world):
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not copy:
         gbs, secs, threads, desc = oracle_sample(args.workload, args.cpu_seconds)
         cpu = {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": desc,
-               "seconds": secs}
+               "seconds": secs, "cpu_model": cpu_model(), "nproc": os.cpu_count()}
     # The dominant roof: HBM bytes or tensor-core FLOPs (multi-token calls
     # with many query rows per KV head do ~4 D T G flops per K/V byte pair).
     tpeak, tpeak_kind = tensor_peak()
@@ -838,6 +884,9 @@ def run_ours(args, rank, world):
                 "partition_blocks": plan["partition_blocks"], "max_partitions": plan["max_partitions"],
                 "warps_per_cta": plan["warps_per_cta"], "stages": plan["stages"]}),
             "kv_bytes_per_step": w.kv_bytes,
+            "kv_bytes_accounting": "unique physical pages read (aliased prefix pages counted once)",
+            "kv_bytes_logical_per_step": w.kv_bytes_logical,
+            "logical_gbs": logical_total / (ms * 1e-3) / 1e9,
             "decode_steps_per_s": 1e3 / ms,
             "pct_of_hbm_peak": 100.0 * value / peak,
             "pct_of_nominal_8tbs": 100.0 * value / 8000.0,
@@ -845,6 +894,8 @@ def run_ours(args, rank, world):
                          ("paged_decode_tc_kernel" if plan["math"] == 3 else "paged_decode_kernel"),
                          "traffic": profile_traffic(args.workload, {1: "ffma", 2: "mma", 3: "tc"}.get(plan["math"], "mma")),
                          "algorithmic_bytes_per_launch": per_call_bytes,
+                         "logical_bytes_per_launch": per_call_logical,
+                         "logical_gbs": per_call_logical / (k_ms * 1e-3) / 1e9,
                          "kernel_ms_mean": k_ms, "kernel_ms_median": statistics.median(kernel_ms)},
             "hbm_read_probe": {"gbs": probe_gbs, "ms": probe_ms, "bytes": 1 << 30, "kernel": "read_probe_kernel",
                                "frac_of_copy_peak": probe_gbs / peak,

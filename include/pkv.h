@@ -326,7 +326,11 @@ pkv_status pkv_decode_multi_describe(const pkv_cache_desc* cache, int32_t batch,
  *     opts->partition_blocks means fewer split-K partials.
  *   - The first call on a device looks up that device's copy of the array
  *     (cudaGetSymbolAddress, with the device current); make that first call
- *     before any stream capture on the device.
+ *     before any stream capture on the device.  The address is kept per
+ *     device together with the CUDA context it belongs to; a call made under
+ *     another context (after cudaDeviceReset, or once the primary context was
+ *     released and made again) looks it up anew, so that call too should come
+ *     before any stream capture.
  *   - The call allocates nothing (no cudaMalloc / cudaFree).  Every call on
  *     a device shares the one array and it keeps the previous call's
  *     contents; each call's planner kernel rewrites everything the decode

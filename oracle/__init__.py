@@ -259,6 +259,88 @@ def paged_decode_multi(q_bits, k_cache, v_cache, block_tables, context_lens, kv_
     return out
 
 
+def _cache_values(cache: np.ndarray, params, slot: int, blocks: np.ndarray) -> np.ndarray:
+    """float64 values of the pages of ``blocks`` in cache slot ``slot``:
+    [len(blocks)][Hkv][bs][D].  bf16 bits widen exactly; E4M3 codes take the
+    oracle codec's value times the page's fp32 scale; INT8 codes give
+    (code - zero) * scale with the page's (scale, zero) -- all exact in
+    float64, the same values ``pkv_oracle.c`` reads element by element."""
+    pages = cache[slot, blocks]
+    kind = _kind(cache)
+    if kind == 0:
+        return (pages.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    if kind == 1:
+        table = e4m3_decode(np.arange(256, dtype=np.uint8))
+        sc = np.asarray(params, np.float32)[slot, blocks].astype(np.float64)
+        return table[pages] * sc[:, :, None, None]
+    pr = np.asarray(params, np.float32)[slot, blocks].astype(np.float64)  # [n][Hkv][2]
+    return (pages.astype(np.float64) - pr[:, :, None, None, 1]) * pr[:, :, None, None, 0]
+
+
+def paged_decode_multi_gemm(q_bits, k_cache, v_cache, block_tables, context_lens, kv_group_ptr,
+                            layer: int, scale: float, k_scale=None, v_scale=None) -> np.ndarray:
+    """float64 [B][T][Hq][D]: the definition of ``paged_decode_multi`` with the
+    logits and the weighted sum of values of each (sequence, KV head) taken
+    as float64 matrix products over the gathered logical sequence.
+
+    For sequence b with n = context_lens[b] cached tokens (the last T of them
+    the new ones) and KV head g ("KV Cache Engineering: PagedAttention,
+    Continuous Batching, Attention Variants, and the Bandwidth Wall", "What
+    the KV Cache Stores and Why", "PagedAttention", "Attention Variants"):
+      K, V  = the n rows of KV head g gathered through block_tables[b] from
+              cache slot kv_group_ptr[layer] (dequantised for E4M3 / INT8);
+      Q     = the (query token t, head h) rows with h / G == g, [T*G][D];
+      S     = double(scale) * Q K^T, with row (t, .) keeping only the keys
+              at positions 0 .. n - T + t (causal among the new tokens);
+      P     = exp(S - rowmax S) / rowsum exp(S - rowmax S);
+      out   = P V  (rows with no position to attend to are zero).
+    The matrix products sum in a different order than the element-by-element
+    C oracle, so the two agree to float64 rounding (about 1e-15 relative),
+    not bit for bit.  Raises ValueError for a context length or a table entry
+    outside its range (nothing is read out of bounds)."""
+    q = _c(q_bits, np.uint16)
+    B, T, Hq, D = q.shape
+    S_, NB, Hkv, bs, Dc = k_cache.shape
+    assert Dc == D and Hq % Hkv == 0
+    G = Hq // Hkv
+    bt = np.asarray(block_tables, np.int64)
+    cl = np.asarray(context_lens, np.int64)
+    slot = int(np.asarray(kv_group_ptr)[layer])
+    if not 0 <= slot < S_:
+        raise ValueError("kv_group_ptr entry outside the cache slots")
+    sc = float(np.float32(scale))
+    qf = (q.astype(np.uint32) << 16).view(np.float32).astype(np.float64)  # [B][T][Hq][D]
+    out = np.zeros((B, T, Hq, D), dtype=np.float64)
+    pos_t = np.arange(T)
+    for b in range(B):
+        n = int(cl[b])
+        if n < 0 or n > bt.shape[1] * bs:
+            raise ValueError(f"context_lens[{b}] = {n} out of range")
+        if n == 0:
+            continue
+        blocks = bt[b, :(n + bs - 1) // bs]
+        if np.any((blocks < 0) | (blocks >= NB)):
+            raise ValueError(f"block_tables[{b}] holds an id outside [0, {NB})")
+        # [Hkv][n][D] in logical token order
+        K = _cache_values(k_cache, k_scale, slot, blocks).transpose(1, 0, 2, 3).reshape(Hkv, -1, D)[:, :n]
+        V = _cache_values(v_cache, v_scale, slot, blocks).transpose(1, 0, 2, 3).reshape(Hkv, -1, D)[:, :n]
+        keys = n - T + pos_t + 1                       # keys query token t sees
+        visible = np.arange(n)[None, :] < keys[:, None]  # [T][n]
+        for g in range(Hkv):
+            Q = qf[b, :, g * G:(g + 1) * G, :].reshape(T * G, D)       # rows (t, i)
+            S = sc * (Q @ K[g].T)                                       # [T*G][n]
+            mask = np.repeat(visible, G, axis=0)
+            S = np.where(mask, S, -np.inf)
+            smax = S.max(axis=1, keepdims=True)
+            live = np.isfinite(smax[:, 0])
+            E = np.where(mask, np.exp(S - np.where(live[:, None], smax, 0.0)), 0.0)
+            z = E.sum(axis=1, keepdims=True)
+            O = (E / np.where(z > 0, z, 1.0)) @ V[g]
+            O[~live] = 0.0
+            out[b, :, g * G:(g + 1) * G, :] = O.reshape(T, G, D)
+    return out
+
+
 def copy_blocks(src_k, src_v, dst_k, dst_v, pairs, src_k_scale=None, src_v_scale=None,
                 dst_k_scale=None, dst_v_scale=None, lib=None) -> int:
     """In-place block copy between pools [NB][Hkv][bs][D] (numpy, any dtype),

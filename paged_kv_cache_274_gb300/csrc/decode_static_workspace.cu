@@ -15,11 +15,17 @@ namespace {
 static __device__ __align__(256) unsigned char g_pkv_static_workspace[PKV_STATIC_WORKSPACE_MAX_BYTES];
 
 constexpr int kMaxDevices = 64;
-void* g_static_ws_addr[kMaxDevices];
+struct StaticWorkspace {
+  void* ctx;   // the CUDA context the address belongs to
+  void* addr;  // device address of this device's copy of the array
+};
+StaticWorkspace g_static_ws[kMaxDevices];
 std::mutex g_static_ws_mutex;
 
-// Device address of this device's copy of the array (looked up once, with
-// the device current).
+// Device address of this device's copy of the array, looked up with the
+// device current on first use and again whenever the device's context has
+// changed since (cudaDeviceReset, or a released and re-created primary
+// context, loads the module again, possibly at another address).
 pkv_status static_workspace_address(void** addr) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -32,9 +38,11 @@ pkv_status static_workspace_address(void** addr) {
     return PKV_ERR_UNSUPPORTED;
   }
   std::lock_guard<std::mutex> lock(g_static_ws_mutex);
-  if (g_static_ws_addr[dev] == nullptr) {
+  StaticWorkspace& w = g_static_ws[dev];
+  void* ctx = pkv::current_context();
+  if (w.addr == nullptr || ctx == nullptr || ctx != w.ctx) {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_pkv_static_workspace);
+    e = cudaGetSymbolAddress(&p, g_pkv_static_workspace);  // makes the device's context current
     if (e != cudaSuccess || p == nullptr) {
       char msg[256];
       std::snprintf(msg, sizeof msg, "cudaGetSymbolAddress(static workspace): %s",
@@ -42,9 +50,10 @@ pkv_status static_workspace_address(void** addr) {
       pkv::set_last_error_message(msg);
       return PKV_ERR_CUDA;
     }
-    g_static_ws_addr[dev] = p;
+    w.addr = p;
+    w.ctx = pkv::current_context();
   }
-  *addr = g_static_ws_addr[dev];
+  *addr = w.addr;
   return PKV_OK;
 }
 

@@ -347,6 +347,7 @@ bool pdl_enabled() {
 static cudaError_t ctas_per_sm(const void* fn, int threads, size_t smem, int* out) {
   struct Entry {
     int dev;
+    void* ctx;  // the kernel attribute set below belongs to this context
     const void* fn;
     int threads;
     size_t smem;
@@ -357,10 +358,11 @@ static cudaError_t ctas_per_sm(const void* fn, int threads, size_t smem, int* ou
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  void* ctx = current_context();
   {
     std::lock_guard<std::mutex> lock(mu);
     for (const Entry& x : cache)
-      if (x.dev == dev && x.fn == fn && x.threads == threads && x.smem == smem) {
+      if (x.dev == dev && x.ctx == ctx && ctx != nullptr && x.fn == fn && x.threads == threads && x.smem == smem) {
         *out = x.n;
         return cudaSuccess;
       }
@@ -377,7 +379,7 @@ static cudaError_t ctas_per_sm(const void* fn, int threads, size_t smem, int* ou
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, smem);
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(mu);
-  cache.push_back(Entry{dev, fn, threads, smem, n});
+  cache.push_back(Entry{dev, current_context(), fn, threads, smem, n});
   *out = n;
   return cudaSuccess;
 }

@@ -48,35 +48,37 @@ pkv_status cuda_fail(cudaError_t e, const char* what) {
 constexpr int kMaxDevices = 64;
 
 struct DeviceInfo {
-  std::atomic<int> ready{0};
+  void* ctx = nullptr;  // CUDA context the facts below belong to
   unsigned* err_word = nullptr;
   int num_sms = 0;
 };
 DeviceInfo g_devices[kMaxDevices];
 std::mutex g_dev_mutex;
 
-// Per-device facts, resolved once with that device current.
-pkv_status device_info(DeviceInfo** out) {
+// Per-device facts, resolved with that device current and looked up again
+// whenever the device's context changes (a cudaDeviceReset, or a released and
+// re-created primary context, loads the module again, possibly at another
+// address).
+pkv_status device_info(DeviceInfo* out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   if (dev < 0 || dev >= kMaxDevices) return fail(PKV_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
   DeviceInfo& d = g_devices[dev];
-  if (!d.ready.load(std::memory_order_acquire)) {
-    std::lock_guard<std::mutex> lock(g_dev_mutex);
-    if (!d.ready.load(std::memory_order_relaxed)) {
-      void* p = nullptr;
-      e = cudaGetSymbolAddress(&p, g_pkv_device_error);
-      if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(device error word)");
-      int sms = 0;
-      e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-      if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
-      d.err_word = static_cast<unsigned*>(p);
-      d.num_sms = sms;
-      d.ready.store(1, std::memory_order_release);
-    }
+  void* ctx = pkv::current_context();
+  if (ctx == nullptr || ctx != d.ctx) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_pkv_device_error);  // makes the device's context current
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(device error word)");
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
+    d.err_word = static_cast<unsigned*>(p);
+    d.num_sms = sms;
+    d.ctx = pkv::current_context();
   }
-  *out = &d;
+  *out = d;
   return PKV_OK;
 }
 
@@ -211,6 +213,21 @@ pkv_status fetch(std::vector<T>& dst, const T* src, size_t n, cudaStream_t strea
 
 namespace pkv {
 void set_last_error_message(const char* msg) { t_last_error = msg; }
+
+void* current_context() {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  static GetCurrent fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<GetCurrent>(p);
+  }();
+  CUcontext ctx = nullptr;
+  if (fn == nullptr || fn(&ctx) != CUDA_SUCCESS) return nullptr;
+  return ctx;
+}
 }  // namespace pkv
 
 extern "C" {
@@ -239,7 +256,7 @@ const char* pkv_last_error_message(void) { return t_last_error.c_str(); }
 static pkv_status prepare_append(const pkv_cache_desc* cache, int32_t slot, const void* k, const void* v,
                                  const int64_t* slot_mapping, int32_t num_tokens, void* k_cache,
                                  void* v_cache, const float* k_scale, const float* v_scale,
-                                 cudaStream_t s, DeviceInfo* dev, pkv::AppendArgs* a) {
+                                 cudaStream_t s, const DeviceInfo* dev, pkv::AppendArgs* a) {
   pkv_status st;
   if (slot < 0 || slot >= cache->num_slots)
     return fail(PKV_ERR_INVALID_ARG, "slot %d outside [0, %d)", slot, cache->num_slots);
@@ -311,8 +328,9 @@ pkv_status pkv_kv_append(const pkv_cache_desc* cache, int32_t slot, const void* 
   if ((reinterpret_cast<uintptr_t>(slot_mapping) & 7u) != 0)
     return fail(PKV_ERR_ALIGNMENT, "slot_mapping must be 8-byte aligned");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  DeviceInfo* dev = nullptr;
-  if ((st = device_info(&dev)) != PKV_OK) return st;
+  DeviceInfo dev_info;
+  const DeviceInfo* dev = &dev_info;
+  if ((st = device_info(&dev_info)) != PKV_OK) return st;
   pkv::AppendArgs a{};
   if ((st = prepare_append(cache, slot, k, v, slot_mapping, num_tokens, k_cache, v_cache, k_scale, v_scale, s,
                            dev, &a)) != PKV_OK)
@@ -569,8 +587,9 @@ static pkv_status decode_call(const pkv_cache_desc* cache, const void* q, int32_
     return fail(PKV_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu", wl.total, workspace_bytes);
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  DeviceInfo* dev = nullptr;
-  if ((st = device_info(&dev)) != PKV_OK) return st;
+  DeviceInfo dev_info;
+  const DeviceInfo* dev = &dev_info;
+  if ((st = device_info(&dev_info)) != PKV_OK) return st;
   L.num_sms = dev->num_sms;
 
   if (env_flag("PKV_VALIDATE")) {
@@ -704,8 +723,9 @@ pkv_status pkv_copy_blocks(const pkv_cache_desc* cache, const void* src_k, const
   if ((reinterpret_cast<uintptr_t>(block_pairs) & 3u) != 0)
     return fail(PKV_ERR_ALIGNMENT, "block_pairs must be 4-byte aligned");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  DeviceInfo* dev = nullptr;
-  if ((st = device_info(&dev)) != PKV_OK) return st;
+  DeviceInfo dev_info;
+  const DeviceInfo* dev = &dev_info;
+  if ((st = device_info(&dev_info)) != PKV_OK) return st;
   if (env_flag("PKV_VALIDATE")) {
     std::vector<int32_t> pr;
     if ((st = fetch(pr, block_pairs, static_cast<size_t>(count) * 2, s)) != PKV_OK) return st;
@@ -737,8 +757,9 @@ pkv_status pkv_read_probe(const void* data, size_t bytes, uint64_t* sum, void* s
   if (bytes % 16 != 0) return fail(PKV_ERR_INVALID_ARG, "bytes %zu is not a multiple of 16", bytes);
   if (reinterpret_cast<uintptr_t>(data) % 16 != 0 || reinterpret_cast<uintptr_t>(sum) % 8 != 0)
     return fail(PKV_ERR_ALIGNMENT, "data must be 16-byte and sum 8-byte aligned");
-  DeviceInfo* dev = nullptr;
-  pkv_status st = device_info(&dev);
+  DeviceInfo dev_info;
+  const DeviceInfo* dev = &dev_info;
+  pkv_status st = device_info(&dev_info);
   if (st != PKV_OK) return st;
   cudaError_t e = pkv::launch_read_probe(data, bytes, reinterpret_cast<unsigned long long*>(sum), dev->num_sms,
                                          static_cast<cudaStream_t>(stream));
@@ -748,8 +769,9 @@ pkv_status pkv_read_probe(const void* data, size_t bytes, uint64_t* sum, void* s
 
 pkv_status pkv_read_device_error(uint32_t* flags, void* stream) {
   if (flags == nullptr) return fail(PKV_ERR_INVALID_ARG, "flags is NULL");
-  DeviceInfo* dev = nullptr;
-  pkv_status st = device_info(&dev);
+  DeviceInfo dev_info;
+  const DeviceInfo* dev = &dev_info;
+  pkv_status st = device_info(&dev_info);
   if (st != PKV_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   unsigned host = 0;

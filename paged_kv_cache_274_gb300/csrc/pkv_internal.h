@@ -91,6 +91,12 @@ int decode_ctas_per_sm(const DecodeLaunch& L, size_t smem);
 // Replace the calling thread's pkv_last_error_message() text.
 void set_last_error_message(const char* msg);
 
+// The calling thread's current CUDA context (a CUcontext), or NULL when none
+// is current.  Device addresses of the library's __device__ variables and
+// kernel attributes belong to one context; a cache of them is valid only
+// while the context it was filled in stays current.
+void* current_context();
+
 // KV append.
 cudaError_t launch_kv_append(int kv_dtype, const AppendArgs& a, cudaStream_t stream);
 

@@ -1,8 +1,10 @@
 """The five workloads and the verify steps at full size, in the launch
 configuration the benchmark times (default options), compared with the
-oracle on sampled (sequence, head) or (sequence, token, head) outputs that it
-computes one by one; plus the invariants that hold at any size (aliased
-prefix == private copies, bitwise)."""
+oracle on every output element (|gpu - oracle| <= 1e-2 + 1e-2 |oracle|);
+plus the invariants that hold at any size (aliased prefix == private copies,
+bitwise).  Single-token calls use the element-by-element C oracle; the
+multi-token verify steps use its matrix-product form, which states the same
+definition and is pinned to it and to torch's SDPA on the CPU."""
 import gc
 
 import numpy as np
@@ -14,7 +16,7 @@ import paged_kv_cache_274_gb300 as pkv
 from workloads import (fp8_shared_case, llama8b_layer_case, long_context_case, mixed_prefix_case,
                        normal_bf16_bits, tiny_case)
 from workloads.gen import unalias_prefix
-from tests._gpu import DeviceCase, assert_close, bf16_dev_to_f64, sample_pairs, to_dev, to_dev_bf16
+from tests._gpu import DeviceCase, assert_close, bf16_dev_to_f64, to_dev, to_dev_bf16
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -26,12 +28,13 @@ def _free():
     torch.cuda.empty_cache()
 
 
-def _check_sampled(dc, out, layer, n, seed, what):
-    pairs = sample_pairs(dc.c, n, seed)
-    want = dc.oracle(layer=layer, pairs=pairs)
-    got = bf16_dev_to_f64(out)
-    b, h = pairs[:, 0], pairs[:, 1]
-    assert_close(got[b, h], want[b, h], what)
+def _check_full(dc, out, layer, what, want=None):
+    """Every (sequence, head, column) of `out` against the oracle; returns
+    the oracle's output so that another back-end can be checked against it."""
+    if want is None:
+        want = dc.oracle(layer=layer)
+    assert_close(bf16_dev_to_f64(out), want, what)
+    return want
 
 
 def test_tiny_full():
@@ -56,9 +59,9 @@ def test_llama8b_layer_step():
         blk, off = divmod(s, c.bs)
         row = dc.k[0, blk, :, off].view(torch.int16).cpu().numpy().view(np.uint16)
         assert np.array_equal(row, c.k_new[b])
-    _check_sampled(dc, out, 0, 48, 2, "llama8b layer")
+    want = _check_full(dc, out, 0, "llama8b layer")
     out_ffma = dc.decode(opts=pkv.decode_opts(math=pkv.MATH_FFMA))
-    _check_sampled(dc, out_ffma, 0, 16, 3, "llama8b layer (ffma)")
+    _check_full(dc, out_ffma, 0, "llama8b layer (ffma)", want)
 
 
 @pytest.mark.parametrize("T", [4, 8, 32, 128])
@@ -66,8 +69,8 @@ def test_spec_verify_full(T):
     # the verify step the benchmark times: T draft tokens per sequence appended
     # at the end of its context (4096 after the append), then one T-token
     # decode with default options (mma.sync tiles for 16 rows per KV head,
-    # the tcgen05 kernel with long units above), sampled (sequence, token,
-    # head) rows against the oracle
+    # the tcgen05 kernel with long units above), every output element
+    # against the oracle
     c = llama8b_layer_case()
     dc = DeviceCase(c)
     pos = c.context_lens.astype(np.int64)[:, None] - T + np.arange(T)[None, :]
@@ -83,14 +86,9 @@ def test_spec_verify_full(T):
     torch.cuda.synchronize()
     assert pkv.read_device_error() == 0
     assert oracle.kv_append(kn, vn, slots, dc.k_host, dc.v_host) == 0
-    rng = np.random.Generator(np.random.PCG64(304 + T))
-    rows = np.stack([rng.integers(0, c.B, 24), rng.integers(0, T, 24), rng.integers(0, c.Hq, 24)], axis=1)
-    rows[0], rows[-1] = (0, 0, 0), (c.B - 1, T - 1, c.Hq - 1)
-    want = oracle.paged_decode_multi(q, dc.k_host, dc.v_host, c.block_tables, c.context_lens, c.kv_group_ptr,
-                                     0, c.scale, rows=rows)
-    got = bf16_dev_to_f64(out)
-    b, t, h = rows[:, 0], rows[:, 1], rows[:, 2]
-    assert_close(got[b, t, h], want[b, t, h], f"verify T={T} ({plan['partition_blocks']}-block partitions)")
+    want = oracle.paged_decode_multi_gemm(q, dc.k_host, dc.v_host, c.block_tables, c.context_lens,
+                                          c.kv_group_ptr, 0, c.scale)
+    assert_close(bf16_dev_to_f64(out), want, f"verify T={T} ({plan['partition_blocks']}-block partitions)")
 
 
 def test_mixed_prefix_batch():
@@ -99,17 +97,7 @@ def test_mixed_prefix_batch():
     out = dc.decode()
     torch.cuda.synchronize()
     assert pkv.read_device_error() == 0
-    # sample shared and private, short and long sequences
-    shared = np.flatnonzero(c.notes["shared"])
-    private = np.flatnonzero(~c.notes["shared"])
-    order = np.argsort(c.context_lens)
-    seqs = sorted(set([int(shared[0]), int(shared[-1]), int(private[0]), int(private[-1]),
-                       int(order[0]), int(order[-1]), int(order[len(order) // 2])]))
-    pairs = np.array([(b, h) for b in seqs for h in (0, 13, 31)], dtype=np.int32)
-    want = dc.oracle(pairs=pairs)
-    got = bf16_dev_to_f64(out)
-    assert_close(got[pairs[:, 0], pairs[:, 1]], want[pairs[:, 0], pairs[:, 1]], "mixed prefix")
-    _check_sampled(dc, out, 0, 32, 4, "mixed prefix (random sample)")
+    _check_full(dc, out, 0, "mixed prefix")
     # aliasing the prefix blocks or giving every sharer private copies: same bits
     cp = unalias_prefix(c)
     del dc
@@ -127,7 +115,7 @@ def test_long_context(variant):
     out = dc.decode()
     torch.cuda.synchronize()
     assert pkv.read_device_error() == 0
-    _check_sampled(dc, out, 0, 16, 5, f"long {variant}")
+    _check_full(dc, out, 0, f"long {variant}")
 
 
 def test_fp8_shared_four_layers():
@@ -138,7 +126,7 @@ def test_fp8_shared_four_layers():
         out = dc.decode(layer=layer)
         torch.cuda.synchronize()
         assert pkv.read_device_error() == 0
-        _check_sampled(dc, out, layer, 12, 10 + layer, f"fp8 layer {layer}")
+        _check_full(dc, out, layer, f"fp8 layer {layer}")
 
 
 def test_int8_shared_two_layers():
@@ -149,4 +137,4 @@ def test_int8_shared_two_layers():
         out = dc.decode(layer=layer)
         torch.cuda.synchronize()
         assert pkv.read_device_error() == 0
-        _check_sampled(dc, out, layer, 12, 20 + layer, f"int8 layer {layer}")
+        _check_full(dc, out, layer, f"int8 layer {layer}")

@@ -206,12 +206,19 @@ def test_tc_large_logits_and_auto_choice(value_scale):
                                  opts=pkv.decode_opts(math=pkv.MATH_MMA))
     torch.cuda.synchronize()
     want = _oracle(dc, q)
-    # Both back-ends round the attention weights P to bf16 (unit roundoff
-    # 2^-8) before P . V, so the numerator's error is up to 2^-8 sum_k w_k |V_k|
-    # <= 2^-8 max|V|, which the unit-scale ATOL does not cover once the values
-    # are scaled up (outputs near 0 by cancellation have no relative slack).
-    v = bf16_dev_to_f64(dc.v)
-    atol = ATOL + 2.0 ** -8 * float(np.abs(v).max())
+    # N(0,1) values (the workloads' distribution) are held to the unit bound
+    # 1e-2 + 1e-2 |oracle|.  With K and V scaled by 4 the bound takes an
+    # absolute term derived from the arithmetic: both back-ends round the
+    # attention weights P to bf16 (unit roundoff 2^-8) before P . V, so the
+    # numerator's error is up to 2^-8 sum_k w_k |V_k| <= 2^-8 max|V|, which
+    # outputs near 0 by cancellation cannot absorb in their relative term.
+    # A float64 emulation of the tcgen05 kernel's steps (64-token steps, lazy
+    # running maximum, bf16 P, fp32 sums) reproduces the elements that exceed
+    # the unit bound at that scale, with the same maximum error.
+    atol = ATOL
+    if value_scale != 1.0:
+        v = bf16_dev_to_f64(dc.v)
+        atol = ATOL + 2.0 ** -8 * float(np.abs(v).max())
     assert_close(bf16_dev_to_f64(tc), want, "tc", atol=atol)
     assert_close(bf16_dev_to_f64(mma), want, "mma", atol=atol)
 
