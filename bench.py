@@ -54,12 +54,15 @@ FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0
 WORKLOADS = ("llama8b_layer", "long_b4_32k", "long_b1_128k", "mixed_prefix", "fp8_shared",
              "int8_shared", "spec_verify_t4", "spec_verify_t8", "spec_verify_t16", "spec_verify_t32",
-             "spec_verify_t64", "spec_verify_t128", "tiny", "copy_blocks")
+             "spec_verify_t64", "spec_verify_t128", "prefill_t256", "prefill_t512", "tiny", "copy_blocks")
 
 
 def query_tokens_of(name):
     """Query tokens per sequence of a workload (1: single-token decode)."""
-    return int(name[len("spec_verify_t"):]) if name.startswith("spec_verify_t") else 1
+    for prefix in ("spec_verify_t", "prefill_t"):
+        if name.startswith(prefix):
+            return int(name[len(prefix):])
+    return 1
 
 
 def parse_args():
@@ -249,7 +252,7 @@ def profile_traffic(workload, math="mma"):
 def structure(name):
     """Block tables, lengths, queries, append slots (no cache contents)."""
     from workloads import gen
-    if name == "llama8b_layer" or name.startswith("spec_verify_t"):
+    if name == "llama8b_layer" or query_tokens_of(name) > 1:
         return gen.llama8b_layer_case(fill=False)
     if name.startswith("long_"):
         return gen.long_context_case(name[len("long_"):], fill=False)

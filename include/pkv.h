@@ -103,7 +103,8 @@ typedef enum {
                         caches); G <= 16 */
   PKV_MATH_TC = 3    /* tcgen05 tiles of 128 (query token, head) rows with TMEM
                         accumulators; multi-token calls (T > 1), bf16 cache,
-                        head_dim 128, G <= 128 */
+                        head_dim 128, G <= 128; with more than one tile per
+                        KV head, pairs of tiles share each page read */
 } pkv_decode_math;
 
 /* Tuning knobs of pkv_paged_decode; a NULL pointer or zero fields = auto. */
@@ -230,7 +231,7 @@ pkv_status pkv_paged_decode(const pkv_cache_desc* cache,
                             const pkv_decode_opts* opts, void* stream);
 
 /* Largest number of query tokens per sequence of pkv_paged_decode_multi. */
-#define PKV_MAX_QUERY_TOKENS 128
+#define PKV_MAX_QUERY_TOKENS 512
 
 /*
  * Decode with T >= 1 new query tokens per sequence (T = 1 is
@@ -250,10 +251,13 @@ pkv_status pkv_paged_decode(const pkv_cache_desc* cache,
  *   q, out         device bf16 [B][T][Hq][D] (must not overlap).
  *   workspace      pkv_decode_multi_workspace_bytes() bytes.
  *   everything else as in pkv_paged_decode.
- * The tensor-core back-end only (PKV_MATH_FFMA with T > 1 gives
+ * The tensor-core back-ends only (PKV_MATH_FFMA with T > 1 gives
  * PKV_ERR_UNSUPPORTED).  The (query token, head) rows of one KV head form
- * row tiles of at most 16 rows (whole query tokens per tile); each tile is
- * a separate stream over the pages, so G * T <= 16 reads the cache once.
+ * row tiles of whole query tokens: at most 16 rows for PKV_MATH_MMA, each
+ * tile a separate stream over the pages (G * T <= 16 reads the cache once);
+ * 128 rows for PKV_MATH_TC, where a KV head with two or more tiles is served
+ * by CTAs that each hold a pair of its tiles and read every page once for
+ * both.
  */
 pkv_status pkv_paged_decode_multi(const pkv_cache_desc* cache,
                                   const void* q, int32_t batch, int32_t num_query_tokens,

@@ -60,7 +60,7 @@ class DecodePlan(ctypes.Structure):
                 ("workspace_bytes", ctypes.c_size_t), ("smem_bytes_per_cta", ctypes.c_size_t),
                 ("query_tokens_per_tile", ctypes.c_int32), ("row_tiles", ctypes.c_int32)]
 
-MAX_QUERY_TOKENS = 128
+MAX_QUERY_TOKENS = 512
 ABI_VERSION = 2
 
 

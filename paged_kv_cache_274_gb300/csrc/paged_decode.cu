@@ -19,11 +19,13 @@
 #include "kv_append.cuh"
 #include "paged_decode.cuh"
 #include "paged_decode_tc.cuh"
+#include "paged_decode_tc2.cuh"
 #include "pkv_internal.h"
 
 namespace pkv {
 
 static_assert(kTcMaxPages == kTcUnitMaxPages, "the tcgen05 unit's page table");
+static_assert(kT2Threads == 32 * kTcPairWarps, "the tile-pair kernel's warps");
 
 // Kernel tables of the instantiation units.
 const void* decode_kernel_bf16_d64(int bs, int math, int gt);
@@ -33,6 +35,7 @@ const void* decode_kernel_int8_d128(int bs, int math, int gt);
 const void* decode_kernel_mt_bf16(int D, int bs, int gt);
 const void* decode_kernel_mt_1byte(int kv_dtype, int bs, int gt);
 const void* decode_kernel_tc(int bs, bool rot);
+const void* decode_kernel_tc2(int bs);
 
 // ---------------------------------------------------------------------------
 // planner: one CTA validates context lengths, counts each sequence's
@@ -307,7 +310,8 @@ WorkspaceLayout workspace_layout(int B, int T, int Hq, int Hkv, int NT, int D, i
   return w;
 }
 
-size_t decode_smem_bytes(int kv_fp8, int D, int bs, int warps, int stages, int tc) {
+size_t decode_smem_bytes(int kv_fp8, int D, int bs, int warps, int stages, int tc, int tc2) {
+  if (tc2) return tc2_smem_layout_bytes();
   if (tc) return tc_smem_layout_bytes();
   if (kv_fp8) {
     return bs == 16 ? decode_smem_layout_bytes<128, 16, true>(warps, stages)
@@ -320,8 +324,10 @@ size_t decode_smem_bytes(int kv_fp8, int D, int bs, int warps, int stages, int t
                   : decode_smem_layout_bytes<128, 32, false>(warps, stages);
 }
 
-// gt: query rows per tile; mt: multi-token kernel (T > 1).
-static const void* pick_kernel(int kv_dtype, int D, int bs, int math, int gt, bool mt) {
+// gt: query rows per tile; mt: multi-token kernel (T > 1); tc2: the
+// tcgen05 kernel for pairs of row tiles.
+static const void* pick_kernel(int kv_dtype, int D, int bs, int math, int gt, bool mt, bool tc2 = false) {
+  if (math == PKV_MATH_TC && tc2) return (kv_dtype == PKV_KV_BF16 && D == 128) ? decode_kernel_tc2(bs) : nullptr;
   if (math == PKV_MATH_TC)
     return (kv_dtype == PKV_KV_BF16 && D == 128) ? decode_kernel_tc(bs, gt <= kTcRotMaxRows) : nullptr;
   if (mt) {
@@ -385,7 +391,7 @@ static cudaError_t ctas_per_sm(const void* fn, int threads, size_t smem, int* ou
 }
 
 int decode_ctas_per_sm(const DecodeLaunch& L, size_t smem) {
-  const void* fn = pick_kernel(L.kv_dtype, L.D, L.bs, L.math, L.G * L.Tt, L.T > 1);
+  const void* fn = pick_kernel(L.kv_dtype, L.D, L.bs, L.math, L.G * L.Tt, L.T > 1, L.tc2 != 0);
   int n = 0;
   if (fn == nullptr || ctas_per_sm(fn, L.warps * 32, smem, &n) != cudaSuccess) return 0;
   return n;
@@ -393,9 +399,9 @@ int decode_ctas_per_sm(const DecodeLaunch& L, size_t smem) {
 
 cudaError_t launch_decode(const DecodeLaunch& L, int* launched) {
   *launched = 0;
-  const void* fn = pick_kernel(L.kv_dtype, L.D, L.bs, L.math, L.G * L.Tt, L.T > 1);
+  const void* fn = pick_kernel(L.kv_dtype, L.D, L.bs, L.math, L.G * L.Tt, L.T > 1, L.tc2 != 0);
   if (fn == nullptr) return cudaErrorInvalidDeviceFunction;
-  const size_t smem = decode_smem_bytes(L.kv_fp8, L.D, L.bs, L.warps, L.stages, L.tc);
+  const size_t smem = decode_smem_bytes(L.kv_fp8, L.D, L.bs, L.warps, L.stages, L.tc, L.tc2);
   int per_sm = 0;
   cudaError_t e = ctas_per_sm(fn, L.warps * 32, smem, &per_sm);
   if (e != cudaSuccess) return e;
@@ -433,10 +439,13 @@ cudaError_t launch_decode(const DecodeLaunch& L, int* launched) {
   }
 
   // 2. decode: persistent grid, at most one warp per possible unit
-  const long long max_units = static_cast<long long>(L.B) * L.Hkv * L.NT * L.pmax;
+  // (the tile-pair kernel: one unit per pair of row tiles)
+  const long long max_units =
+      static_cast<long long>(L.B) * L.Hkv * (L.tc2 ? (L.NT + 1) / 2 : L.NT) * L.pmax;
   // The tcgen05 kernel holds 256 of an SM's 512 TMEM columns: two CTAs per SM
-  // (the occupancy query does not see the tensor memory and may say one).
-  if (L.tc) per_sm = 2;
+  // (the occupancy query does not see the tensor memory and may say one);
+  // the tile-pair kernel holds all 512: one CTA per SM.
+  if (L.tc) per_sm = L.tc2 ? 1 : 2;
   long long grid = static_cast<long long>(L.num_sms) * per_sm;
   // a warp of the mma.sync kernels, a CTA of the tcgen05 kernel, per unit
   grid = std::min(grid, L.tc ? max_units : (max_units + L.warps - 1) / L.warps);
@@ -472,10 +481,11 @@ cudaError_t launch_decode(const DecodeLaunch& L, int* launched) {
   p.fused_merge = (!L.tc && L.pmax <= kFusedMergeMaxParts) ? 1 : 0;
   p.row_base = L.row_base;
   p.scale_log2 = L.scale_log2;
-  CUtensorMap kmap = L.kmap, vmap = L.vmap, pmap = L.pmap, omap = L.omap;
+  CUtensorMap kmap = L.kmap, vmap = L.vmap, pmap = L.pmap, omap = L.omap, qmap = L.qmap;
   void* args_mma[] = {&kmap, &vmap, &p};
   void* args_tc[] = {&kmap, &vmap, &pmap, &omap, &p};  // + the partial and output store maps
-  void** args = L.tc ? args_tc : args_mma;
+  void* args_tc2[] = {&kmap, &vmap, &qmap, &p};        // + the query load map
+  void** args = L.tc2 ? args_tc2 : L.tc ? args_tc : args_mma;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(L.warps * 32);

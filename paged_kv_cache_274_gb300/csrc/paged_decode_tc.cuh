@@ -597,6 +597,24 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       auto write_p = [&](const uint32_t (&sc)[32], uint32_t hm, bool all32, uint8_t* pbuf, int half) -> float {
         const float neg_m = (m == -INFINITY) ? 0.f : -m;
         float psum = 0.f;
+        // the common all-valid case without per-element mask tests (kept out
+        // of the unrolled loop: they cost ALU issue slots on every score)
+        if (all32) {
+#pragma unroll
+          for (int k8 = 0; k8 < 4; ++k8) {
+            uint32_t pw[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int kk = 8 * k8 + 2 * e;
+              const float p0 = ex2_approx(fmaf(__uint_as_float(sc[kk]), c, neg_m));
+              const float p1 = ex2_approx(fmaf(__uint_as_float(sc[kk + 1]), c, neg_m));
+              psum += p0 + p1;
+              pw[e] = pack_bf16x2(p0, p1);
+            }
+            *reinterpret_cast<uint4*>(pbuf + tc_p_off(tid, 4 * half + k8)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+          }
+          return psum;
+        }
 #pragma unroll
         for (int k8 = 0; k8 < 4; ++k8) {
           uint32_t pw[4];
@@ -605,10 +623,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             const int kk = 8 * k8 + 2 * e;
             float p0 = ex2_approx(fmaf(__uint_as_float(sc[kk]), c, neg_m));
             float p1 = ex2_approx(fmaf(__uint_as_float(sc[kk + 1]), c, neg_m));
-            if (!all32) {
-              p0 = ((hm >> kk) & 1u) ? p0 : 0.f;
-              p1 = ((hm >> (kk + 1)) & 1u) ? p1 : 0.f;
-            }
+            p0 = ((hm >> kk) & 1u) ? p0 : 0.f;
+            p1 = ((hm >> (kk + 1)) & 1u) ? p1 : 0.f;
             psum += p0 + p1;
             pw[e] = pack_bf16x2(p0, p1);
           }

@@ -198,6 +198,27 @@ pkv_status encode_output_map(CUtensorMap* map, void* out, int B, int T, int Hq, 
   return PKV_OK;
 }
 
+// Load map of the queries q [B][T][Hq][D] bf16 for the tile-pair tcgen05
+// kernel: a box of 64 columns x the G heads of a KV head x the Tt query
+// tokens of a row tile (128-byte rows, 128-byte swizzle, the K-major layout
+// of the MMA's A operand); tokens past T read as zeros.
+pkv_status encode_query_map(CUtensorMap* map, const void* q, int B, int T, int Hq, int D, int G, int Tt) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+  pkv_status st = tensor_map_encoder(&enc);
+  if (st != PKV_OK) return st;
+  const cuuint64_t row = static_cast<cuuint64_t>(D) * 2;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hq), static_cast<cuuint64_t>(T),
+                        static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {row, row * Hq, row * Hq * T};
+  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(Tt), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(q), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled (queries) failed (%d)", static_cast<int>(r));
+  return PKV_OK;
+}
+
 // Host copies of device tables for PKV_VALIDATE.
 template <typename T>
 pkv_status fetch(std::vector<T>& dst, const T* src, size_t n, cudaStream_t stream) {
@@ -388,14 +409,19 @@ static pkv_status resolve_decode(const pkv_cache_desc* c, int32_t batch, int32_t
   // Defaults measured on GB300: 4 warps per CTA with shallow (2-stage)
   // rings give several CTAs, i.e. 8+ streaming warps, per SM; deeper rings
   // only cost occupancy.
-  // (the tcgen05 kernel has a fixed shape: 4 compute warps, an MMA warp and
-  // two copy warps, a 4-stage K ring and a 2-stage V ring of 64 tokens)
-  int warps = tc ? 7 : (o.warps_per_cta != 0 ? o.warps_per_cta : env_int("PKV_DECODE_WARPS", 4));
-  int stages = tc ? 4 : (o.stages != 0 ? o.stages : env_int("PKV_DECODE_STAGES", 0));
+  // (the tcgen05 kernels have fixed shapes: one 128-row tile per CTA with 4
+  // compute warps, an MMA warp and two copy warps, a 4-stage K ring and a
+  // 2-stage V ring of 64 tokens; or, with two or more row tiles per KV head,
+  // a pair of tiles per CTA with 8 softmax warps, an MMA warp and two copy
+  // warps, 2-stage K and V rings of 128 tokens -- PKV_TC_PAIR=0 keeps the
+  // one-tile kernel there)
+  const bool tc2 = tc && NT >= 2 && env_int("PKV_TC_PAIR", 1) != 0;
+  int warps = tc2 ? pkv::kTcPairWarps : tc ? 7 : (o.warps_per_cta != 0 ? o.warps_per_cta : env_int("PKV_DECODE_WARPS", 4));
+  int stages = tc2 ? 2 : tc ? 4 : (o.stages != 0 ? o.stages : env_int("PKV_DECODE_STAGES", 0));
   if (stages == 0) stages = stage_bytes >= (8u << 10) ? 2 : 3;
-  if (warps < 1 || warps > 8) return fail(PKV_ERR_INVALID_ARG, "warps_per_cta %d outside 1..8", warps);
+  if (!tc && (warps < 1 || warps > 8)) return fail(PKV_ERR_INVALID_ARG, "warps_per_cta %d outside 1..8", warps);
   if (stages < 2 || stages > 8) return fail(PKV_ERR_INVALID_ARG, "stages %d outside 2..8", stages);
-  const size_t smem = pkv::decode_smem_bytes(fp8, c->head_dim, c->block_size, warps, stages, tc);
+  const size_t smem = pkv::decode_smem_bytes(fp8, c->head_dim, c->block_size, warps, stages, tc, tc2);
   if (smem > 227u * 1024u)
     return fail(PKV_ERR_INVALID_ARG, "warps x stages need %zu bytes of shared memory", smem);
   int ppu = o.partition_blocks != 0 ? o.partition_blocks : env_int("PKV_DECODE_PARTITION_BLOCKS", 0);
@@ -414,9 +440,13 @@ static pkv_status resolve_decode(const pkv_cache_desc* c, int32_t batch, int32_t
     const long long ctas_regs = std::max<long long>(1, 65536LL / (warps * 32LL * 200));
     // streams: warps of the mma.sync kernels; CTAs of the tcgen05 kernel
     // (two per SM: their accumulators fill the SM's tensor memory)
-    const long long W = tc ? 2LL * num_sms : static_cast<long long>(num_sms) * std::min(ctas_smem, ctas_regs) * warps;
+    const long long W = tc2 ? static_cast<long long>(num_sms)
+                        : tc ? 2LL * num_sms
+                             : static_cast<long long>(num_sms) * std::min(ctas_smem, ctas_regs) * warps;
+    const int tiles_per_unit = tc2 ? 2 : 1;
     auto units = [&](int pp) {
-      return static_cast<long long>(std::max(batch, 1)) * c->num_kv_heads * NT * ((MB + pp - 1) / pp);
+      return static_cast<long long>(std::max(batch, 1)) * c->num_kv_heads * ((NT + tiles_per_unit - 1) / tiles_per_unit) *
+             ((MB + pp - 1) / pp);
     };
     // Multi-token units carry T times the partials and load up to 16 query
     // rows each, so they stay at 32 or 64 blocks (measured on the 4- and
@@ -432,7 +462,9 @@ static pkv_status resolve_decode(const pkv_cache_desc* c, int32_t batch, int32_t
       // each way, at about 4 MB per modelled step (measured on GB300: the
       // 64-token verify step with 128-block units ran 393 us against 345
       // with whole-sequence units, whose kernel alone is 18 us slower).
-      const double partial_bytes = static_cast<double>(G) * Tt * (c->head_dim + 2) * 4.0;
+      // The tile-pair kernel: steps of 128 tokens for two tiles, i.e. about
+      // two 64-token steps of the one-tile kernel, and units twice as wide.
+      const double partial_bytes = static_cast<double>(G) * Tt * (c->head_dim + 2) * 4.0 * tiles_per_unit;
       double best = 0.0;
       for (int pp : {64, 128, 256}) {
         const long long rounds = (units(pp) + W - 1) / W;
@@ -446,7 +478,14 @@ static pkv_status resolve_decode(const pkv_cache_desc* c, int32_t batch, int32_t
         if (pp >= MB) break;  // one partition per sequence already
       }
     } else if (units(64) <= W) {
-      ppu = 64;
+      // one round holds every unit: cut the sequences so that each SM gets
+      // the same number of units, one per warp of a CTA per SM (measured on
+      // GB300: 64-block units of the 70B-shaped 32K x 4 and 128K x 1 contexts
+      // filled 128 CTAs of 4 warps on 152 SMs), in partitions of 16 to 64
+      // blocks
+      const long long seq_units = static_cast<long long>(std::max(batch, 1)) * c->num_kv_heads * NT;
+      const long long parts = std::max<long long>((MB + 63) / 64, (static_cast<long long>(num_sms) * warps) / seq_units);
+      ppu = static_cast<int>(std::min<long long>(64, std::max<long long>(16, (MB + parts - 1) / parts)));
     } else {
       double best = -1.0;
       for (int pp : sizes) {
@@ -471,6 +510,7 @@ static pkv_status resolve_decode(const pkv_cache_desc* c, int32_t batch, int32_t
   L->Tt = Tt;
   L->NT = NT;
   L->tc = tc ? 1 : 0;
+  L->tc2 = tc2 ? 1 : 0;
   L->MB = MB;
   L->NB = c->num_blocks;
   L->bs = c->block_size;
@@ -524,7 +564,7 @@ pkv_status pkv_decode_multi_describe(const pkv_cache_desc* cache, int32_t batch,
   // the merge kernel runs above 4 partitions (tcgen05 kernel: above 1)
   plan->kernels_per_call = L.pmax > (L.tc ? 1 : 4) ? 3 : 2;
   plan->workspace_bytes = layout_of(L).total;
-  plan->smem_bytes_per_cta = pkv::decode_smem_bytes(L.kv_fp8, L.D, L.bs, L.warps, L.stages, L.tc);
+  plan->smem_bytes_per_cta = pkv::decode_smem_bytes(L.kv_fp8, L.D, L.bs, L.warps, L.stages, L.tc, L.tc2);
   plan->query_tokens_per_tile = L.Tt;
   plan->row_tiles = L.NT;
   return PKV_OK;
@@ -626,10 +666,12 @@ static pkv_status decode_call(const pkv_cache_desc* cache, const void* q, int32_
   L.arrive = reinterpret_cast<int32_t*>(ws + wl.arrive);
   L.part_ml = reinterpret_cast<float*>(ws + wl.part_ml);
   L.part_o = reinterpret_cast<float*>(ws + wl.part_o);
-  if (L.tc && L.pmax > 1 &&
+  if (L.tc && !L.tc2 && L.pmax > 1 &&
       (st = encode_partial_map(&L.pmap, L.part_o, batch, L.T, L.Hq, L.pmax, L.D, L.G, L.Tt)) != PKV_OK)
     return st;
-  if (L.tc && (st = encode_output_map(&L.omap, out, batch, L.T, L.Hq, L.D, L.G, L.Tt)) != PKV_OK) return st;
+  if (L.tc && !L.tc2 && (st = encode_output_map(&L.omap, out, batch, L.T, L.Hq, L.D, L.G, L.Tt)) != PKV_OK)
+    return st;
+  if (L.tc2 && (st = encode_query_map(&L.qmap, q, batch, L.T, L.Hq, L.D, L.G, L.Tt)) != PKV_OK) return st;
   L.err = dev->err_word;
   L.row_base = static_cast<int>(static_cast<long long>(slot) * cache->num_blocks * cache->num_kv_heads *
                                 cache->block_size);

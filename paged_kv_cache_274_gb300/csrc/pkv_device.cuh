@@ -96,6 +96,44 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
+// try_wait with a suspend-time hint: a thread whose phase is not complete
+// sleeps until it completes (or the hint runs out) instead of returning at
+// once, so a waiting warp issues almost no instructions.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n"
+      " .reg .pred p;\n"
+      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// mbar_wait_bounded with suspending waits of up to 0.1 ms each: for waits
+// whose warps share a sub-partition with warps that compute.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait_hint(bar, parity, 100000u)) return true;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// Bounded wait for threads on the critical path of a pipeline (the tcgen05
+// issuing thread): the phase is first tested without suspending -- a
+// try_wait on a completed phase still costs on the order of a hundred
+// cycles -- then waited for with suspending try_waits.
+__device__ __forceinline__ bool mbar_test_wait_fwd(uint64_t* bar, uint32_t parity);
+__device__ __forceinline__ bool mbar_wait_fast(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_test_wait_fwd(bar, parity)) return true;
+  return mbar_wait_bounded(bar, parity, limit_ns);
+}
+
 // Non-blocking test of phase `parity`.
 __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
@@ -110,6 +148,8 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+
+__device__ __forceinline__ bool mbar_test_wait_fwd(uint64_t* bar, uint32_t parity) { return mbar_test_wait(bar, parity); }
 
 // Same as mbar_wait_bounded, spinning on the non-blocking test instead of the
 // potentially suspending try_wait: for phases that complete within a
@@ -386,6 +426,32 @@ __device__ __forceinline__ void tc_mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem,
       "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u));
+}
+
+// Warp-wide variants: every lane of the warp executes them with the same
+// (warp-uniform) operands and lane 0 issues.  The warp stays converged, so
+// the descriptors live in uniform registers instead of being moved there
+// from one divergent lane before each product.
+__device__ __forceinline__ void tc_mma_bf16_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                 bool accumulate, bool leader) {
+  asm volatile(
+      "{\n .reg .pred p, e;\n setp.ne.u32 p, %4, 0;\n setp.ne.u32 e, %5, 0;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u), "r"(leader ? 1u : 0u));
+}
+__device__ __forceinline__ void tc_mma_bf16_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                    bool accumulate, bool leader) {
+  asm volatile(
+      "{\n .reg .pred p, e;\n setp.ne.u32 p, %4, 0;\n setp.ne.u32 e, %5, 0;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u), "r"(leader ? 1u : 0u));
+}
+__device__ __forceinline__ void tc_commit_warp(uint64_t* bar, bool leader) {
+  asm volatile(
+      "{\n .reg .pred e;\n setp.ne.u32 e, %1, 0;\n"
+      " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(smem_addr(bar)),
+      "r"(leader ? 1u : 0u)
+      : "memory");
 }
 
 // The MMAs this thread issued so far arrive on `bar` when complete.

@@ -48,6 +48,7 @@ struct DecodeLaunch {
   int Tt;  // query tokens per row tile (G * Tt <= 16 rows)
   int NT;  // row tiles per (sequence, KV head): ceil(T / Tt)
   int tc;  // 1: tcgen05 kernel (128-row tiles, math PKV_MATH_TC)
+  int tc2; // 1: the tcgen05 kernel that serves a pair of row tiles per CTA (NT >= 2)
   int kv_fp8;    // one-byte elements (E4M3 or INT8)
   int kv_dtype;  // pkv_kv_dtype
   int pmax;  // max partitions of a sequence (ceil(MB / ppu))
@@ -60,6 +61,7 @@ struct DecodeLaunch {
   CUtensorMap kmap, vmap;
   CUtensorMap pmap;  // tcgen05 kernel with split-K: store map of part_o ([B][T][Hq][pmax][D] fp32)
   CUtensorMap omap;  // tcgen05 kernel: store map of out ([B][T][Hq][D] bf16)
+  CUtensorMap qmap;  // tile-pair kernel: load map of q ([B][T][Hq][D] bf16, box 64 x G x Tt)
   cudaStream_t stream;
   int num_sms;
   cudaEvent_t ev_start, ev_end;  // optional, recorded around the decode kernel
@@ -79,7 +81,9 @@ bool pdl_enabled();
 // Shared memory per CTA of the decode kernel.
 // pages a tcgen05 work unit may span (its descriptor slot's page table)
 constexpr int kTcUnitMaxPages = 256;
-size_t decode_smem_bytes(int kv_fp8, int D, int bs, int warps, int stages, int tc);
+// warps per CTA of the tile-pair tcgen05 kernel (8 softmax, MMA, 2 copy)
+constexpr int kTcPairWarps = 11;
+size_t decode_smem_bytes(int kv_fp8, int D, int bs, int warps, int stages, int tc, int tc2 = 0);
 
 // Launch planner + decode (the decode merges split-K partials itself).  Returns cudaSuccess or
 // the first launch error.

@@ -64,7 +64,7 @@ def test_llama8b_layer_step():
     _check_full(dc, out_ffma, 0, "llama8b layer (ffma)", want)
 
 
-@pytest.mark.parametrize("T", [4, 8, 32, 128])
+@pytest.mark.parametrize("T", [4, 8, 32, 64, 128, 256])
 def test_spec_verify_full(T):
     # the verify step the benchmark times: T draft tokens per sequence appended
     # at the end of its context (4096 after the append), then one T-token

@@ -172,6 +172,12 @@ TC_SWEEP = [  # (bs, Hq, Hkv, T, lens)
     (16, 32, 8, 33, [40, 100, 260]),            # two tiles (32 + 1 tokens)
     (16, 64, 8, 128, [130, 300]),               # G 8: eight tiles, a prefill chunk
     (32, 16, 2, 17, [17, 64, 65, 700]),
+    # two or more tiles per KV head: CTAs that hold a pair of tiles
+    (16, 32, 8, 64, [64, 65, 300, 1000]),        # one full pair
+    (32, 32, 8, 96, [96, 200, 701]),             # three tiles: the second pair half empty
+    (16, 8, 1, 40, [41, 500, 77]),               # G 8: 16 tokens a tile, three tiles
+    (16, 24, 8, 50, [50, 51, 260]),              # G 3: 42 tokens (126 rows) a tile
+    (32, 32, 8, 256, [256, 300, 1100]),          # a 256-token prefill chunk, eight tiles
 ]
 
 
@@ -274,7 +280,7 @@ def test_tc_bad_block_id_flagged_and_skipped():
     assert np.all(np.isfinite(got[1]))
 
 
-@pytest.mark.parametrize("T,ppu", [(8, 0), (8, 1), (32, 0), (32, 1)])
+@pytest.mark.parametrize("T,ppu", [(8, 0), (8, 1), (32, 0), (32, 1), (64, 0), (64, 1)])
 def test_tc_first_token_is_v0_exactly(T, ppu):
     # context_lens == T: the first query token attends to position 0 alone,
     # so its softmax weight is 1 and its output is bf16(V_0) bit for bit, in
@@ -295,7 +301,7 @@ def test_tc_first_token_is_v0_exactly(T, ppu):
             assert np.array_equal(got[b, h], dc.v_host[0, blk, h // G, 0]), (b, h)
 
 
-@pytest.mark.parametrize("T", [8, 32])
+@pytest.mark.parametrize("T", [8, 32, 64])
 def test_tc_physical_permutation_bitwise_identical(T):
     # the same logical sequences stored in two different block permutations
     # give the same output bits: the order of every sum depends only on
@@ -317,7 +323,7 @@ def test_tc_physical_permutation_bitwise_identical(T):
         assert torch.equal(oa, ob), f"T={T} ppu={ppu}"
 
 
-@pytest.mark.parametrize("T", [8, 32])
+@pytest.mark.parametrize("T", [8, 32, 64])
 def test_tc_aliased_prefix_bitwise_identical(T):
     # sequences 1 and 2 point at sequence 0's first 4 blocks instead of
     # private copies holding the same tokens
@@ -339,3 +345,56 @@ def test_tc_aliased_prefix_bitwise_identical(T):
     osh = pkv.paged_decode_multi(q, shared.k, shared.v, shared.bt, shared.cl, [0], 0, c2.scale, opts=_tc_opts(2))
     torch.cuda.synchronize()
     assert torch.equal(op, osh)
+
+
+@pytest.mark.parametrize("T,ppu", [(512, 0), (512, 5), (200, 3)])
+def test_tc_prefill_chunks(T, ppu):
+    # chunked prefill over a paged cache ("Continuous Batching"): windows of
+    # up to 512 new tokens per sequence, with and without split-K partitions,
+    # every element against the oracle
+    Hq, Hkv = 32, 8
+    lens = [T, T + 37, 1500]
+    c = random_case(1100 + T + ppu, len(lens), Hq, Hkv, 128, 16, lens, poison=True)
+    dc = DeviceCase(c)
+    q = _q(1101 + T, c.B, T, Hq, 128)
+    plan = pkv.decode_plan(dc.k, c.B, Hq, c.MB, _tc_opts(ppu), T)
+    assert plan["math"] == pkv.MATH_TC and plan["row_tiles"] == (T * 4 + 127) // 128
+    out = pkv.paged_decode_multi(to_dev_bf16(q), dc.k, dc.v, dc.bt, dc.cl, [0], 0, c.scale, opts=_tc_opts(ppu))
+    torch.cuda.synchronize()
+    assert pkv.read_device_error() == 0
+    want = oracle.paged_decode_multi_gemm(q, dc.k_host, dc.v_host, c.block_tables, c.context_lens,
+                                          c.kv_group_ptr, 0, c.scale)
+    assert_close(bf16_dev_to_f64(out), want, f"prefill T={T} ppu={ppu}")
+
+
+def test_tc_pair_matches_one_tile_kernel():
+    # the pair kernel and the one-tile kernel (PKV_TC_PAIR=0 in a child
+    # process) compute the same products; their outputs agree to rounding
+    import os
+    import subprocess
+    import sys
+    env = dict(os.environ, PKV_TC_PAIR="0")
+    code = (
+        "import sys, numpy as np, torch\n"
+        "sys.path.insert(0, %r)\n"
+        "import paged_kv_cache_274_gb300 as pkv\n"
+        "from workloads import random_case, normal_bf16_bits\n"
+        "from tests._gpu import DeviceCase, to_dev_bf16\n"
+        "c = random_case(1200, 3, 32, 8, 128, 16, [64, 300, 900])\n"
+        "dc = DeviceCase(c)\n"
+        "q = normal_bf16_bits(1201, (3, 64, 32, 128))\n"
+        "o = pkv.paged_decode_multi(to_dev_bf16(q), dc.k, dc.v, dc.bt, dc.cl, [0], 0, c.scale,"
+        " opts=pkv.decode_opts(math=pkv.MATH_TC))\n"
+        "np.save(sys.argv[1], o.float().cpu().numpy())\n"
+    ) % (os.path.dirname(os.path.dirname(os.path.abspath(__file__))),)
+    import tempfile
+    with tempfile.TemporaryDirectory() as td:
+        path = os.path.join(td, "one_tile.npy")
+        subprocess.run([sys.executable, "-c", code, path], env=env, check=True, timeout=600)
+        one_tile = np.load(path).astype(np.float64)
+    c = random_case(1200, 3, 32, 8, 128, 16, [64, 300, 900])
+    dc = DeviceCase(c)
+    q = _q(1201, 3, 64, 32, 128)
+    pair = pkv.paged_decode_multi(to_dev_bf16(q), dc.k, dc.v, dc.bt, dc.cl, [0], 0, c.scale, opts=_tc_opts())
+    torch.cuda.synchronize()
+    assert_close(bf16_dev_to_f64(pair), one_tile, "pair vs one-tile kernel")
