@@ -9,8 +9,12 @@ One step = one pass of the whole hot path over one batch:
   mixed_prefix: 256 sequences, log-uniform lengths, shared prefix blocks;
   fp8_shared: four layer calls that read one E4M3 cache (shared-with pointer);
   int8_shared: the same with an INT8 cache, per-page (scale, zero) pairs;
-  spec_verify_t4: the Llama-8B layer scoring 4 draft tokens per sequence
-      (append 4 tokens, then one multi-token decode, causal among them).
+  spec_verify_tN (N = 4 .. 128): the Llama-8B layer scoring N draft tokens
+      per sequence (append N tokens, then one multi-token decode, causal
+      among them); spec_verify_t32_fp8 / _int8: the same with an E4M3 or an
+      asymmetric INT8 cache;
+  prefill_t256 / prefill_t512: chunked prefill, windows of 256 / 512 new
+      tokens per sequence over the same layer.
 
 Metric: KV bytes read per step / step time (GB/s, 1e9), with % of the
 measured HBM peak and decode steps/s beside it.  Inputs (>= 512 MiB of KV)
@@ -54,14 +58,15 @@ FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0
 WORKLOADS = ("llama8b_layer", "long_b4_32k", "long_b1_128k", "mixed_prefix", "fp8_shared",
              "int8_shared", "spec_verify_t4", "spec_verify_t8", "spec_verify_t16", "spec_verify_t32",
-             "spec_verify_t64", "spec_verify_t128", "prefill_t256", "prefill_t512", "tiny", "copy_blocks")
+             "spec_verify_t64", "spec_verify_t128", "prefill_t256", "prefill_t512",
+             "spec_verify_t32_fp8", "spec_verify_t32_int8", "tiny", "copy_blocks")
 
 
 def query_tokens_of(name):
     """Query tokens per sequence of a workload (1: single-token decode)."""
     for prefix in ("spec_verify_t", "prefill_t"):
         if name.startswith(prefix):
-            return int(name[len(prefix):])
+            return int(name[len(prefix):].split("_")[0])
     return 1
 
 
@@ -253,7 +258,12 @@ def structure(name):
     """Block tables, lengths, queries, append slots (no cache contents)."""
     from workloads import gen
     if name == "llama8b_layer" or query_tokens_of(name) > 1:
-        return gen.llama8b_layer_case(fill=False)
+        c = gen.llama8b_layer_case(fill=False)
+        if name.endswith("_fp8"):      # the same layer with an E4M3 cache
+            c.kv_dtype = "fp8"
+        elif name.endswith("_int8"):   # ... or an asymmetric INT8 cache
+            c.kv_dtype = "int8a"
+        return c
     if name.startswith("long_"):
         return gen.long_context_case(name[len("long_"):], fill=False)
     if name == "mixed_prefix":

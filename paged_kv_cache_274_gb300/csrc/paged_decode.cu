@@ -34,7 +34,7 @@ const void* decode_kernel_fp8_d128(int bs, int math, int gt);
 const void* decode_kernel_int8_d128(int bs, int math, int gt);
 const void* decode_kernel_mt_bf16(int D, int bs, int gt);
 const void* decode_kernel_mt_1byte(int kv_dtype, int bs, int gt);
-const void* decode_kernel_tc(int bs, bool rot);
+const void* decode_kernel_tc(int bs, bool rot, int kv_dtype);
 const void* decode_kernel_tc2(int bs);
 
 // ---------------------------------------------------------------------------
@@ -328,8 +328,7 @@ size_t decode_smem_bytes(int kv_fp8, int D, int bs, int warps, int stages, int t
 // tcgen05 kernel for pairs of row tiles.
 static const void* pick_kernel(int kv_dtype, int D, int bs, int math, int gt, bool mt, bool tc2 = false) {
   if (math == PKV_MATH_TC && tc2) return (kv_dtype == PKV_KV_BF16 && D == 128) ? decode_kernel_tc2(bs) : nullptr;
-  if (math == PKV_MATH_TC)
-    return (kv_dtype == PKV_KV_BF16 && D == 128) ? decode_kernel_tc(bs, gt <= kTcRotMaxRows) : nullptr;
+  if (math == PKV_MATH_TC) return D == 128 ? decode_kernel_tc(bs, gt <= kTcRotMaxRows, kv_dtype) : nullptr;
   if (mt) {
     if (math != PKV_MATH_MMA) return nullptr;
     return kv_dtype == PKV_KV_BF16 ? decode_kernel_mt_bf16(D, bs, gt) : decode_kernel_mt_1byte(kv_dtype, bs, gt);

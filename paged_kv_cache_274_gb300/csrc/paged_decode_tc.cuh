@@ -45,6 +45,15 @@
 //     never stored): at T x G = 32, say, only warp 3 works, and warp 0, which
 //     shares its sub-partition with the MMA warp, stays idle.
 //
+// One-byte caches (E4M3, INT8) take the same path after a converter warp
+// widens each step's pages in shared memory: the copy warps land the codes
+// in the upper half of a stage, and the converter rewrites the stage as
+// bf16(code value x page scale) (INT8: (code - zero) x scale), row by row,
+// so that the products, the softmax and the output see a bf16 cache.  The
+// page parameters are applied in fp32 once per element ("KV Cache
+// Engineering: PagedAttention, Continuous Batching, Attention Variants, and
+// the Bandwidth Wall", "Quantized KV Cache": dequantise on read).
+//
 // Units are (sequence, KV head, row tile, partition) from the planner's
 // counter; the merge kernel combines partitions.  Every wait is bounded; a
 // CTA that gives up records PKV_DEVERR_TIMEOUT, lets the copies and products
@@ -62,6 +71,10 @@ constexpr int kTcVStages = 2;       // V ring
 constexpr int kTcMaxPages = 256;    // pages of a unit (the planner's partition length for this kernel)
 constexpr int kTcComputeWarps = 4;  // one row of the tile per thread
 constexpr int kTcThreads = 32 * (kTcComputeWarps + 3);  // + MMA warp + K copy warp + V copy warp
+// one-byte caches add a converter warp (two CTAs of 8 warps x 128 registers
+// fill an SM's register file)
+constexpr int kTcThreads1B = kTcThreads + 32;
+__host__ __device__ constexpr int tc_threads(int kv) { return kv == PKV_KV_BF16 ? kTcThreads : kTcThreads1B; }
 constexpr uint32_t kTcCols = 256;   // TMEM columns: S at 0, Q at 64, O at 128
 constexpr uint32_t kTcSCol = 0;     // S(g): 64 fp32 columns
 constexpr uint32_t kTcQCol = 64;    // query tile: 128 d as 64 columns of bf16 pairs
@@ -76,8 +89,8 @@ struct TcLayout {  // byte offsets from the 1024-aligned shared-memory base
   static constexpr uint32_t kBars = kV + kTcVStages * kTile;
   // full_k[4], kp_free[4], full_v[2], v_free[2], s_done, s_free, p_ready[4],
   // q_ready, slot_full[2], slot_free[2], stg_full, stg_free, o_ready,
-  // mma_drain
-  static constexpr int kNumBars = 3 * kTcKStages + 2 * kTcVStages + 3 + 4 + 4;
+  // mma_drain, then for one-byte caches tma_k[4], tma_v[2] (codes landed)
+  static constexpr int kNumBars = 3 * kTcKStages + 2 * kTcVStages + 3 + 4 + 4 + kTcKStages + kTcVStages;
   static constexpr uint32_t kMisc = kBars + 8 * kNumBars;    // TMEM base
   static constexpr uint32_t kSlots = kMisc + 16;             // 2 unit slots
   static constexpr uint32_t kSlotPages = 32;                 // after 8 int32 of descriptor
@@ -129,10 +142,77 @@ struct TcUnit {
   int u, b, pidx, nparts, ctx, kvh, tile, t0, t1, npages, nsteps;
 };
 
-template <int BS, bool kRot>
+// Widen 16 one-byte codes (a 16-byte chunk, element i in byte i) to bf16 of
+// (code value) x scale, INT8 (code - zero) x scale, as two 16-byte chunks.
+// The code value converts exactly (E4M3 and code - zero are exact in f16);
+// the product is rounded once in fp32, then to bf16 (round to nearest even).
+template <int KV>
+__device__ __forceinline__ void widen16(const uint4 c, float scale, uint32_t zc, uint4& o0, uint4& o1) {
+  const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+  uint32_t r[8];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t lo, hi;
+    if constexpr (KV == PKV_KV_INT8)
+      int8x4_to_f16x2x2(w[q], zc, lo, hi);
+    else
+      e4m3x4_to_f16x2x2(w[q], lo, hi);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+    r[2 * q] = pack_bf16x2(a.x * scale, a.y * scale);
+    r[2 * q + 1] = pack_bf16x2(b.x * scale, b.y * scale);
+  }
+  o0 = make_uint4(r[0], r[1], r[2], r[3]);
+  o1 = make_uint4(r[4], r[5], r[6], r[7]);
+}
+
+// Rewrite a stage of `rows` token rows (64-d halves kRegion apart, 128-byte
+// rows, 16-byte chunks XOR-swizzled by row % 8) whose one-byte codes a
+// tensor-map copy put in the upper half (row r's 128 codes at
+// kRegion + 128 r) as bf16 values; the caller gives row r's scale (and INT8
+// zero constant).  One warp; lane l takes rows l, l + 32, ...: the lower half
+// first (codes 0-63 of every row), then the upper half row by row, each
+// row's last codes read before its row is overwritten.
+template <int KV, int ROWS>
+__device__ __forceinline__ void widen_stage(uint8_t* stage, uint32_t region, int lane, const float (&scale)[ROWS / 32],
+                                            const uint32_t (&zc)[ROWS / 32], int valid_rows) {
+#pragma unroll
+  for (int rr = 0; rr < ROWS / 32; ++rr) {
+    const int r = lane + 32 * rr;
+    if (r >= valid_rows) continue;
+    const uint8_t* src = stage + region + r * 128;
+    uint8_t* dst = stage + r * 128;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint4 codes = *reinterpret_cast<const uint4*>(src + ((c ^ (r & 7)) << 4));
+      uint4 o0, o1;
+      widen16<KV>(codes, scale[rr], zc[rr], o0, o1);
+      *reinterpret_cast<uint4*>(dst + (((2 * c) ^ (r & 7)) << 4)) = o0;
+      *reinterpret_cast<uint4*>(dst + (((2 * c + 1) ^ (r & 7)) << 4)) = o1;
+    }
+  }
+#pragma unroll
+  for (int rr = 0; rr < ROWS / 32; ++rr) {
+    const int r = lane + 32 * rr;
+    if (r >= valid_rows) continue;
+    uint8_t* row = stage + region + r * 128;
+    uint4 codes[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) codes[c] = *reinterpret_cast<const uint4*>(row + (((4 + c) ^ (r & 7)) << 4));
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint4 o0, o1;
+      widen16<KV>(codes[c], scale[rr], zc[rr], o0, o1);
+      *reinterpret_cast<uint4*>(row + (((2 * c) ^ (r & 7)) << 4)) = o0;
+      *reinterpret_cast<uint4*>(row + (((2 * c + 1) ^ (r & 7)) << 4)) = o1;
+    }
+  }
+}
+
+template <int BS, bool kRot, int KV = PKV_KV_BF16>
 // Two CTAs per SM: a sub-partition's 16384 registers hold four of the 14
-// warps at 128 registers a thread.
-__global__ void __launch_bounds__(kTcThreads, 2)
+// (16 with a converter warp) warps at 128 registers a thread.
+__global__ void __launch_bounds__(tc_threads(KV), 2)
     paged_decode_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                            const __grid_constant__ CUtensorMap vmap,
                            const __grid_constant__ CUtensorMap pmap,  // split-K partials (pmax > 1)
@@ -140,6 +220,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                            const DecodeParams p) {
   constexpr int D = 128;
   constexpr int PPI = kTcTokens / BS;  // pages per step
+  constexpr bool kOneByte = KV != PKV_KV_BF16;
   static_assert(kTcMaxPages % PPI == 0, "");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(
@@ -169,6 +250,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   uint64_t* stg_free = stg_full + 1;          // split-K partials: a store has read its staging buffer
   uint64_t* o_ready = stg_free + 1;           // a unit's last P . V done: O final, its K and V stages idle
   uint64_t* mma_drain = o_ready + 1;          // after a timeout: every product issued is done
+  uint64_t* tma_k = mma_drain + 1;            // [4] one-byte caches: K(g)'s codes landed (then full_k: widened)
+  uint64_t* tma_v = tma_k + kTcKStages;       // [2] one-byte caches: V(g)'s codes landed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + TcLayout::kMisc);
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -176,6 +259,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   const bool mma_warp = warp == kTcComputeWarps;
   const bool kcopy = warp == kTcComputeWarps + 1;
   const bool vcopy = warp == kTcComputeWarps + 2;
+  const bool widen = kOneByte && warp == kTcComputeWarps + 3;  // converter warp (one-byte caches)
 
   if (tid == 0) {
     for (int s = 0; s < kTcKStages; ++s) {
@@ -192,7 +276,12 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     mbar_init(q_ready, kTcComputeWarps);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&slot_full[s], 1);
-      mbar_init(&slot_free[s], kTcComputeWarps + 2);  // compute warps, MMA warp, V copy warp
+      // compute warps, MMA warp, V copy warp (and the converter warp)
+      mbar_init(&slot_free[s], kTcComputeWarps + 2 + (kOneByte ? 1 : 0));
+    }
+    if (kOneByte) {
+      for (int s = 0; s < kTcKStages; ++s) mbar_init(&tma_k[s], 1);
+      for (int s = 0; s < kTcVStages; ++s) mbar_init(&tma_v[s], 1);
     }
     mbar_init(stg_full, kTcComputeWarps);
     mbar_init(stg_free, 1);
@@ -255,6 +344,48 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     if (lane == 0)
       ok = (suspend ? mbar_wait_bounded(bar, parity, kWaitLimitNs) : mbar_wait_spin(bar, parity, kWaitLimitNs)) ? 1 : 0;
     return __shfl_sync(kFull, ok, 0) != 0;
+  };
+
+  // One-byte caches: wait until step g's K (is_k) or V codes have landed,
+  // widen them in the stage to bf16 with each row's page parameters, publish
+  // with full_k / full_v.  Rows of pages past the unit's end are left as
+  // they are (their scores are masked and their V rows cleared).  Whole
+  // warp; false on timeout.
+  auto widen_pages = [&](bool is_k, const TcUnit& U, const volatile int* pages, int j, uint32_t g) -> bool {
+    if constexpr (!kOneByte) {
+      return true;
+    } else {
+      uint64_t* landed = is_k ? &tma_k[g % kTcKStages] : &tma_v[g % kTcVStages];
+      const uint32_t parity = is_k ? (g / kTcKStages) & 1u : (g / kTcVStages) & 1u;
+      if (!warp_wait(landed, parity, true)) return false;
+      uint8_t* st = sm + (is_k ? TcLayout::kK + (g % kTcKStages) * TcLayout::kTile
+                               : TcLayout::kV + (g % kTcVStages) * TcLayout::kTile);
+      const int np = min(PPI, U.npages - j * PPI);
+      const float* sc = is_k ? p.k_scale : p.v_scale;
+      float scale[2];
+      uint32_t zc[2];
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        const int q = (lane + 32 * rr) / BS;
+        scale[rr] = 0.f;
+        zc[rr] = 0u;
+        if (q < np) {
+          const size_t pi = static_cast<size_t>(pages[j * PPI + q]) * p.Hkv + U.kvh;
+          if constexpr (KV == PKV_KV_INT8) {
+            const float2 sz = __ldg(reinterpret_cast<const float2*>(sc) + pi);
+            scale[rr] = sz.x;
+            zc[rr] = int8_zero_const(sz.y);
+          } else {
+            scale[rr] = __ldg(sc + pi);
+          }
+        }
+      }
+      widen_stage<KV, kTcTokens>(st, TcLayout::kRegion, lane, scale, zc, np * BS);
+      fence_proxy_async_smem();  // the widened rows are read by the tensor cores
+      __syncwarp();
+      if (lane == 0) mbar_arrive(is_k ? &full_k[g % kTcKStages] : &full_v[g % kTcVStages]);
+      return true;
+    }
   };
 
   if (kcopy) {
@@ -333,14 +464,19 @@ __global__ void __launch_bounds__(kTcThreads, 2)
           break;
         }
         uint8_t* st = sm + TcLayout::kK + (g % kTcKStages) * TcLayout::kTile;
-        uint64_t* bar = &full_k[g % kTcKStages];
+        uint64_t* bar = kOneByte ? &tma_k[g % kTcKStages] : &full_k[g % kTcKStages];
         const int np = min(PPI, npages_total - j * PPI);
         if (lane == 0) {
           fence_proxy_async_smem();  // the stage held P (generic writes) before
-          mbar_arrive_expect_tx(bar, static_cast<uint32_t>(np) * 2u * 64u * BS * 2u);
+          mbar_arrive_expect_tx(bar, static_cast<uint32_t>(np) * (kOneByte ? 128u : 2u * 64u * 2u) * BS);
         }
         __syncwarp();
-        if (lane < 2 * np) {
+        if (kOneByte) {  // one box of 128 codes per page, into the upper half for the converter
+          if (lane < np) {
+            const int row = p.row_base + (pages[j * PPI + lane] * p.Hkv + kvh) * BS;
+            tma_load_2d(st + TcLayout::kRegion + lane * BS * 128, &kmap, bar, 0, row, policy);
+          }
+        } else if (lane < 2 * np) {
           const int q = lane >> 1, half = lane & 1;
           const int row = p.row_base + (pages[j * PPI + q] * p.Hkv + kvh) * BS;
           tma_load_2d(st + half * TcLayout::kRegion + q * BS * 128, &kmap, bar, half * 64, row, policy);
@@ -368,14 +504,19 @@ __global__ void __launch_bounds__(kTcThreads, 2)
           break;
         }
         uint8_t* st = sm + TcLayout::kV + (g % kTcVStages) * TcLayout::kTile;
-        uint64_t* bar = &full_v[g % kTcVStages];
+        uint64_t* bar = kOneByte ? &tma_v[g % kTcVStages] : &full_v[g % kTcVStages];
         const int np = min(PPI, U.npages - j * PPI);
         if (lane == 0) {
           fence_proxy_async_smem();  // after the compute warps' clearing of stale V rows
-          mbar_arrive_expect_tx(bar, static_cast<uint32_t>(np) * 2u * 64u * BS * 2u);
+          mbar_arrive_expect_tx(bar, static_cast<uint32_t>(np) * (kOneByte ? 128u : 2u * 64u * 2u) * BS);
         }
         __syncwarp();
-        if (lane < 2 * np) {
+        if (kOneByte) {
+          if (lane < np) {
+            const int row = p.row_base + (pages[j * PPI + lane] * p.Hkv + U.kvh) * BS;
+            tma_load_2d(st + TcLayout::kRegion + lane * BS * 128, &vmap, bar, 0, row, policy);
+          }
+        } else if (lane < 2 * np) {
           const int q = lane >> 1, half = lane & 1;
           const int row = p.row_base + (pages[j * PPI + q] * p.Hkv + U.kvh) * BS;
           tma_load_2d(st + half * TcLayout::kRegion + q * BS * 128, &vmap, bar, half * 64, row, policy);
@@ -383,6 +524,35 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         copies_end = g + 1;
       }
       if (timed_out) break;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&slot_free[k]);
+    }
+  } else if (widen) {
+    // Converter (one-byte caches): per unit, K of its first step, then per
+    // step j the K codes of step j + 1 and the V codes of step j (the order
+    // the MMA warp needs them: S runs one step ahead of P . V), each once its
+    // codes have landed.  (Widening V in the V copy warp instead, between
+    // its copies, delayed the next copy: 780 against 573 us for the 32-token
+    // verify step on an E4M3 cache.)
+    uint32_t gk = 0, gv = 0;
+    for (int i = 0;; ++i) {
+      const int k = i & 1;
+      if (!warp_wait(&slot_full[k], (i >> 1) & 1u, true)) {
+        timed_out = true;
+        break;
+      }
+      const TcUnit U = read_unit(k);
+      if (U.u >= total_units) break;
+      const volatile int* pages = slot_pages(k);
+      bool ok = widen_pages(true, U, pages, 0, gk++);
+      for (int j = 0; ok && j < U.nsteps; ++j) {
+        if (j + 1 < U.nsteps) ok = widen_pages(true, U, pages, j + 1, gk++);
+        if (ok) ok = widen_pages(false, U, pages, j, gv++);
+      }
+      if (!ok) {
+        timed_out = true;
+        break;
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&slot_free[k]);
     }
@@ -853,10 +1023,12 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     // warp's last commits (each covers every earlier product)
     if (kcopy && lane == 0)
       for (uint32_t g = copies_end > kTcKStages ? copies_end - kTcKStages : 0; g < copies_end; ++g)
-        mbar_wait_bounded(&full_k[g % kTcKStages], (g / kTcKStages) & 1u, kWaitLimitNs / 16);
+        mbar_wait_bounded(kOneByte ? &tma_k[g % kTcKStages] : &full_k[g % kTcKStages], (g / kTcKStages) & 1u,
+                          kWaitLimitNs / 16);
     if (vcopy && lane == 0)
       for (uint32_t g = copies_end > kTcVStages ? copies_end - kTcVStages : 0; g < copies_end; ++g)
-        mbar_wait_bounded(&full_v[g % kTcVStages], (g / kTcVStages) & 1u, kWaitLimitNs / 16);
+        mbar_wait_bounded(kOneByte ? &tma_v[g % kTcVStages] : &full_v[g % kTcVStages], (g / kTcVStages) & 1u,
+                          kWaitLimitNs / 16);
     if (mma_warp && lane == 0 && (s_end > 0 || pv_end > 0)) {  // one commit covers every product issued
       tc_commit(mma_drain);
       mbar_wait_bounded(mma_drain, 0, kWaitLimitNs / 16);

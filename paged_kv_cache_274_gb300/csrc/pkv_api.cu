@@ -380,15 +380,16 @@ static pkv_status resolve_decode(const pkv_cache_desc* c, int32_t batch, int32_t
   pkv_decode_opts o{};
   if (opts) o = *opts;
   int math = o.math != 0 ? o.math : env_int("PKV_DECODE_MATH", PKV_MATH_AUTO);
-  // tcgen05 tiles: multi-token calls on bf16 caches with head_dim 128
-  const bool tc_ok = c->dtype == PKV_KV_BF16 && c->head_dim == 128 && T > 1 && G <= 128;
+  // tcgen05 tiles: multi-token calls with head_dim 128 (one-byte caches are
+  // widened to bf16 in shared memory)
+  const bool tc_ok = c->head_dim == 128 && T > 1 && G <= 128;
   // measured on GB300 (Llama-8B layer, G 4): mma.sync tiles are faster up to
   // 16 rows per KV head (172 us at 4 tokens, one tile), tcgen05 tiles from 32
   // rows on (kernel 173 vs 234 us at 8 tokens, 173 vs 451 at 16, 183 vs 865
   // at 32, 583 vs 3402 at 128)
   if (math == PKV_MATH_AUTO) math = (tc_ok && static_cast<long long>(T) * G > 16) ? PKV_MATH_TC : PKV_MATH_MMA;
   if (math == PKV_MATH_TC && !tc_ok)
-    return fail(PKV_ERR_UNSUPPORTED, "tcgen05 tiles need T > 1, a bf16 cache, head_dim 128 and G <= 128");
+    return fail(PKV_ERR_UNSUPPORTED, "tcgen05 tiles need T > 1, head_dim 128 and G <= 128");
   if (math == PKV_MATH_MMA && G > 16)
     return fail(PKV_ERR_UNSUPPORTED, "G = %d query heads per KV head (mma supports <= 16)", G);
   if (math == PKV_MATH_FFMA && G != 1 && G != 2 && G != 4 && G != 8)
@@ -415,8 +416,10 @@ static pkv_status resolve_decode(const pkv_cache_desc* c, int32_t batch, int32_t
   // a pair of tiles per CTA with 8 softmax warps, an MMA warp and two copy
   // warps, 2-stage K and V rings of 128 tokens -- PKV_TC_PAIR=0 keeps the
   // one-tile kernel there)
-  const bool tc2 = tc && NT >= 2 && env_int("PKV_TC_PAIR", 1) != 0;
-  int warps = tc2 ? pkv::kTcPairWarps : tc ? 7 : (o.warps_per_cta != 0 ? o.warps_per_cta : env_int("PKV_DECODE_WARPS", 4));
+  const bool tc2 = tc && NT >= 2 && c->dtype == PKV_KV_BF16 && env_int("PKV_TC_PAIR", 1) != 0;
+  int warps = tc2 ? pkv::kTcPairWarps
+              : tc ? (c->dtype == PKV_KV_BF16 ? 7 : 8)  // + the converter warp of one-byte caches
+                   : (o.warps_per_cta != 0 ? o.warps_per_cta : env_int("PKV_DECODE_WARPS", 4));
   int stages = tc2 ? 2 : tc ? 4 : (o.stages != 0 ? o.stages : env_int("PKV_DECODE_STAGES", 0));
   if (stages == 0) stages = stage_bytes >= (8u << 10) ? 2 : 3;
   if (!tc && (warps < 1 || warps > 8)) return fail(PKV_ERR_INVALID_ARG, "warps_per_cta %d outside 1..8", warps);

@@ -250,11 +250,11 @@ def test_tc_speculative_verify_flow():
 
 
 def test_tc_unsupported_shapes_rejected():
-    c8 = random_case(970, 2, 32, 8, 128, 16, [40, 50], kv_dtype="fp8")
-    d8 = DeviceCase(c8)
-    q = to_dev_bf16(_q(971, 2, 8, 32, 128))
+    c64 = random_case(970, 2, 32, 8, 64, 16, [40, 50])   # head_dim 64
+    d64 = DeviceCase(c64)
+    q = to_dev_bf16(_q(971, 2, 8, 32, 64))
     with pytest.raises(pkv.PkvError):
-        pkv.paged_decode_multi(q, d8.k, d8.v, d8.bt, d8.cl, k_scale=d8.ks, v_scale=d8.vs, opts=_tc_opts())
+        pkv.paged_decode_multi(q, d64.k, d64.v, d64.bt, d64.cl, opts=_tc_opts())
     c = random_case(972, 2, 32, 8, 128, 16, [40, 50])
     dc = DeviceCase(c)
     with pytest.raises(pkv.PkvError):   # T = 1
@@ -398,3 +398,87 @@ def test_tc_pair_matches_one_tile_kernel():
     pair = pkv.paged_decode_multi(to_dev_bf16(q), dc.k, dc.v, dc.bt, dc.cl, [0], 0, c.scale, opts=_tc_opts())
     torch.cuda.synchronize()
     assert_close(bf16_dev_to_f64(pair), one_tile, "pair vs one-tile kernel")
+
+
+# ---------------------------------------------------------------------------
+# one-byte caches (E4M3, INT8) on the tcgen05 tiles: pages widened in shared
+# memory to bf16 of (code value) x page scale ((code - zero) x scale)
+# ---------------------------------------------------------------------------
+TC_1B_SWEEP = [  # (dtype, bs, Hq, Hkv, T, lens)
+    ("fp8", 16, 32, 8, 8, [1, 9, 40, 300, 1000]),      # 32 rows of 128, a context below T
+    ("fp8", 32, 32, 8, 33, [40, 100, 260]),            # two tiles
+    ("fp8", 16, 16, 1, 20, [20, 50, 129]),             # G 16
+    ("int8", 16, 16, 1, 3, [3, 50, 129]),
+    ("int8a", 32, 32, 8, 32, [32, 64, 700]),           # one full tile
+    ("int8a", 16, 8, 8, 20, [19, 20, 21, 333]),        # MHA
+]
+
+
+@pytest.mark.parametrize("dtype,bs,Hq,Hkv,T,lens", TC_1B_SWEEP)
+@pytest.mark.parametrize("ppu", [0, 3])
+def test_tc_one_byte_sweep(dtype, bs, Hq, Hkv, T, lens, ppu):
+    seed = 1300 + 3 * bs + 7 * Hq + 11 * Hkv + 13 * T + len(dtype)
+    c = random_case(seed, len(lens), Hq, Hkv, 128, bs, lens, kv_dtype=dtype, poison=True)
+    dc = DeviceCase(c)
+    q = _q(seed + 1, c.B, T, Hq, 128)
+    plan = pkv.decode_plan(dc.k, c.B, Hq, c.MB, _tc_opts(ppu), T)
+    assert plan["math"] == pkv.MATH_TC
+    out = pkv.paged_decode_multi(to_dev_bf16(q), dc.k, dc.v, dc.bt, dc.cl, [0], 0, c.scale,
+                                 k_scale=dc.ks, v_scale=dc.vs, opts=_tc_opts(ppu))
+    torch.cuda.synchronize()
+    assert pkv.read_device_error() == 0
+    assert_close(bf16_dev_to_f64(out), _oracle(dc, q), f"tc {dtype} T={T} G={Hq // Hkv} bs={bs} ppu={ppu}")
+
+
+def _widened_bits(dc, blk, kvh, row):
+    """bf16 bits of bf16(fp32(code value) x fp32 scale) ((code - zero) for
+    INT8) of V row `row` of page (blk, kvh): what the widened page holds."""
+    c = dc.c
+    codes = dc.v_host[0, blk, kvh, row]
+    if c.kv_dtype == "fp8":
+        val = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float32)
+        val = val * torch.tensor(float(c.v_scale[0, blk, kvh]), dtype=torch.float32)
+    else:
+        s_, z_ = c.v_scale[0, blk, kvh]
+        val = (torch.from_numpy(codes.astype(np.float32)) - torch.tensor(float(z_))) * torch.tensor(float(s_))
+    return val.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("dtype", ["fp8", "int8a"])
+@pytest.mark.parametrize("T,ppu", [(8, 0), (32, 1)])
+def test_tc_one_byte_first_token_is_widened_v0_exactly(dtype, T, ppu):
+    # context_lens == T: the first query token attends to position 0 alone
+    # (weight 1), so its output is the widened V_0 row bit for bit
+    c = random_case(1400 + T + ppu, 3, 32, 8, 128, 16, [T, T, T], kv_dtype=dtype)
+    dc = DeviceCase(c)
+    q = _q(1401 + T, c.B, T, 32, 128)
+    out = pkv.paged_decode_multi(to_dev_bf16(q), dc.k, dc.v, dc.bt, dc.cl, [0], 0, c.scale,
+                                 k_scale=dc.ks, v_scale=dc.vs, opts=_tc_opts(ppu))
+    torch.cuda.synchronize()
+    assert pkv.read_device_error() == 0
+    got = out[:, 0].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    G = c.Hq // c.Hkv
+    for b in range(c.B):
+        blk = int(c.block_tables[b, 0])
+        for h in range(c.Hq):
+            assert np.array_equal(got[b, h], _widened_bits(dc, blk, h // G, 0)), (b, h)
+
+
+def test_tc_one_byte_physical_permutation_bitwise_identical():
+    lens = [70, 300, 40, 129]
+    a = random_case(1450, 4, 32, 8, 128, 16, lens, kv_dtype="fp8")
+    b = random_case(1450, 4, 32, 8, 128, 16, lens, kv_dtype="fp8")
+    perm = np.random.Generator(np.random.PCG64(5)).permutation(a.NB)
+    inv = np.argsort(perm)
+    b.k_src, b.v_src = a.k_src[:, inv].copy(), a.v_src[:, inv].copy()
+    b.k_scale, b.v_scale = a.k_scale[:, inv].copy(), a.v_scale[:, inv].copy()
+    b.block_tables = np.where(a.block_tables >= 0, perm[np.maximum(a.block_tables, 0)], -1).astype(np.int32)
+    da, db = DeviceCase(a), DeviceCase(b)
+    q = to_dev_bf16(_q(1451, a.B, 8, 32, 128))
+    for ppu in (0, 3):
+        oa = pkv.paged_decode_multi(q, da.k, da.v, da.bt, da.cl, [0], 0, a.scale, k_scale=da.ks, v_scale=da.vs,
+                                    opts=_tc_opts(ppu))
+        ob = pkv.paged_decode_multi(q, db.k, db.v, db.bt, db.cl, [0], 0, b.scale, k_scale=db.ks, v_scale=db.vs,
+                                    opts=_tc_opts(ppu))
+        torch.cuda.synchronize()
+        assert torch.equal(oa, ob), f"ppu={ppu}"

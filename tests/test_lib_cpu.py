@@ -175,7 +175,8 @@ def test_auto_back_end_and_tiles(lib, Hq, Hkv, T, math, tokens_per_tile, tiles):
 def test_tc_argument_checks(lib):
     tc = pkv.decode_opts(math=pkv.MATH_TC)
     assert _plan(lib, _desc(), 8, 1, 32, 64, tc)[0] == 2                  # T = 1
-    assert _plan(lib, _desc(dtype=1), 8, 4, 32, 64, tc)[0] == 2           # E4M3 cache
+    st, plan = _plan(lib, _desc(dtype=1), 8, 4, 32, 64, tc)                # E4M3 cache: widened
+    assert st == 0 and plan.math == pkv.MATH_TC and plan.warps_per_cta == 8  # + the converter warp
     assert _plan(lib, _desc(head_dim=64), 8, 4, 32, 64, tc)[0] == 2       # head_dim 64
     assert _plan(lib, _desc(), 8, 4, 32, 64, tc)[0] == 0
 
