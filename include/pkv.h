@@ -96,15 +96,17 @@ typedef struct {
 
 /* How the decode computes its dot products. */
 typedef enum {
-  PKV_MATH_AUTO = 0, /* the library picks: TC for multi-token bf16 calls with more
+  PKV_MATH_AUTO = 0, /* the library picks: TC for multi-token calls with more
                         than 16 query rows per KV head and head_dim 128, else MMA */
   PKV_MATH_FFMA = 1, /* fp32 CUDA-core FMAs; G must be 1, 2, 4 or 8; T = 1 */
   PKV_MATH_MMA = 2,  /* mma.sync tiles of up to 16 rows (bf16, or f16 for one-byte
                         caches); G <= 16 */
   PKV_MATH_TC = 3    /* tcgen05 tiles of 128 (query token, head) rows with TMEM
-                        accumulators; multi-token calls (T > 1), bf16 cache,
-                        head_dim 128, G <= 128; with more than one tile per
-                        KV head, pairs of tiles share each page read */
+                        accumulators; multi-token calls (T > 1), head_dim 128,
+                        G <= 128; bf16 pages as they are, E4M3 / INT8 pages
+                        as f16 code values with the page scales applied to
+                        the scores and to P; with more than one tile per KV
+                        head (bf16), pairs of tiles share each page read */
 } pkv_decode_math;
 
 /* Tuning knobs of pkv_paged_decode; a NULL pointer or zero fields = auto. */

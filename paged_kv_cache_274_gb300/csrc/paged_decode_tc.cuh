@@ -45,14 +45,20 @@
 //     never stored): at T x G = 32, say, only warp 3 works, and warp 0, which
 //     shares its sub-partition with the MMA warp, stays idle.
 //
-// One-byte caches (E4M3, INT8) take the same path after a converter warp
-// widens each step's pages in shared memory: the copy warps land the codes
-// in the upper half of a stage, and the converter rewrites the stage as
-// bf16(code value x page scale) (INT8: (code - zero) x scale), row by row,
-// so that the products, the softmax and the output see a bf16 cache.  The
-// page parameters are applied in fp32 once per element ("KV Cache
-// Engineering: PagedAttention, Continuous Batching, Attention Variants, and
-// the Bandwidth Wall", "Quantized KV Cache": dequantise on read).
+// One-byte caches (E4M3, INT8) take the same path with f16 operands ("KV
+// Cache Engineering: PagedAttention, Continuous Batching, Attention
+// Variants, and the Bandwidth Wall", "Quantized KV Cache": dequantise on
+// read).  The copy warps land a step's codes in the upper half of a stage
+// and a converter warp rewrites the stage as the f16 code values (INT8:
+// code - zero), which are exact in f16: one conversion per two codes, no
+// arithmetic.  The page scales are applied where they cost nothing per
+// element of the cache: a row's scores of page q are S' x c x k_scale[q]
+// (one multiply per score, folded into the softmax), and P carries
+// v_scale[q] / v_max (v_max: the unit's largest |v_scale|, so P stays
+// below 256), the output v_max.  The query rows go to f16 scaled by a power
+// of two per row (largest |q| in [2^14, 2^15)), which the row's softmax
+// coefficient takes back.  With one page, P = 1 and the output is
+// bf16(code value x scale) exactly as the widened value.
 //
 // Units are (sequence, KV head, row tile, partition) from the planner's
 // counter; the merge kernel combines partitions.  Every wait is bounded; a
@@ -142,25 +148,19 @@ struct TcUnit {
   int u, b, pidx, nparts, ctx, kvh, tile, t0, t1, npages, nsteps;
 };
 
-// Widen 16 one-byte codes (a 16-byte chunk, element i in byte i) to bf16 of
-// (code value) x scale, INT8 (code - zero) x scale, as two 16-byte chunks.
-// The code value converts exactly (E4M3 and code - zero are exact in f16);
-// the product is rounded once in fp32, then to bf16 (round to nearest even).
+// Widen 16 one-byte codes (a 16-byte chunk, element i in byte i) to their
+// f16 code values (E4M3 value, INT8 code - zero; both exact in f16) as two
+// 16-byte chunks.
 template <int KV>
-__device__ __forceinline__ void widen16(const uint4 c, float scale, uint32_t zc, uint4& o0, uint4& o1) {
+__device__ __forceinline__ void widen16(const uint4 c, uint32_t zc, uint4& o0, uint4& o1) {
   const uint32_t w[4] = {c.x, c.y, c.z, c.w};
   uint32_t r[8];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    uint32_t lo, hi;
     if constexpr (KV == PKV_KV_INT8)
-      int8x4_to_f16x2x2(w[q], zc, lo, hi);
+      int8x4_to_f16x2x2(w[q], zc, r[2 * q], r[2 * q + 1]);
     else
-      e4m3x4_to_f16x2x2(w[q], lo, hi);
-    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&lo));
-    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&hi));
-    r[2 * q] = pack_bf16x2(a.x * scale, a.y * scale);
-    r[2 * q + 1] = pack_bf16x2(b.x * scale, b.y * scale);
+      e4m3x4_to_f16x2x2(w[q], r[2 * q], r[2 * q + 1]);
   }
   o0 = make_uint4(r[0], r[1], r[2], r[3]);
   o1 = make_uint4(r[4], r[5], r[6], r[7]);
@@ -169,13 +169,13 @@ __device__ __forceinline__ void widen16(const uint4 c, float scale, uint32_t zc,
 // Rewrite a stage of `rows` token rows (64-d halves kRegion apart, 128-byte
 // rows, 16-byte chunks XOR-swizzled by row % 8) whose one-byte codes a
 // tensor-map copy put in the upper half (row r's 128 codes at
-// kRegion + 128 r) as bf16 values; the caller gives row r's scale (and INT8
-// zero constant).  One warp; lane l takes rows l, l + 32, ...: the lower half
+// kRegion + 128 r) as f16 code values; the caller gives row r's INT8 zero
+// constant.  One warp; lane l takes rows l, l + 32, ...: the lower half
 // first (codes 0-63 of every row), then the upper half row by row, each
 // row's last codes read before its row is overwritten.
 template <int KV, int ROWS>
-__device__ __forceinline__ void widen_stage(uint8_t* stage, uint32_t region, int lane, const float (&scale)[ROWS / 32],
-                                            const uint32_t (&zc)[ROWS / 32], int valid_rows) {
+__device__ __forceinline__ void widen_stage(uint8_t* stage, uint32_t region, int lane, const uint32_t (&zc)[ROWS / 32],
+                                            int valid_rows) {
 #pragma unroll
   for (int rr = 0; rr < ROWS / 32; ++rr) {
     const int r = lane + 32 * rr;
@@ -186,7 +186,7 @@ __device__ __forceinline__ void widen_stage(uint8_t* stage, uint32_t region, int
     for (int c = 0; c < 4; ++c) {
       const uint4 codes = *reinterpret_cast<const uint4*>(src + ((c ^ (r & 7)) << 4));
       uint4 o0, o1;
-      widen16<KV>(codes, scale[rr], zc[rr], o0, o1);
+      widen16<KV>(codes, zc[rr], o0, o1);
       *reinterpret_cast<uint4*>(dst + (((2 * c) ^ (r & 7)) << 4)) = o0;
       *reinterpret_cast<uint4*>(dst + (((2 * c + 1) ^ (r & 7)) << 4)) = o1;
     }
@@ -202,7 +202,7 @@ __device__ __forceinline__ void widen_stage(uint8_t* stage, uint32_t region, int
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       uint4 o0, o1;
-      widen16<KV>(codes[c], scale[rr], zc[rr], o0, o1);
+      widen16<KV>(codes[c], zc[rr], o0, o1);
       *reinterpret_cast<uint4*>(row + (((2 * c) ^ (r & 7)) << 4)) = o0;
       *reinterpret_cast<uint4*>(row + (((2 * c + 1) ^ (r & 7)) << 4)) = o1;
     }
@@ -300,8 +300,10 @@ __global__ void __launch_bounds__(tc_threads(KV), 2)
   const uint32_t tmem = *tmem_slot;
   const uint32_t t_lane = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);  // compute warp's 32 lanes
   const uint64_t policy = p.NT > 1 ? l2_policy_evict_normal() : l2_policy_evict_first();
-  constexpr uint32_t kIdescS = tc_idesc_bf16_f32(kTcRows, kTcTokens);
-  constexpr uint32_t kIdescO = tc_idesc_bf16_f32(kTcRows, D, /*b_mn_major=*/true);
+  // one-byte caches: f16 query, code values and P
+  constexpr uint32_t kIdescS = kOneByte ? tc_idesc_f16_f32(kTcRows, kTcTokens) : tc_idesc_bf16_f32(kTcRows, kTcTokens);
+  constexpr uint32_t kIdescO = kOneByte ? tc_idesc_f16_f32(kTcRows, D, /*b_mn_major=*/true)
+                                        : tc_idesc_bf16_f32(kTcRows, D, /*b_mn_major=*/true);
   pdl_trigger();
   pdl_wait();
 
@@ -347,8 +349,8 @@ __global__ void __launch_bounds__(tc_threads(KV), 2)
   };
 
   // One-byte caches: wait until step g's K (is_k) or V codes have landed,
-  // widen them in the stage to bf16 with each row's page parameters, publish
-  // with full_k / full_v.  Rows of pages past the unit's end are left as
+  // widen them in the stage to f16 code values (INT8: with each row's page
+  // zero point), publish with full_k / full_v.  Rows of pages past the unit's end are left as
   // they are (their scores are masked and their V rows cleared).  Whole
   // warp; false on timeout.
   auto widen_pages = [&](bool is_k, const TcUnit& U, const volatile int* pages, int j, uint32_t g) -> bool {
@@ -362,25 +364,18 @@ __global__ void __launch_bounds__(tc_threads(KV), 2)
                                : TcLayout::kV + (g % kTcVStages) * TcLayout::kTile);
       const int np = min(PPI, U.npages - j * PPI);
       const float* sc = is_k ? p.k_scale : p.v_scale;
-      float scale[2];
-      uint32_t zc[2];
+      uint32_t zc[2] = {0u, 0u};
+      if constexpr (KV == PKV_KV_INT8) {
 #pragma unroll
-      for (int rr = 0; rr < 2; ++rr) {
-        const int q = (lane + 32 * rr) / BS;
-        scale[rr] = 0.f;
-        zc[rr] = 0u;
-        if (q < np) {
-          const size_t pi = static_cast<size_t>(pages[j * PPI + q]) * p.Hkv + U.kvh;
-          if constexpr (KV == PKV_KV_INT8) {
-            const float2 sz = __ldg(reinterpret_cast<const float2*>(sc) + pi);
-            scale[rr] = sz.x;
-            zc[rr] = int8_zero_const(sz.y);
-          } else {
-            scale[rr] = __ldg(sc + pi);
+        for (int rr = 0; rr < 2; ++rr) {
+          const int q = (lane + 32 * rr) / BS;
+          if (q < np) {
+            const size_t pi = static_cast<size_t>(pages[j * PPI + q]) * p.Hkv + U.kvh;
+            zc[rr] = int8_zero_const(__ldg(reinterpret_cast<const float2*>(sc) + pi).y);
           }
         }
       }
-      widen_stage<KV, kTcTokens>(st, TcLayout::kRegion, lane, scale, zc, np * BS);
+      widen_stage<KV, kTcTokens>(st, TcLayout::kRegion, lane, zc, np * BS);
       fence_proxy_async_smem();  // the widened rows are read by the tensor cores
       __syncwarp();
       if (lane == 0) mbar_arrive(is_k ? &full_k[g % kTcKStages] : &full_v[g % kTcVStages]);
@@ -431,6 +426,7 @@ __global__ void __launch_bounds__(tc_threads(KV), 2)
         const int* trow = p.block_tables + static_cast<size_t>(b) * p.MB + t0 / BS;
         volatile int* pg = reinterpret_cast<volatile int*>(sm + TcLayout::kSlots + k * TcLayout::kSlot + TcLayout::kSlotPages);
         volatile uint8_t* bd = sm + TcLayout::kSlots + k * TcLayout::kSlot + TcLayout::kSlotBad;
+        float vmax = 0.f;
         for (int q = lane; q < npages; q += 32) {
           int e = __ldg(trow + q);
           const bool isbad = static_cast<unsigned>(e) >= static_cast<unsigned>(p.NB);
@@ -440,6 +436,18 @@ __global__ void __launch_bounds__(tc_threads(KV), 2)
           }
           pg[q] = e;
           bd[q] = isbad ? 1 : 0;
+          if constexpr (kOneByte) {
+            if (!isbad) {
+              const size_t pi = static_cast<size_t>(e) * p.Hkv + kvh;
+              vmax = fmaxf(vmax, fabsf(KV == PKV_KV_INT8 ? __ldg(reinterpret_cast<const float2*>(p.v_scale) + pi).x
+                                                         : __ldg(p.v_scale + pi)));
+            }
+          }
+        }
+        if constexpr (kOneByte) {  // the unit's largest |v_scale| (1 if none): P carries v_scale / it
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(kFull, vmax, o));
+          if (lane == 0) d[5] = __float_as_int(vmax > 0.f ? vmax : 1.f);
         }
         __threadfence_block();
         // the unit's query rows into L2, for the compute warps' TMEM fill
@@ -657,6 +665,46 @@ __global__ void __launch_bounds__(tc_threads(KV), 2)
       }
       tc_st32(t_lane + kTcQCol + 32 * half, w);
     };
+    // one-byte caches: the row as f16, scaled by 2^-kq so that its largest
+    // |q| lies in [2^14, 2^15) (exact for every bf16 value within 2^-10 of
+    // it); returns kq, which the row's softmax coefficient takes back
+    auto put_query = [&](const TcUnit& U) -> int {
+      if constexpr (!kOneByte) {
+        for (int half = 0; half < 2; ++half) {
+          uint4 qv[8];
+          load_query(U, half, qv);
+          store_query(half, qv);
+        }
+        return 0;
+      } else {
+        uint4 qv[2][8];
+        load_query(U, 0, qv[0]);
+        load_query(U, 1, qv[1]);
+        uint32_t mx = 0;  // largest |q| as bf16 bits
+#pragma unroll
+        for (int half = 0; half < 2; ++half)
+#pragma unroll
+          for (int c4 = 0; c4 < 8; ++c4) {
+            const uint32_t w4[4] = {qv[half][c4].x, qv[half][c4].y, qv[half][c4].z, qv[half][c4].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) mx = max(mx, max(w4[e] & 0x7fffu, (w4[e] >> 16) & 0x7fffu));
+          }
+        const int kq = mx == 0 ? 0 : max(-100, min(100, static_cast<int>(mx >> 7) - 127 - 14));
+        const float sc = __uint_as_float(static_cast<uint32_t>(127 - kq) << 23);  // 2^-kq
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t w[32];
+#pragma unroll
+          for (int c4 = 0; c4 < 8; ++c4) {
+            const uint32_t w4[4] = {qv[half][c4].x, qv[half][c4].y, qv[half][c4].z, qv[half][c4].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) w[4 * c4 + e] = pack_f16x2(bf16lo_to_f32(w4[e]) * sc, bf16hi_to_f32(w4[e]) * sc);
+          }
+          tc_st32(t_lane + kTcQCol + 32 * half, w);
+        }
+        return kq;
+      }
+    };
     const float c = p.scale_log2;
     uint32_t nchunk = 0, nfree = 0;  // phases of stg_full, stg_free
     // The unit stays in its slot until these warps release it, so only what
@@ -664,13 +712,10 @@ __global__ void __launch_bounds__(tc_threads(KV), 2)
     // output.
     bool ok = warp_wait(&slot_full[0], 0, true);
     bool more = ok && slot_desc(0)[0] < total_units;
+    int kq_next = 0;  // one-byte caches: the next unit's query exponent of this row
     if (more) {
       const TcUnit U = read_unit(0);
-      for (int half = 0; half < 2; ++half) {
-        uint4 qv[8];
-        load_query(U, half, qv);
-        store_query(half, qv);
-      }
+      kq_next = put_query(U);
       tc_wait_st();
       tc_fence_before_sync();
       __syncwarp();
@@ -679,7 +724,7 @@ __global__ void __launch_bounds__(tc_threads(KV), 2)
     uint32_t g0 = 0;
     for (int i = 0; more; ++i) {
       const int k = i & 1;
-      int nsteps, t0, t1, lim;  // steps, token range, keys of this row: positions < lim
+      int nsteps, t0, t1, lim, kvh_u;  // steps, token range, keys of this row: positions < lim
       bool row_ok;
       {
         const TcUnit U = read_unit(k);
@@ -689,10 +734,18 @@ __global__ void __launch_bounds__(tc_threads(KV), 2)
         t0 = U.t0;
         t1 = U.t1;
         lim = U.ctx - p.T + 1 + t;
+        kvh_u = U.kvh;
       }
       const volatile uint8_t* bad = slot_bad(k);
       bool has_next = false;
       float m = -INFINITY, l = 0.f;  // log2-domain running max (lazy) and sum of this row
+      // one-byte caches: the scores arrive as S' x 2^-kq per row and code
+      // value per key; cq = c 2^kq scales them back (with k_scale per page),
+      // and the softmax works on the scaled scores with coefficient 1
+      const float cq = kOneByte ? c * __uint_as_float(static_cast<uint32_t>(127 + kq_next) << 23) : c;
+      const float cs = kOneByte ? 1.f : c;
+      const float inv_vmax = kOneByte ? 1.f / __int_as_float(slot_desc(k)[5]) : 1.f;
+      const int npages_u = (t1 - t0 + BS - 1) / BS;
 
       // tokens of step j that belong to the sequence (and to a valid page),
       // then those this row attends to (its causal limit)
@@ -710,7 +763,7 @@ __global__ void __launch_bounds__(tc_threads(KV), 2)
       // row whose maximum grew by more than 2^8 (grow) rescales l here and
       // its O by the returned factor once P is written (rescale_o)
       auto update_max = [&](float ext, uint64_t rmask, bool& grow) -> float {
-        const float smax = rmask != 0ull ? ext * c : -INFINITY;
+        const float smax = rmask != 0ull ? ext * cs : -INFINITY;
         const float mnew = fmaxf(m, smax);
         grow = (m == -INFINITY) ? (mnew != -INFINITY) : (mnew > m + 8.f);
         float factor = 1.f;
@@ -764,7 +817,10 @@ __global__ void __launch_bounds__(tc_threads(KV), 2)
       };
       // 32 scores (bit patterns) -> P (bf16, 8 tokens per 16-byte store) at
       // token columns 32 half .. +31 of the step's K stage; returns their sum
-      auto write_p = [&](const uint32_t (&sc)[32], uint32_t hm, bool all32, uint8_t* pbuf, int half) -> float {
+      // (one-byte caches: P in f16 times v_scale / v_max of the token's page;
+      // va for tokens 0-15 of the 32, vb for 16-31)
+      auto write_p = [&](const uint32_t (&sc)[32], uint32_t hm, bool all32, uint8_t* pbuf, int half, float va,
+                         float vb) -> float {
         const float neg_m = (m == -INFINITY) ? 0.f : -m;
         float psum = 0.f;
         // the common all-valid case without per-element mask tests (kept out
@@ -776,10 +832,11 @@ __global__ void __launch_bounds__(tc_threads(KV), 2)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int kk = 8 * k8 + 2 * e;
-              const float p0 = ex2_approx(fmaf(__uint_as_float(sc[kk]), c, neg_m));
-              const float p1 = ex2_approx(fmaf(__uint_as_float(sc[kk + 1]), c, neg_m));
+              const float p0 = ex2_approx(fmaf(__uint_as_float(sc[kk]), cs, neg_m));
+              const float p1 = ex2_approx(fmaf(__uint_as_float(sc[kk + 1]), cs, neg_m));
               psum += p0 + p1;
-              pw[e] = pack_bf16x2(p0, p1);
+              const float vq = kk < 16 ? va : vb;
+              pw[e] = kOneByte ? pack_f16x2(p0 * vq, p1 * vq) : pack_bf16x2(p0, p1);
             }
             *reinterpret_cast<uint4*>(pbuf + tc_p_off(tid, 4 * half + k8)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
           }
@@ -791,12 +848,13 @@ __global__ void __launch_bounds__(tc_threads(KV), 2)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int kk = 8 * k8 + 2 * e;
-            float p0 = ex2_approx(fmaf(__uint_as_float(sc[kk]), c, neg_m));
-            float p1 = ex2_approx(fmaf(__uint_as_float(sc[kk + 1]), c, neg_m));
+            float p0 = ex2_approx(fmaf(__uint_as_float(sc[kk]), cs, neg_m));
+            float p1 = ex2_approx(fmaf(__uint_as_float(sc[kk + 1]), cs, neg_m));
             p0 = ((hm >> kk) & 1u) ? p0 : 0.f;
             p1 = ((hm >> (kk + 1)) & 1u) ? p1 : 0.f;
             psum += p0 + p1;
-            pw[e] = pack_bf16x2(p0, p1);
+            const float vq = kk < 16 ? va : vb;
+            pw[e] = kOneByte ? pack_f16x2(p0 * vq, p1 * vq) : pack_bf16x2(p0, p1);
           }
           *reinterpret_cast<uint4*>(pbuf + tc_p_off(tid, 4 * half + k8)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
         }
@@ -812,6 +870,26 @@ __global__ void __launch_bounds__(tc_threads(KV), 2)
         const uint32_t g = g0 + j;
         uint64_t vmask, rmask;
         step_masks(j, vmask, rmask);  // independent of S: computed while it is on its way
+        // one-byte caches: the step's pages' score coefficients and P factors
+        // (pages past the unit's end: 0, their tokens are masked)
+        float ckq[PPI], vrq[PPI];
+#pragma unroll
+        for (int q = 0; q < PPI; ++q) {
+          ckq[q] = 0.f;
+          vrq[q] = 0.f;
+          if constexpr (kOneByte) {
+            if (j * PPI + q < npages_u) {
+              const size_t pi = static_cast<size_t>(slot_pages(k)[j * PPI + q]) * p.Hkv + kvh_u;
+              if constexpr (KV == PKV_KV_INT8) {
+                ckq[q] = cq * __ldg(reinterpret_cast<const float2*>(p.k_scale) + pi).x;
+                vrq[q] = inv_vmax * __ldg(reinterpret_cast<const float2*>(p.v_scale) + pi).x;
+              } else {
+                ckq[q] = cq * __ldg(p.k_scale + pi);
+                vrq[q] = inv_vmax * __ldg(p.v_scale + pi);
+              }
+            }
+          }
+        }
         if (!mbar_wait_bounded(s_done, g & 1u, kWaitLimitNs)) timed_out = true;
         if (__any_sync(kFull, timed_out)) {  // warp-uniform exit (the loads below are collective)
           ok = false;
@@ -828,12 +906,7 @@ __global__ void __launch_bounds__(tc_threads(KV), 2)
           has_next = slot_desc(k ^ 1)[0] < total_units;
           if (has_next) {
             const TcUnit U = read_unit(k ^ 1);
-#pragma unroll 1
-            for (int half = 0; half < 2; ++half) {
-              uint4 qv[8];
-              load_query(U, half, qv);
-              store_query(half, qv);
-            }
+            kq_next = put_query(U);
             tc_wait_st();
             tc_fence_before_sync();
             __syncwarp();
@@ -857,16 +930,21 @@ __global__ void __launch_bounds__(tc_threads(KV), 2)
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(s_free);  // the slot may take S(g + 1)
+        if constexpr (kOneByte) {  // the scaled scores, in log2 units
+#pragma unroll
+          for (int t = 0; t < kTcTokens; ++t) sv[t] = __float_as_uint(__uint_as_float(sv[t]) * ckq[t / BS]);
+        }
         // masked extremum of the raw scores (maximum for a non-negative
         // scale); a step whose tokens are all this row's takes branch-free code
         const bool all = rmask == ~0ull;
+        const bool cpos = kOneByte || c >= 0.f;
         float ext;
         if (all) {
-          if (c >= 0.f)
+          if (cpos)
             ext = tree_ext64<true>(sv);
           else
             ext = tree_ext64<false>(sv);
-        } else if (c >= 0.f) {
+        } else if (cpos) {
           ext = -INFINITY;
 #pragma unroll
           for (int kk = 0; kk < kTcTokens; ++kk)
@@ -884,8 +962,10 @@ __global__ void __launch_bounds__(tc_threads(KV), 2)
           break;
         }
         uint8_t* pbuf = sm + TcLayout::kK + (g % kTcKStages) * TcLayout::kTile;
-        l += write_p(*reinterpret_cast<const uint32_t(*)[32]>(sv), static_cast<uint32_t>(rmask), all, pbuf, 0) +
-             write_p(*reinterpret_cast<const uint32_t(*)[32]>(sv + 32), static_cast<uint32_t>(rmask >> 32), all, pbuf, 1);
+        l += write_p(*reinterpret_cast<const uint32_t(*)[32]>(sv), static_cast<uint32_t>(rmask), all, pbuf, 0, vrq[0],
+                     vrq[16 / BS]) +
+             write_p(*reinterpret_cast<const uint32_t(*)[32]>(sv + 32), static_cast<uint32_t>(rmask >> 32), all, pbuf, 1,
+                     vrq[32 / BS], vrq[48 / BS]);
         if (j > 0 && __any_sync(kFull, grow) && !rescale_o(factor, g)) {
           ok = false;
           break;
@@ -921,7 +1001,7 @@ __global__ void __launch_bounds__(tc_threads(KV), 2)
         // bf16, staged in the last step's K and V stages (16-byte chunks
         // XOR-swizzled by row, as the output map's 128-byte swizzle reads
         // them) and written by thread 0 with one tensor-map store each
-        const float osc = l > 0.f ? 1.f / l : 0.f;
+        const float osc = l > 0.f ? (kOneByte ? __int_as_float(slot_desc(k)[5]) : 1.f) / l : 0.f;
         uint8_t* vbuf = sm + TcLayout::kV + (gl % kTcVStages) * TcLayout::kTile;
 #pragma unroll 1
         for (int k2 = 0; k2 < 2; ++k2, ++nchunk) {
@@ -971,6 +1051,11 @@ __global__ void __launch_bounds__(tc_threads(KV), 2)
           uint32_t ov[32];
           tc_ld32(t_lane + kTcOCol + cc, ov);
           tc_wait_ld();
+          if constexpr (kOneByte) {  // O in value units
+            const float vmx = __int_as_float(slot_desc(i & 1)[5]);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * vmx);
+          }
           if (k >= 2 && !warp_wait(stg_free, (nfree + k - 2) & 1u, false)) {
             timed_out = true;
             break;

@@ -408,6 +408,12 @@ __host__ __device__ constexpr uint32_t tc_idesc_bf16_f32(int M, int N, bool b_mn
   return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn_major ? (1u << 16) : 0u) |
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
+// The same with f16 A and B (both operands of a kind::f16 product have one
+// type).
+__host__ __device__ constexpr uint32_t tc_idesc_f16_f32(int M, int N, bool b_mn_major = false) {
+  return (1u << 4) | (b_mn_major ? (1u << 16) : 0u) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
 
 // D[tmem] (+)= A[smem] . B[smem]^T; issued by one thread.
 __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,

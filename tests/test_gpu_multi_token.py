@@ -432,7 +432,10 @@ def test_tc_one_byte_sweep(dtype, bs, Hq, Hkv, T, lens, ppu):
 
 def _widened_bits(dc, blk, kvh, row):
     """bf16 bits of bf16(fp32(code value) x fp32 scale) ((code - zero) for
-    INT8) of V row `row` of page (blk, kvh): what the widened page holds."""
+    INT8) of V row `row` of page (blk, kvh): the dequantised row, rounded
+    once.  A query row whose only key is that row (weight 1, one page in its
+    unit) gets exactly these bits: the kernel multiplies the exact f16 code
+    value by the page scale once, in fp32."""
     c = dc.c
     codes = dc.v_host[0, blk, kvh, row]
     if c.kv_dtype == "fp8":
