@@ -598,10 +598,16 @@ def time_device(w, steps, warmup, world, mode="eager"):
     return total_ms, kernel_ms, clk.summary()
 
 
+TC_PAIR_WARPS = 11  # warps of the tile-pair tcgen05 kernel (the plan's warps_per_cta)
+
+
 def read_probe_gbs(nbytes=1 << 30, iters=10):
     """The read-only HBM rate of this device: the library's read probe
-    streaming a 1 GiB buffer (larger than L2) once per launch, timed with
-    CUDA events around each launch after three warm-up launches."""
+    streaming an `nbytes` buffer (larger than L2) once per launch, timed with
+    CUDA events around each launch after three warm-up launches.  Taken at
+    the decode's own byte count, it carries the same launch, ramp-up and
+    drain as the decode: the rate a one-pass read of that many bytes can
+    reach on this device."""
     import paged_kv_cache_274_gb300 as pkv
     buf = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
     out = torch.zeros(1, dtype=torch.int64, device="cuda")
@@ -849,7 +855,8 @@ def run_ours(args, rank, world):
     per_call_logical = w.kv_bytes_logical if copy else kv_bytes_of(c, layers=[0])
     k_ms = statistics.mean(kernel_ms)
     achieved = per_call_bytes / (k_ms * 1e-3) / 1e9
-    probe_gbs, probe_ms = read_probe_gbs()
+    probe_bytes = (per_call_bytes // 4096) * 4096 if per_call_bytes >= (256 << 20) else (1 << 30)
+    probe_gbs, probe_ms = read_probe_gbs(probe_bytes)
     e2e = None
     if not args.no_e2e and not copy:
         # enough steps that the pipeline's fill and drain (one upload, one
@@ -904,16 +911,18 @@ def run_ours(args, rank, world):
             "pct_of_hbm_peak": 100.0 * value / peak,
             "pct_of_nominal_8tbs": 100.0 * value / 8000.0,
             "roofline": {**bound_fields, "kernel": "copy_blocks_kernel" if copy else
-                         ("paged_decode_tc_kernel" if plan["math"] == 3 else "paged_decode_kernel"),
+                         (("paged_decode_tc2_kernel" if plan["warps_per_cta"] == TC_PAIR_WARPS else "paged_decode_tc_kernel")
+                          if plan["math"] == 3 else "paged_decode_kernel"),
                          "traffic": profile_traffic(args.workload, {1: "ffma", 2: "mma", 3: "tc"}.get(plan["math"], "mma")),
                          "algorithmic_bytes_per_launch": per_call_bytes,
                          "logical_bytes_per_launch": per_call_logical,
                          "logical_gbs": per_call_logical / (k_ms * 1e-3) / 1e9,
                          "kernel_ms_mean": k_ms, "kernel_ms_median": statistics.median(kernel_ms)},
-            "hbm_read_probe": {"gbs": probe_gbs, "ms": probe_ms, "bytes": 1 << 30, "kernel": "read_probe_kernel",
+            "hbm_read_probe": {"gbs": probe_gbs, "ms": probe_ms, "bytes": probe_bytes, "kernel": "read_probe_kernel",
                                "frac_of_copy_peak": probe_gbs / peak,
                                "kernel_frac_of_read_probe": achieved / probe_gbs,
-                               "note": "read-only streaming rate of this device (the decode's own ceiling); "
+                               "note": "read-only streaming rate of this device over the decode's own byte count "
+                                       "(same launch, ramp-up and drain: the decode's own ceiling); "
                                        "the roofline peak stays the measured copy rate"},
             "cpu_baseline": cpu,
             "e2e": e2e,
