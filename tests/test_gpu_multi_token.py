@@ -430,6 +430,36 @@ def test_tc_one_byte_sweep(dtype, bs, Hq, Hkv, T, lens, ppu):
     assert_close(bf16_dev_to_f64(out), _oracle(dc, q), f"tc {dtype} T={T} G={Hq // Hkv} bs={bs} ppu={ppu}")
 
 
+@pytest.mark.parametrize("dtype", ["fp8", "int8a"])
+@pytest.mark.parametrize("ppu", [0, 3])
+def test_tc_one_byte_wide_scales(dtype, ppu):
+    # per-page scales spread over three decades within one sequence (V pages
+    # scaled by 1e-3 .. 1, K pages by 0.1 .. 3), values O(1): P carries
+    # v_scale / v_max of its page in f16, which keeps 11 bits down to a
+    # ratio of 2^-14 of a weight; the oracle dequantises the same bytes
+    from workloads import bf16_bits_to_f32, bf16_bits_from_f32, fp8_tile_scales, int8_tile_params
+    c = random_case(1480 + ppu, 3, 16, 4, 128, 32, [600, 333, 64], kv_dtype=dtype)
+    rng = np.random.Generator(np.random.PCG64(1481))
+    fv = (10.0 ** rng.uniform(-3, 0, size=(1, c.NB, 1, 1, 1))).astype(np.float32)
+    fk = rng.uniform(0.1, 3.0, size=(1, c.NB, 1, 1, 1)).astype(np.float32)
+    c.k_src = bf16_bits_from_f32(bf16_bits_to_f32(c.k_src) * fk)
+    c.v_src = bf16_bits_from_f32(bf16_bits_to_f32(c.v_src) * fv)
+    if dtype == "fp8":
+        c.k_scale, c.v_scale = fp8_tile_scales(c.k_src), fp8_tile_scales(c.v_src)
+    else:
+        c.k_scale, c.v_scale = int8_tile_params(c.k_src, False), int8_tile_params(c.v_src, False)
+    dc = DeviceCase(c)
+    T = 32
+    q = _q(1482 + ppu, c.B, T, 16, 128)
+    plan = pkv.decode_plan(dc.k, c.B, 16, c.MB, _tc_opts(ppu), T)
+    assert plan["math"] == pkv.MATH_TC
+    out = pkv.paged_decode_multi(to_dev_bf16(q), dc.k, dc.v, dc.bt, dc.cl, [0], 0, c.scale,
+                                 k_scale=dc.ks, v_scale=dc.vs, opts=_tc_opts(ppu))
+    torch.cuda.synchronize()
+    assert pkv.read_device_error() == 0
+    assert_close(bf16_dev_to_f64(out), _oracle(dc, q), f"tc {dtype} wide scales ppu={ppu}")
+
+
 def _widened_bits(dc, blk, kvh, row):
     """bf16 bits of bf16(fp32(code value) x fp32 scale) ((code - zero) for
     INT8) of V row `row` of page (blk, kvh): the dequantised row, rounded
