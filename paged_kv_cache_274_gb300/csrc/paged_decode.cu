@@ -55,7 +55,8 @@ constexpr int kFusedMergeMaxParts = 4;
 template <int KV>
 __global__ void __launch_bounds__(kPlanThreads)
     plan_kernel(const int32_t* __restrict__ context_lens, int B, int num_arrive /* B * Hkv * NT */,
-                int max_ctx, int tokens_per_part, int32_t* work_counter, int32_t* unit_start,
+                int max_ctx, int tokens_per_part, int half_from /* sequences from here: */,
+                int tokens_per_part_half /* partitions of this many tokens */, int32_t* work_counter, int32_t* unit_start,
                 int32_t* ctx_eff, int32_t* part_seq, int32_t* arrive, __nv_bfloat16* out,
                 int row_elems /* T * Hq * D */, unsigned* err, const AppendArgs app) {
   __shared__ int warp_tot[kPlanThreads / 32];
@@ -83,7 +84,8 @@ __global__ void __launch_bounds__(kPlanThreads)
         c = 0;
       }
       ctx_eff[b] = c;
-      parts = (c + tokens_per_part - 1) / tokens_per_part;
+      const int tpp = b >= half_from ? tokens_per_part_half : tokens_per_part;
+      parts = (c + tpp - 1) / tpp;
     }
     // inclusive scan within the warp, then across warps
     int x = parts;
@@ -146,7 +148,7 @@ template <int D>
 __global__ void __launch_bounds__(kMergeThreads)
     merge_kernel(const float* __restrict__ part_ml, const float* __restrict__ part_o,
                  const int32_t* __restrict__ unit_start, int rows_per_seq /* T * Hq */,
-                 int pmax, __nv_bfloat16* __restrict__ out) {
+                 int pmax, int row0, __nv_bfloat16* __restrict__ out) {
   constexpr int kDG = D / 4;                  // threads along head_dim
   constexpr int kPG = kMergeThreads / kDG;    // partition groups
   constexpr int kBatch = 4;                   // partitions in flight per thread
@@ -155,7 +157,7 @@ __global__ void __launch_bounds__(kMergeThreads)
   __shared__ float s_max[kMergeThreads / 32];
   pdl_trigger();
   pdl_wait();
-  const int bh = blockIdx.x;  // row (b * T + t) * Hq + h
+  const int bh = row0 + blockIdx.x;  // row (b * T + t) * Hq + h
   const int b = bh / rows_per_seq;
   const int P = unit_start[b + 1] - unit_start[b];
   if (P < 2) return;  // written by the decode kernel (or zero-filled by the planner)
@@ -237,12 +239,12 @@ template <int D>
 __global__ void __launch_bounds__(kMergeRowsPerCta * 32)
     merge_rows_kernel(const float* __restrict__ part_ml, const float* __restrict__ part_o,
                       const int32_t* __restrict__ unit_start, int rows_per_seq /* T * Hq */,
-                      int pmax, int num_rows, __nv_bfloat16* __restrict__ out) {
+                      int pmax, int row0, int num_rows, __nv_bfloat16* __restrict__ out) {
   constexpr int kPer = D / 32;  // columns per lane
   pdl_trigger();
   pdl_wait();
   const int lane = threadIdx.x & 31;
-  const int row = blockIdx.x * kMergeRowsPerCta + (threadIdx.x >> 5);  // (b * T + t) * Hq + h
+  const int row = row0 + blockIdx.x * kMergeRowsPerCta + (threadIdx.x >> 5);  // (b * T + t) * Hq + h
   if (row >= num_rows) return;
   const int b = row / rows_per_seq;
   const int P = unit_start[b + 1] - unit_start[b];
@@ -431,7 +433,7 @@ cudaError_t launch_decode(const DecodeLaunch& L, int* launched) {
                 : L.append_kind == PKV_KV_FP8_E4M3  ? plan_kernel<PKV_KV_FP8_E4M3>
                                                     : plan_kernel<PKV_KV_BF16>;
     e = cudaLaunchKernelEx(&cfg, plan, L.context_lens, L.B, L.B * L.Hkv * L.NT, L.MB * L.bs,
-                           L.ppu * L.bs, L.work_counter, L.unit_start, L.ctx_eff, L.part_seq, L.arrive,
+                           L.ppu * L.bs, L.half_from, L.ppu_half * L.bs, L.work_counter, L.unit_start, L.ctx_eff, L.part_seq, L.arrive,
                            static_cast<__nv_bfloat16*>(L.out), L.T * L.Hq * L.D, L.err, app);
     if (e != cudaSuccess) return e;
     *launched += 1;
@@ -475,6 +477,8 @@ cudaError_t launch_decode(const DecodeLaunch& L, int* launched) {
   p.NB = L.NB;
   p.pmax = L.pmax;
   p.ppu = L.ppu;
+  p.half_from = L.half_from;
+  p.ppu_half = L.ppu_half;
   p.stages = L.stages;
   // the tcgen05 kernel leaves every split-K merge to the merge kernels
   p.fused_merge = (!L.tc && L.pmax <= kFusedMergeMaxParts) ? 1 : 0;
@@ -504,9 +508,14 @@ cudaError_t launch_decode(const DecodeLaunch& L, int* launched) {
   //    up to 32 partitions, a CTA per row beyond
   if (!p.fused_merge && L.pmax > 1) {
     const int rows = L.B * L.T * L.Hq;
+    // with one partition of ppu >= MB blocks per sequence, only the
+    // half-length sequences (half_from ..) have partials: merge their rows
+    const int row0 = (L.ppu >= L.MB && L.half_from < L.B) ? L.half_from * L.T * L.Hq : 0;
+    const int merge_rows = rows - row0;
     const bool by_warp = L.pmax <= kMergeWarpMaxParts;
     cudaLaunchConfig_t mc{};
-    mc.gridDim = dim3(static_cast<unsigned>(by_warp ? (rows + kMergeRowsPerCta - 1) / kMergeRowsPerCta : rows));
+    mc.gridDim =
+        dim3(static_cast<unsigned>(by_warp ? (merge_rows + kMergeRowsPerCta - 1) / kMergeRowsPerCta : merge_rows));
     mc.blockDim = dim3(by_warp ? kMergeRowsPerCta * 32 : kMergeThreads);
     mc.dynamicSmemBytes = 0;
     mc.stream = L.stream;
@@ -518,11 +527,11 @@ cudaError_t launch_decode(const DecodeLaunch& L, int* launched) {
     __nv_bfloat16* o = static_cast<__nv_bfloat16*>(L.out);
     const int rps = L.T * L.Hq;
     if (by_warp)
-      e = L.D == 64 ? cudaLaunchKernelEx(&mc, merge_rows_kernel<64>, pml, po, us, rps, L.pmax, rows, o)
-                    : cudaLaunchKernelEx(&mc, merge_rows_kernel<128>, pml, po, us, rps, L.pmax, rows, o);
+      e = L.D == 64 ? cudaLaunchKernelEx(&mc, merge_rows_kernel<64>, pml, po, us, rps, L.pmax, row0, rows, o)
+                    : cudaLaunchKernelEx(&mc, merge_rows_kernel<128>, pml, po, us, rps, L.pmax, row0, rows, o);
     else
-      e = L.D == 64 ? cudaLaunchKernelEx(&mc, merge_kernel<64>, pml, po, us, rps, L.pmax, o)
-                    : cudaLaunchKernelEx(&mc, merge_kernel<128>, pml, po, us, rps, L.pmax, o);
+      e = L.D == 64 ? cudaLaunchKernelEx(&mc, merge_kernel<64>, pml, po, us, rps, L.pmax, row0, o)
+                    : cudaLaunchKernelEx(&mc, merge_kernel<128>, pml, po, us, rps, L.pmax, row0, o);
     if (e != cudaSuccess) return e;
     *launched += 1;
   }

@@ -61,6 +61,7 @@ struct DecodeParams {
   int32_t* arrive;  // [B][Hkv] partitions finished so far (zeroed by the planner)
   unsigned* err;
   int B, Hq, Hkv, G, MB, NB, pmax, ppu, stages;
+  int half_from, ppu_half;  // sequences b >= half_from: partitions of ppu_half blocks
   int T, Tt, NT;  // query tokens per sequence, per row tile; row tiles
   int fused_merge;  // 1: the last warp of a (sequence, KV head) merges; 0: the merge kernel does
   int row_base;

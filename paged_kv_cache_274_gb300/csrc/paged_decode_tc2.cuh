@@ -222,7 +222,9 @@ __global__ void __launch_bounds__(kT2Threads, 1)
   const int NP = (p.NT + 1) >> 1;  // tile pairs per KV head
   const int units_per_part = p.Hkv * NP;
   const int total_units = p.unit_start[p.B] * units_per_part;
-  const int ppu_tokens = p.ppu * BS;
+  // partition length of sequence b in tokens (the planner's half-length
+  // partitions for the last sequences balance the last round of units)
+  auto ppu_tokens_of = [&](int b) { return (b >= p.half_from ? p.ppu_half : p.ppu) * BS; };
   const uint32_t q_tile_bytes = 2u * 128u * static_cast<uint32_t>(p.G * p.Tt);  // both d halves
   bool timed_out = false;
   uint32_t copies_end = 0, mma_issued = 0, q_loads = 0;  // for the drain after a timeout
@@ -248,6 +250,7 @@ __global__ void __launch_bounds__(kT2Threads, 1)
     const int rem = U.u - part * units_per_part;
     U.kvh = rem / NP;
     U.tile = 2 * (rem - U.kvh * NP);  // first tile of the pair
+    const int ppu_tokens = ppu_tokens_of(U.b);
     U.t0 = U.pidx * ppu_tokens;
     U.t1 = min(U.ctx, U.t0 + ppu_tokens);
     U.npages = (U.t1 - U.t0 + BS - 1) / BS;
@@ -296,6 +299,7 @@ __global__ void __launch_bounds__(kT2Threads, 1)
         const int rem = u - (u / units_per_part) * units_per_part;
         kvh = rem / NP;
         const int tile0 = 2 * (rem - kvh * NP);
+        const int ppu_tokens = ppu_tokens_of(b);
         const int t0 = pidx * ppu_tokens;
         npages = (min(ctx, t0 + ppu_tokens) - t0 + BS - 1) / BS;  // 1 .. kTcMaxPages
         nsteps = (npages + PPI - 1) / PPI;

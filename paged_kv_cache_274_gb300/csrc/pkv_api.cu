@@ -432,6 +432,7 @@ static pkv_status resolve_decode(const pkv_cache_desc* c, int32_t batch, int32_t
   // page table for the tcgen05 kernel
   const int ppu_max = tc ? pkv::kTcUnitMaxPages : 64;
   if (ppu < 0 || ppu > ppu_max) return fail(PKV_ERR_INVALID_ARG, "partition_blocks %d outside 1..%d", ppu, ppu_max);
+  const bool auto_ppu = ppu == 0;
   if (ppu == 0) {
     // The decode is a persistent grid of W streaming warps pulling units of
     // work; its time follows how full the last round of units is.  Estimate
@@ -504,6 +505,23 @@ static pkv_status resolve_decode(const pkv_cache_desc* c, int32_t batch, int32_t
   ppu = std::min(ppu, MB);
   if ((MB + ppu - 1) / ppu > 65536)
     return fail(PKV_ERR_UNSUPPORTED, "more than 65536 partitions per sequence; raise partition_blocks");
+  // The tile-pair kernel runs one unit per SM at a time, units of equal
+  // length: when the last round of units would be at most half full, the
+  // last sequences take partitions of half the length, so that the last
+  // round's work spreads over twice as many units (with S sequences halved,
+  // S >= r / u: the r units of the last round become at least 2r half
+  // units).  Counted for sequences of the longest allowed context; with
+  // shorter ones the split is still valid, only less useful.
+  int half_from = batch, ppu_half = ppu;
+  if (tc2 && auto_ppu && ppu >= 2 && env_int("PKV_TC_BALANCE", 1) != 0) {
+    const long long u = static_cast<long long>((MB + ppu - 1) / ppu) * c->num_kv_heads * ((NT + 1) / 2);
+    const long long n = static_cast<long long>(std::max(batch, 1)) * u;
+    const long long r = n % num_sms;
+    if (r > 0 && 2 * r <= num_sms) {
+      half_from = batch - static_cast<int>(std::min<long long>(batch, (r + u - 1) / u));
+      ppu_half = (ppu + 1) / 2;
+    }
+  }
   *L = pkv::DecodeLaunch{};
   L->B = batch;
   L->Hq = Hq;
@@ -521,7 +539,9 @@ static pkv_status resolve_decode(const pkv_cache_desc* c, int32_t batch, int32_t
   L->kv_fp8 = fp8;
   L->kv_dtype = c->dtype;
   L->ppu = ppu;
-  L->pmax = (MB + ppu - 1) / ppu;
+  L->half_from = half_from;
+  L->ppu_half = ppu_half;
+  L->pmax = (MB + ppu_half - 1) / ppu_half;  // ppu_half == ppu without half-length partitions
   L->math = math;
   L->warps = warps;
   L->stages = stages;

@@ -51,8 +51,11 @@ struct DecodeLaunch {
   int tc2; // 1: the tcgen05 kernel that serves a pair of row tiles per CTA (NT >= 2)
   int kv_fp8;    // one-byte elements (E4M3 or INT8)
   int kv_dtype;  // pkv_kv_dtype
-  int pmax;  // max partitions of a sequence (ceil(MB / ppu))
+  int pmax;  // max partitions of a sequence (ceil(MB / ppu), or ceil(MB / ppu_half))
   int ppu;   // pages (blocks) per partition
+  // sequences half_from .. B - 1 take partitions of ppu_half blocks (the
+  // tile-pair kernel's balancing of the last round of units; B: none)
+  int half_from, ppu_half;
   int row_base;  // first tensor-map row of the selected slot
   float scale_log2;
   int math;    // PKV_MATH_FFMA or PKV_MATH_MMA (resolved)
