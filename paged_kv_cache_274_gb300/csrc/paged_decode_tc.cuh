@@ -826,21 +826,32 @@ __global__ void __launch_bounds__(tc_threads(KV), 2)
         // the common all-valid case without per-element mask tests (kept out
         // of the unrolled loop: they cost ALU issue slots on every score)
         if (all32) {
+          // arguments, sums (and the one-byte P factors) by packed pair
+          // instructions: one issue slot for two scores
+          float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
           for (int k8 = 0; k8 < 4; ++k8) {
             uint32_t pw[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int kk = 8 * k8 + 2 * e;
-              const float p0 = ex2_approx(fmaf(__uint_as_float(sc[kk]), cs, neg_m));
-              const float p1 = ex2_approx(fmaf(__uint_as_float(sc[kk + 1]), cs, neg_m));
-              psum += p0 + p1;
-              const float vq = kk < 16 ? va : vb;
-              pw[e] = kOneByte ? pack_f16x2(p0 * vq, p1 * vq) : pack_bf16x2(p0, p1);
+              float a0, a1;
+              ffma2(a0, a1, __uint_as_float(sc[kk]), __uint_as_float(sc[kk + 1]), cs, cs, neg_m, neg_m);
+              const float p0 = ex2_approx(a0);
+              const float p1 = ex2_approx(a1);
+              fadd2(ps0, ps1, ps0, ps1, p0, p1);
+              if constexpr (kOneByte) {
+                const float vq = kk < 16 ? va : vb;
+                float q0, q1;
+                fmul2(q0, q1, p0, p1, vq, vq);
+                pw[e] = pack_f16x2(q0, q1);
+              } else {
+                pw[e] = pack_bf16x2(p0, p1);
+              }
             }
             *reinterpret_cast<uint4*>(pbuf + tc_p_off(tid, 4 * half + k8)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
           }
-          return psum;
+          return ps0 + ps1;
         }
 #pragma unroll
         for (int k8 = 0; k8 < 4; ++k8) {

@@ -555,16 +555,21 @@ __global__ void __launch_bounds__(kT2Threads, 1)
             l *= factor;
             m = smax;
           }
-          // P = 2^(s c - m) as bf16 pairs over columns 0 .. 63 of S
+          // P = 2^(s c - m) as bf16 pairs over columns 0 .. 63 of S; the
+          // arguments and the two running sums by packed pair instructions
+          // (one issue slot for two scores: the exponential phase is bound
+          // by issue, measured 7% faster at T = 64 and 128)
           const float neg_m = (m == -INFINITY) ? 0.f : -m;
           float ps[2] = {0.f, 0.f};  // two partial sums: shorter dependency chains
           auto write_p = [&](const uint32_t (&x)[32], int col) {
             uint32_t pw[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-              const float p0 = ex2_approx(fmaf(__uint_as_float(x[2 * e]), c, neg_m));
-              const float p1 = ex2_approx(fmaf(__uint_as_float(x[2 * e + 1]), c, neg_m));
-              ps[e & 1] += p0 + p1;
+              float a0, a1;
+              ffma2(a0, a1, __uint_as_float(x[2 * e]), __uint_as_float(x[2 * e + 1]), c, c, neg_m, neg_m);
+              const float p0 = ex2_approx(a0);
+              const float p1 = ex2_approx(a1);
+              fadd2(ps[0], ps[1], ps[0], ps[1], p0, p1);
               pw[e] = pack_bf16x2(p0, p1);
             }
             tc_st16(t_s + col, pw);

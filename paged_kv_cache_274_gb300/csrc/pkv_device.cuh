@@ -311,6 +311,37 @@ __device__ __forceinline__ void mma_f16_lo(float (&d)[2], uint32_t a0, uint32_t 
 
 // 2^x with the SFU's approximate exponential (relative error about 2^-22;
 // results below 2^-126 flush to zero, -inf gives 0).
+// Packed pairs of fp32 operations (one instruction for two lanes of work on
+// sm_100 and later): d = a * b + c and d = a + b, element-wise, round to
+// nearest even, as two separate fmaf / multiplications / additions would
+// round them.
+__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0,
+                                      float c1) {
+  uint64_t d;
+  asm("{\n .reg .b64 ra, rb, rc;\n mov.b64 ra, {%1, %2};\n mov.b64 rb, {%3, %4};\n mov.b64 rc, {%5, %6};\n"
+      " fma.rn.f32x2 %0, ra, rb, rc;\n}\n"
+      : "=l"(d)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+  d0 = __uint_as_float(static_cast<uint32_t>(d));
+  d1 = __uint_as_float(static_cast<uint32_t>(d >> 32));
+}
+__device__ __forceinline__ void fmul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  uint64_t d;
+  asm("{\n .reg .b64 ra, rb;\n mov.b64 ra, {%1, %2};\n mov.b64 rb, {%3, %4};\n mul.rn.f32x2 %0, ra, rb;\n}\n"
+      : "=l"(d)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+  d0 = __uint_as_float(static_cast<uint32_t>(d));
+  d1 = __uint_as_float(static_cast<uint32_t>(d >> 32));
+}
+__device__ __forceinline__ void fadd2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  uint64_t d;
+  asm("{\n .reg .b64 ra, rb;\n mov.b64 ra, {%1, %2};\n mov.b64 rb, {%3, %4};\n add.rn.f32x2 %0, ra, rb;\n}\n"
+      : "=l"(d)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+  d0 = __uint_as_float(static_cast<uint32_t>(d));
+  d1 = __uint_as_float(static_cast<uint32_t>(d >> 32));
+}
+
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
