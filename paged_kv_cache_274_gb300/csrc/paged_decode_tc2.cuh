@@ -619,7 +619,7 @@ __global__ void __launch_bounds__(kT2Threads, 1)
             m = smax;
           }
           const float neg_m = (m == -INFINITY) ? 0.f : -m;
-          float psum = 0.f;
+          float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll 1
           for (int cq = 0; cq < 4; ++cq) {
             uint32_t x[32];
@@ -630,16 +630,18 @@ __global__ void __launch_bounds__(kT2Threads, 1)
             uint32_t pw[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-              float p0 = ex2_approx(fmaf(__uint_as_float(x[2 * e]), c, neg_m));
-              float p1 = ex2_approx(fmaf(__uint_as_float(x[2 * e + 1]), c, neg_m));
+              float a0, a1;
+              ffma2(a0, a1, __uint_as_float(x[2 * e]), __uint_as_float(x[2 * e + 1]), c, c, neg_m, neg_m);
+              float p0 = ex2_approx(a0);
+              float p1 = ex2_approx(a1);
               p0 = ((mk >> (2 * e)) & 1u) ? p0 : 0.f;
               p1 = ((mk >> (2 * e + 1)) & 1u) ? p1 : 0.f;
-              psum += p0 + p1;
+              fadd2(ps0, ps1, ps0, ps1, p0, p1);
               pw[e] = pack_bf16x2(p0, p1);
             }
             tc_st16(t_s + 16 * cq, pw);
           }
-          l += psum;
+          l += ps0 + ps1;
         }
         // O of the earlier steps, rarely (quiescent: PV_i(g - 1) finished
         // before S_i(g), and PV_i(g) waits for this step's p_full)
