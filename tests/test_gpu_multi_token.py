@@ -367,6 +367,35 @@ def test_tc_prefill_chunks(T, ppu):
     assert_close(bf16_dev_to_f64(out), want, f"prefill T={T} ppu={ppu}")
 
 
+@pytest.mark.parametrize("B,lens_hi", [(24, 4096), (40, 2600), (9, 700)])
+def test_tc_pair_half_length_partitions(B, lens_hi):
+    # the tile-pair kernel's last-round balancing: with automatic partitions
+    # and a last round of units at most half full, the last sequences take
+    # partitions of half the length and the merge covers their rows only;
+    # ragged lengths (some shorter than one partition), every element
+    # against the oracle
+    Hq, Hkv, T = 32, 8, 64
+    rng = np.random.Generator(np.random.PCG64(1200 + B))
+    lens = [int(x) for x in rng.integers(T, lens_hi + 1, size=B)]
+    lens[-1] = lens_hi
+    c = random_case(1201 + B, B, Hq, Hkv, 128, 16, lens, poison=True)
+    dc = DeviceCase(c)
+    q = _q(1202 + B, c.B, T, Hq, 128)
+    plan = pkv.decode_plan(dc.k, c.B, Hq, c.MB, _tc_opts(0), T)
+    assert plan["math"] == pkv.MATH_TC and plan["row_tiles"] == 2
+    full = (c.MB + plan["partition_blocks"] - 1) // plan["partition_blocks"]
+    units = B * full * Hkv   # pair units at the longest context
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    halved = 0 < units % sms <= sms // 2
+    assert (plan["max_partitions"] > full) == halved, (units, sms, plan)
+    out = pkv.paged_decode_multi(to_dev_bf16(q), dc.k, dc.v, dc.bt, dc.cl, [0], 0, c.scale, opts=_tc_opts(0))
+    torch.cuda.synchronize()
+    assert pkv.read_device_error() == 0
+    want = oracle.paged_decode_multi_gemm(q, dc.k_host, dc.v_host, c.block_tables, c.context_lens,
+                                          c.kv_group_ptr, 0, c.scale)
+    assert_close(bf16_dev_to_f64(out), want, f"half-length partitions B={B}")
+
+
 def test_tc_pair_matches_one_tile_kernel():
     # the pair kernel and the one-tile kernel (PKV_TC_PAIR=0 in a child
     # process) compute the same products; their outputs agree to rounding
