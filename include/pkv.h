@@ -113,7 +113,11 @@ typedef enum {
 typedef struct {
   int32_t partition_blocks; /* blocks per split-K partition, 1..64, or 1..256 for
                                PKV_MATH_TC (0 = auto; auto may take 128 or 256 for
-                               PKV_MATH_TC) */
+                               PKV_MATH_TC); with automatic partitions the tile-pair
+                               tcgen05 kernel may give the last sequences
+                               partitions of half this length, so that the
+                               last round of its units is not left under half
+                               full */
   int32_t math;             /* pkv_decode_math */
   int32_t warps_per_cta;    /* 1..8 (0 = auto) */
   int32_t stages;           /* pages in each warp's copy ring, 2..8 (0 = auto) */
@@ -166,7 +170,8 @@ size_t pkv_decode_workspace_bytes(const pkv_cache_desc* cache, int32_t batch,
 /* The launch plan pkv_paged_decode would use for these sizes and options. */
 typedef struct {
   int32_t partition_blocks;  /* blocks per split-K partition */
-  int32_t max_partitions;    /* partitions of a max_blocks_per_seq-block sequence */
+  int32_t max_partitions;    /* partitions of a max_blocks_per_seq-block sequence
+                                (at half-length partitions where those apply) */
   int32_t math;              /* resolved pkv_decode_math */
   int32_t warps_per_cta;
   int32_t stages;
