@@ -151,13 +151,17 @@ struct TcUnit {
 // Widen 16 one-byte codes (a 16-byte chunk, element i in byte i) to their
 // f16 code values (E4M3 value, INT8 code - zero; both exact in f16) as two
 // 16-byte chunks.
-template <int KV>
+// kBiased (INT8 K pages): 1152 + code instead, two instructions fewer per
+// four codes; the compute warps take (1152 + zero) x sum(q) off the scores.
+template <int KV, bool kBiased = false>
 __device__ __forceinline__ void widen16(const uint4 c, uint32_t zc, uint4& o0, uint4& o1) {
   const uint32_t w[4] = {c.x, c.y, c.z, c.w};
   uint32_t r[8];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    if constexpr (KV == PKV_KV_INT8)
+    if constexpr (KV == PKV_KV_INT8 && kBiased)
+      int8x4_to_f16x2x2_biased(w[q], r[2 * q], r[2 * q + 1]);
+    else if constexpr (KV == PKV_KV_INT8)
       int8x4_to_f16x2x2(w[q], zc, r[2 * q], r[2 * q + 1]);
     else
       e4m3x4_to_f16x2x2(w[q], r[2 * q], r[2 * q + 1]);
@@ -173,7 +177,7 @@ __device__ __forceinline__ void widen16(const uint4 c, uint32_t zc, uint4& o0, u
 // constant.  One warp; lane l takes rows l, l + 32, ...: the lower half
 // first (codes 0-63 of every row), then the upper half row by row, each
 // row's last codes read before its row is overwritten.
-template <int KV, int ROWS>
+template <int KV, int ROWS, bool kBiased = false>
 __device__ __forceinline__ void widen_stage(uint8_t* stage, uint32_t region, int lane, const uint32_t (&zc)[ROWS / 32],
                                             int valid_rows) {
 #pragma unroll
@@ -186,7 +190,7 @@ __device__ __forceinline__ void widen_stage(uint8_t* stage, uint32_t region, int
     for (int c = 0; c < 4; ++c) {
       const uint4 codes = *reinterpret_cast<const uint4*>(src + ((c ^ (r & 7)) << 4));
       uint4 o0, o1;
-      widen16<KV>(codes, zc[rr], o0, o1);
+      widen16<KV, kBiased>(codes, zc[rr], o0, o1);
       *reinterpret_cast<uint4*>(dst + (((2 * c) ^ (r & 7)) << 4)) = o0;
       *reinterpret_cast<uint4*>(dst + (((2 * c + 1) ^ (r & 7)) << 4)) = o1;
     }
@@ -202,7 +206,7 @@ __device__ __forceinline__ void widen_stage(uint8_t* stage, uint32_t region, int
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       uint4 o0, o1;
-      widen16<KV>(codes[c], zc[rr], o0, o1);
+      widen16<KV, kBiased>(codes[c], zc[rr], o0, o1);
       *reinterpret_cast<uint4*>(row + (((2 * c) ^ (r & 7)) << 4)) = o0;
       *reinterpret_cast<uint4*>(row + (((2 * c + 1) ^ (r & 7)) << 4)) = o1;
     }
@@ -366,16 +370,22 @@ __global__ void __launch_bounds__(tc_threads(KV), 2)
       const float* sc = is_k ? p.k_scale : p.v_scale;
       uint32_t zc[2] = {0u, 0u};
       if constexpr (KV == PKV_KV_INT8) {
+        if (is_k) {  // K: biased code values, no zero points
+          widen_stage<KV, kTcTokens, true>(st, TcLayout::kRegion, lane, zc, np * BS);
+        } else {
 #pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
-          const int q = (lane + 32 * rr) / BS;
-          if (q < np) {
-            const size_t pi = static_cast<size_t>(pages[j * PPI + q]) * p.Hkv + U.kvh;
-            zc[rr] = int8_zero_const(__ldg(reinterpret_cast<const float2*>(sc) + pi).y);
+          for (int rr = 0; rr < 2; ++rr) {
+            const int q = (lane + 32 * rr) / BS;
+            if (q < np) {
+              const size_t pi = static_cast<size_t>(pages[j * PPI + q]) * p.Hkv + U.kvh;
+              zc[rr] = int8_zero_const(__ldg(reinterpret_cast<const float2*>(sc) + pi).y);
+            }
           }
+          widen_stage<KV, kTcTokens>(st, TcLayout::kRegion, lane, zc, np * BS);
         }
+      } else {
+        widen_stage<KV, kTcTokens>(st, TcLayout::kRegion, lane, zc, np * BS);
       }
-      widen_stage<KV, kTcTokens>(st, TcLayout::kRegion, lane, zc, np * BS);
       fence_proxy_async_smem();  // the widened rows are read by the tensor cores
       __syncwarp();
       if (lane == 0) mbar_arrive(is_k ? &full_k[g % kTcKStages] : &full_v[g % kTcVStages]);
@@ -668,6 +678,7 @@ __global__ void __launch_bounds__(tc_threads(KV), 2)
     // one-byte caches: the row as f16, scaled by 2^-kq so that its largest
     // |q| lies in [2^14, 2^15) (exact for every bf16 value within 2^-10 of
     // it); returns kq, which the row's softmax coefficient takes back
+    float qsum_next = 0.f;  // INT8 caches: sum of the row's stored f16 query values (next unit)
     auto put_query = [&](const TcUnit& U) -> int {
       if constexpr (!kOneByte) {
         for (int half = 0; half < 2; ++half) {
@@ -699,6 +710,16 @@ __global__ void __launch_bounds__(tc_threads(KV), 2)
             const uint32_t w4[4] = {qv[half][c4].x, qv[half][c4].y, qv[half][c4].z, qv[half][c4].w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) w[4 * c4 + e] = pack_f16x2(bf16lo_to_f32(w4[e]) * sc, bf16hi_to_f32(w4[e]) * sc);
+          }
+          if constexpr (KV == PKV_KV_INT8) {  // exact f16 values, summed in fp32
+            float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+              s0 += f.x;
+              s1 += f.y;
+            }
+            qsum_next = (half == 0 ? 0.f : qsum_next) + (s0 + s1);
           }
           tc_st32(t_lane + kTcQCol + 32 * half, w);
         }
@@ -743,6 +764,7 @@ __global__ void __launch_bounds__(tc_threads(KV), 2)
       // value per key; cq = c 2^kq scales them back (with k_scale per page),
       // and the softmax works on the scaled scores with coefficient 1
       const float cq = kOneByte ? c * __uint_as_float(static_cast<uint32_t>(127 + kq_next) << 23) : c;
+      const float qsum = qsum_next;  // INT8: this unit's (the next put_query overwrites qsum_next)
       const float cs = kOneByte ? 1.f : c;
       const float inv_vmax = kOneByte ? 1.f / __int_as_float(slot_desc(k)[5]) : 1.f;
       const int npages_u = (t1 - t0 + BS - 1) / BS;
@@ -883,16 +905,20 @@ __global__ void __launch_bounds__(tc_threads(KV), 2)
         step_masks(j, vmask, rmask);  // independent of S: computed while it is on its way
         // one-byte caches: the step's pages' score coefficients and P factors
         // (pages past the unit's end: 0, their tokens are masked)
-        float ckq[PPI], vrq[PPI];
+        float ckq[PPI], vrq[PPI], cadd[PPI];
 #pragma unroll
         for (int q = 0; q < PPI; ++q) {
           ckq[q] = 0.f;
+          cadd[q] = 0.f;
           vrq[q] = 0.f;
           if constexpr (kOneByte) {
             if (j * PPI + q < npages_u) {
               const size_t pi = static_cast<size_t>(slot_pages(k)[j * PPI + q]) * p.Hkv + kvh_u;
               if constexpr (KV == PKV_KV_INT8) {
-                ckq[q] = cq * __ldg(reinterpret_cast<const float2*>(p.k_scale) + pi).x;
+                const float2 kp = __ldg(reinterpret_cast<const float2*>(p.k_scale) + pi);
+                ckq[q] = cq * kp.x;
+                // the biased K code values add (1152 + zero) x sum(q) to S'
+                cadd[q] = -(kInt8Bias + kp.y) * qsum * ckq[q];
                 vrq[q] = inv_vmax * __ldg(reinterpret_cast<const float2*>(p.v_scale) + pi).x;
               } else {
                 ckq[q] = cq * __ldg(p.k_scale + pi);
@@ -943,7 +969,9 @@ __global__ void __launch_bounds__(tc_threads(KV), 2)
         if (lane == 0) mbar_arrive(s_free);  // the slot may take S(g + 1)
         if constexpr (kOneByte) {  // the scaled scores, in log2 units
 #pragma unroll
-          for (int t = 0; t < kTcTokens; ++t) sv[t] = __float_as_uint(__uint_as_float(sv[t]) * ckq[t / BS]);
+          for (int t = 0; t < kTcTokens; ++t)
+            sv[t] = __float_as_uint(KV == PKV_KV_INT8 ? fmaf(__uint_as_float(sv[t]), ckq[t / BS], cadd[t / BS])
+                                                      : __uint_as_float(sv[t]) * ckq[t / BS]);
         }
         // masked extremum of the raw scores (maximum for a non-negative
         // scale); a step whose tokens are all this row's takes branch-free code
