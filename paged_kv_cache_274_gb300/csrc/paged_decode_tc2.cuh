@@ -123,6 +123,18 @@ __device__ __forceinline__ void tc_wait_ld_regs(uint32_t (&v)[32]) {
       :
       : "memory");
 }
+// After a tcgen05.wait::ld (which covers every earlier tcgen05.ld of the
+// thread): ties more loaded registers to that point without another wait.
+__device__ __forceinline__ void tc_regs_loaded(uint32_t (&v)[32]) {
+  asm volatile(""
+               : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]), "+r"(v[7]),
+                 "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]), "+r"(v[12]), "+r"(v[13]), "+r"(v[14]),
+                 "+r"(v[15]), "+r"(v[16]), "+r"(v[17]), "+r"(v[18]), "+r"(v[19]), "+r"(v[20]), "+r"(v[21]),
+                 "+r"(v[22]), "+r"(v[23]), "+r"(v[24]), "+r"(v[25]), "+r"(v[26]), "+r"(v[27]), "+r"(v[28]),
+                 "+r"(v[29]), "+r"(v[30]), "+r"(v[31])
+               :
+               : "memory");
+}
 __device__ __forceinline__ void tc_wait_ld_regs16(uint32_t (&v)[16]) {
   asm volatile(
       "tcgen05.wait::ld.sync.aligned;"
@@ -538,10 +550,10 @@ __global__ void __launch_bounds__(kT2Threads, 1)
           tc_ld32(t_s + 32, x1);
           tc_ld32(t_s + 64, x2);
           tc_ld32(t_s + 96, x3);
-          tc_wait_ld_regs(x0);
-          tc_wait_ld_regs(x1);
-          tc_wait_ld_regs(x2);
-          tc_wait_ld_regs(x3);
+          tc_wait_ld_regs(x0);  // one wait for the four loads
+          tc_regs_loaded(x1);
+          tc_regs_loaded(x2);
+          tc_regs_loaded(x3);
           const float ext = c >= 0.f ? fmaxf(fmaxf(tree_ext32<true>(x0), tree_ext32<true>(x1)),
                                              fmaxf(tree_ext32<true>(x2), tree_ext32<true>(x3)))
                                      : fminf(fminf(tree_ext32<false>(x0), tree_ext32<false>(x1)),
@@ -652,7 +664,12 @@ __global__ void __launch_bounds__(kT2Threads, 1)
             tc_ld32(t_o + oc, ov);
             tc_wait_ld_regs(ov);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * factor);
+            for (int e = 0; e < 32; e += 2) {
+              float a, b;
+              fmul2(a, b, __uint_as_float(ov[e]), __uint_as_float(ov[e + 1]), factor, factor);
+              ov[e] = __float_as_uint(a);
+              ov[e + 1] = __float_as_uint(b);
+            }
             tc_st32(t_o + oc, ov);
           }
         }
@@ -706,9 +723,14 @@ __global__ void __launch_bounds__(kT2Threads, 1)
             uint4* dst = reinterpret_cast<uint4*>(p.out + qrow * D + cc);
 #pragma unroll
             for (int c8 = 0; c8 < 4; ++c8) {
-              const float* f = reinterpret_cast<const float*>(ov + 8 * c8);
-              dst[c8] = make_uint4(pack_bf16x2(f[0] * osc, f[1] * osc), pack_bf16x2(f[2] * osc, f[3] * osc),
-                                   pack_bf16x2(f[4] * osc, f[5] * osc), pack_bf16x2(f[6] * osc, f[7] * osc));
+              uint32_t w4[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                float a, b;
+                fmul2(a, b, __uint_as_float(ov[8 * c8 + 2 * e]), __uint_as_float(ov[8 * c8 + 2 * e + 1]), osc, osc);
+                w4[e] = pack_bf16x2(a, b);
+              }
+              dst[c8] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
             }
           } else {
             uint4* dst = reinterpret_cast<uint4*>(p.part_o + (qrow * p.pmax + U.pidx) * D + cc);
