@@ -314,7 +314,7 @@ WorkspaceLayout workspace_layout(int B, int T, int Hq, int Hkv, int NT, int D, i
 
 size_t decode_smem_bytes(int kv_fp8, int D, int bs, int warps, int stages, int tc, int tc2) {
   if (tc2) return tc2_smem_layout_bytes();
-  if (tc) return tc_smem_layout_bytes();
+  if (tc) return tc_smem_layout_bytes(kv_fp8 != 0);
   if (kv_fp8) {
     return bs == 16 ? decode_smem_layout_bytes<128, 16, true>(warps, stages)
                     : decode_smem_layout_bytes<128, 32, true>(warps, stages);

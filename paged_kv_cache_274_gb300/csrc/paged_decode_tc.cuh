@@ -14,7 +14,8 @@
 //
 //   * Warp-specialised, with no CTA-wide barrier between units: a K copy
 //     warp takes units from the planner's counter, writes each unit's
-//     descriptor and page ids into a 2-slot ring, and issues the tensor-map
+//     descriptor and page ids (one-byte caches: and the pages' scales and
+//     zero points) into a 2-slot ring, and issues the tensor-map
 //     copies (TMA, 128-byte swizzle) of each step's K pages into a 4-stage
 //     ring; a V copy warp fills a 2-stage V ring; an MMA warp issues
 //     S = Q . K^T (M 128, N 64, K 128; the query tile is the A operand in
@@ -101,11 +102,18 @@ struct TcLayout {  // byte offsets from the 1024-aligned shared-memory base
   static constexpr uint32_t kSlots = kMisc + 16;             // 2 unit slots
   static constexpr uint32_t kSlotPages = 32;                 // after 8 int32 of descriptor
   static constexpr uint32_t kSlotBad = kSlotPages + 4 * kTcMaxPages;
-  static constexpr uint32_t kSlot = kSlotBad + kTcMaxPages;  // 352 bytes
+  static constexpr uint32_t kSlot = kSlotBad + kTcMaxPages;  // 1312 bytes
   static constexpr uint32_t kEnd = kSlots + 2 * kSlot;
+  // one-byte caches: each slot's page parameters (k scale, k zero, v scale,
+  // v zero) as a float4 per page, read by the compute and converter warps
+  static constexpr uint32_t kPar = (kEnd + 15) & ~15u;
+  static constexpr uint32_t kParSlot = 16 * kTcMaxPages;  // 4 KiB
+  static constexpr uint32_t kEnd1B = kPar + 2 * kParSlot;
 };
 
-__host__ __device__ constexpr size_t tc_smem_layout_bytes() { return 1024 + TcLayout::kEnd; }
+__host__ __device__ constexpr size_t tc_smem_layout_bytes(bool one_byte) {
+  return 1024 + (one_byte ? TcLayout::kEnd1B : TcLayout::kEnd);
+}
 
 // K-major, no-swizzle core-matrix layout of a [128 rows x 64 tokens] bf16 P
 // tile: core matrix (r/8, k/8) of 8 rows x 16 bytes at (r/8) * 1024 + (k/8) * 128.
@@ -174,9 +182,10 @@ __device__ __forceinline__ void widen16(const uint4 c, uint32_t zc, uint4& o0, u
 // rows, 16-byte chunks XOR-swizzled by row % 8) whose one-byte codes a
 // tensor-map copy put in the upper half (row r's 128 codes at
 // kRegion + 128 r) as f16 code values; the caller gives row r's INT8 zero
-// constant.  One warp; lane l takes rows l, l + 32, ...: the lower half
-// first (codes 0-63 of every row), then the upper half row by row, each
-// row's last codes read before its row is overwritten.
+// constant.  One warp; lane l takes rows l, l + 32, ...: all of a row's
+// codes are read before any of its 16 widened chunks is written (a row's
+// codes occupy only the bytes of its own upper half), so the eight loads
+// issue back to back.
 template <int KV, int ROWS, bool kBiased = false>
 __device__ __forceinline__ void widen_stage(uint8_t* stage, uint32_t region, int lane, const uint32_t (&zc)[ROWS / 32],
                                             int valid_rows) {
@@ -184,31 +193,19 @@ __device__ __forceinline__ void widen_stage(uint8_t* stage, uint32_t region, int
   for (int rr = 0; rr < ROWS / 32; ++rr) {
     const int r = lane + 32 * rr;
     if (r >= valid_rows) continue;
-    const uint8_t* src = stage + region + r * 128;
-    uint8_t* dst = stage + r * 128;
+    const int sw = r & 7;
+    uint8_t* hi = stage + region + r * 128;  // codes; then d 64 .. 127
+    uint8_t* lo = stage + r * 128;           // d 0 .. 63
+    uint4 codes[8];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const uint4 codes = *reinterpret_cast<const uint4*>(src + ((c ^ (r & 7)) << 4));
-      uint4 o0, o1;
-      widen16<KV, kBiased>(codes, zc[rr], o0, o1);
-      *reinterpret_cast<uint4*>(dst + (((2 * c) ^ (r & 7)) << 4)) = o0;
-      *reinterpret_cast<uint4*>(dst + (((2 * c + 1) ^ (r & 7)) << 4)) = o1;
-    }
-  }
+    for (int c = 0; c < 8; ++c) codes[c] = *reinterpret_cast<const uint4*>(hi + ((c ^ sw) << 4));
 #pragma unroll
-  for (int rr = 0; rr < ROWS / 32; ++rr) {
-    const int r = lane + 32 * rr;
-    if (r >= valid_rows) continue;
-    uint8_t* row = stage + region + r * 128;
-    uint4 codes[4];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) codes[c] = *reinterpret_cast<const uint4*>(row + (((4 + c) ^ (r & 7)) << 4));
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < 8; ++c) {
       uint4 o0, o1;
       widen16<KV, kBiased>(codes[c], zc[rr], o0, o1);
-      *reinterpret_cast<uint4*>(row + (((2 * c) ^ (r & 7)) << 4)) = o0;
-      *reinterpret_cast<uint4*>(row + (((2 * c + 1) ^ (r & 7)) << 4)) = o1;
+      uint8_t* dst = c < 4 ? lo : hi;
+      *reinterpret_cast<uint4*>(dst + (((2 * (c & 3)) ^ sw) << 4)) = o0;
+      *reinterpret_cast<uint4*>(dst + (((2 * (c & 3) + 1) ^ sw) << 4)) = o1;
     }
   }
 }
@@ -326,6 +323,8 @@ __global__ void __launch_bounds__(tc_threads(KV), 2)
   auto slot_bad = [&](int k) {
     return reinterpret_cast<const volatile uint8_t*>(sm + TcLayout::kSlots + k * TcLayout::kSlot + TcLayout::kSlotBad);
   };
+  // one-byte caches: the slot's page parameters (k scale, k zero, v scale, v zero)
+  auto slot_par = [&](int k) { return reinterpret_cast<float4*>(sm + TcLayout::kPar + k * TcLayout::kParSlot); };
   auto read_unit = [&](int k) {
     const volatile int* d = slot_desc(k);
     TcUnit U;
@@ -357,7 +356,7 @@ __global__ void __launch_bounds__(tc_threads(KV), 2)
   // zero point), publish with full_k / full_v.  Rows of pages past the unit's end are left as
   // they are (their scores are masked and their V rows cleared).  Whole
   // warp; false on timeout.
-  auto widen_pages = [&](bool is_k, const TcUnit& U, const volatile int* pages, int j, uint32_t g) -> bool {
+  auto widen_pages = [&](bool is_k, const TcUnit& U, const float4* par, int j, uint32_t g) -> bool {
     if constexpr (!kOneByte) {
       return true;
     } else {
@@ -367,7 +366,6 @@ __global__ void __launch_bounds__(tc_threads(KV), 2)
       uint8_t* st = sm + (is_k ? TcLayout::kK + (g % kTcKStages) * TcLayout::kTile
                                : TcLayout::kV + (g % kTcVStages) * TcLayout::kTile);
       const int np = min(PPI, U.npages - j * PPI);
-      const float* sc = is_k ? p.k_scale : p.v_scale;
       uint32_t zc[2] = {0u, 0u};
       if constexpr (KV == PKV_KV_INT8) {
         if (is_k) {  // K: biased code values, no zero points
@@ -376,10 +374,7 @@ __global__ void __launch_bounds__(tc_threads(KV), 2)
 #pragma unroll
           for (int rr = 0; rr < 2; ++rr) {
             const int q = (lane + 32 * rr) / BS;
-            if (q < np) {
-              const size_t pi = static_cast<size_t>(pages[j * PPI + q]) * p.Hkv + U.kvh;
-              zc[rr] = int8_zero_const(__ldg(reinterpret_cast<const float2*>(sc) + pi).y);
-            }
+            if (q < np) zc[rr] = int8_zero_const(par[j * PPI + q].w);
           }
           widen_stage<KV, kTcTokens>(st, TcLayout::kRegion, lane, zc, np * BS);
         }
@@ -446,12 +441,20 @@ __global__ void __launch_bounds__(tc_threads(KV), 2)
           }
           pg[q] = e;
           bd[q] = isbad ? 1 : 0;
-          if constexpr (kOneByte) {
+          if constexpr (kOneByte) {  // the page's parameters (0 for a bad page: its tokens are masked)
+            float4 par = make_float4(0.f, 0.f, 0.f, 0.f);
             if (!isbad) {
               const size_t pi = static_cast<size_t>(e) * p.Hkv + kvh;
-              vmax = fmaxf(vmax, fabsf(KV == PKV_KV_INT8 ? __ldg(reinterpret_cast<const float2*>(p.v_scale) + pi).x
-                                                         : __ldg(p.v_scale + pi)));
+              if constexpr (KV == PKV_KV_INT8) {
+                const float2 kp = __ldg(reinterpret_cast<const float2*>(p.k_scale) + pi);
+                const float2 vp = __ldg(reinterpret_cast<const float2*>(p.v_scale) + pi);
+                par = make_float4(kp.x, kp.y, vp.x, vp.y);
+              } else {
+                par = make_float4(__ldg(p.k_scale + pi), 0.f, __ldg(p.v_scale + pi), 0.f);
+              }
+              vmax = fmaxf(vmax, fabsf(par.z));
             }
+            slot_par(k)[q] = par;
           }
         }
         if constexpr (kOneByte) {  // the unit's largest |v_scale| (1 if none): P carries v_scale / it
@@ -561,11 +564,11 @@ __global__ void __launch_bounds__(tc_threads(KV), 2)
       }
       const TcUnit U = read_unit(k);
       if (U.u >= total_units) break;
-      const volatile int* pages = slot_pages(k);
-      bool ok = widen_pages(true, U, pages, 0, gk++);
+      const float4* par = slot_par(k);
+      bool ok = widen_pages(true, U, par, 0, gk++);
       for (int j = 0; ok && j < U.nsteps; ++j) {
-        if (j + 1 < U.nsteps) ok = widen_pages(true, U, pages, j + 1, gk++);
-        if (ok) ok = widen_pages(false, U, pages, j, gv++);
+        if (j + 1 < U.nsteps) ok = widen_pages(true, U, par, j + 1, gk++);
+        if (ok) ok = widen_pages(false, U, par, j, gv++);
       }
       if (!ok) {
         timed_out = true;
@@ -745,7 +748,7 @@ __global__ void __launch_bounds__(tc_threads(KV), 2)
     uint32_t g0 = 0;
     for (int i = 0; more; ++i) {
       const int k = i & 1;
-      int nsteps, t0, t1, lim, kvh_u;  // steps, token range, keys of this row: positions < lim
+      int nsteps, t0, t1, lim;  // steps, token range, keys of this row: positions < lim
       bool row_ok;
       {
         const TcUnit U = read_unit(k);
@@ -755,7 +758,6 @@ __global__ void __launch_bounds__(tc_threads(KV), 2)
         t0 = U.t0;
         t1 = U.t1;
         lim = U.ctx - p.T + 1 + t;
-        kvh_u = U.kvh;
       }
       const volatile uint8_t* bad = slot_bad(k);
       bool has_next = false;
@@ -913,17 +915,11 @@ __global__ void __launch_bounds__(tc_threads(KV), 2)
           vrq[q] = 0.f;
           if constexpr (kOneByte) {
             if (j * PPI + q < npages_u) {
-              const size_t pi = static_cast<size_t>(slot_pages(k)[j * PPI + q]) * p.Hkv + kvh_u;
-              if constexpr (KV == PKV_KV_INT8) {
-                const float2 kp = __ldg(reinterpret_cast<const float2*>(p.k_scale) + pi);
-                ckq[q] = cq * kp.x;
-                // the biased K code values add (1152 + zero) x sum(q) to S'
-                cadd[q] = -(kInt8Bias + kp.y) * qsum * ckq[q];
-                vrq[q] = inv_vmax * __ldg(reinterpret_cast<const float2*>(p.v_scale) + pi).x;
-              } else {
-                ckq[q] = cq * __ldg(p.k_scale + pi);
-                vrq[q] = inv_vmax * __ldg(p.v_scale + pi);
-              }
+              const float4 pr = slot_par(k)[j * PPI + q];
+              ckq[q] = cq * pr.x;
+              // the biased INT8 K code values add (1152 + zero) x sum(q) to S'
+              if constexpr (KV == PKV_KV_INT8) cadd[q] = -(kInt8Bias + pr.y) * qsum * ckq[q];
+              vrq[q] = inv_vmax * pr.z;
             }
           }
         }
@@ -967,11 +963,18 @@ __global__ void __launch_bounds__(tc_threads(KV), 2)
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(s_free);  // the slot may take S(g + 1)
-        if constexpr (kOneByte) {  // the scaled scores, in log2 units
+        if constexpr (kOneByte) {  // the scaled scores, in log2 units (two per packed instruction)
 #pragma unroll
-          for (int t = 0; t < kTcTokens; ++t)
-            sv[t] = __float_as_uint(KV == PKV_KV_INT8 ? fmaf(__uint_as_float(sv[t]), ckq[t / BS], cadd[t / BS])
-                                                      : __uint_as_float(sv[t]) * ckq[t / BS]);
+          for (int t = 0; t < kTcTokens; t += 2) {
+            const float kq = ckq[t / BS];
+            float a0, a1;
+            if constexpr (KV == PKV_KV_INT8)
+              ffma2(a0, a1, __uint_as_float(sv[t]), __uint_as_float(sv[t + 1]), kq, kq, cadd[t / BS], cadd[t / BS]);
+            else
+              fmul2(a0, a1, __uint_as_float(sv[t]), __uint_as_float(sv[t + 1]), kq, kq);
+            sv[t] = __float_as_uint(a0);
+            sv[t + 1] = __float_as_uint(a1);
+          }
         }
         // masked extremum of the raw scores (maximum for a non-negative
         // scale); a step whose tokens are all this row's takes branch-free code
