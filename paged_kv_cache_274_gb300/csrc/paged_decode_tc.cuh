@@ -46,20 +46,23 @@
 //     never stored): at T x G = 32, say, only warp 3 works, and warp 0, which
 //     shares its sub-partition with the MMA warp, stays idle.
 //
-// One-byte caches (E4M3, INT8) take the same path with f16 operands ("KV
-// Cache Engineering: PagedAttention, Continuous Batching, Attention
-// Variants, and the Bandwidth Wall", "Quantized KV Cache": dequantise on
-// read).  The copy warps land a step's codes in the upper half of a stage
-// and a converter warp rewrites the stage as the f16 code values (INT8:
-// code - zero), which are exact in f16: one conversion per two codes, no
-// arithmetic.  The page scales are applied where they cost nothing per
-// element of the cache: a row's scores of page q are S' x c x k_scale[q]
-// (one multiply per score, folded into the softmax), and P carries
-// v_scale[q] / v_max (v_max: the unit's largest |v_scale|, so P stays
-// below 256), the output v_max.  The query rows go to f16 scaled by a power
-// of two per row (largest |q| in [2^14, 2^15)), which the row's softmax
-// coefficient takes back.  With one page, P = 1 and the output is
-// bf16(code value x scale) exactly as the widened value.
+// One-byte caches (E4M3, INT8) take the same path ("KV Cache Engineering:
+// PagedAttention, Continuous Batching, Attention Variants, and the
+// Bandwidth Wall", "Quantized KV Cache": dequantise on read).  The copy
+// warps land a step's codes in the upper half of a stage.  V pages, and
+// INT8 K pages, are rewritten there by a converter warp as f16 code values
+// (E4M3 value; INT8 code - zero for V, 1152 + code for K), which are exact
+// in f16, and feed kind::f16 products; E4M3 K pages are an operand of the
+// tensor cores as they are (kind::f8f6f4), against a query tile held as two
+// E4M3 parts (high and residual) whose sum is the scaled query.  The page
+// scales are applied where they cost nothing per element of the cache: a
+// row's scores of page q are S' x c x k_scale[q] (one multiply per score,
+// folded into the softmax; INT8 adds the bias and zero-point term), and P
+// carries v_scale[q] / v_max (v_max: the unit's largest |v_scale|, so P
+// stays below 256), the output v_max.  The query rows are scaled by a power
+// of two per row, which the row's softmax coefficient takes back.  With one
+// page, P = 1 and the output is bf16(code value x scale) exactly as the
+// widened value.
 //
 // Units are (sequence, KV head, row tile, partition) from the planner's
 // counter; the merge kernel combines partitions.  Every wait is bounded; a
@@ -222,6 +225,8 @@ __global__ void __launch_bounds__(tc_threads(KV), 2)
   constexpr int D = 128;
   constexpr int PPI = kTcTokens / BS;  // pages per step
   constexpr bool kOneByte = KV != PKV_KV_BF16;
+  // E4M3 K pages are an operand of the tensor cores as they are (kind::f8f6f4)
+  constexpr bool kF8K = KV == PKV_KV_FP8_E4M3;
   static_assert(kTcMaxPages % PPI == 0, "");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(
@@ -302,7 +307,9 @@ __global__ void __launch_bounds__(tc_threads(KV), 2)
   const uint32_t t_lane = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);  // compute warp's 32 lanes
   const uint64_t policy = p.NT > 1 ? l2_policy_evict_normal() : l2_policy_evict_first();
   // one-byte caches: f16 query, code values and P
-  constexpr uint32_t kIdescS = kOneByte ? tc_idesc_f16_f32(kTcRows, kTcTokens) : tc_idesc_bf16_f32(kTcRows, kTcTokens);
+  constexpr uint32_t kIdescS = kF8K       ? tc_idesc_e4m3_f32(kTcRows, kTcTokens)
+                               : kOneByte ? tc_idesc_f16_f32(kTcRows, kTcTokens)
+                                          : tc_idesc_bf16_f32(kTcRows, kTcTokens);
   constexpr uint32_t kIdescO = kOneByte ? tc_idesc_f16_f32(kTcRows, D, /*b_mn_major=*/true)
                                         : tc_idesc_bf16_f32(kTcRows, D, /*b_mn_major=*/true);
   pdl_trigger();
@@ -485,14 +492,14 @@ __global__ void __launch_bounds__(tc_threads(KV), 2)
           break;
         }
         uint8_t* st = sm + TcLayout::kK + (g % kTcKStages) * TcLayout::kTile;
-        uint64_t* bar = kOneByte ? &tma_k[g % kTcKStages] : &full_k[g % kTcKStages];
+        uint64_t* bar = (kOneByte && !kF8K) ? &tma_k[g % kTcKStages] : &full_k[g % kTcKStages];
         const int np = min(PPI, npages_total - j * PPI);
         if (lane == 0) {
           fence_proxy_async_smem();  // the stage held P (generic writes) before
           mbar_arrive_expect_tx(bar, static_cast<uint32_t>(np) * (kOneByte ? 128u : 2u * 64u * 2u) * BS);
         }
         __syncwarp();
-        if (kOneByte) {  // one box of 128 codes per page, into the upper half for the converter
+        if (kOneByte) {  // one box of 128 codes per page, into the upper half (the converter's input; E4M3: S's operand)
           if (lane < np) {
             const int row = p.row_base + (pages[j * PPI + lane] * p.Hkv + kvh) * BS;
             tma_load_2d(st + TcLayout::kRegion + lane * BS * 128, &kmap, bar, 0, row, policy);
@@ -565,9 +572,9 @@ __global__ void __launch_bounds__(tc_threads(KV), 2)
       const TcUnit U = read_unit(k);
       if (U.u >= total_units) break;
       const float4* par = slot_par(k);
-      bool ok = widen_pages(true, U, par, 0, gk++);
+      bool ok = kF8K || widen_pages(true, U, par, 0, gk++);
       for (int j = 0; ok && j < U.nsteps; ++j) {
-        if (j + 1 < U.nsteps) ok = widen_pages(true, U, par, j + 1, gk++);
+        if (!kF8K && j + 1 < U.nsteps) ok = widen_pages(true, U, par, j + 1, gk++);
         if (ok) ok = widen_pages(false, U, par, j, gv++);
       }
       if (!ok) {
@@ -586,11 +593,23 @@ __global__ void __launch_bounds__(tc_threads(KV), 2)
         if (!mbar_wait_bounded(&full_k[g % kTcKStages], (g / kTcKStages) & 1u, kWaitLimitNs)) return false;
         const uint32_t k_addr = smem_addr(sm + TcLayout::kK + (g % kTcKStages) * TcLayout::kTile);
         tc_fence_after_sync();
+        if constexpr (kF8K) {
+          // E4M3: the codes' 128-byte rows in the upper half, 32 d per
+          // product, once with each part of the query (columns 0-31: the
+          // high part, 32-63: the low part)
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = static_cast<uint32_t>((kk & 3) * 32);  // 16 d = 32 bytes along the row
-          const uint64_t bdesc = tc_smem_desc(k_addr + (kk >> 2) * TcLayout::kRegion + koff, 16, 1024, 2);
-          tc_mma_bf16_ts(tmem + kTcSCol, tmem + kTcQCol + 8 * kk, bdesc, kIdescS, kk > 0);
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t koff = static_cast<uint32_t>((kk & 3) * 32);  // 32 d = 32 bytes along the row
+            const uint64_t bdesc = tc_smem_desc(k_addr + TcLayout::kRegion + koff, 16, 1024, 2);
+            tc_mma_e4m3_ts(tmem + kTcSCol, tmem + kTcQCol + 32 * (kk >> 2) + 8 * (kk & 3), bdesc, kIdescS, kk > 0);
+          }
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t koff = static_cast<uint32_t>((kk & 3) * 32);  // 16 d = 32 bytes along the row
+            const uint64_t bdesc = tc_smem_desc(k_addr + (kk >> 2) * TcLayout::kRegion + koff, 16, 1024, 2);
+            tc_mma_bf16_ts(tmem + kTcSCol, tmem + kTcQCol + 8 * kk, bdesc, kIdescS, kk > 0);
+          }
         }
         tc_commit(s_done);
         s_end = g + 1;
@@ -678,9 +697,15 @@ __global__ void __launch_bounds__(tc_threads(KV), 2)
       }
       tc_st32(t_lane + kTcQCol + 32 * half, w);
     };
-    // one-byte caches: the row as f16, scaled by 2^-kq so that its largest
-    // |q| lies in [2^14, 2^15) (exact for every bf16 value within 2^-10 of
-    // it); returns kq, which the row's softmax coefficient takes back
+    // one-byte caches: the row scaled by 2^-kq, in the type of S's other
+    // operand; returns kq, which the row's softmax coefficient takes back.
+    // INT8 (f16 K code values): the largest |q| in [2^14, 2^15), exact for
+    // every bf16 value within 2^-10 of it.  E4M3 (K codes as they are): the
+    // largest |q'| in [2^7, 2^8), as two E4M3 parts qh = e4m3(q'),
+    // ql = e4m3(q' - qh); q' has 8 significant bits, qh holds the first 4
+    // and the residual the rest, so qh + ql = q' exactly wherever the
+    // residual is no finer than E4M3's 2^-9 (|q'| >= 2^-2), within 2^-10
+    // below
     float qsum_next = 0.f;  // INT8 caches: sum of the row's stored f16 query values (next unit)
     auto put_query = [&](const TcUnit& U) -> int {
       if constexpr (!kOneByte) {
@@ -703,28 +728,59 @@ __global__ void __launch_bounds__(tc_threads(KV), 2)
 #pragma unroll
             for (int e = 0; e < 4; ++e) mx = max(mx, max(w4[e] & 0x7fffu, (w4[e] >> 16) & 0x7fffu));
           }
-        const int kq = mx == 0 ? 0 : max(-100, min(100, static_cast<int>(mx >> 7) - 127 - 14));
+        const int kq = mx == 0 ? 0 : max(-100, min(100, static_cast<int>(mx >> 7) - 127 - (kF8K ? 7 : 14)));
         const float sc = __uint_as_float(static_cast<uint32_t>(127 - kq) << 23);  // 2^-kq
+        if constexpr (kF8K) {
+          // per d half: 16 columns of each part (four E4M3 values a column:
+          // d 4c .. 4c + 3), high part at column 16 half, low at 32 + 16 half
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t w[32];
+          for (int half = 0; half < 2; ++half) {
+            uint32_t wh[16], wl[16];
 #pragma unroll
-          for (int c4 = 0; c4 < 8; ++c4) {
-            const uint32_t w4[4] = {qv[half][c4].x, qv[half][c4].y, qv[half][c4].z, qv[half][c4].w};
+            for (int c4 = 0; c4 < 8; ++c4) {
+              const uint32_t w4[4] = {qv[half][c4].x, qv[half][c4].y, qv[half][c4].z, qv[half][c4].w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) w[4 * c4 + e] = pack_f16x2(bf16lo_to_f32(w4[e]) * sc, bf16hi_to_f32(w4[e]) * sc);
-          }
-          if constexpr (KV == PKV_KV_INT8) {  // exact f16 values, summed in fp32
-            float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
-              s0 += f.x;
-              s1 += f.y;
+              for (int e = 0; e < 4; ++e) {  // d = 64 half + 8 c4 + 2 e, + 1
+                const float2 v = make_float2(bf16lo_to_f32(w4[e]) * sc, bf16hi_to_f32(w4[e]) * sc);
+                const __nv_fp8x2_storage_t h = __nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, __NV_E4M3);
+                const float2 hv = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(h, __NV_E4M3)));
+                const __nv_fp8x2_storage_t lo =
+                    __nv_cvt_float2_to_fp8x2(make_float2(v.x - hv.x, v.y - hv.y), __NV_SATFINITE, __NV_E4M3);
+                const int col = 2 * c4 + (e >> 1);
+                if (e & 1) {
+                  wh[col] |= static_cast<uint32_t>(h) << 16;
+                  wl[col] |= static_cast<uint32_t>(lo) << 16;
+                } else {
+                  wh[col] = static_cast<uint32_t>(h);
+                  wl[col] = static_cast<uint32_t>(lo);
+                }
+              }
             }
-            qsum_next = (half == 0 ? 0.f : qsum_next) + (s0 + s1);
+            tc_st16(t_lane + kTcQCol + 16 * half, wh);
+            tc_st16(t_lane + kTcQCol + 32 + 16 * half, wl);
           }
-          tc_st32(t_lane + kTcQCol + 32 * half, w);
+        } else {
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint32_t w[32];
+#pragma unroll
+            for (int c4 = 0; c4 < 8; ++c4) {
+              const uint32_t w4[4] = {qv[half][c4].x, qv[half][c4].y, qv[half][c4].z, qv[half][c4].w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) w[4 * c4 + e] = pack_f16x2(bf16lo_to_f32(w4[e]) * sc, bf16hi_to_f32(w4[e]) * sc);
+            }
+            if constexpr (KV == PKV_KV_INT8) {  // exact f16 values, summed in fp32
+              float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+              for (int e = 0; e < 32; ++e) {
+                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+                s0 += f.x;
+                s1 += f.y;
+              }
+              qsum_next = (half == 0 ? 0.f : qsum_next) + (s0 + s1);
+            }
+            tc_st32(t_lane + kTcQCol + 32 * half, w);
+          }
         }
         return kq;
       }
@@ -1150,7 +1206,7 @@ __global__ void __launch_bounds__(tc_threads(KV), 2)
     // warp's last commits (each covers every earlier product)
     if (kcopy && lane == 0)
       for (uint32_t g = copies_end > kTcKStages ? copies_end - kTcKStages : 0; g < copies_end; ++g)
-        mbar_wait_bounded(kOneByte ? &tma_k[g % kTcKStages] : &full_k[g % kTcKStages], (g / kTcKStages) & 1u,
+        mbar_wait_bounded((kOneByte && !kF8K) ? &tma_k[g % kTcKStages] : &full_k[g % kTcKStages], (g / kTcKStages) & 1u,
                           kWaitLimitNs / 16);
     if (vcopy && lane == 0)
       for (uint32_t g = copies_end > kTcVStages ? copies_end - kTcVStages : 0; g < copies_end; ++g)

@@ -445,6 +445,11 @@ __host__ __device__ constexpr uint32_t tc_idesc_f16_f32(int M, int N, bool b_mn_
   return (1u << 4) | (b_mn_major ? (1u << 16) : 0u) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
 }
+// kind::f8f6f4 with E4M3 A and B (format code 0 in both fields), fp32 D,
+// both K-major.
+__host__ __device__ constexpr uint32_t tc_idesc_e4m3_f32(int M, int N) {
+  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
 
 // D[tmem] (+)= A[smem] . B[smem]^T; issued by one thread.
 __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
@@ -465,30 +470,16 @@ __device__ __forceinline__ void tc_mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem,
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u));
 }
 
-// Warp-wide variants: every lane of the warp executes them with the same
-// (warp-uniform) operands and lane 0 issues.  The warp stays converged, so
-// the descriptors live in uniform registers instead of being moved there
-// from one divergent lane before each product.
-__device__ __forceinline__ void tc_mma_bf16_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                                 bool accumulate, bool leader) {
+// D[tmem] (+)= A[tmem] . B[smem]^T with E4M3 A and B (kind::f8f6f4, fp32
+// accumulate): row i of A in lane i, four E4M3 values per 32-bit column
+// (byte j = element 4c + j), so a product of K 32 reads 8 columns; B K-major
+// in shared memory (32 bytes of each row per product).  One thread.
+__device__ __forceinline__ void tc_mma_e4m3_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                               bool accumulate) {
   asm volatile(
-      "{\n .reg .pred p, e;\n setp.ne.u32 p, %4, 0;\n setp.ne.u32 e, %5, 0;\n"
-      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u), "r"(leader ? 1u : 0u));
-}
-__device__ __forceinline__ void tc_mma_bf16_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                                    bool accumulate, bool leader) {
-  asm volatile(
-      "{\n .reg .pred p, e;\n setp.ne.u32 p, %4, 0;\n setp.ne.u32 e, %5, 0;\n"
-      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u), "r"(leader ? 1u : 0u));
-}
-__device__ __forceinline__ void tc_commit_warp(uint64_t* bar, bool leader) {
-  asm volatile(
-      "{\n .reg .pred e;\n setp.ne.u32 e, %1, 0;\n"
-      " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(smem_addr(bar)),
-      "r"(leader ? 1u : 0u)
-      : "memory");
+      "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u));
 }
 
 // The MMAs this thread issued so far arrive on `bar` when complete.
@@ -509,6 +500,23 @@ __device__ __forceinline__ void tc_alloc(uint32_t* slot, uint32_t ncols) {
 }
 __device__ __forceinline__ void tc_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// Whole warp: 16 consecutive 32-bit TMEM columns of this thread's lane.
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
 }
 
 // Whole warp: 32 consecutive 32-bit columns of this thread's TMEM lane
