@@ -103,10 +103,12 @@ typedef enum {
                         caches); G <= 16 */
   PKV_MATH_TC = 3    /* tcgen05 tiles of 128 (query token, head) rows with TMEM
                         accumulators; multi-token calls (T > 1), head_dim 128,
-                        G <= 128; bf16 pages as they are, E4M3 / INT8 pages
-                        as f16 code values with the page scales applied to
-                        the scores and to P; with more than one tile per KV
-                        head (bf16), pairs of tiles share each page read */
+                        G <= 128; bf16 pages as they are; E4M3 K pages as
+                        they are (E4M3 products against a two-part E4M3
+                        query), INT8 K and all one-byte V pages as f16 code
+                        values, with the page scales applied to the scores
+                        and to P; with more than one tile per KV head
+                        (bf16), pairs of tiles share each page read */
 } pkv_decode_math;
 
 /* Tuning knobs of pkv_paged_decode; a NULL pointer or zero fields = auto. */
