@@ -430,8 +430,10 @@ def test_tc_pair_matches_one_tile_kernel():
 
 
 # ---------------------------------------------------------------------------
-# one-byte caches (E4M3, INT8) on the tcgen05 tiles: pages widened in shared
-# memory to bf16 of (code value) x page scale ((code - zero) x scale)
+# one-byte caches (E4M3, INT8) on the tcgen05 tiles: products on exact code
+# values (E4M3 K pages as they are, against a two-part E4M3 query; INT8 K
+# and all V pages widened to f16 in shared memory), the page scales applied
+# to the scores and to P
 # ---------------------------------------------------------------------------
 TC_1B_SWEEP = [  # (dtype, bs, Hq, Hkv, T, lens)
     ("fp8", 16, 32, 8, 8, [1, 9, 40, 300, 1000]),      # 32 rows of 128, a context below T
@@ -487,6 +489,30 @@ def test_tc_one_byte_wide_scales(dtype, ppu):
     torch.cuda.synchronize()
     assert pkv.read_device_error() == 0
     assert_close(bf16_dev_to_f64(out), _oracle(dc, q), f"tc {dtype} wide scales ppu={ppu}")
+
+
+@pytest.mark.parametrize("dtype", ["fp8", "int8a"])
+def test_tc_one_byte_query_dynamic_range(dtype):
+    # query rows whose elements span 16 binades (|q| = |N(0,1)| x 2^U(-14, 2)),
+    # rows of zeros, and rows with one element 2^10 above the rest: the E4M3
+    # path splits each scaled row into two E4M3 parts that are exact down to
+    # 2^-10 of the row's largest element and within 2^-17 of it below; the
+    # INT8 path holds the row in f16 scaled to [2^14, 2^15)
+    c = random_case(1470, 3, 32, 8, 128, 16, [500, 129, 64], kv_dtype=dtype)
+    dc = DeviceCase(c)
+    T = 32
+    rng = np.random.Generator(np.random.PCG64(1471))
+    q = rng.standard_normal((c.B, T, 32, 128)) * 2.0 ** rng.uniform(-14, 2, size=(c.B, T, 32, 128))
+    q[0, 3] = 0.0                                      # every head of one token: zeros
+    q[1, :, 5] = 1e-3 * rng.standard_normal((T, 128))  # one head: small but not tiny
+    q[1, :, 5, 7] = 1.0                                 # ... with one element 2^10 above
+    from workloads import bf16_bits_from_f32
+    q = bf16_bits_from_f32(q.astype(np.float32))
+    out = pkv.paged_decode_multi(to_dev_bf16(q), dc.k, dc.v, dc.bt, dc.cl, [0], 0, c.scale,
+                                 k_scale=dc.ks, v_scale=dc.vs, opts=_tc_opts(0))
+    torch.cuda.synchronize()
+    assert pkv.read_device_error() == 0
+    assert_close(bf16_dev_to_f64(out), _oracle(dc, q), f"tc {dtype} query dynamic range")
 
 
 def _widened_bits(dc, blk, kvh, row):
