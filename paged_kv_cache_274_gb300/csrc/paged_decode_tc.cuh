@@ -559,9 +559,10 @@ __global__ void __launch_bounds__(tc_threads(KV), 2)
     // Converter (one-byte caches): per unit, K of its first step, then per
     // step j the K codes of step j + 1 and the V codes of step j (the order
     // the MMA warp needs them: S runs one step ahead of P . V), each once its
-    // codes have landed.  (Widening V in the V copy warp instead, between
-    // its copies, delayed the next copy: 780 against 573 us for the 32-token
-    // verify step on an E4M3 cache.)
+    // codes have landed; E4M3 caches only V (their K pages feed the
+    // products as they are).  (Widening V in the V copy warp instead,
+    // between its copies, delayed the next copy: 780 against 573 us for the
+    // 32-token verify step on an E4M3 cache, with the earlier f32 widening.)
     uint32_t gk = 0, gv = 0;
     for (int i = 0;; ++i) {
       const int k = i & 1;

@@ -380,8 +380,9 @@ static pkv_status resolve_decode(const pkv_cache_desc* c, int32_t batch, int32_t
   pkv_decode_opts o{};
   if (opts) o = *opts;
   int math = o.math != 0 ? o.math : env_int("PKV_DECODE_MATH", PKV_MATH_AUTO);
-  // tcgen05 tiles: multi-token calls with head_dim 128 (one-byte caches are
-  // widened to bf16 in shared memory)
+  // tcgen05 tiles: multi-token calls with head_dim 128 (one-byte caches as
+  // exact code values: E4M3 K pages as they are, the other pages widened to
+  // f16 in shared memory)
   const bool tc_ok = c->head_dim == 128 && T > 1 && G <= 128;
   // measured on GB300 (Llama-8B layer, G 4): mma.sync tiles are faster up to
   // 16 rows per KV head (172 us at 4 tokens, one tile), tcgen05 tiles from 32
