@@ -181,6 +181,18 @@ def test_tc_argument_checks(lib):
     assert _plan(lib, _desc(), 8, 4, 32, 64, tc)[0] == 0
 
 
+@pytest.mark.parametrize("dtype", [0, 1, 2])
+def test_tc_one_tile_fits_two_ctas_per_sm(lib, dtype):
+    # the one-tile tcgen05 kernel runs two CTAs per SM (each overlaps the
+    # other's waits; 256 TMEM columns each): its shared memory, plus the
+    # 1 KiB the SM keeps per CTA, must fit twice into the SM's 228 KiB.  The
+    # one-byte instances add the unit slots' page parameters (2 x 4 KiB).
+    st, plan = _plan(lib, _desc(dtype=dtype), 8, 32, 32, 64, pkv.decode_opts(math=pkv.MATH_TC))
+    assert st == 0 and plan.math == pkv.MATH_TC and plan.row_tiles == 1
+    assert plan.warps_per_cta == (7 if dtype == 0 else 8)
+    assert 2 * (plan.smem_bytes_per_cta + 1024) <= 228 * 1024
+
+
 def test_multi_token_arguments(lib):
     d = _desc()
     assert _plan(lib, d, 8, 0, 32, 64)[0] == 1                       # T = 0
