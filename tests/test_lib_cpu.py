@@ -316,3 +316,21 @@ def test_plans_are_consistent_over_random_shapes(lib):
         n = lib.pkv_decode_multi_workspace_bytes(ctypes.byref(d), B, T, G * Hkv, MB, ctypes.byref(opts))
         assert n == plan.workspace_bytes and n > 0
     assert checked > 150
+
+
+def test_two_part_e4m3_query_split():
+    # the E4M3 tcgen05 path holds a query row, scaled to a largest |q'| in
+    # [2^7, 2^8), as qh = e4m3(q') plus ql = e4m3(q' - qh), both rounded to
+    # nearest: for every bf16 value below 2^8 the sum is q' exactly from 2^-2
+    # up (the residual's 4 significant bits are no finer than E4M3's 2^-9),
+    # and within 2^-10 of it below
+    import torch
+    bits = np.arange(0x0001, 0x4380, dtype=np.uint16)  # 0x4380: 256.0 as bf16
+    x = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float32)
+    x = torch.cat([x, -x])
+    qh = x.to(torch.float8_e4m3fn).to(torch.float32)
+    ql = (x - qh).to(torch.float8_e4m3fn).to(torch.float32)  # x - qh is exact in fp32
+    err = (qh + ql - x).abs()
+    big = x.abs() >= 0.25
+    assert bool((err[big] == 0).all())
+    assert float(err[~big].max()) <= 2.0 ** -10
